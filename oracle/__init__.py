@@ -1,0 +1,136 @@
+"""CPU oracle for attention forward over a paged KV cache.
+
+TEST INFRASTRUCTURE ONLY.  Only ``tests/``, ``__graft_entry__.smoke()`` and the
+bench's CPU-baseline leg may import this package.  The product library never
+loads it and has no CPU fallback: it shares no code with the CUDA path.
+
+* ``decode`` / ``prefill``: fp64 attention computed directly from the
+  definition in ``oracle.c`` (two-pass softmax, every element decoded exactly).
+* ``scheduler``: a separate plain restatement of the split-KV scheduling rule.
+* ``bf16_to_f64`` / ``e4m3_to_f64``: the oracle's own element decoders.
+
+Inputs are the raw bit-pattern arrays produced by the seeded generator
+(``uint16`` for bf16, ``uint8`` for e4m3); outputs are float64 numpy arrays.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Optional
+
+import numpy as np
+
+from . import scheduler  # noqa: F401
+from .build import build as _build, LIB as _LIB
+
+_lib = None
+
+
+def _load():
+    global _lib
+    if _lib is None:
+        _build()
+        lib = ctypes.CDLL(_LIB)
+        P = ctypes.c_void_p
+        i32, i64, dbl = ctypes.c_int, ctypes.c_int64, ctypes.c_double
+        lib.oracle_decode.argtypes = [i32, i32, i32, i32, i32, i64, i32, P, P, P, P, P, P, P,
+                                      dbl, P, P]
+        lib.oracle_decode.restype = i32
+        lib.oracle_prefill.argtypes = [i32, i32, i32, i32, i32, i32, i32, i64, P, P, P, P, P, P,
+                                       P, P, i32, dbl, P, i64, P, P]
+        lib.oracle_prefill.restype = i32
+        lib.oracle_bf16_to_double.argtypes = [ctypes.c_uint16]
+        lib.oracle_bf16_to_double.restype = dbl
+        lib.oracle_e4m3_to_double.argtypes = [ctypes.c_uint8]
+        lib.oracle_e4m3_to_double.restype = dbl
+        lib.oracle_num_threads.restype = i32
+        lib.oracle_set_num_threads.argtypes = [i32]
+        _lib = lib
+    return _lib
+
+
+def _p(a: Optional[np.ndarray]):
+    return None if a is None else a.ctypes.data_as(ctypes.c_void_p)
+
+
+def _c(a, dtype):
+    return None if a is None else np.ascontiguousarray(a, dtype=dtype)
+
+
+def num_threads() -> int:
+    return _load().oracle_num_threads()
+
+
+def set_num_threads(n: int) -> None:
+    _load().oracle_set_num_threads(int(n))
+
+
+def bf16_to_f64(bits: np.ndarray) -> np.ndarray:
+    lib = _load()
+    flat = np.asarray(bits, dtype=np.uint16).ravel()
+    return np.array([lib.oracle_bf16_to_double(int(x)) for x in flat]).reshape(np.shape(bits))
+
+
+def e4m3_to_f64(bits: np.ndarray) -> np.ndarray:
+    lib = _load()
+    flat = np.asarray(bits, dtype=np.uint8).ravel()
+    return np.array([lib.oracle_e4m3_to_double(int(x)) for x in flat]).reshape(np.shape(bits))
+
+
+def decode(q, k_pool, v_pool, block_table, seq_lens, scale: float, kv_dtype: str = "bf16",
+           k_scale=None, v_scale=None):
+    """Single-token decode.  q uint16 [B,Hq,D]; pools [P,Hk,64,D] (uint16 bf16 or
+    uint8 e4m3); block_table int32 [B,max_pages]; seq_lens int32 [B].
+    Returns (out float64 [B,Hq,D], lse float64 [B,Hq])."""
+    lib = _load()
+    q = _c(q, np.uint16)
+    kind = {"bf16": 0, "e4m3": 1}[kv_dtype]
+    pdt = np.uint16 if kind == 0 else np.uint8
+    k_pool, v_pool = _c(k_pool, pdt), _c(v_pool, pdt)
+    bt, sl = _c(block_table, np.int32), _c(seq_lens, np.int32)
+    ks, vs = _c(k_scale, np.float64), _c(v_scale, np.float64)
+    B, Hq, D = q.shape
+    P, Hk = k_pool.shape[0], k_pool.shape[1]
+    out = np.zeros((B, Hq, D), dtype=np.float64)
+    lse = np.zeros((B, Hq), dtype=np.float64)
+    rc = lib.oracle_decode(B, Hq, Hk, D, bt.shape[1], P, kind, _p(q), _p(k_pool), _p(v_pool),
+                           _p(ks), _p(vs), _p(bt), _p(sl), float(scale), _p(out), _p(lse))
+    if rc != 0:
+        raise ValueError("oracle_decode: a referenced page id is out of range or "
+                         "seq_len exceeds the block table")
+    return out, lse
+
+
+def prefill(q, k, v, cu_seqlens_q, cu_seqlens_k, scale: float, causal: bool = True,
+            block_table=None, k_rope=None, qo_offset=None, rows=None):
+    """Chunked / ragged (optionally MLA) prefill.  See ``oracle_prefill`` in oracle.c.
+    rows: optional int64 array of (token * Hq + h) to evaluate.
+    Returns (out float64 [rows, Dv] or [total_q, Hq, Dv], lse)."""
+    lib = _load()
+    q, k, v = _c(q, np.uint16), _c(k, np.uint16), _c(v, np.uint16)
+    cq, ck = _c(cu_seqlens_q, np.int32), _c(cu_seqlens_k, np.int32)
+    bt = _c(block_table, np.int32)
+    kr = _c(k_rope, np.uint16)
+    qo = _c(qo_offset, np.int32)
+    if kr is not None and bt is not None:
+        raise ValueError("a shared rope key is defined for ragged keys only")
+    B = len(cq) - 1
+    total_q, Hq, Dqk = q.shape
+    rope = 0 if kr is None else kr.shape[-1]
+    Hk = k.shape[1]
+    Dv = v.shape[-1]
+    num_pages = k.shape[0] if bt is not None else 0
+    max_pages = bt.shape[1] if bt is not None else 0
+    rr = _c(rows, np.int64)
+    nrows = total_q * Hq if rr is None else len(rr)
+    out = np.zeros((nrows, Dv), dtype=np.float64)
+    lse = np.zeros(nrows, dtype=np.float64)
+    rc = lib.oracle_prefill(B, Hq, Hk, Dqk, Dv, rope, max_pages, num_pages, _p(q), _p(k), _p(v),
+                            _p(kr), _p(cq), _p(ck), _p(bt), _p(qo), int(bool(causal)),
+                            float(scale), _p(rr), nrows if rr is not None else 0,
+                            _p(out), _p(lse))
+    if rc != 0:
+        raise ValueError("oracle_prefill: a referenced page id is out of range")
+    if rr is None:
+        return out.reshape(total_q, Hq, Dv), lse.reshape(total_q, Hq)
+    return out, lse

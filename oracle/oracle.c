@@ -1,0 +1,253 @@
+/*
+ * oracle.c -- plain fp64 CPU oracle for attention forward over a paged KV cache.
+ *
+ * TEST INFRASTRUCTURE ONLY.  Nothing on the product path may link, load or
+ * call this file; only the tests, the package's smoke check and the bench's
+ * CPU-baseline leg do.  It shares no code, header or table with the CUDA
+ * library.
+ *
+ * What it computes (the plain definition, evaluated directly):
+ *   out[i, h] = sum_j softmax_j(scale * <q[i, h], k_j>) * v_j
+ *   lse[i, h] = log(sum_j exp(scale * <q[i, h], k_j>))       (natural log)
+ * over the key set J of query row i:
+ *   - keys live in 64-row pages; logical key j of sequence b is row j % 64 of
+ *     physical page block_table[b, j / 64]  (FlashMLA "Tensor Shapes
+ *     Reference", section "Prefill to Cache Mapping"; the paged K/V blocks of
+ *     section 1, flash_mla_with_kvcache, one 64 x D slab per page and head);
+ *   - query head h reads KV head h / (Hq / Hk), contiguous groups (same page,
+ *     "Grouped-Query Attention" diagram: q heads 0-1 -> kv head 0, ...);
+ *   - only keys j < seq_len are used: "unused slots ignored via seq_lens"
+ *     (section 1 notes);
+ *   - with causal masking, query row i of a segment sees key j iff
+ *     j <= qo_offset + i, where qo_offset defaults to kv_len - q_len (MATE
+ *     msa_interface, _normalize_qo_offset and _resolve_seqused_k);
+ *   - MLA (Modular flare_mla_prefill): the last rope_dim entries of each q row
+ *     pair with k_rope[token, 0, :], one row shared by all heads; the first
+ *     q_depth - rope_dim pair with the per-head k.
+ * Every element is decoded exactly to double before use (bf16: the upper half
+ * of an fp32 word; e4m3: sign, 4-bit exponent with bias 7, 3-bit mantissa,
+ * subnormals, S.1111.111 = NaN, times the per-KV-head scale).  Scores, maximum,
+ * sum and output are formed in double with a two-pass softmax: no online
+ * rescaling, no splits, no tiles.  An empty key set gives out = 0 and
+ * lse = -inf (the pages are silent on this case; this is the reading used).
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+#ifdef _OPENMP
+#include <omp.h>
+#endif
+
+#define ORACLE_PAGE 64
+
+int oracle_num_threads(void) {
+#ifdef _OPENMP
+    return omp_get_max_threads();
+#else
+    return 1;
+#endif
+}
+
+void oracle_set_num_threads(int n) {
+#ifdef _OPENMP
+    if (n > 0) omp_set_num_threads(n);
+#else
+    (void)n;
+#endif
+}
+
+/* bf16 -> double: the 16 bits are the high half of an IEEE binary32 word. */
+double oracle_bf16_to_double(uint16_t bits) {
+    uint32_t w = ((uint32_t)bits) << 16;
+    float f;
+    memcpy(&f, &w, sizeof f);
+    return (double)f;
+}
+
+/* OCP FP8 E4M3 ("fn": no infinities) -> double. */
+double oracle_e4m3_to_double(uint8_t bits) {
+    int sign = (bits >> 7) & 1;
+    int e = (bits >> 3) & 15;
+    int m = bits & 7;
+    double mag;
+    if (e == 15 && m == 7) return NAN;
+    if (e == 0)
+        mag = ldexp((double)m / 8.0, -6);          /* subnormal: 2^-6 * m/8 */
+    else
+        mag = ldexp(1.0 + (double)m / 8.0, e - 7); /* normal: 2^(e-7) * 1.m */
+    return sign ? -mag : mag;
+}
+
+/* Element decoders over raw buffers: kind 0 = bf16 (uint16), 1 = e4m3 (uint8). */
+static double load_elem(const void* base, int kind, int64_t idx) {
+    if (kind == 0) return oracle_bf16_to_double(((const uint16_t*)base)[idx]);
+    return oracle_e4m3_to_double(((const uint8_t*)base)[idx]);
+}
+
+/*
+ * Attention for one query row over n keys whose rows are already decoded:
+ *   q[dqk], kd[n][dqk], vd[n][dv]  ->  out[dv], *lse.
+ * Two passes: scores and their maximum, then exp-weights, sum, weighted V.
+ */
+static void attend_row(const double* q, const double* kd, const double* vd, int64_t n,
+                       int dqk, int dv, double scale, double* s, double* out, double* lse) {
+    for (int d = 0; d < dv; ++d) out[d] = 0.0;
+    if (n == 0) {
+        *lse = -INFINITY;
+        return;
+    }
+    double m = -INFINITY;
+    for (int64_t j = 0; j < n; ++j) {
+        double acc = 0.0;
+        for (int d = 0; d < dqk; ++d) acc += q[d] * kd[j * dqk + d];
+        s[j] = scale * acc;
+        if (s[j] > m) m = s[j];
+    }
+    double l = 0.0;
+    for (int64_t j = 0; j < n; ++j) {
+        double p = exp(s[j] - m);
+        l += p;
+        for (int d = 0; d < dv; ++d) out[d] += p * vd[j * dv + d];
+    }
+    for (int d = 0; d < dv; ++d) out[d] /= l;
+    *lse = m + log(l);
+}
+
+/*
+ * Single-token decode over a paged cache.
+ *   q        bf16 [B, Hq, D]
+ *   k_pool   [P, Hk, 64, D] of kind kv_kind (0 bf16, 1 e4m3); v_pool the same
+ *   k_scale, v_scale  double [Hk] dequantisation scales (NULL -> 1)
+ *   block_table int32 [B, max_pages]; seq_lens int32 [B]
+ *   out double [B, Hq, D]; lse double [B, Hq]
+ * Returns 0, or -1 when a referenced page id is outside [0, P) or
+ * seq_len > max_pages * 64 (the row is then left as zeros / NaN).
+ */
+int oracle_decode(int B, int Hq, int Hk, int D, int max_pages, int64_t num_pages, int kv_kind,
+                  const uint16_t* q, const void* k_pool, const void* v_pool,
+                  const double* k_scale, const double* v_scale,
+                  const int32_t* block_table, const int32_t* seq_lens, double scale,
+                  double* out, double* lse) {
+    int bad = 0;
+    int group = Hq / Hk;
+#pragma omp parallel for schedule(dynamic, 1) reduction(| : bad)
+    for (int64_t bh = 0; bh < (int64_t)B * Hq; ++bh) {
+        int b = (int)(bh / Hq), h = (int)(bh % Hq);
+        int kvh = h / group;
+        int64_t n = seq_lens[b] > 0 ? seq_lens[b] : 0;
+        double* o = out + bh * D;
+        if (n > (int64_t)max_pages * ORACLE_PAGE) {
+            for (int d = 0; d < D; ++d) o[d] = NAN;
+            lse[bh] = NAN;
+            bad |= 1;
+            continue;
+        }
+        double* qd = (double*)malloc(sizeof(double) * D);
+        double* kd = (double*)malloc(sizeof(double) * (size_t)(n ? n : 1) * D);
+        double* vd = (double*)malloc(sizeof(double) * (size_t)(n ? n : 1) * D);
+        double* s = (double*)malloc(sizeof(double) * (size_t)(n ? n : 1));
+        double ks = k_scale ? k_scale[kvh] : 1.0, vs = v_scale ? v_scale[kvh] : 1.0;
+        for (int d = 0; d < D; ++d) qd[d] = oracle_bf16_to_double(q[bh * D + d]);
+        int ok = 1;
+        for (int64_t j = 0; j < n && ok; ++j) {
+            int64_t page = block_table[(int64_t)b * max_pages + j / ORACLE_PAGE];
+            if (page < 0 || page >= num_pages) { ok = 0; break; }
+            int64_t row = ((page * Hk + kvh) * ORACLE_PAGE + j % ORACLE_PAGE) * D;
+            for (int d = 0; d < D; ++d) {
+                kd[j * D + d] = load_elem(k_pool, kv_kind, row + d) * ks;
+                vd[j * D + d] = load_elem(v_pool, kv_kind, row + d) * vs;
+            }
+        }
+        if (ok) {
+            attend_row(qd, kd, vd, n, D, D, scale, s, o, &lse[bh]);
+        } else {
+            for (int d = 0; d < D; ++d) o[d] = NAN;
+            lse[bh] = NAN;
+            bad |= 1;
+        }
+        free(qd); free(kd); free(vd); free(s);
+    }
+    return bad ? -1 : 0;
+}
+
+/*
+ * Prefill / ragged attention (chunked causal against a paged cache, ragged
+ * causal, and the MLA shape with a shared rope key).
+ *   q      bf16 [total_q, Hq, Dqk]
+ *   k      paged: bf16 [P, Hk, 64, Dk]   ragged: bf16 [total_k, Hk, Dk]
+ *   v      paged: bf16 [P, Hk, 64, Dv]   ragged: bf16 [total_k, Hk, Dv]
+ *          with Dk = Dqk - rope_dim
+ *   k_rope bf16 [total_k, 1, rope_dim] (ragged only), or NULL with rope_dim 0
+ *   cu_q, cu_k  int32 [B+1] running offsets of query rows / keys
+ *   block_table int32 [B, max_pages] or NULL (ragged keys)
+ *   qo_offset   int32 [B] or NULL (-> kv_len - q_len)
+ *   rows   optional list of (token * Hq + h) rows to evaluate (NULL: all);
+ *          out/lse are then [nrows, Dv] / [nrows]
+ * Returns 0, or -1 on an out-of-range page id.
+ */
+int oracle_prefill(int B, int Hq, int Hk, int Dqk, int Dv, int rope_dim, int max_pages,
+                   int64_t num_pages, const uint16_t* q, const uint16_t* k, const uint16_t* v,
+                   const uint16_t* k_rope, const int32_t* cu_q, const int32_t* cu_k,
+                   const int32_t* block_table, const int32_t* qo_offset, int causal,
+                   double scale, const int64_t* rows, int64_t nrows, double* out, double* lse) {
+    int group = Hq / Hk;
+    int Dk = Dqk - rope_dim;
+    int64_t total_q = cu_q[B];
+    if (!rows) nrows = total_q * Hq;
+    int bad = 0;
+#pragma omp parallel for schedule(dynamic, 1) reduction(| : bad)
+    for (int64_t r = 0; r < nrows; ++r) {
+        int64_t flat = rows ? rows[r] : r;
+        int64_t tok = flat / Hq;
+        int h = (int)(flat % Hq);
+        int kvh = h / group;
+        /* the segment holding this query token */
+        int b = 0;
+        while (b < B - 1 && cu_q[b + 1] <= tok) ++b;
+        int64_t i = tok - cu_q[b];
+        int64_t q_len = cu_q[b + 1] - cu_q[b];
+        int64_t kv_len = cu_k[b + 1] - cu_k[b];
+        int64_t off = qo_offset ? qo_offset[b] : kv_len - q_len;
+        int64_t n = kv_len;
+        if (causal) {
+            int64_t lim = off + i + 1; /* keys 0 .. off + i */
+            if (lim < n) n = lim;
+            if (n < 0) n = 0;
+        }
+        double* o = out + r * Dv;
+        double* qd = (double*)malloc(sizeof(double) * Dqk);
+        double* kd = (double*)malloc(sizeof(double) * (size_t)(n ? n : 1) * Dqk);
+        double* vd = (double*)malloc(sizeof(double) * (size_t)(n ? n : 1) * Dv);
+        double* s = (double*)malloc(sizeof(double) * (size_t)(n ? n : 1));
+        for (int d = 0; d < Dqk; ++d) qd[d] = oracle_bf16_to_double(q[(tok * Hq + h) * Dqk + d]);
+        int ok = 1;
+        for (int64_t j = 0; j < n; ++j) {
+            int64_t krow, vrow;
+            if (block_table) {
+                int64_t page = block_table[(int64_t)b * max_pages + j / ORACLE_PAGE];
+                if (page < 0 || page >= num_pages) { ok = 0; break; }
+                int64_t slab = (page * Hk + kvh) * ORACLE_PAGE + j % ORACLE_PAGE;
+                krow = slab * Dk;
+                vrow = slab * Dv;
+            } else {
+                int64_t t = cu_k[b] + j;
+                krow = (t * Hk + kvh) * Dk;
+                vrow = (t * Hk + kvh) * Dv;
+            }
+            for (int d = 0; d < Dk; ++d) kd[j * Dqk + d] = oracle_bf16_to_double(k[krow + d]);
+            for (int d = 0; d < rope_dim; ++d)
+                kd[j * Dqk + Dk + d] = oracle_bf16_to_double(k_rope[(cu_k[b] + j) * rope_dim + d]);
+            for (int d = 0; d < Dv; ++d) vd[j * Dv + d] = oracle_bf16_to_double(v[vrow + d]);
+        }
+        if (ok) {
+            attend_row(qd, kd, vd, n, Dqk, Dv, scale, s, o, &lse[r]);
+        } else {
+            for (int d = 0; d < Dv; ++d) o[d] = NAN;
+            lse[r] = NAN;
+            bad |= 1;
+        }
+        free(qd); free(kd); free(vd); free(s);
+    }
+    return bad ? -1 : 0;
+}

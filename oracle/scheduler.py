@@ -1,0 +1,116 @@
+"""Oracle for the split-KV scheduler: a plain restatement of the split rule.
+
+TEST INFRASTRUCTURE ONLY (see the package header in ``oracle/__init__``).
+
+The pages fix the ingredients and leave the rule open.  MATE's
+``msa_interface`` passes ``num_splits`` (0 = choose automatically) and
+``page_size`` to ``get_scheduler_metadata`` and counts pages per sequence as
+``ceil(kv_len / page_size)`` (``_page_counts``); FlashMLA's ``get_mla_metadata``
+(section 2 of its "Tensor Shapes Reference") takes the shapes, the block table
+and ``seq_lens`` and returns the metadata the decode kernel consumes.  The
+reading used here, written out step by step:
+
+  pages_b   = ceil(max(seq_b, 0) / 64)
+  units     = sum_b pages_b * Hk
+  cap       = num_sms * ctas_per_sm                      (persistent CTAs)
+  chunk     = max(4, ceil(units / (cap * 4)))            (4 items per CTA share)
+  n_b       = 1                              if pages_b <= 1
+            = min(forced, pages_b, 64)       if forced > 0
+            = min(ceil(pages_b / chunk), 64) otherwise
+  split s of sequence b covers pages [floor(s P / n), floor((s+1) P / n))
+  items     = (b, s, kvh) in (b, s, kvh) order, cost = pages of the split + 1
+  grid      = min(#items, cap)
+  assignment: items sorted by (cost descending, index ascending); each goes to
+            the CTA with the smallest (load, CTA index); its load grows by cost.
+
+Packed metadata (int32), the layout the library's scheduler must reproduce
+bit for bit:
+  [0] 0x50414D31  [1] B  [2] Hk  [3] total_splits  [4] num_items  [5] grid
+  [6] chunk  [7] ctas_per_sm
+  n_splits[B], split_indptr[B+1], cta_indptr[grid+1],
+  items[2 * num_items] as (b, (s << 16) | kvh) in per-CTA assignment order.
+"""
+from __future__ import annotations
+
+import heapq
+
+MAGIC = 0x50414D31
+PAGE = 64
+MAX_SPLITS = 64
+ITEMS_PER_SHARE = 4
+MIN_CHUNK = 4
+
+
+def _cdiv(a: int, b: int) -> int:
+    return -(-a // b)
+
+
+def split_counts(seq_lens, num_kv_heads: int, num_sms: int, ctas_per_sm: int,
+                 forced_splits: int = 0):
+    pages = [_cdiv(max(int(s), 0), PAGE) for s in seq_lens]
+    units = sum(pages) * num_kv_heads
+    cap = num_sms * ctas_per_sm
+    chunk = max(MIN_CHUNK, _cdiv(units, cap * ITEMS_PER_SHARE))
+    n = []
+    for p in pages:
+        if p <= 1:
+            n.append(1)
+        elif forced_splits > 0:
+            n.append(min(forced_splits, p, MAX_SPLITS))
+        else:
+            n.append(min(_cdiv(p, chunk), MAX_SPLITS))
+    return pages, n, chunk
+
+
+def split_range(pages: int, nsplit: int, s: int):
+    return (s * pages) // nsplit, ((s + 1) * pages) // nsplit
+
+
+def schedule(seq_lens, num_kv_heads: int, num_sms: int, ctas_per_sm: int,
+             forced_splits: int = 0):
+    """Return the packed metadata as a list of Python ints."""
+    B = len(seq_lens)
+    pages, n, chunk = split_counts(seq_lens, num_kv_heads, num_sms, ctas_per_sm, forced_splits)
+    indptr = [0]
+    for x in n:
+        indptr.append(indptr[-1] + x)
+    items = []  # (cost, index, b, s, kvh)
+    for b in range(B):
+        for s in range(n[b]):
+            lo, hi = split_range(pages[b], n[b], s)
+            for kvh in range(num_kv_heads):
+                items.append((hi - lo + 1, len(items), b, s, kvh))
+    cap = num_sms * ctas_per_sm
+    grid = min(len(items), cap)
+    order = sorted(items, key=lambda it: (-it[0], it[1]))
+    heap = [(0, c) for c in range(grid)]
+    per_cta = [[] for _ in range(grid)]
+    for cost, _, b, s, kvh in order:
+        load, c = heapq.heappop(heap)
+        per_cta[c].append((b, s, kvh))
+        heapq.heappush(heap, (load + cost, c))
+    out = [MAGIC, B, num_kv_heads, indptr[-1], len(items), grid, chunk, ctas_per_sm]
+    out += n
+    out += indptr
+    cta_ptr = [0]
+    for lst in per_cta:
+        cta_ptr.append(cta_ptr[-1] + len(lst))
+    out += cta_ptr
+    for lst in per_cta:
+        for b, s, kvh in lst:
+            out += [b, (s << 16) | kvh]
+    return out
+
+
+def unpack(meta):
+    """Split packed metadata into its named parts (for tests)."""
+    B, hk, total, nitems, grid = meta[1], meta[2], meta[3], meta[4], meta[5]
+    o = 8
+    n = list(meta[o:o + B]); o += B
+    indptr = list(meta[o:o + B + 1]); o += B + 1
+    cta_ptr = list(meta[o:o + grid + 1]); o += grid + 1
+    raw = list(meta[o:o + 2 * nitems]); o += 2 * nitems
+    items = [(raw[2 * i], raw[2 * i + 1] >> 16, raw[2 * i + 1] & 0xFFFF) for i in range(nitems)]
+    return dict(batch=B, num_kv_heads=hk, total_splits=total, num_items=nitems, grid=grid,
+                chunk=meta[6], ctas_per_sm=meta[7], n_splits=n, split_indptr=indptr,
+                cta_indptr=cta_ptr, items=items, length=o)

@@ -1,0 +1,341 @@
+"""Pins for the CPU oracle: closed forms, invariants, page-printed fixtures and
+library routines (torch CPU float64), chosen so that a dropped term, a wrong
+index, sign or grouping in the oracle fails at least one of them."""
+import math
+import os
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from paged_kv_attention_fwd_gb300 import workloads as W
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def _golden(name):
+    rows = []
+    with open(os.path.join(GOLDEN, name)) as f:
+        for line in f:
+            line = line.strip()
+            if line and not line.startswith("#"):
+                rows.append([int(x) for x in line.split()])
+    return np.array(rows)
+
+
+def t_bf16(bits):
+    """bf16 bit patterns -> float64 through torch's own bfloat16 type."""
+    return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).view(torch.bfloat16).to(torch.float64)
+
+
+def t_e4m3(bits):
+    return torch.from_numpy(np.ascontiguousarray(bits)).view(torch.float8_e4m3fn).to(torch.float64)
+
+
+# ---------------------------------------------------------------- element decoders
+
+def test_bf16_decoder_all_codes():
+    codes = np.arange(65536, dtype=np.uint32).astype(np.uint16)
+    ref = t_bf16(codes).numpy()
+    got = oracle.bf16_to_f64(codes)
+    nan = np.isnan(ref)
+    assert np.array_equal(np.isnan(got), nan)
+    assert np.array_equal(got[~nan], ref[~nan])
+
+
+def test_e4m3_decoder_all_codes():
+    codes = np.arange(256, dtype=np.uint8)
+    ref = t_e4m3(codes).numpy()
+    got = oracle.e4m3_to_f64(codes)
+    nan = np.isnan(ref)
+    assert nan.sum() == 2  # S.1111.111
+    assert np.array_equal(np.isnan(got), nan)
+    assert np.array_equal(got[~nan], ref[~nan])
+    assert got[0x7E] == 448.0 and got[0x01] == 2.0 ** -9
+
+
+def test_generator_encoders_match_torch():
+    x = W.normal_f32(3, 99, 20000) * np.float32(40.0)
+    ref = torch.from_numpy(x).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    assert np.array_equal(W.f32_to_bf16_bits(x), ref)
+    xc = np.clip(x, -448, 448)
+    ref8 = torch.from_numpy(xc).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    assert np.array_equal(W.f32_to_e4m3_bits(xc), ref8)
+    # saturation beyond the largest finite value
+    assert W.f32_to_e4m3_bits(np.array([1e6, -1e6])).tolist() == [0x7E, 0xFE]
+
+
+# ---------------------------------------------------------------- library cross-check
+
+def _gather_dense(pool, bt_row, n):
+    """[Hk, n, D] keys of one sequence via torch indexing (a route independent of the oracle)."""
+    pages = torch.as_tensor(bt_row[: (n + 63) // 64], dtype=torch.long)
+    blk = pool[pages]                          # [np, Hk, 64, D]
+    return blk.permute(1, 0, 2, 3).reshape(pool.shape[1], -1, pool.shape[-1])[:, :n]
+
+
+def _sdpa(q, k, v, scale, mask=None):
+    """torch float64 attention; q [H, Lq, D], k/v [H, Lk, *]; returns out, lse."""
+    out = torch.nn.functional.scaled_dot_product_attention(
+        q[None], k[None], v[None], attn_mask=mask, scale=scale)[0]
+    s = (q @ k.transpose(-1, -2)) * scale
+    if mask is not None:
+        s = s.masked_fill(~mask, float("-inf"))
+    return out, torch.logsumexp(s, dim=-1)
+
+
+@pytest.mark.parametrize("kv_dtype", ["bf16", "e4m3"])
+def test_decode_matches_torch_sdpa(kv_dtype):
+    inp = W.make_decode(3, 8, 2, 64, [1, 65, 200], seed=5, kv_dtype=kv_dtype, extra_pages=3)
+    out, lse = oracle.decode(inp.q, inp.k_pool, inp.v_pool, inp.block_table, inp.seq_lens,
+                             inp.scale, kv_dtype, inp.k_scale, inp.v_scale)
+    dec = t_bf16 if kv_dtype == "bf16" else t_e4m3
+    kp, vp = dec(inp.k_pool), dec(inp.v_pool)
+    if kv_dtype == "e4m3":
+        kp = kp * torch.as_tensor(inp.k_scale, dtype=torch.float64)[None, :, None, None]
+        vp = vp * torch.as_tensor(inp.v_scale, dtype=torch.float64)[None, :, None, None]
+    q = t_bf16(inp.q)
+    G = inp.num_q_heads // inp.num_kv_heads
+    for b, n in enumerate(inp.seq_lens):
+        k = _gather_dense(kp, inp.block_table[b], int(n)).repeat_interleave(G, 0)
+        v = _gather_dense(vp, inp.block_table[b], int(n)).repeat_interleave(G, 0)
+        ro, rl = _sdpa(q[b][:, None, :], k, v, inp.scale)
+        np.testing.assert_allclose(out[b], ro[:, 0].numpy(), rtol=1e-12, atol=1e-12)
+        np.testing.assert_allclose(lse[b], rl[:, 0].numpy(), rtol=1e-12, atol=1e-12)
+
+
+def test_paged_prefill_matches_torch_sdpa():
+    inp = W.make_paged_prefill([5, 70, 1], [40, 200, 64], 4, 2, 64, seed=9, extra_pages=2)
+    out, lse = oracle.prefill(inp.q, inp.k, inp.v, inp.cu_seqlens_q, inp.cu_seqlens_k, inp.scale,
+                              True, block_table=inp.block_table)
+    kp, vp, q = t_bf16(inp.k), t_bf16(inp.v), t_bf16(inp.q)
+    for b in range(inp.batch):
+        q0, q1 = inp.cu_seqlens_q[b], inp.cu_seqlens_q[b + 1]
+        n = int(inp.cu_seqlens_k[b + 1] - inp.cu_seqlens_k[b])
+        lq = q1 - q0
+        k = _gather_dense(kp, inp.block_table[b], n).repeat_interleave(2, 0)
+        v = _gather_dense(vp, inp.block_table[b], n).repeat_interleave(2, 0)
+        mask = torch.ones(lq, n, dtype=torch.bool).tril(diagonal=n - lq)
+        ro, rl = _sdpa(q[q0:q1].transpose(0, 1), k, v, inp.scale, mask)
+        np.testing.assert_allclose(out[q0:q1], ro.transpose(0, 1).numpy(), rtol=1e-12, atol=1e-12)
+        np.testing.assert_allclose(lse[q0:q1], rl.transpose(0, 1).numpy(), rtol=1e-12, atol=1e-12)
+
+
+def test_mla_ragged_matches_concatenated_keys():
+    """MLA reduces exactly to standard attention with K = [k_nope[h], k_rope]."""
+    inp = W.make_ragged_prefill([9, 130], 4, 48, 32, rope_dim=16, seed=2)
+    out, lse = oracle.prefill(inp.q, inp.k, inp.v, inp.cu_seqlens_q, inp.cu_seqlens_k, inp.scale,
+                              True, k_rope=inp.k_rope)
+    q, k, v, kr = t_bf16(inp.q), t_bf16(inp.k), t_bf16(inp.v), t_bf16(inp.k_rope)
+    for b in range(inp.batch):
+        a, e = inp.cu_seqlens_q[b], inp.cu_seqlens_q[b + 1]
+        L = e - a
+        kk = torch.cat([k[a:e], kr[a:e].expand(L, 4, 16)], dim=-1).transpose(0, 1)
+        ro, rl = _sdpa(q[a:e].transpose(0, 1), kk, v[a:e].transpose(0, 1), inp.scale,
+                       torch.ones(L, L, dtype=torch.bool).tril())
+        np.testing.assert_allclose(out[a:e], ro.transpose(0, 1).numpy(), rtol=1e-12, atol=1e-12)
+        np.testing.assert_allclose(lse[a:e], rl.transpose(0, 1).numpy(), rtol=1e-12, atol=1e-12)
+
+
+def test_prefix_zero_is_textbook_causal():
+    inp = W.make_ragged_prefill([33], 2, 32, 32, seed=4)
+    out, lse = oracle.prefill(inp.q, inp.k, inp.v, inp.cu_seqlens_q, inp.cu_seqlens_k, inp.scale, True)
+    q, k, v = (t_bf16(x).transpose(0, 1) for x in (inp.q, inp.k, inp.v))
+    ref = torch.nn.functional.scaled_dot_product_attention(q[None], k[None], v[None], is_causal=True,
+                                                           scale=inp.scale)[0]
+    np.testing.assert_allclose(out, ref.transpose(0, 1).numpy(), rtol=1e-12, atol=1e-12)
+
+
+# ---------------------------------------------------------------- closed forms
+
+def _dec(bits):
+    return t_bf16(bits).numpy()
+
+
+def test_single_key_gives_v0_and_score():
+    inp = W.make_decode(2, 4, 2, 64, [1, 1], seed=11)
+    out, lse = oracle.decode(inp.q, inp.k_pool, inp.v_pool, inp.block_table, inp.seq_lens, inp.scale)
+    for b in range(2):
+        page = inp.block_table[b, 0]
+        for h in range(4):
+            kv = h // 2
+            v0 = _dec(inp.v_pool[page, kv, 0])
+            k0 = _dec(inp.k_pool[page, kv, 0])
+            assert np.array_equal(out[b, h], v0)
+            assert lse[b, h] == pytest.approx(inp.scale * float(np.dot(_dec(inp.q[b, h]), k0)), rel=1e-13)
+
+
+def test_zero_query_gives_mean_of_v_and_log_n():
+    inp = W.make_decode(2, 2, 1, 64, [100, 7], seed=12)
+    inp.q[:] = 0
+    out, lse = oracle.decode(inp.q, inp.k_pool, inp.v_pool, inp.block_table, inp.seq_lens, inp.scale)
+    vp = _dec(inp.v_pool)
+    for b, n in enumerate(inp.seq_lens):
+        rows = np.concatenate([vp[inp.block_table[b, j], 0] for j in range((n + 63) // 64)])[:n]
+        np.testing.assert_allclose(out[b, 0], rows.mean(0), rtol=0, atol=1e-14)
+        assert lse[b, 0] == pytest.approx(math.log(n), abs=1e-14)
+
+
+def test_constant_v_gives_v():
+    inp = W.make_decode(3, 4, 4, 64, [5, 64, 129], seed=13)
+    c = W.f32_to_bf16_bits(np.linspace(-2, 2, 64, dtype=np.float32))
+    inp.v_pool[:] = c
+    out, _ = oracle.decode(inp.q, inp.k_pool, inp.v_pool, inp.block_table, inp.seq_lens, inp.scale)
+    np.testing.assert_allclose(out, np.broadcast_to(_dec(c), out.shape), rtol=0, atol=1e-14)
+
+
+def test_output_in_convex_hull_of_values():
+    inp = W.make_decode(2, 4, 2, 64, [90, 3], seed=14)
+    out, _ = oracle.decode(inp.q, inp.k_pool, inp.v_pool, inp.block_table, inp.seq_lens, inp.scale)
+    vp = _dec(inp.v_pool)
+    for b, n in enumerate(inp.seq_lens):
+        for h in range(4):
+            rows = np.concatenate([vp[inp.block_table[b, j], h // 2] for j in range((n + 63) // 64)])[:n]
+            assert np.all(out[b, h] <= rows.max(0) + 1e-12) and np.all(out[b, h] >= rows.min(0) - 1e-12)
+
+
+def test_empty_key_set():
+    inp = W.make_decode(2, 2, 1, 64, [0, 3], seed=15)
+    out, lse = oracle.decode(inp.q, inp.k_pool, inp.v_pool, inp.block_table, inp.seq_lens, inp.scale)
+    assert np.all(out[0] == 0) and np.all(np.isneginf(lse[0])) and np.all(np.isfinite(lse[1]))
+
+
+# ---------------------------------------------------------------- page-printed fixtures
+
+def test_gqa_grouping_matches_page_diagram():
+    """V of kv head g is the constant g; then out of q head h is exactly its kv head."""
+    table = _golden("gqa_map_hq8_hk4.txt")
+    inp = W.make_decode(1, 8, 4, 64, [77], seed=16)
+    for g in range(4):
+        inp.v_pool[:, g] = W.f32_to_bf16_bits(np.float32([g]))[0]
+    out, _ = oracle.decode(inp.q, inp.k_pool, inp.v_pool, inp.block_table, inp.seq_lens, inp.scale)
+    for qh, kvh in table:
+        np.testing.assert_allclose(out[0, qh], kvh, rtol=1e-14, atol=0)
+        others = [g for g in range(4) if g != kvh]
+        assert all(np.all(np.abs(out[0, qh] - g) > 0.5) for g in others)
+
+
+def test_token_to_page_mapping_matches_page_diagram():
+    """With q = 0 the output is the mean of the visible V rows; marking the rows of
+    one physical page with 1 reveals exactly which tokens that page serves."""
+    table = _golden("token_page_map.txt")
+    n = 192
+    inp = W.make_decode(1, 1, 1, 64, [n], seed=17, extra_pages=2)
+    inp.q[:] = 0
+    one = W.f32_to_bf16_bits(np.float32([1.0]))[0]
+    for first, last, col in table:
+        inp.v_pool[:] = 0
+        inp.v_pool[inp.block_table[0, col]] = one
+        out, _ = oracle.decode(inp.q, inp.k_pool, inp.v_pool, inp.block_table, inp.seq_lens, inp.scale)
+        np.testing.assert_allclose(out[0, 0], (last - first + 1) / n, atol=1e-15)
+        # shortening the sequence to end inside this range keeps only its first tokens
+        m = first + 10
+        out2, _ = oracle.decode(inp.q, inp.k_pool, inp.v_pool, inp.block_table, np.array([m], np.int32),
+                                inp.scale)
+        np.testing.assert_allclose(out2[0, 0], 10 / m, atol=1e-15)
+
+
+# ---------------------------------------------------------------- invariants
+
+def test_page_permutation_invariance_exact():
+    inp = W.make_decode(3, 4, 2, 64, [64, 150, 20], seed=18, extra_pages=4)
+    out, lse = oracle.decode(inp.q, inp.k_pool, inp.v_pool, inp.block_table, inp.seq_lens, inp.scale)
+    perm = np.random.default_rng(0).permutation(inp.num_pool_pages)
+    inv = np.argsort(perm)
+    k2 = inp.k_pool[perm]     # new page i holds old page perm[i]
+    v2 = inp.v_pool[perm]
+    bt2 = inv[inp.block_table].astype(np.int32)
+    out2, lse2 = oracle.decode(inp.q, k2, v2, bt2, inp.seq_lens, inp.scale)
+    assert np.array_equal(out, out2) and np.array_equal(lse, lse2)
+
+
+@pytest.mark.parametrize("kv_dtype", ["bf16", "e4m3"])
+def test_poisoned_unused_rows_and_slots_change_nothing(kv_dtype):
+    inp = W.make_decode(3, 4, 2, 64, [37, 130, 64], seed=19, kv_dtype=kv_dtype, extra_pages=3,
+                        max_pages=5)
+    args = (inp.scale, kv_dtype, inp.k_scale, inp.v_scale)
+    out, lse = oracle.decode(inp.q, inp.k_pool, inp.v_pool, inp.block_table, inp.seq_lens, *args)
+    p = W.poison_stale_slots(W.poison_unused(inp))
+    out2, lse2 = oracle.decode(p.q, p.k_pool, p.v_pool, p.block_table, p.seq_lens, *args)
+    assert np.array_equal(out, out2) and np.array_equal(lse, lse2)
+    assert np.all(np.isfinite(out2))
+
+
+def test_decode_equals_prefill_with_one_query_row():
+    inp = W.make_decode(3, 4, 2, 64, [1, 100, 257], seed=20)
+    out, lse = oracle.decode(inp.q, inp.k_pool, inp.v_pool, inp.block_table, inp.seq_lens, inp.scale)
+    cu_q = W.cu_seqlens(np.ones(3, np.int32))
+    cu_k = W.cu_seqlens(inp.seq_lens)
+    out2, lse2 = oracle.prefill(inp.q, inp.k_pool, inp.v_pool, cu_q, cu_k, inp.scale, True,
+                                block_table=inp.block_table)
+    np.testing.assert_allclose(out2, out, rtol=0, atol=1e-15)
+    np.testing.assert_allclose(lse2, lse, rtol=0, atol=1e-15)
+
+
+def test_chunk_row_equals_decode_at_its_length():
+    """Row i of a causal chunk with offset o sees exactly keys 0 .. o + i."""
+    inp = W.make_paged_prefill([20], [150], 2, 2, 64, seed=21)
+    out, lse = oracle.prefill(inp.q, inp.k, inp.v, inp.cu_seqlens_q, inp.cu_seqlens_k, inp.scale,
+                              True, block_table=inp.block_table)
+    off = 150 - 20
+    for i in (0, 7, 19):
+        lens = np.array([off + i + 1], np.int32)
+        o, l = oracle.decode(inp.q[i:i + 1], inp.k, inp.v, inp.block_table, lens, inp.scale)
+        np.testing.assert_allclose(out[i], o[0], rtol=0, atol=1e-15)
+        np.testing.assert_allclose(lse[i], l[0], rtol=0, atol=1e-15)
+
+
+def test_explicit_qo_offset_and_non_causal():
+    inp = W.make_paged_prefill([8, 8], [64, 100], 2, 1, 64, seed=22)
+    default = oracle.prefill(inp.q, inp.k, inp.v, inp.cu_seqlens_q, inp.cu_seqlens_k, inp.scale, True,
+                             block_table=inp.block_table)
+    explicit = oracle.prefill(inp.q, inp.k, inp.v, inp.cu_seqlens_q, inp.cu_seqlens_k, inp.scale, True,
+                              block_table=inp.block_table, qo_offset=np.array([56, 92], np.int32))
+    assert np.array_equal(default[0], explicit[0])
+    # an offset past the end sees every key: same as non-causal
+    wide = oracle.prefill(inp.q, inp.k, inp.v, inp.cu_seqlens_q, inp.cu_seqlens_k, inp.scale, True,
+                          block_table=inp.block_table, qo_offset=np.array([1000, 1000], np.int32))
+    nc = oracle.prefill(inp.q, inp.k, inp.v, inp.cu_seqlens_q, inp.cu_seqlens_k, inp.scale, False,
+                        block_table=inp.block_table)
+    assert np.array_equal(wide[0], nc[0])
+    # a negative offset hides keys; row i sees min(kv_len, max(i + 1 + off, 0)) keys
+    neg = oracle.prefill(inp.q, inp.k, inp.v, inp.cu_seqlens_q, inp.cu_seqlens_k, inp.scale, True,
+                         block_table=inp.block_table, qo_offset=np.array([-3, 0], np.int32))
+    assert np.all(np.isneginf(neg[1][:3, :])) and np.all(np.isfinite(neg[1][3:8]))
+
+
+def test_ragged_equals_separate_calls():
+    inp = W.make_ragged_prefill([5, 40, 17], 4, 32, 32, seed=23, num_kv_heads=2)
+    out, lse = oracle.prefill(inp.q, inp.k, inp.v, inp.cu_seqlens_q, inp.cu_seqlens_k, inp.scale, True)
+    for b in range(3):
+        a, e = inp.cu_seqlens_q[b], inp.cu_seqlens_q[b + 1]
+        cu = np.array([0, e - a], np.int32)
+        o, l = oracle.prefill(inp.q[a:e], inp.k[a:e], inp.v[a:e], cu, cu, inp.scale, True)
+        assert np.array_equal(o, out[a:e]) and np.array_equal(l, lse[a:e])
+
+
+def test_row_sampling_matches_full():
+    inp = W.make_ragged_prefill([30, 45], 4, 32, 32, seed=24, rope_dim=0)
+    out, lse = oracle.prefill(inp.q, inp.k, inp.v, inp.cu_seqlens_q, inp.cu_seqlens_k, inp.scale, True)
+    rows = np.array([0, 5, 4 * 30 + 3, 4 * 74 + 3], np.int64)
+    o, l = oracle.prefill(inp.q, inp.k, inp.v, inp.cu_seqlens_q, inp.cu_seqlens_k, inp.scale, True,
+                          rows=rows)
+    flat_o = out.reshape(-1, 32)
+    assert np.array_equal(o, flat_o[rows]) and np.array_equal(l, lse.reshape(-1)[rows])
+
+
+def test_fp8_scales_fold_into_scores_and_values():
+    """Dequantisation multiplies each element by its head's scale: doubling the
+    K scale doubles every score (same as doubling the softmax scale) and the
+    V scale multiplies the output."""
+    inp = W.make_decode(2, 4, 2, 64, [70, 9], seed=25, kv_dtype="e4m3")
+    base = oracle.decode(inp.q, inp.k_pool, inp.v_pool, inp.block_table, inp.seq_lens, inp.scale,
+                         "e4m3", inp.k_scale, inp.v_scale)
+    o2 = oracle.decode(inp.q, inp.k_pool, inp.v_pool, inp.block_table, inp.seq_lens, 2 * inp.scale,
+                       "e4m3", inp.k_scale, 3 * inp.v_scale.astype(np.float64))
+    o3 = oracle.decode(inp.q, inp.k_pool, inp.v_pool, inp.block_table, inp.seq_lens, inp.scale,
+                       "e4m3", 2 * inp.k_scale.astype(np.float64), inp.v_scale)
+    np.testing.assert_allclose(o2[0], 3 * o3[0], rtol=1e-12, atol=1e-13)
+    np.testing.assert_allclose(o2[1], o3[1], rtol=1e-12)
+    assert not np.allclose(base[0], o3[0])

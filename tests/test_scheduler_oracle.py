@@ -1,0 +1,90 @@
+"""Pins for the oracle's split-KV scheduler: a hand-worked fixture and the
+partition / balance properties the rule guarantees."""
+import os
+
+import numpy as np
+import pytest
+
+from oracle import scheduler as S
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def load_schedule_fixture(name="schedule_small.txt"):
+    vals = {}
+    with open(os.path.join(GOLDEN, name)) as f:
+        for line in f:
+            if line.startswith("#") or not line.strip():
+                continue
+            key, *rest = line.split()
+            vals[key] = [int(x) for x in rest]
+    return vals
+
+
+def test_hand_worked_fixture():
+    g = load_schedule_fixture()
+    meta = S.schedule(g["seq_lens"], g["num_kv_heads"][0], g["num_sms"][0], g["ctas_per_sm"][0],
+                      g["forced_splits"][0])
+    assert meta == g["meta"]
+    assert g["meta"][0] == 0x50414D31
+
+
+def check_properties(seq_lens, hk, sms, cps, forced):
+    meta = S.schedule(seq_lens, hk, sms, cps, forced)
+    u = S.unpack(meta)
+    assert u["length"] == len(meta)
+    pages = [-(-max(s, 0) // 64) for s in seq_lens]
+    n = u["n_splits"]
+    assert u["split_indptr"][0] == 0 and u["split_indptr"][-1] == u["total_splits"] == sum(n)
+    for b, p in enumerate(pages):
+        assert 1 <= n[b] <= 64
+        if forced > 0 and p > 1:
+            assert n[b] == min(forced, p, 64)
+        # splits tile [0, p) contiguously and in order, non-empty when p >= n
+        ranges = [S.split_range(p, n[b], s) for s in range(n[b])]
+        assert ranges[0][0] == 0 and ranges[-1][1] == p
+        for (a0, a1), (b0, b1) in zip(ranges, ranges[1:]):
+            assert a1 == b0
+        if p > 0:
+            assert all(hi > lo for lo, hi in ranges)
+    # every (b, s, kvh) appears exactly once
+    want = {(b, s, k) for b in range(len(seq_lens)) for s in range(n[b]) for k in range(hk)}
+    assert len(u["items"]) == len(want) and set(u["items"]) == want
+    assert u["grid"] == min(len(want), sms * cps)
+    # list scheduling bound: max load - min load <= max item cost
+    cost = {}
+    for b in range(len(seq_lens)):
+        for s in range(n[b]):
+            lo, hi = S.split_range(pages[b], n[b], s)
+            for k in range(hk):
+                cost[(b, s, k)] = hi - lo + 1
+    cp = u["cta_indptr"]
+    loads = [sum(cost[it] for it in u["items"][cp[c]:cp[c + 1]]) for c in range(u["grid"])]
+    assert max(loads) - min(loads) <= max(cost.values())
+    # items inside one CTA run longest first
+    for c in range(u["grid"]):
+        cs = [cost[it] for it in u["items"][cp[c]:cp[c + 1]]]
+        assert cs == sorted(cs, reverse=True)
+    return u
+
+
+@pytest.mark.parametrize("forced", [0, 1, 2, 7])
+def test_properties_uniform(forced):
+    rng = np.random.default_rng(1)
+    lens = rng.integers(1, 4097, size=64).tolist()
+    check_properties(lens, 8, 152, 1, forced)
+
+
+def test_properties_lognormal_and_edges():
+    rng = np.random.default_rng(2)
+    lens = np.clip(np.floor(np.exp(np.log(2048) + rng.standard_normal(128))), 64, 16384).astype(int)
+    u = check_properties(lens.tolist(), 8, 152, 1, 0)
+    assert u["total_splits"] > 128  # long sequences do get split
+    check_properties([0, 0, 1, 64, 65, 128, 129], 3, 4, 2, 0)
+    check_properties([16384] * 3, 1, 152, 1, 0)
+    check_properties([5], 1, 1, 1, 0)
+
+
+def test_deterministic():
+    lens = list(range(0, 5000, 37))
+    assert S.schedule(lens, 4, 152, 1) == S.schedule(lens, 4, 152, 1)
