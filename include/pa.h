@@ -1,0 +1,225 @@
+/*
+ * pa.h -- C ABI of libpa: attention forward over a paged KV cache on GB300 (sm_103a).
+ *
+ *   out[i, h] = sum_j softmax_j(scale * <q[i, h], k_j>) * v_j      (bf16)
+ *   lse[i, h] = ln sum_j exp(scale * <q[i, h], k_j>)               (fp32, natural log)
+ *
+ * Keys and values live in 64-row pages.  Logical key j of sequence b is row
+ * j % 64 of physical page block_table[b, j / 64] (FlashMLA "Tensor Shapes
+ * Reference", diagram "Prefill to Cache Mapping"); query head h reads KV head
+ * h / (Hq / Hk), contiguous groups (same page, diagram "Grouped-Query
+ * Attention").  Keys at or past seq_len are never read ("unused slots ignored
+ * via seq_lens", section 1 notes).  An empty key set yields out = 0 and
+ * lse = -inf.
+ *
+ * Conventions shared by every call:
+ *  - Ownership: the caller allocates and owns every buffer.  The library never
+ *    allocates device memory and never synchronises inside pa_decode /
+ *    pa_prefill; work is enqueued on `stream` and runs asynchronously.
+ *  - Pointers named *_host are host memory; every other pointer is device
+ *    memory on the current device, 16-byte aligned, contiguous in the layout
+ *    given.
+ *  - Errors: arguments are validated on the host before anything is enqueued;
+ *    a failing check returns a non-zero pa_status and leaves a message for
+ *    pa_last_error().  Faults the kernels detect themselves (a page id out of
+ *    range, a wait that ran past its time limit) are recorded in the status
+ *    word at the start of the caller's workspace and reported by
+ *    pa_check_status().  Nothing traps.
+ *  - Page size is 64 ("Blk: block size for paged cache (always 64)").
+ *  - The pool layout is [num_pool_pages, Hk, 64, D] ("HND"): each (page, KV
+ *    head) is one contiguous 64 x D slab (the "64 rows x D cols (contiguous
+ *    slab)" of the paged-cache diagram).
+ */
+#ifndef PA_H_
+#define PA_H_
+
+#include <stddef.h>
+#include <stdint.h>
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    PA_OK = 0,
+    PA_ERR_INVALID_ARG = 1,   /* a pointer, shape or value check failed on the host */
+    PA_ERR_UNSUPPORTED = 2,   /* valid but outside what the kernels implement */
+    PA_ERR_WORKSPACE = 3,     /* metadata or workspace buffer too small */
+    PA_ERR_CUDA = 4,          /* a CUDA runtime call failed */
+    PA_ERR_TIMEOUT = 5,       /* (device) a wait ran past its time limit */
+    PA_ERR_DEVICE_BOUNDS = 6  /* (device) a page id or length was out of range */
+} pa_status;
+
+typedef enum { PA_KV_BF16 = 0, PA_KV_FP8_E4M3 = 1 } pa_kv_dtype;
+
+#define PA_PAGE_SIZE 64
+#define PA_MAX_SPLITS 64
+#define PA_MAX_GROUP 16     /* Hq / Hk supported by the decode kernels */
+#define PA_STATUS_BYTES 256 /* status word region at the start of every workspace */
+
+/* ----------------------------------------------------------------- decode */
+
+typedef struct {
+    int32_t batch;             /* B */
+    int32_t num_q_heads;       /* Hq */
+    int32_t num_kv_heads;      /* Hk; Hq % Hk == 0 and Hq / Hk <= 16 */
+    int32_t head_dim;          /* D: 64 or 128 */
+    int32_t page_size;         /* must be 64 */
+    int32_t max_pages_per_seq; /* row stride of block_table */
+    int32_t num_pool_pages;    /* pages in k_pool / v_pool */
+    int32_t kv_dtype;          /* pa_kv_dtype */
+    int32_t num_sms;           /* SMs of the device (cudaDevAttrMultiProcessorCount) */
+    int32_t ctas_per_sm;       /* persistent decode CTAs per SM; 0 = library default (1) */
+    int32_t forced_splits;     /* split-KV count per sequence; 0 = choose automatically */
+} pa_decode_shapes;
+
+typedef struct {
+    int32_t total_splits;   /* sum over sequences of the split count */
+    int32_t num_items;      /* (sequence, split, KV head) work items */
+    int32_t grid;           /* decode CTAs the schedule was built for */
+    int32_t meta_ints;      /* int32 entries of the packed metadata */
+    int32_t ctas_per_sm;    /* resolved value */
+    int32_t reserved;
+    size_t workspace_bytes; /* device workspace pa_decode needs */
+} pa_decode_plan;
+
+/*
+ * pa_get_metadata -- choose the split-KV count of every sequence and the
+ * persistent CTAs' work lists (the scheduler-metadata step: FlashMLA
+ * get_mla_metadata, "Tensor Shapes Reference" section 2; MATE
+ * get_scheduler_metadata with num_splits 0 = automatic).  Pure host code.
+ *
+ *   seq_lens_host     int32 [B] keys per sequence, 0 <= len <= max_pages * 64
+ *   block_table_host  int32 [B, max_pages] or NULL; when given, every live slot
+ *                     (column < ceil(len / 64)) is checked to hold a page id in
+ *                     [0, num_pool_pages)
+ *   shapes            see pa_decode_shapes
+ *   meta_host         int32 [meta_capacity_ints] output, or NULL to only size
+ *   plan              output: sizes and counts (always filled on PA_OK)
+ *
+ * Split rule (integers only, deterministic):
+ *   pages_b = ceil(len_b / 64); units = sum_b pages_b * Hk;
+ *   cap = num_sms * ctas_per_sm; chunk = max(4, ceil(units / (4 * cap)));
+ *   n_b = 1 if pages_b <= 1, else min(forced, pages_b, 64) if forced > 0,
+ *   else min(ceil(pages_b / chunk), 64).  Split s of b covers pages
+ *   [floor(s * pages_b / n_b), floor((s + 1) * pages_b / n_b)).
+ * Work items (b, s, kv head), cost = pages + 1, are dealt longest first to the
+ * least-loaded of grid = min(#items, cap) CTAs (ties: lowest index).
+ *
+ * Packed layout (int32): [0] 0x50414D31 [1] B [2] Hk [3] total_splits
+ * [4] num_items [5] grid [6] chunk [7] ctas_per_sm, then n_splits[B],
+ * split_indptr[B+1], cta_indptr[grid+1], items[2*num_items] = (b, s<<16 | kvh).
+ *
+ * Returns PA_ERR_WORKSPACE (plan filled) if meta_capacity_ints < plan->meta_ints.
+ */
+pa_status pa_get_metadata(const int32_t* seq_lens_host, const int32_t* block_table_host,
+                          const pa_decode_shapes* shapes, int32_t* meta_host, size_t meta_capacity_ints,
+                          pa_decode_plan* plan);
+
+/*
+ * pa_decode -- single-token decode over the paged cache (FlashMLA
+ * flash_mla_with_kvcache, "Tensor Shapes Reference" section 1; MATE paged mode,
+ * flash_attn_with_kvcache), with split-KV partials merged by a log-sum-exp
+ * combine when any sequence has more than one split.
+ *
+ *   q            bf16 [B, Hq, D]
+ *   k_pool       [num_pool_pages, Hk, 64, D], bf16 or e4m3 per shapes->kv_dtype
+ *   v_pool       same layout and type as k_pool
+ *   k_scale      fp32 [Hk] per-KV-head dequantisation scale (e4m3 only, else NULL)
+ *   v_scale      fp32 [Hk] (e4m3 only, else NULL); an e4m3 element x of head g
+ *                stands for x * k_scale[g] (keys) or x * v_scale[g] (values)
+ *   block_table  int32 [B, max_pages_per_seq]; slots past ceil(len/64) never read
+ *   seq_lens     int32 [B] (device copy of the lengths given to pa_get_metadata)
+ *   meta_dev     int32 [plan->meta_ints], device copy of pa_get_metadata's output
+ *   scale        softmax scale (e.g. 1/sqrt(D))
+ *   out          bf16 [B, Hq, D]
+ *   lse          fp32 [B, Hq] or NULL
+ *   workspace    >= plan->workspace_bytes device bytes; the first 256 bytes hold
+ *                the status word.  Zero-fill it once before first use; the
+ *                library leaves the status word at zero on success.  A
+ *                workspace must not be used by two calls that may overlap.
+ *
+ * With fp8 KV the query is used in fp16 (exact for |q| in [2^-14, 65504];
+ * smaller magnitudes round to fp16 subnormals).
+ */
+pa_status pa_decode(const pa_decode_shapes* shapes, const pa_decode_plan* plan, const void* q,
+                    const void* k_pool, const void* v_pool, const float* k_scale, const float* v_scale,
+                    const int32_t* block_table, const int32_t* seq_lens, const int32_t* meta_dev,
+                    float scale, void* out, float* lse, void* workspace, size_t workspace_bytes,
+                    cudaStream_t stream);
+
+/* ----------------------------------------------------------------- prefill */
+
+typedef struct {
+    int32_t batch;             /* B sequences */
+    int32_t num_q_heads;       /* Hq */
+    int32_t num_kv_heads;      /* Hk, Hq % Hk == 0 */
+    int32_t head_dim_qk;       /* q depth: 128, or 192 with rope_dim 64 */
+    int32_t head_dim_v;        /* 128 */
+    int32_t rope_dim;          /* 0, or 64: last 64 q entries pair with k_rope */
+    int32_t max_seqlen_q;      /* upper bound on every q segment length */
+    int32_t total_q;           /* cu_seqlens_q[B] */
+    int32_t total_k;           /* cu_seqlens_k[B] (ragged keys); for paged keys the
+                                  sum of kv lengths */
+    int32_t page_size;         /* 64 when block_table is given */
+    int32_t max_pages_per_seq; /* block_table row stride (paged) */
+    int32_t num_pool_pages;    /* pages in the pools (paged) */
+    int32_t num_sms;
+} pa_prefill_shapes;
+
+/*
+ * pa_prefill -- causal (or full) attention for a ragged batch of query
+ * segments: chunked prefill against a paged cache (FlashMLA mha_fwd_kvcache,
+ * section 4), ragged prefill (MATE dense mode, flash_attn_varlen_func) and the
+ * MLA shape with one 64-wide rope key shared by all heads (Modular
+ * flare_mla_prefill).
+ *
+ *   q            bf16 [total_q, Hq, head_dim_qk]
+ *   k, v         paged (block_table != NULL): bf16 pools [num_pool_pages, Hk, 64, Dk]
+ *                and [num_pool_pages, Hk, 64, Dv]; ragged: bf16 [total_k, Hk, Dk]
+ *                and [total_k, Hk, Dv]; Dk = head_dim_qk - rope_dim
+ *   k_rope       bf16 [total_k, 1, rope_dim] (ragged keys only) or NULL
+ *   cu_seqlens_q int32 [B+1] running offsets of the query segments
+ *   cu_seqlens_k int32 [B+1] running offsets of the key segments (kv lengths)
+ *   qo_offset    int32 [B] or NULL (= kv_len - q_len): with causal != 0 query row
+ *                i of segment b sees key j iff j <= qo_offset[b] + i (MATE
+ *                _normalize_qo_offset / _resolve_seqused_k)
+ *   out          bf16 [total_q, Hq, head_dim_v];  lse fp32 [total_q, Hq] or NULL
+ *   workspace    >= PA_STATUS_BYTES device bytes (status word), zero-filled once
+ */
+pa_status pa_prefill(const pa_prefill_shapes* shapes, const void* q, const void* k, const void* v,
+                     const void* k_rope, const int32_t* cu_seqlens_q, const int32_t* cu_seqlens_k,
+                     const int32_t* block_table, const int32_t* qo_offset, int causal, float scale,
+                     void* out, float* lse, void* workspace, size_t workspace_bytes, cudaStream_t stream);
+
+/* ----------------------------------------------------------------- status */
+
+/*
+ * Synchronise `stream`, read the status word at the start of `workspace`
+ * (device), clear it, and return what the kernels recorded (PA_OK if nothing).
+ * The first fault recorded since the last check wins.
+ */
+pa_status pa_check_status(void* workspace, cudaStream_t stream);
+
+/* Message describing the last non-OK status returned on this host thread. */
+const char* pa_last_error(void);
+
+/* Time limit, in nanoseconds, of every device-side wait in launches made after
+ * this call (default 2e9).  Process-wide. */
+pa_status pa_set_wait_limit_ns(uint64_t limit_ns);
+
+/*
+ * Test hook for failure detection: launch one CTA that waits, with the time
+ * limit given, on a barrier that nothing arrives on, then records
+ * PA_ERR_TIMEOUT in the status word and returns.  The context stays usable.
+ */
+pa_status pa_debug_wait_timeout(void* workspace, uint64_t limit_ns, cudaStream_t stream);
+
+/* Library version, e.g. 100 for 0.1.0. */
+int32_t pa_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* PA_H_ */

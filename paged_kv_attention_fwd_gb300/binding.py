@@ -1,0 +1,163 @@
+"""Python binding of libpa: the C-ABI calls under the same names.
+
+Argument marshalling only -- every step of the computation runs in the CUDA
+kernels behind ``libpa.so``.  Device buffers are torch tensors (used for their
+memory and stream, nothing else); host buffers are numpy arrays.  A missing
+library is an error, never a fallback.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import re
+from typing import Optional
+
+import numpy as np
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(HERE, "libpa.so")
+HEADER = os.path.join(os.path.dirname(HERE), "include", "pa.h")
+
+PA_OK, PA_ERR_INVALID_ARG, PA_ERR_UNSUPPORTED, PA_ERR_WORKSPACE, PA_ERR_CUDA, PA_ERR_TIMEOUT, \
+    PA_ERR_DEVICE_BOUNDS = range(7)
+PA_KV_BF16, PA_KV_FP8_E4M3 = 0, 1
+PA_STATUS_BYTES = 256
+STATUS_NAMES = {0: "PA_OK", 1: "PA_ERR_INVALID_ARG", 2: "PA_ERR_UNSUPPORTED", 3: "PA_ERR_WORKSPACE",
+                4: "PA_ERR_CUDA", 5: "PA_ERR_TIMEOUT", 6: "PA_ERR_DEVICE_BOUNDS"}
+
+
+class PaError(RuntimeError):
+    def __init__(self, status: int, message: str):
+        super().__init__(f"{STATUS_NAMES.get(status, status)}: {message}")
+        self.status = status
+
+
+class pa_decode_shapes(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_int32) for n in (
+        "batch", "num_q_heads", "num_kv_heads", "head_dim", "page_size", "max_pages_per_seq",
+        "num_pool_pages", "kv_dtype", "num_sms", "ctas_per_sm", "forced_splits")]
+
+
+class pa_decode_plan(ctypes.Structure):
+    _fields_ = [("total_splits", ctypes.c_int32), ("num_items", ctypes.c_int32), ("grid", ctypes.c_int32),
+                ("meta_ints", ctypes.c_int32), ("ctas_per_sm", ctypes.c_int32), ("reserved", ctypes.c_int32),
+                ("workspace_bytes", ctypes.c_size_t)]
+
+
+class pa_prefill_shapes(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_int32) for n in (
+        "batch", "num_q_heads", "num_kv_heads", "head_dim_qk", "head_dim_v", "rope_dim", "max_seqlen_q",
+        "total_q", "total_k", "page_size", "max_pages_per_seq", "num_pool_pages", "num_sms")]
+
+
+_lib = None
+_P = ctypes.c_void_p
+
+
+def lib() -> ctypes.CDLL:
+    """The loaded libpa.so (raises if it has not been built)."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(f"libpa.so is not built ({LIB_PATH}); run __graft_entry__.build() "
+                               "or python -m paged_kv_attention_fwd_gb300.build")
+        L = ctypes.CDLL(LIB_PATH)
+        i32, u64, sz, f32 = ctypes.c_int32, ctypes.c_uint64, ctypes.c_size_t, ctypes.c_float
+        L.pa_get_metadata.argtypes = [_P, _P, ctypes.POINTER(pa_decode_shapes), _P, sz,
+                                      ctypes.POINTER(pa_decode_plan)]
+        L.pa_decode.argtypes = [ctypes.POINTER(pa_decode_shapes), ctypes.POINTER(pa_decode_plan), _P, _P, _P, _P,
+                                _P, _P, _P, _P, f32, _P, _P, _P, sz, _P]
+        L.pa_prefill.argtypes = [ctypes.POINTER(pa_prefill_shapes), _P, _P, _P, _P, _P, _P, _P, _P, ctypes.c_int,
+                                 f32, _P, _P, _P, sz, _P]
+        L.pa_check_status.argtypes = [_P, _P]
+        L.pa_last_error.restype = ctypes.c_char_p
+        L.pa_set_wait_limit_ns.argtypes = [u64]
+        L.pa_debug_wait_timeout.argtypes = [_P, u64, _P]
+        L.pa_version.restype = i32
+        for f in ("pa_get_metadata", "pa_decode", "pa_prefill", "pa_check_status", "pa_set_wait_limit_ns",
+                  "pa_debug_wait_timeout"):
+            getattr(L, f).restype = ctypes.c_int
+        _lib = L
+    return _lib
+
+
+def declared_symbols() -> list:
+    """Every function the public header declares."""
+    with open(HEADER) as f:
+        text = f.read()
+    return sorted(set(re.findall(r"^\s*(?:pa_status|const char\*|int32_t)\s+(pa_\w+)\s*\(", text, re.M)))
+
+
+def _check(st: int) -> None:
+    if st != PA_OK:
+        raise PaError(st, lib().pa_last_error().decode())
+
+
+def _ptr(x) -> Optional[int]:
+    if x is None:
+        return None
+    if isinstance(x, np.ndarray):
+        return x.ctypes.data
+    return x.data_ptr()  # torch tensor
+
+
+def _stream(stream) -> Optional[int]:
+    if stream is None:
+        import torch
+        return torch.cuda.current_stream().cuda_stream
+    return stream if isinstance(stream, int) else stream.cuda_stream
+
+
+def pa_version() -> int:
+    return lib().pa_version()
+
+
+def pa_last_error() -> str:
+    return lib().pa_last_error().decode()
+
+
+def pa_get_metadata(seq_lens_host: np.ndarray, block_table_host: Optional[np.ndarray], shapes: pa_decode_shapes):
+    """Returns (meta int32 numpy array, pa_decode_plan)."""
+    sl = np.ascontiguousarray(seq_lens_host, dtype=np.int32)
+    bt = None if block_table_host is None else np.ascontiguousarray(block_table_host, dtype=np.int32)
+    plan = pa_decode_plan()
+    _check(lib().pa_get_metadata(_ptr(sl), _ptr(bt), ctypes.byref(shapes), None, 0, ctypes.byref(plan)))
+    meta = np.zeros(plan.meta_ints, dtype=np.int32)
+    _check(lib().pa_get_metadata(_ptr(sl), _ptr(bt), ctypes.byref(shapes), _ptr(meta), meta.size,
+                                 ctypes.byref(plan)))
+    return meta, plan
+
+
+def pa_decode(shapes: pa_decode_shapes, plan: pa_decode_plan, q, k_pool, v_pool, k_scale, v_scale, block_table,
+              seq_lens, meta_dev, scale: float, out, lse, workspace, workspace_bytes: Optional[int] = None,
+              stream=None) -> None:
+    if workspace_bytes is None:
+        workspace_bytes = workspace.numel() * workspace.element_size()
+    _check(lib().pa_decode(ctypes.byref(shapes), ctypes.byref(plan), _ptr(q), _ptr(k_pool), _ptr(v_pool),
+                           _ptr(k_scale), _ptr(v_scale), _ptr(block_table), _ptr(seq_lens), _ptr(meta_dev),
+                           float(scale), _ptr(out), _ptr(lse), _ptr(workspace), int(workspace_bytes),
+                           _stream(stream)))
+
+
+def pa_prefill(shapes: pa_prefill_shapes, q, k, v, k_rope, cu_seqlens_q, cu_seqlens_k, block_table, qo_offset,
+               causal: bool, scale: float, out, lse, workspace, workspace_bytes: Optional[int] = None,
+               stream=None) -> None:
+    if workspace_bytes is None:
+        workspace_bytes = workspace.numel() * workspace.element_size()
+    _check(lib().pa_prefill(ctypes.byref(shapes), _ptr(q), _ptr(k), _ptr(v), _ptr(k_rope), _ptr(cu_seqlens_q),
+                            _ptr(cu_seqlens_k), _ptr(block_table), _ptr(qo_offset), int(bool(causal)),
+                            float(scale), _ptr(out), _ptr(lse), _ptr(workspace), int(workspace_bytes),
+                            _stream(stream)))
+
+
+def pa_check_status(workspace, stream=None) -> int:
+    """Synchronise, read and clear the device status word; returns the pa_status code."""
+    return lib().pa_check_status(_ptr(workspace), _stream(stream))
+
+
+def pa_set_wait_limit_ns(limit_ns: int) -> None:
+    _check(lib().pa_set_wait_limit_ns(int(limit_ns)))
+
+
+def pa_debug_wait_timeout(workspace, limit_ns: int, stream=None) -> None:
+    _check(lib().pa_debug_wait_timeout(_ptr(workspace), int(limit_ns), _stream(stream)))

@@ -1,0 +1,726 @@
+// decode.cu -- single-token attention over a paged KV cache on sm_103a.
+//
+// One persistent CTA per SM walks the work list the host scheduler dealt it:
+// items (sequence b, split s, KV head g), each a contiguous range of 64-row
+// pages (FlashMLA "Tensor Shapes Reference": paged K/V blocks of section 1,
+// logical token -> block_table column as in "Prefill to Cache Mapping").
+// Within a CTA the pages stream through a multi-stage shared-memory ring:
+//
+//   warp 0      producer: block_table lookup, TMA (bf16, 128-byte swizzle) or
+//               plain bulk copies (e4m3) of whole 64 x D page slabs
+//   warp 1      MMA issuer: tcgen05.mma, f32 accumulators in TMEM
+//                 S^T[128 keys, 16 heads] = K_tile[128, D] . Q_group[16, D]^T
+//                 O^T[D, 16 heads]        = V_tile^T[D, 128] . P^T[128, 16]
+//               (the query heads of one KV group -- contiguous groups, as in
+//               the "Grouped-Query Attention" diagram -- padded to 16 form N)
+//   warps 2-5   softmax: one TMEM lane (= key of the tile, = d of the output)
+//               per thread; per-head running max by warp transpose-reduce,
+//               exp2, partial sums, P written back to shared memory; the
+//               output accumulates in registers with the usual rescale
+//   warps 6-9   (e4m3 only) convert e4m3 pages to f16 operand tiles (exact)
+//
+// Items whose sequence has more than one split write fp32 partials (output
+// normalised by its own sum, plus its log-sum-exp); combine_kernel merges
+// them.  Every wait is bounded; a timeout raises the CTA's abort flag,
+// records PA_ERR_TIMEOUT, drains in-flight copies and MMAs, frees TMEM and
+// returns.
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_fp8.h>
+
+#include "pa_internal.h"
+#include "pa_ptx.cuh"
+
+namespace pa {
+namespace {
+
+constexpr int kNPad = 16;  // MMA N: query heads of one KV group, padded
+constexpr float kLn2 = 0.69314718055994531f;
+
+// barrier slots
+enum : int {
+    B_FULL = 0,    // [4] stage filled (TMA bytes landed)
+    B_EMPTY = 4,   // [4] stage free again
+    B_QF = 8,      // [2] query tile written
+    B_SF = 10,     // [2] S tile in TMEM
+    B_PF = 12,     // [2] P written (and dead V rows zeroed)
+    B_OF = 14,     // [2] O tile in TMEM
+    B_DONE = 16,   // all MMAs retired (teardown)
+    B_KHF = 17,    // e4m3: converted K tile ready
+    B_KHE = 18,    // e4m3: converted K tile consumed
+    B_VHF = 19,    // [2] e4m3: converted V tile ready
+    B_VHE = 21,    // [2] e4m3: converted V tile consumed
+    B_COUNT = 23
+};
+
+constexpr uint32_t kTmemCols = 64;
+__host__ __device__ constexpr uint32_t s_col(uint32_t b) { return b * 16u; }
+__host__ __device__ constexpr uint32_t o_col(uint32_t b) { return 32u + b * 16u; }
+
+template <int D, bool FP8>
+struct DecodeLayout {
+    static constexpr int kChunks = D / 64;             // 64-column (128-byte) chunks of a 16-bit row
+    static constexpr int kTile16 = kChunks * 2 * 8192;  // 128-key tile of 16-bit K or V, swizzled
+    static constexpr int kRawPage = 64 * D;             // one e4m3 page slab, row-major
+    static constexpr int kRawTile = 2 * kRawPage;
+    static constexpr int kStages = FP8 ? 3 : (D == 128 ? 3 : 4);
+    static constexpr int kStageBytes = FP8 ? 2 * kRawTile : 2 * kTile16;
+    static constexpr int kKhOff = kStages * kStageBytes;
+    static constexpr int kVhOff = kKhOff + (FP8 ? kTile16 : 0);
+    static constexpr int kQOff = kVhOff + (FP8 ? 2 * kTile16 : 0);
+    static constexpr int kQBytes = kChunks * kNPad * 128;
+    static constexpr int kPOff = kQOff + 2 * kQBytes;
+    static constexpr int kPBytes = 2 * kNPad * 128;
+    static constexpr int kRedOff = kPOff + 2 * kPBytes;
+    static constexpr int kRedBytes = 4 * kNPad * 4 * 4;
+    static constexpr int kEnd = kRedOff + kRedBytes;
+    // With D = 64 the PV MMA (M = 128) also reads a second 64-row MN atom
+    // 16 KB past each V tile; its rows are discarded, but the window must be
+    // inside the allocation.
+    static constexpr int kLastV = FP8 ? kVhOff + kTile16 : (kStages - 1) * kStageBytes + kTile16;
+    static constexpr int kGuardEnd = D == 64 ? kLastV + 32768 : 0;
+    static constexpr int kBytes = kEnd > kGuardEnd ? kEnd : kGuardEnd;
+    static constexpr int kSmem = kBytes + 1024;
+    static constexpr int kThreads = FP8 ? 320 : 192;
+    static_assert(kStages <= 4, "barrier slots");
+};
+
+struct Item {
+    int b, s, kvh, nsplit, split_base, p0, p1, seq_len;
+};
+
+__device__ __forceinline__ void record(int* status, int code) { atomicCAS(status, 0, code); }
+
+__device__ __forceinline__ void fail(const DecodeArgs& a, volatile int* abort_flag, int code) {
+    *abort_flag = 1;
+    record(a.status, code);
+}
+
+__device__ __forceinline__ int items_offset(const int32_t* meta, int B) {
+    return kMetaHeader + 2 * B + 1 + meta[5] + 1;
+}
+
+__device__ __forceinline__ Item load_item(const DecodeArgs& a, int idx, int items_off) {
+    const int32_t* meta = a.meta;
+    Item it;
+    int b = __ldg(&meta[items_off + 2 * idx]);
+    const int w = __ldg(&meta[items_off + 2 * idx + 1]);
+    int s = w >> 16, kvh = w & 0xFFFF;
+    bool ok = (unsigned)b < (unsigned)a.batch && kvh < a.num_kv_heads;
+    if (!ok) b = 0;
+    int nsplit = __ldg(&meta[kMetaHeader + b]);
+    if (nsplit < 1 || s >= nsplit) ok = false;
+    int len = __ldg(&a.seq_lens[b]);
+    len = len < 0 ? 0 : len;
+    int pages = (len + kPage - 1) / kPage;
+    if (pages > a.max_pages) {
+        record(a.status, PA_ERR_DEVICE_BOUNDS);
+        pages = a.max_pages;
+        len = pages * kPage;
+    }
+    if (!ok) {
+        record(a.status, PA_ERR_DEVICE_BOUNDS);
+        nsplit = 1; s = 0; kvh = 0; pages = 0; len = 0;
+    }
+    it.b = b; it.s = s; it.kvh = kvh; it.nsplit = nsplit;
+    it.split_base = __ldg(&meta[kMetaHeader + a.batch + b]);
+    it.p0 = (int)(((long long)s * pages) / nsplit);
+    it.p1 = (int)(((long long)(s + 1) * pages) / nsplit);
+    it.seq_len = len;
+    return it;
+}
+
+__device__ __forceinline__ int item_tiles(const Item& it) { return (it.p1 - it.p0 + 1) >> 1; }
+
+// All-reduce 16 per-thread values over a warp by transposition: 16 shuffles
+// instead of 80.  Returns the reduction of head head_of_lane(lane), which is
+// held by lanes 2h' and 2h'+1.
+template <bool kMax>
+__device__ __forceinline__ float warp_xreduce16(const float (&x)[16], int lane) {
+    float v[16];
+#pragma unroll
+    for (int i = 0; i < 16; ++i) v[i] = x[i];
+#define PA_OP(a, b) (kMax ? fmaxf((a), (b)) : ((a) + (b)))
+    {
+        const bool up = lane & 16;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const float send = up ? v[i] : v[i + 8];
+            const float keep = up ? v[i + 8] : v[i];
+            v[i] = PA_OP(keep, __shfl_xor_sync(0xffffffffu, send, 16));
+        }
+    }
+    {
+        const bool up = lane & 8;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const float send = up ? v[i] : v[i + 4];
+            const float keep = up ? v[i + 4] : v[i];
+            v[i] = PA_OP(keep, __shfl_xor_sync(0xffffffffu, send, 8));
+        }
+    }
+    {
+        const bool up = lane & 4;
+#pragma unroll
+        for (int i = 0; i < 2; ++i) {
+            const float send = up ? v[i] : v[i + 2];
+            const float keep = up ? v[i + 2] : v[i];
+            v[i] = PA_OP(keep, __shfl_xor_sync(0xffffffffu, send, 4));
+        }
+    }
+    {
+        const bool up = lane & 2;
+        const float send = up ? v[0] : v[1];
+        const float keep = up ? v[1] : v[0];
+        v[0] = PA_OP(keep, __shfl_xor_sync(0xffffffffu, send, 2));
+    }
+    v[0] = PA_OP(v[0], __shfl_xor_sync(0xffffffffu, v[0], 1));
+#undef PA_OP
+    return v[0];
+}
+
+__device__ __forceinline__ int head_of_lane(int lane) {
+    return ((lane >> 4) & 1) * 8 + ((lane >> 3) & 1) * 4 + ((lane >> 2) & 1) * 2 + ((lane >> 1) & 1);
+}
+
+// Barrier over the 128 softmax threads that also ORs a flag across them, so
+// that every thread takes the same abort decision.
+__device__ __forceinline__ bool softmax_bar_or(bool pred) {
+    uint32_t r;
+    asm volatile(
+        "{\n\t.reg .pred p, q;\n\t"
+        "setp.ne.u32 p, %1, 0;\n\t"
+        "bar.red.or.pred q, 1, 128, p;\n\t"
+        "selp.u32 %0, 1, 0, q;\n\t}"
+        : "=r"(r)
+        : "r"((uint32_t)pred)
+        : "memory");
+    return r != 0;
+}
+
+__device__ __forceinline__ uint16_t f32_to_16(float x, bool f16) {
+    if (f16) return __half_as_ushort(__float2half_rn(x));
+    return __bfloat16_as_ushort(__float2bfloat16_rn(x));
+}
+
+template <int D, bool FP8>
+__global__ void __launch_bounds__(DecodeLayout<D, FP8>::kThreads, 1)
+    decode_kernel(const __grid_constant__ DecodeArgs a, const __grid_constant__ CUtensorMap map_k,
+                  const __grid_constant__ CUtensorMap map_v) {
+    using L = DecodeLayout<D, FP8>;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    __shared__ __align__(8) uint64_t bars[B_COUNT];
+    __shared__ uint32_t tmem_base_sh;
+    __shared__ int abort_store;
+    volatile int* abort_sh = &abort_store;
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int32_t* meta = a.meta;
+    const int B = a.batch;
+    const int items_off = items_offset(meta, B);
+    int it_lo = 0, it_hi = 0;
+    if ((int)blockIdx.x < __ldg(&meta[5])) {
+        it_lo = __ldg(&meta[kMetaHeader + 2 * B + 1 + blockIdx.x]);
+        it_hi = __ldg(&meta[kMetaHeader + 2 * B + 1 + blockIdx.x + 1]);
+    }
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < L::kStages; ++s) {
+            mbar_init(&bars[B_FULL + s], 1);
+            mbar_init(&bars[B_EMPTY + s], FP8 ? 128 : 1);
+        }
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(&bars[B_QF + i], 128);
+            mbar_init(&bars[B_SF + i], 1);
+            mbar_init(&bars[B_PF + i], 128);
+            mbar_init(&bars[B_OF + i], 1);
+            mbar_init(&bars[B_VHF + i], 128);
+            mbar_init(&bars[B_VHE + i], 1);
+        }
+        mbar_init(&bars[B_DONE], 1);
+        mbar_init(&bars[B_KHF], 128);
+        mbar_init(&bars[B_KHE], 1);
+        *abort_sh = 0;
+        fence_barrier_init();
+    }
+    if (warp == 1) {
+        tmem_alloc(&tmem_base_sh, kTmemCols);
+        tmem_relinquish();
+    }
+    if (warp >= 2 && warp < 6) {
+        // P rows of padding heads must read as zero in every PV product
+        uint4* p = reinterpret_cast<uint4*>(sm + L::kPOff);
+        for (int i = threadIdx.x - 64; i < 2 * L::kPBytes / 16; i += 128) p[i] = make_uint4(0, 0, 0, 0);
+        fence_proxy_async_smem();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tbase = tmem_base_sh;
+
+    if (warp == 0) {
+        // ------------------------------------------------------------ producer
+        if (lane == 0) {
+            uint32_t g = 0;
+            uint32_t last_par[4] = {0, 0, 0, 0};
+            bool issued[4] = {false, false, false, false};
+            bool ok = true;
+            constexpr uint32_t page_bytes = FP8 ? 64u * D : 64u * D * 2u;
+            for (int j = it_lo; j < it_hi && ok; ++j) {
+                const Item it = load_item(a, j, items_off);
+                const int ntiles = item_tiles(it);
+                const long long bt_row = (long long)it.b * a.max_pages;
+                for (int t = 0; t < ntiles; ++t, ++g) {
+                    const int stage = g % L::kStages;
+                    const int pa0 = it.p0 + 2 * t;
+                    const int npg = min(2, it.p1 - pa0);
+                    int pid[2];
+                    pid[0] = __ldg(&a.block_table[bt_row + pa0]);
+                    pid[1] = npg > 1 ? __ldg(&a.block_table[bt_row + pa0 + 1]) : 0;
+                    if (!mbar_wait(&bars[B_EMPTY + stage], ((g / L::kStages) & 1) ^ 1, abort_sh, a.wait_ns)) {
+                        fail(a, abort_sh, PA_ERR_TIMEOUT);
+                        ok = false;
+                        break;
+                    }
+                    bool valid[2];
+                    uint32_t nvalid = 0;
+                    for (int i = 0; i < 2; ++i) {
+                        valid[i] = i < npg && (unsigned)pid[i] < (unsigned)a.num_pool_pages;
+                        if (i < npg && !valid[i]) record(a.status, PA_ERR_DEVICE_BOUNDS);
+                        nvalid += valid[i];
+                    }
+                    uint64_t* full = &bars[B_FULL + stage];
+                    mbar_arrive_expect_tx(full, nvalid * 2u * page_bytes);
+                    uint8_t* st = sm + stage * L::kStageBytes;
+                    for (int i = 0; i < 2; ++i) {
+                        if (!valid[i]) continue;
+                        const long long slab = (long long)pid[i] * a.num_kv_heads + it.kvh;
+                        if constexpr (FP8) {
+                            bulk_load(st + i * L::kRawPage, a.k_pool + slab * L::kRawPage, L::kRawPage, full);
+                            bulk_load(st + L::kRawTile + i * L::kRawPage, a.v_pool + slab * L::kRawPage, L::kRawPage,
+                                      full);
+                        } else {
+#pragma unroll
+                            for (int c = 0; c < L::kChunks; ++c) {
+                                tma_load_2d(st + c * 16384 + i * 8192, &map_k, full, c * 64, (int)(slab * 64));
+                                tma_load_2d(st + L::kTile16 + c * 16384 + i * 8192, &map_v, full, c * 64,
+                                            (int)(slab * 64));
+                            }
+                        }
+                    }
+                    last_par[stage] = (g / L::kStages) & 1;
+                    issued[stage] = true;
+                }
+            }
+            // every issued copy must land before the CTA may exit
+            for (int s = 0; s < L::kStages; ++s)
+                if (issued[s]) mbar_wait(&bars[B_FULL + s], last_par[s], nullptr, a.wait_ns);
+        }
+    } else if (warp == 1) {
+        // ------------------------------------------------------------ MMA issuer
+        if (lane == 0) {
+            constexpr uint32_t idesc_qk = idesc_f16(128, kNPad, !FP8, false, false);
+            constexpr uint32_t idesc_pv = idesc_f16(128, kNPad, !FP8, true, false);
+            uint32_t g = 0, qi = 0;
+            bool pending = false, ok = true;
+            auto issue_pv = [&](uint32_t k) -> bool {
+                if (!mbar_wait(&bars[B_PF + (k & 1)], (k >> 1) & 1, abort_sh, a.wait_ns)) return false;
+                if (FP8 && !mbar_wait(&bars[B_VHF + (k & 1)], (k >> 1) & 1, abort_sh, a.wait_ns)) return false;
+                tc_fence_after();
+                const uint32_t vbase = FP8 ? smem_u32(sm + L::kVhOff + (k & 1) * L::kTile16)
+                                           : smem_u32(sm + (k % L::kStages) * L::kStageBytes + L::kTile16);
+                const uint32_t pbase = smem_u32(sm + L::kPOff + (k & 1) * L::kPBytes);
+#pragma unroll
+                for (int kk = 0; kk < 8; ++kk) {
+                    const int page = kk >> 2, grp = kk & 3;
+                    const uint64_t adesc = sdesc_sw128(vbase + page * 8192 + grp * 2048, 16384, 1024);
+                    const uint64_t bdesc = sdesc_sw128(pbase + page * 2048 + grp * 32, 16, 1024);
+                    mma_ss(tbase + o_col(k & 1), adesc, bdesc, idesc_pv, kk > 0);
+                }
+                mma_commit(&bars[B_OF + (k & 1)]);
+                if (FP8) mma_commit(&bars[B_VHE + (k & 1)]);
+                else mma_commit(&bars[B_EMPTY + (k % L::kStages)]);
+                return true;
+            };
+            for (int j = it_lo; j < it_hi && ok; ++j) {
+                const Item it = load_item(a, j, items_off);
+                const int ntiles = item_tiles(it);
+                if (ntiles == 0) continue;
+                if (!mbar_wait(&bars[B_QF + (qi & 1)], (qi >> 1) & 1, abort_sh, a.wait_ns)) {
+                    fail(a, abort_sh, PA_ERR_TIMEOUT);
+                    ok = false;
+                    break;
+                }
+                const uint32_t qbase = smem_u32(sm + L::kQOff + (qi & 1) * L::kQBytes);
+                ++qi;
+                for (int t = 0; t < ntiles; ++t, ++g) {
+                    const int stage = g % L::kStages;
+                    const bool got = FP8 ? mbar_wait(&bars[B_KHF], g & 1, abort_sh, a.wait_ns)
+                                         : mbar_wait(&bars[B_FULL + stage], (g / L::kStages) & 1, abort_sh, a.wait_ns);
+                    if (!got) {
+                        fail(a, abort_sh, PA_ERR_TIMEOUT);
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t kbase = FP8 ? smem_u32(sm + L::kKhOff) : smem_u32(sm + stage * L::kStageBytes);
+#pragma unroll
+                    for (int kk = 0; kk < D / 16; ++kk) {
+                        const int c = kk >> 2, off = (kk & 3) * 32;
+                        const uint64_t adesc = sdesc_sw128(kbase + c * 16384 + off, 16, 1024);
+                        const uint64_t bdesc = sdesc_sw128(qbase + c * 2048 + off, 16, 1024);
+                        mma_ss(tbase + s_col(g & 1), adesc, bdesc, idesc_qk, kk > 0);
+                    }
+                    mma_commit(&bars[B_SF + (g & 1)]);
+                    if (FP8) mma_commit(&bars[B_KHE]);
+                    if (pending && !issue_pv(g - 1)) {
+                        fail(a, abort_sh, PA_ERR_TIMEOUT);
+                        ok = false;
+                        break;
+                    }
+                    pending = true;
+                }
+            }
+            if (ok && pending && !issue_pv(g - 1)) fail(a, abort_sh, PA_ERR_TIMEOUT);
+            // all MMAs must retire before TMEM is freed and shared memory released
+            mma_commit(&bars[B_DONE]);
+            mbar_wait(&bars[B_DONE], 0, nullptr, a.wait_ns);
+        }
+    } else if (warp < 6) {
+        // ------------------------------------------------------------ softmax
+        const int q4 = warp & 3;          // TMEM lane quarter this warp may access
+        const int row = q4 * 32 + lane;   // key of the tile (S) / output column d (O)
+        const int hl = head_of_lane(lane);
+        const int G = a.group;
+        const uint32_t lane_addr = (uint32_t)(q4 * 32) << 16;
+        float* red = reinterpret_cast<float*>(sm + L::kRedOff);
+
+        auto next_nonempty = [&](int j) {
+            while (j < it_hi && item_tiles(load_item(a, j, items_off)) == 0) ++j;
+            return j;
+        };
+        // query rows of the item's KV group -> swizzled K-major tile of 16 rows
+        auto load_q = [&](int j, uint32_t qidx) {
+            const Item it = load_item(a, j, items_off);
+            uint8_t* qb = sm + L::kQOff + (qidx & 1) * L::kQBytes;
+            constexpr int kRowChunks = D / 8;  // 16-byte chunks per row
+            for (int c = row; c < kNPad * kRowChunks; c += 128) {
+                const int h = c / kRowChunks, dc = c % kRowChunks;
+                uint4 v = make_uint4(0, 0, 0, 0);
+                if (h < G) {
+                    const long long qrow = (long long)it.b * a.num_q_heads + (long long)it.kvh * G + h;
+                    v = __ldg(reinterpret_cast<const uint4*>(a.q + qrow * D) + dc);
+                    if constexpr (FP8) {
+                        uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+                        for (int i = 0; i < 4; ++i) {
+                            const float lo = __uint_as_float(w[i] << 16), hi = __uint_as_float(w[i] & 0xFFFF0000u);
+                            w[i] = (uint32_t)__half_as_ushort(__float2half_rn(lo)) |
+                                   ((uint32_t)__half_as_ushort(__float2half_rn(hi)) << 16);
+                        }
+                        v = make_uint4(w[0], w[1], w[2], w[3]);
+                    }
+                }
+                *reinterpret_cast<uint4*>(qb + (dc >> 3) * (kNPad * 128) + h * 128 + (((dc & 7) ^ (h & 7)) << 4)) = v;
+            }
+            fence_proxy_async_smem();
+            mbar_arrive(&bars[B_QF + (qidx & 1)]);
+        };
+
+        int qload = next_nonempty(it_lo);
+        uint32_t qload_idx = 0;
+        for (int k = 0; k < 2 && qload < it_hi; ++k) {
+            load_q(qload, qload_idx++);
+            qload = next_nonempty(qload + 1);
+        }
+
+        uint32_t g = 0, qi = 0;
+        bool aborted = false;
+        for (int j = it_lo; j < it_hi && !aborted; ++j) {
+            const Item it = load_item(a, j, items_off);
+            const int ntiles = item_tiles(it);
+            const bool partial = it.nsplit > 1;
+            const long long head0 = (long long)it.kvh * G;
+            const long long orow = partial ? (long long)(it.split_base + it.s) * a.num_q_heads + head0
+                                           : (long long)it.b * a.num_q_heads + head0;
+            if (ntiles == 0) {
+                // empty key range: out = 0, lse = -inf
+                for (int h = 0; h < G; ++h) {
+                    if (row < D) {
+                        if (partial) a.o_part[(orow + h) * D + row] = 0.f;
+                        else a.out[(orow + h) * D + row] = 0;
+                    }
+                }
+                if (row < G) {
+                    if (partial) a.lse_part[orow + row] = -INFINITY;
+                    else if (a.lse) a.lse[orow + row] = -INFINITY;
+                }
+                continue;
+            }
+            if (qi >= 1 && qload < it_hi) {
+                load_q(qload, qload_idx++);
+                qload = next_nonempty(qload + 1);
+            }
+            ++qi;
+            const float sl2 = a.scale_log2 * (FP8 ? __ldg(&a.k_scale[it.kvh]) : 1.f);
+            const int key_end = min(it.seq_len, it.p1 * kPage);
+            float m[16], lp[16], o[16], alpha_prev[16];
+#pragma unroll
+            for (int h = 0; h < 16; ++h) { m[h] = -INFINITY; lp[h] = 0.f; o[h] = 0.f; alpha_prev[h] = 1.f; }
+
+            auto fold = [&](uint32_t k) {
+                if (!mbar_wait(&bars[B_OF + (k & 1)], (k >> 1) & 1, abort_sh, a.wait_ns)) fail(a, abort_sh, PA_ERR_TIMEOUT);
+                tc_fence_after();
+                uint32_t r[16];
+                tmem_ld_x16(tbase + lane_addr + o_col(k & 1), r);
+                tmem_ld_wait();
+                reg_fence(r);
+#pragma unroll
+                for (int h = 0; h < 16; ++h) o[h] = fmaf(o[h], alpha_prev[h], __uint_as_float(r[h]));
+            };
+
+            for (int t = 0; t < ntiles; ++t, ++g) {
+                const int pa0 = it.p0 + 2 * t;
+                const int npg = min(2, it.p1 - pa0);
+                const int key = pa0 * kPage + row;
+                const bool valid = row < npg * kPage && key < key_end;
+                if (!mbar_wait(&bars[B_SF + (g & 1)], (g >> 1) & 1, abort_sh, a.wait_ns))
+                    fail(a, abort_sh, PA_ERR_TIMEOUT);
+                tc_fence_after();
+                uint32_t sr[16];
+                tmem_ld_x16(tbase + lane_addr + s_col(g & 1), sr);
+                tmem_ld_wait();
+                reg_fence(sr);
+                float x[16];
+#pragma unroll
+                for (int h = 0; h < 16; ++h) x[h] = valid ? __uint_as_float(sr[h]) * sl2 : -INFINITY;
+                const float wmax = warp_xreduce16<true>(x, lane);
+                float* rb = red + (g & 1) * 64;
+                if (!(lane & 1)) rb[hl * 4 + q4] = wmax;
+                if (softmax_bar_or(*abort_sh != 0)) { aborted = true; break; }
+                float alpha[16];
+#pragma unroll
+                for (int h = 0; h < 16; ++h) {
+                    const float4 r4 = reinterpret_cast<const float4*>(rb)[h];
+                    const float mt = fmaxf(fmaxf(r4.x, r4.y), fmaxf(r4.z, r4.w));
+                    const float mn = fmaxf(m[h], mt);
+                    const bool none = mn == -INFINITY;
+                    alpha[h] = none ? 1.f : exp2f(m[h] - mn);
+                    x[h] = none ? 0.f : exp2f(x[h] - mn);  // x[h] = -inf -> 0
+                    lp[h] = fmaf(lp[h], alpha[h], x[h]);
+                    m[h] = mn;
+                }
+                // P^T tile (K-major: rows = heads, 128 keys in two 64-key chunks)
+                uint8_t* pb = sm + L::kPOff + (g & 1) * L::kPBytes + (row >> 6) * (kNPad * 128);
+#pragma unroll
+                for (int h = 0; h < 16; ++h)
+                    if (h < G) *reinterpret_cast<uint16_t*>(pb + sw128_offset(h, row & 63)) = f32_to_16(x[h], FP8);
+                if (!FP8 && !valid) {
+                    // a dead key's V row may hold anything (NaN included); 0 * NaN
+                    // would poison the PV product, so zero the row first
+                    const int stage = g % L::kStages;
+                    mbar_wait(&bars[B_FULL + stage], (g / L::kStages) & 1, abort_sh, a.wait_ns);
+                    uint8_t* vr = sm + stage * L::kStageBytes + L::kTile16 + (row >> 6) * 8192 + (row & 63) * 128;
+#pragma unroll
+                    for (int c = 0; c < L::kChunks; ++c)
+#pragma unroll
+                        for (int i = 0; i < 8; ++i) *reinterpret_cast<uint4*>(vr + c * 16384 + i * 16) = make_uint4(0, 0, 0, 0);
+                }
+                fence_proxy_async_smem();
+                tc_fence_before();
+                mbar_arrive(&bars[B_PF + (g & 1)]);
+                if (t > 0) fold(g - 1);
+#pragma unroll
+                for (int h = 0; h < 16; ++h) alpha_prev[h] = alpha[h];
+            }
+            if (aborted) break;
+            fold(g - 1);
+            tc_fence_before();
+
+            // ---- epilogue: total sums, normalise, write
+            const float wsum = warp_xreduce16<false>(lp, lane);
+            float* rl = red + 128 + (qi & 1) * 64;
+            if (!(lane & 1)) rl[hl * 4 + q4] = wsum;
+            if (softmax_bar_or(*abort_sh != 0)) { aborted = true; break; }
+            const float vs = FP8 ? __ldg(&a.v_scale[it.kvh]) : 1.f;
+            float mine_m = 0.f, mine_l = 0.f;
+#pragma unroll
+            for (int h = 0; h < 16; ++h) {
+                const float4 r4 = reinterpret_cast<const float4*>(rl)[h];
+                const float l = (r4.x + r4.y) + (r4.z + r4.w);
+                if (h == row) { mine_m = m[h]; mine_l = l; }
+                if (h < G && row < D) {
+                    const float val = l > 0.f ? o[h] * (vs / l) : 0.f;
+                    if (partial) a.o_part[(orow + h) * D + row] = val;
+                    else a.out[(orow + h) * D + row] = __bfloat16_as_ushort(__float2bfloat16_rn(val));
+                }
+            }
+            if (row < G) {
+                const float lse = mine_l > 0.f ? (mine_m + log2f(mine_l)) * kLn2 : -INFINITY;
+                if (partial) a.lse_part[orow + row] = lse;
+                else if (a.lse) a.lse[orow + row] = lse;
+            }
+        }
+        tc_fence_before();
+    } else {
+        // ------------------------------------------------------------ e4m3 -> f16 converters
+        if constexpr (FP8) {
+            const int ct = threadIdx.x - 192;  // tile row (key) this thread converts
+            const int page = ct >> 6, r = ct & 63;
+            uint32_t g = 0;
+            bool ok = true;
+            constexpr int kSrcChunks = D / 16;  // 16 e4m3 per 16-byte chunk
+            auto convert_row = [&](const uint8_t* src, uint8_t* dst_tile, bool zero) {
+#pragma unroll 4
+                for (int i = 0; i < kSrcChunks; ++i) {
+                    const int cc = (i + ct) % kSrcChunks;  // staggered: no bank conflicts
+                    uint4 lo = make_uint4(0, 0, 0, 0), hi = make_uint4(0, 0, 0, 0);
+                    if (!zero) {
+                        const uint4 raw = *reinterpret_cast<const uint4*>(src + cc * 16);
+                        const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
+                        uint32_t h2[8];
+#pragma unroll
+                        for (int k = 0; k < 4; ++k) {
+                            const __half2_raw a0 = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)(w[k] & 0xFFFFu), __NV_E4M3);
+                            const __half2_raw a1 = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)(w[k] >> 16), __NV_E4M3);
+                            h2[2 * k] = (uint32_t)a0.x | ((uint32_t)a0.y << 16);
+                            h2[2 * k + 1] = (uint32_t)a1.x | ((uint32_t)a1.y << 16);
+                        }
+                        lo = make_uint4(h2[0], h2[1], h2[2], h2[3]);
+                        hi = make_uint4(h2[4], h2[5], h2[6], h2[7]);
+                    }
+                    const int d = cc * 16;  // first of the 16 elements
+                    uint8_t* t = dst_tile + (d >> 6) * 16384 + page * 8192;
+                    *reinterpret_cast<uint4*>(t + sw128_offset(r, d & 63)) = lo;
+                    *reinterpret_cast<uint4*>(t + sw128_offset(r, (d & 63) + 8)) = hi;
+                }
+            };
+            for (int j = it_lo; j < it_hi && ok; ++j) {
+                const Item it = load_item(a, j, items_off);
+                const int ntiles = item_tiles(it);
+                const int key_end = min(it.seq_len, it.p1 * kPage);
+                for (int t = 0; t < ntiles; ++t, ++g) {
+                    const int stage = g % L::kStages;
+                    const int pa0 = it.p0 + 2 * t;
+                    const int npg = min(2, it.p1 - pa0);
+                    const bool row_live = page < npg;
+                    const bool key_live = row_live && pa0 * kPage + ct < key_end;
+                    if (!mbar_wait(&bars[B_FULL + stage], (g / L::kStages) & 1, abort_sh, a.wait_ns) ||
+                        (g > 0 && !mbar_wait(&bars[B_KHE], (g - 1) & 1, abort_sh, a.wait_ns))) {
+                        fail(a, abort_sh, PA_ERR_TIMEOUT);
+                        ok = false;
+                        break;
+                    }
+                    const uint8_t* raw = sm + stage * L::kStageBytes;
+                    if (row_live) convert_row(raw + page * L::kRawPage + r * D, sm + L::kKhOff, false);
+                    fence_proxy_async_smem();
+                    mbar_arrive(&bars[B_KHF]);
+                    if (g >= 2 && !mbar_wait(&bars[B_VHE + (g & 1)], ((g - 2) >> 1) & 1, abort_sh, a.wait_ns)) {
+                        fail(a, abort_sh, PA_ERR_TIMEOUT);
+                        ok = false;
+                        break;
+                    }
+                    convert_row(raw + L::kRawTile + page * L::kRawPage + r * D, sm + L::kVhOff + (g & 1) * L::kTile16,
+                                !key_live);
+                    fence_proxy_async_smem();
+                    mbar_arrive(&bars[B_VHF + (g & 1)]);
+                    mbar_arrive(&bars[B_EMPTY + stage]);
+                }
+            }
+        }
+    }
+
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tbase, kTmemCols);
+    }
+}
+
+// Merge split partials: L = m + ln sum_s exp(lse_s - m), out = sum_s exp(lse_s - L) o_s.
+// One warp per (sequence, query head); sequences with one split were written
+// directly by the decode kernel and are skipped.
+__global__ void __launch_bounds__(128) combine_kernel(const CombineArgs a) {
+    const int w = blockIdx.x * 4 + (threadIdx.x >> 5);
+    const int lane = threadIdx.x & 31;
+    if (w >= a.batch * a.num_q_heads) return;
+    const int b = w / a.num_q_heads, h = w % a.num_q_heads;
+    const int n = __ldg(&a.meta[kMetaHeader + b]);
+    if (n <= 1) return;
+    const int base = __ldg(&a.meta[kMetaHeader + a.batch + b]);
+    float mx = -INFINITY;
+    for (int s = 0; s < n; ++s) mx = fmaxf(mx, __ldg(&a.lse_part[(long long)(base + s) * a.num_q_heads + h]));
+    const long long orow = (long long)b * a.num_q_heads + h;
+    if (mx == -INFINITY) {
+        for (int d = lane; d < a.head_dim; d += 32) a.out[orow * a.head_dim + d] = 0;
+        if (lane == 0 && a.lse) a.lse[orow] = -INFINITY;
+        return;
+    }
+    float acc[4] = {0.f, 0.f, 0.f, 0.f};
+    float wsum = 0.f;
+    for (int s = 0; s < n; ++s) {
+        const long long prow = (long long)(base + s) * a.num_q_heads + h;
+        const float wgt = __expf(__ldg(&a.lse_part[prow]) - mx);
+        wsum += wgt;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const int d = lane + 32 * i;
+            if (d < a.head_dim) acc[i] = fmaf(wgt, __ldg(&a.o_part[prow * a.head_dim + d]), acc[i]);
+        }
+    }
+    const float inv = 1.f / wsum;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const int d = lane + 32 * i;
+        if (d < a.head_dim) a.out[orow * a.head_dim + d] = __bfloat16_as_ushort(__float2bfloat16_rn(acc[i] * inv));
+    }
+    if (lane == 0 && a.lse) a.lse[orow] = mx + __logf(wsum);
+}
+
+__global__ void wait_probe_kernel(int* status, uint64_t limit_ns) {
+    __shared__ __align__(8) uint64_t bar;
+    if (threadIdx.x == 0) {
+        mbar_init(&bar, 1);
+        fence_barrier_init();
+    }
+    __syncthreads();
+    // nothing ever arrives on `bar`: the bounded wait must give up on its own
+    if (threadIdx.x == 0 && !mbar_wait(&bar, 0, nullptr, limit_ns)) atomicCAS(status, 0, PA_ERR_TIMEOUT);
+}
+
+template <int D, bool FP8>
+cudaError_t launch_decode_t(const DecodeArgs& a, const CUtensorMap* mk, const CUtensorMap* mv, int grid,
+                            cudaStream_t stream) {
+    using L = DecodeLayout<D, FP8>;
+    static bool configured = false;
+    if (!configured) {
+        cudaError_t e = cudaFuncSetAttribute(decode_kernel<D, FP8>, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kSmem);
+        if (e != cudaSuccess) return e;
+        configured = true;
+    }
+    decode_kernel<D, FP8><<<grid, L::kThreads, L::kSmem, stream>>>(a, *mk, *mv);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_decode(int head_dim, bool fp8, const DecodeArgs& a, const CUtensorMap* mk, const CUtensorMap* mv,
+                          int grid, cudaStream_t stream) {
+    if (head_dim == 128) return fp8 ? launch_decode_t<128, true>(a, mk, mv, grid, stream)
+                                    : launch_decode_t<128, false>(a, mk, mv, grid, stream);
+    return fp8 ? launch_decode_t<64, true>(a, mk, mv, grid, stream) : launch_decode_t<64, false>(a, mk, mv, grid, stream);
+}
+
+cudaError_t launch_combine(const CombineArgs& a, cudaStream_t stream) {
+    const int warps = a.batch * a.num_q_heads;
+    combine_kernel<<<(warps + 3) / 4, 128, 0, stream>>>(a);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_wait_timeout_probe(int* status, uint64_t limit_ns, cudaStream_t stream) {
+    wait_probe_kernel<<<1, 32, 0, stream>>>(status, limit_ns);
+    return cudaGetLastError();
+}
+
+}  // namespace pa

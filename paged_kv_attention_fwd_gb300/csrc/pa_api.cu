@@ -1,0 +1,329 @@
+// pa_api.cu -- host side of libpa: argument validation, the split-KV
+// scheduler (pa_get_metadata), tensor-map construction and kernel launches.
+// Nothing here allocates device memory or synchronises a stream, except
+// pa_check_status, whose job is to synchronise and read the status word.
+#include <algorithm>
+#include <atomic>
+#include <cmath>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+#include <queue>
+#include <string>
+#include <vector>
+
+#include "pa_internal.h"
+
+namespace {
+
+thread_local std::string g_last_error;
+std::atomic<uint64_t> g_wait_limit_ns{2000000000ull};
+
+pa_status fail(pa_status st, const char* fmt, ...) {
+    char buf[512];
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(buf, sizeof buf, fmt, ap);
+    va_end(ap);
+    g_last_error = buf;
+    return st;
+}
+
+pa_status cuda_fail(cudaError_t e, const char* what) {
+    return fail(PA_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+int64_t cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
+
+// ------------------------------------------------------------ tensor maps
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+    static EncodeTiledFn fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(p);
+    });
+    return fn;
+}
+
+// Tiled map over a bf16 tensor of `rank` dims (innermost first), box of 64
+// elements (128 bytes) innermost, 128-byte swizzle.
+pa_status make_map_bf16(CUtensorMap* map, const void* base, int rank, const uint64_t* dims, const uint64_t* strides_bytes,
+                        const uint32_t* box) {
+    EncodeTiledFn enc = encode_fn();
+    if (!enc) return fail(PA_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
+    cuuint64_t d[5], s[4];
+    cuuint32_t b[5], e[5];
+    for (int i = 0; i < rank; ++i) {
+        d[i] = dims[i];
+        b[i] = box[i];
+        e[i] = 1;
+        if (i + 1 < rank) s[i] = strides_bytes[i];
+    }
+    CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, rank, const_cast<void*>(base), d, s, b, e,
+                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return fail(PA_ERR_INVALID_ARG, "cuTensorMapEncodeTiled failed (CUresult %d)", (int)r);
+    return PA_OK;
+}
+
+// ------------------------------------------------------------ scheduler
+
+struct SchedItem {
+    int cost, index, b, s, kvh;
+};
+
+}  // namespace
+
+extern "C" {
+
+int32_t pa_version(void) { return 100; }
+
+const char* pa_last_error(void) { return g_last_error.c_str(); }
+
+pa_status pa_set_wait_limit_ns(uint64_t limit_ns) {
+    if (limit_ns == 0) return fail(PA_ERR_INVALID_ARG, "wait limit must be positive");
+    g_wait_limit_ns.store(limit_ns);
+    return PA_OK;
+}
+
+pa_status pa_get_metadata(const int32_t* seq_lens_host, const int32_t* block_table_host, const pa_decode_shapes* sh,
+                          int32_t* meta_host, size_t meta_capacity_ints, pa_decode_plan* plan) {
+    if (!sh || !plan) return fail(PA_ERR_INVALID_ARG, "shapes and plan must not be NULL");
+    const int B = sh->batch, Hk = sh->num_kv_heads;
+    if (B < 0) return fail(PA_ERR_INVALID_ARG, "batch must be >= 0 (got %d)", B);
+    if (B > 0 && !seq_lens_host) return fail(PA_ERR_INVALID_ARG, "seq_lens_host must not be NULL");
+    if (Hk <= 0 || Hk > 65535) return fail(PA_ERR_INVALID_ARG, "num_kv_heads must be in [1, 65535] (got %d)", Hk);
+    if (sh->page_size != pa::kPage) return fail(PA_ERR_INVALID_ARG, "page_size must be 64 (got %d)", sh->page_size);
+    if (sh->max_pages_per_seq <= 0) return fail(PA_ERR_INVALID_ARG, "max_pages_per_seq must be positive");
+    if (sh->num_sms <= 0) return fail(PA_ERR_INVALID_ARG, "num_sms must be positive (got %d)", sh->num_sms);
+    if (sh->ctas_per_sm < 0) return fail(PA_ERR_INVALID_ARG, "ctas_per_sm must be >= 0");
+    if (sh->forced_splits < 0) return fail(PA_ERR_INVALID_ARG, "forced_splits must be >= 0");
+    const int cps = sh->ctas_per_sm == 0 ? 1 : sh->ctas_per_sm;
+
+    std::vector<int> pages(B);
+    int64_t units = 0;
+    for (int b = 0; b < B; ++b) {
+        const int len = seq_lens_host[b];
+        if (len < 0) return fail(PA_ERR_INVALID_ARG, "seq_lens[%d] = %d is negative", b, len);
+        if ((int64_t)len > (int64_t)sh->max_pages_per_seq * pa::kPage)
+            return fail(PA_ERR_INVALID_ARG, "seq_lens[%d] = %d exceeds max_pages_per_seq * 64 = %lld", b, len,
+                        (long long)sh->max_pages_per_seq * pa::kPage);
+        pages[b] = (int)cdiv(len, pa::kPage);
+        units += (int64_t)pages[b] * Hk;
+        if (block_table_host) {
+            for (int p = 0; p < pages[b]; ++p) {
+                const int32_t id = block_table_host[(int64_t)b * sh->max_pages_per_seq + p];
+                if (id < 0 || id >= sh->num_pool_pages)
+                    return fail(PA_ERR_INVALID_ARG, "block_table[%d, %d] = %d is outside [0, %d)", b, p, id,
+                                sh->num_pool_pages);
+            }
+        }
+    }
+    const int64_t cap = (int64_t)sh->num_sms * cps;
+    const int64_t chunk = std::max<int64_t>(4, cdiv(units, 4 * cap));
+    std::vector<int32_t> nsplit(B), indptr(B + 1, 0);
+    for (int b = 0; b < B; ++b) {
+        int n;
+        if (pages[b] <= 1) n = 1;
+        else if (sh->forced_splits > 0) n = std::min({sh->forced_splits, pages[b], PA_MAX_SPLITS});
+        else n = (int)std::min<int64_t>(cdiv(pages[b], chunk), PA_MAX_SPLITS);
+        nsplit[b] = n;
+        indptr[b + 1] = indptr[b] + n;
+    }
+    const int64_t total_splits = indptr[B];
+    std::vector<SchedItem> items;
+    items.reserve((size_t)total_splits * Hk);
+    for (int b = 0; b < B; ++b)
+        for (int s = 0; s < nsplit[b]; ++s) {
+            const int lo = (int)((int64_t)s * pages[b] / nsplit[b]);
+            const int hi = (int)((int64_t)(s + 1) * pages[b] / nsplit[b]);
+            for (int g = 0; g < Hk; ++g) items.push_back({hi - lo + 1, (int)items.size(), b, s, g});
+        }
+    const int64_t nitems = (int64_t)items.size();
+    const int64_t grid = std::min<int64_t>(nitems, cap);
+    const int64_t meta_ints = pa::kMetaHeader + 2 * (int64_t)B + 1 + grid + 1 + 2 * nitems;
+    if (meta_ints > INT32_MAX) return fail(PA_ERR_UNSUPPORTED, "metadata would exceed 2^31 entries");
+
+    plan->total_splits = (int32_t)total_splits;
+    plan->num_items = (int32_t)nitems;
+    plan->grid = (int32_t)grid;
+    plan->meta_ints = (int32_t)meta_ints;
+    plan->ctas_per_sm = cps;
+    plan->reserved = 0;
+    const int64_t hq = std::max(sh->num_q_heads, 0), d = std::max(sh->head_dim, 0);
+    plan->workspace_bytes = (size_t)PA_STATUS_BYTES + (size_t)(total_splits * hq * d * 4) +
+                            (size_t)(((total_splits * hq * 4) + 255) / 256 * 256);
+    if (!meta_host) return PA_OK;
+    if (meta_capacity_ints < (size_t)meta_ints)
+        return fail(PA_ERR_WORKSPACE, "metadata needs %lld int32 entries, capacity is %zu", (long long)meta_ints,
+                    meta_capacity_ints);
+
+    // longest first; each to the least-loaded CTA, ties to the lowest index
+    std::vector<SchedItem> order(items);
+    std::stable_sort(order.begin(), order.end(), [](const SchedItem& x, const SchedItem& y) {
+        return x.cost != y.cost ? x.cost > y.cost : x.index < y.index;
+    });
+    typedef std::pair<int64_t, int32_t> Load;  // (load, cta)
+    std::priority_queue<Load, std::vector<Load>, std::greater<Load>> heap;
+    for (int32_t c = 0; c < grid; ++c) heap.push({0, c});
+    std::vector<std::vector<int32_t>> per_cta(grid);
+    for (const SchedItem& it : order) {
+        Load l = heap.top();
+        heap.pop();
+        per_cta[l.second].push_back(it.index);
+        heap.push({l.first + it.cost, l.second});
+    }
+    int32_t* m = meta_host;
+    m[0] = pa::kMetaMagic;
+    m[1] = B;
+    m[2] = Hk;
+    m[3] = (int32_t)total_splits;
+    m[4] = (int32_t)nitems;
+    m[5] = (int32_t)grid;
+    m[6] = (int32_t)std::min<int64_t>(chunk, INT32_MAX);
+    m[7] = cps;
+    int64_t o = pa::kMetaHeader;
+    for (int b = 0; b < B; ++b) m[o++] = nsplit[b];
+    for (int b = 0; b <= B; ++b) m[o++] = indptr[b];
+    int32_t acc = 0;
+    m[o++] = 0;
+    for (int64_t c = 0; c < grid; ++c) {
+        acc += (int32_t)per_cta[c].size();
+        m[o++] = acc;
+    }
+    for (int64_t c = 0; c < grid; ++c)
+        for (int32_t idx : per_cta[c]) {
+            const SchedItem& it = items[idx];
+            m[o++] = it.b;
+            m[o++] = (it.s << 16) | it.kvh;
+        }
+    return PA_OK;
+}
+
+pa_status pa_decode(const pa_decode_shapes* sh, const pa_decode_plan* plan, const void* q, const void* k_pool,
+                    const void* v_pool, const float* k_scale, const float* v_scale, const int32_t* block_table,
+                    const int32_t* seq_lens, const int32_t* meta_dev, float scale, void* out, float* lse,
+                    void* workspace, size_t workspace_bytes, cudaStream_t stream) {
+    if (!sh || !plan) return fail(PA_ERR_INVALID_ARG, "shapes and plan must not be NULL");
+    const int B = sh->batch, Hq = sh->num_q_heads, Hk = sh->num_kv_heads, D = sh->head_dim;
+    if (B < 0) return fail(PA_ERR_INVALID_ARG, "batch must be >= 0");
+    if (B == 0) return PA_OK;
+    if (Hq <= 0 || Hk <= 0 || Hq % Hk != 0)
+        return fail(PA_ERR_INVALID_ARG, "num_q_heads (%d) must be a positive multiple of num_kv_heads (%d)", Hq, Hk);
+    if (Hq / Hk > PA_MAX_GROUP)
+        return fail(PA_ERR_UNSUPPORTED, "Hq / Hk = %d exceeds the supported group size %d", Hq / Hk, PA_MAX_GROUP);
+    if (D != 64 && D != 128) return fail(PA_ERR_UNSUPPORTED, "head_dim must be 64 or 128 (got %d)", D);
+    if (sh->page_size != pa::kPage) return fail(PA_ERR_INVALID_ARG, "page_size must be 64 (got %d)", sh->page_size);
+    if (sh->kv_dtype != PA_KV_BF16 && sh->kv_dtype != PA_KV_FP8_E4M3)
+        return fail(PA_ERR_INVALID_ARG, "unknown kv_dtype %d", sh->kv_dtype);
+    const bool fp8 = sh->kv_dtype == PA_KV_FP8_E4M3;
+    if (sh->max_pages_per_seq <= 0 || sh->num_pool_pages <= 0)
+        return fail(PA_ERR_INVALID_ARG, "max_pages_per_seq and num_pool_pages must be positive");
+    if ((int64_t)sh->num_pool_pages * Hk * pa::kPage >= ((int64_t)1 << 31))
+        return fail(PA_ERR_UNSUPPORTED, "pool rows (pages * Hk * 64) must be below 2^31");
+    if (!q || !k_pool || !v_pool || !block_table || !seq_lens || !meta_dev || !out || !workspace)
+        return fail(PA_ERR_INVALID_ARG, "a required pointer is NULL");
+    if (fp8 && (!k_scale || !v_scale)) return fail(PA_ERR_INVALID_ARG, "e4m3 KV needs k_scale and v_scale");
+    if (!aligned16(q) || !aligned16(k_pool) || !aligned16(v_pool) || !aligned16(out) || !aligned16(workspace))
+        return fail(PA_ERR_INVALID_ARG, "q, pools, out and workspace must be 16-byte aligned");
+    if (!std::isfinite(scale)) return fail(PA_ERR_INVALID_ARG, "scale must be finite");
+    if (plan->grid <= 0 || plan->total_splits < B || plan->meta_ints <= 0)
+        return fail(PA_ERR_INVALID_ARG, "plan does not come from pa_get_metadata for this batch");
+    if (workspace_bytes < plan->workspace_bytes)
+        return fail(PA_ERR_WORKSPACE, "workspace has %zu bytes, the plan needs %zu", workspace_bytes,
+                    plan->workspace_bytes);
+
+    pa::DecodeArgs a;
+    a.q = static_cast<const uint16_t*>(q);
+    a.k_pool = static_cast<const uint8_t*>(k_pool);
+    a.v_pool = static_cast<const uint8_t*>(v_pool);
+    a.k_scale = k_scale;
+    a.v_scale = v_scale;
+    a.block_table = block_table;
+    a.seq_lens = seq_lens;
+    a.meta = meta_dev;
+    a.out = static_cast<uint16_t*>(out);
+    a.lse = lse;
+    a.status = static_cast<int*>(workspace);
+    a.o_part = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + PA_STATUS_BYTES);
+    a.lse_part = a.o_part + (size_t)plan->total_splits * Hq * D;
+    a.batch = B;
+    a.num_q_heads = Hq;
+    a.num_kv_heads = Hk;
+    a.group = Hq / Hk;
+    a.max_pages = sh->max_pages_per_seq;
+    a.num_pool_pages = sh->num_pool_pages;
+    a.scale_log2 = scale * 1.4426950408889634f;
+    a.wait_ns = g_wait_limit_ns.load();
+
+    CUtensorMap mk, mv;
+    std::memset(&mk, 0, sizeof mk);
+    std::memset(&mv, 0, sizeof mv);
+    if (!fp8) {
+        const uint64_t dims[2] = {(uint64_t)D, (uint64_t)sh->num_pool_pages * Hk * pa::kPage};
+        const uint64_t strides[1] = {(uint64_t)D * 2};
+        const uint32_t box[2] = {64, 64};
+        pa_status st = make_map_bf16(&mk, k_pool, 2, dims, strides, box);
+        if (st != PA_OK) return st;
+        st = make_map_bf16(&mv, v_pool, 2, dims, strides, box);
+        if (st != PA_OK) return st;
+    }
+    cudaError_t e = pa::launch_decode(D, fp8, a, &mk, &mv, plan->grid, stream);
+    if (e != cudaSuccess) return cuda_fail(e, "decode launch");
+    if (plan->total_splits > B) {
+        pa::CombineArgs c;
+        c.meta = meta_dev;
+        c.o_part = a.o_part;
+        c.lse_part = a.lse_part;
+        c.out = a.out;
+        c.lse = lse;
+        c.batch = B;
+        c.num_q_heads = Hq;
+        c.head_dim = D;
+        e = pa::launch_combine(c, stream);
+        if (e != cudaSuccess) return cuda_fail(e, "combine launch");
+    }
+    return PA_OK;
+}
+
+pa_status pa_check_status(void* workspace, cudaStream_t stream) {
+    if (!workspace) return fail(PA_ERR_INVALID_ARG, "workspace must not be NULL");
+    int32_t word = 0;
+    cudaError_t e = cudaMemcpyAsync(&word, workspace, sizeof word, cudaMemcpyDeviceToHost, stream);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(stream);
+    if (e != cudaSuccess) return cuda_fail(e, "reading the status word");
+    if (word == 0) return PA_OK;
+    e = cudaMemsetAsync(workspace, 0, sizeof word, stream);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(stream);
+    if (e != cudaSuccess) return cuda_fail(e, "clearing the status word");
+    switch (word) {
+        case PA_ERR_TIMEOUT:
+            return fail(PA_ERR_TIMEOUT, "a device-side wait ran past its time limit");
+        case PA_ERR_DEVICE_BOUNDS:
+            return fail(PA_ERR_DEVICE_BOUNDS, "a kernel met a page id or length out of range");
+        default:
+            return fail((pa_status)word, "device status %d", word);
+    }
+}
+
+pa_status pa_debug_wait_timeout(void* workspace, uint64_t limit_ns, cudaStream_t stream) {
+    if (!workspace) return fail(PA_ERR_INVALID_ARG, "workspace must not be NULL");
+    cudaError_t e = pa::launch_wait_timeout_probe(static_cast<int*>(workspace), limit_ns, stream);
+    if (e != cudaSuccess) return cuda_fail(e, "wait-timeout probe launch");
+    return PA_OK;
+}
+
+}  // extern "C"

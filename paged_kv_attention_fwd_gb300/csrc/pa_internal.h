@@ -1,0 +1,72 @@
+// pa_internal.h -- declarations shared by the host API and the kernel files.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include "../../include/pa.h"
+
+namespace pa {
+
+constexpr int kPage = 64;
+constexpr int kMetaHeader = 8;
+constexpr int32_t kMetaMagic = 0x50414D31;
+
+// Arguments of the persistent decode kernel (passed by value as a grid constant).
+struct DecodeArgs {
+    const uint16_t* q;         // bf16 [B, Hq, D]
+    const uint8_t* k_pool;     // raw pool bytes (used by the e4m3 kernel's bulk copies)
+    const uint8_t* v_pool;
+    const float* k_scale;      // [Hk] (e4m3) or nullptr
+    const float* v_scale;
+    const int32_t* block_table;
+    const int32_t* seq_lens;
+    const int32_t* meta;
+    uint16_t* out;             // bf16 [B, Hq, D]
+    float* lse;                // [B, Hq] or nullptr
+    float* o_part;             // fp32 [total_splits, Hq, D]
+    float* lse_part;           // fp32 [total_splits, Hq]
+    int* status;               // status word
+    int32_t batch, num_q_heads, num_kv_heads, group, max_pages, num_pool_pages;
+    float scale_log2;          // softmax scale * log2(e)
+    uint64_t wait_ns;
+};
+
+struct CombineArgs {
+    const int32_t* meta;
+    const float* o_part;
+    const float* lse_part;
+    uint16_t* out;
+    float* lse;
+    int32_t batch, num_q_heads, head_dim;
+};
+
+// Launchers (decode.cu).  Return the CUDA error of the launch.
+cudaError_t launch_decode(int head_dim, bool fp8, const DecodeArgs& a, const CUtensorMap* map_k,
+                          const CUtensorMap* map_v, int grid, cudaStream_t stream);
+cudaError_t launch_combine(const CombineArgs& a, cudaStream_t stream);
+cudaError_t launch_wait_timeout_probe(int* status, uint64_t limit_ns, cudaStream_t stream);
+
+// Prefill (prefill.cu)
+struct PrefillArgs {
+    const int32_t* cu_q;
+    const int32_t* cu_k;
+    const int32_t* block_table;
+    const int32_t* qo_offset;
+    uint16_t* out;   // bf16 [total_q, Hq, Dv]
+    float* lse;      // [total_q, Hq] or nullptr
+    int* status;
+    int32_t batch, num_q_heads, num_kv_heads, group, max_pages, num_pool_pages, total_q;
+    int32_t num_q_tiles;  // ceil(max_seqlen_q / 128)
+    int32_t causal, paged, rope;
+    float scale_log2;
+    uint64_t wait_ns;
+};
+
+cudaError_t launch_prefill(const PrefillArgs& a, int head_dim_qk, const CUtensorMap* map_q,
+                           const CUtensorMap* map_k, const CUtensorMap* map_v, const CUtensorMap* map_r,
+                           cudaStream_t stream);
+
+}  // namespace pa

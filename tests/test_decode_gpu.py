@@ -1,0 +1,192 @@
+"""Decode parity on the GPU: libpa (through the C ABI) against the fp64 oracle
+on the same seeded inputs.  Tolerances: bf16 out max-abs 1e-2 and mean-abs
+1e-3, e4m3-KV out max-abs 5e-2, lse abs 1e-3; metadata bit-exact."""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from oracle import scheduler as S
+from paged_kv_attention_fwd_gb300 import binding as B
+from paged_kv_attention_fwd_gb300 import ops
+from paged_kv_attention_fwd_gb300 import workloads as W
+from paged_kv_attention_fwd_gb300.build import build
+
+pytestmark = pytest.mark.gpu
+
+TOL = {"bf16": (1e-2, 1e-3), "e4m3": (5e-2, 5e-3)}
+LSE_TOL = 1e-3
+
+
+@pytest.fixture(scope="module", autouse=True)
+def gpu():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    build()
+    torch.cuda.init()
+
+
+def to_dev(inp: W.DecodeInputs, dev="cuda"):
+    q = ops.as_bf16(inp.q, dev)
+    conv = ops.as_bf16 if inp.kv_dtype == "bf16" else ops.as_e4m3
+    kp, vp = conv(inp.k_pool, dev), conv(inp.v_pool, dev)
+    bt = torch.from_numpy(np.ascontiguousarray(inp.block_table)).to(dev)
+    sl = torch.from_numpy(np.ascontiguousarray(inp.seq_lens)).to(dev)
+    ks = vs = None
+    if inp.kv_dtype == "e4m3":
+        ks = torch.from_numpy(inp.k_scale).to(dev)
+        vs = torch.from_numpy(inp.v_scale).to(dev)
+    return q, kp, vp, bt, sl, ks, vs
+
+
+def run(inp: W.DecodeInputs, forced=0, check_host_table=True, **kw):
+    q, kp, vp, bt, sl, ks, vs = to_dev(inp)
+    p = ops.plan_decode(inp.seq_lens, inp.block_table if check_host_table else None, inp.num_q_heads,
+                        inp.num_kv_heads, inp.head_dim, inp.max_pages, inp.num_pool_pages, inp.kv_dtype,
+                        forced_splits=forced, **kw)
+    out, lse = ops.decode(p, q, kp, vp, bt, sl, inp.scale, ks, vs)
+    st = B.pa_check_status(p.workspace)
+    return out.float().cpu().numpy(), lse.cpu().numpy(), st, p
+
+
+def reference(inp: W.DecodeInputs):
+    return oracle.decode(inp.q, inp.k_pool, inp.v_pool, inp.block_table, inp.seq_lens, inp.scale,
+                         inp.kv_dtype, inp.k_scale, inp.v_scale)
+
+
+def assert_close(out, lse, ref_out, ref_lse, kv_dtype):
+    mx, mean = TOL[kv_dtype]
+    err = np.abs(out - ref_out)
+    assert np.all(np.isfinite(out))
+    assert err.max() <= mx, f"max abs err {err.max():.3g}"
+    assert err.mean() <= mean, f"mean abs err {err.mean():.3g}"
+    neg = np.isneginf(ref_lse)
+    assert np.array_equal(np.isneginf(lse), neg)
+    if (~neg).any():
+        lerr = np.abs(lse[~neg] - ref_lse[~neg])
+        assert lerr.max() <= LSE_TOL, f"lse err {lerr.max():.3g}"
+
+
+def test_tiny_paged_decode():
+    inp = W.tiny_decode(0)
+    out, lse, st, p = run(inp)
+    assert st == B.PA_OK
+    assert out.shape == (2, 8, 64) and lse.shape == (2, 8)
+    assert p.meta.tolist() == S.schedule(inp.seq_lens.tolist(), 4, ops.num_sms(), 1)
+    ref_out, ref_lse = reference(inp)
+    assert_close(out, lse, ref_out, ref_lse, "bf16")
+
+
+def test_gqa_decode_full_size():
+    inp = W.gqa_decode(0)
+    out, lse, st, p = run(inp)
+    assert st == B.PA_OK
+    assert p.plan.total_splits > inp.batch  # the auto rule splits the longer sequences
+    ref_out, ref_lse = reference(inp)
+    assert_close(out, lse, ref_out, ref_lse, "bf16")
+
+
+@pytest.mark.parametrize("forced", [1, 2, 7, 0])
+def test_split_count_does_not_change_result(forced):
+    inp = W.make_decode(8, 32, 8, 128, [1, 64, 65, 700, 1500, 2049, 3000, 129], seed=3)
+    out, lse, st, p = run(inp, forced=forced)
+    assert st == B.PA_OK
+    ref_out, ref_lse = reference(inp)
+    assert_close(out, lse, ref_out, ref_lse, "bf16")
+    base_out, base_lse, _, _ = run(inp, forced=1)
+    assert np.abs(out - base_out).max() <= 1e-2 and np.abs(lse - base_lse).max() <= 1e-4
+
+
+@pytest.mark.parametrize("hq,hk,d", [(8, 8, 128), (16, 8, 128), (64, 4, 128), (8, 4, 64), (16, 1, 64),
+                                     (32, 2, 128)])
+def test_group_sizes_and_edge_lengths(hq, hk, d):
+    lens = [0, 1, 2, 63, 64, 65, 127, 128, 129, 191, 255, 256, 257, 1000]
+    inp = W.make_decode(len(lens), hq, hk, d, lens, seed=hq + hk + d, extra_pages=2)
+    out, lse, st, _ = run(inp)
+    assert st == B.PA_OK
+    ref_out, ref_lse = reference(inp)
+    assert_close(out, lse, ref_out, ref_lse, "bf16")
+    assert np.all(out[0] == 0) and np.all(np.isneginf(lse[0]))
+
+
+@pytest.mark.parametrize("forced", [0, 3])
+def test_poisoned_rows_pages_and_stale_slots(forced):
+    inp = W.make_decode(6, 16, 4, 128, [37, 130, 64, 1, 700, 255], seed=4, extra_pages=5, max_pages=16)
+    clean = run(inp, forced=forced)
+    p = W.poison_stale_slots(W.poison_unused(inp))
+    dirty = run(p, forced=forced, check_host_table=False)
+    assert dirty[2] == B.PA_OK
+    assert np.all(np.isfinite(dirty[0]))
+    assert np.array_equal(clean[0], dirty[0]) and np.array_equal(clean[1], dirty[1])
+    ref_out, ref_lse = reference(inp)
+    assert_close(dirty[0], dirty[1], ref_out, ref_lse, "bf16")
+
+
+def test_deterministic_bitwise():
+    inp = W.make_decode(16, 32, 8, 128, W.uniform_lengths(9, 16, 1, 3000), seed=9)
+    a = run(inp)
+    b = run(inp)
+    assert np.array_equal(a[0], b[0]) and np.array_equal(a[1], b[1])
+
+
+def test_fp8_kv_decode():
+    lens = W.lognormal_lengths(5, 24, math.log(700.0), 1.0, 64, 4000)
+    inp = W.make_decode(24, 64, 8, 128, lens, seed=5, kv_dtype="e4m3")
+    out, lse, st, p = run(inp)
+    assert st == B.PA_OK
+    ref_out, ref_lse = reference(inp)
+    assert_close(out, lse, ref_out, ref_lse, "e4m3")
+
+
+@pytest.mark.parametrize("hq,hk,d", [(8, 4, 64), (16, 16, 128)])
+def test_fp8_edges(hq, hk, d):
+    lens = [0, 1, 63, 64, 65, 129, 300]
+    inp = W.make_decode(len(lens), hq, hk, d, lens, seed=6, kv_dtype="e4m3", extra_pages=3)
+    p = W.poison_unused(inp)
+    out, lse, st, _ = run(p)
+    assert st == B.PA_OK
+    ref_out, ref_lse = reference(inp)
+    assert_close(out, lse, ref_out, ref_lse, "e4m3")
+
+
+def test_fp8_long_context_full_size_sampled():
+    """The full long-context e4m3 workload; every output is checked against the
+    oracle on a sample of 16 sequences (longest and shortest included)."""
+    inp = W.fp8_long_decode(0)
+    out, lse, st, p = run(inp)
+    assert st == B.PA_OK
+    assert p.plan.total_splits > inp.batch
+    order = np.argsort(inp.seq_lens)
+    pick = np.unique(np.concatenate([order[:4], order[-6:], np.arange(0, 128, 21)]))
+    sub = W.DecodeInputs(q=inp.q[pick], k_pool=inp.k_pool, v_pool=inp.v_pool, block_table=inp.block_table[pick],
+                         seq_lens=inp.seq_lens[pick], scale=inp.scale, kv_dtype="e4m3", k_scale=inp.k_scale,
+                         v_scale=inp.v_scale)
+    ref_out, ref_lse = reference(sub)
+    assert_close(out[pick], lse[pick], ref_out, ref_lse, "e4m3")
+    assert np.all(np.isfinite(out))
+
+
+def test_device_bounds_are_reported_not_faulted():
+    inp = W.make_decode(2, 8, 4, 128, [100, 200], seed=7)
+    bad = W.DecodeInputs(**{**inp.__dict__})
+    bad.block_table = inp.block_table.copy()
+    bad.block_table[1, 2] = inp.num_pool_pages + 5  # live slot (200 keys -> 4 pages)
+    out, lse, st, _ = run(bad, check_host_table=False)
+    assert st == B.PA_ERR_DEVICE_BOUNDS
+    # the context is still usable and a clean call still succeeds
+    out2, lse2, st2, _ = run(inp)
+    assert st2 == B.PA_OK
+    ref_out, ref_lse = reference(inp)
+    assert_close(out2, lse2, ref_out, ref_lse, "bf16")
+
+
+def test_bounded_wait_times_out_cleanly():
+    ws = torch.zeros(B.PA_STATUS_BYTES, dtype=torch.uint8, device="cuda")
+    B.pa_debug_wait_timeout(ws, 20_000_000)  # 20 ms on a barrier nothing arrives on
+    assert B.pa_check_status(ws) == B.PA_ERR_TIMEOUT
+    assert B.pa_check_status(ws) == B.PA_OK  # cleared by the read
+    inp = W.tiny_decode(0)
+    out, lse, st, _ = run(inp)
+    assert st == B.PA_OK
