@@ -1,0 +1,446 @@
+#!/usr/bin/env python
+"""Benchmark: attention forward over a paged KV cache on GB300.
+
+Default workload (the headline): batched GQA decode -- B=64, Hq=32, Hk=8,
+D=128, bf16 KV in 64-row pages, seq_lens uniform in [1, 4096], seed 0.  The
+metric is decode KV-read bandwidth: the K+V page bytes the step must read
+(sum_b ceil(len_b/64) * 64 * Hk * D * 2 bytes * 2) per second.
+
+One step = one pass of the decode hot path over the batch: the split-KV
+attention kernel and the log-sum-exp combine (the host scheduler's metadata
+is an input resident in HBM, as in serving where one schedule serves every
+layer; the end-to-end number recomputes it every step).
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
+  python bench.py --impl reference ...   # the fp64 CPU oracle as the reference arm
+
+Prints one JSON line (rank 0).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "paged-attn decode KV-read GB/s (%HBM peak); prefill TFLOP/s (%TC peak)"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+L2_FLUSH_BYTES = 256 << 20
+PROFILES = os.path.join(ROOT, "profiles")
+CSRC = os.path.join(ROOT, "paged_kv_attention_fwd_gb300", "csrc")
+
+
+# ------------------------------------------------------------------ helpers
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            p = json.load(f)
+        return p, "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+def source_sha(files):
+    h = hashlib.sha256()
+    for f in files:
+        with open(os.path.join(CSRC, f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic(profile_name, files):
+    """DRAM bytes per launch recorded by an ncu capture of this kernel, if the
+    kernel source is unchanged since the capture (else None)."""
+    path = os.path.join(PROFILES, profile_name)
+    if not os.path.exists(path):
+        return None
+    vals = {}
+    with open(path) as f:
+        for line in f:
+            if ":" in line and line.strip().startswith(("source_sha256", "dram_bytes_per_launch_full")):
+                k, v = line.split(":", 1)
+                vals[k.strip()] = v.strip().strip("`")
+    if vals.get("source_sha256") != source_sha(files):
+        return None
+    try:
+        return float(vals["dram_bytes_per_launch_full"])
+    except (KeyError, ValueError):
+        return None
+
+
+class ClockSampler:
+    """nvidia-smi sampling of SM clock and throttle reasons during the timed region."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+        self.out_path = os.path.join("/tmp", f"pa_clocks_{os.getpid()}.csv")
+
+    def __enter__(self):
+        try:
+            self.fh = open(self.out_path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=self.fh, stderr=subprocess.DEVNULL)
+            time.sleep(0.3)
+        except OSError:
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            time.sleep(0.25)
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+            self.fh.close()
+
+    def summary(self):
+        if self.proc is None or not os.path.exists(self.out_path):
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        sm, mx, power, reasons = [], [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        with open(self.out_path) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) < 7:
+                    continue
+                try:
+                    sm.append(float(parts[0]))
+                    mx.append(float(parts[1]))
+                    power.append(float(parts[2]))
+                except ValueError:
+                    continue
+                for n, v in zip(names, parts[3:7]):
+                    if v.lower() == "active":
+                        reasons.add(n)
+        os.unlink(self.out_path)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "power_w_max": max(power),
+                "samples": len(sm), "reasons": sorted(reasons)}
+
+
+def gpu_index(local_rank):
+    vis = os.environ.get("CUDA_VISIBLE_DEVICES")
+    if vis:
+        ids = [x.strip() for x in vis.split(",") if x.strip()]
+        if local_rank < len(ids):
+            return ids[local_rank]
+    return local_rank
+
+
+# ------------------------------------------------------------------ workloads
+
+def decode_workload(name):
+    from paged_kv_attention_fwd_gb300 import workloads as W
+    if name == "decode_gqa":
+        inp = W.gqa_decode(0)
+        desc = ("batched GQA decode: B=64, Hq=32, Hk=8, D=128, bf16 KV, page 64, q_len 1, "
+                "seq_lens uniform[1,4096], seed 0")
+    elif name == "decode_fp8":
+        inp = W.fp8_long_decode(0)
+        desc = ("long-context decode, e4m3 KV with per-KV-head fp32 scales: B=128, Hq=64, Hk=8, D=128, page 64, "
+                "seq_lens lognormal(ln 2048, 1) clipped to [64,16384], seed 0")
+    elif name == "decode_tiny":
+        inp = W.tiny_decode(0)
+        desc = "tiny paged decode: B=2, Hq=8, Hk=4, D=64, seq_lens {37,130}, 8-page pool, seed 0"
+    else:
+        raise ValueError(name)
+    return inp, desc
+
+
+def kv_bytes(inp):
+    el = 2 if inp.kv_dtype == "bf16" else 1
+    pages = sum((int(s) + 63) // 64 for s in inp.seq_lens)
+    full = pages * 64 * inp.num_kv_heads * inp.head_dim * el * 2
+    exact = int(np.sum(inp.seq_lens)) * inp.num_kv_heads * inp.head_dim * el * 2
+    return full, exact
+
+
+# ------------------------------------------------------------------ reference arm (the oracle)
+
+def cpu_oracle_decode_sample(inp, budget_s=None, steps=None, warmup=0):
+    """Time the fp64 oracle on one sequence per step (cycling the batch).
+    With budget_s: run until the budget is spent.  Returns (GB/s, seconds,
+    sequences done, bytes)."""
+    import oracle
+    order = list(range(inp.batch))
+
+    def one(b):
+        sub = slice(b, b + 1)
+        oracle.decode(inp.q[sub], inp.k_pool, inp.v_pool, inp.block_table[sub], inp.seq_lens[sub], inp.scale,
+                      inp.kv_dtype, inp.k_scale, inp.v_scale)
+        el = 2 if inp.kv_dtype == "bf16" else 1
+        return ((int(inp.seq_lens[b]) + 63) // 64) * 64 * inp.num_kv_heads * inp.head_dim * el * 2
+
+    for i in range(warmup):
+        one(order[i % len(order)])
+    done, nbytes = 0, 0
+    t0 = time.perf_counter()
+    while True:
+        nbytes += one(order[done % len(order)])
+        done += 1
+        el = time.perf_counter() - t0
+        if steps is not None and done >= steps:
+            break
+        if budget_s is not None and el >= budget_s and done >= 1:
+            break
+    return nbytes / el / 1e9, el, done, nbytes
+
+
+def run_reference(args):
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    import oracle
+    inp, desc = decode_workload(args.workload)
+    gbs, el, done, nbytes = cpu_oracle_decode_sample(inp, steps=args.steps, warmup=args.warmup)
+    cores = oracle.num_threads()
+    sample = f"{done} single-sequence decode steps cycling the batch ({nbytes / 1e9:.3f} GB of K+V pages)"
+    line = {
+        "impl": "reference", "metric": METRIC, "value": round(gbs, 4), "unit": "GB/s", "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(el / done * 1e3, 4),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": desc, "implementation": "fp64 CPU oracle (oracle/oracle.c), OpenMP"},
+        "cpu_baseline": {"value": round(gbs, 4), "unit": "GB/s", "cores": cores, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": round(gbs, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+# ------------------------------------------------------------------ our arm
+
+def run_decode(args, rank, world, local_rank, dist):
+    import torch
+    from paged_kv_attention_fwd_gb300 import binding as B
+    from paged_kv_attention_fwd_gb300 import ops
+
+    dev = torch.device("cuda", local_rank)
+    torch.cuda.set_device(dev)
+    inp, desc = decode_workload(args.workload)
+    full_bytes, exact_bytes = kv_bytes(inp)
+    fp8 = inp.kv_dtype == "e4m3"
+    q = ops.as_bf16(inp.q, dev)
+    conv = ops.as_e4m3 if fp8 else ops.as_bf16
+    kp, vp = conv(inp.k_pool, dev), conv(inp.v_pool, dev)
+    bt = torch.from_numpy(inp.block_table).to(dev)
+    sl = torch.from_numpy(inp.seq_lens).to(dev)
+    ks = torch.from_numpy(inp.k_scale).to(dev) if fp8 else None
+    vs = torch.from_numpy(inp.v_scale).to(dev) if fp8 else None
+    p = ops.plan_decode(inp.seq_lens, inp.block_table, inp.num_q_heads, inp.num_kv_heads, inp.head_dim,
+                        inp.max_pages, inp.num_pool_pages, inp.kv_dtype, device=dev)
+    out = torch.empty((inp.batch, inp.num_q_heads, inp.head_dim), dtype=torch.bfloat16, device=dev)
+    lse = torch.empty((inp.batch, inp.num_q_heads), dtype=torch.float32, device=dev)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    sh, plan = p.shapes, p.plan
+    combine = plan.total_splits > inp.batch
+
+    def attend():
+        B.pa_decode_attend(sh, plan, q, kp, vp, ks, vs, bt, sl, p.meta_dev, inp.scale, out, lse, p.workspace,
+                           stream=stream)
+
+    def comb():
+        B.pa_decode_combine(sh, plan, p.meta_dev, out, lse, p.workspace, stream=stream)
+
+    for _ in range(args.warmup):
+        flush.zero_()
+        attend()
+        comb()
+    torch.cuda.synchronize(dev)
+    st = B.pa_check_status(p.workspace, stream)
+    if st != B.PA_OK:
+        raise RuntimeError(f"device status {st}: {B.pa_last_error()}")
+
+    K = args.steps
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(K)]
+    if dist is not None:
+        dist.barrier()
+    torch.cuda.synchronize(dev)
+    with ClockSampler(gpu_index(local_rank)) as clk:
+        for i in range(K):
+            flush.zero_()  # L2 flush between timed iterations (outside the events)
+            ev[i][0].record(stream)
+            attend()
+            ev[i][1].record(stream)
+            comb()
+            ev[i][2].record(stream)
+        torch.cuda.synchronize(dev)
+    if dist is not None:
+        dist.barrier()
+    attend_ms = [ev[i][0].elapsed_time(ev[i][1]) for i in range(K)]
+    step_ms = [ev[i][0].elapsed_time(ev[i][2]) for i in range(K)]
+    ms = sum(step_ms) / K
+    kern_ms = sum(attend_ms) / K
+    if dist is not None:
+        t = torch.tensor([ms, kern_ms], dtype=torch.float64, device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms, kern_ms = float(t[0]), float(t[1])
+    st = B.pa_check_status(p.workspace, stream)
+    if st != B.PA_OK:
+        raise RuntimeError(f"device status {st}: {B.pa_last_error()}")
+    clocks = clk.summary()
+
+    pk, pk_src = peaks()
+    value = world * full_bytes / (ms * 1e-3) / 1e9
+    achieved = full_bytes / (kern_ms * 1e-3) / 1e9
+    kernel_files = ["decode.cu", "pa_ptx.cuh", "pa_internal.h"]
+    prof = "decode_kernel_" + args.workload + ".md"
+    roofline = {"bound": "hbm", "achieved": round(achieved, 1), "peak": pk["hbm_gbs"], "unit": "GB/s",
+                "frac": round(achieved / pk["hbm_gbs"], 4), "traffic": profiled_traffic(prof, kernel_files),
+                "kernel": "decode_kernel", "peak_source": f"{pk_src} (copy bandwidth)",
+                "algorithmic_bytes_per_launch": full_bytes, "kernel_ms": round(kern_ms, 5)}
+
+    e2e = None
+    if not args.no_e2e:
+        e2e = decode_e2e(inp, dev, stream, sh, full_bytes, world, dist, args)
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        import oracle
+        gbs, el, done, nbytes = cpu_oracle_decode_sample(inp, budget_s=args.cpu_seconds)
+        cpu = {"value": round(gbs, 4), "unit": "GB/s", "cores": oracle.num_threads(), "kind": "oracle",
+               "sample": f"{done} sequences of this batch through the fp64 oracle "
+                         f"({nbytes / 1e9:.3f} GB of K+V pages, {el:.1f} s)"}
+    launches = K * (1 + int(combine))
+    line = {
+        "metric": METRIC, "value": round(value, 1), "unit": "GB/s", "n_gpus": world, "steps": K,
+        "warmup": args.warmup, "ms_per_step": round(ms, 5), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "e4m3+bf16" if fp8 else "bf16", "data": "synthetic",
+        "config": {"workload": desc, "batch": inp.batch, "num_q_heads": inp.num_q_heads,
+                   "num_kv_heads": inp.num_kv_heads, "head_dim": inp.head_dim, "page_size": 64,
+                   "kv_bytes_per_step": full_bytes, "kv_bytes_token_exact": exact_bytes,
+                   "pct_hbm_peak": round(100 * value / world / pk["hbm_gbs"], 2),
+                   "splits": plan.total_splits, "ctas": plan.grid,
+                   "l2": f"flushed between steps ({L2_FLUSH_BYTES >> 20} MiB write, outside the events)",
+                   "parallelism": f"replicas x{world}"},
+        "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": launches, "clocks": clocks,
+    }
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
+def decode_e2e(inp, dev, stream, sh, full_bytes, world, dist, args):
+    """End to end through the public calls with host buffers: every step
+    computes the schedule on the host, copies all inputs from pinned memory,
+    runs pa_decode and reads out + lse back."""
+    import torch
+    from paged_kv_attention_fwd_gb300 import binding as B
+
+    fp8 = inp.kv_dtype == "e4m3"
+
+    def pinned(a):
+        t = torch.from_numpy(np.ascontiguousarray(a))
+        return t.pin_memory()
+
+    h = {"q": pinned(inp.q.view(np.int16)), "k": pinned(inp.k_pool if fp8 else inp.k_pool.view(np.int16)),
+         "v": pinned(inp.v_pool if fp8 else inp.v_pool.view(np.int16)), "bt": pinned(inp.block_table),
+         "sl": pinned(inp.seq_lens)}
+    if fp8:
+        h["ks"], h["vs"] = pinned(inp.k_scale), pinned(inp.v_scale)
+    d = {k: torch.empty_like(v, device=dev) for k, v in h.items()}
+    meta0, plan0 = B.pa_get_metadata(inp.seq_lens, None, sh)
+    meta_pin = torch.empty(plan0.meta_ints, dtype=torch.int32).pin_memory()
+    meta_dev = torch.empty(plan0.meta_ints, dtype=torch.int32, device=dev)
+    ws = torch.zeros(plan0.workspace_bytes, dtype=torch.uint8, device=dev)
+    out_h = torch.empty((inp.batch, inp.num_q_heads, inp.head_dim), dtype=torch.int16).pin_memory()
+    lse_h = torch.empty((inp.batch, inp.num_q_heads), dtype=torch.float32).pin_memory()
+    out_d = torch.empty_like(out_h, device=dev)
+    lse_d = torch.empty_like(lse_h, device=dev)
+    sl_host = inp.seq_lens
+
+    def step():
+        meta, plan = B.pa_get_metadata(sl_host, None, sh)
+        meta_pin.numpy()[: meta.size] = meta
+        for k in h:
+            d[k].copy_(h[k], non_blocking=True)
+        meta_dev[: meta.size].copy_(meta_pin[: meta.size], non_blocking=True)
+        B.pa_decode(sh, plan, d["q"], d["k"], d["v"], d.get("ks"), d.get("vs"), d["bt"], d["sl"], meta_dev,
+                    inp.scale, out_d, lse_d, ws, stream=stream)
+        out_h.copy_(out_d, non_blocking=True)
+        lse_h.copy_(lse_d, non_blocking=True)
+        torch.cuda.synchronize(dev)
+
+    for _ in range(3):
+        step()
+    E = max(3, min(args.steps, args.e2e_steps))
+    if dist is not None:
+        dist.barrier()
+    torch.cuda.synchronize(dev)
+    t0 = time.perf_counter()
+    for _ in range(E):
+        step()
+    el = time.perf_counter() - t0
+    if dist is not None:
+        t = torch.tensor([el], dtype=torch.float64, device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        el = float(t[0])
+    h2d = sum(v.numel() * v.element_size() for v in h.values()) + plan0.meta_ints * 4
+    d2h = out_h.numel() * 2 + lse_h.numel() * 4
+    return {"value": round(world * full_bytes * E / el / 1e9, 2), "unit": "GB/s", "h2d_bytes_per_step": h2d,
+            "d2h_bytes_per_step": d2h, "steps": E, "ms_per_step": round(el / E * 1e3, 4),
+            "includes": "host schedule + pinned H2D of all inputs + pa_decode + D2H of out/lse + sync"}
+
+
+# ------------------------------------------------------------------ main
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=5000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default="decode_gqa", choices=["decode_gqa", "decode_fp8", "decode_tiny"])
+    ap.add_argument("--e2e-steps", type=int, default=20)
+    ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+
+    if args.impl == "reference":
+        run_reference(args)
+        return
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    dist = None
+    if world > 1:
+        import torch
+        import torch.distributed as tdist
+        torch.cuda.set_device(local_rank)
+        tdist.init_process_group("nccl", device_id=torch.device("cuda", local_rank))
+        dist = tdist
+    from paged_kv_attention_fwd_gb300.build import build
+    if rank == 0 or world == 1:
+        build()
+    if dist is not None:
+        dist.barrier()
+    run_decode(args, rank, world, local_rank, dist)
+    if dist is not None:
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -149,6 +149,27 @@ pa_status pa_decode(const pa_decode_shapes* shapes, const pa_decode_plan* plan, 
                     float scale, void* out, float* lse, void* workspace, size_t workspace_bytes,
                     cudaStream_t stream);
 
+/*
+ * The two steps pa_decode runs, callable on their own (same arguments and
+ * rules as pa_decode):
+ *   pa_decode_attend   the decode kernel alone: sequences with one split get
+ *                      their final out / lse; split sequences leave fp32
+ *                      partials (output normalised by its split's own sum, and
+ *                      the split's log-sum-exp) in the workspace;
+ *   pa_decode_combine  merges those partials: with m = max_s lse_s,
+ *                      lse = m + ln sum_s exp(lse_s - m) and
+ *                      out = sum_s exp(lse_s - lse) * o_s.
+ *                      A no-op when plan->total_splits == batch.
+ */
+pa_status pa_decode_attend(const pa_decode_shapes* shapes, const pa_decode_plan* plan, const void* q,
+                           const void* k_pool, const void* v_pool, const float* k_scale, const float* v_scale,
+                           const int32_t* block_table, const int32_t* seq_lens, const int32_t* meta_dev,
+                           float scale, void* out, float* lse, void* workspace, size_t workspace_bytes,
+                           cudaStream_t stream);
+
+pa_status pa_decode_combine(const pa_decode_shapes* shapes, const pa_decode_plan* plan, const int32_t* meta_dev,
+                            void* out, float* lse, void* workspace, size_t workspace_bytes, cudaStream_t stream);
+
 /* ----------------------------------------------------------------- prefill */
 
 typedef struct {

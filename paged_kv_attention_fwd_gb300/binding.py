@@ -67,6 +67,9 @@ def lib() -> ctypes.CDLL:
                                       ctypes.POINTER(pa_decode_plan)]
         L.pa_decode.argtypes = [ctypes.POINTER(pa_decode_shapes), ctypes.POINTER(pa_decode_plan), _P, _P, _P, _P,
                                 _P, _P, _P, _P, f32, _P, _P, _P, sz, _P]
+        L.pa_decode_attend.argtypes = L.pa_decode.argtypes
+        L.pa_decode_combine.argtypes = [ctypes.POINTER(pa_decode_shapes), ctypes.POINTER(pa_decode_plan), _P, _P,
+                                        _P, _P, sz, _P]
         L.pa_prefill.argtypes = [ctypes.POINTER(pa_prefill_shapes), _P, _P, _P, _P, _P, _P, _P, _P, ctypes.c_int,
                                  f32, _P, _P, _P, sz, _P]
         L.pa_check_status.argtypes = [_P, _P]
@@ -74,7 +77,7 @@ def lib() -> ctypes.CDLL:
         L.pa_set_wait_limit_ns.argtypes = [u64]
         L.pa_debug_wait_timeout.argtypes = [_P, u64, _P]
         L.pa_version.restype = i32
-        for f in ("pa_get_metadata", "pa_decode", "pa_prefill", "pa_check_status", "pa_set_wait_limit_ns",
+        for f in ("pa_get_metadata", "pa_decode", "pa_decode_attend", "pa_decode_combine", "pa_prefill", "pa_check_status", "pa_set_wait_limit_ns",
                   "pa_debug_wait_timeout"):
             getattr(L, f).restype = ctypes.c_int
         _lib = L
@@ -137,6 +140,25 @@ def pa_decode(shapes: pa_decode_shapes, plan: pa_decode_plan, q, k_pool, v_pool,
                            _ptr(k_scale), _ptr(v_scale), _ptr(block_table), _ptr(seq_lens), _ptr(meta_dev),
                            float(scale), _ptr(out), _ptr(lse), _ptr(workspace), int(workspace_bytes),
                            _stream(stream)))
+
+
+def pa_decode_attend(shapes: pa_decode_shapes, plan: pa_decode_plan, q, k_pool, v_pool, k_scale, v_scale,
+                     block_table, seq_lens, meta_dev, scale: float, out, lse, workspace,
+                     workspace_bytes: Optional[int] = None, stream=None) -> None:
+    if workspace_bytes is None:
+        workspace_bytes = workspace.numel() * workspace.element_size()
+    _check(lib().pa_decode_attend(ctypes.byref(shapes), ctypes.byref(plan), _ptr(q), _ptr(k_pool), _ptr(v_pool),
+                                  _ptr(k_scale), _ptr(v_scale), _ptr(block_table), _ptr(seq_lens),
+                                  _ptr(meta_dev), float(scale), _ptr(out), _ptr(lse), _ptr(workspace),
+                                  int(workspace_bytes), _stream(stream)))
+
+
+def pa_decode_combine(shapes: pa_decode_shapes, plan: pa_decode_plan, meta_dev, out, lse, workspace,
+                      workspace_bytes: Optional[int] = None, stream=None) -> None:
+    if workspace_bytes is None:
+        workspace_bytes = workspace.numel() * workspace.element_size()
+    _check(lib().pa_decode_combine(ctypes.byref(shapes), ctypes.byref(plan), _ptr(meta_dev), _ptr(out), _ptr(lse),
+                                   _ptr(workspace), int(workspace_bytes), _stream(stream)))
 
 
 def pa_prefill(shapes: pa_prefill_shapes, q, k, v, k_rope, cu_seqlens_q, cu_seqlens_k, block_table, qo_offset,

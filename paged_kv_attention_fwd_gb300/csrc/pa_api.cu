@@ -213,10 +213,10 @@ pa_status pa_get_metadata(const int32_t* seq_lens_host, const int32_t* block_tab
     return PA_OK;
 }
 
-pa_status pa_decode(const pa_decode_shapes* sh, const pa_decode_plan* plan, const void* q, const void* k_pool,
-                    const void* v_pool, const float* k_scale, const float* v_scale, const int32_t* block_table,
-                    const int32_t* seq_lens, const int32_t* meta_dev, float scale, void* out, float* lse,
-                    void* workspace, size_t workspace_bytes, cudaStream_t stream) {
+namespace {
+
+pa_status validate_decode_common(const pa_decode_shapes* sh, const pa_decode_plan* plan, const void* out,
+                                 const void* meta_dev, const void* workspace, size_t workspace_bytes) {
     if (!sh || !plan) return fail(PA_ERR_INVALID_ARG, "shapes and plan must not be NULL");
     const int B = sh->batch, Hq = sh->num_q_heads, Hk = sh->num_kv_heads, D = sh->head_dim;
     if (B < 0) return fail(PA_ERR_INVALID_ARG, "batch must be >= 0");
@@ -227,6 +227,31 @@ pa_status pa_decode(const pa_decode_shapes* sh, const pa_decode_plan* plan, cons
         return fail(PA_ERR_UNSUPPORTED, "Hq / Hk = %d exceeds the supported group size %d", Hq / Hk, PA_MAX_GROUP);
     if (D != 64 && D != 128) return fail(PA_ERR_UNSUPPORTED, "head_dim must be 64 or 128 (got %d)", D);
     if (sh->page_size != pa::kPage) return fail(PA_ERR_INVALID_ARG, "page_size must be 64 (got %d)", sh->page_size);
+    if (!out || !meta_dev || !workspace) return fail(PA_ERR_INVALID_ARG, "a required pointer is NULL");
+    if (!aligned16(out) || !aligned16(workspace))
+        return fail(PA_ERR_INVALID_ARG, "q, pools, out and workspace must be 16-byte aligned");
+    if (plan->grid <= 0 || plan->total_splits < B || plan->meta_ints <= 0)
+        return fail(PA_ERR_INVALID_ARG, "plan does not come from pa_get_metadata for this batch");
+    if (workspace_bytes < plan->workspace_bytes)
+        return fail(PA_ERR_WORKSPACE, "workspace has %zu bytes, the plan needs %zu", workspace_bytes,
+                    plan->workspace_bytes);
+    return PA_OK;
+}
+
+float* partial_o(void* workspace) {
+    return reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + PA_STATUS_BYTES);
+}
+
+}  // namespace
+
+pa_status pa_decode_attend(const pa_decode_shapes* sh, const pa_decode_plan* plan, const void* q,
+                           const void* k_pool, const void* v_pool, const float* k_scale, const float* v_scale,
+                           const int32_t* block_table, const int32_t* seq_lens, const int32_t* meta_dev,
+                           float scale, void* out, float* lse, void* workspace, size_t workspace_bytes,
+                           cudaStream_t stream) {
+    pa_status st = validate_decode_common(sh, plan, out, meta_dev, workspace, workspace_bytes);
+    if (st != PA_OK || sh->batch == 0) return st;
+    const int B = sh->batch, Hq = sh->num_q_heads, Hk = sh->num_kv_heads, D = sh->head_dim;
     if (sh->kv_dtype != PA_KV_BF16 && sh->kv_dtype != PA_KV_FP8_E4M3)
         return fail(PA_ERR_INVALID_ARG, "unknown kv_dtype %d", sh->kv_dtype);
     const bool fp8 = sh->kv_dtype == PA_KV_FP8_E4M3;
@@ -234,17 +259,12 @@ pa_status pa_decode(const pa_decode_shapes* sh, const pa_decode_plan* plan, cons
         return fail(PA_ERR_INVALID_ARG, "max_pages_per_seq and num_pool_pages must be positive");
     if ((int64_t)sh->num_pool_pages * Hk * pa::kPage >= ((int64_t)1 << 31))
         return fail(PA_ERR_UNSUPPORTED, "pool rows (pages * Hk * 64) must be below 2^31");
-    if (!q || !k_pool || !v_pool || !block_table || !seq_lens || !meta_dev || !out || !workspace)
+    if (!q || !k_pool || !v_pool || !block_table || !seq_lens)
         return fail(PA_ERR_INVALID_ARG, "a required pointer is NULL");
     if (fp8 && (!k_scale || !v_scale)) return fail(PA_ERR_INVALID_ARG, "e4m3 KV needs k_scale and v_scale");
-    if (!aligned16(q) || !aligned16(k_pool) || !aligned16(v_pool) || !aligned16(out) || !aligned16(workspace))
+    if (!aligned16(q) || !aligned16(k_pool) || !aligned16(v_pool))
         return fail(PA_ERR_INVALID_ARG, "q, pools, out and workspace must be 16-byte aligned");
     if (!std::isfinite(scale)) return fail(PA_ERR_INVALID_ARG, "scale must be finite");
-    if (plan->grid <= 0 || plan->total_splits < B || plan->meta_ints <= 0)
-        return fail(PA_ERR_INVALID_ARG, "plan does not come from pa_get_metadata for this batch");
-    if (workspace_bytes < plan->workspace_bytes)
-        return fail(PA_ERR_WORKSPACE, "workspace has %zu bytes, the plan needs %zu", workspace_bytes,
-                    plan->workspace_bytes);
 
     pa::DecodeArgs a;
     a.q = static_cast<const uint16_t*>(q);
@@ -258,7 +278,7 @@ pa_status pa_decode(const pa_decode_shapes* sh, const pa_decode_plan* plan, cons
     a.out = static_cast<uint16_t*>(out);
     a.lse = lse;
     a.status = static_cast<int*>(workspace);
-    a.o_part = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + PA_STATUS_BYTES);
+    a.o_part = partial_o(workspace);
     a.lse_part = a.o_part + (size_t)plan->total_splits * Hq * D;
     a.batch = B;
     a.num_q_heads = Hq;
@@ -276,27 +296,43 @@ pa_status pa_decode(const pa_decode_shapes* sh, const pa_decode_plan* plan, cons
         const uint64_t dims[2] = {(uint64_t)D, (uint64_t)sh->num_pool_pages * Hk * pa::kPage};
         const uint64_t strides[1] = {(uint64_t)D * 2};
         const uint32_t box[2] = {64, 64};
-        pa_status st = make_map_bf16(&mk, k_pool, 2, dims, strides, box);
+        st = make_map_bf16(&mk, k_pool, 2, dims, strides, box);
         if (st != PA_OK) return st;
         st = make_map_bf16(&mv, v_pool, 2, dims, strides, box);
         if (st != PA_OK) return st;
     }
     cudaError_t e = pa::launch_decode(D, fp8, a, &mk, &mv, plan->grid, stream);
     if (e != cudaSuccess) return cuda_fail(e, "decode launch");
-    if (plan->total_splits > B) {
-        pa::CombineArgs c;
-        c.meta = meta_dev;
-        c.o_part = a.o_part;
-        c.lse_part = a.lse_part;
-        c.out = a.out;
-        c.lse = lse;
-        c.batch = B;
-        c.num_q_heads = Hq;
-        c.head_dim = D;
-        e = pa::launch_combine(c, stream);
-        if (e != cudaSuccess) return cuda_fail(e, "combine launch");
-    }
     return PA_OK;
+}
+
+pa_status pa_decode_combine(const pa_decode_shapes* sh, const pa_decode_plan* plan, const int32_t* meta_dev,
+                            void* out, float* lse, void* workspace, size_t workspace_bytes, cudaStream_t stream) {
+    pa_status st = validate_decode_common(sh, plan, out, meta_dev, workspace, workspace_bytes);
+    if (st != PA_OK || sh->batch == 0) return st;
+    if (plan->total_splits == sh->batch) return PA_OK;
+    pa::CombineArgs c;
+    c.meta = meta_dev;
+    c.o_part = partial_o(workspace);
+    c.lse_part = c.o_part + (size_t)plan->total_splits * sh->num_q_heads * sh->head_dim;
+    c.out = static_cast<uint16_t*>(out);
+    c.lse = lse;
+    c.batch = sh->batch;
+    c.num_q_heads = sh->num_q_heads;
+    c.head_dim = sh->head_dim;
+    cudaError_t e = pa::launch_combine(c, stream);
+    if (e != cudaSuccess) return cuda_fail(e, "combine launch");
+    return PA_OK;
+}
+
+pa_status pa_decode(const pa_decode_shapes* sh, const pa_decode_plan* plan, const void* q, const void* k_pool,
+                    const void* v_pool, const float* k_scale, const float* v_scale, const int32_t* block_table,
+                    const int32_t* seq_lens, const int32_t* meta_dev, float scale, void* out, float* lse,
+                    void* workspace, size_t workspace_bytes, cudaStream_t stream) {
+    pa_status st = pa_decode_attend(sh, plan, q, k_pool, v_pool, k_scale, v_scale, block_table, seq_lens, meta_dev,
+                                    scale, out, lse, workspace, workspace_bytes, stream);
+    if (st != PA_OK) return st;
+    return pa_decode_combine(sh, plan, meta_dev, out, lse, workspace, workspace_bytes, stream);
 }
 
 pa_status pa_check_status(void* workspace, cudaStream_t stream) {

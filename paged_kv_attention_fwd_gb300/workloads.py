@@ -162,17 +162,40 @@ class DecodeInputs:
     def max_pages(self): return self.block_table.shape[1]
 
 
-def _quantise_per_head(x: np.ndarray):
-    """x float32 [P, Hk, 64, D] -> (e4m3 bits, per-head scale = amax / 448)."""
+def _to_bf16_bits_fast(x: np.ndarray) -> np.ndarray:
+    """Same result as f32_to_bf16_bits (round to nearest even), via torch's
+    multi-threaded CPU cast; used for the large pools."""
+    import torch
+    t = torch.from_numpy(np.ascontiguousarray(x, dtype=np.float32)).to(torch.bfloat16)
+    return t.view(torch.int16).numpy().view(np.uint16)
+
+
+def _to_e4m3_bits_fast(x: np.ndarray) -> np.ndarray:
+    """Same result as f32_to_e4m3_bits for inputs already inside [-448, 448]."""
+    import torch
+    t = torch.from_numpy(np.ascontiguousarray(x, dtype=np.float32)).to(torch.float8_e4m3fn)
+    return t.view(torch.uint8).numpy()
+
+
+def bf16_normal_fast(seed: int, stream: int, shape) -> np.ndarray:
+    n = int(np.prod(shape)) if len(shape) else 1
+    return _to_bf16_bits_fast(normal_f32(seed, stream, n)).reshape(shape)
+
+
+def quantise_per_head(x: np.ndarray, fast: bool = True):
+    """x float32 [P, Hk, 64, D] -> (e4m3 bits, float32 scale per KV head).
+
+    scale_h = amax(|x[:, h]|) / 448 (1 for an all-zero head); the stored code is
+    e4m3(clamp(float32(x / scale_h), -448, 448)), rounded to nearest even.
+    """
+    import torch
+    xt = torch.from_numpy(np.ascontiguousarray(x, dtype=np.float32))
     hk = x.shape[1]
-    scales = np.empty(hk, dtype=np.float32)
-    bits = np.empty(x.shape, dtype=np.uint8)
-    for h in range(hk):
-        amax = float(np.max(np.abs(x[:, h]))) if x.shape[0] else 1.0
-        s = np.float32(amax / E4M3_MAX) if amax > 0 else np.float32(1.0)
-        scales[h] = s
-        bits[:, h] = f32_to_e4m3_bits(x[:, h].astype(np.float64) / float(s))
-    return bits, scales
+    amax = xt.abs().amax(dim=(0, 2, 3)) if x.shape[0] else torch.zeros(hk)
+    scales = torch.where(amax > 0, amax / E4M3_MAX, torch.ones_like(amax)).to(torch.float32)
+    y = (xt / scales.view(1, hk, 1, 1)).clamp_(-E4M3_MAX, E4M3_MAX)
+    bits = _to_e4m3_bits_fast(y.numpy()) if fast else f32_to_e4m3_bits(y.numpy())
+    return bits.reshape(x.shape), scales.numpy()
 
 
 def make_decode(batch: int, num_q_heads: int, num_kv_heads: int, head_dim: int,
@@ -185,12 +208,12 @@ def make_decode(batch: int, num_q_heads: int, num_kv_heads: int, head_dim: int,
     q = bf16_normal(seed, _S_Q, (batch, num_q_heads, head_dim))
     n = int(np.prod(pool_shape))
     if kv_dtype == "bf16":
-        k = f32_to_bf16_bits(normal_f32(seed, _S_K, n)).reshape(pool_shape)
-        v = f32_to_bf16_bits(normal_f32(seed, _S_V, n)).reshape(pool_shape)
+        k = bf16_normal_fast(seed, _S_K, pool_shape)
+        v = bf16_normal_fast(seed, _S_V, pool_shape)
         ks = vs = None
     elif kv_dtype == "e4m3":
-        k, ks = _quantise_per_head(normal_f32(seed, _S_K, n).reshape(pool_shape))
-        v, vs = _quantise_per_head(normal_f32(seed, _S_V, n).reshape(pool_shape))
+        k, ks = quantise_per_head(normal_f32(seed, _S_K, n).reshape(pool_shape))
+        v, vs = quantise_per_head(normal_f32(seed, _S_V, n).reshape(pool_shape))
     else:
         raise ValueError(kv_dtype)
     return DecodeInputs(q=q, k_pool=k, v_pool=v, block_table=bt, seq_lens=seq_lens,
@@ -282,9 +305,9 @@ def make_paged_prefill(q_lens, kv_lens, num_q_heads: int, num_kv_heads: int, hea
     total_q = int(q_lens.sum())
     pool_shape = (num_pool, num_kv_heads, PAGE_SIZE, head_dim)
     return PrefillInputs(
-        q=bf16_normal(seed, _S_Q, (total_q, num_q_heads, head_dim)),
-        k=bf16_normal(seed, _S_K, pool_shape),
-        v=bf16_normal(seed, _S_V, pool_shape),
+        q=bf16_normal_fast(seed, _S_Q, (total_q, num_q_heads, head_dim)),
+        k=bf16_normal_fast(seed, _S_K, pool_shape),
+        v=bf16_normal_fast(seed, _S_V, pool_shape),
         cu_seqlens_q=cu_seqlens(q_lens), cu_seqlens_k=cu_seqlens(kv_lens),
         scale=1.0 / math.sqrt(head_dim), causal=causal, block_table=bt,
         qo_offset=None if qo_offset is None else np.asarray(qo_offset, dtype=np.int32))
@@ -311,9 +334,9 @@ def make_ragged_prefill(lens, num_heads: int, head_dim_qk: int, head_dim_v: int,
     tq, tk = int(lens.sum()), int(kv_lens.sum())
     dk = head_dim_qk - rope_dim
     return PrefillInputs(
-        q=bf16_normal(seed, _S_Q, (tq, num_heads, head_dim_qk)),
-        k=bf16_normal(seed, _S_K, (tk, hk, dk)),
-        v=bf16_normal(seed, _S_V, (tk, hk, head_dim_v)),
+        q=bf16_normal_fast(seed, _S_Q, (tq, num_heads, head_dim_qk)),
+        k=bf16_normal_fast(seed, _S_K, (tk, hk, dk)),
+        v=bf16_normal_fast(seed, _S_V, (tk, hk, head_dim_v)),
         cu_seqlens_q=cu_seqlens(lens), cu_seqlens_k=cu_seqlens(kv_lens),
         scale=1.0 / math.sqrt(head_dim_qk), causal=causal,
         k_rope=bf16_normal(seed, _S_KROPE, (tk, 1, rope_dim)) if rope_dim else None,

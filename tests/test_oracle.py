@@ -339,3 +339,15 @@ def test_fp8_scales_fold_into_scores_and_values():
     np.testing.assert_allclose(o2[0], 3 * o3[0], rtol=1e-12, atol=1e-13)
     np.testing.assert_allclose(o2[1], o3[1], rtol=1e-12)
     assert not np.allclose(base[0], o3[0])
+
+
+def test_generator_fast_paths_equal_reference_encoders():
+    x = W.normal_f32(7, 98, 50000) * np.float32(3.0)
+    assert np.array_equal(W._to_bf16_bits_fast(x), W.f32_to_bf16_bits(x))
+    pool = x[: 4 * 2 * 64 * 48].reshape(4, 2, 64, 48)
+    fast, s1 = W.quantise_per_head(pool, fast=True)
+    ref, s2 = W.quantise_per_head(pool, fast=False)
+    assert np.array_equal(fast, ref) and np.array_equal(s1, s2)
+    # every head uses its full range: the largest magnitude encodes to +-448
+    dec = oracle.e4m3_to_f64(fast.reshape(-1)).reshape(fast.shape)
+    assert np.allclose(np.abs(dec).max(axis=(0, 2, 3)), 448.0)
