@@ -170,6 +170,33 @@ pa_status pa_decode_attend(const pa_decode_shapes* shapes, const pa_decode_plan*
 pa_status pa_decode_combine(const pa_decode_shapes* shapes, const pa_decode_plan* plan, const int32_t* meta_dev,
                             void* out, float* lse, void* workspace, size_t workspace_bytes, cudaStream_t stream);
 
+/*
+ * pa_decode_noalloc -- pa_decode for callers that cannot allocate device
+ * memory, for instance code whose host framework owns every byte of device
+ * memory through its own pool, or a loop that cannot afford the device-wide
+ * synchronisation an allocation may cause.  (The pages have no counterpart to
+ * this call; it exists for such callers.)
+ *
+ * Same arguments as pa_decode without the workspace: the split partials and
+ * the status word live in one scratch array of 16 MiB in this library's own
+ * device memory, which every GPU that loads the library keeps until the
+ * process exits.  The call allocates nothing and frees nothing.
+ *   - plan->workspace_bytes above 16 MiB is rejected with PA_ERR_WORKSPACE.
+ *   - The first call on a device looks up the scratch array's device address
+ *     (with that device current); make that first call before any stream
+ *     capture.
+ *   - All calls share the one array, which keeps the last call's contents;
+ *     the status word is cleared at the start of each call.  Calls that may
+ *     overlap on the GPU (other streams, other host threads) race on it.
+ *   - status_host: NULL, or a host int32 that receives the device status word
+ *     (PA_OK or the first device-detected fault); the call then waits for
+ *     `stream` before returning.
+ */
+pa_status pa_decode_noalloc(const pa_decode_shapes* shapes, const pa_decode_plan* plan, const void* q,
+                            const void* k_pool, const void* v_pool, const float* k_scale, const float* v_scale,
+                            const int32_t* block_table, const int32_t* seq_lens, const int32_t* meta_dev,
+                            float scale, void* out, float* lse, int32_t* status_host, cudaStream_t stream);
+
 /* ----------------------------------------------------------------- prefill */
 
 typedef struct {

@@ -70,6 +70,9 @@ def lib() -> ctypes.CDLL:
         L.pa_decode_attend.argtypes = L.pa_decode.argtypes
         L.pa_decode_combine.argtypes = [ctypes.POINTER(pa_decode_shapes), ctypes.POINTER(pa_decode_plan), _P, _P,
                                         _P, _P, sz, _P]
+        L.pa_decode_noalloc.argtypes = [ctypes.POINTER(pa_decode_shapes), ctypes.POINTER(pa_decode_plan), _P, _P,
+                                        _P, _P, _P, _P, _P, _P, f32, _P, _P, _P, _P]
+        L.pa_decode_noalloc.restype = ctypes.c_int
         L.pa_prefill.argtypes = [ctypes.POINTER(pa_prefill_shapes), _P, _P, _P, _P, _P, _P, _P, _P, ctypes.c_int,
                                  f32, _P, _P, _P, sz, _P]
         L.pa_check_status.argtypes = [_P, _P]
@@ -159,6 +162,20 @@ def pa_decode_combine(shapes: pa_decode_shapes, plan: pa_decode_plan, meta_dev, 
         workspace_bytes = workspace.numel() * workspace.element_size()
     _check(lib().pa_decode_combine(ctypes.byref(shapes), ctypes.byref(plan), _ptr(meta_dev), _ptr(out), _ptr(lse),
                                    _ptr(workspace), int(workspace_bytes), _stream(stream)))
+
+
+def pa_decode_noalloc(shapes: pa_decode_shapes, plan: pa_decode_plan, q, k_pool, v_pool, k_scale, v_scale,
+                      block_table, seq_lens, meta_dev, scale: float, out, lse, want_status: bool = True,
+                      stream=None) -> int:
+    """Decode without a caller workspace (the library's own 16 MiB scratch).
+    Returns the device status word when want_status (the call then waits for
+    the stream), else PA_OK without waiting."""
+    status = ctypes.c_int32(-1)
+    _check(lib().pa_decode_noalloc(ctypes.byref(shapes), ctypes.byref(plan), _ptr(q), _ptr(k_pool), _ptr(v_pool),
+                                   _ptr(k_scale), _ptr(v_scale), _ptr(block_table), _ptr(seq_lens),
+                                   _ptr(meta_dev), float(scale), _ptr(out), _ptr(lse),
+                                   ctypes.byref(status) if want_status else None, _stream(stream)))
+    return status.value if want_status else PA_OK
 
 
 def pa_prefill(shapes: pa_prefill_shapes, q, k, v, k_rope, cu_seqlens_q, cu_seqlens_k, block_table, qo_offset,

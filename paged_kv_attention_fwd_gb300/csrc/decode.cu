@@ -28,6 +28,9 @@
 #include <cuda_fp16.h>
 #include <cuda_fp8.h>
 
+#include <cstdio>
+#include <mutex>
+
 #include "pa_internal.h"
 #include "pa_ptx.cuh"
 
@@ -724,3 +727,84 @@ cudaError_t launch_wait_timeout_probe(int* status, uint64_t limit_ns, cudaStream
 }
 
 }  // namespace pa
+
+// ---------------------------------------------------------------------------
+// Decode for callers that cannot allocate device memory.
+//
+// Some callers own no allocator of their own: a host framework may keep every
+// byte of device memory in its own pool and forbid outside allocations, or a
+// serving loop may not tolerate the device-wide synchronisation cudaMalloc
+// can cause.  pa_decode needs a caller-provided workspace for its split-KV
+// partials and status word; pa_decode_noalloc uses instead one scratch array
+// that lives in this library's own device memory for as long as the library
+// is loaded (every GPU that loads it holds kNoAllocScratchBytes).
+namespace {
+
+constexpr size_t kNoAllocScratchBytes = size_t(16) << 20;  // 16 MiB
+static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
+
+std::mutex g_noalloc_mutex;
+void* g_noalloc_ptr[128] = {};  // device address of the scratch, per device ordinal
+
+// In host code the array's name is only a host-side stand-in; its device
+// address has to be asked for, once per device, with that device current.
+pa_status noalloc_scratch(void** out) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess || dev < 0 || dev >= 128) return PA_ERR_CUDA;
+    std::lock_guard<std::mutex> lock(g_noalloc_mutex);
+    if (!g_noalloc_ptr[dev]) {
+        void* p = nullptr;
+        e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+        if (e != cudaSuccess || !p) return PA_ERR_CUDA;
+        g_noalloc_ptr[dev] = p;
+    }
+    *out = g_noalloc_ptr[dev];
+    return PA_OK;
+}
+
+}  // namespace
+
+extern "C" pa_status pa_decode_noalloc(const pa_decode_shapes* shapes, const pa_decode_plan* plan, const void* q,
+                                       const void* k_pool, const void* v_pool, const float* k_scale,
+                                       const float* v_scale, const int32_t* block_table, const int32_t* seq_lens,
+                                       const int32_t* meta_dev, float scale, void* out, float* lse,
+                                       int32_t* status_host, cudaStream_t stream) {
+    if (!plan) {
+        pa::set_last_error("plan must not be NULL");
+        return PA_ERR_INVALID_ARG;
+    }
+    if (plan->workspace_bytes > kNoAllocScratchBytes) {
+        char msg[200];
+        snprintf(msg, sizeof msg,
+                 "this plan needs %zu bytes of scratch; pa_decode_noalloc has a fixed %zu-byte scratch "
+                 "(use pa_decode with a workspace, or fewer splits)",
+                 plan->workspace_bytes, kNoAllocScratchBytes);
+        pa::set_last_error(msg);
+        return PA_ERR_WORKSPACE;
+    }
+    void* scratch = nullptr;
+    pa_status st = noalloc_scratch(&scratch);
+    if (st != PA_OK) {
+        pa::set_last_error("could not look up the device address of the no-alloc scratch array");
+        return st;
+    }
+    // the status word must start at zero; the partials are written before read
+    if (cudaMemsetAsync(scratch, 0, PA_STATUS_BYTES, stream) != cudaSuccess) {
+        pa::set_last_error("clearing the no-alloc status word failed");
+        return PA_ERR_CUDA;
+    }
+    st = pa_decode_attend(shapes, plan, q, k_pool, v_pool, k_scale, v_scale, block_table, seq_lens, meta_dev, scale,
+                          out, lse, scratch, kNoAllocScratchBytes, stream);
+    if (st != PA_OK) return st;
+    st = pa_decode_combine(shapes, plan, meta_dev, out, lse, scratch, kNoAllocScratchBytes, stream);
+    if (st != PA_OK || !status_host) return st;
+    int32_t word = 0;
+    if (cudaMemcpyAsync(&word, scratch, sizeof word, cudaMemcpyDeviceToHost, stream) != cudaSuccess ||
+        cudaStreamSynchronize(stream) != cudaSuccess) {
+        pa::set_last_error("reading the no-alloc status word failed");
+        return PA_ERR_CUDA;
+    }
+    *status_host = word;
+    return PA_OK;
+}

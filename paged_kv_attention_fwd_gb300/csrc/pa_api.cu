@@ -87,6 +87,10 @@ struct SchedItem {
 
 }  // namespace
 
+namespace pa {
+void set_last_error(const char* msg) { g_last_error = msg; }
+}  // namespace pa
+
 extern "C" {
 
 int32_t pa_version(void) { return 100; }

@@ -69,4 +69,7 @@ cudaError_t launch_prefill(const PrefillArgs& a, int head_dim_qk, const CUtensor
                            const CUtensorMap* map_k, const CUtensorMap* map_v, const CUtensorMap* map_r,
                            cudaStream_t stream);
 
+// Record a message for pa_last_error() on this host thread (pa_api.cu).
+void set_last_error(const char* msg);
+
 }  // namespace pa
