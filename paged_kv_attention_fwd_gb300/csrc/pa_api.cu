@@ -339,6 +339,105 @@ pa_status pa_decode(const pa_decode_shapes* sh, const pa_decode_plan* plan, cons
     return pa_decode_combine(sh, plan, meta_dev, out, lse, workspace, workspace_bytes, stream);
 }
 
+pa_status pa_prefill(const pa_prefill_shapes* sh, const void* q, const void* k, const void* v, const void* k_rope,
+                     const int32_t* cu_seqlens_q, const int32_t* cu_seqlens_k, const int32_t* block_table,
+                     const int32_t* qo_offset, int causal, float scale, void* out, float* lse, void* workspace,
+                     size_t workspace_bytes, cudaStream_t stream) {
+    if (!sh) return fail(PA_ERR_INVALID_ARG, "shapes must not be NULL");
+    const int B = sh->batch, Hq = sh->num_q_heads, Hk = sh->num_kv_heads;
+    if (B < 0 || sh->total_q < 0 || sh->total_k < 0 || sh->max_seqlen_q < 0)
+        return fail(PA_ERR_INVALID_ARG, "batch, total_q, total_k and max_seqlen_q must be >= 0");
+    if (B == 0 || sh->total_q == 0 || sh->max_seqlen_q == 0) return PA_OK;
+    if (Hq <= 0 || Hk <= 0 || Hq % Hk != 0)
+        return fail(PA_ERR_INVALID_ARG, "num_q_heads (%d) must be a positive multiple of num_kv_heads (%d)", Hq, Hk);
+    if (Hq > 65535) return fail(PA_ERR_UNSUPPORTED, "num_q_heads above 65535");
+    const bool paged = block_table != nullptr;
+    const bool rope = sh->rope_dim != 0;
+    if (sh->head_dim_v != 128) return fail(PA_ERR_UNSUPPORTED, "head_dim_v must be 128 (got %d)", sh->head_dim_v);
+    if (!((sh->head_dim_qk == 128 && sh->rope_dim == 0) || (sh->head_dim_qk == 192 && sh->rope_dim == 64)))
+        return fail(PA_ERR_UNSUPPORTED, "head_dim_qk / rope_dim must be 128 / 0 or 192 / 64 (got %d / %d)",
+                    sh->head_dim_qk, sh->rope_dim);
+    if (rope && paged) return fail(PA_ERR_UNSUPPORTED, "a shared rope key is supported with ragged keys only");
+    if (rope && !k_rope) return fail(PA_ERR_INVALID_ARG, "rope_dim 64 needs k_rope");
+    if (!rope && k_rope) return fail(PA_ERR_INVALID_ARG, "k_rope given but rope_dim is 0");
+    if (paged) {
+        if (sh->page_size != pa::kPage) return fail(PA_ERR_INVALID_ARG, "page_size must be 64 (got %d)", sh->page_size);
+        if (sh->max_pages_per_seq <= 0 || sh->num_pool_pages <= 0)
+            return fail(PA_ERR_INVALID_ARG, "paged keys need max_pages_per_seq and num_pool_pages > 0");
+        if ((int64_t)sh->num_pool_pages * Hk * pa::kPage >= ((int64_t)1 << 31))
+            return fail(PA_ERR_UNSUPPORTED, "pool rows (pages * Hk * 64) must be below 2^31");
+    } else if (sh->total_k <= 0) {
+        return fail(PA_ERR_INVALID_ARG, "ragged keys need total_k > 0");
+    }
+    if (!q || !k || !v || !cu_seqlens_q || !cu_seqlens_k || !out || !workspace)
+        return fail(PA_ERR_INVALID_ARG, "a required pointer is NULL");
+    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out) || (k_rope && !aligned16(k_rope)) ||
+        !aligned16(workspace))
+        return fail(PA_ERR_INVALID_ARG, "q, k, v, k_rope, out and workspace must be 16-byte aligned");
+    if (!std::isfinite(scale)) return fail(PA_ERR_INVALID_ARG, "scale must be finite");
+    if (workspace_bytes < PA_STATUS_BYTES)
+        return fail(PA_ERR_WORKSPACE, "workspace needs %d bytes, got %zu", PA_STATUS_BYTES, workspace_bytes);
+
+    const int dqk = sh->head_dim_qk, dk = dqk - sh->rope_dim;
+    CUtensorMap mq, mk, mv, mr;
+    std::memset(&mr, 0, sizeof mr);
+    {
+        const uint64_t dims[3] = {(uint64_t)dqk, (uint64_t)Hq, (uint64_t)sh->total_q};
+        const uint64_t strides[2] = {(uint64_t)dqk * 2, (uint64_t)Hq * dqk * 2};
+        const uint32_t box[3] = {64, 1, 128};
+        pa_status st = make_map_bf16(&mq, q, 3, dims, strides, box);
+        if (st != PA_OK) return st;
+    }
+    if (paged) {
+        const uint64_t dims[2] = {128, (uint64_t)sh->num_pool_pages * Hk * pa::kPage};
+        const uint64_t strides[1] = {256};
+        const uint32_t box[2] = {64, 64};
+        pa_status st = make_map_bf16(&mk, k, 2, dims, strides, box);
+        if (st == PA_OK) st = make_map_bf16(&mv, v, 2, dims, strides, box);
+        if (st != PA_OK) return st;
+    } else {
+        const uint64_t dk_dims[3] = {(uint64_t)dk, (uint64_t)Hk, (uint64_t)sh->total_k};
+        const uint64_t dk_str[2] = {(uint64_t)dk * 2, (uint64_t)Hk * dk * 2};
+        const uint64_t dv_dims[3] = {128, (uint64_t)Hk, (uint64_t)sh->total_k};
+        const uint64_t dv_str[2] = {256, (uint64_t)Hk * 256};
+        const uint32_t box[3] = {64, 1, 128};
+        pa_status st = make_map_bf16(&mk, k, 3, dk_dims, dk_str, box);
+        if (st == PA_OK) st = make_map_bf16(&mv, v, 3, dv_dims, dv_str, box);
+        if (st == PA_OK && rope) {
+            const uint64_t rd[2] = {64, (uint64_t)sh->total_k};
+            const uint64_t rs[1] = {128};
+            const uint32_t rb[2] = {64, 128};
+            st = make_map_bf16(&mr, k_rope, 2, rd, rs, rb);
+        }
+        if (st != PA_OK) return st;
+    }
+    pa::PrefillArgs a;
+    a.cu_q = cu_seqlens_q;
+    a.cu_k = cu_seqlens_k;
+    a.block_table = block_table;
+    a.qo_offset = qo_offset;
+    a.out = static_cast<uint16_t*>(out);
+    a.lse = lse;
+    a.status = static_cast<int*>(workspace);
+    a.batch = B;
+    a.num_q_heads = Hq;
+    a.num_kv_heads = Hk;
+    a.group = Hq / Hk;
+    a.max_pages = paged ? sh->max_pages_per_seq : 0;
+    a.num_pool_pages = paged ? sh->num_pool_pages : 0;
+    a.total_q = sh->total_q;
+    a.num_q_tiles = (int32_t)cdiv(sh->max_seqlen_q, 256);
+    a.causal = causal != 0;
+    a.paged = paged;
+    a.rope = rope;
+    a.scale_log2 = scale * 1.4426950408889634f;
+    a.wait_ns = g_wait_limit_ns.load();
+    if ((int64_t)a.num_q_tiles * B > INT32_MAX) return fail(PA_ERR_UNSUPPORTED, "grid too large");
+    cudaError_t e = pa::launch_prefill(a, dqk, &mq, &mk, &mv, &mr, stream);
+    if (e != cudaSuccess) return cuda_fail(e, "prefill launch");
+    return PA_OK;
+}
+
 pa_status pa_check_status(void* workspace, cudaStream_t stream) {
     if (!workspace) return fail(PA_ERR_INVALID_ARG, "workspace must not be NULL");
     int32_t word = 0;

@@ -1,8 +1,504 @@
-// prefill.cu -- placeholder until the tcgen05 prefill kernel lands.
-#include "pa_internal.h"
+// prefill.cu -- causal (or full) attention for ragged query segments on sm_103a:
+// chunked prefill against the paged cache (FlashMLA "Tensor Shapes Reference",
+// section 4 mha_fwd_kvcache: K/V gathered through block_table, "Prefill to
+// Cache Mapping"), ragged prefill (MATE dense mode, flash_attn_varlen_func)
+// and the MLA shape whose 64-wide rope key is shared by all heads (Modular
+// flare_mla_prefill: q depth 192 = 128 per-head + 64 shared, output depth 128).
+//
+// One CTA per (segment b, 256-row query block, query head h): two 128-row
+// query tiles A and B that share every K/V tile.
+//
+//   warp 0     producer: TMA of the two query tiles once, then 128-key K and
+//              V tiles into separate rings (paged: two 64-row page slabs per
+//              tile through block_table; ragged: 3-D boxes over [T, H, D])
+//   warp 1     MMA issuer (tcgen05, fp32 accumulators in TMEM, 512 columns):
+//                S_X[128 q, 128 keys] = Q_X . K^T          (both from smem)
+//                O_X[128 q, 128 dv]  += P_X . V            (P_X from TMEM)
+//              issue order QK_A(j+1) right after PV_A(j), so the softmax of
+//              one tile overlaps the other tile's MMAs
+//   warps 2-5  softmax of tile A, warps 6-9 softmax of tile B: one query row
+//              per thread (its TMEM lane), row max and sum without any
+//              cross-thread exchange; P (bf16) is stored over the S columns;
+//              O is rescaled in TMEM only when the running max grows by more
+//              than 2^8 (otherwise the stale max stays exact and cheaper)
+//
+// Query row i of segment b sees key j iff j < kv_len and (not causal or
+// j <= qo_offset + i), qo_offset defaulting to kv_len - q_len (MATE
+// _normalize_qo_offset / _resolve_seqused_k).  Every wait is bounded.
+#include <cuda_bf16.h>
 
-extern "C" pa_status pa_prefill(const pa_prefill_shapes*, const void*, const void*, const void*, const void*,
-                                const int32_t*, const int32_t*, const int32_t*, const int32_t*, int, float, void*,
-                                float*, void*, size_t, cudaStream_t) {
-    return PA_ERR_UNSUPPORTED;
+#include "pa_internal.h"
+#include "pa_ptx.cuh"
+
+namespace pa {
+namespace {
+
+constexpr float kLn2f = 0.69314718055994531f;
+constexpr float kRescaleThreshold = 8.0f;  // log2 units
+
+enum : int {
+    P_QF = 0,
+    P_KF = 1,   // [2]
+    P_KE = 3,   // [2]
+    P_VF = 5,   // [2]
+    P_VE = 7,   // [2]
+    P_VZ = 9,   // dead V rows of the last tile zeroed
+    P_SF = 10,  // [2] S_A, S_B ready
+    P_PF = 12,  // [2] P_A, P_B written
+    P_OD = 14,  // [2] PV_A, PV_B retired
+    P_DONE = 16,
+    P_COUNT = 17
+};
+
+template <bool ROPE>
+struct PrefillLayout {
+    static constexpr int kDqk = ROPE ? 192 : 128;
+    static constexpr int kQChunks = kDqk / 64;
+    static constexpr int kTile = 16384;                 // 128 rows x 128 bytes
+    static constexpr int kQBytes = kQChunks * kTile;    // one 128-row query tile
+    static constexpr int kKBytes = kQChunks * kTile;    // one 128-key K tile
+    static constexpr int kVBytes = 2 * kTile;           // one 128-key V tile (dv 128)
+    static constexpr int kNK = ROPE ? 1 : 2;
+    static constexpr int kNV = 2;
+    static constexpr int kQOff = 0;
+    static constexpr int kKOff = 2 * kQBytes;
+    static constexpr int kVOff = kKOff + kNK * kKBytes;
+    static constexpr int kBytes = kVOff + kNV * kVBytes;
+    static constexpr int kSmem = kBytes + 1024;
+    static constexpr int kThreads = 320;
+};
+
+__device__ __forceinline__ float ex2(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
 }
+
+struct Seg {
+    int q0, q_len, k0, kv_len, off;
+};
+
+__device__ __forceinline__ Seg load_seg(const PrefillArgs& a, int b) {
+    Seg s;
+    s.q0 = __ldg(&a.cu_q[b]);
+    s.q_len = __ldg(&a.cu_q[b + 1]) - s.q0;
+    s.k0 = __ldg(&a.cu_k[b]);
+    s.kv_len = __ldg(&a.cu_k[b + 1]) - s.k0;
+    s.off = a.qo_offset ? __ldg(&a.qo_offset[b]) : s.kv_len - s.q_len;
+    return s;
+}
+
+// KV tiles (of 128 keys) that query rows [r0, r1) of the segment can see.
+__device__ __forceinline__ int kv_tiles_for(const Seg& s, int r0, int r1, bool causal) {
+    if (r0 >= r1) return 0;
+    long long lim = s.kv_len;
+    if (causal) {
+        const long long c = (long long)s.off + r1;  // keys 0 .. off + r1 - 1
+        lim = c < lim ? c : lim;
+    }
+    if (lim <= 0) return 0;
+    return (int)((lim + 127) / 128);
+}
+
+template <bool ROPE, bool PAGED>
+__global__ void __launch_bounds__(320, 1)
+    prefill_kernel(const __grid_constant__ PrefillArgs a, const __grid_constant__ CUtensorMap map_q,
+                   const __grid_constant__ CUtensorMap map_k, const __grid_constant__ CUtensorMap map_v,
+                   const __grid_constant__ CUtensorMap map_r) {
+    using L = PrefillLayout<ROPE>;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    __shared__ __align__(8) uint64_t bars[P_COUNT];
+    __shared__ uint32_t tmem_base_sh;
+    __shared__ int abort_store;
+    volatile int* abort_sh = &abort_store;
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int b = blockIdx.x % a.batch;
+    const int pair = a.num_q_tiles - 1 - (int)(blockIdx.x / a.batch);  // longest first
+    const int h = blockIdx.y;
+    const int kvh = h / a.group;
+    const Seg sg = load_seg(a, b);
+    const int rA = pair * 256;  // first query row of tile A within the segment
+    if (rA >= sg.q_len) return;  // whole CTA idle (uniform, before any setup)
+    const bool has_b = rA + 128 < sg.q_len;
+    const bool causal = a.causal != 0;
+    const int nA = kv_tiles_for(sg, rA, min(rA + 128, sg.q_len), causal);
+    const int nB = has_b ? kv_tiles_for(sg, rA + 128, min(rA + 256, sg.q_len), causal) : 0;
+    const int nkv = max(nA, nB);
+    const bool zero_tail = nkv > 0 && nkv * 128 > sg.kv_len;  // dead keys in the last tile
+
+    if (threadIdx.x == 0) {
+        mbar_init(&bars[P_QF], 1);
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(&bars[P_KF + i], 1);
+            mbar_init(&bars[P_KE + i], 1);
+            mbar_init(&bars[P_VF + i], 1);
+            mbar_init(&bars[P_VE + i], 1);
+            mbar_init(&bars[P_SF + i], 1);
+            mbar_init(&bars[P_PF + i], 128);
+            mbar_init(&bars[P_OD + i], 1);
+        }
+        mbar_init(&bars[P_VZ], 1);
+        mbar_init(&bars[P_DONE], 1);
+        *abort_sh = 0;
+        fence_barrier_init();
+    }
+    if (warp == 1) {
+        tmem_alloc(&tmem_base_sh, 512);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tbase = tmem_base_sh;
+    // TMEM columns: S_A [0,128) S_B [128,256) O_A [256,384) O_B [384,512)
+    auto s_col = [](int x) { return (uint32_t)(x * 128); };
+    auto o_col = [](int x) { return (uint32_t)(256 + x * 128); };
+
+    if (warp == 0) {
+        // ---------------------------------------------------------------- producer
+        if (lane == 0) {
+            bool ok = true;
+            bool kiss[2] = {false, false}, viss[2] = {false, false};
+            uint32_t kpar[2] = {0, 0}, vpar[2] = {0, 0};
+            const int ntq = has_b ? 2 : 1;
+            mbar_arrive_expect_tx(&bars[P_QF], ntq * L::kQBytes);
+            for (int x = 0; x < ntq; ++x)
+                for (int c = 0; c < L::kQChunks; ++c)
+                    tma_load_3d(sm + L::kQOff + x * L::kQBytes + c * L::kTile, &map_q, &bars[P_QF], c * 64, h,
+                                sg.q0 + rA + x * 128);
+            const int kv_pages = (sg.kv_len + kPage - 1) / kPage;
+            for (int j = 0; j < nkv && ok; ++j) {
+                // page ids of this tile (paged keys)
+                int pid[2] = {-1, -1};
+                if (PAGED) {
+                    for (int i = 0; i < 2; ++i) {
+                        const int p = 2 * j + i;
+                        if (p < kv_pages && p < a.max_pages) {
+                            const int id = __ldg(&a.block_table[(long long)b * a.max_pages + p]);
+                            if ((unsigned)id < (unsigned)a.num_pool_pages) pid[i] = id;
+                            else atomicCAS(a.status, 0, PA_ERR_DEVICE_BOUNDS);
+                        } else if (p < kv_pages) {
+                            atomicCAS(a.status, 0, PA_ERR_DEVICE_BOUNDS);
+                        }
+                    }
+                }
+                const int npid = (pid[0] >= 0) + (pid[1] >= 0);
+                // K tile
+                const int ks = j % L::kNK;
+                if (!mbar_wait(&bars[P_KE + ks], ((j / L::kNK) & 1) ^ 1, abort_sh, a.wait_ns)) {
+                    ok = false;
+                    break;
+                }
+                uint64_t* kf = &bars[P_KF + ks];
+                uint8_t* kt = sm + L::kKOff + ks * L::kKBytes;
+                if (PAGED) {
+                    mbar_arrive_expect_tx(kf, npid * 2 * 8192);
+                    for (int i = 0; i < 2; ++i)
+                        if (pid[i] >= 0)
+                            for (int c = 0; c < 2; ++c)
+                                tma_load_2d(kt + c * L::kTile + i * 8192, &map_k, kf, c * 64,
+                                            (int)(((long long)pid[i] * a.num_kv_heads + kvh) * 64));
+                } else {
+                    mbar_arrive_expect_tx(kf, L::kKBytes);
+                    for (int c = 0; c < 2; ++c)
+                        tma_load_3d(kt + c * L::kTile, &map_k, kf, c * 64, kvh, sg.k0 + j * 128);
+                    if (ROPE) tma_load_2d(kt + 2 * L::kTile, &map_r, kf, 0, sg.k0 + j * 128);
+                }
+                kiss[ks] = true;
+                kpar[ks] = (j / L::kNK) & 1;
+                // V tile
+                const int vs = j % L::kNV;
+                if (!mbar_wait(&bars[P_VE + vs], ((j / L::kNV) & 1) ^ 1, abort_sh, a.wait_ns)) {
+                    ok = false;
+                    break;
+                }
+                uint64_t* vf = &bars[P_VF + vs];
+                uint8_t* vt = sm + L::kVOff + vs * L::kVBytes;
+                if (PAGED) {
+                    mbar_arrive_expect_tx(vf, npid * 2 * 8192);
+                    for (int i = 0; i < 2; ++i)
+                        if (pid[i] >= 0)
+                            for (int c = 0; c < 2; ++c)
+                                tma_load_2d(vt + c * L::kTile + i * 8192, &map_v, vf, c * 64,
+                                            (int)(((long long)pid[i] * a.num_kv_heads + kvh) * 64));
+                } else {
+                    mbar_arrive_expect_tx(vf, L::kVBytes);
+                    for (int c = 0; c < 2; ++c)
+                        tma_load_3d(vt + c * L::kTile, &map_v, vf, c * 64, kvh, sg.k0 + j * 128);
+                }
+                viss[vs] = true;
+                vpar[vs] = (j / L::kNV) & 1;
+            }
+            if (!ok) {
+                *abort_sh = 1;
+                atomicCAS(a.status, 0, PA_ERR_TIMEOUT);
+            }
+            // every issued copy must land before the CTA may exit
+            mbar_wait(&bars[P_QF], 0, nullptr, a.wait_ns);
+            for (int i = 0; i < 2; ++i) {
+                if (kiss[i]) mbar_wait(&bars[P_KF + i], kpar[i], nullptr, a.wait_ns);
+                if (viss[i]) mbar_wait(&bars[P_VF + i], vpar[i], nullptr, a.wait_ns);
+            }
+        }
+        __syncwarp();
+        // dead keys of the last tile: zero their V rows (they may hold anything,
+        // and 0 * NaN would poison the PV product)
+        const bool do_zero = __shfl_sync(0xffffffffu, (int)(zero_tail && !*abort_sh), 0) != 0;
+        if (do_zero) {
+            const int j = nkv - 1, vs = j % L::kNV;
+            bool ok = mbar_wait(&bars[P_VF + vs], (j / L::kNV) & 1, abort_sh, a.wait_ns);
+            ok = __all_sync(0xffffffffu, ok);
+            if (ok) {
+                const int first_dead = sg.kv_len - j * 128;  // 1 .. 127
+                uint8_t* vt = sm + L::kVOff + vs * L::kVBytes;
+                for (int idx = lane; idx < (128 - first_dead) * 16; idx += 32) {
+                    const int row = first_dead + idx / 16, q16 = idx % 16;  // 2 chunks x 8 16-byte pieces
+                    *reinterpret_cast<uint4*>(vt + (q16 >> 3) * L::kTile + row * 128 + (q16 & 7) * 16) =
+                        make_uint4(0, 0, 0, 0);
+                }
+                fence_proxy_async_smem();
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&bars[P_VZ]);
+        }
+    } else if (warp == 1) {
+        // ---------------------------------------------------------------- MMA issuer
+        if (lane == 0) {
+            constexpr uint32_t idesc_qk = idesc_f16(128, 128, true, false, false);
+            constexpr uint32_t idesc_pv = idesc_f16(128, 128, true, false, true);
+            const uint32_t qa = smem_u32(sm + L::kQOff);
+            bool ok = mbar_wait(&bars[P_QF], 0, abort_sh, a.wait_ns);
+            auto qk = [&](int x, int j) {
+                const uint32_t qb = qa + x * L::kQBytes;
+                const uint32_t kb = smem_u32(sm + L::kKOff + (j % L::kNK) * L::kKBytes);
+#pragma unroll
+                for (int kk = 0; kk < L::kDqk / 16; ++kk) {
+                    const int c = kk >> 2, off = (kk & 3) * 32;
+                    mma_ss(tbase + s_col(x), sdesc_sw128(qb + c * L::kTile + off, 16, 1024),
+                           sdesc_sw128(kb + c * L::kTile + off, 16, 1024), idesc_qk, kk > 0);
+                }
+                mma_commit(&bars[P_SF + x]);
+            };
+            auto pv = [&](int x, int j) {
+                const uint32_t vb = smem_u32(sm + L::kVOff + (j % L::kNV) * L::kVBytes);
+#pragma unroll
+                for (int kk = 0; kk < 8; ++kk)
+                    mma_ts(tbase + o_col(x), tbase + s_col(x) + kk * 8, sdesc_sw128(vb + kk * 2048, 16384, 1024),
+                           idesc_pv, (j > 0 || kk > 0) ? 1u : 0u);
+                mma_commit(&bars[P_OD + x]);
+            };
+            const int n[2] = {nA, nB};
+            // prologue: S for tile 0 of both query tiles
+            if (ok && nkv > 0) {
+                ok = mbar_wait(&bars[P_KF], 0, abort_sh, a.wait_ns);
+                if (ok) {
+                    tc_fence_after();
+                    for (int x = 0; x < 2; ++x)
+                        if (n[x] > 0) qk(x, 0);
+                    mma_commit(&bars[P_KE]);
+                }
+            }
+            for (int j = 0; j < nkv && ok; ++j) {
+                const int vs = j % L::kNV;
+                ok = mbar_wait(&bars[P_VF + vs], (j / L::kNV) & 1, abort_sh, a.wait_ns);
+                if (ok && zero_tail && j == nkv - 1) ok = mbar_wait(&bars[P_VZ], 0, abort_sh, a.wait_ns);
+                const bool next_k = j + 1 < nkv;
+                bool k_waited = false;
+                for (int x = 0; x < 2 && ok; ++x) {
+                    if (j >= n[x]) continue;
+                    ok = mbar_wait(&bars[P_PF + x], j & 1, abort_sh, a.wait_ns);
+                    if (!ok) break;
+                    tc_fence_after();
+                    pv(x, j);
+                    if (j + 1 < n[x]) {
+                        // P_x lives in S_x's columns: the next S_x may only be
+                        // written once this PV has read P_x
+                        if (!k_waited) {
+                            ok = mbar_wait(&bars[P_KF + (j + 1) % L::kNK], ((j + 1) / L::kNK) & 1, abort_sh,
+                                           a.wait_ns);
+                            k_waited = true;
+                        }
+                        ok = ok && mbar_wait(&bars[P_OD + x], j & 1, abort_sh, a.wait_ns);
+                        if (!ok) break;
+                        tc_fence_after();
+                        qk(x, j + 1);
+                    }
+                }
+                if (!ok) break;
+                mma_commit(&bars[P_VE + vs]);
+                if (next_k) mma_commit(&bars[P_KE + (j + 1) % L::kNK]);
+            }
+            if (!ok) {
+                *abort_sh = 1;
+                atomicCAS(a.status, 0, PA_ERR_TIMEOUT);
+            }
+            mma_commit(&bars[P_DONE]);
+            mbar_wait(&bars[P_DONE], 0, nullptr, a.wait_ns);
+        }
+    } else {
+        // ---------------------------------------------------------------- softmax (A: warps 2-5, B: 6-9)
+        const int x = warp >= 6 ? 1 : 0;
+        const int q4 = warp & 3;
+        const int row = q4 * 32 + lane;           // query row within the tile = TMEM lane
+        const int i = rA + x * 128 + row;         // query row within the segment
+        const int nx = x ? nB : nA;
+        const bool active = x == 0 || has_b;
+        const uint32_t lane_addr = (uint32_t)(q4 * 32) << 16;
+        const float sl2 = a.scale_log2;
+        // keys this row may see: [0, lim)
+        long long lim = sg.kv_len;
+        if (causal) lim = min(lim, (long long)sg.off + i + 1);
+        if (lim < 0) lim = 0;
+        float m_run = -INFINITY, l_run = 0.f;
+        bool ok = true;
+        for (int j = 0; active && j < nx; ++j) {
+            ok = mbar_wait(&bars[P_SF + x], j & 1, abort_sh, a.wait_ns);
+            ok = __all_sync(0xffffffffu, ok);
+            if (!ok) break;
+            tc_fence_after();
+            const int vis = (int)min(128LL, max(0LL, lim - (long long)j * 128));  // visible keys of this tile
+            // pass 1: row max of the scaled, masked scores (S read from TMEM in 32-column chunks)
+            float mt = -INFINITY;
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+                uint32_t r[32];
+                tmem_ld_x32(tbase + lane_addr + s_col(x) + c * 32, r);
+                tmem_ld_wait();
+                reg_fence(r);
+#pragma unroll
+                for (int k = 0; k < 32; ++k)
+                    if (c * 32 + k < vis) mt = fmaxf(mt, __uint_as_float(r[k]) * sl2);
+            }
+            // conditional rescale: keep the stale max unless the new one is 2^8 larger
+            const bool grow = mt > m_run + kRescaleThreshold;
+            float m_new = grow ? mt : m_run;
+            const bool need_o = __any_sync(0xffffffffu, grow && j > 0 && m_run != -INFINITY);
+            if (need_o) {
+                ok = mbar_wait(&bars[P_OD + x], (j - 1) & 1, abort_sh, a.wait_ns);
+                ok = __all_sync(0xffffffffu, ok);
+                if (!ok) break;
+                tc_fence_after();
+                const float alpha = (grow && m_run != -INFINITY) ? ex2(m_run - m_new) : 1.f;
+#pragma unroll
+                for (int c = 0; c < 4; ++c) {
+                    uint32_t o[32];
+                    tmem_ld_x32(tbase + lane_addr + o_col(x) + c * 32, o);
+                    tmem_ld_wait();
+                    reg_fence(o);
+#pragma unroll
+                    for (int k = 0; k < 32; ++k) o[k] = __float_as_uint(__uint_as_float(o[k]) * alpha);
+                    tmem_st_x32(tbase + lane_addr + o_col(x) + c * 32, o);
+                }
+                tmem_st_wait();
+            }
+            if (grow) {
+                if (m_run != -INFINITY) l_run *= ex2(m_run - m_new);
+                m_run = m_new;
+            }
+            const bool none = m_run == -INFINITY;
+            float rs = 0.f;
+            // pass 2: P = exp2(x - m) in bf16, written over S columns already read
+            // (keys 32c..32c+31 -> P columns 16c..16c+15)
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+                uint32_t r[32], pw[16];
+                tmem_ld_x32(tbase + lane_addr + s_col(x) + c * 32, r);
+                tmem_ld_wait();
+                reg_fence(r);
+#pragma unroll
+                for (int k = 0; k < 16; ++k) {
+                    const int key = c * 32 + 2 * k;
+                    const float p0 = (none || key >= vis) ? 0.f : ex2(__uint_as_float(r[2 * k]) * sl2 - m_run);
+                    const float p1 = (none || key + 1 >= vis) ? 0.f : ex2(__uint_as_float(r[2 * k + 1]) * sl2 - m_run);
+                    rs += p0 + p1;
+                    const __nv_bfloat162 pk = __floats2bfloat162_rn(p0, p1);
+                    pw[k] = *reinterpret_cast<const uint32_t*>(&pk);
+                }
+                tmem_st_x16(tbase + lane_addr + s_col(x) + c * 16, pw);
+            }
+            l_run += rs;
+            tmem_st_wait();
+            tc_fence_before();
+            mbar_arrive(&bars[P_PF + x]);
+        }
+        // ---- epilogue
+        if (active && ok) {
+            const bool write = i < sg.q_len;
+            const long long orow = ((long long)(sg.q0 + i) * a.num_q_heads + h);
+            if (nx > 0) {
+                ok = mbar_wait(&bars[P_OD + x], (nx - 1) & 1, abort_sh, a.wait_ns);
+                ok = __all_sync(0xffffffffu, ok);
+            }
+            if (ok) {
+                tc_fence_after();
+                const float inv = l_run > 0.f ? 1.f / l_run : 0.f;
+                uint16_t* dst = a.out + orow * 128;
+#pragma unroll
+                for (int c = 0; c < 4; ++c) {
+                    uint32_t o[32];
+                    if (nx > 0) {
+                        tmem_ld_x32(tbase + lane_addr + o_col(x) + c * 32, o);
+                        tmem_ld_wait();
+                        reg_fence(o);
+                    } else {
+#pragma unroll
+                        for (int k = 0; k < 32; ++k) o[k] = 0u;
+                    }
+                    if (write) {
+                        uint32_t w[16];
+#pragma unroll
+                        for (int k = 0; k < 16; ++k) {
+                            const __nv_bfloat162 pk = __floats2bfloat162_rn(__uint_as_float(o[2 * k]) * inv,
+                                                                            __uint_as_float(o[2 * k + 1]) * inv);
+                            w[k] = *reinterpret_cast<const uint32_t*>(&pk);
+                        }
+                        uint4* d4 = reinterpret_cast<uint4*>(dst + c * 32);
+#pragma unroll
+                        for (int k = 0; k < 4; ++k) d4[k] = make_uint4(w[4 * k], w[4 * k + 1], w[4 * k + 2], w[4 * k + 3]);
+                    }
+                }
+                if (write && a.lse)
+                    a.lse[orow] = l_run > 0.f ? (m_run + __log2f(l_run)) * kLn2f : -INFINITY;
+            }
+        }
+        if (!ok) {
+            *abort_sh = 1;
+            atomicCAS(a.status, 0, PA_ERR_TIMEOUT);
+        }
+        tc_fence_before();
+    }
+
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tbase, 512);
+    }
+}
+
+template <bool ROPE, bool PAGED>
+cudaError_t launch_t(const PrefillArgs& a, const CUtensorMap* mq, const CUtensorMap* mk, const CUtensorMap* mv,
+                     const CUtensorMap* mr, cudaStream_t stream) {
+    using L = PrefillLayout<ROPE>;
+    static bool configured = false;
+    if (!configured) {
+        cudaError_t e =
+            cudaFuncSetAttribute(prefill_kernel<ROPE, PAGED>, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kSmem);
+        if (e != cudaSuccess) return e;
+        configured = true;
+    }
+    dim3 grid(a.num_q_tiles * a.batch, a.num_q_heads);
+    prefill_kernel<ROPE, PAGED><<<grid, L::kThreads, L::kSmem, stream>>>(a, *mq, *mk, *mv, *mr);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_prefill(const PrefillArgs& a, int head_dim_qk, const CUtensorMap* mq, const CUtensorMap* mk,
+                           const CUtensorMap* mv, const CUtensorMap* mr, cudaStream_t stream) {
+    if (head_dim_qk == 192) return launch_t<true, false>(a, mq, mk, mv, mr, stream);
+    return a.paged ? launch_t<false, true>(a, mq, mk, mv, mr, stream) : launch_t<false, false>(a, mq, mk, mv, mr, stream);
+}
+
+}  // namespace pa

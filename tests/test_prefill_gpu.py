@@ -1,0 +1,176 @@
+"""Prefill parity on the GPU: libpa's pa_prefill (through the C ABI) against
+the fp64 oracle on the same seeded inputs -- chunked causal prefill against the
+paged cache, ragged prefill, and the MLA shape with the shared rope key.
+Tolerances: out max-abs 1e-2 and mean-abs 1e-3, lse abs 1e-3."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from paged_kv_attention_fwd_gb300 import binding as B
+from paged_kv_attention_fwd_gb300 import ops
+from paged_kv_attention_fwd_gb300 import workloads as W
+from paged_kv_attention_fwd_gb300.build import build
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def gpu():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    build()
+
+
+def run(inp: W.PrefillInputs, causal=True):
+    dev = "cuda"
+    q = ops.as_bf16(inp.q, dev)
+    k = ops.as_bf16(inp.k, dev)
+    v = ops.as_bf16(inp.v, dev)
+    kr = ops.as_bf16(inp.k_rope, dev) if inp.k_rope is not None else None
+    cq = torch.from_numpy(inp.cu_seqlens_q).to(dev)
+    ck = torch.from_numpy(inp.cu_seqlens_k).to(dev)
+    bt = torch.from_numpy(inp.block_table).to(dev) if inp.paged else None
+    qo = torch.from_numpy(inp.qo_offset).to(dev) if inp.qo_offset is not None else None
+    kv_total = int(inp.cu_seqlens_k[-1])
+    sh = ops.prefill_shapes(inp.batch, inp.num_q_heads, inp.num_kv_heads, inp.head_dim_qk, inp.head_dim_v,
+                            inp.rope_dim, inp.max_seqlen_q, int(inp.cu_seqlens_q[-1]), kv_total,
+                            max_pages=inp.block_table.shape[1] if inp.paged else 0,
+                            num_pool_pages=inp.k.shape[0] if inp.paged else 0)
+    out, lse, ws = ops.prefill(sh, q, k, v, cq, ck, inp.scale, causal, block_table=bt, k_rope=kr, qo_offset=qo)
+    st = B.pa_check_status(ws)
+    return out.float().cpu().numpy(), lse.cpu().numpy(), st
+
+
+def reference(inp: W.PrefillInputs, causal=True, rows=None):
+    return oracle.prefill(inp.q, inp.k, inp.v, inp.cu_seqlens_q, inp.cu_seqlens_k, inp.scale, causal,
+                          block_table=inp.block_table, k_rope=inp.k_rope, qo_offset=inp.qo_offset, rows=rows)
+
+
+def assert_close(out, lse, ref_out, ref_lse, max_tol=1e-2, mean_tol=1e-3):
+    assert np.all(np.isfinite(out))
+    err = np.abs(out - ref_out)
+    assert err.max() <= max_tol, f"max abs err {err.max():.3g}"
+    assert err.mean() <= mean_tol, f"mean abs err {err.mean():.3g}"
+    neg = np.isneginf(ref_lse)
+    assert np.array_equal(np.isneginf(lse), neg)
+    if (~neg).any():
+        le = np.abs(lse[~neg] - ref_lse[~neg])
+        assert le.max() <= 1e-3, f"lse err {le.max():.3g}"
+
+
+def sample_rows(inp, per_seq=48, heads=None, seed=0):
+    """Query rows across every segment: tile edges, ends and random positions."""
+    rng = np.random.default_rng(seed)
+    hq = inp.num_q_heads
+    heads = heads if heads is not None else sorted({0, hq - 1, hq // 2, int(rng.integers(hq))})
+    rows = []
+    for b in range(inp.batch):
+        a, e = int(inp.cu_seqlens_q[b]), int(inp.cu_seqlens_q[b + 1])
+        n = e - a
+        pos = {0, n - 1, min(127, n - 1), min(128, n - 1), min(255, n - 1), min(256, n - 1)}
+        pos |= set(rng.integers(0, n, size=per_seq).tolist())
+        for p in sorted(pos):
+            for h in heads:
+                rows.append((a + p) * hq + h)
+    return np.array(rows, np.int64)
+
+
+@pytest.mark.parametrize("hq,hk", [(4, 4), (8, 2)])
+def test_paged_chunked_prefill(hq, hk):
+    inp = W.make_paged_prefill([5, 130, 300, 1], [5, 200, 1300, 64], hq, hk, 128, seed=hq + hk, extra_pages=3)
+    out, lse, st = run(inp)
+    assert st == B.PA_OK
+    ro, rl = reference(inp)
+    assert_close(out, lse, ro, rl)
+
+
+def test_paged_prefill_poisoned_tail_rows_and_pages():
+    inp = W.make_paged_prefill([70, 129], [100, 200], 4, 4, 128, seed=31, extra_pages=4)
+    clean = run(inp)
+    # poison: rows past kv_len in each last page and every unreferenced page
+    k, v = inp.k.copy(), inp.v.copy()
+    live = np.zeros((k.shape[0], 64), bool)
+    for b in range(inp.batch):
+        n = int(inp.cu_seqlens_k[b + 1] - inp.cu_seqlens_k[b])
+        for j in range((n + 63) // 64):
+            live[inp.block_table[b, j], : min(64, n - 64 * j)] = True
+    mask = np.broadcast_to(~live[:, None, :, None], k.shape)
+    k[mask] = 0x7FC0
+    v[mask] = 0x7FC0
+    p = W.PrefillInputs(**{**inp.__dict__})
+    p.k, p.v = k, v
+    dirty = run(p)
+    assert dirty[2] == B.PA_OK
+    assert np.all(np.isfinite(dirty[0]))
+    assert np.array_equal(clean[0], dirty[0]) and np.array_equal(clean[1], dirty[1])
+
+
+@pytest.mark.parametrize("causal", [True, False])
+def test_ragged_prefill(causal):
+    lens = [1, 127, 128, 129, 255, 256, 257, 600]
+    inp = W.make_ragged_prefill(lens, 4, 128, 128, seed=5, num_kv_heads=2)
+    out, lse, st = run(inp, causal)
+    assert st == B.PA_OK
+    ro, rl = reference(inp, causal)
+    assert_close(out, lse, ro, rl)
+
+
+def test_ragged_prefill_explicit_offsets():
+    # q shorter than kv; offsets: default-like, zero, negative (rows with no key), past the end
+    inp = W.make_ragged_prefill([40, 200, 130, 10], 4, 128, 128, seed=6, kv_lens=[300, 260, 500, 20],
+                                qo_offset=[260, 0, -50, 1000])
+    out, lse, st = run(inp)
+    assert st == B.PA_OK
+    ro, rl = reference(inp)
+    assert np.isneginf(rl).any()  # the negative offset leaves early rows without keys
+    assert_close(out, lse, ro, rl)
+    assert np.all(out[np.isneginf(rl)] == 0)
+
+
+def test_mla_ragged_prefill():
+    inp = W.make_ragged_prefill([50, 300, 513, 128], 8, 192, 128, rope_dim=64, seed=7)
+    out, lse, st = run(inp)
+    assert st == B.PA_OK
+    ro, rl = reference(inp)
+    assert_close(out, lse, ro, rl)
+
+
+def test_chunked_prefill_full_size_sampled():
+    inp = W.chunked_prefill(0)
+    out, lse, st = run(inp)
+    assert st == B.PA_OK
+    rows = sample_rows(inp, per_seq=40)
+    ro, rl = reference(inp, rows=rows)
+    hq, dv = inp.num_q_heads, inp.head_dim_v
+    assert_close(out.reshape(-1, dv)[rows], lse.reshape(-1)[rows], ro, rl)
+    assert np.all(np.isfinite(out))
+
+
+def test_mla_prefill_full_size_sampled():
+    inp = W.mla_prefill(0)
+    out, lse, st = run(inp)
+    assert st == B.PA_OK
+    rows = sample_rows(inp, per_seq=24)
+    ro, rl = reference(inp, rows=rows)
+    assert_close(out.reshape(-1, 128)[rows], lse.reshape(-1)[rows], ro, rl)
+    assert np.all(np.isfinite(out))
+
+
+def test_prefill_deterministic():
+    inp = W.make_ragged_prefill([300, 77], 4, 128, 128, seed=8)
+    a = run(inp)
+    b = run(inp)
+    assert np.array_equal(a[0], b[0]) and np.array_equal(a[1], b[1])
+
+
+def test_prefill_equals_decode_for_single_query_rows():
+    """Decode is prefill with one query row per sequence (offset kv_len - 1)."""
+    lens = [1, 64, 200, 1000]
+    d = W.make_decode(4, 8, 8, 128, lens, seed=9)
+    p = W.PrefillInputs(q=d.q, k=d.k_pool, v=d.v_pool, cu_seqlens_q=W.cu_seqlens(np.ones(4, np.int32)),
+                        cu_seqlens_k=W.cu_seqlens(d.seq_lens), scale=d.scale, causal=True, block_table=d.block_table)
+    out, lse, st = run(p)
+    assert st == B.PA_OK
+    ro, rl = oracle.decode(d.q, d.k_pool, d.v_pool, d.block_table, d.seq_lens, d.scale)
+    assert_close(out, lse, ro, rl)
