@@ -176,6 +176,39 @@ def kv_bytes(inp):
     return full, exact
 
 
+def prefill_workload(name):
+    from paged_kv_attention_fwd_gb300 import workloads as W
+    if name == "prefill_paged":
+        inp = W.chunked_prefill(0)
+        desc = ("chunked causal prefill against the paged cache: B=8, H=32 (Hq=Hk), D=128, page 64, q_len 512 "
+                "after a cached prefix U[0,8192], qo_offset = kv_len - q_len, seed 0")
+    elif name == "prefill_mla":
+        inp = W.mla_prefill(0)
+        desc = ("MLA ragged causal prefill: 8 sequences L~U[512,4096], H=128, q 192 = 128 nope + 64 rope, "
+                "k_rope [T,1,64] shared by all heads, v/out 128, scale 1/sqrt(192), seed 0")
+    else:
+        raise ValueError(name)
+    return inp, desc
+
+
+def visible_pairs(inp, causal=True):
+    """Per query row, the number of keys it attends (the algorithmic unit)."""
+    out = []
+    for b in range(inp.batch):
+        ql = int(inp.cu_seqlens_q[b + 1] - inp.cu_seqlens_q[b])
+        kl = int(inp.cu_seqlens_k[b + 1] - inp.cu_seqlens_k[b])
+        off = int(inp.qo_offset[b]) if inp.qo_offset is not None else kl - ql
+        i = np.arange(ql, dtype=np.int64)
+        out.append(np.clip(np.minimum(kl, off + i + 1) if causal else np.full(ql, kl), 0, kl))
+    return np.concatenate(out)
+
+
+def prefill_flops(inp, causal=True):
+    """2 flops per multiply-add in QK^T (depth Dqk) and PV (depth Dv), per visible (row, key, head)."""
+    pairs = int(visible_pairs(inp, causal).sum())
+    return pairs * inp.num_q_heads * (2 * inp.head_dim_qk + 2 * inp.head_dim_v)
+
+
 # ------------------------------------------------------------------ reference arm (the oracle)
 
 def cpu_oracle_decode_sample(inp, budget_s=None, steps=None, warmup=0):
@@ -207,14 +240,59 @@ def cpu_oracle_decode_sample(inp, budget_s=None, steps=None, warmup=0):
     return nbytes / el / 1e9, el, done, nbytes
 
 
+def cpu_oracle_prefill_sample(inp, budget_s=None, steps=None, warmup=0, rows_per_step=64, seed=0):
+    """Time the fp64 oracle on random query rows (token, head) of the workload.
+    Returns (TFLOP/s, seconds, rows done, flops)."""
+    import oracle
+    rng = np.random.default_rng(seed)
+    pairs = visible_pairs(inp)
+    hq = inp.num_q_heads
+    per_pair = 2 * inp.head_dim_qk + 2 * inp.head_dim_v
+    total_rows = pairs.size * hq
+
+    def one():
+        rows = rng.integers(0, total_rows, size=rows_per_step).astype(np.int64)
+        oracle.prefill(inp.q, inp.k, inp.v, inp.cu_seqlens_q, inp.cu_seqlens_k, inp.scale, True,
+                       block_table=inp.block_table, k_rope=inp.k_rope, qo_offset=inp.qo_offset, rows=rows)
+        return int(pairs[rows // hq].sum()) * per_pair
+
+    for _ in range(warmup):
+        one()
+    done, flops = 0, 0
+    t0 = time.perf_counter()
+    while True:
+        flops += one()
+        done += 1
+        el = time.perf_counter() - t0
+        if steps is not None and done >= steps:
+            break
+        if budget_s is not None and el >= budget_s:
+            break
+    return flops / el / 1e12, el, done * rows_per_step, flops
+
+
 def run_reference(args):
     rank = int(os.environ.get("RANK", "0"))
     if rank != 0:
         return
     import oracle
+    cores = oracle.num_threads()
+    if args.workload.startswith("prefill"):
+        inp, desc = prefill_workload(args.workload)
+        tfs, el, rows, flops = cpu_oracle_prefill_sample(inp, steps=args.steps, warmup=args.warmup, rows_per_step=8)
+        line = {
+            "impl": "reference", "metric": METRIC, "value": round(tfs, 6), "unit": "TFLOP/s", "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(el / args.steps * 1e3, 4),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": desc, "implementation": "fp64 CPU oracle (oracle/oracle.c), OpenMP"},
+            "cpu_baseline": {"value": round(tfs, 6), "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
+                             "sample": f"{rows} random (token, head) query rows, 8 per step"},
+            "e2e": {"value": round(tfs, 6), "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        }
+        print(json.dumps(line), flush=True)
+        return
     inp, desc = decode_workload(args.workload)
     gbs, el, done, nbytes = cpu_oracle_decode_sample(inp, steps=args.steps, warmup=args.warmup)
-    cores = oracle.num_threads()
     sample = f"{done} single-sequence decode steps cycling the batch ({nbytes / 1e9:.3f} GB of K+V pages)"
     line = {
         "impl": "reference", "metric": METRIC, "value": round(gbs, 4), "unit": "GB/s", "n_gpus": args.gpus,
@@ -401,6 +479,155 @@ def decode_e2e(inp, dev, stream, sh, full_bytes, world, dist, args):
             "includes": "host schedule + pinned H2D of all inputs + pa_decode + D2H of out/lse + sync"}
 
 
+def prefill_device(inp, dev):
+    import torch
+    from paged_kv_attention_fwd_gb300 import ops
+    d = {"q": ops.as_bf16(inp.q, dev), "k": ops.as_bf16(inp.k, dev), "v": ops.as_bf16(inp.v, dev),
+         "cq": torch.from_numpy(inp.cu_seqlens_q).to(dev), "ck": torch.from_numpy(inp.cu_seqlens_k).to(dev)}
+    d["kr"] = ops.as_bf16(inp.k_rope, dev) if inp.k_rope is not None else None
+    d["bt"] = torch.from_numpy(inp.block_table).to(dev) if inp.paged else None
+    sh = ops.prefill_shapes(inp.batch, inp.num_q_heads, inp.num_kv_heads, inp.head_dim_qk, inp.head_dim_v,
+                            inp.rope_dim, inp.max_seqlen_q, int(inp.cu_seqlens_q[-1]), int(inp.cu_seqlens_k[-1]),
+                            max_pages=inp.block_table.shape[1] if inp.paged else 0,
+                            num_pool_pages=inp.k.shape[0] if inp.paged else 0, device=dev)
+    return d, sh
+
+
+def run_prefill(args, rank, world, local_rank, dist):
+    import torch
+    from paged_kv_attention_fwd_gb300 import binding as B
+
+    dev = torch.device("cuda", local_rank)
+    torch.cuda.set_device(dev)
+    inp, desc = prefill_workload(args.workload)
+    flops = prefill_flops(inp)
+    d, sh = prefill_device(inp, dev)
+    tq = int(inp.cu_seqlens_q[-1])
+    out = torch.empty((tq, inp.num_q_heads, inp.head_dim_v), dtype=torch.bfloat16, device=dev)
+    lse = torch.empty((tq, inp.num_q_heads), dtype=torch.float32, device=dev)
+    ws = torch.zeros(B.pa_prefill_workspace_size(sh), dtype=torch.uint8, device=dev)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step():
+        B.pa_prefill(sh, d["q"], d["k"], d["v"], d["kr"], d["cq"], d["ck"], d["bt"], None, True, inp.scale, out,
+                     lse, ws, stream=stream)
+
+    for _ in range(args.warmup):
+        flush.zero_()
+        step()
+    torch.cuda.synchronize(dev)
+    if B.pa_check_status(ws, stream) != B.PA_OK:
+        raise RuntimeError(B.pa_last_error())
+    K = args.steps
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(K)]
+    if dist is not None:
+        dist.barrier()
+    torch.cuda.synchronize(dev)
+    with ClockSampler(gpu_index(local_rank)) as clk:
+        for i in range(K):
+            flush.zero_()
+            ev[i][0].record(stream)
+            step()
+            ev[i][1].record(stream)
+        torch.cuda.synchronize(dev)
+    if dist is not None:
+        dist.barrier()
+    ms = sum(ev[i][0].elapsed_time(ev[i][1]) for i in range(K)) / K
+    if dist is not None:
+        t = torch.tensor([ms], dtype=torch.float64, device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t[0])
+    if B.pa_check_status(ws, stream) != B.PA_OK:
+        raise RuntimeError(B.pa_last_error())
+    clocks = clk.summary()
+    pk, pk_src = peaks()
+    tfs = flops / (ms * 1e-3) / 1e12
+    peak = pk["bf16_tflops"]
+    prof = "prefill_kernel_" + args.workload + ".md"
+    roofline = {"bound": "tensor", "achieved": round(tfs, 2), "peak": peak, "unit": "TFLOP/s",
+                "frac": round(tfs / peak, 4),
+                "traffic": profiled_traffic(prof, ["prefill.cu", "pa_ptx.cuh", "pa_internal.h"]),
+                "kernel": "prefill_kernel", "peak_source": f"{pk_src} (cuBLAS bf16 GEMM, burst)",
+                "algorithmic_flops_per_launch": flops, "kernel_ms": round(ms, 5)}
+    e2e = None
+    if not args.no_e2e:
+        e2e = prefill_e2e(inp, dev, stream, sh, flops, world, dist, args)
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        import oracle
+        ctf, el, rows, cfl = cpu_oracle_prefill_sample(inp, budget_s=args.cpu_seconds)
+        cpu = {"value": round(ctf, 6), "unit": "TFLOP/s", "cores": oracle.num_threads(), "kind": "oracle",
+               "sample": f"{rows} random (token, head) query rows of this workload through the fp64 oracle "
+                         f"({cfl / 1e9:.2f} GFLOP, {el:.1f} s)"}
+    line = {
+        "metric": METRIC, "value": round(world * tfs, 2), "unit": "TFLOP/s", "n_gpus": world, "steps": K,
+        "warmup": args.warmup, "ms_per_step": round(ms, 5), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": desc, "total_q": tq, "num_q_heads": inp.num_q_heads,
+                   "head_dim_qk": inp.head_dim_qk, "head_dim_v": inp.head_dim_v, "flops_per_step": flops,
+                   "pct_tc_peak": round(100 * tfs / peak, 2),
+                   "l2": f"flushed between steps ({L2_FLUSH_BYTES >> 20} MiB write, outside the events)",
+                   "parallelism": f"replicas x{world}"},
+        "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
+        "gpu_launches": K * (2 if B.pa_prefill_workspace_size(sh) > B.PA_STATUS_BYTES else 1), "clocks": clocks,
+    }
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
+def prefill_e2e(inp, dev, stream, sh, flops, world, dist, args):
+    """End to end through pa_prefill with host buffers: copy q, k, v (and rope
+    key, offsets, block table) from pinned memory, run, read out + lse back."""
+    import torch
+    from paged_kv_attention_fwd_gb300 import binding as B
+
+    def pinned(a):
+        return torch.from_numpy(np.ascontiguousarray(a)).pin_memory()
+
+    h = {"q": pinned(inp.q.view(np.int16)), "k": pinned(inp.k.view(np.int16)), "v": pinned(inp.v.view(np.int16)),
+         "cq": pinned(inp.cu_seqlens_q), "ck": pinned(inp.cu_seqlens_k)}
+    if inp.k_rope is not None:
+        h["kr"] = pinned(inp.k_rope.view(np.int16))
+    if inp.paged:
+        h["bt"] = pinned(inp.block_table)
+    d = {k: torch.empty_like(v, device=dev) for k, v in h.items()}
+    tq = int(inp.cu_seqlens_q[-1])
+    out_h = torch.empty((tq, inp.num_q_heads, inp.head_dim_v), dtype=torch.int16).pin_memory()
+    lse_h = torch.empty((tq, inp.num_q_heads), dtype=torch.float32).pin_memory()
+    out_d = torch.empty_like(out_h, device=dev)
+    lse_d = torch.empty_like(lse_h, device=dev)
+    ws = torch.zeros(B.pa_prefill_workspace_size(sh), dtype=torch.uint8, device=dev)
+
+    def step():
+        for k in h:
+            d[k].copy_(h[k], non_blocking=True)
+        B.pa_prefill(sh, d["q"], d["k"], d["v"], d.get("kr"), d["cq"], d["ck"], d.get("bt"), None, True,
+                     inp.scale, out_d, lse_d, ws, stream=stream)
+        out_h.copy_(out_d, non_blocking=True)
+        lse_h.copy_(lse_d, non_blocking=True)
+        torch.cuda.synchronize(dev)
+
+    for _ in range(3):
+        step()
+    E = max(3, min(args.steps, args.e2e_steps))
+    if dist is not None:
+        dist.barrier()
+    t0 = time.perf_counter()
+    for _ in range(E):
+        step()
+    el = time.perf_counter() - t0
+    if dist is not None:
+        t = torch.tensor([el], dtype=torch.float64, device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        el = float(t[0])
+    h2d = sum(v.numel() * v.element_size() for v in h.values())
+    d2h = out_h.numel() * 2 + lse_h.numel() * 4
+    return {"value": round(world * flops * E / el / 1e12, 3), "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
+            "d2h_bytes_per_step": d2h, "steps": E, "ms_per_step": round(el / E * 1e3, 4),
+            "includes": "pinned H2D of q, k, v, offsets (+ rope key / block table) + pa_prefill + D2H of out/lse + sync"}
+
+
 # ------------------------------------------------------------------ main
 
 def main():
@@ -409,7 +636,8 @@ def main():
     ap.add_argument("--steps", type=int, default=5000)
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--workload", default="decode_gqa", choices=["decode_gqa", "decode_fp8", "decode_tiny"])
+    ap.add_argument("--workload", default="decode_gqa",
+                    choices=["decode_gqa", "decode_fp8", "decode_tiny", "prefill_paged", "prefill_mla"])
     ap.add_argument("--e2e-steps", type=int, default=20)
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--no-e2e", action="store_true")
@@ -437,7 +665,10 @@ def main():
         build()
     if dist is not None:
         dist.barrier()
-    run_decode(args, rank, world, local_rank, dist)
+    if args.workload.startswith("prefill"):
+        run_prefill(args, rank, world, local_rank, dist)
+    else:
+        run_decode(args, rank, world, local_rank, dist)
     if dist is not None:
         dist.destroy_process_group()
 

@@ -234,12 +234,20 @@ typedef struct {
  *                i of segment b sees key j iff j <= qo_offset[b] + i (MATE
  *                _normalize_qo_offset / _resolve_seqused_k)
  *   out          bf16 [total_q, Hq, head_dim_v];  lse fp32 [total_q, Hq] or NULL
- *   workspace    >= PA_STATUS_BYTES device bytes (status word), zero-filled once
+ *   workspace    >= PA_STATUS_BYTES device bytes (status word), zero-filled once.
+ *                With pa_prefill_workspace_size(shapes) bytes the call also
+ *                orders its CTAs longest first (a small sorting kernel writes
+ *                the order after the status word); with less it uses a fixed
+ *                order.  Results are identical either way.
  */
 pa_status pa_prefill(const pa_prefill_shapes* shapes, const void* q, const void* k, const void* v,
                      const void* k_rope, const int32_t* cu_seqlens_q, const int32_t* cu_seqlens_k,
                      const int32_t* block_table, const int32_t* qo_offset, int causal, float scale,
                      void* out, float* lse, void* workspace, size_t workspace_bytes, cudaStream_t stream);
+
+/* Workspace bytes with which pa_prefill also orders its work longest first:
+ * PA_STATUS_BYTES + 4 * batch * ceil(max_seqlen_q / 256). */
+size_t pa_prefill_workspace_size(const pa_prefill_shapes* shapes);
 
 /* ----------------------------------------------------------------- status */
 

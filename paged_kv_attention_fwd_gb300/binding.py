@@ -75,6 +75,8 @@ def lib() -> ctypes.CDLL:
         L.pa_decode_noalloc.restype = ctypes.c_int
         L.pa_prefill.argtypes = [ctypes.POINTER(pa_prefill_shapes), _P, _P, _P, _P, _P, _P, _P, _P, ctypes.c_int,
                                  f32, _P, _P, _P, sz, _P]
+        L.pa_prefill_workspace_size.argtypes = [ctypes.POINTER(pa_prefill_shapes)]
+        L.pa_prefill_workspace_size.restype = ctypes.c_size_t
         L.pa_check_status.argtypes = [_P, _P]
         L.pa_last_error.restype = ctypes.c_char_p
         L.pa_set_wait_limit_ns.argtypes = [u64]
@@ -91,7 +93,7 @@ def declared_symbols() -> list:
     """Every function the public header declares."""
     with open(HEADER) as f:
         text = f.read()
-    return sorted(set(re.findall(r"^\s*(?:pa_status|const char\*|int32_t)\s+(pa_\w+)\s*\(", text, re.M)))
+    return sorted(set(re.findall(r"^\s*(?:pa_status|const char\*|int32_t|size_t)\s+(pa_\w+)\s*\(", text, re.M)))
 
 
 def _check(st: int) -> None:
@@ -187,6 +189,10 @@ def pa_prefill(shapes: pa_prefill_shapes, q, k, v, k_rope, cu_seqlens_q, cu_seql
                             _ptr(cu_seqlens_k), _ptr(block_table), _ptr(qo_offset), int(bool(causal)),
                             float(scale), _ptr(out), _ptr(lse), _ptr(workspace), int(workspace_bytes),
                             _stream(stream)))
+
+
+def pa_prefill_workspace_size(shapes: pa_prefill_shapes) -> int:
+    return int(lib().pa_prefill_workspace_size(ctypes.byref(shapes)))
 
 
 def pa_check_status(workspace, stream=None) -> int:

@@ -135,55 +135,48 @@ __device__ __forceinline__ Item load_item(const DecodeArgs& a, int idx, int item
 
 __device__ __forceinline__ int item_tiles(const Item& it) { return (it.p1 - it.p0 + 1) >> 1; }
 
-// All-reduce 16 per-thread values over a warp by transposition: 16 shuffles
-// instead of 80.  Returns the reduction of head head_of_lane(lane), which is
-// held by lanes 2h' and 2h'+1.
-template <bool kMax>
-__device__ __forceinline__ float warp_xreduce16(const float (&x)[16], int lane) {
-    float v[16];
+// All-reduce NP per-thread values over a warp by transposition: each
+// shuffle level exchanges half of the remaining values, so NP = 16 costs 16
+// shuffles instead of 80.  Returns the reduction of value head_of_lane<NP>(lane).
+template <int NP, bool kMax>
+__device__ __forceinline__ float warp_xreduce(const float (&x)[NP], int lane) {
+    float v[NP];
 #pragma unroll
-    for (int i = 0; i < 16; ++i) v[i] = x[i];
-#define PA_OP(a, b) (kMax ? fmaxf((a), (b)) : ((a) + (b)))
-    {
-        const bool up = lane & 16;
+    for (int i = 0; i < NP; ++i) v[i] = x[i];
 #pragma unroll
-        for (int i = 0; i < 8; ++i) {
-            const float send = up ? v[i] : v[i + 8];
-            const float keep = up ? v[i + 8] : v[i];
-            v[i] = PA_OP(keep, __shfl_xor_sync(0xffffffffu, send, 16));
+    for (int cnt = NP, off = 16; cnt > 1; cnt >>= 1, off >>= 1) {
+        const bool up = lane & off;
+#pragma unroll
+        for (int i = 0; i < cnt / 2; ++i) {
+            const float send = up ? v[i] : v[i + cnt / 2];
+            const float keep = up ? v[i + cnt / 2] : v[i];
+            const float got = __shfl_xor_sync(0xffffffffu, send, off);
+            v[i] = kMax ? fmaxf(keep, got) : keep + got;
         }
     }
-    {
-        const bool up = lane & 8;
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            const float send = up ? v[i] : v[i + 4];
-            const float keep = up ? v[i + 4] : v[i];
-            v[i] = PA_OP(keep, __shfl_xor_sync(0xffffffffu, send, 8));
-        }
+    for (int off = 16 / NP; off >= 1; off >>= 1) {
+        const float got = __shfl_xor_sync(0xffffffffu, v[0], off);
+        v[0] = kMax ? fmaxf(v[0], got) : v[0] + got;
     }
-    {
-        const bool up = lane & 4;
-#pragma unroll
-        for (int i = 0; i < 2; ++i) {
-            const float send = up ? v[i] : v[i + 2];
-            const float keep = up ? v[i + 2] : v[i];
-            v[i] = PA_OP(keep, __shfl_xor_sync(0xffffffffu, send, 4));
-        }
-    }
-    {
-        const bool up = lane & 2;
-        const float send = up ? v[0] : v[1];
-        const float keep = up ? v[1] : v[0];
-        v[0] = PA_OP(keep, __shfl_xor_sync(0xffffffffu, send, 2));
-    }
-    v[0] = PA_OP(v[0], __shfl_xor_sync(0xffffffffu, v[0], 1));
-#undef PA_OP
     return v[0];
 }
 
+// Which of the NP values lane `lane` holds after warp_xreduce<NP>.
+template <int NP>
 __device__ __forceinline__ int head_of_lane(int lane) {
-    return ((lane >> 4) & 1) * 8 + ((lane >> 3) & 1) * 4 + ((lane >> 2) & 1) * 2 + ((lane >> 1) & 1);
+    int h = 0;
+#pragma unroll
+    for (int cnt = NP, off = 16; cnt > 1; cnt >>= 1, off >>= 1)
+        if (lane & off) h += cnt / 2;
+    return h;
+}
+
+// One lane per value writes it out: the lanes whose bits below the last
+// transposition offset are zero.
+template <int NP>
+__device__ __forceinline__ bool lane_writes(int lane) {
+    return (lane & ((32 / NP) - 1)) == 0;
 }
 
 // Barrier over the 128 softmax threads that also ORs a flag across them, so
@@ -206,7 +199,7 @@ __device__ __forceinline__ uint16_t f32_to_16(float x, bool f16) {
     return __bfloat16_as_ushort(__float2bfloat16_rn(x));
 }
 
-template <int D, bool FP8>
+template <int D, bool FP8, int NP>
 __global__ void __launch_bounds__(DecodeLayout<D, FP8>::kThreads, 1)
     decode_kernel(const __grid_constant__ DecodeArgs a, const __grid_constant__ CUtensorMap map_k,
                   const __grid_constant__ CUtensorMap map_v) {
@@ -394,7 +387,8 @@ __global__ void __launch_bounds__(DecodeLayout<D, FP8>::kThreads, 1)
         // ------------------------------------------------------------ softmax
         const int q4 = warp & 3;          // TMEM lane quarter this warp may access
         const int row = q4 * 32 + lane;   // key of the tile (S) / output column d (O)
-        const int hl = head_of_lane(lane);
+        const int hl = head_of_lane<NP>(lane);
+        const bool writer = lane_writes<NP>(lane);
         const int G = a.group;
         const uint32_t lane_addr = (uint32_t)(q4 * 32) << 16;
         float* red = reinterpret_cast<float*>(sm + L::kRedOff);
@@ -468,19 +462,19 @@ __global__ void __launch_bounds__(DecodeLayout<D, FP8>::kThreads, 1)
             ++qi;
             const float sl2 = a.scale_log2 * (FP8 ? __ldg(&a.k_scale[it.kvh]) : 1.f);
             const int key_end = min(it.seq_len, it.p1 * kPage);
-            float m[16], lp[16], o[16], alpha_prev[16];
+            float m[NP], lp[NP], o[NP], alpha_prev[NP];
 #pragma unroll
-            for (int h = 0; h < 16; ++h) { m[h] = -INFINITY; lp[h] = 0.f; o[h] = 0.f; alpha_prev[h] = 1.f; }
+            for (int h = 0; h < NP; ++h) { m[h] = -INFINITY; lp[h] = 0.f; o[h] = 0.f; alpha_prev[h] = 1.f; }
 
             auto fold = [&](uint32_t k) {
                 if (!mbar_wait(&bars[B_OF + (k & 1)], (k >> 1) & 1, abort_sh, a.wait_ns)) fail(a, abort_sh, PA_ERR_TIMEOUT);
                 tc_fence_after();
-                uint32_t r[16];
-                tmem_ld_x16(tbase + lane_addr + o_col(k & 1), r);
+                uint32_t r[NP];
+                tmem_ld_cols<NP>(tbase + lane_addr + o_col(k & 1), r);
                 tmem_ld_wait();
                 reg_fence(r);
 #pragma unroll
-                for (int h = 0; h < 16; ++h) o[h] = fmaf(o[h], alpha_prev[h], __uint_as_float(r[h]));
+                for (int h = 0; h < NP; ++h) o[h] = fmaf(o[h], alpha_prev[h], __uint_as_float(r[h]));
             };
 
             for (int t = 0; t < ntiles; ++t, ++g) {
@@ -491,20 +485,20 @@ __global__ void __launch_bounds__(DecodeLayout<D, FP8>::kThreads, 1)
                 if (!mbar_wait(&bars[B_SF + (g & 1)], (g >> 1) & 1, abort_sh, a.wait_ns))
                     fail(a, abort_sh, PA_ERR_TIMEOUT);
                 tc_fence_after();
-                uint32_t sr[16];
-                tmem_ld_x16(tbase + lane_addr + s_col(g & 1), sr);
+                uint32_t sr[NP];
+                tmem_ld_cols<NP>(tbase + lane_addr + s_col(g & 1), sr);
                 tmem_ld_wait();
                 reg_fence(sr);
-                float x[16];
+                float x[NP];
 #pragma unroll
-                for (int h = 0; h < 16; ++h) x[h] = valid ? __uint_as_float(sr[h]) * sl2 : -INFINITY;
-                const float wmax = warp_xreduce16<true>(x, lane);
+                for (int h = 0; h < NP; ++h) x[h] = valid ? __uint_as_float(sr[h]) * sl2 : -INFINITY;
+                const float wmax = warp_xreduce<NP, true>(x, lane);
                 float* rb = red + (g & 1) * 64;
-                if (!(lane & 1)) rb[hl * 4 + q4] = wmax;
+                if (writer) rb[hl * 4 + q4] = wmax;
                 if (softmax_bar_or(*abort_sh != 0)) { aborted = true; break; }
-                float alpha[16];
+                float alpha[NP];
 #pragma unroll
-                for (int h = 0; h < 16; ++h) {
+                for (int h = 0; h < NP; ++h) {
                     const float4 r4 = reinterpret_cast<const float4*>(rb)[h];
                     const float mt = fmaxf(fmaxf(r4.x, r4.y), fmaxf(r4.z, r4.w));
                     const float mn = fmaxf(m[h], mt);
@@ -517,7 +511,7 @@ __global__ void __launch_bounds__(DecodeLayout<D, FP8>::kThreads, 1)
                 // P^T tile (K-major: rows = heads, 128 keys in two 64-key chunks)
                 uint8_t* pb = sm + L::kPOff + (g & 1) * L::kPBytes + (row >> 6) * (kNPad * 128);
 #pragma unroll
-                for (int h = 0; h < 16; ++h)
+                for (int h = 0; h < NP; ++h)
                     if (h < G) *reinterpret_cast<uint16_t*>(pb + sw128_offset(h, row & 63)) = f32_to_16(x[h], FP8);
                 if (!FP8 && !valid) {
                     // a dead key's V row may hold anything (NaN included); 0 * NaN
@@ -535,21 +529,21 @@ __global__ void __launch_bounds__(DecodeLayout<D, FP8>::kThreads, 1)
                 mbar_arrive(&bars[B_PF + (g & 1)]);
                 if (t > 0) fold(g - 1);
 #pragma unroll
-                for (int h = 0; h < 16; ++h) alpha_prev[h] = alpha[h];
+                for (int h = 0; h < NP; ++h) alpha_prev[h] = alpha[h];
             }
             if (aborted) break;
             fold(g - 1);
             tc_fence_before();
 
             // ---- epilogue: total sums, normalise, write
-            const float wsum = warp_xreduce16<false>(lp, lane);
+            const float wsum = warp_xreduce<NP, false>(lp, lane);
             float* rl = red + 128 + (qi & 1) * 64;
-            if (!(lane & 1)) rl[hl * 4 + q4] = wsum;
+            if (writer) rl[hl * 4 + q4] = wsum;
             if (softmax_bar_or(*abort_sh != 0)) { aborted = true; break; }
             const float vs = FP8 ? __ldg(&a.v_scale[it.kvh]) : 1.f;
             float mine_m = 0.f, mine_l = 0.f;
 #pragma unroll
-            for (int h = 0; h < 16; ++h) {
+            for (int h = 0; h < NP; ++h) {
                 const float4 r4 = reinterpret_cast<const float4*>(rl)[h];
                 const float l = (r4.x + r4.y) + (r4.z + r4.w);
                 if (h == row) { mine_m = m[h]; mine_l = l; }
@@ -692,18 +686,28 @@ __global__ void wait_probe_kernel(int* status, uint64_t limit_ns) {
     if (threadIdx.x == 0 && !mbar_wait(&bar, 0, nullptr, limit_ns)) atomicCAS(status, 0, PA_ERR_TIMEOUT);
 }
 
-template <int D, bool FP8>
-cudaError_t launch_decode_t(const DecodeArgs& a, const CUtensorMap* mk, const CUtensorMap* mv, int grid,
-                            cudaStream_t stream) {
+template <int D, bool FP8, int NP>
+cudaError_t launch_decode_np(const DecodeArgs& a, const CUtensorMap* mk, const CUtensorMap* mv, int grid,
+                             cudaStream_t stream) {
     using L = DecodeLayout<D, FP8>;
     static bool configured = false;
     if (!configured) {
-        cudaError_t e = cudaFuncSetAttribute(decode_kernel<D, FP8>, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kSmem);
+        cudaError_t e =
+            cudaFuncSetAttribute(decode_kernel<D, FP8, NP>, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kSmem);
         if (e != cudaSuccess) return e;
         configured = true;
     }
-    decode_kernel<D, FP8><<<grid, L::kThreads, L::kSmem, stream>>>(a, *mk, *mv);
+    decode_kernel<D, FP8, NP><<<grid, L::kThreads, L::kSmem, stream>>>(a, *mk, *mv);
     return cudaGetLastError();
+}
+
+// The softmax works on the group's heads padded to 4, 8 or 16 (the MMA N stays 16).
+template <int D, bool FP8>
+cudaError_t launch_decode_t(const DecodeArgs& a, const CUtensorMap* mk, const CUtensorMap* mv, int grid,
+                            cudaStream_t stream) {
+    if (a.group <= 4) return launch_decode_np<D, FP8, 4>(a, mk, mv, grid, stream);
+    if (a.group <= 8) return launch_decode_np<D, FP8, 8>(a, mk, mv, grid, stream);
+    return launch_decode_np<D, FP8, 16>(a, mk, mv, grid, stream);
 }
 
 }  // namespace

@@ -427,15 +427,26 @@ pa_status pa_prefill(const pa_prefill_shapes* sh, const void* q, const void* k, 
     a.num_pool_pages = paged ? sh->num_pool_pages : 0;
     a.total_q = sh->total_q;
     a.num_q_tiles = (int32_t)cdiv(sh->max_seqlen_q, 256);
+    // the longest-first unit order lives after the status word when the
+    // workspace has room for it (see pa_prefill_workspace_size)
+    const int64_t units = (int64_t)a.num_q_tiles * B;
+    if (units > 65535) return fail(PA_ERR_UNSUPPORTED, "batch * ceil(max_seqlen_q / 256) must be <= 65535");
+    a.order = (units <= 4096 && workspace_bytes >= PA_STATUS_BYTES + (size_t)units * 4)
+                  ? reinterpret_cast<const int32_t*>(static_cast<uint8_t*>(workspace) + PA_STATUS_BYTES)
+                  : nullptr;
     a.causal = causal != 0;
     a.paged = paged;
     a.rope = rope;
     a.scale_log2 = scale * 1.4426950408889634f;
     a.wait_ns = g_wait_limit_ns.load();
-    if ((int64_t)a.num_q_tiles * B > INT32_MAX) return fail(PA_ERR_UNSUPPORTED, "grid too large");
     cudaError_t e = pa::launch_prefill(a, dqk, &mq, &mk, &mv, &mr, stream);
     if (e != cudaSuccess) return cuda_fail(e, "prefill launch");
     return PA_OK;
+}
+
+size_t pa_prefill_workspace_size(const pa_prefill_shapes* sh) {
+    if (!sh || sh->batch <= 0 || sh->max_seqlen_q <= 0) return PA_STATUS_BYTES;
+    return PA_STATUS_BYTES + (size_t)sh->batch * (size_t)cdiv(sh->max_seqlen_q, 256) * 4;
 }
 
 pa_status pa_check_status(void* workspace, cudaStream_t stream) {

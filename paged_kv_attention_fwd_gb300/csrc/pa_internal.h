@@ -55,11 +55,12 @@ struct PrefillArgs {
     const int32_t* cu_k;
     const int32_t* block_table;
     const int32_t* qo_offset;
+    const int32_t* order;  // [batch * num_q_tiles] unit order in the workspace, or nullptr
     uint16_t* out;   // bf16 [total_q, Hq, Dv]
     float* lse;      // [total_q, Hq] or nullptr
     int* status;
     int32_t batch, num_q_heads, num_kv_heads, group, max_pages, num_pool_pages, total_q;
-    int32_t num_q_tiles;  // ceil(max_seqlen_q / 128)
+    int32_t num_q_tiles;  // 256-row query blocks per segment: ceil(max_seqlen_q / 256)
     int32_t causal, paged, rope;
     float scale_log2;
     uint64_t wait_ns;

@@ -206,6 +206,27 @@ __device__ __forceinline__ void tmem_ld_x32(uint32_t taddr, uint32_t (&r)[32]) {
         : "r"(taddr));
 }
 
+__device__ __forceinline__ void tmem_ld_x4(uint32_t taddr, uint32_t (&r)[4]) {
+    asm volatile("tcgen05.ld.sync.aligned.32x32b.x4.b32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+                 : "r"(taddr));
+}
+
+__device__ __forceinline__ void tmem_ld_x8(uint32_t taddr, uint32_t (&r)[8]) {
+    asm volatile("tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7])
+                 : "r"(taddr));
+}
+
+// N consecutive 32-bit columns of this thread's TMEM lane, N in {4, 8, 16, 32}
+template <int N>
+__device__ __forceinline__ void tmem_ld_cols(uint32_t taddr, uint32_t (&r)[N]) {
+    if constexpr (N == 4) tmem_ld_x4(taddr, r);
+    else if constexpr (N == 8) tmem_ld_x8(taddr, r);
+    else if constexpr (N == 16) tmem_ld_x16(taddr, r);
+    else tmem_ld_x32(taddr, r);
+}
+
 // Wait for this thread's outstanding TMEM loads.  Registers filled by the
 // loads must not be used before this; pass them through reg_fence() after it
 // so the compiler cannot hoist their uses above the wait.

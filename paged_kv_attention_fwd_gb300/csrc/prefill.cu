@@ -114,9 +114,13 @@ __global__ void __launch_bounds__(320, 1)
     volatile int* abort_sh = &abort_store;
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int b = blockIdx.x % a.batch;
-    const int pair = a.num_q_tiles - 1 - (int)(blockIdx.x / a.batch);  // longest first
-    const int h = blockIdx.y;
+    // blockIdx.x = head (fastest), blockIdx.y = rank of the (segment, query block)
+    // unit; with an order from prefill_order_kernel the costliest units go first
+    const int rank = blockIdx.y;
+    const int unit = a.order ? __ldg(&a.order[rank]) : -1;
+    const int b = unit >= 0 ? unit % a.batch : rank % a.batch;
+    const int pair = unit >= 0 ? unit / a.batch : a.num_q_tiles - 1 - rank / a.batch;
+    const int h = blockIdx.x;
     const int kvh = h / a.group;
     const Seg sg = load_seg(a, b);
     const int rA = pair * 256;  // first query row of tile A within the segment
@@ -359,17 +363,31 @@ __global__ void __launch_bounds__(320, 1)
             if (!ok) break;
             tc_fence_after();
             const int vis = (int)min(128LL, max(0LL, lim - (long long)j * 128));  // visible keys of this tile
-            // pass 1: row max of the scaled, masked scores (S read from TMEM in 32-column chunks)
-            float mt = -INFINITY;
+            // every key of the tile visible to every row of the warp, positive scale:
+            // no per-element masking, and the max can be taken on the raw scores
+            const bool full = __all_sync(0xffffffffu, vis >= 128) && sl2 > 0.f;
+            // pass 1: row max of the scaled, masked scores (S read from TMEM, 64 columns per wait)
+            float mt;
+            {
+                float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
-            for (int c = 0; c < 4; ++c) {
-                uint32_t r[32];
-                tmem_ld_x32(tbase + lane_addr + s_col(x) + c * 32, r);
-                tmem_ld_wait();
-                reg_fence(r);
+                for (int hh = 0; hh < 2; ++hh) {
+                    uint32_t r[64];
+                    tmem_ld_x32(tbase + lane_addr + s_col(x) + hh * 64, *reinterpret_cast<uint32_t(*)[32]>(&r[0]));
+                    tmem_ld_x32(tbase + lane_addr + s_col(x) + hh * 64 + 32, *reinterpret_cast<uint32_t(*)[32]>(&r[32]));
+                    tmem_ld_wait();
+                    reg_fence(r);
+                    if (full) {
 #pragma unroll
-                for (int k = 0; k < 32; ++k)
-                    if (c * 32 + k < vis) mt = fmaxf(mt, __uint_as_float(r[k]) * sl2);
+                        for (int k = 0; k < 64; ++k) m4[k & 3] = fmaxf(m4[k & 3], __uint_as_float(r[k]));
+                    } else {
+#pragma unroll
+                        for (int k = 0; k < 64; ++k)
+                            if (hh * 64 + k < vis) m4[k & 3] = fmaxf(m4[k & 3], __uint_as_float(r[k]) * sl2);
+                    }
+                }
+                mt = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
+                if (full) mt *= sl2;
             }
             // conditional rescale: keep the stale max unless the new one is 2^8 larger
             const bool grow = mt > m_run + kRescaleThreshold;
@@ -398,26 +416,43 @@ __global__ void __launch_bounds__(320, 1)
                 m_run = m_new;
             }
             const bool none = m_run == -INFINITY;
-            float rs = 0.f;
+            const bool fast = __all_sync(0xffffffffu, full && !none);
+            const float neg_m = -m_run;
+            float rs0 = 0.f, rs1 = 0.f;
             // pass 2: P = exp2(x - m) in bf16, written over S columns already read
-            // (keys 32c..32c+31 -> P columns 16c..16c+15)
+            // (keys 64h..64h+63 -> P columns 32h..32h+31)
 #pragma unroll
-            for (int c = 0; c < 4; ++c) {
-                uint32_t r[32], pw[16];
-                tmem_ld_x32(tbase + lane_addr + s_col(x) + c * 32, r);
+            for (int hh = 0; hh < 2; ++hh) {
+                uint32_t r[64], pw[32];
+                tmem_ld_x32(tbase + lane_addr + s_col(x) + hh * 64, *reinterpret_cast<uint32_t(*)[32]>(&r[0]));
+                tmem_ld_x32(tbase + lane_addr + s_col(x) + hh * 64 + 32, *reinterpret_cast<uint32_t(*)[32]>(&r[32]));
                 tmem_ld_wait();
                 reg_fence(r);
+                if (fast) {
 #pragma unroll
-                for (int k = 0; k < 16; ++k) {
-                    const int key = c * 32 + 2 * k;
-                    const float p0 = (none || key >= vis) ? 0.f : ex2(__uint_as_float(r[2 * k]) * sl2 - m_run);
-                    const float p1 = (none || key + 1 >= vis) ? 0.f : ex2(__uint_as_float(r[2 * k + 1]) * sl2 - m_run);
-                    rs += p0 + p1;
-                    const __nv_bfloat162 pk = __floats2bfloat162_rn(p0, p1);
-                    pw[k] = *reinterpret_cast<const uint32_t*>(&pk);
+                    for (int k = 0; k < 32; ++k) {
+                        const float p0 = ex2(fmaf(__uint_as_float(r[2 * k]), sl2, neg_m));
+                        const float p1 = ex2(fmaf(__uint_as_float(r[2 * k + 1]), sl2, neg_m));
+                        rs0 += p0;
+                        rs1 += p1;
+                        const __nv_bfloat162 pk = __floats2bfloat162_rn(p0, p1);
+                        pw[k] = *reinterpret_cast<const uint32_t*>(&pk);
+                    }
+                } else {
+#pragma unroll
+                    for (int k = 0; k < 32; ++k) {
+                        const int key = hh * 64 + 2 * k;
+                        const float p0 = (none || key >= vis) ? 0.f : ex2(__uint_as_float(r[2 * k]) * sl2 - m_run);
+                        const float p1 = (none || key + 1 >= vis) ? 0.f : ex2(__uint_as_float(r[2 * k + 1]) * sl2 - m_run);
+                        rs0 += p0;
+                        rs1 += p1;
+                        const __nv_bfloat162 pk = __floats2bfloat162_rn(p0, p1);
+                        pw[k] = *reinterpret_cast<const uint32_t*>(&pk);
+                    }
                 }
-                tmem_st_x16(tbase + lane_addr + s_col(x) + c * 16, pw);
+                tmem_st_x32(tbase + lane_addr + s_col(x) + hh * 32, pw);
             }
+            const float rs = rs0 + rs1;
             l_run += rs;
             tmem_st_wait();
             tc_fence_before();
@@ -477,6 +512,49 @@ __global__ void __launch_bounds__(320, 1)
     }
 }
 
+// Sort the (segment, 256-row query block) units by KV tiles to process, most
+// first (ties: lower unit index), so the longest CTAs start first.  One CTA;
+// bitonic sort of up to 4096 keys in shared memory.
+__global__ void __launch_bounds__(512) prefill_order_kernel(const PrefillArgs a, int32_t* order) {
+    __shared__ unsigned long long key[4096];
+    const int n = a.batch * a.num_q_tiles;
+    int p2 = 1;
+    while (p2 < n) p2 <<= 1;
+    for (int u = threadIdx.x; u < p2; u += blockDim.x) {
+        unsigned long long k = ~0ull;
+        if (u < n) {
+            const int b = u % a.batch, pair = u / a.batch;
+            const Seg sg = load_seg(a, b);
+            const int rA = pair * 256;
+            int cost = -1;
+            if (rA < sg.q_len) {
+                const bool causal = a.causal != 0;
+                cost = 2 + kv_tiles_for(sg, rA, min(rA + 128, sg.q_len), causal) +
+                       (rA + 128 < sg.q_len ? kv_tiles_for(sg, rA + 128, min(rA + 256, sg.q_len), causal) : 0);
+            }
+            k = ((unsigned long long)(unsigned)(0x7FFFFFFF - cost) << 32) | (unsigned)u;
+        }
+        key[u] = k;
+    }
+    __syncthreads();
+    for (int size = 2; size <= p2; size <<= 1) {
+        for (int stride = size >> 1; stride > 0; stride >>= 1) {
+            for (int t = threadIdx.x; t < p2 / 2; t += blockDim.x) {
+                const int lo = 2 * stride * (t / stride) + (t % stride);
+                const int hi = lo + stride;
+                const bool up = (lo & size) == 0;
+                const unsigned long long x = key[lo], y = key[hi];
+                if ((x > y) == up) {
+                    key[lo] = y;
+                    key[hi] = x;
+                }
+            }
+            __syncthreads();
+        }
+    }
+    for (int u = threadIdx.x; u < n; u += blockDim.x) order[u] = (int32_t)(key[u] & 0xFFFFFFFFu);
+}
+
 template <bool ROPE, bool PAGED>
 cudaError_t launch_t(const PrefillArgs& a, const CUtensorMap* mq, const CUtensorMap* mk, const CUtensorMap* mv,
                      const CUtensorMap* mr, cudaStream_t stream) {
@@ -488,7 +566,12 @@ cudaError_t launch_t(const PrefillArgs& a, const CUtensorMap* mq, const CUtensor
         if (e != cudaSuccess) return e;
         configured = true;
     }
-    dim3 grid(a.num_q_tiles * a.batch, a.num_q_heads);
+    if (a.order) {
+        prefill_order_kernel<<<1, 512, 0, stream>>>(a, const_cast<int32_t*>(a.order));
+        cudaError_t e = cudaGetLastError();
+        if (e != cudaSuccess) return e;
+    }
+    dim3 grid(a.num_q_heads, a.num_q_tiles * a.batch);
     prefill_kernel<ROPE, PAGED><<<grid, L::kThreads, L::kSmem, stream>>>(a, *mq, *mk, *mv, *mr);
     return cudaGetLastError();
 }

@@ -83,7 +83,7 @@ def prefill(sh: B.pa_prefill_shapes, q, k, v, cu_seqlens_q, cu_seqlens_k, scale:
     if lse is None:
         lse = torch.empty((sh.total_q, sh.num_q_heads), dtype=torch.float32, device=dev)
     if workspace is None:
-        workspace = torch.zeros(B.PA_STATUS_BYTES, dtype=torch.uint8, device=dev)
+        workspace = torch.zeros(B.pa_prefill_workspace_size(sh), dtype=torch.uint8, device=dev)
     B.pa_prefill(sh, q, k, v, k_rope, cu_seqlens_q, cu_seqlens_k, block_table, qo_offset, causal, scale, out, lse,
                  workspace, stream=stream)
     return out, lse, workspace

@@ -174,3 +174,22 @@ def test_prefill_equals_decode_for_single_query_rows():
     assert st == B.PA_OK
     ro, rl = oracle.decode(d.q, d.k_pool, d.v_pool, d.block_table, d.seq_lens, d.scale)
     assert_close(out, lse, ro, rl)
+
+
+def test_longest_first_order_changes_nothing():
+    """With the larger workspace the CTAs run in a sorted order; results match
+    the fixed order bit for bit."""
+    inp = W.make_paged_prefill([300, 40, 700, 129], [2300, 40, 900, 4000], 4, 2, 128, seed=12)
+    dev = "cuda"
+    args = [ops.as_bf16(inp.q, dev), ops.as_bf16(inp.k, dev), ops.as_bf16(inp.v, dev),
+            torch.from_numpy(inp.cu_seqlens_q).to(dev), torch.from_numpy(inp.cu_seqlens_k).to(dev), inp.scale]
+    sh = ops.prefill_shapes(inp.batch, 4, 2, 128, 128, 0, inp.max_seqlen_q, int(inp.cu_seqlens_q[-1]),
+                            int(inp.cu_seqlens_k[-1]), max_pages=inp.block_table.shape[1],
+                            num_pool_pages=inp.k.shape[0])
+    bt = torch.from_numpy(inp.block_table).to(dev)
+    assert B.pa_prefill_workspace_size(sh) > B.PA_STATUS_BYTES
+    small = torch.zeros(B.PA_STATUS_BYTES, dtype=torch.uint8, device=dev)
+    o1, l1, ws1 = ops.prefill(sh, *args, True, block_table=bt)
+    o2, l2, ws2 = ops.prefill(sh, *args, True, block_table=bt, workspace=small)
+    assert B.pa_check_status(ws1) == B.PA_OK and B.pa_check_status(ws2) == B.PA_OK
+    assert torch.equal(o1, o2) and torch.equal(l1, l2)
