@@ -114,13 +114,20 @@ __global__ void __launch_bounds__(320, 1)
     volatile int* abort_sh = &abort_store;
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    // blockIdx.x = head (fastest), blockIdx.y = rank of the (segment, query block)
-    // unit; with an order from prefill_order_kernel the costliest units go first
-    const int rank = blockIdx.y;
+    // CTA index -> (unit rank, head): heads come in groups of hg (up to 32);
+    // within a group the unit rank is the slow index and the head the fast one.
+    // With an order from prefill_order_kernel the costliest units start first,
+    // and CTAs that run together share a handful of heads' K/V tiles in L2.
+    const int units = a.num_q_tiles * a.batch;
+    const int hg = a.num_q_heads < 32 ? a.num_q_heads : 32;
+    const int group = (int)(blockIdx.x / (unsigned)(hg * units));
+    const int in_group = (int)(blockIdx.x % (unsigned)(hg * units));
+    const int hg_here = min(hg, a.num_q_heads - group * hg);  // the last group may be narrower
+    const int rank = in_group / hg_here;
+    const int h = group * hg + in_group % hg_here;
     const int unit = a.order ? __ldg(&a.order[rank]) : -1;
     const int b = unit >= 0 ? unit % a.batch : rank % a.batch;
     const int pair = unit >= 0 ? unit / a.batch : a.num_q_tiles - 1 - rank / a.batch;
-    const int h = blockIdx.x;
     const int kvh = h / a.group;
     const Seg sg = load_seg(a, b);
     const int rA = pair * 256;  // first query row of tile A within the segment
@@ -317,16 +324,16 @@ __global__ void __launch_bounds__(320, 1)
                     tc_fence_after();
                     pv(x, j);
                     if (j + 1 < n[x]) {
-                        // P_x lives in S_x's columns: the next S_x may only be
-                        // written once this PV has read P_x
+                        // P_x lives in S_x's columns.  MMAs issued by this thread
+                        // execute in issue order, so the next S_x written here
+                        // cannot overtake PV_x's read of P_x.
                         if (!k_waited) {
                             ok = mbar_wait(&bars[P_KF + (j + 1) % L::kNK], ((j + 1) / L::kNK) & 1, abort_sh,
                                            a.wait_ns);
                             k_waited = true;
+                            if (!ok) break;
+                            tc_fence_after();
                         }
-                        ok = ok && mbar_wait(&bars[P_OD + x], j & 1, abort_sh, a.wait_ns);
-                        if (!ok) break;
-                        tc_fence_after();
                         qk(x, j + 1);
                     }
                 }
@@ -379,7 +386,8 @@ __global__ void __launch_bounds__(320, 1)
                     reg_fence(r);
                     if (full) {
 #pragma unroll
-                        for (int k = 0; k < 64; ++k) m4[k & 3] = fmaxf(m4[k & 3], __uint_as_float(r[k]));
+                        for (int k = 0; k < 64; k += 2)
+                            m4[(k >> 1) & 3] = fmax3(m4[(k >> 1) & 3], __uint_as_float(r[k]), __uint_as_float(r[k + 1]));
                     } else {
 #pragma unroll
                         for (int k = 0; k < 64; ++k)
@@ -429,15 +437,22 @@ __global__ void __launch_bounds__(320, 1)
                 tmem_ld_wait();
                 reg_fence(r);
                 if (fast) {
+                    const uint64_t sc2 = f2_pack(__float_as_uint(sl2), __float_as_uint(sl2));
+                    const uint64_t nm2 = f2_pack(__float_as_uint(neg_m), __float_as_uint(neg_m));
+                    uint64_t acc2 = f2_pack(0u, 0u);
 #pragma unroll
                     for (int k = 0; k < 32; ++k) {
-                        const float p0 = ex2(fmaf(__uint_as_float(r[2 * k]), sl2, neg_m));
-                        const float p1 = ex2(fmaf(__uint_as_float(r[2 * k + 1]), sl2, neg_m));
-                        rs0 += p0;
-                        rs1 += p1;
+                        float x0, x1;
+                        f2_unpack(f2_fma(f2_pack(r[2 * k], r[2 * k + 1]), sc2, nm2), x0, x1);
+                        const float p0 = ex2(x0), p1 = ex2(x1);
+                        acc2 = f2_add(acc2, f2_pack(__float_as_uint(p0), __float_as_uint(p1)));
                         const __nv_bfloat162 pk = __floats2bfloat162_rn(p0, p1);
                         pw[k] = *reinterpret_cast<const uint32_t*>(&pk);
                     }
+                    float a0, a1;
+                    f2_unpack(acc2, a0, a1);
+                    rs0 += a0;
+                    rs1 += a1;
                 } else {
 #pragma unroll
                     for (int k = 0; k < 32; ++k) {
@@ -571,7 +586,7 @@ cudaError_t launch_t(const PrefillArgs& a, const CUtensorMap* mq, const CUtensor
         cudaError_t e = cudaGetLastError();
         if (e != cudaSuccess) return e;
     }
-    dim3 grid(a.num_q_heads, a.num_q_tiles * a.batch);
+    dim3 grid((unsigned)(a.num_q_tiles * a.batch) * (unsigned)a.num_q_heads);
     prefill_kernel<ROPE, PAGED><<<grid, L::kThreads, L::kSmem, stream>>>(a, *mq, *mk, *mv, *mr);
     return cudaGetLastError();
 }
