@@ -635,6 +635,435 @@ __global__ void __launch_bounds__(DecodeLayout<D, FP8>::kThreads, 1)
     }
 }
 
+// ---------------------------------------------------------------------------
+// e4m3 pages, D = 128: both products on the e4m3 tensor path (kind::f8f6f4),
+// straight from the TMA-loaded pages -- no conversion pass, so shared memory
+// holds only the page ring (5 stages of 2 pages of K and V).
+//   S^T[128 keys, 16] = K_tile . Q3^T: the bf16 query of each head is scaled
+//     by a power of two (max |q| -> [128, 256)) and split into three e4m3
+//     levels hi + mid + lo, accumulated into the same TMEM columns (the split
+//     keeps 12 significant bits; bf16 has 8);
+//   O^T[128 d, 32]    = V_tile^T . P2: P * 256 split into two e4m3 levels
+//     (hi + lo, about bf16 precision) in columns 0-15 and 16-31, summed when
+//     the output is folded.
+constexpr int kF8Stages = 5;
+struct F8Layout {
+    static constexpr int kStageBytes = 32768;  // K: 2 pages x 64 rows x 128 B, then V the same
+    static constexpr int kQ3Off = kF8Stages * kStageBytes;
+    static constexpr int kQ3Bytes = 48 * 128;  // rows = level * 16 + head
+    static constexpr int kPOff = kQ3Off + 2 * kQ3Bytes;
+    static constexpr int kPBytes = 128 * 128;  // row = key; bytes 0-15 hi, 16-31 lo (MN-major)
+    static constexpr int kRedOff = kPOff + 2 * kPBytes;
+    static constexpr int kQscOff = kRedOff + 1024;  // [2][16] floats
+    static constexpr int kBytes = kQscOff + 128;
+    static constexpr int kSmem = kBytes + 1024;
+};
+static_assert(F8Layout::kQ3Off % 1024 == 0 && F8Layout::kPOff % 1024 == 0, "swizzle atoms need 1024-byte alignment");
+static_assert(F8Layout::kSmem <= 232448, "shared memory per CTA");
+
+enum : int { F_FULL = 0, F_EMPTY = 5, F_QF = 10, F_SF = 12, F_PF = 14, F_OF = 16, F_DONE = 18, F_COUNT = 19 };
+__host__ __device__ constexpr uint32_t f8_s_col(uint32_t b) { return b * 16u; }
+__host__ __device__ constexpr uint32_t f8_o_col(uint32_t b) { return 32u + b * 32u; }
+
+__device__ __forceinline__ uint32_t e4m3x2(float lo, float hi) {
+    return (uint32_t)__nv_cvt_float2_to_fp8x2(make_float2(lo, hi), __NV_SATFINITE, __NV_E4M3);
+}
+
+__device__ __forceinline__ float2 e4m3x2_to_f2(uint32_t v) {
+    const __half2_raw h = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)v, __NV_E4M3);
+    __half2 hh;
+    hh = *reinterpret_cast<const __half2*>(&h);
+    return __half22float2(hh);
+}
+
+template <int NP>
+__global__ void __launch_bounds__(192, 1)
+    decode_f8_kernel(const __grid_constant__ DecodeArgs a, const __grid_constant__ CUtensorMap map_k,
+                     const __grid_constant__ CUtensorMap map_v) {
+    using L = F8Layout;
+    constexpr int D = 128;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    __shared__ __align__(8) uint64_t bars[F_COUNT];
+    __shared__ uint32_t tmem_base_sh;
+    __shared__ int abort_store;
+    volatile int* abort_sh = &abort_store;
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int32_t* meta = a.meta;
+    const int B = a.batch;
+    const int items_off = items_offset(meta, B);
+    int it_lo = 0, it_hi = 0;
+    if ((int)blockIdx.x < __ldg(&meta[5])) {
+        it_lo = __ldg(&meta[kMetaHeader + 2 * B + 1 + blockIdx.x]);
+        it_hi = __ldg(&meta[kMetaHeader + 2 * B + 1 + blockIdx.x + 1]);
+    }
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < kF8Stages; ++s) {
+            mbar_init(&bars[F_FULL + s], 1);
+            mbar_init(&bars[F_EMPTY + s], 1);
+        }
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(&bars[F_QF + i], 128);
+            mbar_init(&bars[F_SF + i], 1);
+            mbar_init(&bars[F_PF + i], 128);
+            mbar_init(&bars[F_OF + i], 1);
+        }
+        mbar_init(&bars[F_DONE], 1);
+        *abort_sh = 0;
+        fence_barrier_init();
+    }
+    if (warp == 1) {
+        tmem_alloc(&tmem_base_sh, 128);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tbase = tmem_base_sh;
+
+    if (warp == 0) {
+        // ------------------------------------------------------------ producer
+        if (lane == 0) {
+            uint32_t g = 0;
+            uint32_t last_par[kF8Stages] = {};
+            bool issued[kF8Stages] = {};
+            bool ok = true;
+            for (int j = it_lo; j < it_hi && ok; ++j) {
+                const Item it = load_item(a, j, items_off);
+                const int ntiles = item_tiles(it);
+                const long long bt_row = (long long)it.b * a.max_pages;
+                for (int t = 0; t < ntiles; ++t, ++g) {
+                    const int stage = g % kF8Stages;
+                    const int pa0 = it.p0 + 2 * t;
+                    const int npg = min(2, it.p1 - pa0);
+                    int pid[2];
+                    pid[0] = __ldg(&a.block_table[bt_row + pa0]);
+                    pid[1] = npg > 1 ? __ldg(&a.block_table[bt_row + pa0 + 1]) : 0;
+                    if (!mbar_wait(&bars[F_EMPTY + stage], ((g / kF8Stages) & 1) ^ 1, abort_sh, a.wait_ns)) {
+                        fail(a, abort_sh, PA_ERR_TIMEOUT);
+                        ok = false;
+                        break;
+                    }
+                    bool valid[2];
+                    uint32_t nvalid = 0;
+                    for (int i = 0; i < 2; ++i) {
+                        valid[i] = i < npg && (unsigned)pid[i] < (unsigned)a.num_pool_pages;
+                        if (i < npg && !valid[i]) record(a.status, PA_ERR_DEVICE_BOUNDS);
+                        nvalid += valid[i];
+                    }
+                    uint64_t* full = &bars[F_FULL + stage];
+                    mbar_arrive_expect_tx(full, nvalid * 2u * 8192u);
+                    uint8_t* st = sm + stage * L::kStageBytes;
+                    for (int i = 0; i < 2; ++i) {
+                        if (!valid[i]) continue;
+                        const int row = (int)(((long long)pid[i] * a.num_kv_heads + it.kvh) * 64);
+                        tma_load_2d(st + i * 8192, &map_k, full, 0, row);
+                        tma_load_2d(st + 16384 + i * 8192, &map_v, full, 0, row);
+                    }
+                    last_par[stage] = (g / kF8Stages) & 1;
+                    issued[stage] = true;
+                }
+            }
+            for (int s = 0; s < kF8Stages; ++s)
+                if (issued[s]) mbar_wait(&bars[F_FULL + s], last_par[s], nullptr, a.wait_ns);
+        }
+    } else if (warp == 1) {
+        // ------------------------------------------------------------ MMA issuer
+        if (lane == 0) {
+            constexpr uint32_t idesc_qk = idesc_e4m3(128, 16, false, false);
+            constexpr uint32_t idesc_pv = idesc_e4m3(128, 32, true, true);
+            uint32_t g = 0, qi = 0;
+            bool pending = false, ok = true;
+            auto issue_pv = [&](uint32_t k) -> bool {
+                if (!mbar_wait(&bars[F_PF + (k & 1)], (k >> 1) & 1, abort_sh, a.wait_ns)) return false;
+                tc_fence_after();
+                const uint32_t vbase = smem_u32(sm + (k % kF8Stages) * L::kStageBytes + 16384);
+                const uint32_t pbase = smem_u32(sm + L::kPOff + (k & 1) * L::kPBytes);
+#pragma unroll
+                for (int kk = 0; kk < 4; ++kk)  // 32 keys per step
+                    mma_f8_ss(tbase + f8_o_col(k & 1), sdesc_sw128(vbase + kk * 4096, 1024, 1024),
+                              sdesc_sw128(pbase + kk * 4096, 1024, 1024), idesc_pv, kk > 0);
+                mma_commit(&bars[F_OF + (k & 1)]);
+                mma_commit(&bars[F_EMPTY + (k % kF8Stages)]);
+                return true;
+            };
+            for (int j = it_lo; j < it_hi && ok; ++j) {
+                const Item it = load_item(a, j, items_off);
+                const int ntiles = item_tiles(it);
+                if (ntiles == 0) continue;
+                if (!mbar_wait(&bars[F_QF + (qi & 1)], (qi >> 1) & 1, abort_sh, a.wait_ns)) {
+                    fail(a, abort_sh, PA_ERR_TIMEOUT);
+                    ok = false;
+                    break;
+                }
+                const uint32_t qbase = smem_u32(sm + L::kQ3Off + (qi & 1) * L::kQ3Bytes);
+                ++qi;
+                for (int t = 0; t < ntiles; ++t, ++g) {
+                    const int stage = g % kF8Stages;
+                    if (!mbar_wait(&bars[F_FULL + stage], (g / kF8Stages) & 1, abort_sh, a.wait_ns)) {
+                        fail(a, abort_sh, PA_ERR_TIMEOUT);
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t kbase = smem_u32(sm + stage * L::kStageBytes);
+#pragma unroll
+                    for (int kk = 0; kk < 4; ++kk)      // 32 bytes of d per step
+#pragma unroll
+                        for (int lvl = 0; lvl < 3; ++lvl)  // hi, mid, lo query levels
+                            mma_f8_ss(tbase + f8_s_col(g & 1), sdesc_sw128(kbase + kk * 32, 16, 1024),
+                                      sdesc_sw128(qbase + lvl * 2048 + kk * 32, 16, 1024), idesc_qk,
+                                      (kk | lvl) ? 1u : 0u);
+                    mma_commit(&bars[F_SF + (g & 1)]);
+                    if (pending && !issue_pv(g - 1)) {
+                        fail(a, abort_sh, PA_ERR_TIMEOUT);
+                        ok = false;
+                        break;
+                    }
+                    pending = true;
+                }
+            }
+            if (ok && pending && !issue_pv(g - 1)) fail(a, abort_sh, PA_ERR_TIMEOUT);
+            mma_commit(&bars[F_DONE]);
+            mbar_wait(&bars[F_DONE], 0, nullptr, a.wait_ns);
+        }
+    } else {
+        // ------------------------------------------------------------ softmax
+        const int q4 = warp & 3;
+        const int row = q4 * 32 + lane;
+        const int hl = head_of_lane<NP>(lane);
+        const bool writer = lane_writes<NP>(lane);
+        const int G = a.group;
+        const uint32_t lane_addr = (uint32_t)(q4 * 32) << 16;
+        float* red = reinterpret_cast<float*>(sm + L::kRedOff);
+        float* qsc = reinterpret_cast<float*>(sm + L::kQscOff);
+
+        auto next_nonempty = [&](int j) {
+            while (j < it_hi && item_tiles(load_item(a, j, items_off)) == 0) ++j;
+            return j;
+        };
+        // query of the item's KV group -> three e4m3 levels (rows level*16 + head)
+        auto load_q = [&](int j, uint32_t qidx) {
+            const Item it = load_item(a, j, items_off);
+            uint8_t* qb = sm + L::kQ3Off + (qidx & 1) * L::kQ3Bytes;
+            const int h = row >> 3, c = row & 7;  // head, 16-element chunk of d
+            float v[16];
+            if (h < G) {
+                const long long qrow = (long long)it.b * a.num_q_heads + (long long)it.kvh * G + h;
+                const uint4* src = reinterpret_cast<const uint4*>(a.q + qrow * D) + 2 * c;
+                const uint4 w0 = __ldg(src), w1 = __ldg(src + 1);
+                const uint32_t w[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    v[2 * i] = __uint_as_float(w[i] << 16);
+                    v[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
+                }
+            } else {
+#pragma unroll
+                for (int i = 0; i < 16; ++i) v[i] = 0.f;
+            }
+            float mx = 0.f;
+#pragma unroll
+            for (int i = 0; i < 16; ++i) mx = fmaxf(mx, fabsf(v[i]));
+            mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
+            mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
+            mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 4));
+            int e = 0;
+            if (mx > 0.f) frexpf(mx, &e);              // mx in [2^(e-1), 2^e)
+            const float up = ldexpf(1.f, 8 - e);       // scaled max in [128, 256)
+            uint32_t lv[3][4];
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                float r0 = v[2 * i] * up, r1 = v[2 * i + 1] * up;  // exact (power of two)
+#pragma unroll
+                for (int l = 0; l < 3; ++l) {
+                    const uint32_t b2 = e4m3x2(r0, r1);
+                    const float2 back = e4m3x2_to_f2(b2);
+                    r0 -= back.x;
+                    r1 -= back.y;
+                    if (i & 1) lv[l][i >> 1] |= b2 << 16;
+                    else lv[l][i >> 1] = b2;
+                }
+            }
+#pragma unroll
+            for (int l = 0; l < 3; ++l) {
+                const int qr = l * 16 + h;
+                *reinterpret_cast<uint4*>(qb + qr * 128 + ((c ^ (qr & 7)) << 4)) =
+                    make_uint4(lv[l][0], lv[l][1], lv[l][2], lv[l][3]);
+            }
+            if (c == 0) qsc[(qidx & 1) * 16 + h] = ldexpf(1.f, e - 8);
+            fence_proxy_async_smem();
+            mbar_arrive(&bars[F_QF + (qidx & 1)]);
+        };
+
+        int qload = next_nonempty(it_lo);
+        uint32_t qload_idx = 0;
+        for (int k = 0; k < 2 && qload < it_hi; ++k) {
+            load_q(qload, qload_idx++);
+            qload = next_nonempty(qload + 1);
+        }
+        named_bar_sync(1, 128);  // query scales of the first items visible to all
+
+        uint32_t g = 0, qi = 0;
+        bool aborted = false;
+        for (int j = it_lo; j < it_hi && !aborted; ++j) {
+            const Item it = load_item(a, j, items_off);
+            const int ntiles = item_tiles(it);
+            const bool partial = it.nsplit > 1;
+            const long long head0 = (long long)it.kvh * G;
+            const long long orow = partial ? (long long)(it.split_base + it.s) * a.num_q_heads + head0
+                                           : (long long)it.b * a.num_q_heads + head0;
+            if (ntiles == 0) {
+                for (int h = 0; h < G; ++h) {
+                    if (partial) a.o_part[(orow + h) * D + row] = 0.f;
+                    else a.out[(orow + h) * D + row] = 0;
+                }
+                if (row < G) {
+                    if (partial) a.lse_part[orow + row] = -INFINITY;
+                    else if (a.lse) a.lse[orow + row] = -INFINITY;
+                }
+                continue;
+            }
+            if (qi >= 1 && qload < it_hi) {
+                load_q(qload, qload_idx++);
+                qload = next_nonempty(qload + 1);
+            }
+            const float base_l2 = a.scale_log2 * __ldg(&a.k_scale[it.kvh]);
+            float sl2[NP];
+#pragma unroll
+            for (int h = 0; h < NP; ++h) sl2[h] = base_l2 * qsc[(qi & 1) * 16 + h];
+            ++qi;
+            const int key_end = min(it.seq_len, it.p1 * kPage);
+            float m[NP], lp[NP], o[NP], alpha_prev[NP];
+#pragma unroll
+            for (int h = 0; h < NP; ++h) { m[h] = -INFINITY; lp[h] = 0.f; o[h] = 0.f; alpha_prev[h] = 1.f; }
+
+            auto fold = [&](uint32_t k) {
+                if (!mbar_wait(&bars[F_OF + (k & 1)], (k >> 1) & 1, abort_sh, a.wait_ns)) fail(a, abort_sh, PA_ERR_TIMEOUT);
+                tc_fence_after();
+                uint32_t rh[NP], rl[NP];
+                tmem_ld_cols<NP>(tbase + lane_addr + f8_o_col(k & 1), rh);
+                tmem_ld_cols<NP>(tbase + lane_addr + f8_o_col(k & 1) + 16, rl);
+                tmem_ld_wait();
+                reg_fence(rh);
+                reg_fence(rl);
+#pragma unroll
+                for (int h = 0; h < NP; ++h)
+                    o[h] = fmaf(o[h], alpha_prev[h], (__uint_as_float(rh[h]) + __uint_as_float(rl[h])) * (1.f / 256.f));
+            };
+
+            for (int t = 0; t < ntiles; ++t, ++g) {
+                const int pa0 = it.p0 + 2 * t;
+                const int npg = min(2, it.p1 - pa0);
+                const int key = pa0 * kPage + row;
+                const bool valid = row < npg * kPage && key < key_end;
+                if (!mbar_wait(&bars[F_SF + (g & 1)], (g >> 1) & 1, abort_sh, a.wait_ns))
+                    fail(a, abort_sh, PA_ERR_TIMEOUT);
+                tc_fence_after();
+                uint32_t sr[NP];
+                tmem_ld_cols<NP>(tbase + lane_addr + f8_s_col(g & 1), sr);
+                tmem_ld_wait();
+                reg_fence(sr);
+                float x[NP];
+#pragma unroll
+                for (int h = 0; h < NP; ++h) x[h] = valid ? __uint_as_float(sr[h]) * sl2[h] : -INFINITY;
+                const float wmax = warp_xreduce<NP, true>(x, lane);
+                float* rb = red + (g & 1) * 64;
+                if (writer) rb[hl * 4 + q4] = wmax;
+                if (softmax_bar_or(*abort_sh != 0)) { aborted = true; break; }
+                float alpha[NP];
+#pragma unroll
+                for (int h = 0; h < NP; ++h) {
+                    const float4 r4 = reinterpret_cast<const float4*>(rb)[h];
+                    const float mt = fmaxf(fmaxf(r4.x, r4.y), fmaxf(r4.z, r4.w));
+                    const float mn = fmaxf(m[h], mt);
+                    const bool none = mn == -INFINITY;
+                    alpha[h] = none ? 1.f : exp2f(m[h] - mn);
+                    x[h] = (none || h >= G) ? 0.f : exp2f(x[h] - mn);
+                    lp[h] = fmaf(lp[h], alpha[h], x[h]);
+                    m[h] = mn;
+                }
+                // P * 256 as two e4m3 levels; this key's row: bytes 0-15 hi, 16-31 lo
+                uint32_t hw[4] = {0u, 0u, 0u, 0u}, lw[4] = {0u, 0u, 0u, 0u};
+#pragma unroll
+                for (int h = 0; h < NP; h += 2) {
+                    const float p0 = x[h] * 256.f, p1 = x[h + 1] * 256.f;
+                    const uint32_t hb = e4m3x2(p0, p1);
+                    const float2 back = e4m3x2_to_f2(hb);
+                    const uint32_t lb = e4m3x2(p0 - back.x, p1 - back.y);
+                    hw[h >> 2] |= hb << ((h & 2) * 8);
+                    lw[h >> 2] |= lb << ((h & 2) * 8);
+                }
+                uint8_t* pb = sm + L::kPOff + (g & 1) * L::kPBytes + row * 128;
+                *reinterpret_cast<uint4*>(pb + ((0 ^ (row & 7)) << 4)) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
+                *reinterpret_cast<uint4*>(pb + ((1 ^ (row & 7)) << 4)) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
+                if (!valid) {
+                    // a dead key's V row may hold anything (NaN included): zero it
+                    const int stage = g % kF8Stages;
+                    mbar_wait(&bars[F_FULL + stage], (g / kF8Stages) & 1, abort_sh, a.wait_ns);
+                    uint8_t* vr = sm + stage * L::kStageBytes + 16384 + (row >> 6) * 8192 + (row & 63) * 128;
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) *reinterpret_cast<uint4*>(vr + i * 16) = make_uint4(0, 0, 0, 0);
+                }
+                fence_proxy_async_smem();
+                tc_fence_before();
+                mbar_arrive(&bars[F_PF + (g & 1)]);
+                if (t > 0) fold(g - 1);
+#pragma unroll
+                for (int h = 0; h < NP; ++h) alpha_prev[h] = alpha[h];
+            }
+            if (aborted) break;
+            fold(g - 1);
+            tc_fence_before();
+
+            const float wsum = warp_xreduce<NP, false>(lp, lane);
+            float* rl = red + 128 + (qi & 1) * 64;
+            if (writer) rl[hl * 4 + q4] = wsum;
+            if (softmax_bar_or(*abort_sh != 0)) { aborted = true; break; }
+            const float vs = __ldg(&a.v_scale[it.kvh]);
+            float mine_m = 0.f, mine_l = 0.f;
+#pragma unroll
+            for (int h = 0; h < NP; ++h) {
+                const float4 r4 = reinterpret_cast<const float4*>(rl)[h];
+                const float l = (r4.x + r4.y) + (r4.z + r4.w);
+                if (h == row) { mine_m = m[h]; mine_l = l; }
+                if (h < G) {
+                    const float val = l > 0.f ? o[h] * (vs / l) : 0.f;
+                    if (partial) a.o_part[(orow + h) * D + row] = val;
+                    else a.out[(orow + h) * D + row] = __bfloat16_as_ushort(__float2bfloat16_rn(val));
+                }
+            }
+            if (row < G) {
+                const float lse = mine_l > 0.f ? (mine_m + log2f(mine_l)) * kLn2 : -INFINITY;
+                if (partial) a.lse_part[orow + row] = lse;
+                else if (a.lse) a.lse[orow + row] = lse;
+            }
+        }
+        tc_fence_before();
+    }
+
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tbase, 128);
+    }
+}
+
+template <int NP>
+cudaError_t launch_f8_np(const DecodeArgs& a, const CUtensorMap* mk, const CUtensorMap* mv, int grid,
+                         cudaStream_t stream) {
+    static bool configured = false;
+    if (!configured) {
+        cudaError_t e =
+            cudaFuncSetAttribute(decode_f8_kernel<NP>, cudaFuncAttributeMaxDynamicSharedMemorySize, F8Layout::kSmem);
+        if (e != cudaSuccess) return e;
+        configured = true;
+    }
+    decode_f8_kernel<NP><<<grid, 192, F8Layout::kSmem, stream>>>(a, *mk, *mv);
+    return cudaGetLastError();
+}
+
 // Merge split partials: L = m + ln sum_s exp(lse_s - m), out = sum_s exp(lse_s - L) o_s.
 // One warp per (sequence, query head); sequences with one split were written
 // directly by the decode kernel and are skipped.
@@ -714,8 +1143,12 @@ cudaError_t launch_decode_t(const DecodeArgs& a, const CUtensorMap* mk, const CU
 
 cudaError_t launch_decode(int head_dim, bool fp8, const DecodeArgs& a, const CUtensorMap* mk, const CUtensorMap* mv,
                           int grid, cudaStream_t stream) {
-    if (head_dim == 128) return fp8 ? launch_decode_t<128, true>(a, mk, mv, grid, stream)
-                                    : launch_decode_t<128, false>(a, mk, mv, grid, stream);
+    if (head_dim == 128 && fp8) {
+        if (a.group <= 4) return launch_f8_np<4>(a, mk, mv, grid, stream);
+        if (a.group <= 8) return launch_f8_np<8>(a, mk, mv, grid, stream);
+        return launch_f8_np<16>(a, mk, mv, grid, stream);
+    }
+    if (head_dim == 128) return launch_decode_t<128, false>(a, mk, mv, grid, stream);
     return fp8 ? launch_decode_t<64, true>(a, mk, mv, grid, stream) : launch_decode_t<64, false>(a, mk, mv, grid, stream);
 }
 

@@ -60,8 +60,17 @@ EncodeTiledFn encode_fn() {
 
 // Tiled map over a bf16 tensor of `rank` dims (innermost first), box of 64
 // elements (128 bytes) innermost, 128-byte swizzle.
+pa_status make_map(CUtensorMapDataType dtype, CUtensorMap* map, const void* base, int rank, const uint64_t* dims,
+                   const uint64_t* strides_bytes, const uint32_t* box);
+
 pa_status make_map_bf16(CUtensorMap* map, const void* base, int rank, const uint64_t* dims, const uint64_t* strides_bytes,
                         const uint32_t* box) {
+    return make_map(CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, map, base, rank, dims, strides_bytes, box);
+}
+
+// Tiled map, 128-byte swizzle (the box's inner extent is 128 bytes).
+pa_status make_map(CUtensorMapDataType dtype, CUtensorMap* map, const void* base, int rank, const uint64_t* dims,
+                   const uint64_t* strides_bytes, const uint32_t* box) {
     EncodeTiledFn enc = encode_fn();
     if (!enc) return fail(PA_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
     cuuint64_t d[5], s[4];
@@ -72,7 +81,7 @@ pa_status make_map_bf16(CUtensorMap* map, const void* base, int rank, const uint
         e[i] = 1;
         if (i + 1 < rank) s[i] = strides_bytes[i];
     }
-    CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, rank, const_cast<void*>(base), d, s, b, e,
+    CUresult r = enc(map, dtype, rank, const_cast<void*>(base), d, s, b, e,
                      CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                      CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (r != CUDA_SUCCESS) return fail(PA_ERR_INVALID_ARG, "cuTensorMapEncodeTiled failed (CUresult %d)", (int)r);
@@ -303,6 +312,15 @@ pa_status pa_decode_attend(const pa_decode_shapes* sh, const pa_decode_plan* pla
         st = make_map_bf16(&mk, k_pool, 2, dims, strides, box);
         if (st != PA_OK) return st;
         st = make_map_bf16(&mv, v_pool, 2, dims, strides, box);
+        if (st != PA_OK) return st;
+    } else if (D == 128) {
+        // e4m3 pages: one 128-byte row per key, one box per 64-row page slab
+        const uint64_t dims[2] = {128, (uint64_t)sh->num_pool_pages * Hk * pa::kPage};
+        const uint64_t strides[1] = {128};
+        const uint32_t box[2] = {128, 64};
+        st = make_map(CU_TENSOR_MAP_DATA_TYPE_UINT8, &mk, k_pool, 2, dims, strides, box);
+        if (st != PA_OK) return st;
+        st = make_map(CU_TENSOR_MAP_DATA_TYPE_UINT8, &mv, v_pool, 2, dims, strides, box);
         if (st != PA_OK) return st;
     }
     cudaError_t e = pa::launch_decode(D, fp8, a, &mk, &mv, plan->grid, stream);

@@ -164,6 +164,16 @@ __device__ __forceinline__ void mma_ss(uint32_t d_tmem, uint64_t a_desc, uint64_
         : "memory");
 }
 
+// D[tmem] (+)= A[smem desc] * B[smem desc]; kind::f8f6f4 (here: e4m3 x e4m3, f32 accumulate, K = 32)
+__device__ __forceinline__ void mma_f8_ss(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                          uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
 // D[tmem] (+)= A[tmem] * B[smem desc]
 __device__ __forceinline__ void mma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,
                                        uint32_t accumulate) {
@@ -322,12 +332,24 @@ __host__ __device__ constexpr uint32_t idesc_f16(int M, int N, bool bf16, bool a
            (static_cast<uint32_t>(M >> 4) << 24);
 }
 
+// Instruction descriptor, kind::f8f6f4 with e4m3 A and B (format 0) and an f32 accumulator.
+__host__ __device__ constexpr uint32_t idesc_e4m3(int M, int N, bool a_mn_major, bool b_mn_major) {
+    return (1u << 4) | ((a_mn_major ? 1u : 0u) << 15) | ((b_mn_major ? 1u : 0u) << 16) |
+           (static_cast<uint32_t>(N >> 3) << 17) | (static_cast<uint32_t>(M >> 4) << 24);
+}
+
 // Byte offset of element (row, col) inside a K-major, 128-byte-swizzled tile
 // of 16-bit elements whose rows are 64 elements (128 bytes) wide: one 8-row x
 // 128-byte atom per 1024 bytes, 16-byte chunks XOR-ed with (row % 8).
 __host__ __device__ __forceinline__ uint32_t sw128_offset(uint32_t row, uint32_t col16) {
     const uint32_t chunk = col16 >> 3;  // 8 elements of 2 bytes per 16-byte chunk
     return row * 128u + (((chunk ^ (row & 7u)) << 4) | ((col16 & 7u) << 1));
+}
+
+// Byte offset of byte `col` of row `row` in a 128-byte-swizzled tile of 8-bit
+// elements (128 per row, 1024-byte atoms of 8 rows).
+__host__ __device__ __forceinline__ uint32_t sw128_offset8(uint32_t row, uint32_t col) {
+    return row * 128u + ((((col >> 4) ^ (row & 7u)) << 4) | (col & 15u));
 }
 
 }  // namespace pa
