@@ -6,10 +6,11 @@ D=128, bf16 KV in 64-row pages, seq_lens uniform in [1, 4096], seed 0.  The
 metric is decode KV-read bandwidth: the K+V page bytes the step must read
 (sum_b ceil(len_b/64) * 64 * Hk * D * 2 bytes * 2) per second.
 
-One step = one pass of the decode hot path over the batch: the split-KV
-attention kernel and the log-sum-exp combine (the host scheduler's metadata
-is an input resident in HBM, as in serving where one schedule serves every
-layer; the end-to-end number recomputes it every step).
+One step = one pass of the decode hot path over the batch: pa_decode, whose
+single kernel gathers the pages, attends and merges the split-KV partials
+(the host scheduler's metadata is an input resident in HBM, as in serving
+where one schedule serves every layer; the end-to-end number recomputes it
+every step).
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
   python bench.py --impl reference ...   # the fp64 CPU oracle as the reference arm
@@ -332,26 +333,21 @@ def run_decode(args, rank, world, local_rank, dist):
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream(dev)
     sh, plan = p.shapes, p.plan
-    combine = plan.total_splits > inp.batch
 
-    def attend():
-        B.pa_decode_attend(sh, plan, q, kp, vp, ks, vs, bt, sl, p.meta_dev, inp.scale, out, lse, p.workspace,
-                           stream=stream)
-
-    def comb():
-        B.pa_decode_combine(sh, plan, p.meta_dev, out, lse, p.workspace, stream=stream)
+    def step_call():
+        B.pa_decode(sh, plan, q, kp, vp, ks, vs, bt, sl, p.meta_dev, inp.scale, out, lse, p.workspace,
+                    stream=stream)
 
     for _ in range(args.warmup):
         flush.zero_()
-        attend()
-        comb()
+        step_call()
     torch.cuda.synchronize(dev)
     st = B.pa_check_status(p.workspace, stream)
     if st != B.PA_OK:
         raise RuntimeError(f"device status {st}: {B.pa_last_error()}")
 
     K = args.steps
-    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(K)]
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(K)]
     if dist is not None:
         dist.barrier()
     torch.cuda.synchronize(dev)
@@ -359,17 +355,14 @@ def run_decode(args, rank, world, local_rank, dist):
         for i in range(K):
             flush.zero_()  # L2 flush between timed iterations (outside the events)
             ev[i][0].record(stream)
-            attend()
+            step_call()  # one launch: decode with the split merge fused in
             ev[i][1].record(stream)
-            comb()
-            ev[i][2].record(stream)
         torch.cuda.synchronize(dev)
     if dist is not None:
         dist.barrier()
-    attend_ms = [ev[i][0].elapsed_time(ev[i][1]) for i in range(K)]
-    step_ms = [ev[i][0].elapsed_time(ev[i][2]) for i in range(K)]
+    step_ms = [ev[i][0].elapsed_time(ev[i][1]) for i in range(K)]
     ms = sum(step_ms) / K
-    kern_ms = sum(attend_ms) / K
+    kern_ms = ms
     if dist is not None:
         t = torch.tensor([ms, kern_ms], dtype=torch.float64, device=dev)
         dist.all_reduce(t, op=dist.ReduceOp.MAX)
@@ -399,7 +392,7 @@ def run_decode(args, rank, world, local_rank, dist):
         cpu = {"value": round(gbs, 4), "unit": "GB/s", "cores": oracle.num_threads(), "kind": "oracle",
                "sample": f"{done} sequences of this batch through the fp64 oracle "
                          f"({nbytes / 1e9:.3f} GB of K+V pages, {el:.1f} s)"}
-    launches = K * (1 + int(combine))
+    launches = K
     line = {
         "metric": METRIC, "value": round(value, 1), "unit": "GB/s", "n_gpus": world, "steps": K,
         "warmup": args.warmup, "ms_per_step": round(ms, 5), "higher_is_better": True, "scaling": "weak",

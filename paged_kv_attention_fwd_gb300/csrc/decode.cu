@@ -53,7 +53,9 @@ enum : int {
     B_KHE = 18,    // e4m3: converted K tile consumed
     B_VHF = 19,    // [2] e4m3: converted V tile ready
     B_VHE = 21,    // [2] e4m3: converted V tile consumed
-    B_COUNT = 23
+    B_PW = 23,     // [2] an item's partials written (merge warp)
+    B_HD = 25,     // [2] merge warp done with an item
+    B_COUNT = 27
 };
 
 constexpr uint32_t kTmemCols = 64;
@@ -84,7 +86,8 @@ struct DecodeLayout {
     static constexpr int kGuardEnd = D == 64 ? kLastV + 32768 : 0;
     static constexpr int kBytes = kEnd > kGuardEnd ? kEnd : kGuardEnd;
     static constexpr int kSmem = kBytes + 1024;
-    static constexpr int kThreads = FP8 ? 320 : 192;
+    static constexpr int kMergeWarp = FP8 ? 10 : 6;  // last warp: split merge (pa_decode)
+    static constexpr int kThreads = (kMergeWarp + 1) * 32;
     static_assert(kStages <= 4, "barrier slots");
 };
 
@@ -194,6 +197,81 @@ __device__ __forceinline__ bool softmax_bar_or(bool pred) {
     return r != 0;
 }
 
+
+// Split merge inside the decode kernel (pa_decode).  The softmax threads
+// write an item's partials, then arrive on a barrier; one extra warp -- the
+// merge warp -- takes it from there, off the softmax's critical path: it
+// counts the split's arrival in the workspace (device-scope acquire-release)
+// and, if that arrival completes the sequence's splits, merges them
+//   L = m + ln sum_s exp(lse_s - m),  out = sum_s exp(lse_s - L) o_s
+// and resets the counter for the next call.  Two barrier pairs (written /
+// merged) let the softmax run up to two partial items ahead.
+
+// Softmax side: all 128 threads, after writing partial item number k.
+__device__ __forceinline__ bool partials_written(uint64_t* pw, uint64_t* hd, uint32_t k, volatile int* abort_sh,
+                                                 uint64_t wait_ns) {
+    if (k >= 2 && !mbar_wait(&hd[k & 1], ((k - 2) >> 1) & 1, abort_sh, wait_ns)) return false;
+    mbar_arrive(&pw[k & 1]);
+    return true;
+}
+
+template <int D>
+__device__ void merge_warp(const DecodeArgs& a, int it_lo, int it_hi, int items_off, uint64_t* pw, uint64_t* hd,
+                           volatile int* abort_sh, int lane) {
+    uint32_t k = 0;
+    const int G = a.group;
+    for (int j = it_lo; j < it_hi; ++j) {
+        const Item it = load_item(a, j, items_off);
+        if (it.nsplit <= 1) continue;
+        bool ok = mbar_wait(&pw[k & 1], (k >> 1) & 1, abort_sh, a.wait_ns);
+        ok = __all_sync(0xffffffffu, ok);
+        if (!ok) {
+            if (lane == 0) fail(a, abort_sh, PA_ERR_TIMEOUT);
+            return;
+        }
+        int last = 0;
+        int* ctr = a.counters + (long long)it.b * a.num_kv_heads + it.kvh;
+        if (lane == 0) {
+            int prev;
+            asm volatile("atom.add.acq_rel.gpu.s32 %0, [%1], 1;" : "=r"(prev) : "l"(ctr) : "memory");
+            last = prev == it.nsplit - 1;
+        }
+        last = __shfl_sync(0xffffffffu, last, 0);
+        __syncwarp();
+        if (last) {
+            const long long base = (long long)it.split_base * a.num_q_heads + (long long)it.kvh * G;
+            const long long orow = (long long)it.b * a.num_q_heads + (long long)it.kvh * G;
+            for (int h = 0; h < G; ++h) {
+                float mx = -INFINITY;
+                for (int s = 0; s < it.nsplit; ++s)
+                    mx = fmaxf(mx, __ldcg(&a.lse_part[base + (long long)s * a.num_q_heads + h]));
+                float acc[D / 32];
+#pragma unroll
+                for (int i = 0; i < D / 32; ++i) acc[i] = 0.f;
+                float wsum = 0.f;
+                if (mx != -INFINITY) {
+                    for (int s = 0; s < it.nsplit; ++s) {
+                        const long long prow = base + (long long)s * a.num_q_heads + h;
+                        const float w = __expf(__ldcg(&a.lse_part[prow]) - mx);
+                        wsum += w;
+#pragma unroll
+                        for (int i = 0; i < D / 32; ++i) acc[i] = fmaf(w, __ldcg(&a.o_part[prow * D + lane + 32 * i]), acc[i]);
+                    }
+                }
+                const float inv = wsum > 0.f ? 1.f / wsum : 0.f;
+#pragma unroll
+                for (int i = 0; i < D / 32; ++i)
+                    a.out[(orow + h) * D + lane + 32 * i] = __bfloat16_as_ushort(__float2bfloat16_rn(acc[i] * inv));
+                if (lane == 0 && a.lse) a.lse[orow + h] = wsum > 0.f ? mx + __logf(wsum) : -INFINITY;
+            }
+            if (lane == 0) *ctr = 0;
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&hd[k & 1]);
+        ++k;
+    }
+}
+
 __device__ __forceinline__ uint16_t f32_to_16(float x, bool f16) {
     if (f16) return __half_as_ushort(__float2half_rn(x));
     return __bfloat16_as_ushort(__float2bfloat16_rn(x));
@@ -237,6 +315,10 @@ __global__ void __launch_bounds__(DecodeLayout<D, FP8>::kThreads, 1)
         mbar_init(&bars[B_DONE], 1);
         mbar_init(&bars[B_KHF], 128);
         mbar_init(&bars[B_KHE], 1);
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(&bars[B_PW + i], 128);
+            mbar_init(&bars[B_HD + i], 1);
+        }
         *abort_sh = 0;
         fence_barrier_init();
     }
@@ -432,7 +514,7 @@ __global__ void __launch_bounds__(DecodeLayout<D, FP8>::kThreads, 1)
             qload = next_nonempty(qload + 1);
         }
 
-        uint32_t g = 0, qi = 0;
+        uint32_t g = 0, qi = 0, npartial = 0;
         bool aborted = false;
         for (int j = it_lo; j < it_hi && !aborted; ++j) {
             const Item it = load_item(a, j, items_off);
@@ -452,6 +534,13 @@ __global__ void __launch_bounds__(DecodeLayout<D, FP8>::kThreads, 1)
                 if (row < G) {
                     if (partial) a.lse_part[orow + row] = -INFINITY;
                     else if (a.lse) a.lse[orow + row] = -INFINITY;
+                }
+                if (partial && a.counters) {
+                    if (!partials_written(&bars[B_PW], &bars[B_HD], npartial++, abort_sh, a.wait_ns)) {
+                        fail(a, abort_sh, PA_ERR_TIMEOUT);
+                        aborted = true;
+                        break;
+                    }
                 }
                 continue;
             }
@@ -558,8 +647,18 @@ __global__ void __launch_bounds__(DecodeLayout<D, FP8>::kThreads, 1)
                 if (partial) a.lse_part[orow + row] = lse;
                 else if (a.lse) a.lse[orow + row] = lse;
             }
+            if (partial && a.counters) {
+                if (!partials_written(&bars[B_PW], &bars[B_HD], npartial++, abort_sh, a.wait_ns)) {
+                    fail(a, abort_sh, PA_ERR_TIMEOUT);
+                    aborted = true;
+                    break;
+                }
+            }
         }
         tc_fence_before();
+    } else if (warp == L::kMergeWarp) {
+        // ------------------------------------------------------------ split merge
+        if (a.counters) merge_warp<D>(a, it_lo, it_hi, items_off, &bars[B_PW], &bars[B_HD], abort_sh, lane);
     } else {
         // ------------------------------------------------------------ e4m3 -> f16 converters
         if constexpr (FP8) {
@@ -661,7 +760,9 @@ struct F8Layout {
 static_assert(F8Layout::kQ3Off % 1024 == 0 && F8Layout::kPOff % 1024 == 0, "swizzle atoms need 1024-byte alignment");
 static_assert(F8Layout::kSmem <= 232448, "shared memory per CTA");
 
-enum : int { F_FULL = 0, F_EMPTY = 5, F_QF = 10, F_SF = 12, F_PF = 14, F_OF = 16, F_DONE = 18, F_COUNT = 19 };
+enum : int {
+    F_FULL = 0, F_EMPTY = 5, F_QF = 10, F_SF = 12, F_PF = 14, F_OF = 16, F_DONE = 18, F_PW = 19, F_HD = 21, F_COUNT = 23
+};
 __host__ __device__ constexpr uint32_t f8_s_col(uint32_t b) { return b * 16u; }
 __host__ __device__ constexpr uint32_t f8_o_col(uint32_t b) { return 32u + b * 32u; }
 
@@ -677,7 +778,7 @@ __device__ __forceinline__ float2 e4m3x2_to_f2(uint32_t v) {
 }
 
 template <int NP>
-__global__ void __launch_bounds__(192, 1)
+__global__ void __launch_bounds__(224, 1)
     decode_f8_kernel(const __grid_constant__ DecodeArgs a, const __grid_constant__ CUtensorMap map_k,
                      const __grid_constant__ CUtensorMap map_v) {
     using L = F8Layout;
@@ -708,6 +809,8 @@ __global__ void __launch_bounds__(192, 1)
             mbar_init(&bars[F_SF + i], 1);
             mbar_init(&bars[F_PF + i], 128);
             mbar_init(&bars[F_OF + i], 1);
+            mbar_init(&bars[F_PW + i], 128);
+            mbar_init(&bars[F_HD + i], 1);
         }
         mbar_init(&bars[F_DONE], 1);
         *abort_sh = 0;
@@ -828,6 +931,9 @@ __global__ void __launch_bounds__(192, 1)
             mma_commit(&bars[F_DONE]);
             mbar_wait(&bars[F_DONE], 0, nullptr, a.wait_ns);
         }
+    } else if (warp == 6) {
+        // ------------------------------------------------------------ split merge
+        if (a.counters) merge_warp<D>(a, it_lo, it_hi, items_off, &bars[F_PW], &bars[F_HD], abort_sh, lane);
     } else {
         // ------------------------------------------------------------ softmax
         const int q4 = warp & 3;
@@ -905,7 +1011,7 @@ __global__ void __launch_bounds__(192, 1)
         }
         named_bar_sync(1, 128);  // query scales of the first items visible to all
 
-        uint32_t g = 0, qi = 0;
+        uint32_t g = 0, qi = 0, npartial = 0;
         bool aborted = false;
         for (int j = it_lo; j < it_hi && !aborted; ++j) {
             const Item it = load_item(a, j, items_off);
@@ -922,6 +1028,13 @@ __global__ void __launch_bounds__(192, 1)
                 if (row < G) {
                     if (partial) a.lse_part[orow + row] = -INFINITY;
                     else if (a.lse) a.lse[orow + row] = -INFINITY;
+                }
+                if (partial && a.counters) {
+                    if (!partials_written(&bars[F_PW], &bars[F_HD], npartial++, abort_sh, a.wait_ns)) {
+                        fail(a, abort_sh, PA_ERR_TIMEOUT);
+                        aborted = true;
+                        break;
+                    }
                 }
                 continue;
             }
@@ -1039,6 +1152,13 @@ __global__ void __launch_bounds__(192, 1)
                 if (partial) a.lse_part[orow + row] = lse;
                 else if (a.lse) a.lse[orow + row] = lse;
             }
+            if (partial && a.counters) {
+                if (!partials_written(&bars[F_PW], &bars[F_HD], npartial++, abort_sh, a.wait_ns)) {
+                    fail(a, abort_sh, PA_ERR_TIMEOUT);
+                    aborted = true;
+                    break;
+                }
+            }
         }
         tc_fence_before();
     }
@@ -1060,7 +1180,7 @@ cudaError_t launch_f8_np(const DecodeArgs& a, const CUtensorMap* mk, const CUten
         if (e != cudaSuccess) return e;
         configured = true;
     }
-    decode_f8_kernel<NP><<<grid, 192, F8Layout::kSmem, stream>>>(a, *mk, *mv);
+    decode_f8_kernel<NP><<<grid, 224, F8Layout::kSmem, stream>>>(a, *mk, *mv);
     return cudaGetLastError();
 }
 

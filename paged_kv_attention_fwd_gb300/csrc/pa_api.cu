@@ -178,7 +178,8 @@ pa_status pa_get_metadata(const int32_t* seq_lens_host, const int32_t* block_tab
     plan->reserved = 0;
     const int64_t hq = std::max(sh->num_q_heads, 0), d = std::max(sh->head_dim, 0);
     plan->workspace_bytes = (size_t)PA_STATUS_BYTES + (size_t)(total_splits * hq * d * 4) +
-                            (size_t)(((total_splits * hq * 4) + 255) / 256 * 256);
+                            (size_t)(((total_splits * hq * 4) + 255) / 256 * 256) +
+                            (size_t)((((int64_t)B * Hk * 4) + 255) / 256 * 256);
     if (!meta_host) return PA_OK;
     if (meta_capacity_ints < (size_t)meta_ints)
         return fail(PA_ERR_WORKSPACE, "metadata needs %lld int32 entries, capacity is %zu", (long long)meta_ints,
@@ -257,11 +258,27 @@ float* partial_o(void* workspace) {
 
 }  // namespace
 
+namespace {
+pa_status decode_launch(bool fused, const pa_decode_shapes* sh, const pa_decode_plan* plan, const void* q,
+                        const void* k_pool, const void* v_pool, const float* k_scale, const float* v_scale,
+                        const int32_t* block_table, const int32_t* seq_lens, const int32_t* meta_dev, float scale,
+                        void* out, float* lse, void* workspace, size_t workspace_bytes, cudaStream_t stream);
+}
+
 pa_status pa_decode_attend(const pa_decode_shapes* sh, const pa_decode_plan* plan, const void* q,
                            const void* k_pool, const void* v_pool, const float* k_scale, const float* v_scale,
                            const int32_t* block_table, const int32_t* seq_lens, const int32_t* meta_dev,
                            float scale, void* out, float* lse, void* workspace, size_t workspace_bytes,
                            cudaStream_t stream) {
+    return decode_launch(false, sh, plan, q, k_pool, v_pool, k_scale, v_scale, block_table, seq_lens, meta_dev,
+                         scale, out, lse, workspace, workspace_bytes, stream);
+}
+
+namespace {
+pa_status decode_launch(bool fused, const pa_decode_shapes* sh, const pa_decode_plan* plan, const void* q,
+                        const void* k_pool, const void* v_pool, const float* k_scale, const float* v_scale,
+                        const int32_t* block_table, const int32_t* seq_lens, const int32_t* meta_dev, float scale,
+                        void* out, float* lse, void* workspace, size_t workspace_bytes, cudaStream_t stream) {
     pa_status st = validate_decode_common(sh, plan, out, meta_dev, workspace, workspace_bytes);
     if (st != PA_OK || sh->batch == 0) return st;
     const int B = sh->batch, Hq = sh->num_q_heads, Hk = sh->num_kv_heads, D = sh->head_dim;
@@ -293,6 +310,12 @@ pa_status pa_decode_attend(const pa_decode_shapes* sh, const pa_decode_plan* pla
     a.status = static_cast<int*>(workspace);
     a.o_part = partial_o(workspace);
     a.lse_part = a.o_part + (size_t)plan->total_splits * Hq * D;
+    {
+        const size_t lse_bytes = ((size_t)plan->total_splits * Hq * 4 + 255) / 256 * 256;
+        int* ctr = reinterpret_cast<int*>(reinterpret_cast<uint8_t*>(a.lse_part) + lse_bytes);
+        const size_t need = PA_STATUS_BYTES + (size_t)plan->total_splits * Hq * D * 4 + lse_bytes + (size_t)B * Hk * 4;
+        a.counters = (fused && plan->total_splits > B && workspace_bytes >= need) ? ctr : nullptr;
+    }
     a.batch = B;
     a.num_q_heads = Hq;
     a.num_kv_heads = Hk;
@@ -325,8 +348,13 @@ pa_status pa_decode_attend(const pa_decode_shapes* sh, const pa_decode_plan* pla
     }
     cudaError_t e = pa::launch_decode(D, fp8, a, &mk, &mv, plan->grid, stream);
     if (e != cudaSuccess) return cuda_fail(e, "decode launch");
+    if (fused && plan->total_splits > B && !a.counters) {
+        // no room for the arrival counters: merge in a second kernel
+        return pa_decode_combine(sh, plan, meta_dev, out, lse, workspace, workspace_bytes, stream);
+    }
     return PA_OK;
 }
+}  // namespace
 
 pa_status pa_decode_combine(const pa_decode_shapes* sh, const pa_decode_plan* plan, const int32_t* meta_dev,
                             void* out, float* lse, void* workspace, size_t workspace_bytes, cudaStream_t stream) {
@@ -351,10 +379,8 @@ pa_status pa_decode(const pa_decode_shapes* sh, const pa_decode_plan* plan, cons
                     const void* v_pool, const float* k_scale, const float* v_scale, const int32_t* block_table,
                     const int32_t* seq_lens, const int32_t* meta_dev, float scale, void* out, float* lse,
                     void* workspace, size_t workspace_bytes, cudaStream_t stream) {
-    pa_status st = pa_decode_attend(sh, plan, q, k_pool, v_pool, k_scale, v_scale, block_table, seq_lens, meta_dev,
-                                    scale, out, lse, workspace, workspace_bytes, stream);
-    if (st != PA_OK) return st;
-    return pa_decode_combine(sh, plan, meta_dev, out, lse, workspace, workspace_bytes, stream);
+    return decode_launch(true, sh, plan, q, k_pool, v_pool, k_scale, v_scale, block_table, seq_lens, meta_dev,
+                         scale, out, lse, workspace, workspace_bytes, stream);
 }
 
 pa_status pa_prefill(const pa_prefill_shapes* sh, const void* q, const void* k, const void* v, const void* k_rope,

@@ -29,6 +29,7 @@ struct DecodeArgs {
     float* o_part;             // fp32 [total_splits, Hq, D]
     float* lse_part;           // fp32 [total_splits, Hq]
     int* status;               // status word
+    int* counters;             // [B * Hk] split arrivals (fused combine), or nullptr: leave partials
     int32_t batch, num_q_heads, num_kv_heads, group, max_pages, num_pool_pages;
     float scale_log2;          // softmax scale * log2(e)
     uint64_t wait_ns;

@@ -190,3 +190,27 @@ def test_bounded_wait_times_out_cleanly():
     inp = W.tiny_decode(0)
     out, lse, st, _ = run(inp)
     assert st == B.PA_OK
+
+
+@pytest.mark.parametrize("kv_dtype", ["bf16", "e4m3"])
+def test_fused_merge_matches_two_kernel_form(kv_dtype):
+    """pa_decode merges split partials inside its kernel; pa_decode_attend +
+    pa_decode_combine do it in a second kernel.  Same results, and the fused
+    form leaves its arrival counters at zero for the next call."""
+    inp = W.make_decode(12, 32, 8, 128, W.uniform_lengths(13, 12, 1, 4096), seed=13, kv_dtype=kv_dtype)
+    q, kp, vp, bt, sl, ks, vs = to_dev(inp)
+    p = ops.plan_decode(inp.seq_lens, inp.block_table, 32, 8, 128, inp.max_pages, inp.num_pool_pages, kv_dtype,
+                        forced_splits=5)
+    assert p.plan.total_splits > inp.batch
+    for _ in range(2):  # twice: the counters must have been reset by the first call
+        o1, l1 = ops.decode(p, q, kp, vp, bt, sl, inp.scale, ks, vs)
+        assert B.pa_check_status(p.workspace) == B.PA_OK
+        o2 = torch.empty_like(o1)
+        l2 = torch.empty_like(l1)
+        B.pa_decode_attend(p.shapes, p.plan, q, kp, vp, ks, vs, bt, sl, p.meta_dev, inp.scale, o2, l2, p.workspace)
+        B.pa_decode_combine(p.shapes, p.plan, p.meta_dev, o2, l2, p.workspace)
+        assert B.pa_check_status(p.workspace) == B.PA_OK
+        assert (o1.float() - o2.float()).abs().max().item() <= 1e-2
+        assert (l1 - l2).abs().max().item() <= 1e-5
+    ref_out, ref_lse = reference(inp)
+    assert_close(o1.float().cpu().numpy(), l1.cpu().numpy(), ref_out, ref_lse, kv_dtype)
