@@ -278,6 +278,24 @@ def run_reference(args):
         return
     import oracle
     cores = oracle.num_threads()
+    if args.workload == "append":
+        inp, prefix, qlen, kn, vn, desc = append_workload()
+        for _ in range(args.warmup):
+            oracle.append_kv(kn[:512], vn[:512], W_cu(qlen[:1]), prefix[:1], inp.block_table[:1], inp.k, inp.v)
+        t0 = time.perf_counter()
+        for _ in range(args.steps):
+            oracle.append_kv(kn[:512], vn[:512], W_cu(qlen[:1]), prefix[:1], inp.block_table[:1], inp.k, inp.v)
+        el = time.perf_counter() - t0
+        gbs = args.steps * 4 * 512 * kn.shape[1] * 128 * 2 / el / 1e9
+        line = {"impl": "reference", "metric": METRIC, "value": round(gbs, 4), "unit": "GB/s", "n_gpus": args.gpus,
+                "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(el / args.steps * 1e3, 4),
+                "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+                "data": "synthetic", "config": {"workload": desc, "implementation": "CPU oracle append"},
+                "cpu_baseline": {"value": round(gbs, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
+                                 "sample": "one sequence's 512 new tokens per step"},
+                "e2e": {"value": round(gbs, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+        print(json.dumps(line), flush=True)
+        return
     if args.workload.startswith("prefill"):
         inp, desc = prefill_workload(args.workload)
         tfs, el, rows, flops = cpu_oracle_prefill_sample(inp, steps=args.steps, warmup=args.warmup, rows_per_step=8)
@@ -621,6 +639,128 @@ def prefill_e2e(inp, dev, stream, sh, flops, world, dist, args):
             "includes": "pinned H2D of q, k, v, offsets (+ rope key / block table) + pa_prefill + D2H of out/lse + sync"}
 
 
+def append_workload():
+    """The chunked-prefill workload's new chunk (8 x 512 tokens, 32 KV heads,
+    D=128, bf16) written into its pages after each cached prefix."""
+    from paged_kv_attention_fwd_gb300 import workloads as W
+    inp = W.chunked_prefill(0)
+    prefix = inp.meta["prefix"]
+    qlen = np.diff(inp.cu_seqlens_q).astype(np.int32)
+    kn = W.bf16_normal_fast(0, 90, (int(qlen.sum()), inp.num_kv_heads, 128))
+    vn = W.bf16_normal_fast(0, 91, (int(qlen.sum()), inp.num_kv_heads, 128))
+    desc = ("paged KV append: the chunked-prefill workload's 8 x 512 new tokens, 32 KV heads, D=128, bf16, "
+            "written after cached prefixes U[0,8192] through block_table, seed 0")
+    return inp, prefix, qlen, kn, vn, desc
+
+
+def run_append(args, rank, world, local_rank, dist):
+    import torch
+    from paged_kv_attention_fwd_gb300 import binding as B
+    from paged_kv_attention_fwd_gb300 import ops
+
+    dev = torch.device("cuda", local_rank)
+    torch.cuda.set_device(dev)
+    inp, prefix, qlen, kn, vn, desc = append_workload()
+    T, hk = kn.shape[0], kn.shape[1]
+    nbytes = 4 * T * hk * 128 * 2  # read K and V rows, write K and V rows
+    kp, vp = ops.as_bf16(inp.k, dev), ops.as_bf16(inp.v, dev)
+    knd, vnd = ops.as_bf16(kn, dev), ops.as_bf16(vn, dev)
+    cu = torch.from_numpy(W_cu(qlen)).to(dev)
+    sp = torch.from_numpy(prefix).to(dev)
+    bt = torch.from_numpy(inp.block_table).to(dev)
+    sh = B.pa_append_shapes(batch=len(qlen), num_kv_heads=hk, head_dim=128, page_size=64,
+                            max_pages_per_seq=inp.block_table.shape[1], num_pool_pages=inp.k.shape[0], total_new=T,
+                            kv_dtype=B.PA_KV_BF16)
+    ws = torch.zeros(B.PA_STATUS_BYTES, dtype=torch.uint8, device=dev)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step():
+        B.pa_append_kv(sh, knd, vnd, cu, sp, bt, kp, vp, None, None, ws, stream=stream)
+
+    for _ in range(args.warmup):
+        flush.zero_()
+        step()
+    K = args.steps
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(K)]
+    if dist is not None:
+        dist.barrier()
+    torch.cuda.synchronize(dev)
+    with ClockSampler(gpu_index(local_rank)) as clk:
+        for i in range(K):
+            flush.zero_()
+            ev[i][0].record(stream)
+            step()
+            ev[i][1].record(stream)
+        torch.cuda.synchronize(dev)
+    ms = sum(ev[i][0].elapsed_time(ev[i][1]) for i in range(K)) / K
+    if dist is not None:
+        t = torch.tensor([ms], dtype=torch.float64, device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t[0])
+    if B.pa_check_status(ws, stream) != B.PA_OK:
+        raise RuntimeError(B.pa_last_error())
+    pk, pk_src = peaks()
+    gbs = nbytes / (ms * 1e-3) / 1e9
+    # end to end: new rows from pinned host memory, append, status word back
+    kh = torch.from_numpy(kn.view(np.int16)).pin_memory()
+    vh = torch.from_numpy(vn.view(np.int16)).pin_memory()
+    st_h = torch.empty(1, dtype=torch.int32).pin_memory()
+
+    def e2e_step():
+        knd.view(torch.int16).copy_(kh, non_blocking=True)
+        vnd.view(torch.int16).copy_(vh, non_blocking=True)
+        step()
+        st_h.copy_(ws[:4].view(torch.int32), non_blocking=True)
+        torch.cuda.synchronize(dev)
+
+    for _ in range(3):
+        e2e_step()
+    E = max(3, min(K, args.e2e_steps))
+    t0 = time.perf_counter()
+    for _ in range(E):
+        e2e_step()
+    el = time.perf_counter() - t0
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        import oracle
+        cut = 2  # two sequences of the batch per oracle pass
+        c_new = qlen[:cut]
+        kn_s, vn_s = kn[: int(c_new.sum())], vn[: int(c_new.sum())]
+        t0 = time.perf_counter()
+        n = 0
+        while time.perf_counter() - t0 < min(args.cpu_seconds, 5.0) or n == 0:
+            oracle.append_kv(kn_s, vn_s, W_cu(c_new), prefix[:cut], inp.block_table[:cut], inp.k, inp.v)
+            n += 1
+        cel = time.perf_counter() - t0
+        cb = n * 4 * int(c_new.sum()) * hk * 128 * 2
+        cpu = {"value": round(cb / cel / 1e9, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
+               "sample": f"{n} oracle appends of 2 sequences' new tokens (copies the pools each time; {cel:.1f} s)"}
+    line = {
+        "metric": METRIC, "value": round(world * gbs, 1), "unit": "GB/s", "n_gpus": world, "steps": K,
+        "warmup": args.warmup, "ms_per_step": round(ms, 5), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": desc, "bytes_per_step": nbytes, "l2": "flushed between steps",
+                   "parallelism": f"replicas x{world}"},
+        "roofline": {"bound": "hbm", "achieved": round(gbs, 1), "peak": pk["hbm_gbs"], "unit": "GB/s",
+                     "frac": round(gbs / pk["hbm_gbs"], 4), "traffic": None, "kernel": "append_kernel",
+                     "peak_source": f"{pk_src} (copy bandwidth)", "algorithmic_bytes_per_launch": nbytes,
+                     "kernel_ms": round(ms, 5)},
+        "cpu_baseline": cpu,
+        "e2e": {"value": round(world * nbytes * E / el / 1e9, 2), "unit": "GB/s",
+                "h2d_bytes_per_step": 2 * T * hk * 128 * 2, "d2h_bytes_per_step": 4, "steps": E,
+                "ms_per_step": round(el / E * 1e3, 4)},
+        "gpu_launches": K, "clocks": clk.summary(),
+    }
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
+def W_cu(lengths):
+    from paged_kv_attention_fwd_gb300 import workloads as W
+    return W.cu_seqlens(lengths)
+
+
 # ------------------------------------------------------------------ main
 
 def main():
@@ -630,7 +770,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="decode_gqa",
-                    choices=["decode_gqa", "decode_fp8", "decode_tiny", "prefill_paged", "prefill_mla"])
+                    choices=["decode_gqa", "decode_fp8", "decode_tiny", "prefill_paged", "prefill_mla", "append"])
     ap.add_argument("--e2e-steps", type=int, default=20)
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--no-e2e", action="store_true")
@@ -660,6 +800,8 @@ def main():
         dist.barrier()
     if args.workload.startswith("prefill"):
         run_prefill(args, rank, world, local_rank, dist)
+    elif args.workload == "append":
+        run_append(args, rank, world, local_rank, dist)
     else:
         run_decode(args, rank, world, local_rank, dist)
     if dist is not None:

@@ -249,6 +249,45 @@ pa_status pa_prefill(const pa_prefill_shapes* shapes, const void* q, const void*
  * PA_STATUS_BYTES + 4 * batch * ceil(max_seqlen_q / 256). */
 size_t pa_prefill_workspace_size(const pa_prefill_shapes* shapes);
 
+/* ----------------------------------------------------------------- append */
+
+typedef struct {
+    int32_t batch;             /* B sequences */
+    int32_t num_kv_heads;      /* Hk */
+    int32_t head_dim;          /* D: 64 or 128 */
+    int32_t page_size;         /* must be 64 */
+    int32_t max_pages_per_seq; /* block_table row stride */
+    int32_t num_pool_pages;
+    int32_t total_new;         /* cu_seqlens_new[B] */
+    int32_t kv_dtype;          /* pa_kv_dtype of the pools */
+} pa_append_shapes;
+
+/*
+ * pa_append_kv -- write new tokens' keys and values into their pages, the
+ * step before a chunked prefill ("prefill writes into paged cache", FlashMLA
+ * "Tensor Shapes Reference" section 4).  New token i of sequence b goes to
+ * logical position p = start_pos[b] + i: row p % 64 of page
+ * block_table[b, p / 64] ("Prefill to Cache Mapping").
+ *
+ *   k_new, v_new    bf16 [total_new, Hk, D], ragged by cu_seqlens_new
+ *   cu_seqlens_new  int32 [B+1] running offsets of the new tokens
+ *   start_pos       int32 [B] position of each sequence's first new token (the
+ *                   number of tokens already cached)
+ *   block_table     int32 [B, max_pages_per_seq]; must already list the pages
+ *                   that the new positions fall in
+ *   k_pool, v_pool  [num_pool_pages, Hk, 64, D]: bf16 (values copied bit for
+ *                   bit), or e4m3 with k_scale / v_scale fp32 [Hk]: the stored
+ *                   code is e4m3(x / scale) in fp32, nearest even, saturating
+ *   workspace       >= PA_STATUS_BYTES (status word)
+ * A position outside the block table or a page id outside the pool is skipped
+ * and recorded as PA_ERR_DEVICE_BOUNDS.  Rows of different calls or tokens
+ * must not collide (two writers to one row race).
+ */
+pa_status pa_append_kv(const pa_append_shapes* shapes, const void* k_new, const void* v_new,
+                       const int32_t* cu_seqlens_new, const int32_t* start_pos, const int32_t* block_table,
+                       void* k_pool, void* v_pool, const float* k_scale, const float* v_scale, void* workspace,
+                       size_t workspace_bytes, cudaStream_t stream);
+
 /* ----------------------------------------------------------------- status */
 
 /*

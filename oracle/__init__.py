@@ -43,6 +43,10 @@ def _load():
         lib.oracle_bf16_to_double.restype = dbl
         lib.oracle_e4m3_to_double.argtypes = [ctypes.c_uint8]
         lib.oracle_e4m3_to_double.restype = dbl
+        lib.oracle_e4m3_from_float.argtypes = [ctypes.c_float]
+        lib.oracle_e4m3_from_float.restype = ctypes.c_uint8
+        lib.oracle_append_kv.argtypes = [i32, i32, i32, i32, i64, i32, P, P, P, P, P, P, P, P, P]
+        lib.oracle_append_kv.restype = i32
         lib.oracle_num_threads.restype = i32
         lib.oracle_set_num_threads.argtypes = [i32]
         _lib = lib
@@ -134,3 +138,29 @@ def prefill(q, k, v, cu_seqlens_q, cu_seqlens_k, scale: float, causal: bool = Tr
     if rr is None:
         return out.reshape(total_q, Hq, Dv), lse.reshape(total_q, Hq)
     return out, lse
+
+
+def e4m3_from_f32(x) -> np.ndarray:
+    """The oracle's own float -> e4m3 encoder (nearest-even, saturating)."""
+    lib = _load()
+    flat = np.asarray(x, dtype=np.float32).ravel()
+    return np.array([lib.oracle_e4m3_from_float(float(v)) for v in flat], dtype=np.uint8).reshape(np.shape(x))
+
+
+def append_kv(k_new, v_new, cu_new, start_pos, block_table, k_pool, v_pool, k_scale=None, v_scale=None):
+    """Write new tokens into copies of the pools; returns (k_pool', v_pool').
+    k_new/v_new uint16 bf16 [total_new, Hk, D]; pools [P, Hk, 64, D] uint16
+    (bf16) or uint8 (e4m3, needs k_scale / v_scale float32 [Hk])."""
+    lib = _load()
+    kn, vn = _c(k_new, np.uint16), _c(v_new, np.uint16)
+    kind = 0 if np.asarray(k_pool).dtype == np.uint16 else 1
+    kp = np.array(k_pool, copy=True, order="C")
+    vp = np.array(v_pool, copy=True, order="C")
+    cu, sp, bt = _c(cu_new, np.int32), _c(start_pos, np.int32), _c(block_table, np.int32)
+    ks, vs = _c(k_scale, np.float32), _c(v_scale, np.float32)
+    B = len(cu) - 1
+    rc = lib.oracle_append_kv(B, kp.shape[1], kp.shape[3], bt.shape[1], kp.shape[0], kind, _p(kn), _p(vn),
+                              _p(cu), _p(sp), _p(bt), _p(kp), _p(vp), _p(ks), _p(vs))
+    if rc != 0:
+        raise ValueError("oracle_append_kv: a position falls outside the block table or the pool")
+    return kp, vp

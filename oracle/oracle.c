@@ -251,3 +251,72 @@ int oracle_prefill(int B, int Hq, int Hk, int Dqk, int Dv, int rope_dim, int max
     }
     return bad ? -1 : 0;
 }
+
+/*
+ * float -> OCP FP8 E4M3 ("fn"), rounding to nearest with ties to even and
+ * saturating to +-448 (the largest finite value).  From the format's
+ * definition: sign, 4-bit exponent with bias 7, 3-bit mantissa, subnormals
+ * (exponent field 0: value = mantissa/8 * 2^-6).
+ */
+uint8_t oracle_e4m3_from_float(float x) {
+    uint8_t sign = signbit(x) ? 0x80 : 0x00;
+    double a = fabs((double)x);
+    if (isnan(x)) return 0x7F;
+    if (a >= 448.0) return sign | 0x7E;
+    if (a == 0.0) return sign;
+    int e;
+    frexp(a, &e);      /* a = f * 2^e, f in [0.5, 1): a in [2^(e-1), 2^e) */
+    e -= 1;            /* a in [2^e, 2^(e+1)) */
+    if (e < -6) {      /* subnormal range: multiples of 2^-9 */
+        double m = nearbyint(ldexp(a, 9));  /* default rounding: ties to even */
+        if (m >= 8.0) return sign | 0x08;    /* rounded up to the smallest normal */
+        return sign | (uint8_t)m;
+    }
+    double m = nearbyint(ldexp(a, 3 - e));   /* in [8, 16] */
+    if (m >= 16.0) { m = 8.0; e += 1; }
+    int field = e + 7;
+    int mant = (int)m - 8;
+    if (field > 15 || (field == 15 && mant == 7)) return sign | 0x7E;
+    return sign | (uint8_t)((field << 3) | mant);
+}
+
+/*
+ * Append new tokens' keys and values to their pages: token i of sequence b
+ * (new rows cu_new[b] .. cu_new[b+1]-1) sits at logical position
+ * p = start_pos[b] + i, i.e. row p % 64 of page block_table[b, p / 64]
+ * (FlashMLA "Tensor Shapes Reference", "Prefill to Cache Mapping").
+ *   k_new, v_new  bf16 [total_new, Hk, D]
+ *   pools         [P, Hk, 64, D]: kind 0 bf16 (bits copied), kind 1 e4m3:
+ *                 code = e4m3(float(x) / scale[h]) (fp32 division)
+ * Returns 0, or -1 if a position falls outside the block table or the pool.
+ */
+int oracle_append_kv(int B, int Hk, int D, int max_pages, int64_t num_pages, int kind,
+                     const uint16_t* k_new, const uint16_t* v_new, const int32_t* cu_new,
+                     const int32_t* start_pos, const int32_t* block_table, void* k_pool, void* v_pool,
+                     const float* k_scale, const float* v_scale) {
+    int bad = 0;
+    for (int b = 0; b < B; ++b) {
+        for (int64_t t = cu_new[b]; t < cu_new[b + 1]; ++t) {
+            int64_t p = (int64_t)start_pos[b] + (t - cu_new[b]);
+            if (p < 0 || p / ORACLE_PAGE >= max_pages) { bad = 1; continue; }
+            int64_t page = block_table[(int64_t)b * max_pages + p / ORACLE_PAGE];
+            if (page < 0 || page >= num_pages) { bad = 1; continue; }
+            for (int h = 0; h < Hk; ++h) {
+                int64_t dst = ((page * Hk + h) * ORACLE_PAGE + p % ORACLE_PAGE) * D;
+                int64_t src = (t * Hk + h) * D;
+                for (int d = 0; d < D; ++d) {
+                    if (kind == 0) {
+                        ((uint16_t*)k_pool)[dst + d] = k_new[src + d];
+                        ((uint16_t*)v_pool)[dst + d] = v_new[src + d];
+                    } else {
+                        float kf = (float)oracle_bf16_to_double(k_new[src + d]) / k_scale[h];
+                        float vf = (float)oracle_bf16_to_double(v_new[src + d]) / v_scale[h];
+                        ((uint8_t*)k_pool)[dst + d] = oracle_e4m3_from_float(kf);
+                        ((uint8_t*)v_pool)[dst + d] = oracle_e4m3_from_float(vf);
+                    }
+                }
+            }
+        }
+    }
+    return bad ? -1 : 0;
+}

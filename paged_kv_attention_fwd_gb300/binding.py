@@ -50,6 +50,12 @@ class pa_prefill_shapes(ctypes.Structure):
         "total_q", "total_k", "page_size", "max_pages_per_seq", "num_pool_pages", "num_sms")]
 
 
+class pa_append_shapes(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_int32) for n in (
+        "batch", "num_kv_heads", "head_dim", "page_size", "max_pages_per_seq", "num_pool_pages", "total_new",
+        "kv_dtype")]
+
+
 _lib = None
 _P = ctypes.c_void_p
 
@@ -75,6 +81,8 @@ def lib() -> ctypes.CDLL:
         L.pa_decode_noalloc.restype = ctypes.c_int
         L.pa_prefill.argtypes = [ctypes.POINTER(pa_prefill_shapes), _P, _P, _P, _P, _P, _P, _P, _P, ctypes.c_int,
                                  f32, _P, _P, _P, sz, _P]
+        L.pa_append_kv.argtypes = [ctypes.POINTER(pa_append_shapes), _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, sz, _P]
+        L.pa_append_kv.restype = ctypes.c_int
         L.pa_prefill_workspace_size.argtypes = [ctypes.POINTER(pa_prefill_shapes)]
         L.pa_prefill_workspace_size.restype = ctypes.c_size_t
         L.pa_check_status.argtypes = [_P, _P]
@@ -189,6 +197,15 @@ def pa_prefill(shapes: pa_prefill_shapes, q, k, v, k_rope, cu_seqlens_q, cu_seql
                             _ptr(cu_seqlens_k), _ptr(block_table), _ptr(qo_offset), int(bool(causal)),
                             float(scale), _ptr(out), _ptr(lse), _ptr(workspace), int(workspace_bytes),
                             _stream(stream)))
+
+
+def pa_append_kv(shapes: pa_append_shapes, k_new, v_new, cu_seqlens_new, start_pos, block_table, k_pool, v_pool,
+                 k_scale, v_scale, workspace, workspace_bytes: Optional[int] = None, stream=None) -> None:
+    if workspace_bytes is None:
+        workspace_bytes = workspace.numel() * workspace.element_size()
+    _check(lib().pa_append_kv(ctypes.byref(shapes), _ptr(k_new), _ptr(v_new), _ptr(cu_seqlens_new), _ptr(start_pos),
+                              _ptr(block_table), _ptr(k_pool), _ptr(v_pool), _ptr(k_scale), _ptr(v_scale),
+                              _ptr(workspace), int(workspace_bytes), _stream(stream)))
 
 
 def pa_prefill_workspace_size(shapes: pa_prefill_shapes) -> int:

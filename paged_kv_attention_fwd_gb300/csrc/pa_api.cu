@@ -488,6 +488,52 @@ pa_status pa_prefill(const pa_prefill_shapes* sh, const void* q, const void* k, 
     return PA_OK;
 }
 
+pa_status pa_append_kv(const pa_append_shapes* sh, const void* k_new, const void* v_new,
+                       const int32_t* cu_seqlens_new, const int32_t* start_pos, const int32_t* block_table,
+                       void* k_pool, void* v_pool, const float* k_scale, const float* v_scale, void* workspace,
+                       size_t workspace_bytes, cudaStream_t stream) {
+    if (!sh) return fail(PA_ERR_INVALID_ARG, "shapes must not be NULL");
+    if (sh->batch < 0 || sh->total_new < 0) return fail(PA_ERR_INVALID_ARG, "batch and total_new must be >= 0");
+    if (sh->batch == 0 || sh->total_new == 0) return PA_OK;
+    if (sh->num_kv_heads <= 0) return fail(PA_ERR_INVALID_ARG, "num_kv_heads must be positive");
+    if (sh->head_dim != 64 && sh->head_dim != 128)
+        return fail(PA_ERR_UNSUPPORTED, "head_dim must be 64 or 128 (got %d)", sh->head_dim);
+    if (sh->page_size != pa::kPage) return fail(PA_ERR_INVALID_ARG, "page_size must be 64 (got %d)", sh->page_size);
+    if (sh->max_pages_per_seq <= 0 || sh->num_pool_pages <= 0)
+        return fail(PA_ERR_INVALID_ARG, "max_pages_per_seq and num_pool_pages must be positive");
+    if (sh->kv_dtype != PA_KV_BF16 && sh->kv_dtype != PA_KV_FP8_E4M3)
+        return fail(PA_ERR_INVALID_ARG, "unknown kv_dtype %d", sh->kv_dtype);
+    const bool fp8 = sh->kv_dtype == PA_KV_FP8_E4M3;
+    if (!k_new || !v_new || !cu_seqlens_new || !start_pos || !block_table || !k_pool || !v_pool || !workspace)
+        return fail(PA_ERR_INVALID_ARG, "a required pointer is NULL");
+    if (fp8 && (!k_scale || !v_scale)) return fail(PA_ERR_INVALID_ARG, "e4m3 pools need k_scale and v_scale");
+    if (!aligned16(k_new) || !aligned16(v_new) || !aligned16(k_pool) || !aligned16(v_pool))
+        return fail(PA_ERR_INVALID_ARG, "k_new, v_new and the pools must be 16-byte aligned");
+    if (workspace_bytes < PA_STATUS_BYTES)
+        return fail(PA_ERR_WORKSPACE, "workspace needs %d bytes, got %zu", PA_STATUS_BYTES, workspace_bytes);
+    pa::AppendArgs a;
+    a.k_new = static_cast<const uint16_t*>(k_new);
+    a.v_new = static_cast<const uint16_t*>(v_new);
+    a.cu_new = cu_seqlens_new;
+    a.start_pos = start_pos;
+    a.block_table = block_table;
+    a.k_pool = k_pool;
+    a.v_pool = v_pool;
+    a.k_scale = k_scale;
+    a.v_scale = v_scale;
+    a.status = static_cast<int*>(workspace);
+    a.batch = sh->batch;
+    a.num_kv_heads = sh->num_kv_heads;
+    a.head_dim = sh->head_dim;
+    a.max_pages = sh->max_pages_per_seq;
+    a.num_pool_pages = sh->num_pool_pages;
+    a.total_new = sh->total_new;
+    a.fp8 = fp8;
+    cudaError_t e = pa::launch_append(a, stream);
+    if (e != cudaSuccess) return cuda_fail(e, "append launch");
+    return PA_OK;
+}
+
 size_t pa_prefill_workspace_size(const pa_prefill_shapes* sh) {
     if (!sh || sh->batch <= 0 || sh->max_seqlen_q <= 0) return PA_STATUS_BYTES;
     return PA_STATUS_BYTES + (size_t)sh->batch * (size_t)cdiv(sh->max_seqlen_q, 256) * 4;

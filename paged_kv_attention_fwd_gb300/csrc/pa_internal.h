@@ -71,6 +71,22 @@ cudaError_t launch_prefill(const PrefillArgs& a, int head_dim_qk, const CUtensor
                            const CUtensorMap* map_k, const CUtensorMap* map_v, const CUtensorMap* map_r,
                            cudaStream_t stream);
 
+struct AppendArgs {
+    const uint16_t* k_new;  // bf16 [total_new, Hk, D]
+    const uint16_t* v_new;
+    const int32_t* cu_new;
+    const int32_t* start_pos;
+    const int32_t* block_table;
+    void* k_pool;
+    void* v_pool;
+    const float* k_scale;
+    const float* v_scale;
+    int* status;
+    int32_t batch, num_kv_heads, head_dim, max_pages, num_pool_pages, total_new, fp8;
+};
+
+cudaError_t launch_append(const AppendArgs& a, cudaStream_t stream);
+
 // Record a message for pa_last_error() on this host thread (pa_api.cu).
 void set_last_error(const char* msg);
 

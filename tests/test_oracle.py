@@ -351,3 +351,68 @@ def test_generator_fast_paths_equal_reference_encoders():
     # every head uses its full range: the largest magnitude encodes to +-448
     dec = oracle.e4m3_to_f64(fast.reshape(-1)).reshape(fast.shape)
     assert np.allclose(np.abs(dec).max(axis=(0, 2, 3)), 448.0)
+
+
+# ---------------------------------------------------------------- paged KV append
+
+def test_e4m3_encoder_matches_torch():
+    x = np.concatenate([W.normal_f32(8, 97, 40000) * np.float32(60.0),
+                        np.float32([0.0, -0.0, 448.0, 460.0, 1e-9, 2.0 ** -10, 3 * 2.0 ** -10, 2.0 ** -6 * 0.9375])])
+    xc = np.clip(x, -448, 448)
+    ref = torch.from_numpy(xc).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    got = oracle.e4m3_from_f32(xc)
+    assert np.array_equal(got, ref)
+    assert oracle.e4m3_from_f32(np.float32([1e6, -1e6])).tolist() == [0x7E, 0xFE]  # saturates
+
+
+def _append_case(kv_dtype, seed=40):
+    hk, d = 2, 64
+    prior = np.array([0, 63, 64, 130], np.int32)   # cached tokens before the append
+    new = np.array([5, 1, 70, 200], np.int32)
+    base = W.make_decode(4, 4, hk, d, prior + new, seed=seed, kv_dtype=kv_dtype, extra_pages=2)
+    kn = W.bf16_normal(seed, 90, (int(new.sum()), hk, d))
+    vn = W.bf16_normal(seed, 91, (int(new.sum()), hk, d))
+    return base, prior, new, kn, vn
+
+
+@pytest.mark.parametrize("kv_dtype", ["bf16", "e4m3"])
+def test_append_then_decode_sees_the_new_tokens(kv_dtype):
+    """Appending at position prior_b and decoding over prior_b + new_b keys equals
+    attention over keys gathered from the old pool (first prior_b) followed by
+    the new rows -- the token -> page mapping of the page diagram."""
+    base, prior, new, kn, vn = _append_case(kv_dtype)
+    cu = W.cu_seqlens(new)
+    kp, vp = oracle.append_kv(kn, vn, cu, prior, base.block_table, base.k_pool, base.v_pool,
+                              base.k_scale, base.v_scale)
+    # untouched rows are unchanged; written rows hold exactly the (quantised) new values
+    enc = (lambda x, s: x) if kv_dtype == "bf16" else (
+        lambda x, s: oracle.e4m3_from_f32(t_bf16(x).numpy().astype(np.float32) / s[None, :, None]))
+    changed = 0
+    for b in range(4):
+        for i in range(new[b]):
+            p = prior[b] + i
+            pg, r = base.block_table[b, p // 64], p % 64
+            row_k = enc(kn[cu[b] + i][None], base.k_scale)[0] if kv_dtype == "e4m3" else kn[cu[b] + i]
+            assert np.array_equal(kp[pg, :, r], row_k)
+            changed += 1
+    diff = np.any(kp != base.k_pool, axis=(1, 3))  # [P, 64] rows touched
+    assert diff.sum() <= changed * 1  # nothing else written
+    out, lse = oracle.decode(base.q, kp, vp, base.block_table, prior + new, base.scale, kv_dtype,
+                             base.k_scale, base.v_scale)
+    # reference: keys from the old pool for the prior tokens, then the new rows
+    dec = t_bf16 if kv_dtype == "bf16" else t_e4m3
+    for b in range(4):
+        pages = base.block_table[b, : (prior[b] + new[b] + 63) // 64]
+        kk = dec(kp)[pages].permute(1, 0, 2, 3).reshape(2, -1, 64)[:, : prior[b] + new[b]]
+        vv = dec(vp)[pages].permute(1, 0, 2, 3).reshape(2, -1, 64)[:, : prior[b] + new[b]]
+        if kv_dtype == "e4m3":
+            kk = kk * torch.as_tensor(base.k_scale, dtype=torch.float64)[:, None, None]
+            vv = vv * torch.as_tensor(base.v_scale, dtype=torch.float64)[:, None, None]
+        ro, rl = _sdpa(t_bf16(base.q[b])[:, None, :], kk.repeat_interleave(2, 0), vv.repeat_interleave(2, 0),
+                       base.scale)
+        np.testing.assert_allclose(out[b], ro[:, 0].numpy(), rtol=1e-12, atol=1e-12)
+        np.testing.assert_allclose(lse[b], rl[:, 0].numpy(), rtol=1e-12, atol=1e-12)
+    # the bf16 append is an exact copy: decoding only the new tokens of a sequence
+    # whose cache was empty (b = 0) sees exactly the appended values
+    if kv_dtype == "bf16":
+        np.testing.assert_array_equal(kp[base.block_table[0, 0], :, :5], np.transpose(kn[:5], (1, 0, 2)))
