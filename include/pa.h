@@ -249,6 +249,56 @@ pa_status pa_prefill(const pa_prefill_shapes* shapes, const void* q, const void*
  * PA_STATUS_BYTES + 4 * batch * ceil(max_seqlen_q / 256). */
 size_t pa_prefill_workspace_size(const pa_prefill_shapes* shapes);
 
+/* ----------------------------------------------------------------- mixed batches */
+
+typedef struct {
+    int32_t batch;             /* B sequences, decode (one query token) first */
+    int32_t num_q_heads, num_kv_heads, head_dim; /* D = 128 */
+    int32_t page_size;         /* must be 64 */
+    int32_t max_pages_per_seq, num_pool_pages;
+    int32_t kv_dtype;          /* PA_KV_BF16 */
+    int32_t num_sms, ctas_per_sm, forced_splits;  /* for the decode part, as in pa_decode_shapes */
+} pa_mixed_shapes;
+
+typedef struct {
+    int32_t num_decode;     /* leading sequences with one query token: the decode part */
+    int32_t total_q;        /* cu_seqlens_q[B] */
+    int32_t max_seqlen_q;   /* longest query segment of the prefill part */
+    int32_t reserved;
+    pa_decode_plan decode;  /* plan of the decode part (metadata = the first decode.meta_ints ints) */
+    size_t workspace_bytes; /* decode workspace followed by the prefill workspace */
+} pa_mixed_plan;
+
+/*
+ * A batch mixing single-token decode and longer (prefill / multi-token)
+ * segments over one paged cache, as MATE's planner splits a batch at the first
+ * sequence whose query length passes a threshold and runs a decode plan and a
+ * prefill plan.  Here the threshold is one token: the leading sequences with
+ * q_len == 1 run through the decode kernel (split-KV, merged), every sequence
+ * from the first q_len > 1 on runs through the prefill kernel (which also takes
+ * q_len == 1 rows).  Queries, outputs and lse stay in one ragged layout.
+ *
+ * pa_get_mixed_plan (host): cu_seqlens_q_host int32 [B+1], kv_lens_host int32 [B]
+ * (keys per sequence, new tokens included, already in the cache),
+ * block_table_host int32 [B, max_pages] or NULL; fills plan and writes the decode
+ * part's metadata to meta_host (NULL: size only; PA_ERR_WORKSPACE if
+ * meta_capacity_ints < plan->decode.meta_ints).
+ *
+ * pa_mixed (device): q bf16 [total_q, Hq, D]; pools [P, Hk, 64, D];
+ * block_table [B, max_pages]; cu_seqlens_q [B+1]; cu_seqlens_k [B+1] (running
+ * offsets of kv_lens); kv_lens [B]; meta_dev = the uploaded metadata; causal
+ * rows see keys j <= kv_len - q_len + i; out bf16 [total_q, Hq, D]; lse fp32
+ * [total_q, Hq] or NULL; workspace >= plan->workspace_bytes, zero-filled once.
+ */
+pa_status pa_get_mixed_plan(const int32_t* cu_seqlens_q_host, const int32_t* kv_lens_host,
+                        const int32_t* block_table_host, const pa_mixed_shapes* shapes, int32_t* meta_host,
+                        size_t meta_capacity_ints, pa_mixed_plan* plan);
+
+pa_status pa_mixed(const pa_mixed_shapes* shapes, const pa_mixed_plan* plan, const void* q, const void* k_pool,
+                   const void* v_pool, const int32_t* block_table, const int32_t* cu_seqlens_q,
+                   const int32_t* cu_seqlens_k, const int32_t* kv_lens, const int32_t* meta_dev, float scale,
+                   void* out, float* lse, void* workspace, size_t workspace_bytes, cudaStream_t stream);
+
 /* ----------------------------------------------------------------- append */
 
 typedef struct {

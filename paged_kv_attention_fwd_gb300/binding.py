@@ -50,6 +50,17 @@ class pa_prefill_shapes(ctypes.Structure):
         "total_q", "total_k", "page_size", "max_pages_per_seq", "num_pool_pages", "num_sms")]
 
 
+class pa_mixed_shapes(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_int32) for n in (
+        "batch", "num_q_heads", "num_kv_heads", "head_dim", "page_size", "max_pages_per_seq", "num_pool_pages",
+        "kv_dtype", "num_sms", "ctas_per_sm", "forced_splits")]
+
+
+class pa_mixed_plan(ctypes.Structure):
+    _fields_ = [("num_decode", ctypes.c_int32), ("total_q", ctypes.c_int32), ("max_seqlen_q", ctypes.c_int32),
+                ("reserved", ctypes.c_int32), ("decode", pa_decode_plan), ("workspace_bytes", ctypes.c_size_t)]
+
+
 class pa_append_shapes(ctypes.Structure):
     _fields_ = [(n, ctypes.c_int32) for n in (
         "batch", "num_kv_heads", "head_dim", "page_size", "max_pages_per_seq", "num_pool_pages", "total_new",
@@ -81,6 +92,12 @@ def lib() -> ctypes.CDLL:
         L.pa_decode_noalloc.restype = ctypes.c_int
         L.pa_prefill.argtypes = [ctypes.POINTER(pa_prefill_shapes), _P, _P, _P, _P, _P, _P, _P, _P, ctypes.c_int,
                                  f32, _P, _P, _P, sz, _P]
+        L.pa_get_mixed_plan.argtypes = [_P, _P, _P, ctypes.POINTER(pa_mixed_shapes), _P, sz,
+                                         ctypes.POINTER(pa_mixed_plan)]
+        L.pa_get_mixed_plan.restype = ctypes.c_int
+        L.pa_mixed.argtypes = [ctypes.POINTER(pa_mixed_shapes), ctypes.POINTER(pa_mixed_plan), _P, _P, _P, _P, _P, _P,
+                               _P, _P, f32, _P, _P, _P, sz, _P]
+        L.pa_mixed.restype = ctypes.c_int
         L.pa_append_kv.argtypes = [ctypes.POINTER(pa_append_shapes), _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, sz, _P]
         L.pa_append_kv.restype = ctypes.c_int
         L.pa_prefill_workspace_size.argtypes = [ctypes.POINTER(pa_prefill_shapes)]
@@ -197,6 +214,32 @@ def pa_prefill(shapes: pa_prefill_shapes, q, k, v, k_rope, cu_seqlens_q, cu_seql
                             _ptr(cu_seqlens_k), _ptr(block_table), _ptr(qo_offset), int(bool(causal)),
                             float(scale), _ptr(out), _ptr(lse), _ptr(workspace), int(workspace_bytes),
                             _stream(stream)))
+
+
+def pa_get_mixed_plan(cu_seqlens_q_host, kv_lens_host, block_table_host, shapes: pa_mixed_shapes):
+    """Returns (decode-part metadata int32 numpy array, pa_mixed_plan)."""
+    cq = np.ascontiguousarray(cu_seqlens_q_host, dtype=np.int32)
+    kl = np.ascontiguousarray(kv_lens_host, dtype=np.int32)
+    bt = None if block_table_host is None else np.ascontiguousarray(block_table_host, dtype=np.int32)
+    plan = pa_mixed_plan()
+    st = lib().pa_get_mixed_plan(_ptr(cq), _ptr(kl), _ptr(bt), ctypes.byref(shapes), None, 0, ctypes.byref(plan))
+    if st not in (PA_OK, PA_ERR_WORKSPACE):
+        _check(st)
+    meta = np.zeros(max(plan.decode.meta_ints, 1), dtype=np.int32)
+    _check(lib().pa_get_mixed_plan(_ptr(cq), _ptr(kl), _ptr(bt), ctypes.byref(shapes), _ptr(meta), meta.size,
+                                   ctypes.byref(plan)))
+    return meta, plan
+
+
+def pa_mixed(shapes: pa_mixed_shapes, plan: pa_mixed_plan, q, k_pool, v_pool, block_table, cu_seqlens_q,
+             cu_seqlens_k, kv_lens, meta_dev, scale: float, out, lse, workspace, workspace_bytes: Optional[int] = None,
+             stream=None) -> None:
+    if workspace_bytes is None:
+        workspace_bytes = workspace.numel() * workspace.element_size()
+    _check(lib().pa_mixed(ctypes.byref(shapes), ctypes.byref(plan), _ptr(q), _ptr(k_pool), _ptr(v_pool),
+                          _ptr(block_table), _ptr(cu_seqlens_q), _ptr(cu_seqlens_k), _ptr(kv_lens), _ptr(meta_dev),
+                          float(scale), _ptr(out), _ptr(lse), _ptr(workspace), int(workspace_bytes),
+                          _stream(stream)))
 
 
 def pa_append_kv(shapes: pa_append_shapes, k_new, v_new, cu_seqlens_new, start_pos, block_table, k_pool, v_pool,

@@ -534,6 +534,118 @@ pa_status pa_append_kv(const pa_append_shapes* sh, const void* k_new, const void
     return PA_OK;
 }
 
+namespace {
+pa_decode_shapes mixed_decode_shapes(const pa_mixed_shapes* sh, int num_decode) {
+    pa_decode_shapes d;
+    d.batch = num_decode;
+    d.num_q_heads = sh->num_q_heads;
+    d.num_kv_heads = sh->num_kv_heads;
+    d.head_dim = sh->head_dim;
+    d.page_size = sh->page_size;
+    d.max_pages_per_seq = sh->max_pages_per_seq;
+    d.num_pool_pages = sh->num_pool_pages;
+    d.kv_dtype = sh->kv_dtype;
+    d.num_sms = sh->num_sms;
+    d.ctas_per_sm = sh->ctas_per_sm;
+    d.forced_splits = sh->forced_splits;
+    return d;
+}
+
+pa_prefill_shapes mixed_prefill_shapes(const pa_mixed_shapes* sh, const pa_mixed_plan* plan) {
+    pa_prefill_shapes p;
+    p.batch = sh->batch - plan->num_decode;
+    p.num_q_heads = sh->num_q_heads;
+    p.num_kv_heads = sh->num_kv_heads;
+    p.head_dim_qk = sh->head_dim;
+    p.head_dim_v = sh->head_dim;
+    p.rope_dim = 0;
+    p.max_seqlen_q = plan->max_seqlen_q;
+    p.total_q = plan->total_q;
+    p.total_k = 0;
+    p.page_size = sh->page_size;
+    p.max_pages_per_seq = sh->max_pages_per_seq;
+    p.num_pool_pages = sh->num_pool_pages;
+    p.num_sms = sh->num_sms;
+    return p;
+}
+}  // namespace
+
+pa_status pa_get_mixed_plan(const int32_t* cu_q, const int32_t* kv_lens, const int32_t* block_table_host,
+                        const pa_mixed_shapes* sh, int32_t* meta_host, size_t meta_capacity_ints,
+                        pa_mixed_plan* plan) {
+    if (!sh || !plan) return fail(PA_ERR_INVALID_ARG, "shapes and plan must not be NULL");
+    const int B = sh->batch;
+    if (B < 0) return fail(PA_ERR_INVALID_ARG, "batch must be >= 0");
+    if (B > 0 && (!cu_q || !kv_lens)) return fail(PA_ERR_INVALID_ARG, "cu_seqlens_q_host and kv_lens_host are needed");
+    if (sh->head_dim != 128) return fail(PA_ERR_UNSUPPORTED, "mixed batches need head_dim 128 (got %d)", sh->head_dim);
+    if (sh->kv_dtype != PA_KV_BF16) return fail(PA_ERR_UNSUPPORTED, "mixed batches need bf16 pools");
+    std::memset(plan, 0, sizeof *plan);
+    int nd = 0;
+    while (nd < B && cu_q[nd + 1] - cu_q[nd] == 1) ++nd;
+    int maxq = 0;
+    for (int b = 0; b < B; ++b) {
+        const int ql = cu_q[b + 1] - cu_q[b];
+        if (ql < 0) return fail(PA_ERR_INVALID_ARG, "cu_seqlens_q must not decrease (at %d)", b);
+        if (ql > kv_lens[b])
+            return fail(PA_ERR_INVALID_ARG, "sequence %d has %d query tokens but only %d keys", b, ql, kv_lens[b]);
+        if (b >= nd) maxq = std::max(maxq, ql);
+    }
+    plan->num_decode = nd;
+    plan->total_q = B > 0 ? cu_q[B] : 0;
+    plan->max_seqlen_q = maxq;
+    size_t dec_ws = 0;
+    if (nd > 0) {
+        pa_decode_shapes d = mixed_decode_shapes(sh, nd);
+        pa_status st = pa_get_metadata(kv_lens, block_table_host, &d, meta_host, meta_capacity_ints, &plan->decode);
+        if (st != PA_OK && !(st == PA_ERR_WORKSPACE && !meta_host)) return st;
+        dec_ws = (plan->decode.workspace_bytes + 255) / 256 * 256;
+    }
+    pa_prefill_shapes p = mixed_prefill_shapes(sh, plan);
+    const size_t pre_ws = B - nd > 0 ? pa_prefill_workspace_size(&p) : PA_STATUS_BYTES;
+    plan->workspace_bytes = dec_ws + pre_ws;
+    if (block_table_host && B - nd > 0) {
+        for (int b = nd; b < B; ++b) {
+            if ((int64_t)kv_lens[b] > (int64_t)sh->max_pages_per_seq * pa::kPage)
+                return fail(PA_ERR_INVALID_ARG, "kv_lens[%d] exceeds max_pages_per_seq * 64", b);
+            for (int j = 0; j < (kv_lens[b] + pa::kPage - 1) / pa::kPage; ++j) {
+                const int32_t id = block_table_host[(int64_t)b * sh->max_pages_per_seq + j];
+                if (id < 0 || id >= sh->num_pool_pages)
+                    return fail(PA_ERR_INVALID_ARG, "block_table[%d, %d] = %d is outside [0, %d)", b, j, id,
+                                sh->num_pool_pages);
+            }
+        }
+    }
+    return PA_OK;
+}
+
+pa_status pa_mixed(const pa_mixed_shapes* sh, const pa_mixed_plan* plan, const void* q, const void* k_pool,
+                   const void* v_pool, const int32_t* block_table, const int32_t* cu_seqlens_q,
+                   const int32_t* cu_seqlens_k, const int32_t* kv_lens, const int32_t* meta_dev, float scale,
+                   void* out, float* lse, void* workspace, size_t workspace_bytes, cudaStream_t stream) {
+    if (!sh || !plan) return fail(PA_ERR_INVALID_ARG, "shapes and plan must not be NULL");
+    if (workspace_bytes < plan->workspace_bytes)
+        return fail(PA_ERR_WORKSPACE, "workspace has %zu bytes, the plan needs %zu", workspace_bytes,
+                    plan->workspace_bytes);
+    if (!workspace || !block_table || !cu_seqlens_q || !cu_seqlens_k)
+        return fail(PA_ERR_INVALID_ARG, "a required pointer is NULL");
+    const int nd = plan->num_decode;
+    size_t dec_ws = 0;
+    if (nd > 0) {
+        pa_decode_shapes d = mixed_decode_shapes(sh, nd);
+        dec_ws = (plan->decode.workspace_bytes + 255) / 256 * 256;
+        pa_status st = pa_decode(&d, &plan->decode, q, k_pool, v_pool, nullptr, nullptr, block_table, kv_lens,
+                                 meta_dev, scale, out, lse, workspace, plan->decode.workspace_bytes, stream);
+        if (st != PA_OK) return st;
+    }
+    if (sh->batch - nd > 0) {
+        pa_prefill_shapes p = mixed_prefill_shapes(sh, plan);
+        return pa_prefill(&p, q, k_pool, v_pool, nullptr, cu_seqlens_q + nd, cu_seqlens_k + nd,
+                          block_table + (size_t)nd * sh->max_pages_per_seq, nullptr, 1, scale, out, lse,
+                          static_cast<uint8_t*>(workspace) + dec_ws, workspace_bytes - dec_ws, stream);
+    }
+    return PA_OK;
+}
+
 size_t pa_prefill_workspace_size(const pa_prefill_shapes* sh) {
     if (!sh || sh->batch <= 0 || sh->max_seqlen_q <= 0) return PA_STATUS_BYTES;
     return PA_STATUS_BYTES + (size_t)sh->batch * (size_t)cdiv(sh->max_seqlen_q, 256) * 4;

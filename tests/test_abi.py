@@ -152,3 +152,29 @@ def test_wait_limit_validation():
     with pytest.raises(B.PaError):
         B.pa_set_wait_limit_ns(0)
     B.pa_set_wait_limit_ns(2_000_000_000)
+
+
+def mixed_shapes(B_, hq=8, hk=2, max_pages=40, pool=10**5):
+    return B.pa_mixed_shapes(batch=B_, num_q_heads=hq, num_kv_heads=hk, head_dim=128, page_size=64,
+                             max_pages_per_seq=max_pages, num_pool_pages=pool, kv_dtype=B.PA_KV_BF16, num_sms=152,
+                             ctas_per_sm=0, forced_splits=0)
+
+
+def test_mixed_plan_splits_at_first_multi_token_segment():
+    # MATE splits a mixed batch at the first sequence whose query length passes
+    # its threshold; here the decode kernel takes the leading single-token rows
+    cq = np.array([0, 1, 2, 3, 43, 44, 344], np.int32)  # q_len 1 1 1 40 1 300
+    kl = np.array([10, 500, 1000, 100, 64, 400], np.int32)
+    meta, plan = B.pa_get_mixed_plan(cq, kl, None, mixed_shapes(6))
+    assert plan.num_decode == 3 and plan.total_q == 344 and plan.max_seqlen_q == 300
+    assert meta.tolist() == S.schedule(kl[:3].tolist(), 2, 152, 1)  # decode part = the plain scheduler's plan
+    # all-prefill and all-decode batches
+    _, p2 = B.pa_get_mixed_plan(np.array([0, 5, 6], np.int32), np.array([5, 9], np.int32), None, mixed_shapes(2))
+    assert p2.num_decode == 0 and p2.max_seqlen_q == 5
+    _, p3 = B.pa_get_mixed_plan(np.array([0, 1, 2], np.int32), np.array([5, 9], np.int32), None, mixed_shapes(2))
+    assert p3.num_decode == 2
+
+
+def test_mixed_plan_rejects_more_queries_than_keys():
+    with pytest.raises(B.PaError, match="query tokens"):
+        B.pa_get_mixed_plan(np.array([0, 1, 30], np.int32), np.array([5, 9], np.int32), None, mixed_shapes(2))

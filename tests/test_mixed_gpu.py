@@ -1,0 +1,63 @@
+"""Mixed decode + prefill batches on the GPU: pa_mixed (through the C ABI)
+runs the leading single-token sequences through the decode kernel and the rest
+through the prefill kernel; the whole ragged output must match the oracle's
+prefill over the batch (a decode row is a one-row segment)."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from paged_kv_attention_fwd_gb300 import binding as B
+from paged_kv_attention_fwd_gb300 import ops
+from paged_kv_attention_fwd_gb300 import workloads as W
+from paged_kv_attention_fwd_gb300.build import build
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def gpu():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    build()
+
+
+def run_mixed(q_lens, kv_lens, hq=8, hk=2, seed=60):
+    inp = W.make_paged_prefill(q_lens, kv_lens, hq, hk, 128, seed=seed, extra_pages=2)
+    dev = "cuda"
+    kl = np.asarray(kv_lens, np.int32)
+    sh = B.pa_mixed_shapes(batch=len(q_lens), num_q_heads=hq, num_kv_heads=hk, head_dim=128, page_size=64,
+                           max_pages_per_seq=inp.block_table.shape[1], num_pool_pages=inp.k.shape[0],
+                           kv_dtype=B.PA_KV_BF16, num_sms=ops.num_sms(), ctas_per_sm=0, forced_splits=0)
+    meta, plan = B.pa_get_mixed_plan(inp.cu_seqlens_q, kl, inp.block_table, sh)
+    tq = int(inp.cu_seqlens_q[-1])
+    out = torch.empty((tq, hq, 128), dtype=torch.bfloat16, device=dev)
+    lse = torch.empty((tq, hq), dtype=torch.float32, device=dev)
+    ws = torch.zeros(plan.workspace_bytes, dtype=torch.uint8, device=dev)
+    B.pa_mixed(sh, plan, ops.as_bf16(inp.q, dev), ops.as_bf16(inp.k, dev), ops.as_bf16(inp.v, dev),
+               torch.from_numpy(inp.block_table).to(dev), torch.from_numpy(inp.cu_seqlens_q).to(dev),
+               torch.from_numpy(inp.cu_seqlens_k).to(dev), torch.from_numpy(kl).to(dev),
+               torch.from_numpy(meta).to(dev), inp.scale, out, lse, ws)
+    # status words of both parts (decode workspace first, prefill after it)
+    dec = (plan.decode.workspace_bytes + 255) // 256 * 256 if plan.num_decode else 0
+    st = (B.pa_check_status(ws), B.pa_check_status(ws[dec:]))
+    ro, rl = oracle.prefill(inp.q, inp.k, inp.v, inp.cu_seqlens_q, inp.cu_seqlens_k, inp.scale, True,
+                            block_table=inp.block_table)
+    return out.float().cpu().numpy(), lse.cpu().numpy(), ro, rl, plan, st
+
+
+@pytest.mark.parametrize("q_lens,kv_lens", [
+    ([1, 1, 1, 40, 300, 1, 128], [700, 1, 3000, 40, 1300, 65, 2000]),   # decode head, then mixed
+    ([1] * 9, [5, 64, 65, 900, 4000, 1, 2, 129, 3000]),                  # decode only
+    ([17, 1, 1, 256], [17, 100, 200, 1000]),                              # prefill from the first row
+])
+def test_mixed_batch_matches_oracle(q_lens, kv_lens):
+    out, lse, ro, rl, plan, st = run_mixed(q_lens, kv_lens)
+    assert st == (B.PA_OK, B.PA_OK)
+    lead = 0
+    while lead < len(q_lens) and q_lens[lead] == 1:
+        lead += 1
+    assert plan.num_decode == lead
+    err = np.abs(out - ro)
+    assert np.all(np.isfinite(out)) and err.max() <= 1e-2 and err.mean() <= 1e-3
+    assert np.abs(lse - rl).max() <= 1e-3
