@@ -118,6 +118,31 @@ pa_status pa_get_metadata(const int32_t* seq_lens_host, const int32_t* block_tab
                           pa_decode_plan* plan);
 
 /*
+ * Device-side scheduling, for decode steps captured once in a CUDA graph and
+ * replayed with new lengths (MATE's static plans: a plan built from
+ * capacities, per-call lengths in device buffers, no host reads while
+ * capturing).
+ *
+ * pa_get_static_plan (host, no lengths): a plan that covers every length mix
+ * of `batch` sequences -- the split rule yields at most
+ * batch + ceil(4 * num_sms * ctas_per_sm / Hk) splits (batch * min(forced, 64)
+ * with forced splits).  Use it for pa_decode and for sizing the metadata
+ * buffer (plan->meta_ints) and the workspace.  Limits: batch <= 8192, at most
+ * 16384 work items (splits * Hk); PA_ERR_UNSUPPORTED beyond.
+ *
+ * pa_get_metadata_device (device, async on `stream`): one CTA reads
+ * seq_lens_dev int32 [B] and writes the packed metadata of pa_get_metadata to
+ * meta_dev int32 [plan->meta_ints] -- the same split rule, but the items,
+ * sorted longest first, are dealt to the CTAs in snake order (0..grid-1, then
+ * grid-1..0, ...) instead of least-loaded first.  Lengths above
+ * max_pages_per_seq * 64 are clamped.
+ */
+pa_status pa_get_static_plan(const pa_decode_shapes* shapes, pa_decode_plan* plan);
+
+pa_status pa_get_metadata_device(const pa_decode_shapes* shapes, const pa_decode_plan* static_plan,
+                                 const int32_t* seq_lens_dev, int32_t* meta_dev, cudaStream_t stream);
+
+/*
  * pa_decode -- single-token decode over the paged cache (FlashMLA
  * flash_mla_with_kvcache, "Tensor Shapes Reference" section 1; MATE paged mode,
  * flash_attn_with_kvcache), with split-KV partials merged by a log-sum-exp

@@ -20,8 +20,12 @@ reading used here, written out step by step:
   split s of sequence b covers pages [floor(s P / n), floor((s+1) P / n))
   items     = (b, s, kvh) in (b, s, kvh) order, cost = pages of the split + 1
   grid      = min(#items, cap)
-  assignment: items sorted by (cost descending, index ascending); each goes to
-            the CTA with the smallest (load, CTA index); its load grows by cost.
+  assignment ("lpt", the host scheduler): items sorted by (cost descending,
+            index ascending); each goes to the CTA with the smallest (load, CTA
+            index); its load grows by cost.
+  assignment ("snake", the device scheduler): the same sorted list dealt in
+            rounds of `grid` items, CTA order 0..grid-1 in even rounds and
+            grid-1..0 in odd rounds; a CTA's items keep their sorted order.
 
 Packed metadata (int32), the layout the library's scheduler must reproduce
 bit for bit:
@@ -67,7 +71,7 @@ def split_range(pages: int, nsplit: int, s: int):
 
 
 def schedule(seq_lens, num_kv_heads: int, num_sms: int, ctas_per_sm: int,
-             forced_splits: int = 0):
+             forced_splits: int = 0, dealing: str = "lpt"):
     """Return the packed metadata as a list of Python ints."""
     B = len(seq_lens)
     pages, n, chunk = split_counts(seq_lens, num_kv_heads, num_sms, ctas_per_sm, forced_splits)
@@ -83,12 +87,19 @@ def schedule(seq_lens, num_kv_heads: int, num_sms: int, ctas_per_sm: int,
     cap = num_sms * ctas_per_sm
     grid = min(len(items), cap)
     order = sorted(items, key=lambda it: (-it[0], it[1]))
-    heap = [(0, c) for c in range(grid)]
     per_cta = [[] for _ in range(grid)]
-    for cost, _, b, s, kvh in order:
-        load, c = heapq.heappop(heap)
-        per_cta[c].append((b, s, kvh))
-        heapq.heappush(heap, (load + cost, c))
+    if dealing == "lpt":
+        heap = [(0, c) for c in range(grid)]
+        for cost, _, b, s, kvh in order:
+            load, c = heapq.heappop(heap)
+            per_cta[c].append((b, s, kvh))
+            heapq.heappush(heap, (load + cost, c))
+    elif dealing == "snake":
+        for r, (cost, _, b, s, kvh) in enumerate(order):
+            rnd, pos = divmod(r, grid)
+            per_cta[pos if rnd % 2 == 0 else grid - 1 - pos].append((b, s, kvh))
+    else:
+        raise ValueError(dealing)
     out = [MAGIC, B, num_kv_heads, indptr[-1], len(items), grid, chunk, ctas_per_sm]
     out += n
     out += indptr
@@ -114,3 +125,12 @@ def unpack(meta):
     return dict(batch=B, num_kv_heads=hk, total_splits=total, num_items=nitems, grid=grid,
                 chunk=meta[6], ctas_per_sm=meta[7], n_splits=n, split_indptr=indptr,
                 cta_indptr=cta_ptr, items=items, length=o)
+
+
+def static_split_capacity(batch: int, num_kv_heads: int, num_sms: int, ctas_per_sm: int, forced_splits: int = 0):
+    """Most splits the rule can produce for `batch` sequences of any lengths:
+    sum_b ceil(pages_b / chunk) <= sum_b pages_b / chunk + B <= 4 * cap / Hk + B."""
+    if forced_splits > 0:
+        return batch * min(forced_splits, MAX_SPLITS)
+    cap = num_sms * ctas_per_sm
+    return batch + _cdiv(4 * cap, num_kv_heads)

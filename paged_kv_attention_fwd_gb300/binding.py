@@ -92,6 +92,11 @@ def lib() -> ctypes.CDLL:
         L.pa_decode_noalloc.restype = ctypes.c_int
         L.pa_prefill.argtypes = [ctypes.POINTER(pa_prefill_shapes), _P, _P, _P, _P, _P, _P, _P, _P, ctypes.c_int,
                                  f32, _P, _P, _P, sz, _P]
+        L.pa_get_static_plan.argtypes = [ctypes.POINTER(pa_decode_shapes), ctypes.POINTER(pa_decode_plan)]
+        L.pa_get_static_plan.restype = ctypes.c_int
+        L.pa_get_metadata_device.argtypes = [ctypes.POINTER(pa_decode_shapes), ctypes.POINTER(pa_decode_plan), _P, _P,
+                                             _P]
+        L.pa_get_metadata_device.restype = ctypes.c_int
         L.pa_get_mixed_plan.argtypes = [_P, _P, _P, ctypes.POINTER(pa_mixed_shapes), _P, sz,
                                          ctypes.POINTER(pa_mixed_plan)]
         L.pa_get_mixed_plan.restype = ctypes.c_int
@@ -214,6 +219,18 @@ def pa_prefill(shapes: pa_prefill_shapes, q, k, v, k_rope, cu_seqlens_q, cu_seql
                             _ptr(cu_seqlens_k), _ptr(block_table), _ptr(qo_offset), int(bool(causal)),
                             float(scale), _ptr(out), _ptr(lse), _ptr(workspace), int(workspace_bytes),
                             _stream(stream)))
+
+
+def pa_get_static_plan(shapes: pa_decode_shapes) -> pa_decode_plan:
+    plan = pa_decode_plan()
+    _check(lib().pa_get_static_plan(ctypes.byref(shapes), ctypes.byref(plan)))
+    return plan
+
+
+def pa_get_metadata_device(shapes: pa_decode_shapes, static_plan: pa_decode_plan, seq_lens_dev, meta_dev,
+                           stream=None) -> None:
+    _check(lib().pa_get_metadata_device(ctypes.byref(shapes), ctypes.byref(static_plan), _ptr(seq_lens_dev),
+                                        _ptr(meta_dev), _stream(stream)))
 
 
 def pa_get_mixed_plan(cu_seqlens_q_host, kv_lens_host, block_table_host, shapes: pa_mixed_shapes):

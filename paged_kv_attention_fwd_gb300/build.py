@@ -16,7 +16,7 @@ ROOT = os.path.dirname(HERE)
 CSRC = os.path.join(HERE, "csrc")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libpa.so")
-SOURCES = ["pa_api.cu", "decode.cu", "prefill.cu", "append.cu"]
+SOURCES = ["pa_api.cu", "decode.cu", "prefill.cu", "append.cu", "schedule.cu"]
 HEADERS = ["pa_ptx.cuh", "pa_internal.h"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "--expt-relaxed-constexpr",

@@ -651,6 +651,54 @@ size_t pa_prefill_workspace_size(const pa_prefill_shapes* sh) {
     return PA_STATUS_BYTES + (size_t)sh->batch * (size_t)cdiv(sh->max_seqlen_q, 256) * 4;
 }
 
+pa_status pa_get_static_plan(const pa_decode_shapes* sh, pa_decode_plan* plan) {
+    if (!sh || !plan) return fail(PA_ERR_INVALID_ARG, "shapes and plan must not be NULL");
+    const int B = sh->batch, Hk = sh->num_kv_heads;
+    if (B <= 0 || B > 8192) return fail(PA_ERR_UNSUPPORTED, "device scheduling needs 1 <= batch <= 8192 (got %d)", B);
+    if (Hk <= 0 || Hk > 65535) return fail(PA_ERR_INVALID_ARG, "num_kv_heads must be in [1, 65535] (got %d)", Hk);
+    if (sh->page_size != pa::kPage) return fail(PA_ERR_INVALID_ARG, "page_size must be 64 (got %d)", sh->page_size);
+    if (sh->max_pages_per_seq <= 0) return fail(PA_ERR_INVALID_ARG, "max_pages_per_seq must be positive");
+    if (sh->num_sms <= 0 || sh->ctas_per_sm < 0 || sh->forced_splits < 0)
+        return fail(PA_ERR_INVALID_ARG, "num_sms must be positive, ctas_per_sm and forced_splits >= 0");
+    const int cps = sh->ctas_per_sm == 0 ? 1 : sh->ctas_per_sm;
+    const int64_t cap = (int64_t)sh->num_sms * cps;
+    const int64_t splits = sh->forced_splits > 0 ? (int64_t)B * std::min(sh->forced_splits, PA_MAX_SPLITS)
+                                                 : B + cdiv(4 * cap, Hk);
+    const int64_t items = splits * Hk;
+    if (items > 16384) return fail(PA_ERR_UNSUPPORTED, "device scheduling handles up to 16384 work items (%lld)",
+                                   (long long)items);
+    plan->total_splits = (int32_t)splits;
+    plan->num_items = (int32_t)items;
+    plan->grid = (int32_t)cap;
+    plan->meta_ints = (int32_t)(pa::kMetaHeader + 2 * (int64_t)B + 1 + cap + 1 + 2 * items);
+    plan->ctas_per_sm = cps;
+    plan->reserved = 1;  // capacity plan
+    const int64_t hq = std::max(sh->num_q_heads, 0), d = std::max(sh->head_dim, 0);
+    plan->workspace_bytes = (size_t)PA_STATUS_BYTES + (size_t)(splits * hq * d * 4) +
+                            (size_t)(((splits * hq * 4) + 255) / 256 * 256) +
+                            (size_t)((((int64_t)B * Hk * 4) + 255) / 256 * 256);
+    return PA_OK;
+}
+
+pa_status pa_get_metadata_device(const pa_decode_shapes* sh, const pa_decode_plan* plan, const int32_t* seq_lens_dev,
+                                 int32_t* meta_dev, cudaStream_t stream) {
+    if (!sh || !plan) return fail(PA_ERR_INVALID_ARG, "shapes and plan must not be NULL");
+    if (!seq_lens_dev || !meta_dev) return fail(PA_ERR_INVALID_ARG, "seq_lens_dev and meta_dev must not be NULL");
+    pa_decode_plan check;
+    pa_status st = pa_get_static_plan(sh, &check);
+    if (st != PA_OK) return st;
+    if (plan->reserved != 1 || plan->num_items != check.num_items || plan->grid != check.grid)
+        return fail(PA_ERR_INVALID_ARG, "the plan must come from pa_get_static_plan for these shapes");
+    int p2 = 1;
+    while (p2 < plan->num_items) p2 <<= 1;
+    const size_t smem = pa::schedule_smem_bytes(sh->batch, p2);
+    if (smem > 227 * 1024) return fail(PA_ERR_UNSUPPORTED, "schedule needs %zu bytes of shared memory", smem);
+    cudaError_t e = pa::launch_schedule(seq_lens_dev, sh->batch, sh->num_kv_heads, sh->max_pages_per_seq,
+                                        plan->ctas_per_sm, plan->grid, sh->forced_splits, p2, meta_dev, stream);
+    if (e != cudaSuccess) return cuda_fail(e, "schedule launch");
+    return PA_OK;
+}
+
 pa_status pa_check_status(void* workspace, cudaStream_t stream) {
     if (!workspace) return fail(PA_ERR_INVALID_ARG, "workspace must not be NULL");
     int32_t word = 0;

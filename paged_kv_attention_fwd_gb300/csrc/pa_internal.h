@@ -87,6 +87,11 @@ struct AppendArgs {
 
 cudaError_t launch_append(const AppendArgs& a, cudaStream_t stream);
 
+// Device-side scheduler (schedule.cu)
+size_t schedule_smem_bytes(int B, int p2cap);
+cudaError_t launch_schedule(const int32_t* seq_lens, int B, int Hk, int max_pages, int cps, int cap, int forced,
+                            int p2cap, int32_t* meta, cudaStream_t stream);
+
 // Record a message for pa_last_error() on this host thread (pa_api.cu).
 void set_last_error(const char* msg);
 

@@ -1,0 +1,187 @@
+// schedule.cu -- the split-KV schedule computed on the device from device
+// sequence lengths, so a decode step can be captured once in a CUDA graph and
+// replayed with new lengths (MATE's static plans: capacities fixed at plan
+// time, per-call lengths in device buffers, no host reads in the captured
+// region).  Same split rule and packed layout as pa_get_metadata; the items,
+// sorted longest first, are dealt to the CTAs in "snake" rounds (0..grid-1,
+// then grid-1..0, ...) instead of least-loaded-first, which is sequential.
+// One CTA of 1024 threads; shared memory holds the sort keys and the
+// per-sequence page counts, split counts and split offsets.
+#include "pa_internal.h"
+
+namespace pa {
+namespace {
+
+constexpr int kThreads = 1024;
+
+__device__ __forceinline__ long long block_sum(long long v, long long* tmp) {
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    const int w = threadIdx.x >> 5, l = threadIdx.x & 31;
+    if (l == 0) tmp[w] = v;
+    __syncthreads();
+    if (threadIdx.x < 32) {
+        long long t = tmp[threadIdx.x];
+        for (int o = 16; o > 0; o >>= 1) t += __shfl_xor_sync(0xffffffffu, t, o);
+        if (threadIdx.x == 0) tmp[0] = t;
+    }
+    __syncthreads();
+    const long long t = tmp[0];
+    __syncthreads();
+    return t;
+}
+
+// out[i] = in[0] + ... + in[i-1] for i in [0, n]
+__device__ void block_exclusive_scan(const int* in, int* out, int n, int* tmp) {
+    const int per = (n + kThreads - 1) / kThreads;
+    const int lo = min(n, (int)threadIdx.x * per), hi = min(n, lo + per);
+    int local = 0;
+    for (int i = lo; i < hi; ++i) local += in[i];
+    const int w = threadIdx.x >> 5, l = threadIdx.x & 31;
+    int x = local;  // inclusive scan within the warp
+    for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, x, o);
+        if (l >= o) x += y;
+    }
+    if (l == 31) tmp[w] = x;
+    __syncthreads();
+    if (threadIdx.x < 32) {  // inclusive scan of the warp totals
+        int t = tmp[threadIdx.x];
+        for (int o = 1; o < 32; o <<= 1) {
+            const int y = __shfl_up_sync(0xffffffffu, t, o);
+            if (threadIdx.x >= o) t += y;
+        }
+        tmp[threadIdx.x] = t;
+    }
+    __syncthreads();
+    int run = (x - local) + (w > 0 ? tmp[w - 1] : 0);
+    for (int i = lo; i < hi; ++i) {
+        out[i] = run;
+        run += in[i];
+    }
+    if (threadIdx.x == 0) out[n] = tmp[31];
+    __syncthreads();
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
+    schedule_kernel(const int32_t* seq_lens, int B, int Hk, int max_pages, int cps, int cap, int forced,
+                    int p2cap, int32_t* meta) {
+    extern __shared__ unsigned long long dyn[];
+    unsigned long long* key = dyn;                              // [p2cap]
+    int* pages = reinterpret_cast<int*>(dyn + p2cap);           // [B]
+    int* nsp = pages + B;                                       // [B]
+    int* ind = nsp + B;                                         // [B + 1]
+    __shared__ long long tmp64[32];
+    __shared__ int tmp32[32];
+
+    long long local = 0;
+    for (int b = threadIdx.x; b < B; b += kThreads) {
+        const int len = max(seq_lens[b], 0);
+        const int p = min((len + kPage - 1) / kPage, max_pages);
+        pages[b] = p;
+        local += p;
+    }
+    const long long units = block_sum(local, tmp64) * Hk;
+    const long long c4 = 4LL * cap;
+    const long long chunk = max(4LL, (units + c4 - 1) / c4);
+    for (int b = threadIdx.x; b < B; b += kThreads) {
+        const int p = pages[b];
+        int n;
+        if (p <= 1) n = 1;
+        else if (forced > 0) n = min(min(forced, p), PA_MAX_SPLITS);
+        else n = (int)min((long long)PA_MAX_SPLITS, (p + chunk - 1) / chunk);
+        nsp[b] = n;
+    }
+    __syncthreads();
+    block_exclusive_scan(nsp, ind, B, tmp32);
+    const int total = ind[B];
+    const int items = total * Hk;
+    const int grid = min(items, cap);
+    int p2 = 1;
+    while (p2 < items) p2 <<= 1;
+    // sort keys: cost descending, then item index ascending (as the host rule)
+    for (int i = threadIdx.x; i < p2; i += kThreads) {
+        unsigned long long k = ~0ull;
+        if (i < items) {
+            const int g = i / Hk;
+            int lo = 0, hi = B - 1;  // last b with ind[b] <= g
+            while (lo < hi) {
+                const int mid = (lo + hi + 1) >> 1;
+                if (ind[mid] <= g) lo = mid;
+                else hi = mid - 1;
+            }
+            const int b = lo, s = g - ind[b], n = nsp[b], p = pages[b];
+            const int cost = (int)(((long long)(s + 1) * p) / n - ((long long)s * p) / n) + 1;
+            k = ((unsigned long long)(unsigned)(0x7FFFFFFF - cost) << 32) | (unsigned)i;
+        }
+        key[i] = k;
+    }
+    __syncthreads();
+    for (int size = 2; size <= p2; size <<= 1) {
+        for (int stride = size >> 1; stride > 0; stride >>= 1) {
+            for (int t = threadIdx.x; t < p2 / 2; t += kThreads) {
+                const int lo = 2 * stride * (t / stride) + (t % stride);
+                const int hi = lo + stride;
+                const bool up = (lo & size) == 0;
+                const unsigned long long x = key[lo], y = key[hi];
+                if ((x > y) == up) {
+                    key[lo] = y;
+                    key[hi] = x;
+                }
+            }
+            __syncthreads();
+        }
+    }
+    // packed metadata: header, n_splits, split_indptr, cta_indptr, items
+    if (threadIdx.x == 0) {
+        meta[0] = kMetaMagic;
+        meta[1] = B;
+        meta[2] = Hk;
+        meta[3] = total;
+        meta[4] = items;
+        meta[5] = grid;
+        meta[6] = (int)min(chunk, (long long)0x7FFFFFFF);
+        meta[7] = cps;
+    }
+    for (int b = threadIdx.x; b < B; b += kThreads) meta[kMetaHeader + b] = nsp[b];
+    for (int b = threadIdx.x; b <= B; b += kThreads) meta[kMetaHeader + B + b] = ind[b];
+    const int full = items / grid, rem = items % grid;
+    const bool last_even = (full & 1) == 0;
+    int32_t* cta_ptr = meta + kMetaHeader + 2 * B + 1;
+    for (int c = threadIdx.x; c <= grid; c += kThreads)
+        cta_ptr[c] = c * full + (last_even ? min(c, rem) : max(0, c - (grid - rem)));
+    int32_t* out_items = cta_ptr + grid + 1;
+    for (int r = threadIdx.x; r < items; r += kThreads) {
+        const int i = (int)(key[r] & 0xFFFFFFFFu);
+        const int g = i / Hk, kvh = i % Hk;
+        int lo = 0, hi = B - 1;
+        while (lo < hi) {
+            const int mid = (lo + hi + 1) >> 1;
+            if (ind[mid] <= g) lo = mid;
+            else hi = mid - 1;
+        }
+        const int rnd = r / grid, pos = r % grid;
+        const int c = (rnd & 1) == 0 ? pos : grid - 1 - pos;
+        const int slot = c * full + (last_even ? min(c, rem) : max(0, c - (grid - rem))) + rnd;
+        out_items[2 * slot] = lo;
+        out_items[2 * slot + 1] = ((g - ind[lo]) << 16) | kvh;
+    }
+}
+
+}  // namespace
+
+size_t schedule_smem_bytes(int B, int p2cap) { return (size_t)p2cap * 8 + (size_t)(3 * B + 1) * 4; }
+
+cudaError_t launch_schedule(const int32_t* seq_lens, int B, int Hk, int max_pages, int cps, int cap, int forced,
+                            int p2cap, int32_t* meta, cudaStream_t stream) {
+    const size_t smem = schedule_smem_bytes(B, p2cap);
+    static size_t configured = 0;
+    if (smem > 48 * 1024 && smem > configured) {
+        cudaError_t e = cudaFuncSetAttribute(schedule_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        if (e != cudaSuccess) return e;
+        configured = smem;
+    }
+    schedule_kernel<<<1, kThreads, smem, stream>>>(seq_lens, B, Hk, max_pages, cps, cap, forced, p2cap, meta);
+    return cudaGetLastError();
+}
+
+}  // namespace pa

@@ -88,3 +88,34 @@ def test_properties_lognormal_and_edges():
 def test_deterministic():
     lens = list(range(0, 5000, 37))
     assert S.schedule(lens, 4, 152, 1) == S.schedule(lens, 4, 152, 1)
+
+
+def test_snake_dealing_properties():
+    rng = np.random.default_rng(7)
+    lens = rng.integers(0, 8000, size=50).tolist()
+    meta = S.schedule(lens, 4, 20, 1, dealing="snake")
+    u = S.unpack(meta)
+    lpt = S.unpack(S.schedule(lens, 4, 20, 1))
+    assert u["n_splits"] == lpt["n_splits"] and sorted(u["items"]) == sorted(lpt["items"])
+    cp = u["cta_indptr"]
+    sizes = [cp[c + 1] - cp[c] for c in range(u["grid"])]
+    assert max(sizes) - min(sizes) <= 1  # one item per CTA per round
+
+
+@pytest.mark.parametrize("hk,sms,cps,forced", [(8, 152, 1, 0), (1, 4, 2, 0), (3, 7, 1, 5)])
+def test_static_capacity_bounds_every_length_mix(hk, sms, cps, forced):
+    rng = np.random.default_rng(hk * 10 + sms)
+    B = 40
+    bound = S.static_split_capacity(B, hk, sms, cps, forced)
+    for trial in range(200):
+        kind = trial % 4
+        if kind == 0:
+            lens = rng.integers(0, 20000, size=B)
+        elif kind == 1:
+            lens = np.full(B, int(rng.integers(0, 300000)))
+        elif kind == 2:
+            lens = np.where(rng.random(B) < 0.1, 200000, 1)
+        else:
+            lens = rng.integers(0, 300, size=B)
+        u = S.unpack(S.schedule(lens.tolist(), hk, sms, cps, forced))
+        assert u["total_splits"] <= bound
