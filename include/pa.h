@@ -51,7 +51,10 @@ typedef enum {
     PA_ERR_DEVICE_BOUNDS = 6  /* (device) a page id or length was out of range */
 } pa_status;
 
-typedef enum { PA_KV_BF16 = 0, PA_KV_FP8_E4M3 = 1 } pa_kv_dtype;
+/* Element type of the KV pools.  With PA_KV_FP16 the query, the pools and the
+ * output are all fp16 (q, k, v share one type, as MATE's forward requires);
+ * otherwise the query and output are bf16. */
+typedef enum { PA_KV_BF16 = 0, PA_KV_FP8_E4M3 = 1, PA_KV_FP16 = 2 } pa_kv_dtype;
 
 #define PA_PAGE_SIZE 64
 #define PA_MAX_SPLITS 64
@@ -148,8 +151,8 @@ pa_status pa_get_metadata_device(const pa_decode_shapes* shapes, const pa_decode
  * flash_attn_with_kvcache), with split-KV partials merged by a log-sum-exp
  * combine when any sequence has more than one split.
  *
- *   q            bf16 [B, Hq, D]
- *   k_pool       [num_pool_pages, Hk, 64, D], bf16 or e4m3 per shapes->kv_dtype
+ *   q            bf16 [B, Hq, D] (fp16 with PA_KV_FP16)
+ *   k_pool       [num_pool_pages, Hk, 64, D], bf16, e4m3 or fp16 per shapes->kv_dtype
  *   v_pool       same layout and type as k_pool
  *   k_scale      fp32 [Hk] per-KV-head dequantisation scale (e4m3 only, else NULL)
  *   v_scale      fp32 [Hk] (e4m3 only, else NULL); an e4m3 element x of head g
@@ -158,7 +161,7 @@ pa_status pa_get_metadata_device(const pa_decode_shapes* shapes, const pa_decode
  *   seq_lens     int32 [B] (device copy of the lengths given to pa_get_metadata)
  *   meta_dev     int32 [plan->meta_ints], device copy of pa_get_metadata's output
  *   scale        softmax scale (e.g. 1/sqrt(D))
- *   out          bf16 [B, Hq, D]
+ *   out          bf16 [B, Hq, D] (fp16 with PA_KV_FP16)
  *   lse          fp32 [B, Hq] or NULL
  *   workspace    >= plan->workspace_bytes device bytes; the first 256 bytes hold
  *                the status word.  Zero-fill it once before first use; the
@@ -239,6 +242,7 @@ typedef struct {
     int32_t max_pages_per_seq; /* block_table row stride (paged) */
     int32_t num_pool_pages;    /* pages in the pools (paged) */
     int32_t num_sms;
+    int32_t dtype;             /* PA_KV_BF16 or PA_KV_FP16: q, k, v, k_rope and out */
 } pa_prefill_shapes;
 
 /*
@@ -344,14 +348,14 @@ typedef struct {
  * logical position p = start_pos[b] + i: row p % 64 of page
  * block_table[b, p / 64] ("Prefill to Cache Mapping").
  *
- *   k_new, v_new    bf16 [total_new, Hk, D], ragged by cu_seqlens_new
+ *   k_new, v_new    bf16 [total_new, Hk, D] (fp16 for fp16 pools), ragged by cu_seqlens_new
  *   cu_seqlens_new  int32 [B+1] running offsets of the new tokens
  *   start_pos       int32 [B] position of each sequence's first new token (the
  *                   number of tokens already cached)
  *   block_table     int32 [B, max_pages_per_seq]; must already list the pages
  *                   that the new positions fall in
- *   k_pool, v_pool  [num_pool_pages, Hk, 64, D]: bf16 (values copied bit for
- *                   bit), or e4m3 with k_scale / v_scale fp32 [Hk]: the stored
+ *   k_pool, v_pool  [num_pool_pages, Hk, 64, D]: bf16 or fp16 (values copied bit
+ *                   for bit), or e4m3 with k_scale / v_scale fp32 [Hk]: the stored
  *                   code is e4m3(x / scale) in fp32, nearest even, saturating
  *   workspace       >= PA_STATUS_BYTES (status word)
  * A position outside the block table or a page id outside the pool is skipped

@@ -37,12 +37,14 @@ def _load():
                                       dbl, P, P]
         lib.oracle_decode.restype = i32
         lib.oracle_prefill.argtypes = [i32, i32, i32, i32, i32, i32, i32, i64, P, P, P, P, P, P,
-                                       P, P, i32, dbl, P, i64, P, P]
+                                       P, P, i32, dbl, P, i64, P, P, i32]
         lib.oracle_prefill.restype = i32
         lib.oracle_bf16_to_double.argtypes = [ctypes.c_uint16]
         lib.oracle_bf16_to_double.restype = dbl
         lib.oracle_e4m3_to_double.argtypes = [ctypes.c_uint8]
         lib.oracle_e4m3_to_double.restype = dbl
+        lib.oracle_f16_to_double.argtypes = [ctypes.c_uint16]
+        lib.oracle_f16_to_double.restype = dbl
         lib.oracle_e4m3_from_float.argtypes = [ctypes.c_float]
         lib.oracle_e4m3_from_float.restype = ctypes.c_uint8
         lib.oracle_append_kv.argtypes = [i32, i32, i32, i32, i64, i32, P, P, P, P, P, P, P, P, P]
@@ -75,6 +77,12 @@ def bf16_to_f64(bits: np.ndarray) -> np.ndarray:
     return np.array([lib.oracle_bf16_to_double(int(x)) for x in flat]).reshape(np.shape(bits))
 
 
+def f16_to_f64(bits: np.ndarray) -> np.ndarray:
+    lib = _load()
+    flat = np.asarray(bits, dtype=np.uint16).ravel()
+    return np.array([lib.oracle_f16_to_double(int(x)) for x in flat]).reshape(np.shape(bits))
+
+
 def e4m3_to_f64(bits: np.ndarray) -> np.ndarray:
     lib = _load()
     flat = np.asarray(bits, dtype=np.uint8).ravel()
@@ -83,13 +91,14 @@ def e4m3_to_f64(bits: np.ndarray) -> np.ndarray:
 
 def decode(q, k_pool, v_pool, block_table, seq_lens, scale: float, kv_dtype: str = "bf16",
            k_scale=None, v_scale=None):
-    """Single-token decode.  q uint16 [B,Hq,D]; pools [P,Hk,64,D] (uint16 bf16 or
-    uint8 e4m3); block_table int32 [B,max_pages]; seq_lens int32 [B].
+    """Single-token decode.  q uint16 [B,Hq,D] (bf16, or fp16 with kv_dtype "f16");
+    pools [P,Hk,64,D] (uint16 bf16/fp16 or uint8 e4m3); block_table int32
+    [B,max_pages]; seq_lens int32 [B].
     Returns (out float64 [B,Hq,D], lse float64 [B,Hq])."""
     lib = _load()
     q = _c(q, np.uint16)
-    kind = {"bf16": 0, "e4m3": 1}[kv_dtype]
-    pdt = np.uint16 if kind == 0 else np.uint8
+    kind = {"bf16": 0, "e4m3": 1, "f16": 2}[kv_dtype]
+    pdt = np.uint8 if kind == 1 else np.uint16
     k_pool, v_pool = _c(k_pool, pdt), _c(v_pool, pdt)
     bt, sl = _c(block_table, np.int32), _c(seq_lens, np.int32)
     ks, vs = _c(k_scale, np.float64), _c(v_scale, np.float64)
@@ -106,7 +115,7 @@ def decode(q, k_pool, v_pool, block_table, seq_lens, scale: float, kv_dtype: str
 
 
 def prefill(q, k, v, cu_seqlens_q, cu_seqlens_k, scale: float, causal: bool = True,
-            block_table=None, k_rope=None, qo_offset=None, rows=None):
+            block_table=None, k_rope=None, qo_offset=None, rows=None, dtype: str = "bf16"):
     """Chunked / ragged (optionally MLA) prefill.  See ``oracle_prefill`` in oracle.c.
     rows: optional int64 array of (token * Hq + h) to evaluate.
     Returns (out float64 [rows, Dv] or [total_q, Hq, Dv], lse)."""
@@ -132,7 +141,7 @@ def prefill(q, k, v, cu_seqlens_q, cu_seqlens_k, scale: float, causal: bool = Tr
     rc = lib.oracle_prefill(B, Hq, Hk, Dqk, Dv, rope, max_pages, num_pages, _p(q), _p(k), _p(v),
                             _p(kr), _p(cq), _p(ck), _p(bt), _p(qo), int(bool(causal)),
                             float(scale), _p(rr), nrows if rr is not None else 0,
-                            _p(out), _p(lse))
+                            _p(out), _p(lse), {"bf16": 0, "f16": 2}[dtype])
     if rc != 0:
         raise ValueError("oracle_prefill: a referenced page id is out of range")
     if rr is None:

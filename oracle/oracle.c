@@ -65,6 +65,19 @@ double oracle_bf16_to_double(uint16_t bits) {
     return (double)f;
 }
 
+/* IEEE binary16 -> double: sign, 5-bit exponent with bias 15, 10-bit mantissa,
+ * subnormals (exponent field 0: value = mantissa/1024 * 2^-14), inf, NaN. */
+double oracle_f16_to_double(uint16_t bits) {
+    int sign = (bits >> 15) & 1;
+    int e = (bits >> 10) & 31;
+    int m = bits & 1023;
+    double mag;
+    if (e == 31) mag = m ? NAN : INFINITY;
+    else if (e == 0) mag = ldexp((double)m / 1024.0, -14);
+    else mag = ldexp(1.0 + (double)m / 1024.0, e - 15);
+    return sign ? -mag : mag;
+}
+
 /* OCP FP8 E4M3 ("fn": no infinities) -> double. */
 double oracle_e4m3_to_double(uint8_t bits) {
     int sign = (bits >> 7) & 1;
@@ -79,9 +92,11 @@ double oracle_e4m3_to_double(uint8_t bits) {
     return sign ? -mag : mag;
 }
 
-/* Element decoders over raw buffers: kind 0 = bf16 (uint16), 1 = e4m3 (uint8). */
+/* Element decoders over raw buffers: kind 0 = bf16 (uint16), 1 = e4m3 (uint8),
+ * 2 = fp16 (uint16). */
 static double load_elem(const void* base, int kind, int64_t idx) {
     if (kind == 0) return oracle_bf16_to_double(((const uint16_t*)base)[idx]);
+    if (kind == 2) return oracle_f16_to_double(((const uint16_t*)base)[idx]);
     return oracle_e4m3_to_double(((const uint8_t*)base)[idx]);
 }
 
@@ -116,8 +131,8 @@ static void attend_row(const double* q, const double* kd, const double* vd, int6
 
 /*
  * Single-token decode over a paged cache.
- *   q        bf16 [B, Hq, D]
- *   k_pool   [P, Hk, 64, D] of kind kv_kind (0 bf16, 1 e4m3); v_pool the same
+ *   q        bf16 [B, Hq, D] (fp16 when kv_kind is 2: q and the pools share the type)
+ *   k_pool   [P, Hk, 64, D] of kind kv_kind (0 bf16, 1 e4m3, 2 fp16); v_pool the same
  *   k_scale, v_scale  double [Hk] dequantisation scales (NULL -> 1)
  *   block_table int32 [B, max_pages]; seq_lens int32 [B]
  *   out double [B, Hq, D]; lse double [B, Hq]
@@ -148,7 +163,7 @@ int oracle_decode(int B, int Hq, int Hk, int D, int max_pages, int64_t num_pages
         double* vd = (double*)malloc(sizeof(double) * (size_t)(n ? n : 1) * D);
         double* s = (double*)malloc(sizeof(double) * (size_t)(n ? n : 1));
         double ks = k_scale ? k_scale[kvh] : 1.0, vs = v_scale ? v_scale[kvh] : 1.0;
-        for (int d = 0; d < D; ++d) qd[d] = oracle_bf16_to_double(q[bh * D + d]);
+        for (int d = 0; d < D; ++d) qd[d] = load_elem(q, kv_kind == 2 ? 2 : 0, bh * D + d);
         int ok = 1;
         for (int64_t j = 0; j < n && ok; ++j) {
             int64_t page = block_table[(int64_t)b * max_pages + j / ORACLE_PAGE];
@@ -184,13 +199,15 @@ int oracle_decode(int B, int Hq, int Hk, int D, int max_pages, int64_t num_pages
  *   qo_offset   int32 [B] or NULL (-> kv_len - q_len)
  *   rows   optional list of (token * Hq + h) rows to evaluate (NULL: all);
  *          out/lse are then [nrows, Dv] / [nrows]
+ *   elem_kind  0: q, k, v, k_rope are bf16; 2: fp16
  * Returns 0, or -1 on an out-of-range page id.
  */
 int oracle_prefill(int B, int Hq, int Hk, int Dqk, int Dv, int rope_dim, int max_pages,
                    int64_t num_pages, const uint16_t* q, const uint16_t* k, const uint16_t* v,
                    const uint16_t* k_rope, const int32_t* cu_q, const int32_t* cu_k,
                    const int32_t* block_table, const int32_t* qo_offset, int causal,
-                   double scale, const int64_t* rows, int64_t nrows, double* out, double* lse) {
+                   double scale, const int64_t* rows, int64_t nrows, double* out, double* lse,
+                   int elem_kind) {
     int group = Hq / Hk;
     int Dk = Dqk - rope_dim;
     int64_t total_q = cu_q[B];
@@ -220,7 +237,7 @@ int oracle_prefill(int B, int Hq, int Hk, int Dqk, int Dv, int rope_dim, int max
         double* kd = (double*)malloc(sizeof(double) * (size_t)(n ? n : 1) * Dqk);
         double* vd = (double*)malloc(sizeof(double) * (size_t)(n ? n : 1) * Dv);
         double* s = (double*)malloc(sizeof(double) * (size_t)(n ? n : 1));
-        for (int d = 0; d < Dqk; ++d) qd[d] = oracle_bf16_to_double(q[(tok * Hq + h) * Dqk + d]);
+        for (int d = 0; d < Dqk; ++d) qd[d] = load_elem(q, elem_kind, (tok * Hq + h) * Dqk + d);
         int ok = 1;
         for (int64_t j = 0; j < n; ++j) {
             int64_t krow, vrow;
@@ -235,10 +252,10 @@ int oracle_prefill(int B, int Hq, int Hk, int Dqk, int Dv, int rope_dim, int max
                 krow = (t * Hk + kvh) * Dk;
                 vrow = (t * Hk + kvh) * Dv;
             }
-            for (int d = 0; d < Dk; ++d) kd[j * Dqk + d] = oracle_bf16_to_double(k[krow + d]);
+            for (int d = 0; d < Dk; ++d) kd[j * Dqk + d] = load_elem(k, elem_kind, krow + d);
             for (int d = 0; d < rope_dim; ++d)
-                kd[j * Dqk + Dk + d] = oracle_bf16_to_double(k_rope[(cu_k[b] + j) * rope_dim + d]);
-            for (int d = 0; d < Dv; ++d) vd[j * Dv + d] = oracle_bf16_to_double(v[vrow + d]);
+                kd[j * Dqk + Dk + d] = load_elem(k_rope, elem_kind, (cu_k[b] + j) * rope_dim + d);
+            for (int d = 0; d < Dv; ++d) vd[j * Dv + d] = load_elem(v, elem_kind, vrow + d);
         }
         if (ok) {
             attend_row(qd, kd, vd, n, Dqk, Dv, scale, s, o, &lse[r]);

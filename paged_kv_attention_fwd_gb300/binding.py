@@ -20,7 +20,7 @@ HEADER = os.path.join(os.path.dirname(HERE), "include", "pa.h")
 
 PA_OK, PA_ERR_INVALID_ARG, PA_ERR_UNSUPPORTED, PA_ERR_WORKSPACE, PA_ERR_CUDA, PA_ERR_TIMEOUT, \
     PA_ERR_DEVICE_BOUNDS = range(7)
-PA_KV_BF16, PA_KV_FP8_E4M3 = 0, 1
+PA_KV_BF16, PA_KV_FP8_E4M3, PA_KV_FP16 = 0, 1, 2
 PA_STATUS_BYTES = 256
 STATUS_NAMES = {0: "PA_OK", 1: "PA_ERR_INVALID_ARG", 2: "PA_ERR_UNSUPPORTED", 3: "PA_ERR_WORKSPACE",
                 4: "PA_ERR_CUDA", 5: "PA_ERR_TIMEOUT", 6: "PA_ERR_DEVICE_BOUNDS"}
@@ -47,7 +47,7 @@ class pa_decode_plan(ctypes.Structure):
 class pa_prefill_shapes(ctypes.Structure):
     _fields_ = [(n, ctypes.c_int32) for n in (
         "batch", "num_q_heads", "num_kv_heads", "head_dim_qk", "head_dim_v", "rope_dim", "max_seqlen_q",
-        "total_q", "total_k", "page_size", "max_pages_per_seq", "num_pool_pages", "num_sms")]
+        "total_q", "total_k", "page_size", "max_pages_per_seq", "num_pool_pages", "num_sms", "dtype")]
 
 
 class pa_mixed_shapes(ctypes.Structure):

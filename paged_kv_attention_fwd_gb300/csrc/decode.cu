@@ -198,6 +198,11 @@ __device__ __forceinline__ bool softmax_bar_or(bool pred) {
 }
 
 
+// the 16-bit output element: fp16 when the inputs are fp16, else bf16
+__device__ __forceinline__ uint16_t out16(float x, bool f16) {
+    return f16 ? __half_as_ushort(__float2half_rn(x)) : __bfloat16_as_ushort(__float2bfloat16_rn(x));
+}
+
 // Split merge inside the decode kernel (pa_decode).  The softmax threads
 // write an item's partials, then arrive on a barrier; one extra warp -- the
 // merge warp -- takes it from there, off the softmax's critical path: it
@@ -261,7 +266,7 @@ __device__ void merge_warp(const DecodeArgs& a, int it_lo, int it_hi, int items_
                 const float inv = wsum > 0.f ? 1.f / wsum : 0.f;
 #pragma unroll
                 for (int i = 0; i < D / 32; ++i)
-                    a.out[(orow + h) * D + lane + 32 * i] = __bfloat16_as_ushort(__float2bfloat16_rn(acc[i] * inv));
+                    a.out[(orow + h) * D + lane + 32 * i] = out16(acc[i] * inv, a.f16);
                 if (lane == 0 && a.lse) a.lse[orow + h] = wsum > 0.f ? mx + __logf(wsum) : -INFINITY;
             }
             if (lane == 0) *ctr = 0;
@@ -398,8 +403,9 @@ __global__ void __launch_bounds__(DecodeLayout<D, FP8>::kThreads, 1)
     } else if (warp == 1) {
         // ------------------------------------------------------------ MMA issuer
         if (lane == 0) {
-            constexpr uint32_t idesc_qk = idesc_f16(128, kNPad, !FP8, false, false);
-            constexpr uint32_t idesc_pv = idesc_f16(128, kNPad, !FP8, true, false);
+            const bool as_f16 = FP8 || a.f16;  // operand format: fp16, else bf16
+            const uint32_t idesc_qk = idesc_f16(128, kNPad, !as_f16, false, false);
+            const uint32_t idesc_pv = idesc_f16(128, kNPad, !as_f16, true, false);
             uint32_t g = 0, qi = 0;
             bool pending = false, ok = true;
             auto issue_pv = [&](uint32_t k) -> bool {
@@ -601,7 +607,8 @@ __global__ void __launch_bounds__(DecodeLayout<D, FP8>::kThreads, 1)
                 uint8_t* pb = sm + L::kPOff + (g & 1) * L::kPBytes + (row >> 6) * (kNPad * 128);
 #pragma unroll
                 for (int h = 0; h < NP; ++h)
-                    if (h < G) *reinterpret_cast<uint16_t*>(pb + sw128_offset(h, row & 63)) = f32_to_16(x[h], FP8);
+                    if (h < G)
+                        *reinterpret_cast<uint16_t*>(pb + sw128_offset(h, row & 63)) = f32_to_16(x[h], FP8 || a.f16);
                 if (!FP8 && !valid) {
                     // a dead key's V row may hold anything (NaN included); 0 * NaN
                     // would poison the PV product, so zero the row first
@@ -639,7 +646,7 @@ __global__ void __launch_bounds__(DecodeLayout<D, FP8>::kThreads, 1)
                 if (h < G && row < D) {
                     const float val = l > 0.f ? o[h] * (vs / l) : 0.f;
                     if (partial) a.o_part[(orow + h) * D + row] = val;
-                    else a.out[(orow + h) * D + row] = __bfloat16_as_ushort(__float2bfloat16_rn(val));
+                    else a.out[(orow + h) * D + row] = out16(val, a.f16);
                 }
             }
             if (row < G) {
@@ -1219,7 +1226,7 @@ __global__ void __launch_bounds__(128) combine_kernel(const CombineArgs a) {
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
         const int d = lane + 32 * i;
-        if (d < a.head_dim) a.out[orow * a.head_dim + d] = __bfloat16_as_ushort(__float2bfloat16_rn(acc[i] * inv));
+        if (d < a.head_dim) a.out[orow * a.head_dim + d] = out16(acc[i] * inv, a.f16);
     }
     if (lane == 0 && a.lse) a.lse[orow] = mx + __logf(wsum);
 }

@@ -68,6 +68,13 @@ pa_status make_map_bf16(CUtensorMap* map, const void* base, int rank, const uint
     return make_map(CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, map, base, rank, dims, strides_bytes, box);
 }
 
+// 16-bit elements: the swizzled layout does not depend on which 16-bit type
+pa_status make_map_16(bool f16, CUtensorMap* map, const void* base, int rank, const uint64_t* dims,
+                      const uint64_t* strides_bytes, const uint32_t* box) {
+    return make_map(f16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, map, base, rank, dims,
+                    strides_bytes, box);
+}
+
 // Tiled map, 128-byte swizzle (the box's inner extent is 128 bytes).
 pa_status make_map(CUtensorMapDataType dtype, CUtensorMap* map, const void* base, int rank, const uint64_t* dims,
                    const uint64_t* strides_bytes, const uint32_t* box) {
@@ -282,9 +289,10 @@ pa_status decode_launch(bool fused, const pa_decode_shapes* sh, const pa_decode_
     pa_status st = validate_decode_common(sh, plan, out, meta_dev, workspace, workspace_bytes);
     if (st != PA_OK || sh->batch == 0) return st;
     const int B = sh->batch, Hq = sh->num_q_heads, Hk = sh->num_kv_heads, D = sh->head_dim;
-    if (sh->kv_dtype != PA_KV_BF16 && sh->kv_dtype != PA_KV_FP8_E4M3)
+    if (sh->kv_dtype != PA_KV_BF16 && sh->kv_dtype != PA_KV_FP8_E4M3 && sh->kv_dtype != PA_KV_FP16)
         return fail(PA_ERR_INVALID_ARG, "unknown kv_dtype %d", sh->kv_dtype);
     const bool fp8 = sh->kv_dtype == PA_KV_FP8_E4M3;
+    const bool f16 = sh->kv_dtype == PA_KV_FP16;
     if (sh->max_pages_per_seq <= 0 || sh->num_pool_pages <= 0)
         return fail(PA_ERR_INVALID_ARG, "max_pages_per_seq and num_pool_pages must be positive");
     if ((int64_t)sh->num_pool_pages * Hk * pa::kPage >= ((int64_t)1 << 31))
@@ -322,6 +330,7 @@ pa_status decode_launch(bool fused, const pa_decode_shapes* sh, const pa_decode_
     a.group = Hq / Hk;
     a.max_pages = sh->max_pages_per_seq;
     a.num_pool_pages = sh->num_pool_pages;
+    a.f16 = f16;
     a.scale_log2 = scale * 1.4426950408889634f;
     a.wait_ns = g_wait_limit_ns.load();
 
@@ -332,9 +341,9 @@ pa_status decode_launch(bool fused, const pa_decode_shapes* sh, const pa_decode_
         const uint64_t dims[2] = {(uint64_t)D, (uint64_t)sh->num_pool_pages * Hk * pa::kPage};
         const uint64_t strides[1] = {(uint64_t)D * 2};
         const uint32_t box[2] = {64, 64};
-        st = make_map_bf16(&mk, k_pool, 2, dims, strides, box);
+        st = make_map_16(f16, &mk, k_pool, 2, dims, strides, box);
         if (st != PA_OK) return st;
-        st = make_map_bf16(&mv, v_pool, 2, dims, strides, box);
+        st = make_map_16(f16, &mv, v_pool, 2, dims, strides, box);
         if (st != PA_OK) return st;
     } else if (D == 128) {
         // e4m3 pages: one 128-byte row per key, one box per 64-row page slab
@@ -370,6 +379,7 @@ pa_status pa_decode_combine(const pa_decode_shapes* sh, const pa_decode_plan* pl
     c.batch = sh->batch;
     c.num_q_heads = sh->num_q_heads;
     c.head_dim = sh->head_dim;
+    c.f16 = sh->kv_dtype == PA_KV_FP16;
     cudaError_t e = pa::launch_combine(c, stream);
     if (e != cudaSuccess) return cuda_fail(e, "combine launch");
     return PA_OK;
@@ -395,6 +405,9 @@ pa_status pa_prefill(const pa_prefill_shapes* sh, const void* q, const void* k, 
     if (Hq <= 0 || Hk <= 0 || Hq % Hk != 0)
         return fail(PA_ERR_INVALID_ARG, "num_q_heads (%d) must be a positive multiple of num_kv_heads (%d)", Hq, Hk);
     if (Hq > 65535) return fail(PA_ERR_UNSUPPORTED, "num_q_heads above 65535");
+    if (sh->dtype != PA_KV_BF16 && sh->dtype != PA_KV_FP16)
+        return fail(PA_ERR_UNSUPPORTED, "prefill dtype must be PA_KV_BF16 or PA_KV_FP16 (got %d)", sh->dtype);
+    const bool f16 = sh->dtype == PA_KV_FP16;
     const bool paged = block_table != nullptr;
     const bool rope = sh->rope_dim != 0;
     if (sh->head_dim_v != 128) return fail(PA_ERR_UNSUPPORTED, "head_dim_v must be 128 (got %d)", sh->head_dim_v);
@@ -429,15 +442,15 @@ pa_status pa_prefill(const pa_prefill_shapes* sh, const void* q, const void* k, 
         const uint64_t dims[3] = {(uint64_t)dqk, (uint64_t)Hq, (uint64_t)sh->total_q};
         const uint64_t strides[2] = {(uint64_t)dqk * 2, (uint64_t)Hq * dqk * 2};
         const uint32_t box[3] = {64, 1, 128};
-        pa_status st = make_map_bf16(&mq, q, 3, dims, strides, box);
+        pa_status st = make_map_16(f16, &mq, q, 3, dims, strides, box);
         if (st != PA_OK) return st;
     }
     if (paged) {
         const uint64_t dims[2] = {128, (uint64_t)sh->num_pool_pages * Hk * pa::kPage};
         const uint64_t strides[1] = {256};
         const uint32_t box[2] = {64, 64};
-        pa_status st = make_map_bf16(&mk, k, 2, dims, strides, box);
-        if (st == PA_OK) st = make_map_bf16(&mv, v, 2, dims, strides, box);
+        pa_status st = make_map_16(f16, &mk, k, 2, dims, strides, box);
+        if (st == PA_OK) st = make_map_16(f16, &mv, v, 2, dims, strides, box);
         if (st != PA_OK) return st;
     } else {
         const uint64_t dk_dims[3] = {(uint64_t)dk, (uint64_t)Hk, (uint64_t)sh->total_k};
@@ -445,13 +458,13 @@ pa_status pa_prefill(const pa_prefill_shapes* sh, const void* q, const void* k, 
         const uint64_t dv_dims[3] = {128, (uint64_t)Hk, (uint64_t)sh->total_k};
         const uint64_t dv_str[2] = {256, (uint64_t)Hk * 256};
         const uint32_t box[3] = {64, 1, 128};
-        pa_status st = make_map_bf16(&mk, k, 3, dk_dims, dk_str, box);
-        if (st == PA_OK) st = make_map_bf16(&mv, v, 3, dv_dims, dv_str, box);
+        pa_status st = make_map_16(f16, &mk, k, 3, dk_dims, dk_str, box);
+        if (st == PA_OK) st = make_map_16(f16, &mv, v, 3, dv_dims, dv_str, box);
         if (st == PA_OK && rope) {
             const uint64_t rd[2] = {64, (uint64_t)sh->total_k};
             const uint64_t rs[1] = {128};
             const uint32_t rb[2] = {64, 128};
-            st = make_map_bf16(&mr, k_rope, 2, rd, rs, rb);
+            st = make_map_16(f16, &mr, k_rope, 2, rd, rs, rb);
         }
         if (st != PA_OK) return st;
     }
@@ -481,6 +494,7 @@ pa_status pa_prefill(const pa_prefill_shapes* sh, const void* q, const void* k, 
     a.causal = causal != 0;
     a.paged = paged;
     a.rope = rope;
+    a.f16 = f16;
     a.scale_log2 = scale * 1.4426950408889634f;
     a.wait_ns = g_wait_limit_ns.load();
     cudaError_t e = pa::launch_prefill(a, dqk, &mq, &mk, &mv, &mr, stream);
@@ -501,7 +515,7 @@ pa_status pa_append_kv(const pa_append_shapes* sh, const void* k_new, const void
     if (sh->page_size != pa::kPage) return fail(PA_ERR_INVALID_ARG, "page_size must be 64 (got %d)", sh->page_size);
     if (sh->max_pages_per_seq <= 0 || sh->num_pool_pages <= 0)
         return fail(PA_ERR_INVALID_ARG, "max_pages_per_seq and num_pool_pages must be positive");
-    if (sh->kv_dtype != PA_KV_BF16 && sh->kv_dtype != PA_KV_FP8_E4M3)
+    if (sh->kv_dtype != PA_KV_BF16 && sh->kv_dtype != PA_KV_FP8_E4M3 && sh->kv_dtype != PA_KV_FP16)
         return fail(PA_ERR_INVALID_ARG, "unknown kv_dtype %d", sh->kv_dtype);
     const bool fp8 = sh->kv_dtype == PA_KV_FP8_E4M3;
     if (!k_new || !v_new || !cu_seqlens_new || !start_pos || !block_table || !k_pool || !v_pool || !workspace)
@@ -566,6 +580,7 @@ pa_prefill_shapes mixed_prefill_shapes(const pa_mixed_shapes* sh, const pa_mixed
     p.max_pages_per_seq = sh->max_pages_per_seq;
     p.num_pool_pages = sh->num_pool_pages;
     p.num_sms = sh->num_sms;
+    p.dtype = sh->kv_dtype;
     return p;
 }
 }  // namespace
@@ -578,7 +593,8 @@ pa_status pa_get_mixed_plan(const int32_t* cu_q, const int32_t* kv_lens, const i
     if (B < 0) return fail(PA_ERR_INVALID_ARG, "batch must be >= 0");
     if (B > 0 && (!cu_q || !kv_lens)) return fail(PA_ERR_INVALID_ARG, "cu_seqlens_q_host and kv_lens_host are needed");
     if (sh->head_dim != 128) return fail(PA_ERR_UNSUPPORTED, "mixed batches need head_dim 128 (got %d)", sh->head_dim);
-    if (sh->kv_dtype != PA_KV_BF16) return fail(PA_ERR_UNSUPPORTED, "mixed batches need bf16 pools");
+    if (sh->kv_dtype != PA_KV_BF16 && sh->kv_dtype != PA_KV_FP16)
+        return fail(PA_ERR_UNSUPPORTED, "mixed batches need bf16 or fp16 pools");
     std::memset(plan, 0, sizeof *plan);
     int nd = 0;
     while (nd < B && cu_q[nd + 1] - cu_q[nd] == 1) ++nd;

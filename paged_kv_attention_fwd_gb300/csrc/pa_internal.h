@@ -31,6 +31,7 @@ struct DecodeArgs {
     int* status;               // status word
     int* counters;             // [B * Hk] split arrivals (fused combine), or nullptr: leave partials
     int32_t batch, num_q_heads, num_kv_heads, group, max_pages, num_pool_pages;
+    int32_t f16;               // 16-bit pages are fp16 (q and out fp16 too), else bf16
     float scale_log2;          // softmax scale * log2(e)
     uint64_t wait_ns;
 };
@@ -42,6 +43,7 @@ struct CombineArgs {
     uint16_t* out;
     float* lse;
     int32_t batch, num_q_heads, head_dim;
+    int32_t f16;  // out is fp16, else bf16
 };
 
 // Launchers (decode.cu).  Return the CUDA error of the launch.
@@ -63,6 +65,7 @@ struct PrefillArgs {
     int32_t batch, num_q_heads, num_kv_heads, group, max_pages, num_pool_pages, total_q;
     int32_t num_q_tiles;  // 256-row query blocks per segment: ceil(max_seqlen_q / 256)
     int32_t causal, paged, rope;
+    int32_t f16;  // q, k, v, k_rope and out are fp16, else bf16
     float scale_log2;
     uint64_t wait_ns;
 };

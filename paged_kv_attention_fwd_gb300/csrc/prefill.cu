@@ -26,6 +26,7 @@
 // j <= qo_offset + i), qo_offset defaulting to kv_len - q_len (MATE
 // _normalize_qo_offset / _resolve_seqused_k).  Every wait is bounded.
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 
 #include "pa_internal.h"
 #include "pa_ptx.cuh"
@@ -67,6 +68,16 @@ struct PrefillLayout {
     static constexpr int kSmem = kBytes + 1024;
     static constexpr int kThreads = 320;
 };
+
+// two values as a packed 16-bit pair (low half first): fp16 or bf16
+__device__ __forceinline__ uint32_t pack16x2(float lo, float hi, bool f16) {
+    if (f16) {
+        const __half2 h = __floats2half2_rn(lo, hi);
+        return *reinterpret_cast<const uint32_t*>(&h);
+    }
+    const __nv_bfloat162 b = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<const uint32_t*>(&b);
+}
 
 __device__ __forceinline__ float ex2(float x) {
     float y;
@@ -277,8 +288,8 @@ __global__ void __launch_bounds__(320, 1)
     } else if (warp == 1) {
         // ---------------------------------------------------------------- MMA issuer
         if (lane == 0) {
-            constexpr uint32_t idesc_qk = idesc_f16(128, 128, true, false, false);
-            constexpr uint32_t idesc_pv = idesc_f16(128, 128, true, false, true);
+            const uint32_t idesc_qk = idesc_f16(128, 128, !a.f16, false, false);
+            const uint32_t idesc_pv = idesc_f16(128, 128, !a.f16, false, true);
             const uint32_t qa = smem_u32(sm + L::kQOff);
             bool ok = mbar_wait(&bars[P_QF], 0, abort_sh, a.wait_ns);
             auto qk = [&](int x, int j) {
@@ -358,6 +369,7 @@ __global__ void __launch_bounds__(320, 1)
         const bool active = x == 0 || has_b;
         const uint32_t lane_addr = (uint32_t)(q4 * 32) << 16;
         const float sl2 = a.scale_log2;
+        const bool f16 = a.f16 != 0;
         // keys this row may see: [0, lim)
         long long lim = sg.kv_len;
         if (causal) lim = min(lim, (long long)sg.off + i + 1);
@@ -446,8 +458,7 @@ __global__ void __launch_bounds__(320, 1)
                         f2_unpack(f2_fma(f2_pack(r[2 * k], r[2 * k + 1]), sc2, nm2), x0, x1);
                         const float p0 = ex2(x0), p1 = ex2(x1);
                         acc2 = f2_add(acc2, f2_pack(__float_as_uint(p0), __float_as_uint(p1)));
-                        const __nv_bfloat162 pk = __floats2bfloat162_rn(p0, p1);
-                        pw[k] = *reinterpret_cast<const uint32_t*>(&pk);
+                        pw[k] = pack16x2(p0, p1, f16);
                     }
                     float a0, a1;
                     f2_unpack(acc2, a0, a1);
@@ -461,8 +472,7 @@ __global__ void __launch_bounds__(320, 1)
                         const float p1 = (none || key + 1 >= vis) ? 0.f : ex2(__uint_as_float(r[2 * k + 1]) * sl2 - m_run);
                         rs0 += p0;
                         rs1 += p1;
-                        const __nv_bfloat162 pk = __floats2bfloat162_rn(p0, p1);
-                        pw[k] = *reinterpret_cast<const uint32_t*>(&pk);
+                        pw[k] = pack16x2(p0, p1, f16);
                     }
                 }
                 tmem_st_x32(tbase + lane_addr + s_col(x) + hh * 32, pw);
@@ -499,11 +509,8 @@ __global__ void __launch_bounds__(320, 1)
                     if (write) {
                         uint32_t w[16];
 #pragma unroll
-                        for (int k = 0; k < 16; ++k) {
-                            const __nv_bfloat162 pk = __floats2bfloat162_rn(__uint_as_float(o[2 * k]) * inv,
-                                                                            __uint_as_float(o[2 * k + 1]) * inv);
-                            w[k] = *reinterpret_cast<const uint32_t*>(&pk);
-                        }
+                        for (int k = 0; k < 16; ++k)
+                            w[k] = pack16x2(__uint_as_float(o[2 * k]) * inv, __uint_as_float(o[2 * k + 1]) * inv, f16);
                         uint4* d4 = reinterpret_cast<uint4*>(dst + c * 32);
 #pragma unroll
                         for (int k = 0; k < 4; ++k) d4[k] = make_uint4(w[4 * k], w[4 * k + 1], w[4 * k + 2], w[4 * k + 3]);

@@ -25,6 +25,15 @@ def as_bf16(bits: np.ndarray, device) -> torch.Tensor:
     return t.to(device).view(torch.bfloat16)
 
 
+def as_f16(bits: np.ndarray, device) -> torch.Tensor:
+    """uint16 fp16 bit patterns -> torch.float16 tensor on `device`."""
+    return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).to(device).view(torch.float16)
+
+
+def as_16(bits: np.ndarray, device, dtype: str) -> torch.Tensor:
+    return as_f16(bits, device) if dtype == "f16" else as_bf16(bits, device)
+
+
 def as_e4m3(bits: np.ndarray, device) -> torch.Tensor:
     return torch.from_numpy(np.ascontiguousarray(bits)).to(device).view(torch.float8_e4m3fn)
 
@@ -45,7 +54,7 @@ def plan_decode(seq_lens_host, block_table_host, num_q_heads: int, num_kv_heads:
     sh = B.pa_decode_shapes(batch=len(seq_lens_host), num_q_heads=num_q_heads, num_kv_heads=num_kv_heads,
                             head_dim=head_dim, page_size=64, max_pages_per_seq=max_pages,
                             num_pool_pages=num_pool_pages,
-                            kv_dtype=B.PA_KV_BF16 if kv_dtype == "bf16" else B.PA_KV_FP8_E4M3,
+                            kv_dtype={"bf16": B.PA_KV_BF16, "e4m3": B.PA_KV_FP8_E4M3, "f16": B.PA_KV_FP16}[kv_dtype],
                             num_sms=sms if sms is not None else num_sms(device), ctas_per_sm=ctas_per_sm,
                             forced_splits=forced_splits)
     meta, plan = B.pa_get_metadata(seq_lens_host, block_table_host, sh)
@@ -58,7 +67,8 @@ def decode(p: DecodePlan, q, k_pool, v_pool, block_table, seq_lens, scale: float
            out=None, lse=None, stream=None):
     sh = p.shapes
     if out is None:
-        out = torch.empty((sh.batch, sh.num_q_heads, sh.head_dim), dtype=torch.bfloat16, device=q.device)
+        odt = torch.float16 if sh.kv_dtype == B.PA_KV_FP16 else torch.bfloat16
+        out = torch.empty((sh.batch, sh.num_q_heads, sh.head_dim), dtype=odt, device=q.device)
     if lse is None:
         lse = torch.empty((sh.batch, sh.num_q_heads), dtype=torch.float32, device=q.device)
     B.pa_decode(sh, p.plan, q, k_pool, v_pool, k_scale, v_scale, block_table, seq_lens, p.meta_dev, scale, out,
@@ -67,19 +77,20 @@ def decode(p: DecodePlan, q, k_pool, v_pool, block_table, seq_lens, scale: float
 
 
 def prefill_shapes(batch, num_q_heads, num_kv_heads, head_dim_qk, head_dim_v, rope_dim, max_seqlen_q, total_q,
-                   total_k, max_pages=0, num_pool_pages=0, device="cuda") -> B.pa_prefill_shapes:
+                   total_k, max_pages=0, num_pool_pages=0, device="cuda", dtype: str = "bf16") -> B.pa_prefill_shapes:
     return B.pa_prefill_shapes(batch=batch, num_q_heads=num_q_heads, num_kv_heads=num_kv_heads,
                                head_dim_qk=head_dim_qk, head_dim_v=head_dim_v, rope_dim=rope_dim,
                                max_seqlen_q=max_seqlen_q, total_q=total_q, total_k=total_k, page_size=64,
                                max_pages_per_seq=max_pages, num_pool_pages=num_pool_pages,
-                               num_sms=num_sms(device))
+                               num_sms=num_sms(device), dtype=B.PA_KV_FP16 if dtype == "f16" else B.PA_KV_BF16)
 
 
 def prefill(sh: B.pa_prefill_shapes, q, k, v, cu_seqlens_q, cu_seqlens_k, scale: float, causal: bool = True,
             block_table=None, k_rope=None, qo_offset=None, out=None, lse=None, workspace=None, stream=None):
     dev = q.device
     if out is None:
-        out = torch.empty((sh.total_q, sh.num_q_heads, sh.head_dim_v), dtype=torch.bfloat16, device=dev)
+        odt = torch.float16 if sh.dtype == B.PA_KV_FP16 else torch.bfloat16
+        out = torch.empty((sh.total_q, sh.num_q_heads, sh.head_dim_v), dtype=odt, device=dev)
     if lse is None:
         lse = torch.empty((sh.total_q, sh.num_q_heads), dtype=torch.float32, device=dev)
     if workspace is None:

@@ -100,6 +100,16 @@ def bf16_normal(seed: int, stream: int, shape) -> np.ndarray:
     return f32_to_bf16_bits(normal_f32(seed, stream, n)).reshape(shape)
 
 
+def f16_normal(seed: int, stream: int, shape) -> np.ndarray:
+    """N(0,1) rounded to IEEE fp16 (nearest even); uint16 bit patterns."""
+    n = int(np.prod(shape)) if len(shape) else 1
+    return normal_f32(seed, stream, n).astype(np.float16).view(np.uint16).reshape(shape)
+
+
+def normal_16(seed: int, stream: int, shape, dtype: str) -> np.ndarray:
+    return f16_normal(seed, stream, shape) if dtype == "f16" else bf16_normal_fast(seed, stream, shape)
+
+
 def cu_seqlens(lengths: np.ndarray) -> np.ndarray:
     """int32 [n+1] running offsets of ragged segments (first entry 0)."""
     out = np.zeros(len(lengths) + 1, dtype=np.int64)
@@ -143,7 +153,7 @@ class DecodeInputs:
     block_table: np.ndarray  # int32 [B, max_pages]
     seq_lens: np.ndarray     # int32 [B]
     scale: float
-    kv_dtype: str            # "bf16" | "e4m3"
+    kv_dtype: str            # "bf16" | "e4m3" | "f16" (fp16 q and pools)
     k_scale: Optional[np.ndarray] = None   # float32 [Hk] (e4m3 only)
     v_scale: Optional[np.ndarray] = None
     meta: dict = field(default_factory=dict)
@@ -205,11 +215,11 @@ def make_decode(batch: int, num_q_heads: int, num_kv_heads: int, head_dim: int,
     assert len(seq_lens) == batch
     bt, num_pool = assign_pages(seq_lens, seed, extra_pages, max_pages)
     pool_shape = (num_pool, num_kv_heads, PAGE_SIZE, head_dim)
-    q = bf16_normal(seed, _S_Q, (batch, num_q_heads, head_dim))
+    q = (f16_normal if kv_dtype == "f16" else bf16_normal)(seed, _S_Q, (batch, num_q_heads, head_dim))
     n = int(np.prod(pool_shape))
-    if kv_dtype == "bf16":
-        k = bf16_normal_fast(seed, _S_K, pool_shape)
-        v = bf16_normal_fast(seed, _S_V, pool_shape)
+    if kv_dtype in ("bf16", "f16"):
+        k = normal_16(seed, _S_K, pool_shape, kv_dtype)
+        v = normal_16(seed, _S_V, pool_shape, kv_dtype)
         ks = vs = None
     elif kv_dtype == "e4m3":
         k, ks = quantise_per_head(normal_f32(seed, _S_K, n).reshape(pool_shape))
@@ -276,6 +286,7 @@ class PrefillInputs:
     block_table: Optional[np.ndarray] = None   # int32 [B, max_pages] when paged
     k_rope: Optional[np.ndarray] = None        # uint16 [total_k, 1, rope_dim]
     qo_offset: Optional[np.ndarray] = None     # int32 [B] (None: kv_len - q_len)
+    dtype: str = "bf16"                         # element type of q, k, v, k_rope: "bf16" | "f16"
     meta: dict = field(default_factory=dict)
 
     @property
@@ -298,19 +309,19 @@ class PrefillInputs:
 
 def make_paged_prefill(q_lens, kv_lens, num_q_heads: int, num_kv_heads: int, head_dim: int,
                        seed: int = 0, extra_pages: int = 0, qo_offset=None,
-                       causal: bool = True) -> PrefillInputs:
+                       causal: bool = True, dtype: str = "bf16") -> PrefillInputs:
     q_lens = np.asarray(q_lens, dtype=np.int32)
     kv_lens = np.asarray(kv_lens, dtype=np.int32)
     bt, num_pool = assign_pages(kv_lens, seed, extra_pages)
     total_q = int(q_lens.sum())
     pool_shape = (num_pool, num_kv_heads, PAGE_SIZE, head_dim)
     return PrefillInputs(
-        q=bf16_normal_fast(seed, _S_Q, (total_q, num_q_heads, head_dim)),
-        k=bf16_normal_fast(seed, _S_K, pool_shape),
-        v=bf16_normal_fast(seed, _S_V, pool_shape),
+        q=normal_16(seed, _S_Q, (total_q, num_q_heads, head_dim), dtype),
+        k=normal_16(seed, _S_K, pool_shape, dtype),
+        v=normal_16(seed, _S_V, pool_shape, dtype),
         cu_seqlens_q=cu_seqlens(q_lens), cu_seqlens_k=cu_seqlens(kv_lens),
         scale=1.0 / math.sqrt(head_dim), causal=causal, block_table=bt,
-        qo_offset=None if qo_offset is None else np.asarray(qo_offset, dtype=np.int32))
+        qo_offset=None if qo_offset is None else np.asarray(qo_offset, dtype=np.int32), dtype=dtype)
 
 
 def chunked_prefill(seed: int = 0, batch: int = 8, q_len: int = 512, max_prefix: int = 8192,
@@ -325,7 +336,7 @@ def chunked_prefill(seed: int = 0, batch: int = 8, q_len: int = 512, max_prefix:
 
 def make_ragged_prefill(lens, num_heads: int, head_dim_qk: int, head_dim_v: int,
                         rope_dim: int = 0, seed: int = 0, num_kv_heads: Optional[int] = None,
-                        kv_lens=None, causal: bool = True, qo_offset=None) -> PrefillInputs:
+                        kv_lens=None, causal: bool = True, qo_offset=None, dtype: str = "bf16") -> PrefillInputs:
     """Ragged q/k/v packed by running offsets; with rope_dim > 0 the MLA layout:
     q [T, H, Dk + rope], k [T, H, Dk], k_rope [T, 1, rope], v [T, H, Dv]."""
     lens = np.asarray(lens, dtype=np.int32)
@@ -334,13 +345,13 @@ def make_ragged_prefill(lens, num_heads: int, head_dim_qk: int, head_dim_v: int,
     tq, tk = int(lens.sum()), int(kv_lens.sum())
     dk = head_dim_qk - rope_dim
     return PrefillInputs(
-        q=bf16_normal_fast(seed, _S_Q, (tq, num_heads, head_dim_qk)),
-        k=bf16_normal_fast(seed, _S_K, (tk, hk, dk)),
-        v=bf16_normal_fast(seed, _S_V, (tk, hk, head_dim_v)),
+        q=normal_16(seed, _S_Q, (tq, num_heads, head_dim_qk), dtype),
+        k=normal_16(seed, _S_K, (tk, hk, dk), dtype),
+        v=normal_16(seed, _S_V, (tk, hk, head_dim_v), dtype),
         cu_seqlens_q=cu_seqlens(lens), cu_seqlens_k=cu_seqlens(kv_lens),
         scale=1.0 / math.sqrt(head_dim_qk), causal=causal,
-        k_rope=bf16_normal(seed, _S_KROPE, (tk, 1, rope_dim)) if rope_dim else None,
-        qo_offset=None if qo_offset is None else np.asarray(qo_offset, dtype=np.int32))
+        k_rope=normal_16(seed, _S_KROPE, (tk, 1, rope_dim), dtype) if rope_dim else None,
+        qo_offset=None if qo_offset is None else np.asarray(qo_offset, dtype=np.int32), dtype=dtype)
 
 
 def mla_prefill(seed: int = 0, batch: int = 8, lo: int = 512, hi: int = 4096,

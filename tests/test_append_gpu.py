@@ -26,33 +26,35 @@ def case(kv_dtype, hk=4, d=128, prior=(0, 63, 64, 130, 1000), new=(5, 1, 70, 200
     prior = np.array(prior, np.int32)
     new = np.array(new, np.int32)
     base = W.make_decode(len(prior), hk, hk, d, prior + new, seed=seed, kv_dtype=kv_dtype, extra_pages=3)
-    kn = W.bf16_normal(seed, 90, (int(new.sum()), hk, d))
-    vn = W.bf16_normal(seed, 91, (int(new.sum()), hk, d))
+    src = "f16" if kv_dtype == "f16" else "bf16"
+    kn = W.normal_16(seed, 90, (int(new.sum()), hk, d), src)
+    vn = W.normal_16(seed, 91, (int(new.sum()), hk, d), src)
     return base, prior, new, kn, vn
 
 
 def gpu_append(base, prior, new, kn, vn, block_table=None):
     dev = "cuda"
-    conv = ops.as_bf16 if base.kv_dtype == "bf16" else ops.as_e4m3
+    conv = {"bf16": ops.as_bf16, "e4m3": ops.as_e4m3, "f16": ops.as_f16}[base.kv_dtype]
     kp, vp = conv(base.k_pool, dev), conv(base.v_pool, dev)
     bt = base.block_table if block_table is None else block_table
     sh = B.pa_append_shapes(batch=len(prior), num_kv_heads=base.num_kv_heads, head_dim=base.head_dim, page_size=64,
                             max_pages_per_seq=bt.shape[1], num_pool_pages=base.num_pool_pages,
                             total_new=int(new.sum()),
-                            kv_dtype=B.PA_KV_BF16 if base.kv_dtype == "bf16" else B.PA_KV_FP8_E4M3)
+                            kv_dtype={"bf16": B.PA_KV_BF16, "e4m3": B.PA_KV_FP8_E4M3, "f16": B.PA_KV_FP16}[base.kv_dtype])
     ks = torch.from_numpy(base.k_scale).to(dev) if base.k_scale is not None else None
     vs = torch.from_numpy(base.v_scale).to(dev) if base.v_scale is not None else None
     ws = torch.zeros(B.PA_STATUS_BYTES, dtype=torch.uint8, device=dev)
-    B.pa_append_kv(sh, ops.as_bf16(kn, dev), ops.as_bf16(vn, dev), torch.from_numpy(W.cu_seqlens(new)).to(dev),
+    src = ops.as_f16 if base.kv_dtype == "f16" else ops.as_bf16
+    B.pa_append_kv(sh, src(kn, dev), src(vn, dev), torch.from_numpy(W.cu_seqlens(new)).to(dev),
                    torch.from_numpy(prior).to(dev), torch.from_numpy(bt).to(dev), kp, vp, ks, vs, ws)
     st = B.pa_check_status(ws)
-    npdt = np.int16 if base.kv_dtype == "bf16" else np.uint8
-    k_out = kp.view(torch.int16 if base.kv_dtype == "bf16" else torch.uint8).cpu().numpy().view(base.k_pool.dtype)
-    v_out = vp.view(torch.int16 if base.kv_dtype == "bf16" else torch.uint8).cpu().numpy().view(base.v_pool.dtype)
+    raw = torch.uint8 if base.kv_dtype == "e4m3" else torch.int16
+    k_out = kp.view(raw).cpu().numpy().view(base.k_pool.dtype)
+    v_out = vp.view(raw).cpu().numpy().view(base.v_pool.dtype)
     return k_out, v_out, st
 
 
-@pytest.mark.parametrize("kv_dtype,d", [("bf16", 128), ("bf16", 64), ("e4m3", 128), ("e4m3", 64)])
+@pytest.mark.parametrize("kv_dtype,d", [("bf16", 128), ("bf16", 64), ("e4m3", 128), ("e4m3", 64), ("f16", 128)])
 def test_append_bit_exact(kv_dtype, d):
     base, prior, new, kn, vn = case(kv_dtype, d=d)
     k_gpu, v_gpu, st = gpu_append(base, prior, new, kn, vn)

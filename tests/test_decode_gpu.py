@@ -16,7 +16,7 @@ from paged_kv_attention_fwd_gb300.build import build
 
 pytestmark = pytest.mark.gpu
 
-TOL = {"bf16": (1e-2, 1e-3), "e4m3": (5e-2, 5e-3)}
+TOL = {"bf16": (1e-2, 1e-3), "e4m3": (5e-2, 5e-3), "f16": (1e-2, 1e-3)}
 LSE_TOL = 1e-3
 
 
@@ -29,8 +29,8 @@ def gpu():
 
 
 def to_dev(inp: W.DecodeInputs, dev="cuda"):
-    q = ops.as_bf16(inp.q, dev)
-    conv = ops.as_bf16 if inp.kv_dtype == "bf16" else ops.as_e4m3
+    q = ops.as_f16(inp.q, dev) if inp.kv_dtype == "f16" else ops.as_bf16(inp.q, dev)
+    conv = {"bf16": ops.as_bf16, "e4m3": ops.as_e4m3, "f16": ops.as_f16}[inp.kv_dtype]
     kp, vp = conv(inp.k_pool, dev), conv(inp.v_pool, dev)
     bt = torch.from_numpy(np.ascontiguousarray(inp.block_table)).to(dev)
     sl = torch.from_numpy(np.ascontiguousarray(inp.seq_lens)).to(dev)
@@ -214,3 +214,15 @@ def test_fused_merge_matches_two_kernel_form(kv_dtype):
         assert (l1 - l2).abs().max().item() <= 1e-5
     ref_out, ref_lse = reference(inp)
     assert_close(o1.float().cpu().numpy(), l1.cpu().numpy(), ref_out, ref_lse, kv_dtype)
+
+
+
+@pytest.mark.parametrize("hq,hk,d", [(32, 8, 128), (8, 4, 64), (16, 1, 128)])
+def test_fp16_decode(hq, hk, d):
+    """fp16 query, pools and output (the three share one type)."""
+    lens = [0, 1, 63, 64, 65, 200, 1000, 3000]
+    inp = W.make_decode(len(lens), hq, hk, d, lens, seed=80 + hq, kv_dtype="f16", extra_pages=2)
+    out, lse, st, p = run(inp)
+    assert st == B.PA_OK
+    ref_out, ref_lse = reference(inp)
+    assert_close(out, lse, ref_out, ref_lse, "f16")

@@ -44,6 +44,18 @@ def test_bf16_decoder_all_codes():
     assert np.array_equal(got[~nan], ref[~nan])
 
 
+def test_f16_decoder_all_codes():
+    codes = np.arange(65536, dtype=np.uint32).astype(np.uint16)
+    ref = torch.from_numpy(codes.view(np.int16)).view(torch.float16).to(torch.float64).numpy()
+    got = oracle.f16_to_f64(codes)
+    nan = np.isnan(ref)
+    assert np.array_equal(np.isnan(got), nan) and np.array_equal(got[~nan], ref[~nan])
+
+
+def t_f16(bits):
+    return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).view(torch.float16).to(torch.float64)
+
+
 def test_e4m3_decoder_all_codes():
     codes = np.arange(256, dtype=np.uint8)
     ref = t_e4m3(codes).numpy()
@@ -85,17 +97,17 @@ def _sdpa(q, k, v, scale, mask=None):
     return out, torch.logsumexp(s, dim=-1)
 
 
-@pytest.mark.parametrize("kv_dtype", ["bf16", "e4m3"])
+@pytest.mark.parametrize("kv_dtype", ["bf16", "e4m3", "f16"])
 def test_decode_matches_torch_sdpa(kv_dtype):
     inp = W.make_decode(3, 8, 2, 64, [1, 65, 200], seed=5, kv_dtype=kv_dtype, extra_pages=3)
     out, lse = oracle.decode(inp.q, inp.k_pool, inp.v_pool, inp.block_table, inp.seq_lens,
                              inp.scale, kv_dtype, inp.k_scale, inp.v_scale)
-    dec = t_bf16 if kv_dtype == "bf16" else t_e4m3
+    dec = {"bf16": t_bf16, "e4m3": t_e4m3, "f16": t_f16}[kv_dtype]
     kp, vp = dec(inp.k_pool), dec(inp.v_pool)
     if kv_dtype == "e4m3":
         kp = kp * torch.as_tensor(inp.k_scale, dtype=torch.float64)[None, :, None, None]
         vp = vp * torch.as_tensor(inp.v_scale, dtype=torch.float64)[None, :, None, None]
-    q = t_bf16(inp.q)
+    q = t_f16(inp.q) if kv_dtype == "f16" else t_bf16(inp.q)
     G = inp.num_q_heads // inp.num_kv_heads
     for b, n in enumerate(inp.seq_lens):
         k = _gather_dense(kp, inp.block_table[b], int(n)).repeat_interleave(G, 0)
@@ -105,11 +117,13 @@ def test_decode_matches_torch_sdpa(kv_dtype):
         np.testing.assert_allclose(lse[b], rl[:, 0].numpy(), rtol=1e-12, atol=1e-12)
 
 
-def test_paged_prefill_matches_torch_sdpa():
-    inp = W.make_paged_prefill([5, 70, 1], [40, 200, 64], 4, 2, 64, seed=9, extra_pages=2)
+@pytest.mark.parametrize("dtype", ["bf16", "f16"])
+def test_paged_prefill_matches_torch_sdpa(dtype):
+    inp = W.make_paged_prefill([5, 70, 1], [40, 200, 64], 4, 2, 64, seed=9, extra_pages=2, dtype=dtype)
     out, lse = oracle.prefill(inp.q, inp.k, inp.v, inp.cu_seqlens_q, inp.cu_seqlens_k, inp.scale,
-                              True, block_table=inp.block_table)
-    kp, vp, q = t_bf16(inp.k), t_bf16(inp.v), t_bf16(inp.q)
+                              True, block_table=inp.block_table, dtype=dtype)
+    dec = t_f16 if dtype == "f16" else t_bf16
+    kp, vp, q = dec(inp.k), dec(inp.v), dec(inp.q)
     for b in range(inp.batch):
         q0, q1 = inp.cu_seqlens_q[b], inp.cu_seqlens_q[b + 1]
         n = int(inp.cu_seqlens_k[b + 1] - inp.cu_seqlens_k[b])

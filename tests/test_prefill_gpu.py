@@ -24,10 +24,10 @@ def gpu():
 
 def run(inp: W.PrefillInputs, causal=True):
     dev = "cuda"
-    q = ops.as_bf16(inp.q, dev)
-    k = ops.as_bf16(inp.k, dev)
-    v = ops.as_bf16(inp.v, dev)
-    kr = ops.as_bf16(inp.k_rope, dev) if inp.k_rope is not None else None
+    q = ops.as_16(inp.q, dev, inp.dtype)
+    k = ops.as_16(inp.k, dev, inp.dtype)
+    v = ops.as_16(inp.v, dev, inp.dtype)
+    kr = ops.as_16(inp.k_rope, dev, inp.dtype) if inp.k_rope is not None else None
     cq = torch.from_numpy(inp.cu_seqlens_q).to(dev)
     ck = torch.from_numpy(inp.cu_seqlens_k).to(dev)
     bt = torch.from_numpy(inp.block_table).to(dev) if inp.paged else None
@@ -36,7 +36,7 @@ def run(inp: W.PrefillInputs, causal=True):
     sh = ops.prefill_shapes(inp.batch, inp.num_q_heads, inp.num_kv_heads, inp.head_dim_qk, inp.head_dim_v,
                             inp.rope_dim, inp.max_seqlen_q, int(inp.cu_seqlens_q[-1]), kv_total,
                             max_pages=inp.block_table.shape[1] if inp.paged else 0,
-                            num_pool_pages=inp.k.shape[0] if inp.paged else 0)
+                            num_pool_pages=inp.k.shape[0] if inp.paged else 0, dtype=inp.dtype)
     out, lse, ws = ops.prefill(sh, q, k, v, cq, ck, inp.scale, causal, block_table=bt, k_rope=kr, qo_offset=qo)
     st = B.pa_check_status(ws)
     return out.float().cpu().numpy(), lse.cpu().numpy(), st
@@ -44,7 +44,8 @@ def run(inp: W.PrefillInputs, causal=True):
 
 def reference(inp: W.PrefillInputs, causal=True, rows=None):
     return oracle.prefill(inp.q, inp.k, inp.v, inp.cu_seqlens_q, inp.cu_seqlens_k, inp.scale, causal,
-                          block_table=inp.block_table, k_rope=inp.k_rope, qo_offset=inp.qo_offset, rows=rows)
+                          block_table=inp.block_table, k_rope=inp.k_rope, qo_offset=inp.qo_offset, rows=rows,
+                          dtype=inp.dtype)
 
 
 def assert_close(out, lse, ref_out, ref_lse, max_tol=1e-2, mean_tol=1e-3):
@@ -204,3 +205,18 @@ def test_full_size_repeats_bitwise(name):
         again = run(inp)
         assert again[2] == B.PA_OK
         assert np.array_equal(first[0], again[0]) and np.array_equal(first[1], again[1])
+
+
+
+@pytest.mark.parametrize("kind", ["paged", "ragged", "mla"])
+def test_fp16_prefill(kind):
+    if kind == "paged":
+        inp = W.make_paged_prefill([5, 130, 300], [5, 400, 1300], 8, 2, 128, seed=81, dtype="f16")
+    elif kind == "ragged":
+        inp = W.make_ragged_prefill([1, 129, 257, 600], 4, 128, 128, seed=82, dtype="f16")
+    else:
+        inp = W.make_ragged_prefill([50, 300, 513], 4, 192, 128, rope_dim=64, seed=83, dtype="f16")
+    out, lse, st = run(inp)
+    assert st == B.PA_OK
+    ro, rl = reference(inp)
+    assert_close(out, lse, ro, rl)
