@@ -103,7 +103,7 @@ typedef struct {
  *
  * Split rule (integers only, deterministic):
  *   pages_b = ceil(len_b / 64); units = sum_b pages_b * Hk;
- *   cap = num_sms * ctas_per_sm; chunk = max(4, ceil(units / (4 * cap)));
+ *   cap = num_sms * ctas_per_sm; chunk = max(4, ceil(units / (2 * cap)));
  *   n_b = 1 if pages_b <= 1, else min(forced, pages_b, 64) if forced > 0,
  *   else min(ceil(pages_b / chunk), 64).  Split s of b covers pages
  *   [floor(s * pages_b / n_b), floor((s + 1) * pages_b / n_b)).
@@ -128,7 +128,7 @@ pa_status pa_get_metadata(const int32_t* seq_lens_host, const int32_t* block_tab
  *
  * pa_get_static_plan (host, no lengths): a plan that covers every length mix
  * of `batch` sequences -- the split rule yields at most
- * batch + ceil(4 * num_sms * ctas_per_sm / Hk) splits (batch * min(forced, 64)
+ * batch + ceil(2 * num_sms * ctas_per_sm / Hk) splits (batch * min(forced, 64)
  * with forced splits).  Use it for pa_decode and for sizing the metadata
  * buffer (plan->meta_ints) and the workspace.  Limits: batch <= 8192, at most
  * 16384 work items (splits * Hk); PA_ERR_UNSUPPORTED beyond.

@@ -13,7 +13,7 @@ reading used here, written out step by step:
   pages_b   = ceil(max(seq_b, 0) / 64)
   units     = sum_b pages_b * Hk
   cap       = num_sms * ctas_per_sm                      (persistent CTAs)
-  chunk     = max(4, ceil(units / (cap * 4)))            (4 items per CTA share)
+  chunk     = max(4, ceil(units / (cap * 2)))            (2 items per CTA share)
   n_b       = 1                              if pages_b <= 1
             = min(forced, pages_b, 64)       if forced > 0
             = min(ceil(pages_b / chunk), 64) otherwise
@@ -41,7 +41,7 @@ import heapq
 MAGIC = 0x50414D31
 PAGE = 64
 MAX_SPLITS = 64
-ITEMS_PER_SHARE = 4
+ITEMS_PER_SHARE = 2
 MIN_CHUNK = 4
 
 
@@ -129,8 +129,8 @@ def unpack(meta):
 
 def static_split_capacity(batch: int, num_kv_heads: int, num_sms: int, ctas_per_sm: int, forced_splits: int = 0):
     """Most splits the rule can produce for `batch` sequences of any lengths:
-    sum_b ceil(pages_b / chunk) <= sum_b pages_b / chunk + B <= 4 * cap / Hk + B."""
+    sum_b ceil(pages_b / chunk) <= sum_b pages_b / chunk + B <= ITEMS_PER_SHARE * cap / Hk + B."""
     if forced_splits > 0:
         return batch * min(forced_splits, MAX_SPLITS)
     cap = num_sms * ctas_per_sm
-    return batch + _cdiv(4 * cap, num_kv_heads)
+    return batch + _cdiv(ITEMS_PER_SHARE * cap, num_kv_heads)

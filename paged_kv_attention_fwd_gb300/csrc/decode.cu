@@ -7,7 +7,10 @@
 // Within a CTA the pages stream through a multi-stage shared-memory ring:
 //
 //   warp 0      producer: block_table lookup, TMA (bf16, 128-byte swizzle) or
-//               plain bulk copies (e4m3) of whole 64 x D page slabs
+//               plain bulk copies (e4m3) of whole 64 x D page slabs; with
+//               16-bit pages also each item's query rows (one TMA box of the
+//               group's heads), so that no thread waits on a global load
+//               between items
 //   warp 1      MMA issuer: tcgen05.mma, f32 accumulators in TMEM
 //                 S^T[128 keys, 16 heads] = K_tile[128, D] . Q_group[16, D]^T
 //                 O^T[D, 16 heads]        = V_tile^T[D, 128] . P^T[128, 16]
@@ -55,7 +58,8 @@ enum : int {
     B_VHE = 21,    // [2] e4m3: converted V tile consumed
     B_PW = 23,     // [2] an item's partials written (merge warp)
     B_HD = 25,     // [2] merge warp done with an item
-    B_COUNT = 27
+    B_QE = 27,     // [2] query tile free again (16-bit pages: its last QK retired)
+    B_COUNT = 29
 };
 
 constexpr uint32_t kTmemCols = 64;
@@ -285,7 +289,7 @@ __device__ __forceinline__ uint16_t f32_to_16(float x, bool f16) {
 template <int D, bool FP8, int NP>
 __global__ void __launch_bounds__(DecodeLayout<D, FP8>::kThreads, 1)
     decode_kernel(const __grid_constant__ DecodeArgs a, const __grid_constant__ CUtensorMap map_k,
-                  const __grid_constant__ CUtensorMap map_v) {
+                  const __grid_constant__ CUtensorMap map_v, const __grid_constant__ CUtensorMap map_q) {
     using L = DecodeLayout<D, FP8>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -310,7 +314,8 @@ __global__ void __launch_bounds__(DecodeLayout<D, FP8>::kThreads, 1)
             mbar_init(&bars[B_EMPTY + s], FP8 ? 128 : 1);
         }
         for (int i = 0; i < 2; ++i) {
-            mbar_init(&bars[B_QF + i], 128);
+            mbar_init(&bars[B_QF + i], FP8 ? 128 : 1);
+            mbar_init(&bars[B_QE + i], 1);
             mbar_init(&bars[B_SF + i], 1);
             mbar_init(&bars[B_PF + i], 128);
             mbar_init(&bars[B_OF + i], 1);
@@ -332,9 +337,15 @@ __global__ void __launch_bounds__(DecodeLayout<D, FP8>::kThreads, 1)
         tmem_relinquish();
     }
     if (warp >= 2 && warp < 6) {
-        // P rows of padding heads must read as zero in every PV product
+        // P rows of padding heads must read as zero in every PV product, and
+        // so must the query rows past the group (the query TMA writes only
+        // the group's rows)
         uint4* p = reinterpret_cast<uint4*>(sm + L::kPOff);
         for (int i = threadIdx.x - 64; i < 2 * L::kPBytes / 16; i += 128) p[i] = make_uint4(0, 0, 0, 0);
+        if constexpr (!FP8) {
+            uint4* qz = reinterpret_cast<uint4*>(sm + L::kQOff);
+            for (int i = threadIdx.x - 64; i < 2 * L::kQBytes / 16; i += 128) qz[i] = make_uint4(0, 0, 0, 0);
+        }
         fence_proxy_async_smem();
     }
     tc_fence_before();
@@ -345,15 +356,33 @@ __global__ void __launch_bounds__(DecodeLayout<D, FP8>::kThreads, 1)
     if (warp == 0) {
         // ------------------------------------------------------------ producer
         if (lane == 0) {
-            uint32_t g = 0;
-            uint32_t last_par[4] = {0, 0, 0, 0};
-            bool issued[4] = {false, false, false, false};
+            uint32_t g = 0, qn = 0;
+            uint32_t last_par[4] = {0, 0, 0, 0}, q_par[2] = {0, 0};
+            bool issued[4] = {false, false, false, false}, q_issued[2] = {false, false};
             bool ok = true;
             constexpr uint32_t page_bytes = FP8 ? 64u * D : 64u * D * 2u;
             for (int j = it_lo; j < it_hi && ok; ++j) {
                 const Item it = load_item(a, j, items_off);
                 const int ntiles = item_tiles(it);
                 const long long bt_row = (long long)it.b * a.max_pages;
+                if (!FP8 && ntiles > 0) {
+                    // the group's query rows -> rows 0..G-1 of query buffer qn & 1
+                    const uint32_t qs = qn & 1;
+                    if (!mbar_wait(&bars[B_QE + qs], ((qn >> 1) & 1) ^ 1, abort_sh, a.wait_ns)) {
+                        fail(a, abort_sh, PA_ERR_TIMEOUT);
+                        ok = false;
+                        break;
+                    }
+                    uint64_t* qf = &bars[B_QF + qs];
+                    mbar_arrive_expect_tx(qf, (uint32_t)a.group * D * 2u);
+                    const int qrow = it.b * a.num_q_heads + it.kvh * a.group;
+#pragma unroll
+                    for (int c = 0; c < L::kChunks; ++c)
+                        tma_load_2d(sm + L::kQOff + qs * L::kQBytes + c * (kNPad * 128), &map_q, qf, c * 64, qrow);
+                    q_par[qs] = (qn >> 1) & 1;
+                    q_issued[qs] = true;
+                    ++qn;
+                }
                 for (int t = 0; t < ntiles; ++t, ++g) {
                     const int stage = g % L::kStages;
                     const int pa0 = it.p0 + 2 * t;
@@ -399,6 +428,8 @@ __global__ void __launch_bounds__(DecodeLayout<D, FP8>::kThreads, 1)
             // every issued copy must land before the CTA may exit
             for (int s = 0; s < L::kStages; ++s)
                 if (issued[s]) mbar_wait(&bars[B_FULL + s], last_par[s], nullptr, a.wait_ns);
+            for (int s = 0; s < 2; ++s)
+                if (q_issued[s]) mbar_wait(&bars[B_QF + s], q_par[s], nullptr, a.wait_ns);
         }
     } else if (warp == 1) {
         // ------------------------------------------------------------ MMA issuer
@@ -436,7 +467,8 @@ __global__ void __launch_bounds__(DecodeLayout<D, FP8>::kThreads, 1)
                     ok = false;
                     break;
                 }
-                const uint32_t qbase = smem_u32(sm + L::kQOff + (qi & 1) * L::kQBytes);
+                const uint32_t qslot = qi & 1;
+                const uint32_t qbase = smem_u32(sm + L::kQOff + qslot * L::kQBytes);
                 ++qi;
                 for (int t = 0; t < ntiles; ++t, ++g) {
                     const int stage = g % L::kStages;
@@ -465,6 +497,7 @@ __global__ void __launch_bounds__(DecodeLayout<D, FP8>::kThreads, 1)
                     }
                     pending = true;
                 }
+                if (!FP8) mma_commit(&bars[B_QE + qslot]);  // the item's QKs are all issued
             }
             if (ok && pending && !issue_pv(g - 1)) fail(a, abort_sh, PA_ERR_TIMEOUT);
             // all MMAs must retire before TMEM is freed and shared memory released
@@ -515,9 +548,11 @@ __global__ void __launch_bounds__(DecodeLayout<D, FP8>::kThreads, 1)
 
         int qload = next_nonempty(it_lo);
         uint32_t qload_idx = 0;
-        for (int k = 0; k < 2 && qload < it_hi; ++k) {
-            load_q(qload, qload_idx++);
-            qload = next_nonempty(qload + 1);
+        if constexpr (FP8) {
+            for (int k = 0; k < 2 && qload < it_hi; ++k) {
+                load_q(qload, qload_idx++);
+                qload = next_nonempty(qload + 1);
+            }
         }
 
         uint32_t g = 0, qi = 0, npartial = 0;
@@ -550,7 +585,7 @@ __global__ void __launch_bounds__(DecodeLayout<D, FP8>::kThreads, 1)
                 }
                 continue;
             }
-            if (qi >= 1 && qload < it_hi) {
+            if (FP8 && qi >= 1 && qload < it_hi) {
                 load_q(qload, qload_idx++);
                 qload = next_nonempty(qload + 1);
             }
@@ -956,25 +991,32 @@ __global__ void __launch_bounds__(224, 1)
             while (j < it_hi && item_tiles(load_item(a, j, items_off)) == 0) ++j;
             return j;
         };
-        // query of the item's KV group -> three e4m3 levels (rows level*16 + head)
-        auto load_q = [&](int j, uint32_t qidx) {
+        // query of the item's KV group -> three e4m3 levels (rows level*16 + head).
+        // fetch_q only issues the global loads (into pf0/pf1); store_q, one
+        // item later, converts and writes, so the load latency is hidden.
+        const int qh = row >> 3, qc = row & 7;  // head, 16-element chunk of d
+        uint4 pf0 = make_uint4(0, 0, 0, 0), pf1 = make_uint4(0, 0, 0, 0);
+        auto fetch_q = [&](int j) {
             const Item it = load_item(a, j, items_off);
+            pf0 = pf1 = make_uint4(0, 0, 0, 0);
+            if (qh < G) {
+                const long long qrow = (long long)it.b * a.num_q_heads + (long long)it.kvh * G + qh;
+                const uint4* src = reinterpret_cast<const uint4*>(a.q + qrow * D) + 2 * qc;
+                pf0 = __ldg(src);
+                pf1 = __ldg(src + 1);
+            }
+        };
+        auto store_q = [&](uint32_t qidx) {
             uint8_t* qb = sm + L::kQ3Off + (qidx & 1) * L::kQ3Bytes;
-            const int h = row >> 3, c = row & 7;  // head, 16-element chunk of d
+            const int h = qh, c = qc;
             float v[16];
-            if (h < G) {
-                const long long qrow = (long long)it.b * a.num_q_heads + (long long)it.kvh * G + h;
-                const uint4* src = reinterpret_cast<const uint4*>(a.q + qrow * D) + 2 * c;
-                const uint4 w0 = __ldg(src), w1 = __ldg(src + 1);
-                const uint32_t w[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
+            {
+                const uint32_t w[8] = {pf0.x, pf0.y, pf0.z, pf0.w, pf1.x, pf1.y, pf1.z, pf1.w};
 #pragma unroll
                 for (int i = 0; i < 8; ++i) {
                     v[2 * i] = __uint_as_float(w[i] << 16);
                     v[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
                 }
-            } else {
-#pragma unroll
-                for (int i = 0; i < 16; ++i) v[i] = 0.f;
             }
             float mx = 0.f;
 #pragma unroll
@@ -1013,9 +1055,11 @@ __global__ void __launch_bounds__(224, 1)
         int qload = next_nonempty(it_lo);
         uint32_t qload_idx = 0;
         for (int k = 0; k < 2 && qload < it_hi; ++k) {
-            load_q(qload, qload_idx++);
+            fetch_q(qload);
+            store_q(qload_idx++);
             qload = next_nonempty(qload + 1);
         }
+        if (qload < it_hi) fetch_q(qload);
         named_bar_sync(1, 128);  // query scales of the first items visible to all
 
         uint32_t g = 0, qi = 0, npartial = 0;
@@ -1046,8 +1090,9 @@ __global__ void __launch_bounds__(224, 1)
                 continue;
             }
             if (qi >= 1 && qload < it_hi) {
-                load_q(qload, qload_idx++);
+                store_q(qload_idx++);
                 qload = next_nonempty(qload + 1);
+                if (qload < it_hi) fetch_q(qload);
             }
             const float base_l2 = a.scale_log2 * __ldg(&a.k_scale[it.kvh]);
             float sl2[NP];
@@ -1243,8 +1288,8 @@ __global__ void wait_probe_kernel(int* status, uint64_t limit_ns) {
 }
 
 template <int D, bool FP8, int NP>
-cudaError_t launch_decode_np(const DecodeArgs& a, const CUtensorMap* mk, const CUtensorMap* mv, int grid,
-                             cudaStream_t stream) {
+cudaError_t launch_decode_np(const DecodeArgs& a, const CUtensorMap* mk, const CUtensorMap* mv, const CUtensorMap* mq,
+                             int grid, cudaStream_t stream) {
     using L = DecodeLayout<D, FP8>;
     static bool configured = false;
     if (!configured) {
@@ -1253,30 +1298,31 @@ cudaError_t launch_decode_np(const DecodeArgs& a, const CUtensorMap* mk, const C
         if (e != cudaSuccess) return e;
         configured = true;
     }
-    decode_kernel<D, FP8, NP><<<grid, L::kThreads, L::kSmem, stream>>>(a, *mk, *mv);
+    decode_kernel<D, FP8, NP><<<grid, L::kThreads, L::kSmem, stream>>>(a, *mk, *mv, *mq);
     return cudaGetLastError();
 }
 
 // The softmax works on the group's heads padded to 4, 8 or 16 (the MMA N stays 16).
 template <int D, bool FP8>
-cudaError_t launch_decode_t(const DecodeArgs& a, const CUtensorMap* mk, const CUtensorMap* mv, int grid,
-                            cudaStream_t stream) {
-    if (a.group <= 4) return launch_decode_np<D, FP8, 4>(a, mk, mv, grid, stream);
-    if (a.group <= 8) return launch_decode_np<D, FP8, 8>(a, mk, mv, grid, stream);
-    return launch_decode_np<D, FP8, 16>(a, mk, mv, grid, stream);
+cudaError_t launch_decode_t(const DecodeArgs& a, const CUtensorMap* mk, const CUtensorMap* mv, const CUtensorMap* mq,
+                            int grid, cudaStream_t stream) {
+    if (a.group <= 4) return launch_decode_np<D, FP8, 4>(a, mk, mv, mq, grid, stream);
+    if (a.group <= 8) return launch_decode_np<D, FP8, 8>(a, mk, mv, mq, grid, stream);
+    return launch_decode_np<D, FP8, 16>(a, mk, mv, mq, grid, stream);
 }
 
 }  // namespace
 
 cudaError_t launch_decode(int head_dim, bool fp8, const DecodeArgs& a, const CUtensorMap* mk, const CUtensorMap* mv,
-                          int grid, cudaStream_t stream) {
+                          const CUtensorMap* mq, int grid, cudaStream_t stream) {
     if (head_dim == 128 && fp8) {
         if (a.group <= 4) return launch_f8_np<4>(a, mk, mv, grid, stream);
         if (a.group <= 8) return launch_f8_np<8>(a, mk, mv, grid, stream);
         return launch_f8_np<16>(a, mk, mv, grid, stream);
     }
-    if (head_dim == 128) return launch_decode_t<128, false>(a, mk, mv, grid, stream);
-    return fp8 ? launch_decode_t<64, true>(a, mk, mv, grid, stream) : launch_decode_t<64, false>(a, mk, mv, grid, stream);
+    if (head_dim == 128) return launch_decode_t<128, false>(a, mk, mv, mq, grid, stream);
+    return fp8 ? launch_decode_t<64, true>(a, mk, mv, mq, grid, stream)
+               : launch_decode_t<64, false>(a, mk, mv, mq, grid, stream);
 }
 
 cudaError_t launch_combine(const CombineArgs& a, cudaStream_t stream) {

@@ -153,7 +153,7 @@ pa_status pa_get_metadata(const int32_t* seq_lens_host, const int32_t* block_tab
         }
     }
     const int64_t cap = (int64_t)sh->num_sms * cps;
-    const int64_t chunk = std::max<int64_t>(4, cdiv(units, 4 * cap));
+    const int64_t chunk = std::max<int64_t>(4, cdiv(units, 2 * cap));  // two items per CTA share
     std::vector<int32_t> nsplit(B), indptr(B + 1, 0);
     for (int b = 0; b < B; ++b) {
         int n;
@@ -334,9 +334,10 @@ pa_status decode_launch(bool fused, const pa_decode_shapes* sh, const pa_decode_
     a.scale_log2 = scale * 1.4426950408889634f;
     a.wait_ns = g_wait_limit_ns.load();
 
-    CUtensorMap mk, mv;
+    CUtensorMap mk, mv, mq;
     std::memset(&mk, 0, sizeof mk);
     std::memset(&mv, 0, sizeof mv);
+    std::memset(&mq, 0, sizeof mq);
     if (!fp8) {
         const uint64_t dims[2] = {(uint64_t)D, (uint64_t)sh->num_pool_pages * Hk * pa::kPage};
         const uint64_t strides[1] = {(uint64_t)D * 2};
@@ -344,6 +345,11 @@ pa_status decode_launch(bool fused, const pa_decode_shapes* sh, const pa_decode_
         st = make_map_16(f16, &mk, k_pool, 2, dims, strides, box);
         if (st != PA_OK) return st;
         st = make_map_16(f16, &mv, v_pool, 2, dims, strides, box);
+        if (st != PA_OK) return st;
+        // query rows [B * Hq, D]; one box = the G heads of one KV group
+        const uint64_t qdims[2] = {(uint64_t)D, (uint64_t)B * Hq};
+        const uint32_t qbox[2] = {64, (uint32_t)(Hq / Hk)};
+        st = make_map_16(f16, &mq, q, 2, qdims, strides, qbox);
         if (st != PA_OK) return st;
     } else if (D == 128) {
         // e4m3 pages: one 128-byte row per key, one box per 64-row page slab
@@ -355,7 +361,7 @@ pa_status decode_launch(bool fused, const pa_decode_shapes* sh, const pa_decode_
         st = make_map(CU_TENSOR_MAP_DATA_TYPE_UINT8, &mv, v_pool, 2, dims, strides, box);
         if (st != PA_OK) return st;
     }
-    cudaError_t e = pa::launch_decode(D, fp8, a, &mk, &mv, plan->grid, stream);
+    cudaError_t e = pa::launch_decode(D, fp8, a, &mk, &mv, &mq, plan->grid, stream);
     if (e != cudaSuccess) return cuda_fail(e, "decode launch");
     if (fused && plan->total_splits > B && !a.counters) {
         // no room for the arrival counters: merge in a second kernel
@@ -679,7 +685,7 @@ pa_status pa_get_static_plan(const pa_decode_shapes* sh, pa_decode_plan* plan) {
     const int cps = sh->ctas_per_sm == 0 ? 1 : sh->ctas_per_sm;
     const int64_t cap = (int64_t)sh->num_sms * cps;
     const int64_t splits = sh->forced_splits > 0 ? (int64_t)B * std::min(sh->forced_splits, PA_MAX_SPLITS)
-                                                 : B + cdiv(4 * cap, Hk);
+                                                 : B + cdiv(2 * cap, Hk);
     const int64_t items = splits * Hk;
     if (items > 16384) return fail(PA_ERR_UNSUPPORTED, "device scheduling handles up to 16384 work items (%lld)",
                                    (long long)items);

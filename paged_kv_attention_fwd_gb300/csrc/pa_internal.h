@@ -48,7 +48,7 @@ struct CombineArgs {
 
 // Launchers (decode.cu).  Return the CUDA error of the launch.
 cudaError_t launch_decode(int head_dim, bool fp8, const DecodeArgs& a, const CUtensorMap* map_k,
-                          const CUtensorMap* map_v, int grid, cudaStream_t stream);
+                          const CUtensorMap* map_v, const CUtensorMap* map_q, int grid, cudaStream_t stream);
 cudaError_t launch_combine(const CombineArgs& a, cudaStream_t stream);
 cudaError_t launch_wait_timeout_probe(int* status, uint64_t limit_ns, cudaStream_t stream);
 

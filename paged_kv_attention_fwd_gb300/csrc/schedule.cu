@@ -81,8 +81,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         local += p;
     }
     const long long units = block_sum(local, tmp64) * Hk;
-    const long long c4 = 4LL * cap;
-    const long long chunk = max(4LL, (units + c4 - 1) / c4);
+    const long long shares = 2LL * cap;  // two items per CTA share
+    const long long chunk = max(4LL, (units + shares - 1) / shares);
     for (int b = threadIdx.x; b < B; b += kThreads) {
         const int p = pages[b];
         int n;
