@@ -38,6 +38,39 @@ if ROOT not in sys.path:
 METRIC = "paged-attn decode KV-read GB/s (%HBM peak); prefill TFLOP/s (%TC peak)"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 L2_FLUSH_BYTES = 256 << 20
+L2_NOTE = (f"flushed between steps outside the events: {L2_FLUSH_BYTES >> 20} MiB written (twice L2), then read "
+           "back, so that no line of the previous step and no dirty line is left in L2")
+
+
+class L2Flush:
+    """Write a buffer twice the size of L2, then read it back.  The write
+    evicts the previous step's lines; the read evicts the write's own dirty
+    lines, whose write-back would otherwise compete with the next timed
+    step for HBM bandwidth."""
+
+    def __init__(self, dev):
+        import torch
+        self.buf = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+        self.out = torch.empty((), dtype=torch.float32, device=dev)
+
+    def __call__(self):
+        import torch
+        self.buf.zero_()
+        torch.sum(self.buf, dim=0, out=self.out)
+
+
+def l2_policy(dev, input_bytes: int):
+    """Inputs of at least three times L2 need no flush: a step's first reads
+    evict whatever the previous step left.  Smaller inputs are flushed.
+    Returns (callable run between steps, the config note)."""
+    import torch
+    l2 = int(getattr(torch.cuda.get_device_properties(dev), "L2_cache_size", 0) or 129_000_000)
+    if input_bytes >= 3 * l2:
+        return (lambda: None), (f"no flush between steps: inputs larger than L2 ({input_bytes / 1e6:.0f} MB read "
+                                f"per step = {input_bytes / l2:.1f} x the {l2 / 1e6:.0f} MB L2)")
+    return L2Flush(dev), L2_NOTE
+
+
 PROFILES = os.path.join(ROOT, "profiles")
 CSRC = os.path.join(ROOT, "paged_kv_attention_fwd_gb300", "csrc")
 
@@ -348,7 +381,7 @@ def run_decode(args, rank, world, local_rank, dist):
                         inp.max_pages, inp.num_pool_pages, inp.kv_dtype, device=dev)
     out = torch.empty((inp.batch, inp.num_q_heads, inp.head_dim), dtype=torch.bfloat16, device=dev)
     lse = torch.empty((inp.batch, inp.num_q_heads), dtype=torch.float32, device=dev)
-    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    flush, l2_note = l2_policy(dev, full_bytes + q.numel() * q.element_size())
     stream = torch.cuda.current_stream(dev)
     sh, plan = p.shapes, p.plan
 
@@ -357,7 +390,7 @@ def run_decode(args, rank, world, local_rank, dist):
                     stream=stream)
 
     for _ in range(args.warmup):
-        flush.zero_()
+        flush()
         step_call()
     torch.cuda.synchronize(dev)
     st = B.pa_check_status(p.workspace, stream)
@@ -371,7 +404,7 @@ def run_decode(args, rank, world, local_rank, dist):
     torch.cuda.synchronize(dev)
     with ClockSampler(gpu_index(local_rank)) as clk:
         for i in range(K):
-            flush.zero_()  # L2 flush between timed iterations (outside the events)
+            flush()  # between timed iterations (outside the events)
             ev[i][0].record(stream)
             step_call()  # one launch: decode with the split merge fused in
             ev[i][1].record(stream)
@@ -394,10 +427,11 @@ def run_decode(args, rank, world, local_rank, dist):
     value = world * full_bytes / (ms * 1e-3) / 1e9
     achieved = full_bytes / (kern_ms * 1e-3) / 1e9
     kernel_files = ["decode.cu", "pa_ptx.cuh", "pa_internal.h"]
-    prof = "decode_kernel_" + args.workload + ".md"
+    kname = "decode_f8_kernel" if fp8 and inp.head_dim == 128 else "decode_kernel"
+    prof = kname + "_" + args.workload + ".md"
     roofline = {"bound": "hbm", "achieved": round(achieved, 1), "peak": pk["hbm_gbs"], "unit": "GB/s",
                 "frac": round(achieved / pk["hbm_gbs"], 4), "traffic": profiled_traffic(prof, kernel_files),
-                "kernel": "decode_kernel", "peak_source": f"{pk_src} (copy bandwidth)",
+                "kernel": kname, "peak_source": f"{pk_src} (copy bandwidth)",
                 "algorithmic_bytes_per_launch": full_bytes, "kernel_ms": round(kern_ms, 5)}
 
     e2e = None
@@ -420,7 +454,7 @@ def run_decode(args, rank, world, local_rank, dist):
                    "kv_bytes_per_step": full_bytes, "kv_bytes_token_exact": exact_bytes,
                    "pct_hbm_peak": round(100 * value / world / pk["hbm_gbs"], 2),
                    "splits": plan.total_splits, "ctas": plan.grid,
-                   "l2": f"flushed between steps ({L2_FLUSH_BYTES >> 20} MiB write, outside the events)",
+                   "l2": l2_note,
                    "parallelism": f"replicas x{world}"},
         "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": launches, "clocks": clocks,
     }
@@ -517,7 +551,8 @@ def run_prefill(args, rank, world, local_rank, dist):
     out = torch.empty((tq, inp.num_q_heads, inp.head_dim_v), dtype=torch.bfloat16, device=dev)
     lse = torch.empty((tq, inp.num_q_heads), dtype=torch.float32, device=dev)
     ws = torch.zeros(B.pa_prefill_workspace_size(sh), dtype=torch.uint8, device=dev)
-    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    flush, l2_note = l2_policy(dev, sum(t.numel() * t.element_size() for t in (d["q"], d["k"], d["v"], d["kr"])
+                                        if t is not None))
     stream = torch.cuda.current_stream(dev)
 
     def step():
@@ -525,7 +560,7 @@ def run_prefill(args, rank, world, local_rank, dist):
                      lse, ws, stream=stream)
 
     for _ in range(args.warmup):
-        flush.zero_()
+        flush()
         step()
     torch.cuda.synchronize(dev)
     if B.pa_check_status(ws, stream) != B.PA_OK:
@@ -537,7 +572,7 @@ def run_prefill(args, rank, world, local_rank, dist):
     torch.cuda.synchronize(dev)
     with ClockSampler(gpu_index(local_rank)) as clk:
         for i in range(K):
-            flush.zero_()
+            flush()
             ev[i][0].record(stream)
             step()
             ev[i][1].record(stream)
@@ -578,7 +613,7 @@ def run_prefill(args, rank, world, local_rank, dist):
         "config": {"workload": desc, "total_q": tq, "num_q_heads": inp.num_q_heads,
                    "head_dim_qk": inp.head_dim_qk, "head_dim_v": inp.head_dim_v, "flops_per_step": flops,
                    "pct_tc_peak": round(100 * tfs / peak, 2),
-                   "l2": f"flushed between steps ({L2_FLUSH_BYTES >> 20} MiB write, outside the events)",
+                   "l2": l2_note,
                    "parallelism": f"replicas x{world}"},
         "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
         "gpu_launches": K * (2 if B.pa_prefill_workspace_size(sh) > B.PA_STATUS_BYTES else 1), "clocks": clocks,
@@ -672,14 +707,14 @@ def run_append(args, rank, world, local_rank, dist):
                             max_pages_per_seq=inp.block_table.shape[1], num_pool_pages=inp.k.shape[0], total_new=T,
                             kv_dtype=B.PA_KV_BF16)
     ws = torch.zeros(B.PA_STATUS_BYTES, dtype=torch.uint8, device=dev)
-    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    flush = L2Flush(dev)
     stream = torch.cuda.current_stream(dev)
 
     def step():
         B.pa_append_kv(sh, knd, vnd, cu, sp, bt, kp, vp, None, None, ws, stream=stream)
 
     for _ in range(args.warmup):
-        flush.zero_()
+        flush()
         step()
     K = args.steps
     ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(K)]
@@ -688,7 +723,7 @@ def run_append(args, rank, world, local_rank, dist):
     torch.cuda.synchronize(dev)
     with ClockSampler(gpu_index(local_rank)) as clk:
         for i in range(K):
-            flush.zero_()
+            flush()
             ev[i][0].record(stream)
             step()
             ev[i][1].record(stream)
@@ -740,7 +775,7 @@ def run_append(args, rank, world, local_rank, dist):
         "metric": METRIC, "value": round(world * gbs, 1), "unit": "GB/s", "n_gpus": world, "steps": K,
         "warmup": args.warmup, "ms_per_step": round(ms, 5), "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-        "config": {"workload": desc, "bytes_per_step": nbytes, "l2": "flushed between steps",
+        "config": {"workload": desc, "bytes_per_step": nbytes, "l2": L2_NOTE,
                    "parallelism": f"replicas x{world}"},
         "roofline": {"bound": "hbm", "achieved": round(gbs, 1), "peak": pk["hbm_gbs"], "unit": "GB/s",
                      "frac": round(gbs / pk["hbm_gbs"], 4), "traffic": None, "kernel": "append_kernel",
