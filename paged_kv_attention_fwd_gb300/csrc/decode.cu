@@ -202,6 +202,20 @@ __device__ __forceinline__ bool softmax_bar_or(bool pred) {
 }
 
 
+// Barrier `id` over `nthreads` threads that also ORs a flag across them.
+__device__ __forceinline__ bool named_bar_or(uint32_t id, uint32_t nthreads, bool pred) {
+    uint32_t r;
+    asm volatile(
+        "{\n\t.reg .pred p, q;\n\t"
+        "setp.ne.u32 p, %1, 0;\n\t"
+        "bar.red.or.pred q, %2, %3, p;\n\t"
+        "selp.u32 %0, 1, 0, q;\n\t}"
+        : "=r"(r)
+        : "r"((uint32_t)pred), "r"(id), "r"(nthreads)
+        : "memory");
+    return r != 0;
+}
+
 // the 16-bit output element: fp16 when the inputs are fp16, else bf16
 __device__ __forceinline__ uint16_t out16(float x, bool f16) {
     return f16 ? __half_as_ushort(__float2half_rn(x)) : __bfloat16_as_ushort(__float2bfloat16_rn(x));
@@ -576,13 +590,9 @@ __global__ void __launch_bounds__(DecodeLayout<D, FP8>::kThreads, 1)
                     if (partial) a.lse_part[orow + row] = -INFINITY;
                     else if (a.lse) a.lse[orow + row] = -INFINITY;
                 }
-                if (partial && a.counters) {
-                    if (!partials_written(&bars[B_PW], &bars[B_HD], npartial++, abort_sh, a.wait_ns)) {
-                        fail(a, abort_sh, PA_ERR_TIMEOUT);
-                        aborted = true;
-                        break;
-                    }
-                }
+                if (partial && a.counters &&
+                    !partials_written(&bars[B_PW], &bars[B_HD], npartial++, abort_sh, a.wait_ns))
+                    fail(a, abort_sh, PA_ERR_TIMEOUT);  // the next barrier takes every thread out
                 continue;
             }
             if (FP8 && qi >= 1 && qload < it_hi) {
@@ -689,13 +699,9 @@ __global__ void __launch_bounds__(DecodeLayout<D, FP8>::kThreads, 1)
                 if (partial) a.lse_part[orow + row] = lse;
                 else if (a.lse) a.lse[orow + row] = lse;
             }
-            if (partial && a.counters) {
-                if (!partials_written(&bars[B_PW], &bars[B_HD], npartial++, abort_sh, a.wait_ns)) {
-                    fail(a, abort_sh, PA_ERR_TIMEOUT);
-                    aborted = true;
-                    break;
-                }
-            }
+            if (partial && a.counters &&
+                !partials_written(&bars[B_PW], &bars[B_HD], npartial++, abort_sh, a.wait_ns))
+                fail(a, abort_sh, PA_ERR_TIMEOUT);  // the next barrier takes every thread out
         }
         tc_fence_before();
     } else if (warp == L::kMergeWarp) {
@@ -780,33 +786,69 @@ __global__ void __launch_bounds__(DecodeLayout<D, FP8>::kThreads, 1)
 // e4m3 pages, D = 128: both products on the e4m3 tensor path (kind::f8f6f4),
 // straight from the TMA-loaded pages -- no conversion pass, so shared memory
 // holds only the page ring (5 stages of 2 pages of K and V).
-//   S^T[128 keys, 16] = K_tile . Q3^T: the bf16 query of each head is scaled
+//   S^T[128 keys, 48] = K_tile . Q3^T: the bf16 query of each head is scaled
 //     by a power of two (max |q| -> [128, 256)) and split into three e4m3
-//     levels hi + mid + lo, accumulated into the same TMEM columns (the split
-//     keeps 12 significant bits; bf16 has 8);
+//     levels hi + mid + lo (the split keeps 12 significant bits; bf16 has 8),
+//     stacked as 48 rows of one MMA operand, so that one N = 48 product per
+//     32 bytes of d gives the three level products side by side; the softmax
+//     adds them.  Every tcgen05.mma costs the issuing thread about as much as
+//     a whole tile's worth of the tensor pipe here, so the issue count, not
+//     the math, is what this saves;
 //   O^T[128 d, 32]    = V_tile^T . P2: P * 256 split into two e4m3 levels
 //     (hi + lo, about bf16 precision) in columns 0-15 and 16-31, summed when
 //     the output is folded.
-constexpr int kF8Stages = 5;
+// The per-tile softmax is one long dependent chain (max, exp2, the P split,
+// the fold).  With groups of up to 8 heads two softmax warpgroups (WG = 2)
+// take alternate tiles of an item, each with its own running max, sum and
+// output, so that two chains share every SM sub-partition; at the end of the
+// item the second warpgroup hands (m, l, o) to the first through shared
+// memory, which merges the two and writes.  Larger groups keep one warpgroup
+// (register budget).
+template <int WG>
 struct F8Layout {
-    static constexpr int kStageBytes = 32768;  // K: 2 pages x 64 rows x 128 B, then V the same
-    static constexpr int kQ3Off = kF8Stages * kStageBytes;
-    static constexpr int kQ3Bytes = 48 * 128;  // rows = level * 16 + head
+    static constexpr int kStages = 5;
+    static constexpr int kNB = 2 * WG;          // S, O and P buffers
+    static constexpr int kStageBytes = 32768;   // K: 2 pages x 64 rows x 128 B, then V the same
+    static constexpr int kQ3Off = kStages * kStageBytes;
+    static constexpr int kQ3Bytes = 48 * 128;   // rows = level * 16 + head
     static constexpr int kPOff = kQ3Off + 2 * kQ3Bytes;
-    static constexpr int kPBytes = 128 * 128;  // row = key; bytes 0-15 hi, 16-31 lo (MN-major)
-    static constexpr int kRedOff = kPOff + 2 * kPBytes;
-    static constexpr int kQscOff = kRedOff + 1024;  // [2][16] floats
-    static constexpr int kBytes = kQscOff + 128;
+    // P, MN-major with 128-byte swizzle: row = key; buffer b takes bytes
+    // 32b .. 32b+31 of every row (hi heads, then lo heads), so that all
+    // kNB <= 4 buffers share one region and the MMA descriptor of buffer b
+    // starts 32b bytes in
+    static constexpr int kPBytes = 128 * 128;
+    static constexpr int kRedOff = kPOff + kPBytes;
+    static constexpr int kRedBytes = 1024;      // per warpgroup: [2][64] maxima, [2][64] sums
+    static constexpr int kQscOff = kRedOff + WG * kRedBytes;  // [2][16] floats
+    static constexpr int kXOff = kQscOff + 128;  // hand-over, per item parity: o [8][128], m [8], l [8]
+    static constexpr int kXFloats = 8 * 128 + 16;
+    static constexpr int kXBytes = WG == 2 ? 2 * kXFloats * 4 : 0;
+    static constexpr int kBytes = kXOff + kXBytes;
     static constexpr int kSmem = kBytes + 1024;
+    static constexpr int kMergeWarp = 2 + 4 * WG;
+    static constexpr int kThreads = (kMergeWarp + 1) * 32;
+    // TMEM: S buffers of 48 columns (three query levels x 16) in 64-column
+    // slots, then O buffers of 32 columns (hi and lo P levels x 16)
+    static constexpr uint32_t kTmemCols = WG == 2 ? 512 : 256;
+    __host__ __device__ static constexpr uint32_t s_col(uint32_t b) { return b * 64u; }
+    __host__ __device__ static constexpr uint32_t o_col(uint32_t b) { return kNB * 64u + b * 32u; }
+    static_assert(kQ3Off % 1024 == 0 && kPOff % 1024 == 0, "swizzle atoms need 1024-byte alignment");
+    static_assert(kSmem <= 232448, "shared memory per CTA");
+    static_assert(o_col(kNB - 1) + 32 <= kTmemCols, "TMEM columns");
 };
-static_assert(F8Layout::kQ3Off % 1024 == 0 && F8Layout::kPOff % 1024 == 0, "swizzle atoms need 1024-byte alignment");
-static_assert(F8Layout::kSmem <= 232448, "shared memory per CTA");
 
 enum : int {
-    F_FULL = 0, F_EMPTY = 5, F_QF = 10, F_SF = 12, F_PF = 14, F_OF = 16, F_DONE = 18, F_PW = 19, F_HD = 21, F_COUNT = 23
+    F_FULL = 0,    // [5] stage filled
+    F_EMPTY = 5,   // [5] stage free again
+    F_QF = 10,     // [2] query levels written
+    F_SF = 12,     // [4] S tile in TMEM
+    F_PF = 16,     // [4] P written
+    F_OF = 20,     // [4] O tile in TMEM
+    F_DONE = 24,   // all MMAs retired (teardown)
+    F_PW = 25,     // [2] an item's partials written (merge warp)
+    F_HD = 27,     // [2] merge warp done with an item
+    F_COUNT = 29
 };
-__host__ __device__ constexpr uint32_t f8_s_col(uint32_t b) { return b * 16u; }
-__host__ __device__ constexpr uint32_t f8_o_col(uint32_t b) { return 32u + b * 32u; }
 
 __device__ __forceinline__ uint32_t e4m3x2(float lo, float hi) {
     return (uint32_t)__nv_cvt_float2_to_fp8x2(make_float2(lo, hi), __NV_SATFINITE, __NV_E4M3);
@@ -819,12 +861,14 @@ __device__ __forceinline__ float2 e4m3x2_to_f2(uint32_t v) {
     return __half22float2(hh);
 }
 
-template <int NP>
-__global__ void __launch_bounds__(224, 1)
+template <int NP, int WG>
+__global__ void __launch_bounds__(F8Layout<WG>::kThreads, 1)
     decode_f8_kernel(const __grid_constant__ DecodeArgs a, const __grid_constant__ CUtensorMap map_k,
                      const __grid_constant__ CUtensorMap map_v) {
-    using L = F8Layout;
+    using L = F8Layout<WG>;
+    static_assert(WG == 1 || NP <= 8, "the hand-over buffer holds 8 heads");
     constexpr int D = 128;
+    constexpr int NB = L::kNB, NS = L::kStages;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     __shared__ __align__(8) uint64_t bars[F_COUNT];
@@ -842,15 +886,17 @@ __global__ void __launch_bounds__(224, 1)
         it_hi = __ldg(&meta[kMetaHeader + 2 * B + 1 + blockIdx.x + 1]);
     }
     if (threadIdx.x == 0) {
-        for (int s = 0; s < kF8Stages; ++s) {
+        for (int s = 0; s < NS; ++s) {
             mbar_init(&bars[F_FULL + s], 1);
             mbar_init(&bars[F_EMPTY + s], 1);
         }
-        for (int i = 0; i < 2; ++i) {
-            mbar_init(&bars[F_QF + i], 128);
+        for (int i = 0; i < NB; ++i) {
             mbar_init(&bars[F_SF + i], 1);
             mbar_init(&bars[F_PF + i], 128);
             mbar_init(&bars[F_OF + i], 1);
+        }
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(&bars[F_QF + i], 128);
             mbar_init(&bars[F_PW + i], 128);
             mbar_init(&bars[F_HD + i], 1);
         }
@@ -859,7 +905,7 @@ __global__ void __launch_bounds__(224, 1)
         fence_barrier_init();
     }
     if (warp == 1) {
-        tmem_alloc(&tmem_base_sh, 128);
+        tmem_alloc(&tmem_base_sh, L::kTmemCols);
         tmem_relinquish();
     }
     tc_fence_before();
@@ -871,21 +917,21 @@ __global__ void __launch_bounds__(224, 1)
         // ------------------------------------------------------------ producer
         if (lane == 0) {
             uint32_t g = 0;
-            uint32_t last_par[kF8Stages] = {};
-            bool issued[kF8Stages] = {};
+            uint32_t last_par[NS] = {};
+            bool issued[NS] = {};
             bool ok = true;
             for (int j = it_lo; j < it_hi && ok; ++j) {
                 const Item it = load_item(a, j, items_off);
                 const int ntiles = item_tiles(it);
                 const long long bt_row = (long long)it.b * a.max_pages;
                 for (int t = 0; t < ntiles; ++t, ++g) {
-                    const int stage = g % kF8Stages;
+                    const int stage = g % NS;
                     const int pa0 = it.p0 + 2 * t;
                     const int npg = min(2, it.p1 - pa0);
                     int pid[2];
                     pid[0] = __ldg(&a.block_table[bt_row + pa0]);
                     pid[1] = npg > 1 ? __ldg(&a.block_table[bt_row + pa0 + 1]) : 0;
-                    if (!mbar_wait(&bars[F_EMPTY + stage], ((g / kF8Stages) & 1) ^ 1, abort_sh, a.wait_ns)) {
+                    if (!mbar_wait(&bars[F_EMPTY + stage], ((g / NS) & 1) ^ 1, abort_sh, a.wait_ns)) {
                         fail(a, abort_sh, PA_ERR_TIMEOUT);
                         ok = false;
                         break;
@@ -906,94 +952,108 @@ __global__ void __launch_bounds__(224, 1)
                         tma_load_2d(st + i * 8192, &map_k, full, 0, row);
                         tma_load_2d(st + 16384 + i * 8192, &map_v, full, 0, row);
                     }
-                    last_par[stage] = (g / kF8Stages) & 1;
+                    last_par[stage] = (g / NS) & 1;
                     issued[stage] = true;
                 }
             }
-            for (int s = 0; s < kF8Stages; ++s)
+            for (int s = 0; s < NS; ++s)
                 if (issued[s]) mbar_wait(&bars[F_FULL + s], last_par[s], nullptr, a.wait_ns);
         }
     } else if (warp == 1) {
         // ------------------------------------------------------------ MMA issuer
+        // Tile g uses S/O/P buffer g % NB; its softmax is done by warpgroup g % WG.
+        // Event-driven: every pass issues the next QK if its pages, its query
+        // and its S buffer are ready, and the next PV if its P is written, so
+        // that neither product waits behind the other (two warpgroups consume
+        // S in turn).  QK runs at most NB tiles ahead of PV: S buffer g % NB
+        // is free once PV(g - NB) was issued, since that PV needed P(g - NB).
         if (lane == 0) {
-            constexpr uint32_t idesc_qk = idesc_e4m3(128, 16, false, false);
+            constexpr uint32_t idesc_qk = idesc_e4m3(128, 48, false, false);
             constexpr uint32_t idesc_pv = idesc_e4m3(128, 32, true, true);
-            uint32_t g = 0, qi = 0;
-            bool pending = false, ok = true;
-            auto issue_pv = [&](uint32_t k) -> bool {
-                if (!mbar_wait(&bars[F_PF + (k & 1)], (k >> 1) & 1, abort_sh, a.wait_ns)) return false;
-                tc_fence_after();
-                const uint32_t vbase = smem_u32(sm + (k % kF8Stages) * L::kStageBytes + 16384);
-                const uint32_t pbase = smem_u32(sm + L::kPOff + (k & 1) * L::kPBytes);
-#pragma unroll
-                for (int kk = 0; kk < 4; ++kk)  // 32 keys per step
-                    mma_f8_ss(tbase + f8_o_col(k & 1), sdesc_sw128(vbase + kk * 4096, 1024, 1024),
-                              sdesc_sw128(pbase + kk * 4096, 1024, 1024), idesc_pv, kk > 0);
-                mma_commit(&bars[F_OF + (k & 1)]);
-                mma_commit(&bars[F_EMPTY + (k % kF8Stages)]);
-                return true;
+            uint32_t total = 0;
+            for (int j = it_lo; j < it_hi; ++j) total += (uint32_t)item_tiles(load_item(a, j, items_off));
+            int jq = it_lo;  // item of the next QK, and its tile count
+            uint32_t jq_tiles = 0;
+            auto skip_empty = [&]() {
+                while (jq < it_hi && (jq_tiles = (uint32_t)item_tiles(load_item(a, jq, items_off))) == 0) ++jq;
             };
-            for (int j = it_lo; j < it_hi && ok; ++j) {
-                const Item it = load_item(a, j, items_off);
-                const int ntiles = item_tiles(it);
-                if (ntiles == 0) continue;
-                if (!mbar_wait(&bars[F_QF + (qi & 1)], (qi >> 1) & 1, abort_sh, a.wait_ns)) {
+            skip_empty();
+            uint32_t qk = 0, pv = 0, tq = 0, qi = 0, qbase = 0;
+            bool have_q = false, ok = true;
+            uint64_t t_last = globaltimer_ns();
+            for (uint32_t it = 1; pv < total && ok; ++it) {
+                bool progress = false;
+                if (qk < total && qk < pv + NB) {
+                    if (!have_q && mbar_test(&bars[F_QF + (qi & 1)], (qi >> 1) & 1)) {
+                        qbase = smem_u32(sm + L::kQ3Off + (qi & 1) * L::kQ3Bytes);
+                        ++qi;
+                        have_q = true;
+                    }
+                    if (have_q && mbar_test(&bars[F_FULL + qk % NS], (qk / NS) & 1)) {
+                        tc_fence_after();
+                        const uint32_t kbase = smem_u32(sm + (qk % NS) * L::kStageBytes);
+#pragma unroll
+                        for (int kk = 0; kk < 4; ++kk)  // 32 bytes of d per step; N = 48 = hi, mid, lo levels
+                            mma_f8_ss(tbase + L::s_col(qk % NB), sdesc_sw128(kbase + kk * 32, 16, 1024),
+                                      sdesc_sw128(qbase + kk * 32, 16, 1024), idesc_qk, kk > 0 ? 1u : 0u);
+                        mma_commit(&bars[F_SF + qk % NB]);
+                        ++qk;
+                        if (++tq == jq_tiles) {
+                            ++jq;
+                            tq = 0;
+                            have_q = false;
+                            skip_empty();
+                        }
+                        progress = true;
+                    }
+                }
+                if (pv < qk && mbar_test(&bars[F_PF + pv % NB], (pv / NB) & 1)) {
+                    tc_fence_after();
+                    const uint32_t vbase = smem_u32(sm + (pv % NS) * L::kStageBytes + 16384);
+                    const uint32_t pbase = smem_u32(sm + L::kPOff) + (pv % NB) * 32u;
+#pragma unroll
+                    for (int kk = 0; kk < 4; ++kk)  // 32 keys per step
+                        mma_f8_ss(tbase + L::o_col(pv % NB), sdesc_sw128(vbase + kk * 4096, 1024, 1024),
+                                  sdesc_sw128(pbase + kk * 4096, 1024, 1024), idesc_pv, kk > 0);
+                    mma_commit(&bars[F_OF + pv % NB]);
+                    mma_commit(&bars[F_EMPTY + pv % NS]);
+                    ++pv;
+                    progress = true;
+                }
+                if (progress) {
+                    t_last = globaltimer_ns();
+                } else if ((it & 31u) == 0 &&
+                           (*abort_sh != 0 || globaltimer_ns() - t_last > a.wait_ns || it >= (1u << 30))) {
                     fail(a, abort_sh, PA_ERR_TIMEOUT);
                     ok = false;
-                    break;
-                }
-                const uint32_t qbase = smem_u32(sm + L::kQ3Off + (qi & 1) * L::kQ3Bytes);
-                ++qi;
-                for (int t = 0; t < ntiles; ++t, ++g) {
-                    const int stage = g % kF8Stages;
-                    if (!mbar_wait(&bars[F_FULL + stage], (g / kF8Stages) & 1, abort_sh, a.wait_ns)) {
-                        fail(a, abort_sh, PA_ERR_TIMEOUT);
-                        ok = false;
-                        break;
-                    }
-                    tc_fence_after();
-                    const uint32_t kbase = smem_u32(sm + stage * L::kStageBytes);
-#pragma unroll
-                    for (int kk = 0; kk < 4; ++kk)      // 32 bytes of d per step
-#pragma unroll
-                        for (int lvl = 0; lvl < 3; ++lvl)  // hi, mid, lo query levels
-                            mma_f8_ss(tbase + f8_s_col(g & 1), sdesc_sw128(kbase + kk * 32, 16, 1024),
-                                      sdesc_sw128(qbase + lvl * 2048 + kk * 32, 16, 1024), idesc_qk,
-                                      (kk | lvl) ? 1u : 0u);
-                    mma_commit(&bars[F_SF + (g & 1)]);
-                    if (pending && !issue_pv(g - 1)) {
-                        fail(a, abort_sh, PA_ERR_TIMEOUT);
-                        ok = false;
-                        break;
-                    }
-                    pending = true;
                 }
             }
-            if (ok && pending && !issue_pv(g - 1)) fail(a, abort_sh, PA_ERR_TIMEOUT);
             mma_commit(&bars[F_DONE]);
             mbar_wait(&bars[F_DONE], 0, nullptr, a.wait_ns);
         }
-    } else if (warp == 6) {
+    } else if (warp == L::kMergeWarp) {
         // ------------------------------------------------------------ split merge
         if (a.counters) merge_warp<D>(a, it_lo, it_hi, items_off, &bars[F_PW], &bars[F_HD], abort_sh, lane);
     } else {
         // ------------------------------------------------------------ softmax
+        const int wg = (warp - 2) >> 2;   // warpgroup: takes the tiles g with g % WG == wg
+        const uint32_t wbar = 1 + wg;     // its named barrier (128 threads)
         const int q4 = warp & 3;
         const int row = q4 * 32 + lane;
         const int hl = head_of_lane<NP>(lane);
         const bool writer = lane_writes<NP>(lane);
         const int G = a.group;
         const uint32_t lane_addr = (uint32_t)(q4 * 32) << 16;
-        float* red = reinterpret_cast<float*>(sm + L::kRedOff);
+        float* red = reinterpret_cast<float*>(sm + L::kRedOff + wg * L::kRedBytes);
         float* qsc = reinterpret_cast<float*>(sm + L::kQscOff);
 
         auto next_nonempty = [&](int j) {
             while (j < it_hi && item_tiles(load_item(a, j, items_off)) == 0) ++j;
             return j;
         };
-        // query of the item's KV group -> three e4m3 levels (rows level*16 + head).
-        // fetch_q only issues the global loads (into pf0/pf1); store_q, one
-        // item later, converts and writes, so the load latency is hidden.
+        // query of the item's KV group -> three e4m3 levels (rows level*16 + head),
+        // by warpgroup 0.  fetch_q only issues the global loads (into pf0/pf1);
+        // store_q, one item later, converts and writes, so the load latency is hidden.
         const int qh = row >> 3, qc = row & 7;  // head, 16-element chunk of d
         uint4 pf0 = make_uint4(0, 0, 0, 0), pf1 = make_uint4(0, 0, 0, 0);
         auto fetch_q = [&](int j) {
@@ -1054,15 +1114,20 @@ __global__ void __launch_bounds__(224, 1)
 
         int qload = next_nonempty(it_lo);
         uint32_t qload_idx = 0;
-        for (int k = 0; k < 2 && qload < it_hi; ++k) {
-            fetch_q(qload);
-            store_q(qload_idx++);
-            qload = next_nonempty(qload + 1);
+        if (wg == 0) {
+            for (int k = 0; k < 2 && qload < it_hi; ++k) {
+                fetch_q(qload);
+                store_q(qload_idx++);
+                qload = next_nonempty(qload + 1);
+            }
+            if (qload < it_hi) fetch_q(qload);
         }
-        if (qload < it_hi) fetch_q(qload);
-        named_bar_sync(1, 128);  // query scales of the first items visible to all
+        named_bar_sync(3, 128 * WG);  // query scales of the first items visible to every softmax thread
 
-        uint32_t g = 0, qi = 0, npartial = 0;
+        // Only barrier results (uniform over the threads that take part) end
+        // a loop: a failed wait records the error and raises the abort flag,
+        // and the next barrier takes everyone out together.
+        uint32_t g0 = 0, qi = 0, npartial = 0, lt = 0;
         bool aborted = false;
         for (int j = it_lo; j < it_hi && !aborted; ++j) {
             const Item it = load_item(a, j, items_off);
@@ -1072,24 +1137,22 @@ __global__ void __launch_bounds__(224, 1)
             const long long orow = partial ? (long long)(it.split_base + it.s) * a.num_q_heads + head0
                                            : (long long)it.b * a.num_q_heads + head0;
             if (ntiles == 0) {
-                for (int h = 0; h < G; ++h) {
-                    if (partial) a.o_part[(orow + h) * D + row] = 0.f;
-                    else a.out[(orow + h) * D + row] = 0;
-                }
-                if (row < G) {
-                    if (partial) a.lse_part[orow + row] = -INFINITY;
-                    else if (a.lse) a.lse[orow + row] = -INFINITY;
-                }
-                if (partial && a.counters) {
-                    if (!partials_written(&bars[F_PW], &bars[F_HD], npartial++, abort_sh, a.wait_ns)) {
-                        fail(a, abort_sh, PA_ERR_TIMEOUT);
-                        aborted = true;
-                        break;
+                if (wg == 0) {
+                    for (int h = 0; h < G; ++h) {
+                        if (partial) a.o_part[(orow + h) * D + row] = 0.f;
+                        else a.out[(orow + h) * D + row] = 0;
                     }
+                    if (row < G) {
+                        if (partial) a.lse_part[orow + row] = -INFINITY;
+                        else if (a.lse) a.lse[orow + row] = -INFINITY;
+                    }
+                    if (partial && a.counters &&
+                        !partials_written(&bars[F_PW], &bars[F_HD], npartial++, abort_sh, a.wait_ns))
+                        fail(a, abort_sh, PA_ERR_TIMEOUT);
                 }
                 continue;
             }
-            if (qi >= 1 && qload < it_hi) {
+            if (wg == 0 && qi >= 1 && qload < it_hi) {
                 store_q(qload_idx++);
                 qload = next_nonempty(qload + 1);
                 if (qload < it_hi) fetch_q(qload);
@@ -1105,11 +1168,11 @@ __global__ void __launch_bounds__(224, 1)
             for (int h = 0; h < NP; ++h) { m[h] = -INFINITY; lp[h] = 0.f; o[h] = 0.f; alpha_prev[h] = 1.f; }
 
             auto fold = [&](uint32_t k) {
-                if (!mbar_wait(&bars[F_OF + (k & 1)], (k >> 1) & 1, abort_sh, a.wait_ns)) fail(a, abort_sh, PA_ERR_TIMEOUT);
+                if (!mbar_wait(&bars[F_OF + k % NB], (k / NB) & 1, abort_sh, a.wait_ns)) fail(a, abort_sh, PA_ERR_TIMEOUT);
                 tc_fence_after();
                 uint32_t rh[NP], rl[NP];
-                tmem_ld_cols<NP>(tbase + lane_addr + f8_o_col(k & 1), rh);
-                tmem_ld_cols<NP>(tbase + lane_addr + f8_o_col(k & 1) + 16, rl);
+                tmem_ld_cols<NP>(tbase + lane_addr + L::o_col(k % NB), rh);
+                tmem_ld_cols<NP>(tbase + lane_addr + L::o_col(k % NB) + 16, rl);
                 tmem_ld_wait();
                 reg_fence(rh);
                 reg_fence(rl);
@@ -1118,25 +1181,35 @@ __global__ void __launch_bounds__(224, 1)
                     o[h] = fmaf(o[h], alpha_prev[h], (__uint_as_float(rh[h]) + __uint_as_float(rl[h])) * (1.f / 256.f));
             };
 
-            for (int t = 0; t < ntiles; ++t, ++g) {
+            bool have_prev = false;
+            uint32_t gprev = 0;
+            const int t0 = (int)((uint32_t)(wg - (int)g0) & (uint32_t)(WG - 1));
+            for (int t = t0; t < ntiles; t += WG, ++lt) {
+                const uint32_t g = g0 + t;
                 const int pa0 = it.p0 + 2 * t;
                 const int npg = min(2, it.p1 - pa0);
                 const int key = pa0 * kPage + row;
                 const bool valid = row < npg * kPage && key < key_end;
-                if (!mbar_wait(&bars[F_SF + (g & 1)], (g >> 1) & 1, abort_sh, a.wait_ns))
+                if (!mbar_wait(&bars[F_SF + g % NB], (g / NB) & 1, abort_sh, a.wait_ns))
                     fail(a, abort_sh, PA_ERR_TIMEOUT);
                 tc_fence_after();
-                uint32_t sr[NP];
-                tmem_ld_cols<NP>(tbase + lane_addr + f8_s_col(g & 1), sr);
+                uint32_t sh[NP], sm_[NP], slo[NP];  // the three query-level products
+                tmem_ld_cols<NP>(tbase + lane_addr + L::s_col(g % NB), sh);
+                tmem_ld_cols<NP>(tbase + lane_addr + L::s_col(g % NB) + 16, sm_);
+                tmem_ld_cols<NP>(tbase + lane_addr + L::s_col(g % NB) + 32, slo);
                 tmem_ld_wait();
-                reg_fence(sr);
+                reg_fence(sh);
+                reg_fence(sm_);
+                reg_fence(slo);
                 float x[NP];
 #pragma unroll
-                for (int h = 0; h < NP; ++h) x[h] = valid ? __uint_as_float(sr[h]) * sl2[h] : -INFINITY;
+                for (int h = 0; h < NP; ++h)
+                    x[h] = valid ? ((__uint_as_float(sh[h]) + __uint_as_float(sm_[h])) + __uint_as_float(slo[h])) * sl2[h]
+                                 : -INFINITY;
                 const float wmax = warp_xreduce<NP, true>(x, lane);
-                float* rb = red + (g & 1) * 64;
+                float* rb = red + (lt & 1) * 64;
                 if (writer) rb[hl * 4 + q4] = wmax;
-                if (softmax_bar_or(*abort_sh != 0)) { aborted = true; break; }
+                if (named_bar_or(wbar, 128, *abort_sh != 0)) { aborted = true; break; }
                 float alpha[NP];
 #pragma unroll
                 for (int h = 0; h < NP; ++h) {
@@ -1160,56 +1233,88 @@ __global__ void __launch_bounds__(224, 1)
                     hw[h >> 2] |= hb << ((h & 2) * 8);
                     lw[h >> 2] |= lb << ((h & 2) * 8);
                 }
-                uint8_t* pb = sm + L::kPOff + (g & 1) * L::kPBytes + row * 128;
-                *reinterpret_cast<uint4*>(pb + ((0 ^ (row & 7)) << 4)) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
-                *reinterpret_cast<uint4*>(pb + ((1 ^ (row & 7)) << 4)) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
+                uint8_t* pb = sm + L::kPOff + row * 128;
+                const int c0 = 2 * (int)(g % NB);  // this buffer's first 16-byte chunk of the row
+                *reinterpret_cast<uint4*>(pb + ((c0 ^ (row & 7)) << 4)) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
+                *reinterpret_cast<uint4*>(pb + (((c0 + 1) ^ (row & 7)) << 4)) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
                 if (!valid) {
                     // a dead key's V row may hold anything (NaN included): zero it
-                    const int stage = g % kF8Stages;
-                    mbar_wait(&bars[F_FULL + stage], (g / kF8Stages) & 1, abort_sh, a.wait_ns);
+                    const int stage = g % NS;
+                    mbar_wait(&bars[F_FULL + stage], (g / NS) & 1, abort_sh, a.wait_ns);
                     uint8_t* vr = sm + stage * L::kStageBytes + 16384 + (row >> 6) * 8192 + (row & 63) * 128;
 #pragma unroll
                     for (int i = 0; i < 8; ++i) *reinterpret_cast<uint4*>(vr + i * 16) = make_uint4(0, 0, 0, 0);
                 }
                 fence_proxy_async_smem();
                 tc_fence_before();
-                mbar_arrive(&bars[F_PF + (g & 1)]);
-                if (t > 0) fold(g - 1);
+                mbar_arrive(&bars[F_PF + g % NB]);
+                if (have_prev) fold(gprev);
 #pragma unroll
                 for (int h = 0; h < NP; ++h) alpha_prev[h] = alpha[h];
+                have_prev = true;
+                gprev = g;
             }
-            if (aborted) break;
-            fold(g - 1);
+            g0 += ntiles;
+            if (have_prev && !aborted) fold(gprev);
             tc_fence_before();
 
+            // ---- end of item: this warpgroup's sums; with two warpgroups the
+            // second hands (m, l, o) to the first, which merges and writes
             const float wsum = warp_xreduce<NP, false>(lp, lane);
             float* rl = red + 128 + (qi & 1) * 64;
             if (writer) rl[hl * 4 + q4] = wsum;
-            if (softmax_bar_or(*abort_sh != 0)) { aborted = true; break; }
-            const float vs = __ldg(&a.v_scale[it.kvh]);
-            float mine_m = 0.f, mine_l = 0.f;
+            bool ab = named_bar_or(wbar, 128, *abort_sh != 0);
+            float* xo = reinterpret_cast<float*>(sm + L::kXOff) + (qi & 1) * L::kXFloats;
+            float l_own[NP];
 #pragma unroll
             for (int h = 0; h < NP; ++h) {
                 const float4 r4 = reinterpret_cast<const float4*>(rl)[h];
-                const float l = (r4.x + r4.y) + (r4.z + r4.w);
-                if (h == row) { mine_m = m[h]; mine_l = l; }
-                if (h < G) {
-                    const float val = l > 0.f ? o[h] * (vs / l) : 0.f;
-                    if (partial) a.o_part[(orow + h) * D + row] = val;
-                    else a.out[(orow + h) * D + row] = __bfloat16_as_ushort(__float2bfloat16_rn(val));
+                l_own[h] = (r4.x + r4.y) + (r4.z + r4.w);
+            }
+            if constexpr (WG == 2) {
+                if (wg == 1 && !ab) {
+#pragma unroll
+                    for (int h = 0; h < NP; ++h) {
+                        xo[h * 128 + row] = o[h];
+                        if (row == h) {
+                            xo[1024 + h] = m[h];
+                            xo[1032 + h] = l_own[h];
+                        }
+                    }
                 }
+                ab = named_bar_or(3, 256, ab || *abort_sh != 0);
             }
-            if (row < G) {
-                const float lse = mine_l > 0.f ? (mine_m + log2f(mine_l)) * kLn2 : -INFINITY;
-                if (partial) a.lse_part[orow + row] = lse;
-                else if (a.lse) a.lse[orow + row] = lse;
-            }
-            if (partial && a.counters) {
-                if (!partials_written(&bars[F_PW], &bars[F_HD], npartial++, abort_sh, a.wait_ns)) {
+            if (ab) { aborted = true; break; }
+            if (wg == 0) {
+                const float vs = __ldg(&a.v_scale[it.kvh]);
+                float mine_m = -INFINITY, mine_l = 0.f;
+#pragma unroll
+                for (int h = 0; h < NP; ++h) {
+                    float mm = m[h], ll = l_own[h], oo = o[h];
+                    if constexpr (WG == 2) {
+                        const float m1 = xo[1024 + h], l1 = xo[1032 + h], o1 = xo[h * 128 + row];
+                        const float mx = fmaxf(mm, m1);
+                        const float a0 = mm == -INFINITY ? 0.f : exp2f(mm - mx);
+                        const float a1 = m1 == -INFINITY ? 0.f : exp2f(m1 - mx);
+                        mm = mx;
+                        ll = ll * a0 + l1 * a1;
+                        oo = oo * a0 + o1 * a1;
+                    }
+                    if (h == row) { mine_m = mm; mine_l = ll; }
+                    if (h < G) {
+                        const float val = ll > 0.f ? oo * (vs / ll) : 0.f;
+                        if (partial) a.o_part[(orow + h) * D + row] = val;
+                        else a.out[(orow + h) * D + row] = __bfloat16_as_ushort(__float2bfloat16_rn(val));
+                    }
+                }
+                if (row < G) {
+                    const float lse = mine_l > 0.f ? (mine_m + log2f(mine_l)) * kLn2 : -INFINITY;
+                    if (partial) a.lse_part[orow + row] = lse;
+                    else if (a.lse) a.lse[orow + row] = lse;
+                }
+                if (partial && a.counters &&
+                    !partials_written(&bars[F_PW], &bars[F_HD], npartial++, abort_sh, a.wait_ns))
                     fail(a, abort_sh, PA_ERR_TIMEOUT);
-                    aborted = true;
-                    break;
-                }
             }
         }
         tc_fence_before();
@@ -1218,21 +1323,22 @@ __global__ void __launch_bounds__(224, 1)
     __syncthreads();
     if (warp == 1) {
         tc_fence_after();
-        tmem_dealloc(tbase, 128);
+        tmem_dealloc(tbase, L::kTmemCols);
     }
 }
 
-template <int NP>
+template <int NP, int WG>
 cudaError_t launch_f8_np(const DecodeArgs& a, const CUtensorMap* mk, const CUtensorMap* mv, int grid,
                          cudaStream_t stream) {
+    using L = F8Layout<WG>;
     static bool configured = false;
     if (!configured) {
         cudaError_t e =
-            cudaFuncSetAttribute(decode_f8_kernel<NP>, cudaFuncAttributeMaxDynamicSharedMemorySize, F8Layout::kSmem);
+            cudaFuncSetAttribute(decode_f8_kernel<NP, WG>, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kSmem);
         if (e != cudaSuccess) return e;
         configured = true;
     }
-    decode_f8_kernel<NP><<<grid, 224, F8Layout::kSmem, stream>>>(a, *mk, *mv);
+    decode_f8_kernel<NP, WG><<<grid, L::kThreads, L::kSmem, stream>>>(a, *mk, *mv);
     return cudaGetLastError();
 }
 
@@ -1316,9 +1422,9 @@ cudaError_t launch_decode_t(const DecodeArgs& a, const CUtensorMap* mk, const CU
 cudaError_t launch_decode(int head_dim, bool fp8, const DecodeArgs& a, const CUtensorMap* mk, const CUtensorMap* mv,
                           const CUtensorMap* mq, int grid, cudaStream_t stream) {
     if (head_dim == 128 && fp8) {
-        if (a.group <= 4) return launch_f8_np<4>(a, mk, mv, grid, stream);
-        if (a.group <= 8) return launch_f8_np<8>(a, mk, mv, grid, stream);
-        return launch_f8_np<16>(a, mk, mv, grid, stream);
+        if (a.group <= 4) return launch_f8_np<4, 2>(a, mk, mv, grid, stream);
+        if (a.group <= 8) return launch_f8_np<8, 2>(a, mk, mv, grid, stream);
+        return launch_f8_np<16, 1>(a, mk, mv, grid, stream);
     }
     if (head_dim == 128) return launch_decode_t<128, false>(a, mk, mv, mq, grid, stream);
     return fp8 ? launch_decode_t<64, true>(a, mk, mv, mq, grid, stream)
