@@ -100,7 +100,7 @@ def test_split_count_does_not_change_result(forced):
 
 
 @pytest.mark.parametrize("hq,hk,d", [(8, 8, 128), (16, 8, 128), (64, 4, 128), (8, 4, 64), (16, 1, 64),
-                                     (32, 2, 128)])
+                                     (32, 2, 128), (24, 8, 128), (40, 8, 128), (96, 8, 64)])
 def test_group_sizes_and_edge_lengths(hq, hk, d):
     lens = [0, 1, 2, 63, 64, 65, 127, 128, 129, 191, 255, 256, 257, 1000]
     inp = W.make_decode(len(lens), hq, hk, d, lens, seed=hq + hk + d, extra_pages=2)
@@ -140,7 +140,10 @@ def test_fp8_kv_decode():
     assert_close(out, lse, ref_out, ref_lse, "e4m3")
 
 
-@pytest.mark.parametrize("hq,hk,d", [(8, 4, 64), (16, 16, 128)])
+# e4m3 at D = 128: groups of <= 4 and <= 8 heads run two softmax warpgroups,
+# larger groups one; non-power-of-two groups pad the softmax heads
+@pytest.mark.parametrize("hq,hk,d", [(8, 4, 64), (16, 16, 128), (24, 8, 128), (40, 8, 128), (64, 8, 128),
+                                     (128, 8, 128), (12, 1, 128)])
 def test_fp8_edges(hq, hk, d):
     lens = [0, 1, 63, 64, 65, 129, 300]
     inp = W.make_decode(len(lens), hq, hk, d, lens, seed=6, kv_dtype="e4m3", extra_pages=3)
