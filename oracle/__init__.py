@@ -7,7 +7,10 @@ loads it and has no CPU fallback: it shares no code with the CUDA path.
 * ``decode`` / ``prefill``: fp64 attention computed directly from the
   definition in ``oracle.c`` (two-pass softmax, every element decoded exactly).
 * ``scheduler``: a separate plain restatement of the split-KV scheduling rule.
-* ``bf16_to_f64`` / ``e4m3_to_f64``: the oracle's own element decoders.
+* ``prefill_mla_e4m3``: the MLA prefill with per-head e4m3 q/k parts and scales.
+* ``append_kv``: new tokens written into copies of the pools.
+* ``bf16_to_f64`` / ``f16_to_f64`` / ``e4m3_to_f64`` / ``e4m3_from_f32``: the
+  oracle's own element decoders and encoder.
 
 Inputs are the raw bit-pattern arrays produced by the seeded generator
 (``uint16`` for bf16, ``uint8`` for e4m3); outputs are float64 numpy arrays.
@@ -49,6 +52,9 @@ def _load():
         lib.oracle_e4m3_from_float.restype = ctypes.c_uint8
         lib.oracle_append_kv.argtypes = [i32, i32, i32, i32, i64, i32, P, P, P, P, P, P, P, P, P]
         lib.oracle_append_kv.restype = i32
+        lib.oracle_prefill_mla_e4m3.argtypes = [i32, i32, i32, P, P, P, P, P, P, P, P, P, P, i32, dbl, P, i64,
+                                                P, P]
+        lib.oracle_prefill_mla_e4m3.restype = i32
         lib.oracle_num_threads.restype = i32
         lib.oracle_set_num_threads.argtypes = [i32]
         _lib = lib
@@ -173,3 +179,30 @@ def append_kv(k_new, v_new, cu_new, start_pos, block_table, k_pool, v_pool, k_sc
     if rc != 0:
         raise ValueError("oracle_append_kv: a position falls outside the block table or the pool")
     return kp, vp
+
+
+def prefill_mla_e4m3(q_nope, q_rope, q_scale, k_nope, k_scale, v, k_rope, cu_seqlens_q, cu_seqlens_k,
+                     scale: float, causal: bool = True, qo_offset=None, rows=None):
+    """fp8 MLA prefill (see ``oracle_prefill_mla_e4m3`` in oracle.c).
+    q_nope / k_nope uint8 e4m3 [T, H, 128]; q_rope uint16 bf16 [Tq, Hq, 64];
+    k_rope uint16 bf16 [Tk, 1, 64]; v uint16 bf16 [Tk, Hk, 128]; scales float32.
+    Returns (out float64 [rows, 128] or [Tq, Hq, 128], lse)."""
+    lib = _load()
+    qn, kn = _c(q_nope, np.uint8), _c(k_nope, np.uint8)
+    qr, kr, vv = _c(q_rope, np.uint16), _c(k_rope, np.uint16), _c(v, np.uint16)
+    qs, ks = _c(q_scale, np.float32), _c(k_scale, np.float32)
+    cq, ck = _c(cu_seqlens_q, np.int32), _c(cu_seqlens_k, np.int32)
+    qo = _c(qo_offset, np.int32)
+    rr = _c(rows, np.int64)
+    B = len(cq) - 1
+    total_q, Hq = qn.shape[0], qn.shape[1]
+    Hk = kn.shape[1]
+    nrows = total_q * Hq if rr is None else len(rr)
+    out = np.zeros((nrows, 128), dtype=np.float64)
+    lse = np.zeros(nrows, dtype=np.float64)
+    lib.oracle_prefill_mla_e4m3(B, Hq, Hk, _p(qn), _p(qr), _p(qs), _p(kn), _p(ks), _p(vv), _p(kr), _p(cq), _p(ck),
+                                _p(qo), int(bool(causal)), float(scale), _p(rr), nrows if rr is not None else 0,
+                                _p(out), _p(lse))
+    if rr is None:
+        return out.reshape(total_q, Hq, 128), lse.reshape(total_q, Hq)
+    return out, lse

@@ -24,6 +24,12 @@
  *   - MLA (Modular flare_mla_prefill): the last rope_dim entries of each q row
  *     pair with k_rope[token, 0, :], one row shared by all heads; the first
  *     q_depth - rope_dim pair with the per-head k.
+ *   - fp8 MLA (flare_mla_prefill's overload with q_nope, q_rope, q_scale and
+ *     k_scales): the per-head parts of q and k are e4m3 codes times their
+ *     head's scale; the rope parts and v stay 16-bit.
+ * New tokens are written into pages by oracle_append_kv ("prefill writes into
+ * paged cache", section 4): token p of a sequence goes to row p % 64 of page
+ * block_table[b, p / 64].
  * Every element is decoded exactly to double before use (bf16: the upper half
  * of an fp32 word; e4m3: sign, 4-bit exponent with bias 7, 3-bit mantissa,
  * subnormals, S.1111.111 = NaN, times the per-KV-head scale).  Scores, maximum,
@@ -336,4 +342,63 @@ int oracle_append_kv(int B, int Hk, int D, int max_pages, int64_t num_pages, int
         }
     }
     return bad ? -1 : 0;
+}
+
+/*
+ * fp8 MLA prefill, ragged (Modular flare_mla_prefill, the overload taking
+ * q_nope, q_rope, q_scale and k_scales).  The page lists those arguments
+ * without their granularity; the reading here: one fp32 scale per head.
+ *   q_nope  e4m3 [total_q, Hq, 128]    q_rope bf16 [total_q, Hq, 64]
+ *   k_nope  e4m3 [total_k, Hk, 128]    k_rope bf16 [total_k, 1, 64]
+ *   v       bf16 [total_k, Hk, 128]
+ *   q_scale float [Hq], k_scale float [Hk]
+ * Query row (i, h) is the vector (q_scale[h] * q_nope[i, h], q_rope[i, h]) and
+ * key j of KV head g the vector (k_scale[g] * k_nope[j, g], k_rope[j, 0]);
+ * then the attention of oracle_prefill (masking, offsets, row sampling, outputs
+ * as there; out double [rows, 128]).
+ */
+int oracle_prefill_mla_e4m3(int B, int Hq, int Hk, const uint8_t* q_nope, const uint16_t* q_rope,
+                            const float* q_scale, const uint8_t* k_nope, const float* k_scale,
+                            const uint16_t* v, const uint16_t* k_rope, const int32_t* cu_q,
+                            const int32_t* cu_k, const int32_t* qo_offset, int causal, double scale,
+                            const int64_t* rows, int64_t nrows, double* out, double* lse) {
+    enum { DN = 128, DR = 64, DQK = 192, DV = 128 };
+    int group = Hq / Hk;
+    int64_t total_q = cu_q[B];
+    if (!rows) nrows = total_q * Hq;
+#pragma omp parallel for schedule(dynamic, 1)
+    for (int64_t r = 0; r < nrows; ++r) {
+        int64_t flat = rows ? rows[r] : r;
+        int64_t tok = flat / Hq;
+        int h = (int)(flat % Hq);
+        int g = h / group;
+        int b = 0;
+        while (b < B - 1 && cu_q[b + 1] <= tok) ++b;
+        int64_t i = tok - cu_q[b];
+        int64_t q_len = cu_q[b + 1] - cu_q[b];
+        int64_t kv_len = cu_k[b + 1] - cu_k[b];
+        int64_t off = qo_offset ? qo_offset[b] : kv_len - q_len;
+        int64_t n = kv_len;
+        if (causal) {
+            int64_t lim = off + i + 1;
+            if (lim < n) n = lim;
+            if (n < 0) n = 0;
+        }
+        double* qd = (double*)malloc(sizeof(double) * DQK);
+        double* kd = (double*)malloc(sizeof(double) * (size_t)(n ? n : 1) * DQK);
+        double* vd = (double*)malloc(sizeof(double) * (size_t)(n ? n : 1) * DV);
+        double* sc = (double*)malloc(sizeof(double) * (size_t)(n ? n : 1));
+        double qs = (double)q_scale[h], ks = (double)k_scale[g];
+        for (int d = 0; d < DN; ++d) qd[d] = qs * oracle_e4m3_to_double(q_nope[(tok * Hq + h) * DN + d]);
+        for (int d = 0; d < DR; ++d) qd[DN + d] = oracle_bf16_to_double(q_rope[(tok * Hq + h) * DR + d]);
+        for (int64_t j = 0; j < n; ++j) {
+            int64_t t = cu_k[b] + j;
+            for (int d = 0; d < DN; ++d) kd[j * DQK + d] = ks * oracle_e4m3_to_double(k_nope[(t * Hk + g) * DN + d]);
+            for (int d = 0; d < DR; ++d) kd[j * DQK + DN + d] = oracle_bf16_to_double(k_rope[t * DR + d]);
+            for (int d = 0; d < DV; ++d) vd[j * DV + d] = oracle_bf16_to_double(v[(t * Hk + g) * DV + d]);
+        }
+        attend_row(qd, kd, vd, n, DQK, DV, scale, sc, out + r * DV, &lse[r]);
+        free(qd); free(kd); free(vd); free(sc);
+    }
+    return 0;
 }

@@ -32,7 +32,7 @@ PAGE_SIZE = 64
 _CHUNK = 1 << 22
 
 # stream ids: one per tensor role, so adding a tensor never shifts another
-_S_SEQLENS, _S_PERM, _S_Q, _S_K, _S_V, _S_KROPE, _S_PREFIX = 1, 2, 3, 4, 5, 6, 7
+_S_SEQLENS, _S_PERM, _S_Q, _S_K, _S_V, _S_KROPE, _S_PREFIX, _S_QROPE = 1, 2, 3, 4, 5, 6, 7, 8
 
 
 def _rng(seed: int, stream: int, chunk: int = 0) -> np.random.Generator:
@@ -359,6 +359,72 @@ def mla_prefill(seed: int = 0, batch: int = 8, lo: int = 512, hi: int = 4096,
     """8 sequences, lengths uniform in [512, 4096]; q 192 = 128 nope + 64 rope; v 128."""
     lens = uniform_lengths(seed, batch, lo, hi)
     return make_ragged_prefill(lens, heads, 192, 128, rope_dim=64, seed=seed)
+
+
+@dataclass
+class MlaE4m3Inputs:
+    """MLA prefill with the per-head parts of q and k in e4m3 plus fp32 scales."""
+    q_nope: np.ndarray        # uint8 e4m3 [total_q, Hq, 128]
+    q_rope: np.ndarray        # uint16 bf16 [total_q, Hq, 64]
+    q_scale: np.ndarray       # float32 [Hq]
+    k_nope: np.ndarray        # uint8 e4m3 [total_k, Hk, 128]
+    k_scale: np.ndarray       # float32 [Hk]
+    k_rope: np.ndarray        # uint16 bf16 [total_k, 1, 64]
+    v: np.ndarray             # uint16 bf16 [total_k, Hk, 128]
+    cu_seqlens_q: np.ndarray
+    cu_seqlens_k: np.ndarray
+    scale: float
+    causal: bool = True
+    qo_offset: Optional[np.ndarray] = None
+    meta: dict = field(default_factory=dict)
+
+    @property
+    def batch(self) -> int:
+        return len(self.cu_seqlens_q) - 1
+
+    @property
+    def num_q_heads(self) -> int:
+        return self.q_nope.shape[1]
+
+    @property
+    def num_kv_heads(self) -> int:
+        return self.k_nope.shape[1]
+
+    @property
+    def max_seqlen_q(self) -> int:
+        return int(np.diff(self.cu_seqlens_q).max()) if self.batch else 0
+
+
+def _quantise_heads_3d(x: np.ndarray):
+    """[T, H, D] float32 -> (e4m3 codes, float32 [H] scales), one scale per head
+    (amax / 448, the rule of quantise_per_head)."""
+    t, h, d = x.shape
+    codes, scales = quantise_per_head(x.reshape(t, h, 1, d))
+    return codes.reshape(t, h, d), scales
+
+
+def make_mla_e4m3(lens, num_heads: int, seed: int = 0, num_kv_heads: Optional[int] = None, kv_lens=None,
+                  causal: bool = True, qo_offset=None) -> MlaE4m3Inputs:
+    """Ragged MLA prefill with e4m3 q_nope / k_nope: N(0,1) float32 quantised per
+    head; q_rope, k_rope and v N(0,1) rounded to bf16; scale 1/sqrt(192)."""
+    lens = np.asarray(lens, dtype=np.int32)
+    kv_lens = lens if kv_lens is None else np.asarray(kv_lens, dtype=np.int32)
+    hk = num_heads if num_kv_heads is None else num_kv_heads
+    tq, tk = int(lens.sum()), int(kv_lens.sum())
+    qn, qs = _quantise_heads_3d(normal_f32(seed, _S_Q, tq * num_heads * 128).reshape(tq, num_heads, 128))
+    kn, ks = _quantise_heads_3d(normal_f32(seed, _S_K, tk * hk * 128).reshape(tk, hk, 128))
+    return MlaE4m3Inputs(
+        q_nope=qn, q_rope=bf16_normal(seed, _S_QROPE, (tq, num_heads, 64)), q_scale=qs,
+        k_nope=kn, k_scale=ks, k_rope=bf16_normal(seed, _S_KROPE, (tk, 1, 64)),
+        v=bf16_normal(seed, _S_V, (tk, hk, 128)),
+        cu_seqlens_q=cu_seqlens(lens), cu_seqlens_k=cu_seqlens(kv_lens), scale=1.0 / math.sqrt(192.0),
+        causal=causal, qo_offset=None if qo_offset is None else np.asarray(qo_offset, dtype=np.int32))
+
+
+def mla_e4m3_prefill(seed: int = 0, batch: int = 8, lo: int = 512, hi: int = 4096,
+                     heads: int = 128) -> MlaE4m3Inputs:
+    """The MLA prefill workload's lengths and heads with e4m3 q_nope / k_nope."""
+    return make_mla_e4m3(uniform_lengths(seed, batch, lo, hi), heads, seed=seed)
 
 
 def poison_unused(inp: DecodeInputs, nan_bits: Optional[int] = None) -> DecodeInputs:

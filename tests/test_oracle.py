@@ -430,3 +430,67 @@ def test_append_then_decode_sees_the_new_tokens(kv_dtype):
     # whose cache was empty (b = 0) sees exactly the appended values
     if kv_dtype == "bf16":
         np.testing.assert_array_equal(kp[base.block_table[0, 0], :, :5], np.transpose(kn[:5], (1, 0, 2)))
+
+
+# ---------------------------------------------------------------- fp8 MLA prefill
+
+def _mla_e4m3_small(seed=7, heads=4, hk=None):
+    return W.make_mla_e4m3([9, 130, 1], heads, seed=seed, num_kv_heads=hk)
+
+
+def test_mla_e4m3_with_power_of_two_scales_equals_the_bf16_mla_oracle():
+    """e4m3 values times powers of two are exactly representable in bf16: the fp8
+    MLA oracle must then reproduce the (separately pinned) bf16 MLA oracle bit for
+    bit on the same values -- a dropped scale, a swapped operand or a wrong head
+    index breaks the equality."""
+    inp = _mla_e4m3_small(heads=4, hk=2)
+    rng = np.random.default_rng(0)
+    inp.q_scale = np.exp2(rng.integers(-9, -3, size=4)).astype(np.float32)
+    inp.k_scale = np.exp2(rng.integers(-9, -3, size=2)).astype(np.float32)
+    lut = t_e4m3(np.arange(256, dtype=np.uint8)).numpy()
+    qn = lut[inp.q_nope] * inp.q_scale[None, :, None]
+    kn = lut[inp.k_nope] * inp.k_scale[None, :, None]
+    q16 = np.concatenate([W.f32_to_bf16_bits(qn.astype(np.float32)), inp.q_rope], axis=-1)
+    k16 = W.f32_to_bf16_bits(kn.astype(np.float32))
+    assert np.array_equal(t_bf16(k16).numpy(), kn)  # the re-encoding is exact
+    ref_out, ref_lse = oracle.prefill(q16, k16, inp.v, inp.cu_seqlens_q, inp.cu_seqlens_k, inp.scale, True,
+                                      k_rope=inp.k_rope)
+    out, lse = oracle.prefill_mla_e4m3(inp.q_nope, inp.q_rope, inp.q_scale, inp.k_nope, inp.k_scale, inp.v,
+                                       inp.k_rope, inp.cu_seqlens_q, inp.cu_seqlens_k, inp.scale)
+    assert np.array_equal(out, ref_out) and np.array_equal(lse, ref_lse)
+
+
+def test_mla_e4m3_matches_torch_sdpa_with_general_scales():
+    inp = _mla_e4m3_small(seed=8)
+    out, lse = oracle.prefill_mla_e4m3(inp.q_nope, inp.q_rope, inp.q_scale, inp.k_nope, inp.k_scale, inp.v,
+                                       inp.k_rope, inp.cu_seqlens_q, inp.cu_seqlens_k, inp.scale)
+    qs = torch.from_numpy(inp.q_scale.astype(np.float64))[None, :, None]
+    ks = torch.from_numpy(inp.k_scale.astype(np.float64))[None, :, None]
+    q = torch.cat([t_e4m3(inp.q_nope) * qs, t_bf16(inp.q_rope)], dim=-1)
+    k = t_e4m3(inp.k_nope) * ks
+    v, kr = t_bf16(inp.v), t_bf16(inp.k_rope)
+    for b in range(inp.batch):
+        a, e = inp.cu_seqlens_q[b], inp.cu_seqlens_q[b + 1]
+        L = e - a
+        kk = torch.cat([k[a:e], kr[a:e].expand(L, 4, 64)], dim=-1).transpose(0, 1)
+        ro, rl = _sdpa(q[a:e].transpose(0, 1), kk, v[a:e].transpose(0, 1), inp.scale,
+                       torch.ones(L, L, dtype=torch.bool).tril())
+        np.testing.assert_allclose(out[a:e], ro.transpose(0, 1).numpy(), rtol=1e-12, atol=1e-12)
+        np.testing.assert_allclose(lse[a:e], rl.transpose(0, 1).numpy(), rtol=1e-12, atol=1e-12)
+
+
+def test_mla_e4m3_scale_moves_between_q_and_k():
+    """Only q_scale * k_scale matters: multiplying one by c and dividing the
+    other by c leaves the result unchanged (up to double rounding)."""
+    inp = _mla_e4m3_small(seed=9)
+    args = (inp.v, inp.k_rope, inp.cu_seqlens_q, inp.cu_seqlens_k, inp.scale)
+    o1, l1 = oracle.prefill_mla_e4m3(inp.q_nope, inp.q_rope, inp.q_scale, inp.k_nope, inp.k_scale, *args)
+    o2, l2 = oracle.prefill_mla_e4m3(inp.q_nope, inp.q_rope, (inp.q_scale * 3).astype(np.float32), inp.k_nope,
+                                     (inp.k_scale.astype(np.float64) / 3).astype(np.float32), *args)
+    # float32 scales: (3 q)(k / 3) differs from q k by at most a few float32 ulps
+    np.testing.assert_allclose(o1, o2, rtol=0, atol=1e-5)
+    np.testing.assert_allclose(l1, l2, rtol=0, atol=1e-5)
+    # and the rope term is not scaled: doubling q_scale changes the result
+    o3, _ = oracle.prefill_mla_e4m3(inp.q_nope, inp.q_rope, (inp.q_scale * 2).astype(np.float32), inp.k_nope,
+                                    inp.k_scale, *args)
+    assert np.abs(o3 - o1).max() > 1e-3
