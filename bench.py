@@ -220,6 +220,10 @@ def prefill_workload(name):
         inp = W.mla_prefill(0)
         desc = ("MLA ragged causal prefill: 8 sequences L~U[512,4096], H=128, q 192 = 128 nope + 64 rope, "
                 "k_rope [T,1,64] shared by all heads, v/out 128, scale 1/sqrt(192), seed 0")
+    elif name == "prefill_mla_fp8":
+        inp = W.mla_e4m3_prefill(0)
+        desc = ("fp8 MLA ragged causal prefill: the MLA workload (8 sequences L~U[512,4096], H=128) with q_nope / "
+                "k_nope in e4m3 + per-head fp32 scales (amax/448), q_rope / k_rope / v bf16, seed 0")
     else:
         raise ValueError(name)
     return inp, desc
@@ -286,8 +290,13 @@ def cpu_oracle_prefill_sample(inp, budget_s=None, steps=None, warmup=0, rows_per
 
     def one():
         rows = rng.integers(0, total_rows, size=rows_per_step).astype(np.int64)
-        oracle.prefill(inp.q, inp.k, inp.v, inp.cu_seqlens_q, inp.cu_seqlens_k, inp.scale, True,
-                       block_table=inp.block_table, k_rope=inp.k_rope, qo_offset=inp.qo_offset, rows=rows)
+        if is_fp8_mla(inp):
+            oracle.prefill_mla_e4m3(inp.q_nope, inp.q_rope, inp.q_scale, inp.k_nope, inp.k_scale, inp.v, inp.k_rope,
+                                    inp.cu_seqlens_q, inp.cu_seqlens_k, inp.scale, True, qo_offset=inp.qo_offset,
+                                    rows=rows)
+        else:
+            oracle.prefill(inp.q, inp.k, inp.v, inp.cu_seqlens_q, inp.cu_seqlens_k, inp.scale, True,
+                           block_table=inp.block_table, k_rope=inp.k_rope, qo_offset=inp.qo_offset, rows=rows)
         return int(pairs[rows // hq].sum()) * per_pair
 
     for _ in range(warmup):
@@ -524,18 +533,52 @@ def decode_e2e(inp, dev, stream, sh, full_bytes, world, dist, args):
             "includes": "host schedule + pinned H2D of all inputs + pa_decode + D2H of out/lse + sync"}
 
 
-def prefill_device(inp, dev):
-    import torch
+def is_fp8_mla(inp):
+    return hasattr(inp, "q_nope")
+
+
+def prefill_host_arrays(inp):
+    """Name -> host array (16-bit elements as int16 bit patterns) of every input the call reads."""
+    h = {"cq": inp.cu_seqlens_q, "ck": inp.cu_seqlens_k}
+    if is_fp8_mla(inp):
+        h.update(qn=inp.q_nope, qr=inp.q_rope.view(np.int16), qs=inp.q_scale, kn=inp.k_nope, ks=inp.k_scale,
+                 v=inp.v.view(np.int16), kr=inp.k_rope.view(np.int16))
+        return h
+    h.update(q=inp.q.view(np.int16), k=inp.k.view(np.int16), v=inp.v.view(np.int16))
+    if inp.k_rope is not None:
+        h["kr"] = inp.k_rope.view(np.int16)
+    if inp.paged:
+        h["bt"] = inp.block_table
+    return h
+
+
+def prefill_shapes_for(inp, dev):
+    from paged_kv_attention_fwd_gb300 import binding as B
     from paged_kv_attention_fwd_gb300 import ops
-    d = {"q": ops.as_bf16(inp.q, dev), "k": ops.as_bf16(inp.k, dev), "v": ops.as_bf16(inp.v, dev),
-         "cq": torch.from_numpy(inp.cu_seqlens_q).to(dev), "ck": torch.from_numpy(inp.cu_seqlens_k).to(dev)}
-    d["kr"] = ops.as_bf16(inp.k_rope, dev) if inp.k_rope is not None else None
-    d["bt"] = torch.from_numpy(inp.block_table).to(dev) if inp.paged else None
     sh = ops.prefill_shapes(inp.batch, inp.num_q_heads, inp.num_kv_heads, inp.head_dim_qk, inp.head_dim_v,
                             inp.rope_dim, inp.max_seqlen_q, int(inp.cu_seqlens_q[-1]), int(inp.cu_seqlens_k[-1]),
                             max_pages=inp.block_table.shape[1] if inp.paged else 0,
                             num_pool_pages=inp.k.shape[0] if inp.paged else 0, device=dev)
-    return d, sh
+    if is_fp8_mla(inp):
+        sh.dtype = B.PA_KV_FP8_E4M3
+    return sh
+
+
+def prefill_launch(inp, sh, d, out, lse, ws, stream):
+    """One call of the library's prefill entry for this workload on device buffers `d`."""
+    from paged_kv_attention_fwd_gb300 import binding as B
+    if is_fp8_mla(inp):
+        B.pa_prefill_mla_fp8(sh, d["qn"], d["qr"], d["qs"], d["kn"], d["ks"], d["v"], d["kr"], d["cq"], d["ck"], None,
+                             True, inp.scale, out, lse, ws, stream=stream)
+    else:
+        B.pa_prefill(sh, d["q"], d["k"], d["v"], d.get("kr"), d["cq"], d["ck"], d.get("bt"), None, True, inp.scale,
+                     out, lse, ws, stream=stream)
+
+
+def prefill_device(inp, dev):
+    import torch
+    d = {k: torch.from_numpy(np.ascontiguousarray(v)).to(dev) for k, v in prefill_host_arrays(inp).items()}
+    return d, prefill_shapes_for(inp, dev)
 
 
 def run_prefill(args, rank, world, local_rank, dist):
@@ -551,13 +594,11 @@ def run_prefill(args, rank, world, local_rank, dist):
     out = torch.empty((tq, inp.num_q_heads, inp.head_dim_v), dtype=torch.bfloat16, device=dev)
     lse = torch.empty((tq, inp.num_q_heads), dtype=torch.float32, device=dev)
     ws = torch.zeros(B.pa_prefill_workspace_size(sh), dtype=torch.uint8, device=dev)
-    flush, l2_note = l2_policy(dev, sum(t.numel() * t.element_size() for t in (d["q"], d["k"], d["v"], d["kr"])
-                                        if t is not None))
+    flush, l2_note = l2_policy(dev, sum(t.numel() * t.element_size() for t in d.values()))
     stream = torch.cuda.current_stream(dev)
 
     def step():
-        B.pa_prefill(sh, d["q"], d["k"], d["v"], d["kr"], d["cq"], d["ck"], d["bt"], None, True, inp.scale, out,
-                     lse, ws, stream=stream)
+        prefill_launch(inp, sh, d, out, lse, ws, stream)
 
     for _ in range(args.warmup):
         flush()
@@ -590,11 +631,18 @@ def run_prefill(args, rank, world, local_rank, dist):
     pk, pk_src = peaks()
     tfs = flops / (ms * 1e-3) / 1e12
     peak = pk["bf16_tflops"]
+    peak_source = f"{pk_src} (cuBLAS bf16 GEMM, burst)"
+    if is_fp8_mla(inp):
+        # 256 of the 640 flops per visible pair (q_nope . k_nope) run on e4m3 at twice
+        # the bf16 rate (the nominal dense ratio): the time-weighted peak is
+        # 640 / (256 / 2 + 384) = 1.25 x the bf16 peak
+        peak = round(1.25 * peak, 1)
+        peak_source += " x 1.25: e4m3 share of the flops at the nominal 2x bf16 rate"
     prof = "prefill_kernel_" + args.workload + ".md"
     roofline = {"bound": "tensor", "achieved": round(tfs, 2), "peak": peak, "unit": "TFLOP/s",
                 "frac": round(tfs / peak, 4),
                 "traffic": profiled_traffic(prof, ["prefill.cu", "pa_ptx.cuh", "pa_internal.h"]),
-                "kernel": "prefill_kernel", "peak_source": f"{pk_src} (cuBLAS bf16 GEMM, burst)",
+                "kernel": "prefill_kernel", "peak_source": peak_source,
                 "algorithmic_flops_per_launch": flops, "kernel_ms": round(ms, 5)}
     e2e = None
     if not args.no_e2e:
@@ -631,12 +679,7 @@ def prefill_e2e(inp, dev, stream, sh, flops, world, dist, args):
     def pinned(a):
         return torch.from_numpy(np.ascontiguousarray(a)).pin_memory()
 
-    h = {"q": pinned(inp.q.view(np.int16)), "k": pinned(inp.k.view(np.int16)), "v": pinned(inp.v.view(np.int16)),
-         "cq": pinned(inp.cu_seqlens_q), "ck": pinned(inp.cu_seqlens_k)}
-    if inp.k_rope is not None:
-        h["kr"] = pinned(inp.k_rope.view(np.int16))
-    if inp.paged:
-        h["bt"] = pinned(inp.block_table)
+    h = {k: pinned(v) for k, v in prefill_host_arrays(inp).items()}
     d = {k: torch.empty_like(v, device=dev) for k, v in h.items()}
     tq = int(inp.cu_seqlens_q[-1])
     out_h = torch.empty((tq, inp.num_q_heads, inp.head_dim_v), dtype=torch.int16).pin_memory()
@@ -648,8 +691,7 @@ def prefill_e2e(inp, dev, stream, sh, flops, world, dist, args):
     def step():
         for k in h:
             d[k].copy_(h[k], non_blocking=True)
-        B.pa_prefill(sh, d["q"], d["k"], d["v"], d.get("kr"), d["cq"], d["ck"], d.get("bt"), None, True,
-                     inp.scale, out_d, lse_d, ws, stream=stream)
+        prefill_launch(inp, sh, d, out_d, lse_d, ws, stream)
         out_h.copy_(out_d, non_blocking=True)
         lse_h.copy_(lse_d, non_blocking=True)
         torch.cuda.synchronize(dev)
@@ -805,7 +847,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="decode_gqa",
-                    choices=["decode_gqa", "decode_fp8", "decode_tiny", "prefill_paged", "prefill_mla", "append"])
+                    choices=["decode_gqa", "decode_fp8", "decode_tiny", "prefill_paged", "prefill_mla", "prefill_mla_fp8",
+                             "append"])
     ap.add_argument("--e2e-steps", type=int, default=20)
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--no-e2e", action="store_true")

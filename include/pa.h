@@ -278,6 +278,31 @@ pa_status pa_prefill(const pa_prefill_shapes* shapes, const void* q, const void*
  * PA_STATUS_BYTES + 4 * batch * ceil(max_seqlen_q / 256). */
 size_t pa_prefill_workspace_size(const pa_prefill_shapes* shapes);
 
+/*
+ * pa_prefill_mla_fp8 -- the MLA prefill of pa_prefill with the per-head parts
+ * of q and k in e4m3: Modular flare_mla_prefill's overload taking q_nope,
+ * q_rope, q_scale and k_scales.  The page gives those arguments but not the
+ * granularity of the scales; here there is one fp32 scale per head:
+ *   score(i, j, h) = scale * (q_scale[h] * k_scale[g] * <q_nope[i, h], k_nope[j, g]>
+ *                             + <q_rope[i, h], k_rope[j, 0]>),   g = h / (Hq / Hk)
+ *   q_nope   e4m3 [total_q, Hq, 128]      q_rope  bf16 [total_q, Hq, 64]
+ *   k_nope   e4m3 [total_k, Hk, 128]      k_rope  bf16 [total_k, 1, 64]
+ *   v        bf16 [total_k, Hk, 128]      out     bf16 [total_q, Hq, 128]
+ *   q_scale  fp32 [Hq], k_scale fp32 [Hk] (device), positive and finite
+ * shapes: dtype PA_KV_FP8_E4M3, head_dim_qk 192, rope_dim 64, head_dim_v 128;
+ * keys are ragged (no block table); cu_seqlens, qo_offset, causal, lse and the
+ * workspace as for pa_prefill.  The q_nope . k_nope products run on the e4m3
+ * tensor path, the rope part and P.V in bf16; to add both into one
+ * accumulator the kernel divides the query's rope part by q_scale * k_scale
+ * once (rounded to bf16).  A scale that is not positive and finite is
+ * recorded as PA_ERR_INVALID_ARG in the status word.
+ */
+pa_status pa_prefill_mla_fp8(const pa_prefill_shapes* shapes, const void* q_nope, const void* q_rope,
+                             const float* q_scale, const void* k_nope, const float* k_scale, const void* v,
+                             const void* k_rope, const int32_t* cu_seqlens_q, const int32_t* cu_seqlens_k,
+                             const int32_t* qo_offset, int causal, float scale, void* out, float* lse,
+                             void* workspace, size_t workspace_bytes, cudaStream_t stream);
+
 /* ----------------------------------------------------------------- mixed batches */
 
 typedef struct {

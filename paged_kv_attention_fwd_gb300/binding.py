@@ -92,6 +92,9 @@ def lib() -> ctypes.CDLL:
         L.pa_decode_noalloc.restype = ctypes.c_int
         L.pa_prefill.argtypes = [ctypes.POINTER(pa_prefill_shapes), _P, _P, _P, _P, _P, _P, _P, _P, ctypes.c_int,
                                  f32, _P, _P, _P, sz, _P]
+        L.pa_prefill_mla_fp8.argtypes = [ctypes.POINTER(pa_prefill_shapes), _P, _P, _P, _P, _P, _P, _P, _P, _P, _P,
+                                         ctypes.c_int, f32, _P, _P, _P, sz, _P]
+        L.pa_prefill_mla_fp8.restype = ctypes.c_int
         L.pa_get_static_plan.argtypes = [ctypes.POINTER(pa_decode_shapes), ctypes.POINTER(pa_decode_plan)]
         L.pa_get_static_plan.restype = ctypes.c_int
         L.pa_get_metadata_device.argtypes = [ctypes.POINTER(pa_decode_shapes), ctypes.POINTER(pa_decode_plan), _P, _P,
@@ -219,6 +222,17 @@ def pa_prefill(shapes: pa_prefill_shapes, q, k, v, k_rope, cu_seqlens_q, cu_seql
                             _ptr(cu_seqlens_k), _ptr(block_table), _ptr(qo_offset), int(bool(causal)),
                             float(scale), _ptr(out), _ptr(lse), _ptr(workspace), int(workspace_bytes),
                             _stream(stream)))
+
+
+def pa_prefill_mla_fp8(shapes: pa_prefill_shapes, q_nope, q_rope, q_scale, k_nope, k_scale, v, k_rope, cu_seqlens_q,
+                       cu_seqlens_k, qo_offset, causal: bool, scale: float, out, lse, workspace,
+                       workspace_bytes: Optional[int] = None, stream=None) -> None:
+    if workspace_bytes is None:
+        workspace_bytes = workspace.numel() * workspace.element_size()
+    _check(lib().pa_prefill_mla_fp8(ctypes.byref(shapes), _ptr(q_nope), _ptr(q_rope), _ptr(q_scale), _ptr(k_nope),
+                                    _ptr(k_scale), _ptr(v), _ptr(k_rope), _ptr(cu_seqlens_q), _ptr(cu_seqlens_k),
+                                    _ptr(qo_offset), int(bool(causal)), float(scale), _ptr(out), _ptr(lse),
+                                    _ptr(workspace), int(workspace_bytes), _stream(stream)))
 
 
 def pa_get_static_plan(shapes: pa_decode_shapes) -> pa_decode_plan:

@@ -399,6 +399,49 @@ pa_status pa_decode(const pa_decode_shapes* sh, const pa_decode_plan* plan, cons
                          scale, out, lse, workspace, workspace_bytes, stream);
 }
 
+namespace {
+// The launch arguments common to pa_prefill and pa_prefill_mla_fp8.
+pa_status fill_prefill_args(const pa_prefill_shapes* sh, const int32_t* cu_seqlens_q, const int32_t* cu_seqlens_k,
+                            const int32_t* block_table, const int32_t* qo_offset, int causal, float scale, void* out,
+                            float* lse, void* workspace, size_t workspace_bytes, bool f16, pa::PrefillArgs* a) {
+    const int B = sh->batch, Hq = sh->num_q_heads, Hk = sh->num_kv_heads;
+    const bool paged = block_table != nullptr;
+    const bool rope = sh->rope_dim != 0;
+    a->cu_q = cu_seqlens_q;
+    a->cu_k = cu_seqlens_k;
+    a->block_table = block_table;
+    a->qo_offset = qo_offset;
+    a->out = static_cast<uint16_t*>(out);
+    a->lse = lse;
+    a->status = static_cast<int*>(workspace);
+    a->batch = B;
+    a->num_q_heads = Hq;
+    a->num_kv_heads = Hk;
+    a->group = Hq / Hk;
+    a->max_pages = paged ? sh->max_pages_per_seq : 0;
+    a->num_pool_pages = paged ? sh->num_pool_pages : 0;
+    a->total_q = sh->total_q;
+    a->num_q_tiles = (int32_t)cdiv(sh->max_seqlen_q, 256);
+    // the longest-first unit order lives after the status word when the
+    // workspace has room for it (see pa_prefill_workspace_size)
+    const int64_t units = (int64_t)a->num_q_tiles * B;
+    if (units > 65535) return fail(PA_ERR_UNSUPPORTED, "batch * ceil(max_seqlen_q / 256) must be <= 65535");
+    a->order = (units <= 4096 && workspace_bytes >= PA_STATUS_BYTES + (size_t)units * 4)
+                  ? reinterpret_cast<const int32_t*>(static_cast<uint8_t*>(workspace) + PA_STATUS_BYTES)
+                  : nullptr;
+    a->causal = causal != 0;
+    a->paged = paged;
+    a->rope = rope;
+    a->f16 = f16;
+    a->scale_log2 = scale * 1.4426950408889634f;
+    a->wait_ns = g_wait_limit_ns.load();
+    a->f8 = 0;
+    a->q_scale = nullptr;
+    a->k_scale = nullptr;
+    return PA_OK;
+}
+}  // namespace
+
 pa_status pa_prefill(const pa_prefill_shapes* sh, const void* q, const void* k, const void* v, const void* k_rope,
                      const int32_t* cu_seqlens_q, const int32_t* cu_seqlens_k, const int32_t* block_table,
                      const int32_t* qo_offset, int causal, float scale, void* out, float* lse, void* workspace,
@@ -442,6 +485,7 @@ pa_status pa_prefill(const pa_prefill_shapes* sh, const void* q, const void* k, 
         return fail(PA_ERR_WORKSPACE, "workspace needs %d bytes, got %zu", PA_STATUS_BYTES, workspace_bytes);
 
     const int dqk = sh->head_dim_qk, dk = dqk - sh->rope_dim;
+    pa_status st = PA_OK;
     CUtensorMap mq, mk, mv, mr;
     std::memset(&mr, 0, sizeof mr);
     {
@@ -475,35 +519,12 @@ pa_status pa_prefill(const pa_prefill_shapes* sh, const void* q, const void* k, 
         if (st != PA_OK) return st;
     }
     pa::PrefillArgs a;
-    a.cu_q = cu_seqlens_q;
-    a.cu_k = cu_seqlens_k;
-    a.block_table = block_table;
-    a.qo_offset = qo_offset;
-    a.out = static_cast<uint16_t*>(out);
-    a.lse = lse;
-    a.status = static_cast<int*>(workspace);
-    a.batch = B;
-    a.num_q_heads = Hq;
-    a.num_kv_heads = Hk;
-    a.group = Hq / Hk;
-    a.max_pages = paged ? sh->max_pages_per_seq : 0;
-    a.num_pool_pages = paged ? sh->num_pool_pages : 0;
-    a.total_q = sh->total_q;
-    a.num_q_tiles = (int32_t)cdiv(sh->max_seqlen_q, 256);
-    // the longest-first unit order lives after the status word when the
-    // workspace has room for it (see pa_prefill_workspace_size)
-    const int64_t units = (int64_t)a.num_q_tiles * B;
-    if (units > 65535) return fail(PA_ERR_UNSUPPORTED, "batch * ceil(max_seqlen_q / 256) must be <= 65535");
-    a.order = (units <= 4096 && workspace_bytes >= PA_STATUS_BYTES + (size_t)units * 4)
-                  ? reinterpret_cast<const int32_t*>(static_cast<uint8_t*>(workspace) + PA_STATUS_BYTES)
-                  : nullptr;
-    a.causal = causal != 0;
-    a.paged = paged;
-    a.rope = rope;
-    a.f16 = f16;
-    a.scale_log2 = scale * 1.4426950408889634f;
-    a.wait_ns = g_wait_limit_ns.load();
-    cudaError_t e = pa::launch_prefill(a, dqk, &mq, &mk, &mv, &mr, stream);
+    st = fill_prefill_args(sh, cu_seqlens_q, cu_seqlens_k, block_table, qo_offset, causal, scale, out, lse, workspace,
+                           workspace_bytes, f16, &a);
+    if (st != PA_OK) return st;
+    CUtensorMap mqr;
+    std::memset(&mqr, 0, sizeof mqr);
+    cudaError_t e = pa::launch_prefill(a, dqk, &mq, &mk, &mv, &mr, &mqr, stream);
     if (e != cudaSuccess) return cuda_fail(e, "prefill launch");
     return PA_OK;
 }
@@ -665,6 +686,67 @@ pa_status pa_mixed(const pa_mixed_shapes* sh, const pa_mixed_plan* plan, const v
                           block_table + (size_t)nd * sh->max_pages_per_seq, nullptr, 1, scale, out, lse,
                           static_cast<uint8_t*>(workspace) + dec_ws, workspace_bytes - dec_ws, stream);
     }
+    return PA_OK;
+}
+
+pa_status pa_prefill_mla_fp8(const pa_prefill_shapes* sh, const void* q_nope, const void* q_rope,
+                             const float* q_scale, const void* k_nope, const float* k_scale, const void* v,
+                             const void* k_rope, const int32_t* cu_seqlens_q, const int32_t* cu_seqlens_k,
+                             const int32_t* qo_offset, int causal, float scale, void* out, float* lse,
+                             void* workspace, size_t workspace_bytes, cudaStream_t stream) {
+    if (!sh) return fail(PA_ERR_INVALID_ARG, "shapes must not be NULL");
+    const int B = sh->batch, Hq = sh->num_q_heads, Hk = sh->num_kv_heads;
+    if (B < 0 || sh->total_q < 0 || sh->total_k < 0 || sh->max_seqlen_q < 0)
+        return fail(PA_ERR_INVALID_ARG, "batch, total_q, total_k and max_seqlen_q must be >= 0");
+    if (B == 0 || sh->total_q == 0 || sh->max_seqlen_q == 0) return PA_OK;
+    if (Hq <= 0 || Hk <= 0 || Hq % Hk != 0)
+        return fail(PA_ERR_INVALID_ARG, "num_q_heads (%d) must be a positive multiple of num_kv_heads (%d)", Hq, Hk);
+    if (Hq > 65535) return fail(PA_ERR_UNSUPPORTED, "num_q_heads above 65535");
+    if (sh->dtype != PA_KV_FP8_E4M3)
+        return fail(PA_ERR_INVALID_ARG, "pa_prefill_mla_fp8 needs dtype PA_KV_FP8_E4M3 (got %d)", sh->dtype);
+    if (sh->head_dim_qk != 192 || sh->rope_dim != 64 || sh->head_dim_v != 128)
+        return fail(PA_ERR_UNSUPPORTED, "pa_prefill_mla_fp8 needs head_dim_qk 192, rope_dim 64, head_dim_v 128");
+    if (sh->total_k <= 0) return fail(PA_ERR_INVALID_ARG, "ragged keys need total_k > 0");
+    if (!q_nope || !q_rope || !q_scale || !k_nope || !k_scale || !v || !k_rope || !cu_seqlens_q || !cu_seqlens_k ||
+        !out || !workspace)
+        return fail(PA_ERR_INVALID_ARG, "a required pointer is NULL");
+    if (!aligned16(q_nope) || !aligned16(q_rope) || !aligned16(k_nope) || !aligned16(v) || !aligned16(k_rope) ||
+        !aligned16(out) || !aligned16(workspace))
+        return fail(PA_ERR_INVALID_ARG, "q_nope, q_rope, k_nope, v, k_rope, out and workspace must be 16-byte aligned");
+    if (!std::isfinite(scale)) return fail(PA_ERR_INVALID_ARG, "scale must be finite");
+    if (workspace_bytes < PA_STATUS_BYTES)
+        return fail(PA_ERR_WORKSPACE, "workspace needs %d bytes, got %zu", PA_STATUS_BYTES, workspace_bytes);
+
+    CUtensorMap mq, mqr, mk, mv, mr;
+    const uint64_t tq = (uint64_t)sh->total_q, tk = (uint64_t)sh->total_k;
+    {   // per-head parts: one 128-byte e4m3 row per (token, head)
+        const uint64_t qd[3] = {128, (uint64_t)Hq, tq}, qs[2] = {128, (uint64_t)Hq * 128};
+        const uint64_t kd[3] = {128, (uint64_t)Hk, tk}, ks[2] = {128, (uint64_t)Hk * 128};
+        const uint32_t box[3] = {128, 1, 128};
+        pa_status st = make_map(CU_TENSOR_MAP_DATA_TYPE_UINT8, &mq, q_nope, 3, qd, qs, box);
+        if (st == PA_OK) st = make_map(CU_TENSOR_MAP_DATA_TYPE_UINT8, &mk, k_nope, 3, kd, ks, box);
+        if (st != PA_OK) return st;
+    }
+    {   // bf16 parts: q_rope [Tq, Hq, 64], v [Tk, Hk, 128], k_rope [Tk, 64]
+        const uint64_t rd[3] = {64, (uint64_t)Hq, tq}, rs[2] = {128, (uint64_t)Hq * 128};
+        const uint64_t vd[3] = {128, (uint64_t)Hk, tk}, vs[2] = {256, (uint64_t)Hk * 256};
+        const uint32_t box[3] = {64, 1, 128};
+        const uint64_t krd[2] = {64, tk}, krs[1] = {128};
+        const uint32_t krb[2] = {64, 128};
+        pa_status st = make_map_bf16(&mqr, q_rope, 3, rd, rs, box);
+        if (st == PA_OK) st = make_map_bf16(&mv, v, 3, vd, vs, box);
+        if (st == PA_OK) st = make_map_bf16(&mr, k_rope, 2, krd, krs, krb);
+        if (st != PA_OK) return st;
+    }
+    pa::PrefillArgs a;
+    pa_status st = fill_prefill_args(sh, cu_seqlens_q, cu_seqlens_k, nullptr, qo_offset, causal, scale, out, lse,
+                                     workspace, workspace_bytes, false, &a);
+    if (st != PA_OK) return st;
+    a.f8 = 1;
+    a.q_scale = q_scale;
+    a.k_scale = k_scale;
+    cudaError_t e = pa::launch_prefill(a, 192, &mq, &mk, &mv, &mr, &mqr, stream);
+    if (e != cudaSuccess) return cuda_fail(e, "prefill launch");
     return PA_OK;
 }
 

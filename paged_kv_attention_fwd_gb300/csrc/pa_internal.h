@@ -66,13 +66,16 @@ struct PrefillArgs {
     int32_t num_q_tiles;  // 256-row query blocks per segment: ceil(max_seqlen_q / 256)
     int32_t causal, paged, rope;
     int32_t f16;  // q, k, v, k_rope and out are fp16, else bf16
+    int32_t f8;   // MLA with e4m3 q_nope / k_nope and per-head scales
+    const float* q_scale;  // f8: fp32 [Hq]
+    const float* k_scale;  // f8: fp32 [Hk]
     float scale_log2;
     uint64_t wait_ns;
 };
 
 cudaError_t launch_prefill(const PrefillArgs& a, int head_dim_qk, const CUtensorMap* map_q,
                            const CUtensorMap* map_k, const CUtensorMap* map_v, const CUtensorMap* map_r,
-                           cudaStream_t stream);
+                           const CUtensorMap* map_qr, cudaStream_t stream);
 
 struct AppendArgs {
     const uint16_t* k_new;  // bf16 [total_new, Hk, D]

@@ -3,7 +3,9 @@
 // section 4 mha_fwd_kvcache: K/V gathered through block_table, "Prefill to
 // Cache Mapping"), ragged prefill (MATE dense mode, flash_attn_varlen_func)
 // and the MLA shape whose 64-wide rope key is shared by all heads (Modular
-// flare_mla_prefill: q depth 192 = 128 per-head + 64 shared, output depth 128).
+// flare_mla_prefill: q depth 192 = 128 per-head + 64 shared, output depth 128),
+// also with the per-head parts of q and k in e4m3 (its overload with q_nope,
+// q_rope, q_scale and k_scales; one fp32 scale per head).
 //
 // One CTA per (segment b, 256-row query block, query head h): two 128-row
 // query tiles A and B that share every K/V tile.
@@ -48,24 +50,31 @@ enum : int {
     P_PF = 12,  // [2] P_A, P_B written
     P_OD = 14,  // [2] PV_A, PV_B retired
     P_DONE = 16,
-    P_COUNT = 17
+    P_QS = 17,  // [2] e4m3 MLA: query tile A / B rope part rescaled
+    P_COUNT = 19
 };
 
-template <bool ROPE>
+// F8 (MLA only): a key row is 128 e4m3 bytes (the per-head part) then 64 bf16
+// (the rope part); a query row the same plus a third chunk: its rope part,
+// divided by the head's scale, is held as two bf16 levels hi + lo (chunks 1
+// and 2), so the division costs no precision.
+template <bool ROPE, bool F8>
 struct PrefillLayout {
     static constexpr int kDqk = ROPE ? 192 : 128;
-    static constexpr int kQChunks = kDqk / 64;
+    static constexpr int kQChunks = F8 ? 3 : kDqk / 64;
+    static constexpr int kKChunks = F8 ? 2 : kDqk / 64;
     static constexpr int kTile = 16384;                 // 128 rows x 128 bytes
     static constexpr int kQBytes = kQChunks * kTile;    // one 128-row query tile
-    static constexpr int kKBytes = kQChunks * kTile;    // one 128-key K tile
+    static constexpr int kKBytes = kKChunks * kTile;    // one 128-key K tile
     static constexpr int kVBytes = 2 * kTile;           // one 128-key V tile (dv 128)
-    static constexpr int kNK = ROPE ? 1 : 2;
+    static constexpr int kNK = (ROPE && !F8) ? 1 : 2;
     static constexpr int kNV = 2;
     static constexpr int kQOff = 0;
     static constexpr int kKOff = 2 * kQBytes;
     static constexpr int kVOff = kKOff + kNK * kKBytes;
     static constexpr int kBytes = kVOff + kNV * kVBytes;
     static constexpr int kSmem = kBytes + 1024;
+    static_assert(kSmem + 256 <= 232448, "shared memory per CTA (dynamic + static)");
     static constexpr int kThreads = 320;
 };
 
@@ -111,12 +120,13 @@ __device__ __forceinline__ int kv_tiles_for(const Seg& s, int r0, int r1, bool c
     return (int)((lim + 127) / 128);
 }
 
-template <bool ROPE, bool PAGED>
+template <bool ROPE, bool PAGED, bool F8>
 __global__ void __launch_bounds__(320, 1)
     prefill_kernel(const __grid_constant__ PrefillArgs a, const __grid_constant__ CUtensorMap map_q,
                    const __grid_constant__ CUtensorMap map_k, const __grid_constant__ CUtensorMap map_v,
-                   const __grid_constant__ CUtensorMap map_r) {
-    using L = PrefillLayout<ROPE>;
+                   const __grid_constant__ CUtensorMap map_r, const __grid_constant__ CUtensorMap map_qr) {
+    static_assert(!F8 || (ROPE && !PAGED), "e4m3 query/key parts: MLA with ragged keys only");
+    using L = PrefillLayout<ROPE, F8>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     __shared__ __align__(8) uint64_t bars[P_COUNT];
@@ -163,6 +173,8 @@ __global__ void __launch_bounds__(320, 1)
         }
         mbar_init(&bars[P_VZ], 1);
         mbar_init(&bars[P_DONE], 1);
+        mbar_init(&bars[P_QS + 0], 128);
+        mbar_init(&bars[P_QS + 1], 128);
         *abort_sh = 0;
         fence_barrier_init();
     }
@@ -185,11 +197,17 @@ __global__ void __launch_bounds__(320, 1)
             bool kiss[2] = {false, false}, viss[2] = {false, false};
             uint32_t kpar[2] = {0, 0}, vpar[2] = {0, 0};
             const int ntq = has_b ? 2 : 1;
-            mbar_arrive_expect_tx(&bars[P_QF], ntq * L::kQBytes);
-            for (int x = 0; x < ntq; ++x)
-                for (int c = 0; c < L::kQChunks; ++c)
-                    tma_load_3d(sm + L::kQOff + x * L::kQBytes + c * L::kTile, &map_q, &bars[P_QF], c * 64, h,
-                                sg.q0 + rA + x * 128);
+            mbar_arrive_expect_tx(&bars[P_QF], ntq * (F8 ? 2 * L::kTile : L::kQBytes));
+            for (int x = 0; x < ntq; ++x) {
+                uint8_t* qt = sm + L::kQOff + x * L::kQBytes;
+                if constexpr (F8) {
+                    tma_load_3d(qt, &map_q, &bars[P_QF], 0, h, sg.q0 + rA + x * 128);             // q_nope e4m3
+                    tma_load_3d(qt + L::kTile, &map_qr, &bars[P_QF], 0, h, sg.q0 + rA + x * 128);  // q_rope bf16
+                } else {
+                    for (int c = 0; c < L::kQChunks; ++c)
+                        tma_load_3d(qt + c * L::kTile, &map_q, &bars[P_QF], c * 64, h, sg.q0 + rA + x * 128);
+                }
+            }
             const int kv_pages = (sg.kv_len + kPage - 1) / kPage;
             for (int j = 0; j < nkv && ok; ++j) {
                 // page ids of this tile (paged keys)
@@ -222,6 +240,10 @@ __global__ void __launch_bounds__(320, 1)
                             for (int c = 0; c < 2; ++c)
                                 tma_load_2d(kt + c * L::kTile + i * 8192, &map_k, kf, c * 64,
                                             (int)(((long long)pid[i] * a.num_kv_heads + kvh) * 64));
+                } else if constexpr (F8) {
+                    mbar_arrive_expect_tx(kf, L::kKBytes);
+                    tma_load_3d(kt, &map_k, kf, 0, kvh, sg.k0 + j * 128);           // k_nope e4m3
+                    tma_load_2d(kt + L::kTile, &map_r, kf, 0, sg.k0 + j * 128);    // k_rope bf16
                 } else {
                     mbar_arrive_expect_tx(kf, L::kKBytes);
                     for (int c = 0; c < 2; ++c)
@@ -290,16 +312,39 @@ __global__ void __launch_bounds__(320, 1)
         if (lane == 0) {
             const uint32_t idesc_qk = idesc_f16(128, 128, !a.f16, false, false);
             const uint32_t idesc_pv = idesc_f16(128, 128, !a.f16, false, true);
+            constexpr uint32_t idesc_qk8 = idesc_e4m3(128, 128, false, false);
             const uint32_t qa = smem_u32(sm + L::kQOff);
             bool ok = mbar_wait(&bars[P_QF], 0, abort_sh, a.wait_ns);
+            if constexpr (F8) {
+                // the softmax threads divide the query's rope part by the head's scale first
+                const int nq[2] = {nA, nB};
+                for (int x = 0; x < 2 && ok; ++x)
+                    if (nq[x] > 0) ok = mbar_wait(&bars[P_QS + x], 0, abort_sh, a.wait_ns);
+            }
             auto qk = [&](int x, int j) {
                 const uint32_t qb = qa + x * L::kQBytes;
                 const uint32_t kb = smem_u32(sm + L::kKOff + (j % L::kNK) * L::kKBytes);
+                if constexpr (F8) {
+                    // per-head part on the e4m3 path (32 bytes of depth per MMA), then
+                    // the rope part in bf16, hi and lo query levels against the same
+                    // k_rope chunk, all into one accumulator
 #pragma unroll
-                for (int kk = 0; kk < L::kDqk / 16; ++kk) {
-                    const int c = kk >> 2, off = (kk & 3) * 32;
-                    mma_ss(tbase + s_col(x), sdesc_sw128(qb + c * L::kTile + off, 16, 1024),
-                           sdesc_sw128(kb + c * L::kTile + off, 16, 1024), idesc_qk, kk > 0);
+                    for (int kk = 0; kk < 4; ++kk)
+                        mma_f8_ss(tbase + s_col(x), sdesc_sw128(qb + kk * 32, 16, 1024),
+                                  sdesc_sw128(kb + kk * 32, 16, 1024), idesc_qk8, kk > 0);
+#pragma unroll
+                    for (int lvl = 1; lvl <= 2; ++lvl)
+#pragma unroll
+                        for (int kk = 0; kk < 4; ++kk)
+                            mma_ss(tbase + s_col(x), sdesc_sw128(qb + lvl * L::kTile + kk * 32, 16, 1024),
+                                   sdesc_sw128(kb + L::kTile + kk * 32, 16, 1024), idesc_qk, 1u);
+                } else {
+#pragma unroll
+                    for (int kk = 0; kk < L::kDqk / 16; ++kk) {
+                        const int c = kk >> 2, off = (kk & 3) * 32;
+                        mma_ss(tbase + s_col(x), sdesc_sw128(qb + c * L::kTile + off, 16, 1024),
+                               sdesc_sw128(kb + c * L::kTile + off, 16, 1024), idesc_qk, kk > 0);
+                    }
                 }
                 mma_commit(&bars[P_SF + x]);
             };
@@ -368,15 +413,53 @@ __global__ void __launch_bounds__(320, 1)
         const int nx = x ? nB : nA;
         const bool active = x == 0 || has_b;
         const uint32_t lane_addr = (uint32_t)(q4 * 32) << 16;
-        const float sl2 = a.scale_log2;
+        float sl2 = a.scale_log2;
         const bool f16 = a.f16 != 0;
+        bool ok = true;
+        if constexpr (F8) {
+            // score = scale * (s * <q_nope, k_nope> + <q_rope, k_rope>), s = q_scale[h] * k_scale[kvh]:
+            // the rope part of this thread's query row is divided by s and held as
+            // hi + lo bf16 levels (about 16 significant bits) so that both products
+            // add in one accumulator, and s joins the softmax scale
+            const float s = __ldg(&a.q_scale[h]) * __ldg(&a.k_scale[kvh]);
+            const float inv = 1.f / s;
+            if (!(s > 0.f) || !isfinite(s) || !isfinite(inv)) atomicCAS(a.status, 0, PA_ERR_INVALID_ARG);
+            sl2 *= s;
+            if (active) {
+                ok = mbar_wait(&bars[P_QF], 0, abort_sh, a.wait_ns);
+                ok = __all_sync(0xffffffffu, ok);
+                if (ok) {
+                    // chunk 1 holds the row's 64 bf16 (TMA); chunks 1 and 2 share the
+                    // swizzle pattern, so the lo level goes to the same offset in chunk 2
+                    uint4* qh = reinterpret_cast<uint4*>(sm + L::kQOff + x * L::kQBytes + L::kTile + row * 128);
+                    uint4* ql = qh + L::kTile / 16;
+#pragma unroll
+                    for (int u = 0; u < 8; ++u) {
+                        const uint4 w = qh[u];
+                        const uint32_t e[4] = {w.x, w.y, w.z, w.w};
+                        uint32_t eh[4], el[4];
+#pragma unroll
+                        for (int t = 0; t < 4; ++t) {
+                            const float a0 = __uint_as_float(e[t] << 16) * inv;
+                            const float a1 = __uint_as_float(e[t] & 0xFFFF0000u) * inv;
+                            eh[t] = pack16x2(a0, a1, false);
+                            const float h0 = __uint_as_float(eh[t] << 16), h1 = __uint_as_float(eh[t] & 0xFFFF0000u);
+                            el[t] = pack16x2(a0 - h0, a1 - h1, false);
+                        }
+                        qh[u] = make_uint4(eh[0], eh[1], eh[2], eh[3]);
+                        ql[u] = make_uint4(el[0], el[1], el[2], el[3]);
+                    }
+                    fence_proxy_async_smem();
+                    mbar_arrive(&bars[P_QS + x]);
+                }
+            }
+        }
         // keys this row may see: [0, lim)
         long long lim = sg.kv_len;
         if (causal) lim = min(lim, (long long)sg.off + i + 1);
         if (lim < 0) lim = 0;
         float m_run = -INFINITY, l_run = 0.f;
-        bool ok = true;
-        for (int j = 0; active && j < nx; ++j) {
+        for (int j = 0; active && ok && j < nx; ++j) {
             ok = mbar_wait(&bars[P_SF + x], j & 1, abort_sh, a.wait_ns);
             ok = __all_sync(0xffffffffu, ok);
             if (!ok) break;
@@ -577,14 +660,14 @@ __global__ void __launch_bounds__(512) prefill_order_kernel(const PrefillArgs a,
     for (int u = threadIdx.x; u < n; u += blockDim.x) order[u] = (int32_t)(key[u] & 0xFFFFFFFFu);
 }
 
-template <bool ROPE, bool PAGED>
+template <bool ROPE, bool PAGED, bool F8>
 cudaError_t launch_t(const PrefillArgs& a, const CUtensorMap* mq, const CUtensorMap* mk, const CUtensorMap* mv,
-                     const CUtensorMap* mr, cudaStream_t stream) {
-    using L = PrefillLayout<ROPE>;
+                     const CUtensorMap* mr, const CUtensorMap* mqr, cudaStream_t stream) {
+    using L = PrefillLayout<ROPE, F8>;
     static bool configured = false;
     if (!configured) {
-        cudaError_t e =
-            cudaFuncSetAttribute(prefill_kernel<ROPE, PAGED>, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kSmem);
+        cudaError_t e = cudaFuncSetAttribute(prefill_kernel<ROPE, PAGED, F8>,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize, L::kSmem);
         if (e != cudaSuccess) return e;
         configured = true;
     }
@@ -594,16 +677,19 @@ cudaError_t launch_t(const PrefillArgs& a, const CUtensorMap* mq, const CUtensor
         if (e != cudaSuccess) return e;
     }
     dim3 grid((unsigned)(a.num_q_tiles * a.batch) * (unsigned)a.num_q_heads);
-    prefill_kernel<ROPE, PAGED><<<grid, L::kThreads, L::kSmem, stream>>>(a, *mq, *mk, *mv, *mr);
+    prefill_kernel<ROPE, PAGED, F8><<<grid, L::kThreads, L::kSmem, stream>>>(a, *mq, *mk, *mv, *mr, *mqr);
     return cudaGetLastError();
 }
 
 }  // namespace
 
 cudaError_t launch_prefill(const PrefillArgs& a, int head_dim_qk, const CUtensorMap* mq, const CUtensorMap* mk,
-                           const CUtensorMap* mv, const CUtensorMap* mr, cudaStream_t stream) {
-    if (head_dim_qk == 192) return launch_t<true, false>(a, mq, mk, mv, mr, stream);
-    return a.paged ? launch_t<false, true>(a, mq, mk, mv, mr, stream) : launch_t<false, false>(a, mq, mk, mv, mr, stream);
+                           const CUtensorMap* mv, const CUtensorMap* mr, const CUtensorMap* mqr,
+                           cudaStream_t stream) {
+    if (a.f8) return launch_t<true, false, true>(a, mq, mk, mv, mr, mqr, stream);
+    if (head_dim_qk == 192) return launch_t<true, false, false>(a, mq, mk, mv, mr, mqr, stream);
+    return a.paged ? launch_t<false, true, false>(a, mq, mk, mv, mr, mqr, stream)
+                   : launch_t<false, false, false>(a, mq, mk, mv, mr, mqr, stream);
 }
 
 }  // namespace pa

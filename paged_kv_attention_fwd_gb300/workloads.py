@@ -394,6 +394,12 @@ class MlaE4m3Inputs:
     def max_seqlen_q(self) -> int:
         return int(np.diff(self.cu_seqlens_q).max()) if self.batch else 0
 
+    head_dim_qk = 192
+    head_dim_v = 128
+    rope_dim = 64
+    block_table = None
+    paged = False
+
 
 def _quantise_heads_3d(x: np.ndarray):
     """[T, H, D] float32 -> (e4m3 codes, float32 [H] scales), one scale per head

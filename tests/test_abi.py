@@ -178,3 +178,30 @@ def test_mixed_plan_splits_at_first_multi_token_segment():
 def test_mixed_plan_rejects_more_queries_than_keys():
     with pytest.raises(B.PaError, match="query tokens"):
         B.pa_get_mixed_plan(np.array([0, 1, 30], np.int32), np.array([5, 9], np.int32), None, mixed_shapes(2))
+
+
+def _mla_fp8_shapes(**over):
+    d = dict(batch=2, num_q_heads=8, num_kv_heads=8, head_dim_qk=192, head_dim_v=128, rope_dim=64,
+             max_seqlen_q=100, total_q=150, total_k=150, page_size=64, max_pages_per_seq=0, num_pool_pages=0,
+             num_sms=152, dtype=B.PA_KV_FP8_E4M3)
+    d.update(over)
+    return B.pa_prefill_shapes(**d)
+
+
+@pytest.mark.parametrize("over,args,status,needle", [
+    ({"dtype": B.PA_KV_BF16}, {}, B.PA_ERR_INVALID_ARG, "PA_KV_FP8_E4M3"),
+    ({"head_dim_qk": 128, "rope_dim": 0}, {}, B.PA_ERR_UNSUPPORTED, "192"),
+    ({"num_q_heads": 6, "num_kv_heads": 4}, {}, B.PA_ERR_INVALID_ARG, "multiple"),
+    ({}, {"q_scale": None}, B.PA_ERR_INVALID_ARG, "NULL"),
+    ({}, {"k_rope": _Fake(addr=(1 << 20) + 4)}, B.PA_ERR_INVALID_ARG, "aligned"),
+    ({}, {"scale": float("inf")}, B.PA_ERR_INVALID_ARG, "finite"),
+    ({}, {"workspace": _Fake(n=16)}, B.PA_ERR_WORKSPACE, "workspace"),
+])
+def test_prefill_mla_fp8_host_validation(over, args, status, needle):
+    f = _Fake()
+    kw = dict(q_nope=f, q_rope=f, q_scale=f, k_nope=f, k_scale=f, v=f, k_rope=f, cu_seqlens_q=f, cu_seqlens_k=f,
+              qo_offset=None, causal=True, scale=0.07, out=f, lse=None, workspace=f)
+    kw.update(args)
+    with pytest.raises(B.PaError) as e:
+        B.pa_prefill_mla_fp8(_mla_fp8_shapes(**over), stream=1, **kw)
+    assert e.value.status == status and needle in str(e.value)
