@@ -1,10 +1,12 @@
 // append.cu -- write new tokens' K and V into their pages (FlashMLA "Tensor
 // Shapes Reference", section 4: prefill writes into the paged cache; token p
 // of a sequence is row p % 64 of page block_table[b, p / 64], "Prefill to
-// Cache Mapping").  A copy, so HBM-bound: one warp per (new token, KV head);
-// lanes 0-15 move the key row and lanes 16-31 the value row in 16-byte pieces
-// (for e4m3 pools each piece of 8 elements is divided by the head's scale and
-// rounded to e4m3, nearest even, saturating).
+// Cache Mapping").  A copy, so HBM-bound: one warp per (new token, group of up
+// to 4 KV heads).  The warp finds the token's sequence, position and page
+// once, then every lane issues all of its 16-byte loads (key and value rows of
+// the group's heads, 8 elements each) before any store, so several loads per
+// lane are in flight.  For e4m3 pools each piece of 8 elements is divided by
+// the head's scale and rounded to e4m3, nearest even, saturating.
 #include <cuda_bf16.h>
 #include <cuda_fp8.h>
 
@@ -13,11 +15,17 @@
 namespace pa {
 namespace {
 
+constexpr int kHeadsPerWarp = 4;
+constexpr int kPiecesPerLane = kHeadsPerWarp * 2 * (128 / 8) / 32;  // D = 128: 4
+
 __global__ void __launch_bounds__(256) append_kernel(const AppendArgs a) {
+    const int hk = a.num_kv_heads;
+    const int groups = (hk + kHeadsPerWarp - 1) / kHeadsPerWarp;
     const long long w = (long long)blockIdx.x * 8 + (threadIdx.x >> 5);
     const int lane = threadIdx.x & 31;
-    if (w >= (long long)a.total_new * a.num_kv_heads) return;
-    const int tok = (int)(w / a.num_kv_heads), h = (int)(w % a.num_kv_heads);
+    if (w >= (long long)a.total_new * groups) return;
+    const int tok = (int)(w / groups), h0 = (int)(w % groups) * kHeadsPerWarp;
+    const int nh = min(kHeadsPerWarp, hk - h0);
     // segment holding this token: last b with cu[b] <= tok
     int lo = 0, hi = a.batch - 1;
     while (lo < hi) {
@@ -36,21 +44,34 @@ __global__ void __launch_bounds__(256) append_kernel(const AppendArgs a) {
         if (lane == 0) atomicCAS(a.status, 0, PA_ERR_DEVICE_BOUNDS);
         return;
     }
-    const long long dst_row = ((long long)page * a.num_kv_heads + h) * kPage + pos % kPage;
-    const long long src_row = (long long)tok * a.num_kv_heads + h;
-    const bool is_v = lane >= 16;
-    const uint16_t* src = (is_v ? a.v_new : a.k_new) + src_row * a.head_dim;
-    const int pieces = a.head_dim / 8;  // 8 elements (16 source bytes) per piece
-    if (!a.fp8) {
-        uint16_t* dst = static_cast<uint16_t*>(is_v ? a.v_pool : a.k_pool) + dst_row * a.head_dim;
-        for (int i = lane & 15; i < pieces; i += 16)
-            reinterpret_cast<uint4*>(dst)[i] = __ldg(reinterpret_cast<const uint4*>(src) + i);
-    } else {
-        uint8_t* dst = static_cast<uint8_t*>(is_v ? a.v_pool : a.k_pool) + dst_row * a.head_dim;
-        const float scale = __ldg(&(is_v ? a.v_scale : a.k_scale)[h]);
-        for (int i = lane & 15; i < pieces; i += 16) {
-            const uint4 v = __ldg(reinterpret_cast<const uint4*>(src) + i);
-            const uint32_t w4[4] = {v.x, v.y, v.z, v.w};
+    const int pieces = a.head_dim / 8;  // 8 elements (16 source bytes) per piece of a row
+    const int total = nh * 2 * pieces;  // key and value rows of the group's heads
+    // all loads first: piece idx = lane + 32 i -> head h0 + idx / (2 pieces), row (key, value), piece
+    uint4 v[kPiecesPerLane];
+#pragma unroll
+    for (int i = 0; i < kPiecesPerLane; ++i) {
+        const int idx = lane + 32 * i;
+        if (idx < total) {
+            const int hl = idx / (2 * pieces), rem = idx % (2 * pieces);
+            const uint16_t* src = (rem >= pieces ? a.v_new : a.k_new) + ((long long)tok * hk + h0 + hl) * a.head_dim;
+            v[i] = __ldg(reinterpret_cast<const uint4*>(src) + rem % pieces);
+        }
+    }
+#pragma unroll
+    for (int i = 0; i < kPiecesPerLane; ++i) {
+        const int idx = lane + 32 * i;
+        if (idx >= total) continue;
+        const int hl = idx / (2 * pieces), rem = idx % (2 * pieces), piece = rem % pieces;
+        const bool is_v = rem >= pieces;
+        const int h = h0 + hl;
+        const long long dst_row = ((long long)page * hk + h) * kPage + pos % kPage;
+        if (!a.fp8) {
+            uint16_t* dst = static_cast<uint16_t*>(is_v ? a.v_pool : a.k_pool) + dst_row * a.head_dim;
+            reinterpret_cast<uint4*>(dst)[piece] = v[i];
+        } else {
+            uint8_t* dst = static_cast<uint8_t*>(is_v ? a.v_pool : a.k_pool) + dst_row * a.head_dim;
+            const float scale = __ldg(&(is_v ? a.v_scale : a.k_scale)[h]);
+            const uint32_t w4[4] = {v[i].x, v[i].y, v[i].z, v[i].w};
             uint32_t out[2] = {0u, 0u};
 #pragma unroll
             for (int k = 0; k < 4; ++k) {
@@ -60,7 +81,7 @@ __global__ void __launch_bounds__(256) append_kernel(const AppendArgs a) {
                     (uint32_t)__nv_cvt_float2_to_fp8x2(make_float2(x0, x1), __NV_SATFINITE, __NV_E4M3);
                 out[k >> 1] |= b2 << ((k & 1) * 16);
             }
-            reinterpret_cast<uint2*>(dst)[i] = make_uint2(out[0], out[1]);
+            reinterpret_cast<uint2*>(dst)[piece] = make_uint2(out[0], out[1]);
         }
     }
 }
@@ -68,7 +89,8 @@ __global__ void __launch_bounds__(256) append_kernel(const AppendArgs a) {
 }  // namespace
 
 cudaError_t launch_append(const AppendArgs& a, cudaStream_t stream) {
-    const long long warps = (long long)a.total_new * a.num_kv_heads;
+    const long long groups = (a.num_kv_heads + kHeadsPerWarp - 1) / kHeadsPerWarp;
+    const long long warps = (long long)a.total_new * groups;
     append_kernel<<<(unsigned)((warps + 7) / 8), 256, 0, stream>>>(a);
     return cudaGetLastError();
 }

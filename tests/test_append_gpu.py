@@ -54,9 +54,13 @@ def gpu_append(base, prior, new, kn, vn, block_table=None):
     return k_out, v_out, st
 
 
-@pytest.mark.parametrize("kv_dtype,d", [("bf16", 128), ("bf16", 64), ("e4m3", 128), ("e4m3", 64), ("f16", 128)])
-def test_append_bit_exact(kv_dtype, d):
-    base, prior, new, kn, vn = case(kv_dtype, d=d)
+@pytest.mark.parametrize("kv_dtype,d,hk", [("bf16", 128, 4), ("bf16", 64, 4), ("e4m3", 128, 4), ("e4m3", 64, 4),
+                                          ("f16", 128, 4), ("bf16", 128, 3), ("bf16", 64, 5), ("e4m3", 128, 9),
+                                          ("bf16", 128, 1)])
+def test_append_bit_exact(kv_dtype, d, hk):
+    # a warp moves the rows of up to 4 KV heads: head counts that are not a
+    # multiple of 4 leave a partial last group
+    base, prior, new, kn, vn = case(kv_dtype, d=d, hk=hk)
     k_gpu, v_gpu, st = gpu_append(base, prior, new, kn, vn)
     assert st == B.PA_OK
     k_ref, v_ref = oracle.append_kv(kn, vn, W.cu_seqlens(new), prior, base.block_table, base.k_pool, base.v_pool,
