@@ -820,7 +820,9 @@ def run_append(args, rank, world, local_rank, dist):
         "config": {"workload": desc, "bytes_per_step": nbytes, "l2": L2_NOTE,
                    "parallelism": f"replicas x{world}"},
         "roofline": {"bound": "hbm", "achieved": round(gbs, 1), "peak": pk["hbm_gbs"], "unit": "GB/s",
-                     "frac": round(gbs / pk["hbm_gbs"], 4), "traffic": None, "kernel": "append_kernel",
+                     "frac": round(gbs / pk["hbm_gbs"], 4),
+                     "traffic": profiled_traffic("append_kernel_append.md", ["append.cu", "pa_internal.h"]),
+                     "kernel": "append_kernel",
                      "peak_source": f"{pk_src} (copy bandwidth)", "algorithmic_bytes_per_launch": nbytes,
                      "kernel_ms": round(ms, 5)},
         "cpu_baseline": cpu,

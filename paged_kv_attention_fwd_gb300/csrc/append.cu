@@ -18,13 +18,13 @@ namespace {
 constexpr int kHeadsPerWarp = 4;
 constexpr int kPiecesPerLane = kHeadsPerWarp * 2 * (128 / 8) / 32;  // D = 128: 4
 
+// grid: x = tokens / 8 (one warp each), y = group of kHeadsPerWarp KV heads
 __global__ void __launch_bounds__(256) append_kernel(const AppendArgs a) {
     const int hk = a.num_kv_heads;
-    const int groups = (hk + kHeadsPerWarp - 1) / kHeadsPerWarp;
-    const long long w = (long long)blockIdx.x * 8 + (threadIdx.x >> 5);
+    const int tok = (int)(blockIdx.x * 8u + (threadIdx.x >> 5));
     const int lane = threadIdx.x & 31;
-    if (w >= (long long)a.total_new * groups) return;
-    const int tok = (int)(w / groups), h0 = (int)(w % groups) * kHeadsPerWarp;
+    if (tok >= a.total_new) return;
+    const int h0 = (int)blockIdx.y * kHeadsPerWarp;
     const int nh = min(kHeadsPerWarp, hk - h0);
     // segment holding this token: last b with cu[b] <= tok
     int lo = 0, hi = a.batch - 1;
@@ -44,24 +44,25 @@ __global__ void __launch_bounds__(256) append_kernel(const AppendArgs a) {
         if (lane == 0) atomicCAS(a.status, 0, PA_ERR_DEVICE_BOUNDS);
         return;
     }
-    const int pieces = a.head_dim / 8;  // 8 elements (16 source bytes) per piece of a row
-    const int total = nh * 2 * pieces;  // key and value rows of the group's heads
+    const int lg = a.head_dim == 128 ? 4 : 3;  // log2 of the pieces of 8 elements (16 source bytes) in a row
+    const int pieces = 1 << lg;
+    const int total = nh * 2 * pieces;         // key and value rows of the group's heads
     // all loads first: piece idx = lane + 32 i -> head h0 + idx / (2 pieces), row (key, value), piece
     uint4 v[kPiecesPerLane];
 #pragma unroll
     for (int i = 0; i < kPiecesPerLane; ++i) {
         const int idx = lane + 32 * i;
         if (idx < total) {
-            const int hl = idx / (2 * pieces), rem = idx % (2 * pieces);
+            const int hl = idx >> (lg + 1), rem = idx & (2 * pieces - 1);
             const uint16_t* src = (rem >= pieces ? a.v_new : a.k_new) + ((long long)tok * hk + h0 + hl) * a.head_dim;
-            v[i] = __ldg(reinterpret_cast<const uint4*>(src) + rem % pieces);
+            v[i] = __ldg(reinterpret_cast<const uint4*>(src) + (rem & (pieces - 1)));
         }
     }
 #pragma unroll
     for (int i = 0; i < kPiecesPerLane; ++i) {
         const int idx = lane + 32 * i;
         if (idx >= total) continue;
-        const int hl = idx / (2 * pieces), rem = idx % (2 * pieces), piece = rem % pieces;
+        const int hl = idx >> (lg + 1), rem = idx & (2 * pieces - 1), piece = rem & (pieces - 1);
         const bool is_v = rem >= pieces;
         const int h = h0 + hl;
         const long long dst_row = ((long long)page * hk + h) * kPage + pos % kPage;
@@ -89,9 +90,8 @@ __global__ void __launch_bounds__(256) append_kernel(const AppendArgs a) {
 }  // namespace
 
 cudaError_t launch_append(const AppendArgs& a, cudaStream_t stream) {
-    const long long groups = (a.num_kv_heads + kHeadsPerWarp - 1) / kHeadsPerWarp;
-    const long long warps = (long long)a.total_new * groups;
-    append_kernel<<<(unsigned)((warps + 7) / 8), 256, 0, stream>>>(a);
+    const unsigned groups = (unsigned)((a.num_kv_heads + kHeadsPerWarp - 1) / kHeadsPerWarp);
+    append_kernel<<<dim3((unsigned)((a.total_new + 7) / 8), groups), 256, 0, stream>>>(a);
     return cudaGetLastError();
 }
 

@@ -536,7 +536,8 @@ pa_status pa_append_kv(const pa_append_shapes* sh, const void* k_new, const void
     if (!sh) return fail(PA_ERR_INVALID_ARG, "shapes must not be NULL");
     if (sh->batch < 0 || sh->total_new < 0) return fail(PA_ERR_INVALID_ARG, "batch and total_new must be >= 0");
     if (sh->batch == 0 || sh->total_new == 0) return PA_OK;
-    if (sh->num_kv_heads <= 0) return fail(PA_ERR_INVALID_ARG, "num_kv_heads must be positive");
+    if (sh->num_kv_heads <= 0 || sh->num_kv_heads > 65535)
+        return fail(PA_ERR_INVALID_ARG, "num_kv_heads must be in [1, 65535] (got %d)", sh->num_kv_heads);
     if (sh->head_dim != 64 && sh->head_dim != 128)
         return fail(PA_ERR_UNSUPPORTED, "head_dim must be 64 or 128 (got %d)", sh->head_dim);
     if (sh->page_size != pa::kPage) return fail(PA_ERR_INVALID_ARG, "page_size must be 64 (got %d)", sh->page_size);

@@ -137,8 +137,9 @@ __global__ void __launch_bounds__(320, 1)
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     // CTA index -> (unit rank, head): heads come in groups of hg (up to 32);
     // within a group the unit rank is the slow index and the head the fast one.
-    // With an order from prefill_order_kernel the costliest units start first,
-    // and CTAs that run together share a handful of heads' K/V tiles in L2.
+    // With an order from prefill_order_kernel the units run sequence by
+    // sequence, longest first, so CTAs that run together share one sequence's
+    // K/V tiles in L2 across a group of heads.
     const int units = a.num_q_tiles * a.batch;
     const int hg = a.num_q_heads < 32 ? a.num_q_heads : 32;
     const int group = (int)(blockIdx.x / (unsigned)(hg * units));
@@ -617,9 +618,14 @@ __global__ void __launch_bounds__(320, 1)
     }
 }
 
-// Sort the (segment, 256-row query block) units by KV tiles to process, most
-// first (ties: lower unit index), so the longest CTAs start first.  One CTA;
-// bitonic sort of up to 4096 keys in shared memory.
+// Order the (segment, 256-row query block) units sequence by sequence, the
+// longest key range first, and within a sequence its last query block first
+// (the most KV tiles under causal masking).  CTAs that run together then work
+// on one sequence (across a group of heads), so its K/V tiles are shared in L2,
+// and the costliest work still starts first.  One CTA; bitonic sort of up to
+// 4096 64-bit keys in shared memory:
+//   [63:40] 0xFFFFFF - kv_len   [39:20] b   [19:0] 0xFFFFF - query block
+// with kv_len forced to 0 for idle units (their rows lie past q_len).
 __global__ void __launch_bounds__(512) prefill_order_kernel(const PrefillArgs a, int32_t* order) {
     __shared__ unsigned long long key[4096];
     const int n = a.batch * a.num_q_tiles;
@@ -630,14 +636,9 @@ __global__ void __launch_bounds__(512) prefill_order_kernel(const PrefillArgs a,
         if (u < n) {
             const int b = u % a.batch, pair = u / a.batch;
             const Seg sg = load_seg(a, b);
-            const int rA = pair * 256;
-            int cost = -1;
-            if (rA < sg.q_len) {
-                const bool causal = a.causal != 0;
-                cost = 2 + kv_tiles_for(sg, rA, min(rA + 128, sg.q_len), causal) +
-                       (rA + 128 < sg.q_len ? kv_tiles_for(sg, rA + 128, min(rA + 256, sg.q_len), causal) : 0);
-            }
-            k = ((unsigned long long)(unsigned)(0x7FFFFFFF - cost) << 32) | (unsigned)u;
+            const long long kv = pair * 256 < sg.q_len ? min(max(sg.kv_len, 0), 0xFFFFFF - 1) : -1;
+            k = ((unsigned long long)(0xFFFFFF - 1 - kv) << 40) | ((unsigned long long)b << 20) |
+                (unsigned long long)(0xFFFFF - pair);
         }
         key[u] = k;
     }
@@ -657,7 +658,11 @@ __global__ void __launch_bounds__(512) prefill_order_kernel(const PrefillArgs a,
             __syncthreads();
         }
     }
-    for (int u = threadIdx.x; u < n; u += blockDim.x) order[u] = (int32_t)(key[u] & 0xFFFFFFFFu);
+    for (int u = threadIdx.x; u < n; u += blockDim.x) {
+        const unsigned long long kk = key[u];
+        const int b = (int)((kk >> 20) & 0xFFFFF), pair = 0xFFFFF - (int)(kk & 0xFFFFF);
+        order[u] = pair * a.batch + b;
+    }
 }
 
 template <bool ROPE, bool PAGED, bool F8>
