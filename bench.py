@@ -114,6 +114,23 @@ def profiled_traffic(profile_name, files):
         return None
 
 
+def max_over_ranks(values, dist, device):
+    """The max of each value over all ranks: the slowest rank sets the job's
+    time.  Identity without a process group."""
+    if dist is None:
+        return [float(v) for v in values]
+    import torch
+    t = torch.tensor([float(v) for v in values], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return [float(x) for x in t]
+
+
+def job_value(units_per_rank, world, seconds):
+    """Whole-job throughput under weak scaling: every rank processes the same
+    units, all ranks' units over the (max-over-ranks) time."""
+    return world * units_per_rank / seconds
+
+
 class ClockSampler:
     """nvidia-smi sampling of SM clock and throttle reasons during the timed region."""
 
@@ -423,17 +440,14 @@ def run_decode(args, rank, world, local_rank, dist):
     step_ms = [ev[i][0].elapsed_time(ev[i][1]) for i in range(K)]
     ms = sum(step_ms) / K
     kern_ms = ms
-    if dist is not None:
-        t = torch.tensor([ms, kern_ms], dtype=torch.float64, device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms, kern_ms = float(t[0]), float(t[1])
+    ms, kern_ms = max_over_ranks([ms, kern_ms], dist, dev)
     st = B.pa_check_status(p.workspace, stream)
     if st != B.PA_OK:
         raise RuntimeError(f"device status {st}: {B.pa_last_error()}")
     clocks = clk.summary()
 
     pk, pk_src = peaks()
-    value = world * full_bytes / (ms * 1e-3) / 1e9
+    value = job_value(full_bytes, world, ms * 1e-3) / 1e9
     achieved = full_bytes / (kern_ms * 1e-3) / 1e9
     kernel_files = ["decode.cu", "pa_ptx.cuh", "pa_internal.h"]
     kname = "decode_f8_kernel" if fp8 and inp.head_dim == 128 else "decode_kernel"
@@ -522,10 +536,7 @@ def decode_e2e(inp, dev, stream, sh, full_bytes, world, dist, args):
     for _ in range(E):
         step()
     el = time.perf_counter() - t0
-    if dist is not None:
-        t = torch.tensor([el], dtype=torch.float64, device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        el = float(t[0])
+    el, = max_over_ranks([el], dist, dev)
     h2d = sum(v.numel() * v.element_size() for v in h.values()) + plan0.meta_ints * 4
     d2h = out_h.numel() * 2 + lse_h.numel() * 4
     return {"value": round(world * full_bytes * E / el / 1e9, 2), "unit": "GB/s", "h2d_bytes_per_step": h2d,
@@ -621,10 +632,7 @@ def run_prefill(args, rank, world, local_rank, dist):
     if dist is not None:
         dist.barrier()
     ms = sum(ev[i][0].elapsed_time(ev[i][1]) for i in range(K)) / K
-    if dist is not None:
-        t = torch.tensor([ms], dtype=torch.float64, device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t[0])
+    ms, = max_over_ranks([ms], dist, dev)
     if B.pa_check_status(ws, stream) != B.PA_OK:
         raise RuntimeError(B.pa_last_error())
     clocks = clk.summary()
@@ -705,10 +713,7 @@ def prefill_e2e(inp, dev, stream, sh, flops, world, dist, args):
     for _ in range(E):
         step()
     el = time.perf_counter() - t0
-    if dist is not None:
-        t = torch.tensor([el], dtype=torch.float64, device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        el = float(t[0])
+    el, = max_over_ranks([el], dist, dev)
     h2d = sum(v.numel() * v.element_size() for v in h.values())
     d2h = out_h.numel() * 2 + lse_h.numel() * 4
     return {"value": round(world * flops * E / el / 1e12, 3), "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
@@ -771,10 +776,7 @@ def run_append(args, rank, world, local_rank, dist):
             ev[i][1].record(stream)
         torch.cuda.synchronize(dev)
     ms = sum(ev[i][0].elapsed_time(ev[i][1]) for i in range(K)) / K
-    if dist is not None:
-        t = torch.tensor([ms], dtype=torch.float64, device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t[0])
+    ms, = max_over_ranks([ms], dist, dev)
     if B.pa_check_status(ws, stream) != B.PA_OK:
         raise RuntimeError(B.pa_last_error())
     pk, pk_src = peaks()
