@@ -1331,13 +1331,9 @@ template <int NP, int WG>
 cudaError_t launch_f8_np(const DecodeArgs& a, const CUtensorMap* mk, const CUtensorMap* mv, int grid,
                          cudaStream_t stream) {
     using L = F8Layout<WG>;
-    static bool configured = false;
-    if (!configured) {
-        cudaError_t e =
-            cudaFuncSetAttribute(decode_f8_kernel<NP, WG>, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kSmem);
-        if (e != cudaSuccess) return e;
-        configured = true;
-    }
+    static std::atomic<uint64_t> configured{0};
+    cudaError_t e = ensure_dynamic_smem(decode_f8_kernel<NP, WG>, L::kSmem, configured);
+    if (e != cudaSuccess) return e;
     decode_f8_kernel<NP, WG><<<grid, L::kThreads, L::kSmem, stream>>>(a, *mk, *mv);
     return cudaGetLastError();
 }
@@ -1397,13 +1393,9 @@ template <int D, bool FP8, int NP>
 cudaError_t launch_decode_np(const DecodeArgs& a, const CUtensorMap* mk, const CUtensorMap* mv, const CUtensorMap* mq,
                              int grid, cudaStream_t stream) {
     using L = DecodeLayout<D, FP8>;
-    static bool configured = false;
-    if (!configured) {
-        cudaError_t e =
-            cudaFuncSetAttribute(decode_kernel<D, FP8, NP>, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kSmem);
-        if (e != cudaSuccess) return e;
-        configured = true;
-    }
+    static std::atomic<uint64_t> configured{0};
+    cudaError_t e = ensure_dynamic_smem(decode_kernel<D, FP8, NP>, L::kSmem, configured);
+    if (e != cudaSuccess) return e;
     decode_kernel<D, FP8, NP><<<grid, L::kThreads, L::kSmem, stream>>>(a, *mk, *mv, *mq);
     return cudaGetLastError();
 }

@@ -1,6 +1,7 @@
 // pa_internal.h -- declarations shared by the host API and the kernel files.
 #pragma once
 
+#include <atomic>
 #include <cstddef>
 #include <cstdint>
 #include <cuda.h>
@@ -100,5 +101,21 @@ cudaError_t launch_schedule(const int32_t* seq_lens, int B, int Hk, int max_page
 
 // Record a message for pa_last_error() on this host thread (pa_api.cu).
 void set_last_error(const char* msg);
+
+// Allow `kernel` `bytes` of dynamic shared memory on the current device.  A
+// function attribute belongs to one device's context, so it is set once per
+// (kernel, device): `done` holds one bit per device id (ids >= 64 set it on
+// every launch).  Concurrent first calls may both set it; that is harmless.
+template <typename K>
+cudaError_t ensure_dynamic_smem(K* kernel, int bytes, std::atomic<uint64_t>& done) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    const uint64_t bit = dev >= 0 && dev < 64 ? (uint64_t)1 << dev : 0;
+    if (bit && (done.load(std::memory_order_acquire) & bit)) return cudaSuccess;
+    e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+    if (e == cudaSuccess && bit) done.fetch_or(bit, std::memory_order_acq_rel);
+    return e;
+}
 
 }  // namespace pa

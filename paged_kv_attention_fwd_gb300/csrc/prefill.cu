@@ -669,16 +669,12 @@ template <bool ROPE, bool PAGED, bool F8>
 cudaError_t launch_t(const PrefillArgs& a, const CUtensorMap* mq, const CUtensorMap* mk, const CUtensorMap* mv,
                      const CUtensorMap* mr, const CUtensorMap* mqr, cudaStream_t stream) {
     using L = PrefillLayout<ROPE, F8>;
-    static bool configured = false;
-    if (!configured) {
-        cudaError_t e = cudaFuncSetAttribute(prefill_kernel<ROPE, PAGED, F8>,
-                                             cudaFuncAttributeMaxDynamicSharedMemorySize, L::kSmem);
-        if (e != cudaSuccess) return e;
-        configured = true;
-    }
+    static std::atomic<uint64_t> configured{0};
+    cudaError_t e = ensure_dynamic_smem(prefill_kernel<ROPE, PAGED, F8>, L::kSmem, configured);
+    if (e != cudaSuccess) return e;
     if (a.order) {
         prefill_order_kernel<<<1, 512, 0, stream>>>(a, const_cast<int32_t*>(a.order));
-        cudaError_t e = cudaGetLastError();
+        e = cudaGetLastError();
         if (e != cudaSuccess) return e;
     }
     dim3 grid((unsigned)(a.num_q_tiles * a.batch) * (unsigned)a.num_q_heads);
