@@ -164,9 +164,14 @@ pa_status pa_get_metadata_device(const pa_decode_shapes* shapes, const pa_decode
  *   out          bf16 [B, Hq, D] (fp16 with PA_KV_FP16)
  *   lse          fp32 [B, Hq] or NULL
  *   workspace    >= plan->workspace_bytes device bytes; the first 256 bytes hold
- *                the status word.  Zero-fill it once before first use; the
- *                library leaves the status word at zero on success.  A
- *                workspace must not be used by two calls that may overlap.
+ *                the status word, then the split partials, then one arrival
+ *                counter per (sequence, KV head) for the in-kernel merge.
+ *                Zero-fill it once before first use; on success the library
+ *                leaves the status word and the counters at zero.  After a
+ *                call that returned an error or left a device status (see
+ *                pa_check_status), zero-fill it again: an aborted launch can
+ *                leave counters part-way.  A workspace must not be used by two
+ *                calls that may overlap.
  *
  * With fp8 KV the query is used in fp16 (exact for |q| in [2^-14, 65504];
  * smaller magnitudes round to fp16 subnormals).
