@@ -622,7 +622,7 @@ pa_status pa_get_mixed_plan(const int32_t* cu_q, const int32_t* kv_lens, const i
     if (B > 0 && (!cu_q || !kv_lens)) return fail(PA_ERR_INVALID_ARG, "cu_seqlens_q_host and kv_lens_host are needed");
     if (sh->head_dim != 128) return fail(PA_ERR_UNSUPPORTED, "mixed batches need head_dim 128 (got %d)", sh->head_dim);
     if (sh->kv_dtype != PA_KV_BF16 && sh->kv_dtype != PA_KV_FP16)
-        return fail(PA_ERR_UNSUPPORTED, "mixed batches need bf16 or fp16 pools");
+        return fail(PA_ERR_UNSUPPORTED, "mixed batches need bf16 or fp16 pools (kv_dtype %d)", sh->kv_dtype);
     std::memset(plan, 0, sizeof *plan);
     int nd = 0;
     while (nd < B && cu_q[nd + 1] - cu_q[nd] == 1) ++nd;

@@ -205,3 +205,12 @@ def test_prefill_mla_fp8_host_validation(over, args, status, needle):
     with pytest.raises(B.PaError) as e:
         B.pa_prefill_mla_fp8(_mla_fp8_shapes(**over), stream=1, **kw)
     assert e.value.status == status and needle in str(e.value)
+
+
+def test_mixed_plan_rejects_e4m3_pools():
+    # the prefill part has no e4m3-KV form: a mixed batch needs 16-bit pools
+    sh = mixed_shapes(2)
+    sh.kv_dtype = B.PA_KV_FP8_E4M3
+    with pytest.raises(B.PaError) as e:
+        B.pa_get_mixed_plan(np.array([0, 1, 30], np.int32), np.array([5, 90], np.int32), None, sh)
+    assert e.value.status == B.PA_ERR_UNSUPPORTED and "pools" in str(e.value)

@@ -22,19 +22,20 @@ def gpu():
     build()
 
 
-def run_mixed(q_lens, kv_lens, hq=8, hk=2, seed=60):
-    inp = W.make_paged_prefill(q_lens, kv_lens, hq, hk, 128, seed=seed, extra_pages=2)
+def run_mixed(q_lens, kv_lens, hq=8, hk=2, seed=60, dtype="bf16"):
+    inp = W.make_paged_prefill(q_lens, kv_lens, hq, hk, 128, seed=seed, extra_pages=2, dtype=dtype)
     dev = "cuda"
     kl = np.asarray(kv_lens, np.int32)
     sh = B.pa_mixed_shapes(batch=len(q_lens), num_q_heads=hq, num_kv_heads=hk, head_dim=128, page_size=64,
                            max_pages_per_seq=inp.block_table.shape[1], num_pool_pages=inp.k.shape[0],
-                           kv_dtype=B.PA_KV_BF16, num_sms=ops.num_sms(), ctas_per_sm=0, forced_splits=0)
+                           kv_dtype=B.PA_KV_FP16 if dtype == "f16" else B.PA_KV_BF16, num_sms=ops.num_sms(),
+                           ctas_per_sm=0, forced_splits=0)
     meta, plan = B.pa_get_mixed_plan(inp.cu_seqlens_q, kl, inp.block_table, sh)
     tq = int(inp.cu_seqlens_q[-1])
-    out = torch.empty((tq, hq, 128), dtype=torch.bfloat16, device=dev)
+    out = torch.empty((tq, hq, 128), dtype=torch.float16 if dtype == "f16" else torch.bfloat16, device=dev)
     lse = torch.empty((tq, hq), dtype=torch.float32, device=dev)
     ws = torch.zeros(plan.workspace_bytes, dtype=torch.uint8, device=dev)
-    B.pa_mixed(sh, plan, ops.as_bf16(inp.q, dev), ops.as_bf16(inp.k, dev), ops.as_bf16(inp.v, dev),
+    B.pa_mixed(sh, plan, ops.as_16(inp.q, dev, dtype), ops.as_16(inp.k, dev, dtype), ops.as_16(inp.v, dev, dtype),
                torch.from_numpy(inp.block_table).to(dev), torch.from_numpy(inp.cu_seqlens_q).to(dev),
                torch.from_numpy(inp.cu_seqlens_k).to(dev), torch.from_numpy(kl).to(dev),
                torch.from_numpy(meta).to(dev), inp.scale, out, lse, ws)
@@ -42,7 +43,7 @@ def run_mixed(q_lens, kv_lens, hq=8, hk=2, seed=60):
     dec = (plan.decode.workspace_bytes + 255) // 256 * 256 if plan.num_decode else 0
     st = (B.pa_check_status(ws), B.pa_check_status(ws[dec:]))
     ro, rl = oracle.prefill(inp.q, inp.k, inp.v, inp.cu_seqlens_q, inp.cu_seqlens_k, inp.scale, True,
-                            block_table=inp.block_table)
+                            block_table=inp.block_table, dtype=dtype)
     return out.float().cpu().numpy(), lse.cpu().numpy(), ro, rl, plan, st
 
 
@@ -58,6 +59,15 @@ def test_mixed_batch_matches_oracle(q_lens, kv_lens):
     while lead < len(q_lens) and q_lens[lead] == 1:
         lead += 1
     assert plan.num_decode == lead
+    err = np.abs(out - ro)
+    assert np.all(np.isfinite(out)) and err.max() <= 1e-2 and err.mean() <= 1e-3
+    assert np.abs(lse - rl).max() <= 1e-3
+
+
+def test_mixed_batch_fp16():
+    q_lens, kv_lens = [1, 1, 33, 1, 200], [900, 70, 100, 64, 1500]
+    out, lse, ro, rl, plan, st = run_mixed(q_lens, kv_lens, seed=61, dtype="f16")
+    assert st == (B.PA_OK, B.PA_OK) and plan.num_decode == 2
     err = np.abs(out - ro)
     assert np.all(np.isfinite(out)) and err.max() <= 1e-2 and err.mean() <= 1e-3
     assert np.abs(lse - rl).max() <= 1e-3
