@@ -142,6 +142,22 @@ __device__ __forceinline__ Item load_item(const DecodeArgs& a, int idx, int item
 
 __device__ __forceinline__ int item_tiles(const Item& it) { return (it.p1 - it.p0 + 1) >> 1; }
 
+// The first kItemCache items of a CTA are decoded once, in the prologue, into
+// shared memory: every role reads its next item there instead of repeating
+// the chain of dependent global loads at each item boundary.
+constexpr int kItemCache = 64;
+
+__device__ __forceinline__ void fill_item_cache(Item* cache, const DecodeArgs& a, int it_lo, int it_hi,
+                                                int items_off, int lane) {
+    const int n = min(it_hi - it_lo, kItemCache);
+    for (int i = lane; i < n; i += 32) cache[i] = load_item(a, it_lo + i, items_off);
+}
+
+__device__ __forceinline__ Item get_item(const Item* cache, const DecodeArgs& a, int j, int it_lo, int items_off) {
+    const int i = j - it_lo;
+    return i < kItemCache ? cache[i] : load_item(a, j, items_off);
+}
+
 // All-reduce NP per-thread values over a warp by transposition: each
 // shuffle level exchanges half of the remaining values, so NP = 16 costs 16
 // shuffles instead of 80.  Returns the reduction of value head_of_lane<NP>(lane).
@@ -239,12 +255,13 @@ __device__ __forceinline__ bool partials_written(uint64_t* pw, uint64_t* hd, uin
 }
 
 template <int D>
-__device__ void merge_warp(const DecodeArgs& a, int it_lo, int it_hi, int items_off, uint64_t* pw, uint64_t* hd,
+__device__ void merge_warp(const DecodeArgs& a, const Item* items, int it_lo, int it_hi, int items_off,
+                           uint64_t* pw, uint64_t* hd,
                            volatile int* abort_sh, int lane) {
     uint32_t k = 0;
     const int G = a.group;
     for (int j = it_lo; j < it_hi; ++j) {
-        const Item it = load_item(a, j, items_off);
+        const Item it = get_item(items, a, j, it_lo, items_off);
         if (it.nsplit <= 1) continue;
         bool ok = mbar_wait(&pw[k & 1], (k >> 1) & 1, abort_sh, a.wait_ns);
         ok = __all_sync(0xffffffffu, ok);
@@ -310,6 +327,7 @@ __global__ void __launch_bounds__(DecodeLayout<D, FP8>::kThreads, 1)
     __shared__ __align__(8) uint64_t bars[B_COUNT];
     __shared__ uint32_t tmem_base_sh;
     __shared__ int abort_store;
+    __shared__ __align__(16) Item items_sh[kItemCache];
     volatile int* abort_sh = &abort_store;
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -350,6 +368,7 @@ __global__ void __launch_bounds__(DecodeLayout<D, FP8>::kThreads, 1)
         tmem_alloc(&tmem_base_sh, kTmemCols);
         tmem_relinquish();
     }
+    if (warp == L::kMergeWarp) fill_item_cache(items_sh, a, it_lo, it_hi, items_off, lane);
     if (warp >= 2 && warp < 6) {
         // P rows of padding heads must read as zero in every PV product, and
         // so must the query rows past the group (the query TMA writes only
@@ -376,7 +395,7 @@ __global__ void __launch_bounds__(DecodeLayout<D, FP8>::kThreads, 1)
             bool ok = true;
             constexpr uint32_t page_bytes = FP8 ? 64u * D : 64u * D * 2u;
             for (int j = it_lo; j < it_hi && ok; ++j) {
-                const Item it = load_item(a, j, items_off);
+                const Item it = get_item(items_sh, a, j, it_lo, items_off);
                 const int ntiles = item_tiles(it);
                 const long long bt_row = (long long)it.b * a.max_pages;
                 if (!FP8 && ntiles > 0) {
@@ -473,7 +492,7 @@ __global__ void __launch_bounds__(DecodeLayout<D, FP8>::kThreads, 1)
                 return true;
             };
             for (int j = it_lo; j < it_hi && ok; ++j) {
-                const Item it = load_item(a, j, items_off);
+                const Item it = get_item(items_sh, a, j, it_lo, items_off);
                 const int ntiles = item_tiles(it);
                 if (ntiles == 0) continue;
                 if (!mbar_wait(&bars[B_QF + (qi & 1)], (qi >> 1) & 1, abort_sh, a.wait_ns)) {
@@ -529,12 +548,12 @@ __global__ void __launch_bounds__(DecodeLayout<D, FP8>::kThreads, 1)
         float* red = reinterpret_cast<float*>(sm + L::kRedOff);
 
         auto next_nonempty = [&](int j) {
-            while (j < it_hi && item_tiles(load_item(a, j, items_off)) == 0) ++j;
+            while (j < it_hi && item_tiles(get_item(items_sh, a, j, it_lo, items_off)) == 0) ++j;
             return j;
         };
         // query rows of the item's KV group -> swizzled K-major tile of 16 rows
         auto load_q = [&](int j, uint32_t qidx) {
-            const Item it = load_item(a, j, items_off);
+            const Item it = get_item(items_sh, a, j, it_lo, items_off);
             uint8_t* qb = sm + L::kQOff + (qidx & 1) * L::kQBytes;
             constexpr int kRowChunks = D / 8;  // 16-byte chunks per row
             for (int c = row; c < kNPad * kRowChunks; c += 128) {
@@ -572,7 +591,7 @@ __global__ void __launch_bounds__(DecodeLayout<D, FP8>::kThreads, 1)
         uint32_t g = 0, qi = 0, npartial = 0;
         bool aborted = false;
         for (int j = it_lo; j < it_hi && !aborted; ++j) {
-            const Item it = load_item(a, j, items_off);
+            const Item it = get_item(items_sh, a, j, it_lo, items_off);
             const int ntiles = item_tiles(it);
             const bool partial = it.nsplit > 1;
             const long long head0 = (long long)it.kvh * G;
@@ -706,7 +725,7 @@ __global__ void __launch_bounds__(DecodeLayout<D, FP8>::kThreads, 1)
         tc_fence_before();
     } else if (warp == L::kMergeWarp) {
         // ------------------------------------------------------------ split merge
-        if (a.counters) merge_warp<D>(a, it_lo, it_hi, items_off, &bars[B_PW], &bars[B_HD], abort_sh, lane);
+        if (a.counters) merge_warp<D>(a, items_sh, it_lo, it_hi, items_off, &bars[B_PW], &bars[B_HD], abort_sh, lane);
     } else {
         // ------------------------------------------------------------ e4m3 -> f16 converters
         if constexpr (FP8) {
@@ -741,7 +760,7 @@ __global__ void __launch_bounds__(DecodeLayout<D, FP8>::kThreads, 1)
                 }
             };
             for (int j = it_lo; j < it_hi && ok; ++j) {
-                const Item it = load_item(a, j, items_off);
+                const Item it = get_item(items_sh, a, j, it_lo, items_off);
                 const int ntiles = item_tiles(it);
                 const int key_end = min(it.seq_len, it.p1 * kPage);
                 for (int t = 0; t < ntiles; ++t, ++g) {
@@ -874,6 +893,7 @@ __global__ void __launch_bounds__(F8Layout<WG>::kThreads, 1)
     __shared__ __align__(8) uint64_t bars[F_COUNT];
     __shared__ uint32_t tmem_base_sh;
     __shared__ int abort_store;
+    __shared__ __align__(16) Item items_sh[kItemCache];
     volatile int* abort_sh = &abort_store;
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -908,6 +928,7 @@ __global__ void __launch_bounds__(F8Layout<WG>::kThreads, 1)
         tmem_alloc(&tmem_base_sh, L::kTmemCols);
         tmem_relinquish();
     }
+    if (warp == L::kMergeWarp) fill_item_cache(items_sh, a, it_lo, it_hi, items_off, lane);
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
@@ -921,7 +942,7 @@ __global__ void __launch_bounds__(F8Layout<WG>::kThreads, 1)
             bool issued[NS] = {};
             bool ok = true;
             for (int j = it_lo; j < it_hi && ok; ++j) {
-                const Item it = load_item(a, j, items_off);
+                const Item it = get_item(items_sh, a, j, it_lo, items_off);
                 const int ntiles = item_tiles(it);
                 const long long bt_row = (long long)it.b * a.max_pages;
                 for (int t = 0; t < ntiles; ++t, ++g) {
@@ -971,11 +992,11 @@ __global__ void __launch_bounds__(F8Layout<WG>::kThreads, 1)
             constexpr uint32_t idesc_qk = idesc_e4m3(128, 48, false, false);
             constexpr uint32_t idesc_pv = idesc_e4m3(128, 32, true, true);
             uint32_t total = 0;
-            for (int j = it_lo; j < it_hi; ++j) total += (uint32_t)item_tiles(load_item(a, j, items_off));
+            for (int j = it_lo; j < it_hi; ++j) total += (uint32_t)item_tiles(get_item(items_sh, a, j, it_lo, items_off));
             int jq = it_lo;  // item of the next QK, and its tile count
             uint32_t jq_tiles = 0;
             auto skip_empty = [&]() {
-                while (jq < it_hi && (jq_tiles = (uint32_t)item_tiles(load_item(a, jq, items_off))) == 0) ++jq;
+                while (jq < it_hi && (jq_tiles = (uint32_t)item_tiles(get_item(items_sh, a, jq, it_lo, items_off))) == 0) ++jq;
             };
             skip_empty();
             uint32_t qk = 0, pv = 0, tq = 0, qi = 0, qbase = 0;
@@ -1033,7 +1054,7 @@ __global__ void __launch_bounds__(F8Layout<WG>::kThreads, 1)
         }
     } else if (warp == L::kMergeWarp) {
         // ------------------------------------------------------------ split merge
-        if (a.counters) merge_warp<D>(a, it_lo, it_hi, items_off, &bars[F_PW], &bars[F_HD], abort_sh, lane);
+        if (a.counters) merge_warp<D>(a, items_sh, it_lo, it_hi, items_off, &bars[F_PW], &bars[F_HD], abort_sh, lane);
     } else {
         // ------------------------------------------------------------ softmax
         const int wg = (warp - 2) >> 2;   // warpgroup: takes the tiles g with g % WG == wg
@@ -1048,7 +1069,7 @@ __global__ void __launch_bounds__(F8Layout<WG>::kThreads, 1)
         float* qsc = reinterpret_cast<float*>(sm + L::kQscOff);
 
         auto next_nonempty = [&](int j) {
-            while (j < it_hi && item_tiles(load_item(a, j, items_off)) == 0) ++j;
+            while (j < it_hi && item_tiles(get_item(items_sh, a, j, it_lo, items_off)) == 0) ++j;
             return j;
         };
         // query of the item's KV group -> three e4m3 levels (rows level*16 + head),
@@ -1057,7 +1078,7 @@ __global__ void __launch_bounds__(F8Layout<WG>::kThreads, 1)
         const int qh = row >> 3, qc = row & 7;  // head, 16-element chunk of d
         uint4 pf0 = make_uint4(0, 0, 0, 0), pf1 = make_uint4(0, 0, 0, 0);
         auto fetch_q = [&](int j) {
-            const Item it = load_item(a, j, items_off);
+            const Item it = get_item(items_sh, a, j, it_lo, items_off);
             pf0 = pf1 = make_uint4(0, 0, 0, 0);
             if (qh < G) {
                 const long long qrow = (long long)it.b * a.num_q_heads + (long long)it.kvh * G + qh;
@@ -1130,7 +1151,7 @@ __global__ void __launch_bounds__(F8Layout<WG>::kThreads, 1)
         uint32_t g0 = 0, qi = 0, npartial = 0, lt = 0;
         bool aborted = false;
         for (int j = it_lo; j < it_hi && !aborted; ++j) {
-            const Item it = load_item(a, j, items_off);
+            const Item it = get_item(items_sh, a, j, it_lo, items_off);
             const int ntiles = item_tiles(it);
             const bool partial = it.nsplit > 1;
             const long long head0 = (long long)it.kvh * G;
