@@ -822,7 +822,8 @@ __global__ void __launch_bounds__(DecodeLayout<D, FP8>::kThreads, 1)
 // output, so that two chains share every SM sub-partition; at the end of the
 // item the second warpgroup hands (m, l, o) to the first through shared
 // memory, which merges the two and writes.  Larger groups keep one warpgroup
-// (register budget).
+// (register budget).  Warps: 0 producer, 1 QK issuer, 2 .. 1 + 4 WG softmax,
+// then the split merge warp and the PV issuer.
 template <int WG>
 struct F8Layout {
     static constexpr int kStages = 5;
@@ -845,7 +846,8 @@ struct F8Layout {
     static constexpr int kBytes = kXOff + kXBytes;
     static constexpr int kSmem = kBytes + 1024;
     static constexpr int kMergeWarp = 2 + 4 * WG;
-    static constexpr int kThreads = (kMergeWarp + 1) * 32;
+    static constexpr int kPvWarp = kMergeWarp + 1;
+    static constexpr int kThreads = (kPvWarp + 1) * 32;
     // TMEM: S buffers of 48 columns (three query levels x 16) in 64-column
     // slots, then O buffers of 32 columns (hi and lo P levels x 16)
     static constexpr uint32_t kTmemCols = WG == 2 ? 512 : 256;
@@ -863,10 +865,11 @@ enum : int {
     F_SF = 12,     // [4] S tile in TMEM
     F_PF = 16,     // [4] P written
     F_OF = 20,     // [4] O tile in TMEM
-    F_DONE = 24,   // all MMAs retired (teardown)
+    F_DONE = 24,   // all QK MMAs retired (teardown)
     F_PW = 25,     // [2] an item's partials written (merge warp)
     F_HD = 27,     // [2] merge warp done with an item
-    F_COUNT = 29
+    F_DONE2 = 29,  // all PV MMAs retired (teardown)
+    F_COUNT = 30
 };
 
 __device__ __forceinline__ uint32_t e4m3x2(float lo, float hi) {
@@ -921,6 +924,7 @@ __global__ void __launch_bounds__(F8Layout<WG>::kThreads, 1)
             mbar_init(&bars[F_HD + i], 1);
         }
         mbar_init(&bars[F_DONE], 1);
+        mbar_init(&bars[F_DONE2], 1);
         *abort_sh = 0;
         fence_barrier_init();
     }
@@ -981,76 +985,80 @@ __global__ void __launch_bounds__(F8Layout<WG>::kThreads, 1)
                 if (issued[s]) mbar_wait(&bars[F_FULL + s], last_par[s], nullptr, a.wait_ns);
         }
     } else if (warp == 1) {
-        // ------------------------------------------------------------ MMA issuer
-        // Tile g uses S/O/P buffer g % NB; its softmax is done by warpgroup g % WG.
-        // Event-driven: every pass issues the next QK if its pages, its query
-        // and its S buffer are ready, and the next PV if its P is written, so
-        // that neither product waits behind the other (two warpgroups consume
-        // S in turn).  QK runs at most NB tiles ahead of PV: S buffer g % NB
-        // is free once PV(g - NB) was issued, since that PV needed P(g - NB).
+        // ------------------------------------------------------------ QK issuer
+        // Tile g uses S/O/P buffer g % NB; its softmax is done by warpgroup
+        // g % WG.  QK and PV are issued by two threads in two warps, each
+        // blocking on its own barriers, so that neither product waits behind
+        // the other and no thread spends its time polling (a tcgen05.commit
+        // tracks the MMAs of the thread that issues it, so each thread
+        // commits its own).  S buffer g % NB is free again once P(g - NB) is
+        // written: the softmax read S(g - NB) before that.
         if (lane == 0) {
             constexpr uint32_t idesc_qk = idesc_e4m3(128, 48, false, false);
+            uint32_t g = 0, qi = 0;
+            bool ok = true;
+            for (int j = it_lo; j < it_hi && ok; ++j) {
+                const int ntiles = item_tiles(get_item(items_sh, a, j, it_lo, items_off));
+                if (ntiles == 0) continue;
+                if (!mbar_wait(&bars[F_QF + (qi & 1)], (qi >> 1) & 1, abort_sh, a.wait_ns)) {
+                    ok = false;
+                    break;
+                }
+                const uint32_t qbase = smem_u32(sm + L::kQ3Off + (qi & 1) * L::kQ3Bytes);
+                ++qi;
+                for (int t = 0; t < ntiles; ++t, ++g) {
+                    if (g >= (uint32_t)NB &&
+                        !mbar_wait(&bars[F_PF + (g - NB) % NB], ((g - NB) / NB) & 1, abort_sh, a.wait_ns)) {
+                        ok = false;
+                        break;
+                    }
+                    if (!mbar_wait(&bars[F_FULL + g % NS], (g / NS) & 1, abort_sh, a.wait_ns)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t kbase = smem_u32(sm + (g % NS) * L::kStageBytes);
+#pragma unroll
+                    for (int kk = 0; kk < 4; ++kk)  // 32 bytes of d per step; N = 48 = hi, mid, lo levels
+                        mma_f8_ss(tbase + L::s_col(g % NB), sdesc_sw128(kbase + kk * 32, 16, 1024),
+                                  sdesc_sw128(qbase + kk * 32, 16, 1024), idesc_qk, kk > 0 ? 1u : 0u);
+                    mma_commit(&bars[F_SF + g % NB]);
+                }
+            }
+            if (!ok) fail(a, abort_sh, PA_ERR_TIMEOUT);
+            mma_commit(&bars[F_DONE]);
+            mbar_wait(&bars[F_DONE], 0, nullptr, a.wait_ns);
+        }
+    } else if (warp == L::kPvWarp) {
+        // ------------------------------------------------------------ PV issuer
+        // PV(g) once P(g) is written; its completion hands O(g) to the fold
+        // and releases ring stage g % NS.
+        if (lane == 0) {
             constexpr uint32_t idesc_pv = idesc_e4m3(128, 32, true, true);
             uint32_t total = 0;
             for (int j = it_lo; j < it_hi; ++j) total += (uint32_t)item_tiles(get_item(items_sh, a, j, it_lo, items_off));
-            int jq = it_lo;  // item of the next QK, and its tile count
-            uint32_t jq_tiles = 0;
-            auto skip_empty = [&]() {
-                while (jq < it_hi && (jq_tiles = (uint32_t)item_tiles(get_item(items_sh, a, jq, it_lo, items_off))) == 0) ++jq;
-            };
-            skip_empty();
-            uint32_t qk = 0, pv = 0, tq = 0, qi = 0, qbase = 0;
-            bool have_q = false, ok = true;
-            uint64_t t_last = globaltimer_ns();
-            for (uint32_t it = 1; pv < total && ok; ++it) {
-                bool progress = false;
-                if (qk < total && qk < pv + NB) {
-                    if (!have_q && mbar_test(&bars[F_QF + (qi & 1)], (qi >> 1) & 1)) {
-                        qbase = smem_u32(sm + L::kQ3Off + (qi & 1) * L::kQ3Bytes);
-                        ++qi;
-                        have_q = true;
-                    }
-                    if (have_q && mbar_test(&bars[F_FULL + qk % NS], (qk / NS) & 1)) {
-                        tc_fence_after();
-                        const uint32_t kbase = smem_u32(sm + (qk % NS) * L::kStageBytes);
-#pragma unroll
-                        for (int kk = 0; kk < 4; ++kk)  // 32 bytes of d per step; N = 48 = hi, mid, lo levels
-                            mma_f8_ss(tbase + L::s_col(qk % NB), sdesc_sw128(kbase + kk * 32, 16, 1024),
-                                      sdesc_sw128(qbase + kk * 32, 16, 1024), idesc_qk, kk > 0 ? 1u : 0u);
-                        mma_commit(&bars[F_SF + qk % NB]);
-                        ++qk;
-                        if (++tq == jq_tiles) {
-                            ++jq;
-                            tq = 0;
-                            have_q = false;
-                            skip_empty();
-                        }
-                        progress = true;
-                    }
-                }
-                if (pv < qk && mbar_test(&bars[F_PF + pv % NB], (pv / NB) & 1)) {
-                    tc_fence_after();
-                    const uint32_t vbase = smem_u32(sm + (pv % NS) * L::kStageBytes + 16384);
-                    const uint32_t pbase = smem_u32(sm + L::kPOff) + (pv % NB) * 32u;
-#pragma unroll
-                    for (int kk = 0; kk < 4; ++kk)  // 32 keys per step
-                        mma_f8_ss(tbase + L::o_col(pv % NB), sdesc_sw128(vbase + kk * 4096, 1024, 1024),
-                                  sdesc_sw128(pbase + kk * 4096, 1024, 1024), idesc_pv, kk > 0);
-                    mma_commit(&bars[F_OF + pv % NB]);
-                    mma_commit(&bars[F_EMPTY + pv % NS]);
-                    ++pv;
-                    progress = true;
-                }
-                if (progress) {
-                    t_last = globaltimer_ns();
-                } else if ((it & 31u) == 0 &&
-                           (*abort_sh != 0 || globaltimer_ns() - t_last > a.wait_ns || it >= (1u << 30))) {
-                    fail(a, abort_sh, PA_ERR_TIMEOUT);
+            bool ok = true;
+            for (uint32_t g = 0; g < total; ++g) {
+                // the stage's pages landed before QK(g) was issued; waiting on
+                // its barrier here as well makes them visible to this thread
+                if (!mbar_wait(&bars[F_PF + g % NB], (g / NB) & 1, abort_sh, a.wait_ns) ||
+                    !mbar_wait(&bars[F_FULL + g % NS], (g / NS) & 1, abort_sh, a.wait_ns)) {
                     ok = false;
+                    break;
                 }
+                tc_fence_after();
+                const uint32_t vbase = smem_u32(sm + (g % NS) * L::kStageBytes + 16384);
+                const uint32_t pbase = smem_u32(sm + L::kPOff) + (g % NB) * 32u;
+#pragma unroll
+                for (int kk = 0; kk < 4; ++kk)  // 32 keys per step
+                    mma_f8_ss(tbase + L::o_col(g % NB), sdesc_sw128(vbase + kk * 4096, 1024, 1024),
+                              sdesc_sw128(pbase + kk * 4096, 1024, 1024), idesc_pv, kk > 0);
+                mma_commit(&bars[F_OF + g % NB]);
+                mma_commit(&bars[F_EMPTY + g % NS]);
             }
-            mma_commit(&bars[F_DONE]);
-            mbar_wait(&bars[F_DONE], 0, nullptr, a.wait_ns);
+            if (!ok) fail(a, abort_sh, PA_ERR_TIMEOUT);
+            mma_commit(&bars[F_DONE2]);
+            mbar_wait(&bars[F_DONE2], 0, nullptr, a.wait_ns);
         }
     } else if (warp == L::kMergeWarp) {
         // ------------------------------------------------------------ split merge
