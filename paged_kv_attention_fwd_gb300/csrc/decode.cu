@@ -824,12 +824,17 @@ __global__ void __launch_bounds__(DecodeLayout<D, FP8>::kThreads, 1)
 // memory, which merges the two and writes.  Larger groups keep one warpgroup
 // (register budget).  Warps: 0 producer, 1 QK issuer, 2 .. 1 + 4 WG softmax,
 // then the split merge warp and the PV issuer.
+// K and V tiles (2 pages x 64 rows x 128 B each) have rings of their own: a
+// K slot is free again once its QK retired, well before the tile's softmax
+// and PV are done, so more of shared memory holds loads still in flight.
 template <int WG>
 struct F8Layout {
-    static constexpr int kStages = 5;
+    static constexpr int kKSlots = 4;
+    static constexpr int kVSlots = 7;
     static constexpr int kNB = 2 * WG;          // S, O and P buffers
-    static constexpr int kStageBytes = 32768;   // K: 2 pages x 64 rows x 128 B, then V the same
-    static constexpr int kQ3Off = kStages * kStageBytes;
+    static constexpr int kSlotBytes = 16384;
+    static constexpr int kVOff = kKSlots * kSlotBytes;
+    static constexpr int kQ3Off = kVOff + kVSlots * kSlotBytes;
     static constexpr int kQ3Bytes = 48 * 128;   // rows = level * 16 + head
     static constexpr int kPOff = kQ3Off + 2 * kQ3Bytes;
     // P, MN-major with 128-byte swizzle: row = key; buffer b takes bytes
@@ -854,22 +859,25 @@ struct F8Layout {
     __host__ __device__ static constexpr uint32_t s_col(uint32_t b) { return b * 64u; }
     __host__ __device__ static constexpr uint32_t o_col(uint32_t b) { return kNB * 64u + b * 32u; }
     static_assert(kQ3Off % 1024 == 0 && kPOff % 1024 == 0, "swizzle atoms need 1024-byte alignment");
-    static_assert(kSmem <= 232448, "shared memory per CTA");
+    static_assert(kSmem <= 232448 - 4096, "shared memory per CTA (dynamic + static)");
+    static_assert(kKSlots <= 8 && kVSlots <= 8, "barrier slots");
     static_assert(o_col(kNB - 1) + 32 <= kTmemCols, "TMEM columns");
 };
 
 enum : int {
-    F_FULL = 0,    // [5] stage filled
-    F_EMPTY = 5,   // [5] stage free again
-    F_QF = 10,     // [2] query levels written
-    F_SF = 12,     // [4] S tile in TMEM
-    F_PF = 16,     // [4] P written
-    F_OF = 20,     // [4] O tile in TMEM
-    F_DONE = 24,   // all QK MMAs retired (teardown)
-    F_PW = 25,     // [2] an item's partials written (merge warp)
-    F_HD = 27,     // [2] merge warp done with an item
-    F_DONE2 = 29,  // all PV MMAs retired (teardown)
-    F_COUNT = 30
+    F_KFULL = 0,    // [8] K slot filled
+    F_KEMPTY = 8,   // [8] K slot free again (its QK retired)
+    F_VFULL = 16,   // [8] V slot filled
+    F_VEMPTY = 24,  // [8] V slot free again (its PV retired)
+    F_QF = 32,      // [2] query levels written
+    F_SF = 34,      // [4] S tile in TMEM
+    F_PF = 38,      // [4] P written
+    F_OF = 42,      // [4] O tile in TMEM
+    F_DONE = 46,    // all QK MMAs retired (teardown)
+    F_PW = 47,      // [2] an item's partials written (merge warp)
+    F_HD = 49,      // [2] merge warp done with an item
+    F_DONE2 = 51,   // all PV MMAs retired (teardown)
+    F_COUNT = 52
 };
 
 __device__ __forceinline__ uint32_t e4m3x2(float lo, float hi) {
@@ -890,7 +898,7 @@ __global__ void __launch_bounds__(F8Layout<WG>::kThreads, 1)
     using L = F8Layout<WG>;
     static_assert(WG == 1 || NP <= 8, "the hand-over buffer holds 8 heads");
     constexpr int D = 128;
-    constexpr int NB = L::kNB, NS = L::kStages;
+    constexpr int NB = L::kNB, NK = L::kKSlots, NV = L::kVSlots;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     __shared__ __align__(8) uint64_t bars[F_COUNT];
@@ -909,9 +917,13 @@ __global__ void __launch_bounds__(F8Layout<WG>::kThreads, 1)
         it_hi = __ldg(&meta[kMetaHeader + 2 * B + 1 + blockIdx.x + 1]);
     }
     if (threadIdx.x == 0) {
-        for (int s = 0; s < NS; ++s) {
-            mbar_init(&bars[F_FULL + s], 1);
-            mbar_init(&bars[F_EMPTY + s], 1);
+        for (int s = 0; s < NK; ++s) {
+            mbar_init(&bars[F_KFULL + s], 1);
+            mbar_init(&bars[F_KEMPTY + s], 1);
+        }
+        for (int s = 0; s < NV; ++s) {
+            mbar_init(&bars[F_VFULL + s], 1);
+            mbar_init(&bars[F_VEMPTY + s], 1);
         }
         for (int i = 0; i < NB; ++i) {
             mbar_init(&bars[F_SF + i], 1);
@@ -941,26 +953,18 @@ __global__ void __launch_bounds__(F8Layout<WG>::kThreads, 1)
     if (warp == 0) {
         // ------------------------------------------------------------ producer
         if (lane == 0) {
-            uint32_t g = 0;
-            uint32_t last_par[NS] = {};
-            bool issued[NS] = {};
+            uint32_t g = 0, issued[2] = {0u, 0u};  // tiles whose K / V copies were issued
             bool ok = true;
             for (int j = it_lo; j < it_hi && ok; ++j) {
                 const Item it = get_item(items_sh, a, j, it_lo, items_off);
                 const int ntiles = item_tiles(it);
                 const long long bt_row = (long long)it.b * a.max_pages;
                 for (int t = 0; t < ntiles; ++t, ++g) {
-                    const int stage = g % NS;
                     const int pa0 = it.p0 + 2 * t;
                     const int npg = min(2, it.p1 - pa0);
                     int pid[2];
                     pid[0] = __ldg(&a.block_table[bt_row + pa0]);
                     pid[1] = npg > 1 ? __ldg(&a.block_table[bt_row + pa0 + 1]) : 0;
-                    if (!mbar_wait(&bars[F_EMPTY + stage], ((g / NS) & 1) ^ 1, abort_sh, a.wait_ns)) {
-                        fail(a, abort_sh, PA_ERR_TIMEOUT);
-                        ok = false;
-                        break;
-                    }
                     bool valid[2];
                     uint32_t nvalid = 0;
                     for (int i = 0; i < 2; ++i) {
@@ -968,21 +972,40 @@ __global__ void __launch_bounds__(F8Layout<WG>::kThreads, 1)
                         if (i < npg && !valid[i]) record(a.status, PA_ERR_DEVICE_BOUNDS);
                         nvalid += valid[i];
                     }
-                    uint64_t* full = &bars[F_FULL + stage];
-                    mbar_arrive_expect_tx(full, nvalid * 2u * 8192u);
-                    uint8_t* st = sm + stage * L::kStageBytes;
-                    for (int i = 0; i < 2; ++i) {
-                        if (!valid[i]) continue;
-                        const int row = (int)(((long long)pid[i] * a.num_kv_heads + it.kvh) * 64);
-                        tma_load_2d(st + i * 8192, &map_k, full, 0, row);
-                        tma_load_2d(st + 16384 + i * 8192, &map_v, full, 0, row);
+                    int row[2];
+                    for (int i = 0; i < 2; ++i) row[i] = (int)(((long long)pid[i] * a.num_kv_heads + it.kvh) * 64);
+                    // K, then V, each into the next slot of its ring
+#pragma unroll
+                    for (int kv = 0; kv < 2 && ok; ++kv) {
+                        const int ns = kv == 0 ? NK : NV;
+                        const int slot = g % ns;
+                        uint64_t* empty = &bars[(kv == 0 ? F_KEMPTY : F_VEMPTY) + slot];
+                        uint64_t* full = &bars[(kv == 0 ? F_KFULL : F_VFULL) + slot];
+                        if (!mbar_wait(empty, ((g / ns) & 1) ^ 1, abort_sh, a.wait_ns)) {
+                            fail(a, abort_sh, PA_ERR_TIMEOUT);
+                            ok = false;
+                            break;
+                        }
+                        mbar_arrive_expect_tx(full, nvalid * 8192u);
+                        uint8_t* dst = sm + (kv == 0 ? 0 : L::kVOff) + slot * L::kSlotBytes;
+                        for (int i = 0; i < 2; ++i)
+                            if (valid[i]) tma_load_2d(dst + i * 8192, kv == 0 ? &map_k : &map_v, full, 0, row[i]);
+                        issued[kv] = g + 1;
                     }
-                    last_par[stage] = (g / NS) & 1;
-                    issued[stage] = true;
+                    if (!ok) break;
                 }
             }
-            for (int s = 0; s < NS; ++s)
-                if (issued[s]) mbar_wait(&bars[F_FULL + s], last_par[s], nullptr, a.wait_ns);
+            // wait for the copies still in flight: with n tiles issued, slot
+            // s last took tile n - 1 - ((n - 1 - s) mod slots), if s < n
+            for (int kv = 0; kv < 2; ++kv) {
+                const int ns = kv == 0 ? NK : NV;
+                const uint32_t n = issued[kv];
+                for (int s2 = 0; s2 < ns; ++s2) {
+                    if ((uint32_t)s2 >= n) continue;
+                    const uint32_t last = n - 1 - ((n - 1 - s2) % ns);
+                    mbar_wait(&bars[(kv == 0 ? F_KFULL : F_VFULL) + s2], (last / ns) & 1, nullptr, a.wait_ns);
+                }
+            }
         }
     } else if (warp == 1) {
         // ------------------------------------------------------------ QK issuer
@@ -1012,17 +1035,18 @@ __global__ void __launch_bounds__(F8Layout<WG>::kThreads, 1)
                         ok = false;
                         break;
                     }
-                    if (!mbar_wait(&bars[F_FULL + g % NS], (g / NS) & 1, abort_sh, a.wait_ns)) {
+                    if (!mbar_wait(&bars[F_KFULL + g % NK], (g / NK) & 1, abort_sh, a.wait_ns)) {
                         ok = false;
                         break;
                     }
                     tc_fence_after();
-                    const uint32_t kbase = smem_u32(sm + (g % NS) * L::kStageBytes);
+                    const uint32_t kbase = smem_u32(sm + (g % NK) * L::kSlotBytes);
 #pragma unroll
                     for (int kk = 0; kk < 4; ++kk)  // 32 bytes of d per step; N = 48 = hi, mid, lo levels
                         mma_f8_ss(tbase + L::s_col(g % NB), sdesc_sw128(kbase + kk * 32, 16, 1024),
                                   sdesc_sw128(qbase + kk * 32, 16, 1024), idesc_qk, kk > 0 ? 1u : 0u);
                     mma_commit(&bars[F_SF + g % NB]);
+                    mma_commit(&bars[F_KEMPTY + g % NK]);
                 }
             }
             if (!ok) fail(a, abort_sh, PA_ERR_TIMEOUT);
@@ -1032,29 +1056,27 @@ __global__ void __launch_bounds__(F8Layout<WG>::kThreads, 1)
     } else if (warp == L::kPvWarp) {
         // ------------------------------------------------------------ PV issuer
         // PV(g) once P(g) is written; its completion hands O(g) to the fold
-        // and releases ring stage g % NS.
+        // and releases V slot g % NV.
         if (lane == 0) {
             constexpr uint32_t idesc_pv = idesc_e4m3(128, 32, true, true);
             uint32_t total = 0;
             for (int j = it_lo; j < it_hi; ++j) total += (uint32_t)item_tiles(get_item(items_sh, a, j, it_lo, items_off));
             bool ok = true;
             for (uint32_t g = 0; g < total; ++g) {
-                // the stage's pages landed before QK(g) was issued; waiting on
-                // its barrier here as well makes them visible to this thread
                 if (!mbar_wait(&bars[F_PF + g % NB], (g / NB) & 1, abort_sh, a.wait_ns) ||
-                    !mbar_wait(&bars[F_FULL + g % NS], (g / NS) & 1, abort_sh, a.wait_ns)) {
+                    !mbar_wait(&bars[F_VFULL + g % NV], (g / NV) & 1, abort_sh, a.wait_ns)) {
                     ok = false;
                     break;
                 }
                 tc_fence_after();
-                const uint32_t vbase = smem_u32(sm + (g % NS) * L::kStageBytes + 16384);
+                const uint32_t vbase = smem_u32(sm + L::kVOff + (g % NV) * L::kSlotBytes);
                 const uint32_t pbase = smem_u32(sm + L::kPOff) + (g % NB) * 32u;
 #pragma unroll
                 for (int kk = 0; kk < 4; ++kk)  // 32 keys per step
                     mma_f8_ss(tbase + L::o_col(g % NB), sdesc_sw128(vbase + kk * 4096, 1024, 1024),
                               sdesc_sw128(pbase + kk * 4096, 1024, 1024), idesc_pv, kk > 0);
                 mma_commit(&bars[F_OF + g % NB]);
-                mma_commit(&bars[F_EMPTY + g % NS]);
+                mma_commit(&bars[F_VEMPTY + g % NV]);
             }
             if (!ok) fail(a, abort_sh, PA_ERR_TIMEOUT);
             mma_commit(&bars[F_DONE2]);
@@ -1268,9 +1290,9 @@ __global__ void __launch_bounds__(F8Layout<WG>::kThreads, 1)
                 *reinterpret_cast<uint4*>(pb + (((c0 + 1) ^ (row & 7)) << 4)) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
                 if (!valid) {
                     // a dead key's V row may hold anything (NaN included): zero it
-                    const int stage = g % NS;
-                    mbar_wait(&bars[F_FULL + stage], (g / NS) & 1, abort_sh, a.wait_ns);
-                    uint8_t* vr = sm + stage * L::kStageBytes + 16384 + (row >> 6) * 8192 + (row & 63) * 128;
+                    const int slot = g % NV;
+                    mbar_wait(&bars[F_VFULL + slot], (g / NV) & 1, abort_sh, a.wait_ns);
+                    uint8_t* vr = sm + L::kVOff + slot * L::kSlotBytes + (row >> 6) * 8192 + (row & 63) * 128;
 #pragma unroll
                     for (int i = 0; i < 8; ++i) *reinterpret_cast<uint4*>(vr + i * 16) = make_uint4(0, 0, 0, 0);
                 }
