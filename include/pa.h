@@ -246,7 +246,7 @@ typedef struct {
     int32_t page_size;         /* 64 when block_table is given */
     int32_t max_pages_per_seq; /* block_table row stride (paged) */
     int32_t num_pool_pages;    /* pages in the pools (paged) */
-    int32_t num_sms;
+    int32_t num_sms;           /* informational: the prefill launch queries the current device */
     int32_t dtype;             /* PA_KV_BF16 or PA_KV_FP16: q, k, v, k_rope and out */
 } pa_prefill_shapes;
 
@@ -269,10 +269,16 @@ typedef struct {
  *                _normalize_qo_offset / _resolve_seqused_k)
  *   out          bf16 [total_q, Hq, head_dim_v];  lse fp32 [total_q, Hq] or NULL
  *   workspace    >= PA_STATUS_BYTES device bytes (status word), zero-filled once.
- *                With pa_prefill_workspace_size(shapes) bytes the call also
- *                orders its CTAs longest first (a small sorting kernel writes
- *                the order after the status word); with less it uses a fixed
- *                order.  Results are identical either way.
+ *                The status region also holds the work counters of the
+ *                persistent kernel (int32 at bytes 64 and 128): one CTA per SM
+ *                takes (256-row query block, head) items from them, and the
+ *                last CTA to finish sets them back to zero, so they need no
+ *                clearing between calls.  With pa_prefill_workspace_size(shapes)
+ *                bytes the call also orders the items longest first (a small
+ *                sorting kernel writes the order after the status region);
+ *                with less it uses a fixed order.  Results are identical
+ *                either way.  Calls that share a workspace must not overlap
+ *                in time (one stream).
  */
 pa_status pa_prefill(const pa_prefill_shapes* shapes, const void* q, const void* k, const void* v,
                      const void* k_rope, const int32_t* cu_seqlens_q, const int32_t* cu_seqlens_k,

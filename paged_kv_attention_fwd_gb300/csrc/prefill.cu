@@ -40,19 +40,26 @@ constexpr float kLn2f = 0.69314718055994531f;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units
 
 enum : int {
-    P_QF = 0,
+    P_QF = 0,   // the item's query tiles landed
     P_KF = 1,   // [2]
     P_KE = 3,   // [2]
     P_VF = 5,   // [2]
     P_VE = 7,   // [2]
-    P_VZ = 9,   // dead V rows of the last tile zeroed
+    P_QE = 9,   // query buffers free again (the item's last QK retired)
     P_SF = 10,  // [2] S_A, S_B ready
     P_PF = 12,  // [2] P_A, P_B written
     P_OD = 14,  // [2] PV_A, PV_B retired
     P_DONE = 16,
     P_QS = 17,  // [2] e4m3 MLA: query tile A / B rope part rescaled
-    P_COUNT = 19
+    P_IF = 19,  // [2] item slot published
+    P_IE = 21,  // [2] item slot read by every consumer
+    P_COUNT = 23
 };
+
+// work counters of the persistent prefill, int32 words of the status region
+// (bytes 64 and 128 of the workspace): next work item, CTAs finished
+constexpr int kPrefillNextWord = 16;
+constexpr int kPrefillDoneWord = 32;
 
 // F8 (MLA only): a key row is 128 e4m3 bytes (the per-head part) then 64 bf16
 // (the rope part); a query row the same plus a third chunk: its rope part,
@@ -74,7 +81,7 @@ struct PrefillLayout {
     static constexpr int kVOff = kKOff + kNK * kKBytes;
     static constexpr int kBytes = kVOff + kNV * kVBytes;
     static constexpr int kSmem = kBytes + 1024;
-    static_assert(kSmem + 256 <= 232448, "shared memory per CTA (dynamic + static)");
+    static_assert(kSmem + 512 <= 232448, "shared memory per CTA (dynamic + static)");
     static constexpr int kThreads = 320;
 };
 
@@ -120,6 +127,47 @@ __device__ __forceinline__ int kv_tiles_for(const Seg& s, int r0, int r1, bool c
     return (int)((lim + 127) / 128);
 }
 
+// One work item as the producer publishes it to the other roles: a 256-row
+// query block of one segment and one query head; valid == 0 ends the loop.
+struct PItem {
+    int valid, b, h, rA, nA, nB;
+    Seg sg;
+};
+
+// Work index -> item.  Heads come in groups of hg (up to 32); within a group
+// the unit rank is the slow index and the head the fast one.  With an order
+// from prefill_order_kernel the units come sequence by sequence, longest
+// first, so the items in flight together share one sequence's K/V tiles in L2
+// across a group of heads.  Returns false for an idle unit (its rows lie past
+// the segment).
+__device__ __forceinline__ bool make_item(const PrefillArgs& a, int w, PItem& it) {
+    const int units = a.num_q_tiles * a.batch;
+    const int hg = a.num_q_heads < 32 ? a.num_q_heads : 32;
+    const int group = w / (hg * units);
+    const int in_group = w % (hg * units);
+    const int hg_here = min(hg, a.num_q_heads - group * hg);  // the last group may be narrower
+    const int rank = in_group / hg_here;
+    const int unit = a.order ? __ldg(&a.order[rank]) : -1;
+    const int b = unit >= 0 ? unit % a.batch : rank % a.batch;
+    const int pair = unit >= 0 ? unit / a.batch : a.num_q_tiles - 1 - rank / a.batch;
+    const Seg sg = load_seg(a, b);
+    const int rA = pair * 256;  // first query row of tile A within the segment
+    if (rA >= sg.q_len) return false;
+    const bool causal = a.causal != 0;
+    it.valid = 1;
+    it.b = b;
+    it.h = group * hg + in_group % hg_here;
+    it.rA = rA;
+    it.sg = sg;
+    it.nA = kv_tiles_for(sg, rA, min(rA + 128, sg.q_len), causal);
+    it.nB = rA + 128 < sg.q_len ? kv_tiles_for(sg, rA + 128, min(rA + 256, sg.q_len), causal) : 0;
+    return true;
+}
+
+// Persistent: one CTA per SM takes work items from a counter in the status
+// region until none is left.  Every barrier's phase runs on across items,
+// so the producer loads the next item's query and first K/V tiles while the
+// current item's last tiles and output are still in progress.
 template <bool ROPE, bool PAGED, bool F8>
 __global__ void __launch_bounds__(320, 1)
     prefill_kernel(const __grid_constant__ PrefillArgs a, const __grid_constant__ CUtensorMap map_q,
@@ -132,37 +180,17 @@ __global__ void __launch_bounds__(320, 1)
     __shared__ __align__(8) uint64_t bars[P_COUNT];
     __shared__ uint32_t tmem_base_sh;
     __shared__ int abort_store;
+    __shared__ PItem item_q[2];
     volatile int* abort_sh = &abort_store;
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    // CTA index -> (unit rank, head): heads come in groups of hg (up to 32);
-    // within a group the unit rank is the slow index and the head the fast one.
-    // With an order from prefill_order_kernel the units run sequence by
-    // sequence, longest first, so CTAs that run together share one sequence's
-    // K/V tiles in L2 across a group of heads.
-    const int units = a.num_q_tiles * a.batch;
-    const int hg = a.num_q_heads < 32 ? a.num_q_heads : 32;
-    const int group = (int)(blockIdx.x / (unsigned)(hg * units));
-    const int in_group = (int)(blockIdx.x % (unsigned)(hg * units));
-    const int hg_here = min(hg, a.num_q_heads - group * hg);  // the last group may be narrower
-    const int rank = in_group / hg_here;
-    const int h = group * hg + in_group % hg_here;
-    const int unit = a.order ? __ldg(&a.order[rank]) : -1;
-    const int b = unit >= 0 ? unit % a.batch : rank % a.batch;
-    const int pair = unit >= 0 ? unit / a.batch : a.num_q_tiles - 1 - rank / a.batch;
-    const int kvh = h / a.group;
-    const Seg sg = load_seg(a, b);
-    const int rA = pair * 256;  // first query row of tile A within the segment
-    if (rA >= sg.q_len) return;  // whole CTA idle (uniform, before any setup)
-    const bool has_b = rA + 128 < sg.q_len;
-    const bool causal = a.causal != 0;
-    const int nA = kv_tiles_for(sg, rA, min(rA + 128, sg.q_len), causal);
-    const int nB = has_b ? kv_tiles_for(sg, rA + 128, min(rA + 256, sg.q_len), causal) : 0;
-    const int nkv = max(nA, nB);
-    const bool zero_tail = nkv > 0 && nkv * 128 > sg.kv_len;  // dead keys in the last tile
+    const int W = a.num_q_tiles * a.batch * a.num_q_heads;  // work items
+    int* next_item = a.status + kPrefillNextWord;
+    int* ctas_done = a.status + kPrefillDoneWord;
 
     if (threadIdx.x == 0) {
         mbar_init(&bars[P_QF], 1);
+        mbar_init(&bars[P_QE], 1);
         for (int i = 0; i < 2; ++i) {
             mbar_init(&bars[P_KF + i], 1);
             mbar_init(&bars[P_KE + i], 1);
@@ -171,11 +199,11 @@ __global__ void __launch_bounds__(320, 1)
             mbar_init(&bars[P_SF + i], 1);
             mbar_init(&bars[P_PF + i], 128);
             mbar_init(&bars[P_OD + i], 1);
+            mbar_init(&bars[P_QS + i], 128);
+            mbar_init(&bars[P_IF + i], 1);
+            mbar_init(&bars[P_IE + i], 9);  // the MMA thread and one lane of each softmax warp
         }
-        mbar_init(&bars[P_VZ], 1);
         mbar_init(&bars[P_DONE], 1);
-        mbar_init(&bars[P_QS + 0], 128);
-        mbar_init(&bars[P_QS + 1], 128);
         *abort_sh = 0;
         fence_barrier_init();
     }
@@ -195,118 +223,131 @@ __global__ void __launch_bounds__(320, 1)
         // ---------------------------------------------------------------- producer
         if (lane == 0) {
             bool ok = true;
-            bool kiss[2] = {false, false}, viss[2] = {false, false};
-            uint32_t kpar[2] = {0, 0}, vpar[2] = {0, 0};
-            const int ntq = has_b ? 2 : 1;
-            mbar_arrive_expect_tx(&bars[P_QF], ntq * (F8 ? 2 * L::kTile : L::kQBytes));
-            for (int x = 0; x < ntq; ++x) {
-                uint8_t* qt = sm + L::kQOff + x * L::kQBytes;
-                if constexpr (F8) {
-                    tma_load_3d(qt, &map_q, &bars[P_QF], 0, h, sg.q0 + rA + x * 128);             // q_nope e4m3
-                    tma_load_3d(qt + L::kTile, &map_qr, &bars[P_QF], 0, h, sg.q0 + rA + x * 128);  // q_rope bf16
-                } else {
-                    for (int c = 0; c < L::kQChunks; ++c)
-                        tma_load_3d(qt + c * L::kTile, &map_q, &bars[P_QF], c * 64, h, sg.q0 + rA + x * 128);
+            uint32_t k = 0;                          // items published
+            uint32_t gt = 0;                         // K/V tiles of the items before this one
+            uint32_t q_loads = 0, k_loads = 0, v_loads = 0;  // copies issued, for the drain
+            for (;;) {
+                PItem it;
+                it.valid = 0;
+                for (;;) {  // the next item that has rows
+                    const int w = atomicAdd(next_item, 1);
+                    if (w >= W) break;
+                    if (make_item(a, w, it)) break;
                 }
-            }
-            const int kv_pages = (sg.kv_len + kPage - 1) / kPage;
-            for (int j = 0; j < nkv && ok; ++j) {
-                // page ids of this tile (paged keys)
-                int pid[2] = {-1, -1};
-                if (PAGED) {
-                    for (int i = 0; i < 2; ++i) {
-                        const int p = 2 * j + i;
-                        if (p < kv_pages && p < a.max_pages) {
-                            const int id = __ldg(&a.block_table[(long long)b * a.max_pages + p]);
-                            if ((unsigned)id < (unsigned)a.num_pool_pages) pid[i] = id;
-                            else atomicCAS(a.status, 0, PA_ERR_DEVICE_BOUNDS);
-                        } else if (p < kv_pages) {
-                            atomicCAS(a.status, 0, PA_ERR_DEVICE_BOUNDS);
-                        }
+                // slot k & 1 is free once every consumer has read item k - 2
+                if (!mbar_wait(&bars[P_IE + (k & 1)], ((k >> 1) & 1) ^ 1, abort_sh, a.wait_ns)) {
+                    ok = false;
+                    break;
+                }
+                item_q[k & 1] = it;
+                mbar_arrive(&bars[P_IF + (k & 1)]);  // release: the consumers' wait sees the item
+                if (!it.valid) break;
+                const Seg& sg = it.sg;
+                const int h = it.h, kvh = h / a.group;
+                const int nkv = max(it.nA, it.nB);
+                const int ntq = it.rA + 128 < sg.q_len ? 2 : 1;
+                // query tiles, once the previous item's last QK retired
+                if (k > 0 && !mbar_wait(&bars[P_QE], (k - 1) & 1, abort_sh, a.wait_ns)) {
+                    ok = false;
+                    break;
+                }
+                mbar_arrive_expect_tx(&bars[P_QF], ntq * (F8 ? 2 * L::kTile : L::kQBytes));
+                for (int x = 0; x < ntq; ++x) {
+                    uint8_t* qt = sm + L::kQOff + x * L::kQBytes;
+                    if constexpr (F8) {
+                        tma_load_3d(qt, &map_q, &bars[P_QF], 0, h, sg.q0 + it.rA + x * 128);             // q_nope e4m3
+                        tma_load_3d(qt + L::kTile, &map_qr, &bars[P_QF], 0, h, sg.q0 + it.rA + x * 128);  // q_rope bf16
+                    } else {
+                        for (int c = 0; c < L::kQChunks; ++c)
+                            tma_load_3d(qt + c * L::kTile, &map_q, &bars[P_QF], c * 64, h, sg.q0 + it.rA + x * 128);
                     }
                 }
-                const int npid = (pid[0] >= 0) + (pid[1] >= 0);
-                // K tile
-                const int ks = j % L::kNK;
-                if (!mbar_wait(&bars[P_KE + ks], ((j / L::kNK) & 1) ^ 1, abort_sh, a.wait_ns)) {
-                    ok = false;
-                    break;
+                q_loads = k + 1;
+                const int kv_pages = (sg.kv_len + kPage - 1) / kPage;
+                for (int j = 0; j < nkv && ok; ++j) {
+                    const uint32_t g = gt + j;
+                    // page ids of this tile (paged keys)
+                    int pid[2] = {-1, -1};
+                    if (PAGED) {
+                        for (int i = 0; i < 2; ++i) {
+                            const int p = 2 * j + i;
+                            if (p < kv_pages && p < a.max_pages) {
+                                const int id = __ldg(&a.block_table[(long long)it.b * a.max_pages + p]);
+                                if ((unsigned)id < (unsigned)a.num_pool_pages) pid[i] = id;
+                                else atomicCAS(a.status, 0, PA_ERR_DEVICE_BOUNDS);
+                            } else if (p < kv_pages) {
+                                atomicCAS(a.status, 0, PA_ERR_DEVICE_BOUNDS);
+                            }
+                        }
+                    }
+                    const int npid = (pid[0] >= 0) + (pid[1] >= 0);
+                    // K tile
+                    const int ks = g % L::kNK;
+                    if (!mbar_wait(&bars[P_KE + ks], ((g / L::kNK) & 1) ^ 1, abort_sh, a.wait_ns)) {
+                        ok = false;
+                        break;
+                    }
+                    uint64_t* kf = &bars[P_KF + ks];
+                    uint8_t* kt = sm + L::kKOff + ks * L::kKBytes;
+                    if (PAGED) {
+                        mbar_arrive_expect_tx(kf, npid * 2 * 8192);
+                        for (int i = 0; i < 2; ++i)
+                            if (pid[i] >= 0)
+                                for (int c = 0; c < 2; ++c)
+                                    tma_load_2d(kt + c * L::kTile + i * 8192, &map_k, kf, c * 64,
+                                                (int)(((long long)pid[i] * a.num_kv_heads + kvh) * 64));
+                    } else if constexpr (F8) {
+                        mbar_arrive_expect_tx(kf, L::kKBytes);
+                        tma_load_3d(kt, &map_k, kf, 0, kvh, sg.k0 + j * 128);           // k_nope e4m3
+                        tma_load_2d(kt + L::kTile, &map_r, kf, 0, sg.k0 + j * 128);    // k_rope bf16
+                    } else {
+                        mbar_arrive_expect_tx(kf, L::kKBytes);
+                        for (int c = 0; c < 2; ++c)
+                            tma_load_3d(kt + c * L::kTile, &map_k, kf, c * 64, kvh, sg.k0 + j * 128);
+                        if (ROPE) tma_load_2d(kt + 2 * L::kTile, &map_r, kf, 0, sg.k0 + j * 128);
+                    }
+                    k_loads = g + 1;
+                    // V tile
+                    const int vs = g % L::kNV;
+                    if (!mbar_wait(&bars[P_VE + vs], ((g / L::kNV) & 1) ^ 1, abort_sh, a.wait_ns)) {
+                        ok = false;
+                        break;
+                    }
+                    uint64_t* vf = &bars[P_VF + vs];
+                    uint8_t* vt = sm + L::kVOff + vs * L::kVBytes;
+                    if (PAGED) {
+                        mbar_arrive_expect_tx(vf, npid * 2 * 8192);
+                        for (int i = 0; i < 2; ++i)
+                            if (pid[i] >= 0)
+                                for (int c = 0; c < 2; ++c)
+                                    tma_load_2d(vt + c * L::kTile + i * 8192, &map_v, vf, c * 64,
+                                                (int)(((long long)pid[i] * a.num_kv_heads + kvh) * 64));
+                    } else {
+                        mbar_arrive_expect_tx(vf, L::kVBytes);
+                        for (int c = 0; c < 2; ++c)
+                            tma_load_3d(vt + c * L::kTile, &map_v, vf, c * 64, kvh, sg.k0 + j * 128);
+                    }
+                    v_loads = g + 1;
                 }
-                uint64_t* kf = &bars[P_KF + ks];
-                uint8_t* kt = sm + L::kKOff + ks * L::kKBytes;
-                if (PAGED) {
-                    mbar_arrive_expect_tx(kf, npid * 2 * 8192);
-                    for (int i = 0; i < 2; ++i)
-                        if (pid[i] >= 0)
-                            for (int c = 0; c < 2; ++c)
-                                tma_load_2d(kt + c * L::kTile + i * 8192, &map_k, kf, c * 64,
-                                            (int)(((long long)pid[i] * a.num_kv_heads + kvh) * 64));
-                } else if constexpr (F8) {
-                    mbar_arrive_expect_tx(kf, L::kKBytes);
-                    tma_load_3d(kt, &map_k, kf, 0, kvh, sg.k0 + j * 128);           // k_nope e4m3
-                    tma_load_2d(kt + L::kTile, &map_r, kf, 0, sg.k0 + j * 128);    // k_rope bf16
-                } else {
-                    mbar_arrive_expect_tx(kf, L::kKBytes);
-                    for (int c = 0; c < 2; ++c)
-                        tma_load_3d(kt + c * L::kTile, &map_k, kf, c * 64, kvh, sg.k0 + j * 128);
-                    if (ROPE) tma_load_2d(kt + 2 * L::kTile, &map_r, kf, 0, sg.k0 + j * 128);
-                }
-                kiss[ks] = true;
-                kpar[ks] = (j / L::kNK) & 1;
-                // V tile
-                const int vs = j % L::kNV;
-                if (!mbar_wait(&bars[P_VE + vs], ((j / L::kNV) & 1) ^ 1, abort_sh, a.wait_ns)) {
-                    ok = false;
-                    break;
-                }
-                uint64_t* vf = &bars[P_VF + vs];
-                uint8_t* vt = sm + L::kVOff + vs * L::kVBytes;
-                if (PAGED) {
-                    mbar_arrive_expect_tx(vf, npid * 2 * 8192);
-                    for (int i = 0; i < 2; ++i)
-                        if (pid[i] >= 0)
-                            for (int c = 0; c < 2; ++c)
-                                tma_load_2d(vt + c * L::kTile + i * 8192, &map_v, vf, c * 64,
-                                            (int)(((long long)pid[i] * a.num_kv_heads + kvh) * 64));
-                } else {
-                    mbar_arrive_expect_tx(vf, L::kVBytes);
-                    for (int c = 0; c < 2; ++c)
-                        tma_load_3d(vt + c * L::kTile, &map_v, vf, c * 64, kvh, sg.k0 + j * 128);
-                }
-                viss[vs] = true;
-                vpar[vs] = (j / L::kNV) & 1;
+                if (!ok) break;
+                gt += nkv;
+                ++k;
             }
             if (!ok) {
                 *abort_sh = 1;
                 atomicCAS(a.status, 0, PA_ERR_TIMEOUT);
             }
-            // every issued copy must land before the CTA may exit
-            mbar_wait(&bars[P_QF], 0, nullptr, a.wait_ns);
-            for (int i = 0; i < 2; ++i) {
-                if (kiss[i]) mbar_wait(&bars[P_KF + i], kpar[i], nullptr, a.wait_ns);
-                if (viss[i]) mbar_wait(&bars[P_VF + i], vpar[i], nullptr, a.wait_ns);
+            // every issued copy must land before the CTA may exit: with n
+            // tiles issued, ring slot s last took tile n - 1 - ((n - 1 - s) mod slots)
+            if (q_loads > 0) mbar_wait(&bars[P_QF], (q_loads - 1) & 1, nullptr, a.wait_ns);
+            for (uint32_t s = 0; s < (uint32_t)L::kNK && s < k_loads; ++s) {
+                const uint32_t last = k_loads - 1 - ((k_loads - 1 - s) % L::kNK);
+                mbar_wait(&bars[P_KF + s], (last / L::kNK) & 1, nullptr, a.wait_ns);
             }
-        }
-        __syncwarp();
-        // dead keys of the last tile: zero their V rows (they may hold anything,
-        // and 0 * NaN would poison the PV product)
-        const bool do_zero = __shfl_sync(0xffffffffu, (int)(zero_tail && !*abort_sh), 0) != 0;
-        if (do_zero) {
-            const int j = nkv - 1, vs = j % L::kNV;
-            bool ok = mbar_wait(&bars[P_VF + vs], (j / L::kNV) & 1, abort_sh, a.wait_ns);
-            ok = __all_sync(0xffffffffu, ok);
-            if (ok) {
-                const int first_dead = sg.kv_len - j * 128;  // 1 .. 127
-                uint8_t* vt = sm + L::kVOff + vs * L::kVBytes;
-                for (int idx = lane; idx < (128 - first_dead) * 16; idx += 32) {
-                    const int row = first_dead + idx / 16, q16 = idx % 16;  // 2 chunks x 8 16-byte pieces
-                    *reinterpret_cast<uint4*>(vt + (q16 >> 3) * L::kTile + row * 128 + (q16 & 7) * 16) =
-                        make_uint4(0, 0, 0, 0);
-                }
-                fence_proxy_async_smem();
+            for (uint32_t s = 0; s < (uint32_t)L::kNV && s < v_loads; ++s) {
+                const uint32_t last = v_loads - 1 - ((v_loads - 1 - s) % L::kNV);
+                mbar_wait(&bars[P_VF + s], (last / L::kNV) & 1, nullptr, a.wait_ns);
             }
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&bars[P_VZ]);
         }
     } else if (warp == 1) {
         // ---------------------------------------------------------------- MMA issuer
@@ -315,16 +356,9 @@ __global__ void __launch_bounds__(320, 1)
             const uint32_t idesc_pv = idesc_f16(128, 128, !a.f16, false, true);
             constexpr uint32_t idesc_qk8 = idesc_e4m3(128, 128, false, false);
             const uint32_t qa = smem_u32(sm + L::kQOff);
-            bool ok = mbar_wait(&bars[P_QF], 0, abort_sh, a.wait_ns);
-            if constexpr (F8) {
-                // the softmax threads divide the query's rope part by the head's scale first
-                const int nq[2] = {nA, nB};
-                for (int x = 0; x < 2 && ok; ++x)
-                    if (nq[x] > 0) ok = mbar_wait(&bars[P_QS + x], 0, abort_sh, a.wait_ns);
-            }
-            auto qk = [&](int x, int j) {
+            auto qk = [&](int x, int kslot) {
                 const uint32_t qb = qa + x * L::kQBytes;
-                const uint32_t kb = smem_u32(sm + L::kKOff + (j % L::kNK) * L::kKBytes);
+                const uint32_t kb = smem_u32(sm + L::kKOff + kslot * L::kKBytes);
                 if constexpr (F8) {
                     // per-head part on the e4m3 path (32 bytes of depth per MMA), then
                     // the rope part in bf16, hi and lo query levels against the same
@@ -349,54 +383,78 @@ __global__ void __launch_bounds__(320, 1)
                 }
                 mma_commit(&bars[P_SF + x]);
             };
-            auto pv = [&](int x, int j) {
-                const uint32_t vb = smem_u32(sm + L::kVOff + (j % L::kNV) * L::kVBytes);
+            auto pv = [&](int x, int vslot, bool first) {
+                const uint32_t vb = smem_u32(sm + L::kVOff + vslot * L::kVBytes);
 #pragma unroll
                 for (int kk = 0; kk < 8; ++kk)
                     mma_ts(tbase + o_col(x), tbase + s_col(x) + kk * 8, sdesc_sw128(vb + kk * 2048, 16384, 1024),
-                           idesc_pv, (j > 0 || kk > 0) ? 1u : 0u);
+                           idesc_pv, (!first || kk > 0) ? 1u : 0u);
                 mma_commit(&bars[P_OD + x]);
             };
-            const int n[2] = {nA, nB};
-            // prologue: S for tile 0 of both query tiles
-            if (ok && nkv > 0) {
-                ok = mbar_wait(&bars[P_KF], 0, abort_sh, a.wait_ns);
-                if (ok) {
-                    tc_fence_after();
-                    for (int x = 0; x < 2; ++x)
-                        if (n[x] > 0) qk(x, 0);
-                    mma_commit(&bars[P_KE]);
+            bool ok = true;
+            uint32_t k = 0, gt = 0, npv[2] = {0u, 0u}, nqs[2] = {0u, 0u};
+            for (;;) {
+                if (!mbar_wait(&bars[P_IF + (k & 1)], (k >> 1) & 1, abort_sh, a.wait_ns)) {
+                    ok = false;
+                    break;
                 }
-            }
-            for (int j = 0; j < nkv && ok; ++j) {
-                const int vs = j % L::kNV;
-                ok = mbar_wait(&bars[P_VF + vs], (j / L::kNV) & 1, abort_sh, a.wait_ns);
-                if (ok && zero_tail && j == nkv - 1) ok = mbar_wait(&bars[P_VZ], 0, abort_sh, a.wait_ns);
-                const bool next_k = j + 1 < nkv;
-                bool k_waited = false;
-                for (int x = 0; x < 2 && ok; ++x) {
-                    if (j >= n[x]) continue;
-                    ok = mbar_wait(&bars[P_PF + x], j & 1, abort_sh, a.wait_ns);
-                    if (!ok) break;
-                    tc_fence_after();
-                    pv(x, j);
-                    if (j + 1 < n[x]) {
-                        // P_x lives in S_x's columns.  MMAs issued by this thread
-                        // execute in issue order, so the next S_x written here
-                        // cannot overtake PV_x's read of P_x.
-                        if (!k_waited) {
-                            ok = mbar_wait(&bars[P_KF + (j + 1) % L::kNK], ((j + 1) / L::kNK) & 1, abort_sh,
-                                           a.wait_ns);
-                            k_waited = true;
-                            if (!ok) break;
-                            tc_fence_after();
-                        }
-                        qk(x, j + 1);
-                    }
+                const PItem it = item_q[k & 1];
+                mbar_arrive(&bars[P_IE + (k & 1)]);
+                if (!it.valid) break;
+                const bool has_b = it.rA + 128 < it.sg.q_len;
+                const int n[2] = {it.nA, it.nB};
+                const int nkv = max(n[0], n[1]);
+                ok = mbar_wait(&bars[P_QF], k & 1, abort_sh, a.wait_ns);
+                if constexpr (F8) {
+                    // the softmax threads divide the query's rope part by the head's scale first
+                    for (int x = 0; x < 2 && ok; ++x)
+                        if (x == 0 || has_b) ok = mbar_wait(&bars[P_QS + x], nqs[x]++ & 1, abort_sh, a.wait_ns);
                 }
                 if (!ok) break;
-                mma_commit(&bars[P_VE + vs]);
-                if (next_k) mma_commit(&bars[P_KE + (j + 1) % L::kNK]);
+                // S for tile 0 of both query tiles
+                if (nkv > 0) {
+                    ok = mbar_wait(&bars[P_KF + gt % L::kNK], (gt / L::kNK) & 1, abort_sh, a.wait_ns);
+                    if (!ok) break;
+                    tc_fence_after();
+                    for (int x = 0; x < 2; ++x)
+                        if (n[x] > 0) qk(x, gt % L::kNK);
+                    mma_commit(&bars[P_KE + gt % L::kNK]);
+                }
+                if (nkv <= 1) mma_commit(&bars[P_QE]);  // the item's last QK is issued
+                for (int j = 0; j < nkv && ok; ++j) {
+                    const uint32_t g = gt + j;
+                    const int vs = g % L::kNV;
+                    ok = mbar_wait(&bars[P_VF + vs], (g / L::kNV) & 1, abort_sh, a.wait_ns);
+                    bool k_waited = false;
+                    for (int x = 0; x < 2 && ok; ++x) {
+                        if (j >= n[x]) continue;
+                        ok = mbar_wait(&bars[P_PF + x], npv[x] & 1, abort_sh, a.wait_ns);
+                        if (!ok) break;
+                        tc_fence_after();
+                        pv(x, vs, j == 0);
+                        ++npv[x];
+                        if (j + 1 < n[x]) {
+                            // P_x lives in S_x's columns.  MMAs issued by this thread
+                            // execute in issue order, so the next S_x written here
+                            // cannot overtake PV_x's read of P_x.
+                            if (!k_waited) {
+                                ok = mbar_wait(&bars[P_KF + (g + 1) % L::kNK], ((g + 1) / L::kNK) & 1, abort_sh,
+                                               a.wait_ns);
+                                k_waited = true;
+                                if (!ok) break;
+                                tc_fence_after();
+                            }
+                            qk(x, (g + 1) % L::kNK);
+                        }
+                    }
+                    if (!ok) break;
+                    mma_commit(&bars[P_VE + vs]);
+                    if (j + 1 < nkv) mma_commit(&bars[P_KE + (g + 1) % L::kNK]);
+                    if (j + 2 == nkv) mma_commit(&bars[P_QE]);  // the item's last QK is issued
+                }
+                if (!ok) break;
+                gt += nkv;
+                ++k;
             }
             if (!ok) {
                 *abort_sh = 1;
@@ -410,26 +468,41 @@ __global__ void __launch_bounds__(320, 1)
         const int x = warp >= 6 ? 1 : 0;
         const int q4 = warp & 3;
         const int row = q4 * 32 + lane;           // query row within the tile = TMEM lane
-        const int i = rA + x * 128 + row;         // query row within the segment
-        const int nx = x ? nB : nA;
-        const bool active = x == 0 || has_b;
         const uint32_t lane_addr = (uint32_t)(q4 * 32) << 16;
-        float sl2 = a.scale_log2;
         const bool f16 = a.f16 != 0;
         bool ok = true;
-        if constexpr (F8) {
-            // score = scale * (s * <q_nope, k_nope> + <q_rope, k_rope>), s = q_scale[h] * k_scale[kvh]:
-            // the rope part of this thread's query row is divided by s and held as
-            // hi + lo bf16 levels (about 16 significant bits) so that both products
-            // add in one accumulator, and s joins the softmax scale
-            const float s = __ldg(&a.q_scale[h]) * __ldg(&a.k_scale[kvh]);
-            const float inv = 1.f / s;
-            if (!(s > 0.f) || !isfinite(s) || !isfinite(inv)) atomicCAS(a.status, 0, PA_ERR_INVALID_ARG);
-            sl2 *= s;
-            if (active) {
-                ok = mbar_wait(&bars[P_QF], 0, abort_sh, a.wait_ns);
-                ok = __all_sync(0xffffffffu, ok);
-                if (ok) {
+        uint32_t kit = 0, gt = 0, ns = 0;  // items, K/V tiles before this item, S tiles of this query tile
+        for (;;) {
+            ok = mbar_wait(&bars[P_IF + (kit & 1)], (kit >> 1) & 1, abort_sh, a.wait_ns);
+            ok = __all_sync(0xffffffffu, ok);
+            if (!ok) break;
+            const PItem it = item_q[kit & 1];
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&bars[P_IE + (kit & 1)]);
+            if (!it.valid) break;
+            const Seg& sg = it.sg;
+            const int h = it.h;
+            const int i = it.rA + x * 128 + row;  // query row within the segment
+            const int nx = x ? it.nB : it.nA;
+            const int nkv = max(it.nA, it.nB);
+            const bool active = x == 0 || it.rA + 128 < sg.q_len;
+            // the query tile that takes the item's last K/V tile first zeroes its dead
+            // V rows (they may hold anything, and 0 * NaN would poison the PV product)
+            const bool zeroer = active && nkv > 0 && nkv * 128 > sg.kv_len && x == (it.nA == nkv ? 0 : 1);
+            float sl2 = a.scale_log2;
+            if constexpr (F8) {
+                // score = scale * (s * <q_nope, k_nope> + <q_rope, k_rope>), s = q_scale[h] * k_scale[kvh]:
+                // the rope part of this thread's query row is divided by s and held as
+                // hi + lo bf16 levels (about 16 significant bits) so that both products
+                // add in one accumulator, and s joins the softmax scale
+                const float s = __ldg(&a.q_scale[h]) * __ldg(&a.k_scale[h / a.group]);
+                const float inv = 1.f / s;
+                if (!(s > 0.f) || !isfinite(s) || !isfinite(inv)) atomicCAS(a.status, 0, PA_ERR_INVALID_ARG);
+                sl2 *= s;
+                if (active) {
+                    ok = mbar_wait(&bars[P_QF], kit & 1, abort_sh, a.wait_ns);
+                    ok = __all_sync(0xffffffffu, ok);
+                    if (!ok) break;
                     // chunk 1 holds the row's 64 bf16 (TMA); chunks 1 and 2 share the
                     // swizzle pattern, so the lo level goes to the same offset in chunk 2
                     uint4* qh = reinterpret_cast<uint4*>(sm + L::kQOff + x * L::kQBytes + L::kTile + row * 128);
@@ -454,155 +527,179 @@ __global__ void __launch_bounds__(320, 1)
                     mbar_arrive(&bars[P_QS + x]);
                 }
             }
-        }
-        // keys this row may see: [0, lim)
-        long long lim = sg.kv_len;
-        if (causal) lim = min(lim, (long long)sg.off + i + 1);
-        if (lim < 0) lim = 0;
-        float m_run = -INFINITY, l_run = 0.f;
-        for (int j = 0; active && ok && j < nx; ++j) {
-            ok = mbar_wait(&bars[P_SF + x], j & 1, abort_sh, a.wait_ns);
-            ok = __all_sync(0xffffffffu, ok);
-            if (!ok) break;
-            tc_fence_after();
-            const int vis = (int)min(128LL, max(0LL, lim - (long long)j * 128));  // visible keys of this tile
-            // every key of the tile visible to every row of the warp, positive scale:
-            // no per-element masking, and the max can be taken on the raw scores
-            const bool full = __all_sync(0xffffffffu, vis >= 128) && sl2 > 0.f;
-            // pass 1: row max of the scaled, masked scores (S read from TMEM, 64 columns per wait)
-            float mt;
-            {
-                float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+            // keys this row may see: [0, lim)
+            long long lim = sg.kv_len;
+            if (a.causal) lim = min(lim, (long long)sg.off + i + 1);
+            if (lim < 0) lim = 0;
+            float m_run = -INFINITY, l_run = 0.f;
+            for (int j = 0; active && ok && j < nx; ++j) {
+                ok = mbar_wait(&bars[P_SF + x], ns & 1, abort_sh, a.wait_ns);
+                ok = __all_sync(0xffffffffu, ok);
+                if (!ok) break;
+                tc_fence_after();
+                const int vis = (int)min(128LL, max(0LL, lim - (long long)j * 128));  // visible keys of this tile
+                // every key of the tile visible to every row of the warp, positive scale:
+                // no per-element masking, and the max can be taken on the raw scores
+                const bool full = __all_sync(0xffffffffu, vis >= 128) && sl2 > 0.f;
+                // pass 1: row max of the scaled, masked scores (S read from TMEM, 64 columns per wait)
+                float mt;
+                {
+                    float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+#pragma unroll 1
+                    for (int hh = 0; hh < 2; ++hh) {
+                        uint32_t r[64];
+                        tmem_ld_x32(tbase + lane_addr + s_col(x) + hh * 64, *reinterpret_cast<uint32_t(*)[32]>(&r[0]));
+                        tmem_ld_x32(tbase + lane_addr + s_col(x) + hh * 64 + 32, *reinterpret_cast<uint32_t(*)[32]>(&r[32]));
+                        tmem_ld_wait();
+                        reg_fence(r);
+                        if (full) {
 #pragma unroll
+                            for (int k = 0; k < 64; k += 2)
+                                m4[(k >> 1) & 3] = fmax3(m4[(k >> 1) & 3], __uint_as_float(r[k]), __uint_as_float(r[k + 1]));
+                        } else {
+#pragma unroll
+                            for (int k = 0; k < 64; ++k)
+                                if (hh * 64 + k < vis) m4[k & 3] = fmaxf(m4[k & 3], __uint_as_float(r[k]) * sl2);
+                        }
+                    }
+                    mt = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
+                    if (full) mt *= sl2;
+                }
+                // conditional rescale: keep the stale max unless the new one is 2^8 larger
+                const bool grow = mt > m_run + kRescaleThreshold;
+                float m_new = grow ? mt : m_run;
+                const bool need_o = __any_sync(0xffffffffu, grow && j > 0 && m_run != -INFINITY);
+                if (need_o) {
+                    ok = mbar_wait(&bars[P_OD + x], (ns - 1) & 1, abort_sh, a.wait_ns);
+                    ok = __all_sync(0xffffffffu, ok);
+                    if (!ok) break;
+                    tc_fence_after();
+                    const float alpha = (grow && m_run != -INFINITY) ? ex2(m_run - m_new) : 1.f;
+#pragma unroll
+                    for (int c = 0; c < 4; ++c) {
+                        uint32_t o[32];
+                        tmem_ld_x32(tbase + lane_addr + o_col(x) + c * 32, o);
+                        tmem_ld_wait();
+                        reg_fence(o);
+#pragma unroll
+                        for (int k = 0; k < 32; ++k) o[k] = __float_as_uint(__uint_as_float(o[k]) * alpha);
+                        tmem_st_x32(tbase + lane_addr + o_col(x) + c * 32, o);
+                    }
+                    tmem_st_wait();
+                }
+                if (grow) {
+                    if (m_run != -INFINITY) l_run *= ex2(m_run - m_new);
+                    m_run = m_new;
+                }
+                const bool none = m_run == -INFINITY;
+                const bool fast = __all_sync(0xffffffffu, full && !none);
+                const float neg_m = -m_run;
+                float rs0 = 0.f, rs1 = 0.f;
+                // pass 2: P = exp2(x - m) in bf16, written over S columns already read
+                // (keys 64h..64h+63 -> P columns 32h..32h+31)
+#pragma unroll 1
                 for (int hh = 0; hh < 2; ++hh) {
-                    uint32_t r[64];
+                    uint32_t r[64], pw[32];
                     tmem_ld_x32(tbase + lane_addr + s_col(x) + hh * 64, *reinterpret_cast<uint32_t(*)[32]>(&r[0]));
                     tmem_ld_x32(tbase + lane_addr + s_col(x) + hh * 64 + 32, *reinterpret_cast<uint32_t(*)[32]>(&r[32]));
                     tmem_ld_wait();
                     reg_fence(r);
-                    if (full) {
+                    if (fast) {
+                        const uint64_t sc2 = f2_pack(__float_as_uint(sl2), __float_as_uint(sl2));
+                        const uint64_t nm2 = f2_pack(__float_as_uint(neg_m), __float_as_uint(neg_m));
+                        uint64_t acc2 = f2_pack(0u, 0u);
 #pragma unroll
-                        for (int k = 0; k < 64; k += 2)
-                            m4[(k >> 1) & 3] = fmax3(m4[(k >> 1) & 3], __uint_as_float(r[k]), __uint_as_float(r[k + 1]));
+                        for (int k = 0; k < 32; ++k) {
+                            float x0, x1;
+                            f2_unpack(f2_fma(f2_pack(r[2 * k], r[2 * k + 1]), sc2, nm2), x0, x1);
+                            const float p0 = ex2(x0), p1 = ex2(x1);
+                            acc2 = f2_add(acc2, f2_pack(__float_as_uint(p0), __float_as_uint(p1)));
+                            pw[k] = pack16x2(p0, p1, f16);
+                        }
+                        float a0, a1;
+                        f2_unpack(acc2, a0, a1);
+                        rs0 += a0;
+                        rs1 += a1;
                     } else {
 #pragma unroll
-                        for (int k = 0; k < 64; ++k)
-                            if (hh * 64 + k < vis) m4[k & 3] = fmaxf(m4[k & 3], __uint_as_float(r[k]) * sl2);
+                        for (int k = 0; k < 32; ++k) {
+                            const int key = hh * 64 + 2 * k;
+                            const float p0 = (none || key >= vis) ? 0.f : ex2(__uint_as_float(r[2 * k]) * sl2 - m_run);
+                            const float p1 = (none || key + 1 >= vis) ? 0.f : ex2(__uint_as_float(r[2 * k + 1]) * sl2 - m_run);
+                            rs0 += p0;
+                            rs1 += p1;
+                            pw[k] = pack16x2(p0, p1, f16);
+                        }
                     }
+                    tmem_st_x32(tbase + lane_addr + s_col(x) + hh * 32, pw);
                 }
-                mt = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
-                if (full) mt *= sl2;
-            }
-            // conditional rescale: keep the stale max unless the new one is 2^8 larger
-            const bool grow = mt > m_run + kRescaleThreshold;
-            float m_new = grow ? mt : m_run;
-            const bool need_o = __any_sync(0xffffffffu, grow && j > 0 && m_run != -INFINITY);
-            if (need_o) {
-                ok = mbar_wait(&bars[P_OD + x], (j - 1) & 1, abort_sh, a.wait_ns);
-                ok = __all_sync(0xffffffffu, ok);
-                if (!ok) break;
-                tc_fence_after();
-                const float alpha = (grow && m_run != -INFINITY) ? ex2(m_run - m_new) : 1.f;
+                const float rs = rs0 + rs1;
+                l_run += rs;
+                if (zeroer && j == nkv - 1) {
+                    const uint32_t g = gt + j;
+                    const int vs = g % L::kNV;
+                    ok = mbar_wait(&bars[P_VF + vs], (g / L::kNV) & 1, abort_sh, a.wait_ns);
+                    ok = __all_sync(0xffffffffu, ok);
+                    if (!ok) break;
+                    if (row >= sg.kv_len - j * 128) {  // this thread's row of the V tile is a dead key
+                        uint8_t* vr = sm + L::kVOff + vs * L::kVBytes + row * 128;
 #pragma unroll
-                for (int c = 0; c < 4; ++c) {
-                    uint32_t o[32];
-                    tmem_ld_x32(tbase + lane_addr + o_col(x) + c * 32, o);
-                    tmem_ld_wait();
-                    reg_fence(o);
+                        for (int c = 0; c < 2; ++c)
 #pragma unroll
-                    for (int k = 0; k < 32; ++k) o[k] = __float_as_uint(__uint_as_float(o[k]) * alpha);
-                    tmem_st_x32(tbase + lane_addr + o_col(x) + c * 32, o);
+                            for (int u = 0; u < 8; ++u)
+                                *reinterpret_cast<uint4*>(vr + c * L::kTile + u * 16) = make_uint4(0, 0, 0, 0);
+                    }
+                    fence_proxy_async_smem();
                 }
                 tmem_st_wait();
+                tc_fence_before();
+                mbar_arrive(&bars[P_PF + x]);
+                ++ns;
             }
-            if (grow) {
-                if (m_run != -INFINITY) l_run *= ex2(m_run - m_new);
-                m_run = m_new;
-            }
-            const bool none = m_run == -INFINITY;
-            const bool fast = __all_sync(0xffffffffu, full && !none);
-            const float neg_m = -m_run;
-            float rs0 = 0.f, rs1 = 0.f;
-            // pass 2: P = exp2(x - m) in bf16, written over S columns already read
-            // (keys 64h..64h+63 -> P columns 32h..32h+31)
-#pragma unroll
-            for (int hh = 0; hh < 2; ++hh) {
-                uint32_t r[64], pw[32];
-                tmem_ld_x32(tbase + lane_addr + s_col(x) + hh * 64, *reinterpret_cast<uint32_t(*)[32]>(&r[0]));
-                tmem_ld_x32(tbase + lane_addr + s_col(x) + hh * 64 + 32, *reinterpret_cast<uint32_t(*)[32]>(&r[32]));
-                tmem_ld_wait();
-                reg_fence(r);
-                if (fast) {
-                    const uint64_t sc2 = f2_pack(__float_as_uint(sl2), __float_as_uint(sl2));
-                    const uint64_t nm2 = f2_pack(__float_as_uint(neg_m), __float_as_uint(neg_m));
-                    uint64_t acc2 = f2_pack(0u, 0u);
-#pragma unroll
-                    for (int k = 0; k < 32; ++k) {
-                        float x0, x1;
-                        f2_unpack(f2_fma(f2_pack(r[2 * k], r[2 * k + 1]), sc2, nm2), x0, x1);
-                        const float p0 = ex2(x0), p1 = ex2(x1);
-                        acc2 = f2_add(acc2, f2_pack(__float_as_uint(p0), __float_as_uint(p1)));
-                        pw[k] = pack16x2(p0, p1, f16);
-                    }
-                    float a0, a1;
-                    f2_unpack(acc2, a0, a1);
-                    rs0 += a0;
-                    rs1 += a1;
-                } else {
-#pragma unroll
-                    for (int k = 0; k < 32; ++k) {
-                        const int key = hh * 64 + 2 * k;
-                        const float p0 = (none || key >= vis) ? 0.f : ex2(__uint_as_float(r[2 * k]) * sl2 - m_run);
-                        const float p1 = (none || key + 1 >= vis) ? 0.f : ex2(__uint_as_float(r[2 * k + 1]) * sl2 - m_run);
-                        rs0 += p0;
-                        rs1 += p1;
-                        pw[k] = pack16x2(p0, p1, f16);
-                    }
+            // ---- epilogue
+            if (active && ok) {
+                const bool write = i < sg.q_len;
+                const long long orow = ((long long)(sg.q0 + i) * a.num_q_heads + h);
+                if (nx > 0) {
+                    ok = mbar_wait(&bars[P_OD + x], (ns - 1) & 1, abort_sh, a.wait_ns);
+                    ok = __all_sync(0xffffffffu, ok);
                 }
-                tmem_st_x32(tbase + lane_addr + s_col(x) + hh * 32, pw);
+                if (ok) {
+                    tc_fence_after();
+                    const float inv = l_run > 0.f ? 1.f / l_run : 0.f;
+                    uint16_t* dst = a.out + orow * 128;
+#pragma unroll
+                    for (int c = 0; c < 4; ++c) {
+                        uint32_t o[32];
+                        if (nx > 0) {
+                            tmem_ld_x32(tbase + lane_addr + o_col(x) + c * 32, o);
+                            tmem_ld_wait();
+                            reg_fence(o);
+                        } else {
+#pragma unroll
+                            for (int kk = 0; kk < 32; ++kk) o[kk] = 0u;
+                        }
+                        if (write) {
+                            uint32_t w[16];
+#pragma unroll
+                            for (int kk = 0; kk < 16; ++kk)
+                                w[kk] = pack16x2(__uint_as_float(o[2 * kk]) * inv, __uint_as_float(o[2 * kk + 1]) * inv, f16);
+                            uint4* d4 = reinterpret_cast<uint4*>(dst + c * 32);
+#pragma unroll
+                            for (int kk = 0; kk < 4; ++kk)
+                                d4[kk] = make_uint4(w[4 * kk], w[4 * kk + 1], w[4 * kk + 2], w[4 * kk + 3]);
+                        }
+                    }
+                    if (write && a.lse)
+                        a.lse[orow] = l_run > 0.f ? (m_run + __log2f(l_run)) * kLn2f : -INFINITY;
+                }
             }
-            const float rs = rs0 + rs1;
-            l_run += rs;
-            tmem_st_wait();
+            if (!ok) break;
+            // the next item's PV into O_x starts from P_x, which this thread
+            // writes only after the reads above: no extra barrier
             tc_fence_before();
-            mbar_arrive(&bars[P_PF + x]);
-        }
-        // ---- epilogue
-        if (active && ok) {
-            const bool write = i < sg.q_len;
-            const long long orow = ((long long)(sg.q0 + i) * a.num_q_heads + h);
-            if (nx > 0) {
-                ok = mbar_wait(&bars[P_OD + x], (nx - 1) & 1, abort_sh, a.wait_ns);
-                ok = __all_sync(0xffffffffu, ok);
-            }
-            if (ok) {
-                tc_fence_after();
-                const float inv = l_run > 0.f ? 1.f / l_run : 0.f;
-                uint16_t* dst = a.out + orow * 128;
-#pragma unroll
-                for (int c = 0; c < 4; ++c) {
-                    uint32_t o[32];
-                    if (nx > 0) {
-                        tmem_ld_x32(tbase + lane_addr + o_col(x) + c * 32, o);
-                        tmem_ld_wait();
-                        reg_fence(o);
-                    } else {
-#pragma unroll
-                        for (int k = 0; k < 32; ++k) o[k] = 0u;
-                    }
-                    if (write) {
-                        uint32_t w[16];
-#pragma unroll
-                        for (int k = 0; k < 16; ++k)
-                            w[k] = pack16x2(__uint_as_float(o[2 * k]) * inv, __uint_as_float(o[2 * k + 1]) * inv, f16);
-                        uint4* d4 = reinterpret_cast<uint4*>(dst + c * 32);
-#pragma unroll
-                        for (int k = 0; k < 4; ++k) d4[k] = make_uint4(w[4 * k], w[4 * k + 1], w[4 * k + 2], w[4 * k + 3]);
-                    }
-                }
-                if (write && a.lse)
-                    a.lse[orow] = l_run > 0.f ? (m_run + __log2f(l_run)) * kLn2f : -INFINITY;
-            }
+            gt += nkv;
+            ++kit;
         }
         if (!ok) {
             *abort_sh = 1;
@@ -615,6 +712,14 @@ __global__ void __launch_bounds__(320, 1)
     if (warp == 1) {
         tc_fence_after();
         tmem_dealloc(tbase, 512);
+    }
+    if (threadIdx.x == 0) {
+        // the last CTA to finish leaves the work counters at zero for the next call
+        __threadfence();
+        if (atomicAdd(ctas_done, 1) == (int)gridDim.x - 1) {
+            atomicExch(next_item, 0);
+            atomicExch(ctas_done, 0);
+        }
     }
 }
 
@@ -677,7 +782,15 @@ cudaError_t launch_t(const PrefillArgs& a, const CUtensorMap* mq, const CUtensor
         e = cudaGetLastError();
         if (e != cudaSuccess) return e;
     }
-    dim3 grid((unsigned)(a.num_q_tiles * a.batch) * (unsigned)a.num_q_heads);
+    // persistent: one CTA per SM, or one per work item when there are fewer
+    const long long items = (long long)a.num_q_tiles * a.batch * a.num_q_heads;
+    if (items <= 0) return cudaSuccess;
+    if (items > 0x7FFFFFFFLL - 65536) return cudaErrorInvalidValue;  // the work counter is an int32
+    int dev = 0, sms = 0;
+    e = cudaGetDevice(&dev);
+    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) return e;
+    const unsigned grid = (unsigned)(items < sms ? items : sms);
     prefill_kernel<ROPE, PAGED, F8><<<grid, L::kThreads, L::kSmem, stream>>>(a, *mq, *mk, *mv, *mr, *mqr);
     return cudaGetLastError();
 }
