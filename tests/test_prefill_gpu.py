@@ -196,6 +196,38 @@ def test_longest_first_order_changes_nothing():
     assert torch.equal(o1, o2) and torch.equal(l1, l2)
 
 
+@pytest.mark.parametrize("lens,heads", [([1000, 700, 1024, 513], 16), ([90, 300], 2)])
+@pytest.mark.parametrize("sorted_order", [True, False])
+def test_persistent_work_counters_reset(lens, heads, sorted_order):
+    """The persistent CTAs take (query block, head) items from two counters in
+    the status region (int32 at bytes 64 and 128); the last CTA leaves both at
+    zero, so back-to-back calls on one workspace give the same bits -- with more
+    items than SMs and with fewer, with and without the longest-first order."""
+    inp = W.make_ragged_prefill(lens, heads, 128, 128, seed=31)
+    dev = "cuda"
+    sh = ops.prefill_shapes(inp.batch, heads, heads, 128, 128, 0, inp.max_seqlen_q, int(inp.cu_seqlens_q[-1]),
+                            int(inp.cu_seqlens_k[-1]))
+    args = [ops.as_bf16(inp.q, dev), ops.as_bf16(inp.k, dev), ops.as_bf16(inp.v, dev),
+            torch.from_numpy(inp.cu_seqlens_q).to(dev), torch.from_numpy(inp.cu_seqlens_k).to(dev), inp.scale]
+    size = B.pa_prefill_workspace_size(sh) if sorted_order else B.PA_STATUS_BYTES
+    ws = torch.zeros(size, dtype=torch.uint8, device=dev)
+    outs = []
+    for _ in range(3):
+        o, l, _ = ops.prefill(sh, *args, True, workspace=ws)
+        torch.cuda.synchronize()
+        words = ws[:B.PA_STATUS_BYTES].view(torch.int32).cpu().numpy()
+        assert words[16] == 0 and words[32] == 0, (words[16], words[32])
+        assert B.pa_check_status(ws) == B.PA_OK
+        outs.append((o.clone(), l.clone()))
+    for o, l in outs[1:]:
+        assert torch.equal(o, outs[0][0]) and torch.equal(l, outs[0][1])
+    rows = sample_rows(inp, per_seq=16)
+    ro, rl = reference(inp, rows=rows)
+    got_o = outs[0][0].float().cpu().numpy().reshape(-1, 128)[rows]
+    got_l = outs[0][1].cpu().numpy().reshape(-1)[rows]
+    assert_close(got_o, got_l, ro, rl)
+
+
 @pytest.mark.parametrize("name", ["chunked", "mla"])
 def test_full_size_repeats_bitwise(name):
     """Three runs of a full-size workload give identical bits (no ordering races)."""
