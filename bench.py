@@ -793,13 +793,18 @@ def run_append(args, rank, world, local_rank, dist):
         st_h.copy_(ws[:4].view(torch.int32), non_blocking=True)
         torch.cuda.synchronize(dev)
 
-    for _ in range(3):
-        e2e_step()
-    E = max(3, min(K, args.e2e_steps))
-    t0 = time.perf_counter()
-    for _ in range(E):
-        e2e_step()
-    el = time.perf_counter() - t0
+    e2e = None
+    if not args.no_e2e:
+        for _ in range(3):
+            e2e_step()
+        E = max(3, min(K, args.e2e_steps))
+        t0 = time.perf_counter()
+        for _ in range(E):
+            e2e_step()
+        el = time.perf_counter() - t0
+        e2e = {"value": round(world * nbytes * E / el / 1e9, 2), "unit": "GB/s",
+               "h2d_bytes_per_step": 2 * T * hk * 128 * 2, "d2h_bytes_per_step": 4, "steps": E,
+               "ms_per_step": round(el / E * 1e3, 4)}
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         import oracle
@@ -828,9 +833,7 @@ def run_append(args, rank, world, local_rank, dist):
                      "peak_source": f"{pk_src} (copy bandwidth)", "algorithmic_bytes_per_launch": nbytes,
                      "kernel_ms": round(ms, 5)},
         "cpu_baseline": cpu,
-        "e2e": {"value": round(world * nbytes * E / el / 1e9, 2), "unit": "GB/s",
-                "h2d_bytes_per_step": 2 * T * hk * 128 * 2, "d2h_bytes_per_step": 4, "steps": E,
-                "ms_per_step": round(el / E * 1e3, 4)},
+        "e2e": e2e,
         "gpu_launches": K, "clocks": clk.summary(),
     }
     if rank == 0:
