@@ -55,6 +55,8 @@ def _load():
         lib.oracle_prefill_mla_e4m3.argtypes = [i32, i32, i32, P, P, P, P, P, P, P, P, P, P, i32, dbl, P, i64,
                                                 P, P]
         lib.oracle_prefill_mla_e4m3.restype = i32
+        lib.oracle_prefill_mla_rope_e4m3.argtypes = [i32, i32, i32, P, P, P, P, P, P, P, P, i32, dbl, P, i64, P, P]
+        lib.oracle_prefill_mla_rope_e4m3.restype = i32
         lib.oracle_num_threads.restype = i32
         lib.oracle_set_num_threads.argtypes = [i32]
         _lib = lib
@@ -203,6 +205,34 @@ def prefill_mla_e4m3(q_nope, q_rope, q_scale, k_nope, k_scale, v, k_rope, cu_seq
     lib.oracle_prefill_mla_e4m3(B, Hq, Hk, _p(qn), _p(qr), _p(qs), _p(kn), _p(ks), _p(vv), _p(kr), _p(cq), _p(ck),
                                 _p(qo), int(bool(causal)), float(scale), _p(rr), nrows if rr is not None else 0,
                                 _p(out), _p(lse))
+    if rr is None:
+        return out.reshape(total_q, Hq, 128), lse.reshape(total_q, Hq)
+    return out, lse
+
+
+def prefill_mla_rope_e4m3(q, k_nope, v, k_rope, k_rope_scales, cu_seqlens_q, cu_seqlens_k, scale: float,
+                          causal: bool = True, qo_offset=None, rows=None):
+    """MLA prefill with an e4m3 rope key (see ``oracle_prefill_mla_rope_e4m3`` in
+    oracle.c).  q uint16 bf16 [Tq, Hq, 192]; k_nope, v uint16 bf16 [Tk, Hk, 128];
+    k_rope uint8 e4m3 [Tk, 1, 64] or [Tk, 64]; k_rope_scales float32 [Tk].
+    Returns (out float64 [rows, 128] or [Tq, Hq, 128], lse)."""
+    lib = _load()
+    qq, kn, vv = _c(q, np.uint16), _c(k_nope, np.uint16), _c(v, np.uint16)
+    kr, rs = _c(k_rope, np.uint8), _c(k_rope_scales, np.float32)
+    cq, ck = _c(cu_seqlens_q, np.int32), _c(cu_seqlens_k, np.int32)
+    qo = _c(qo_offset, np.int32)
+    rr = _c(rows, np.int64)
+    B = len(cq) - 1
+    total_q, Hq = qq.shape[0], qq.shape[1]
+    Hk = kn.shape[1]
+    if kr.size != kn.shape[0] * 64 or rs.size != kn.shape[0]:
+        raise ValueError("k_rope must hold 64 codes and k_rope_scales one scale per key token")
+    nrows = total_q * Hq if rr is None else len(rr)
+    out = np.zeros((nrows, 128), dtype=np.float64)
+    lse = np.zeros(nrows, dtype=np.float64)
+    lib.oracle_prefill_mla_rope_e4m3(B, Hq, Hk, _p(qq), _p(kn), _p(vv), _p(kr), _p(rs), _p(cq), _p(ck), _p(qo),
+                                     int(bool(causal)), float(scale), _p(rr), nrows if rr is not None else 0,
+                                     _p(out), _p(lse))
     if rr is None:
         return out.reshape(total_q, Hq, 128), lse.reshape(total_q, Hq)
     return out, lse

@@ -27,6 +27,9 @@
  *   - fp8 MLA (flare_mla_prefill's overload with q_nope, q_rope, q_scale and
  *     k_scales): the per-head parts of q and k are e4m3 codes times their
  *     head's scale; the rope parts and v stay 16-bit.
+ *   - MLA with a quantised rope key (flare_mla_prefill's overload with
+ *     k_rope and k_rope_scales): the shared rope key of token t is its e4m3
+ *     codes times k_rope_scales[t]; q, the per-head k and v stay bf16.
  * New tokens are written into pages by oracle_append_kv ("prefill writes into
  * paged cache", section 4): token p of a sequence goes to row p % 64 of page
  * block_table[b, p / 64].
@@ -395,6 +398,64 @@ int oracle_prefill_mla_e4m3(int B, int Hq, int Hk, const uint8_t* q_nope, const 
             int64_t t = cu_k[b] + j;
             for (int d = 0; d < DN; ++d) kd[j * DQK + d] = ks * oracle_e4m3_to_double(k_nope[(t * Hk + g) * DN + d]);
             for (int d = 0; d < DR; ++d) kd[j * DQK + DN + d] = oracle_bf16_to_double(k_rope[t * DR + d]);
+            for (int d = 0; d < DV; ++d) vd[j * DV + d] = oracle_bf16_to_double(v[(t * Hk + g) * DV + d]);
+        }
+        attend_row(qd, kd, vd, n, DQK, DV, scale, sc, out + r * DV, &lse[r]);
+        free(qd); free(kd); free(vd); free(sc);
+    }
+    return 0;
+}
+
+/*
+ * MLA prefill with the shared rope key in e4m3 (Modular flare_mla_prefill,
+ * the overload taking k_rope and k_rope_scales).  The page gives the argument
+ * without its granularity; the reading here: one fp32 scale per key token.
+ *   q             bf16 [total_q, Hq, 192]  (128 per-head entries, then 64 rope)
+ *   k_nope        bf16 [total_k, Hk, 128]
+ *   v             bf16 [total_k, Hk, 128]
+ *   k_rope        e4m3 [total_k, 64]       (one row per token, all heads)
+ *   k_rope_scales float [total_k]
+ * Key j (token t = cu_k[b] + j) of KV head g is the vector
+ * (k_nope[t, g], k_rope_scales[t] * k_rope[t]); then the attention of
+ * oracle_prefill (masking, offsets, row sampling, outputs as there; out
+ * double [rows, 128]).
+ */
+int oracle_prefill_mla_rope_e4m3(int B, int Hq, int Hk, const uint16_t* q, const uint16_t* k_nope,
+                                 const uint16_t* v, const uint8_t* k_rope, const float* k_rope_scales,
+                                 const int32_t* cu_q, const int32_t* cu_k, const int32_t* qo_offset, int causal,
+                                 double scale, const int64_t* rows, int64_t nrows, double* out, double* lse) {
+    enum { DN = 128, DR = 64, DQK = 192, DV = 128 };
+    int group = Hq / Hk;
+    int64_t total_q = cu_q[B];
+    if (!rows) nrows = total_q * Hq;
+#pragma omp parallel for schedule(dynamic, 1)
+    for (int64_t r = 0; r < nrows; ++r) {
+        int64_t flat = rows ? rows[r] : r;
+        int64_t tok = flat / Hq;
+        int h = (int)(flat % Hq);
+        int g = h / group;
+        int b = 0;
+        while (b < B - 1 && cu_q[b + 1] <= tok) ++b;
+        int64_t i = tok - cu_q[b];
+        int64_t q_len = cu_q[b + 1] - cu_q[b];
+        int64_t kv_len = cu_k[b + 1] - cu_k[b];
+        int64_t off = qo_offset ? qo_offset[b] : kv_len - q_len;
+        int64_t n = kv_len;
+        if (causal) {
+            int64_t lim = off + i + 1;
+            if (lim < n) n = lim;
+            if (n < 0) n = 0;
+        }
+        double* qd = (double*)malloc(sizeof(double) * DQK);
+        double* kd = (double*)malloc(sizeof(double) * (size_t)(n ? n : 1) * DQK);
+        double* vd = (double*)malloc(sizeof(double) * (size_t)(n ? n : 1) * DV);
+        double* sc = (double*)malloc(sizeof(double) * (size_t)(n ? n : 1));
+        for (int d = 0; d < DQK; ++d) qd[d] = oracle_bf16_to_double(q[(tok * Hq + h) * DQK + d]);
+        for (int64_t j = 0; j < n; ++j) {
+            int64_t t = cu_k[b] + j;
+            double rs = (double)k_rope_scales[t];
+            for (int d = 0; d < DN; ++d) kd[j * DQK + d] = oracle_bf16_to_double(k_nope[(t * Hk + g) * DN + d]);
+            for (int d = 0; d < DR; ++d) kd[j * DQK + DN + d] = rs * oracle_e4m3_to_double(k_rope[t * DR + d]);
             for (int d = 0; d < DV; ++d) vd[j * DV + d] = oracle_bf16_to_double(v[(t * Hk + g) * DV + d]);
         }
         attend_row(qd, kd, vd, n, DQK, DV, scale, sc, out + r * DV, &lse[r]);

@@ -433,6 +433,81 @@ def mla_e4m3_prefill(seed: int = 0, batch: int = 8, lo: int = 512, hi: int = 409
     return make_mla_e4m3(uniform_lengths(seed, batch, lo, hi), heads, seed=seed)
 
 
+@dataclass
+class MlaRopeE4m3Inputs:
+    """MLA prefill with the shared rope key in e4m3 plus one fp32 scale per key
+    token; q, the per-head k and v in bf16."""
+    q: np.ndarray              # uint16 bf16 [total_q, Hq, 192]
+    k_nope: np.ndarray         # uint16 bf16 [total_k, Hk, 128]
+    v: np.ndarray              # uint16 bf16 [total_k, Hk, 128]
+    k_rope: np.ndarray         # uint8 e4m3 [total_k, 1, 64]
+    k_rope_scales: np.ndarray  # float32 [total_k]
+    cu_seqlens_q: np.ndarray
+    cu_seqlens_k: np.ndarray
+    scale: float
+    causal: bool = True
+    qo_offset: Optional[np.ndarray] = None
+    meta: dict = field(default_factory=dict)
+
+    @property
+    def batch(self) -> int:
+        return len(self.cu_seqlens_q) - 1
+
+    @property
+    def num_q_heads(self) -> int:
+        return self.q.shape[1]
+
+    @property
+    def num_kv_heads(self) -> int:
+        return self.k_nope.shape[1]
+
+    @property
+    def max_seqlen_q(self) -> int:
+        return int(np.diff(self.cu_seqlens_q).max()) if self.batch else 0
+
+    head_dim_qk = 192
+    head_dim_v = 128
+    rope_dim = 64
+    block_table = None
+    paged = False
+
+
+def quantise_per_row(x: np.ndarray):
+    """x float32 [T, D] -> (e4m3 codes [T, D], float32 [T] scales): scale_t =
+    amax(|x[t]|) / 448 (1 for an all-zero row), code = e4m3(clamp(float32(x /
+    scale_t), -448, 448)), rounded to nearest even (the rule of quantise_per_head,
+    one scale per row)."""
+    import torch
+    xt = torch.from_numpy(np.ascontiguousarray(x, dtype=np.float32))
+    amax = xt.abs().amax(dim=1) if x.shape[1] else torch.zeros(x.shape[0])
+    scales = torch.where(amax > 0, amax / E4M3_MAX, torch.ones_like(amax)).to(torch.float32)
+    y = (xt / scales.view(-1, 1)).clamp_(-E4M3_MAX, E4M3_MAX)
+    return _to_e4m3_bits_fast(y.numpy()).reshape(x.shape), scales.numpy()
+
+
+def make_mla_rope_e4m3(lens, num_heads: int, seed: int = 0, num_kv_heads: Optional[int] = None, kv_lens=None,
+                       causal: bool = True, qo_offset=None) -> MlaRopeE4m3Inputs:
+    """Ragged MLA prefill whose rope key is e4m3 with one scale per token: q,
+    k_nope and v N(0,1) rounded to bf16, k_rope N(0,1) quantised per token;
+    scale 1/sqrt(192)."""
+    lens = np.asarray(lens, dtype=np.int32)
+    kv_lens = lens if kv_lens is None else np.asarray(kv_lens, dtype=np.int32)
+    hk = num_heads if num_kv_heads is None else num_kv_heads
+    tq, tk = int(lens.sum()), int(kv_lens.sum())
+    codes, scales = quantise_per_row(normal_f32(seed, _S_KROPE, tk * 64).reshape(tk, 64))
+    return MlaRopeE4m3Inputs(
+        q=bf16_normal_fast(seed, _S_Q, (tq, num_heads, 192)), k_nope=bf16_normal_fast(seed, _S_K, (tk, hk, 128)),
+        v=bf16_normal_fast(seed, _S_V, (tk, hk, 128)), k_rope=codes.reshape(tk, 1, 64), k_rope_scales=scales,
+        cu_seqlens_q=cu_seqlens(lens), cu_seqlens_k=cu_seqlens(kv_lens), scale=1.0 / math.sqrt(192.0),
+        causal=causal, qo_offset=None if qo_offset is None else np.asarray(qo_offset, dtype=np.int32))
+
+
+def mla_rope_e4m3_prefill(seed: int = 0, batch: int = 8, lo: int = 512, hi: int = 4096,
+                          heads: int = 128) -> MlaRopeE4m3Inputs:
+    """The MLA prefill workload's lengths and heads with an e4m3 rope key."""
+    return make_mla_rope_e4m3(uniform_lengths(seed, batch, lo, hi), heads, seed=seed)
+
+
 def poison_unused(inp: DecodeInputs, nan_bits: Optional[int] = None) -> DecodeInputs:
     """Fill every pool row that no sequence may read with NaN.
 

@@ -494,3 +494,66 @@ def test_mla_e4m3_scale_moves_between_q_and_k():
     o3, _ = oracle.prefill_mla_e4m3(inp.q_nope, inp.q_rope, (inp.q_scale * 2).astype(np.float32), inp.k_nope,
                                     inp.k_scale, *args)
     assert np.abs(o3 - o1).max() > 1e-3
+
+
+# ---------------------------------------------------------------- MLA with an e4m3 rope key
+
+def _mla_rope_e4m3_small(seed=11, heads=4, hk=None):
+    return W.make_mla_rope_e4m3([9, 130, 1], heads, seed=seed, num_kv_heads=hk)
+
+
+def _rope_e4m3_oracle(inp, **kw):
+    return oracle.prefill_mla_rope_e4m3(inp.q, inp.k_nope, inp.v, inp.k_rope, inp.k_rope_scales, inp.cu_seqlens_q,
+                                        inp.cu_seqlens_k, inp.scale, **kw)
+
+
+def test_mla_rope_e4m3_with_power_of_two_scales_equals_the_bf16_mla_oracle():
+    """An e4m3 code times a power of two (or zero) is exactly a bf16 value, so with
+    such per-token scales the oracle must reproduce the (separately pinned) bf16
+    MLA oracle bit for bit on the decoded rope key -- a scale applied per head or
+    per query row instead of per key token, or to the whole score instead of the
+    rope term, breaks the equality."""
+    inp = _mla_rope_e4m3_small(hk=2)
+    rng = np.random.default_rng(1)
+    tk = inp.k_rope.shape[0]
+    sc = np.exp2(rng.integers(-9, 2, size=tk)).astype(np.float32)
+    sc[5] = 0.0  # a token whose rope term vanishes
+    inp.k_rope_scales = sc
+    kr = t_e4m3(inp.k_rope).numpy() * sc[:, None, None]
+    kr16 = W.f32_to_bf16_bits(kr.astype(np.float32))
+    assert np.array_equal(t_bf16(kr16).numpy(), kr)  # the re-encoding is exact
+    ref_out, ref_lse = oracle.prefill(inp.q, inp.k_nope, inp.v, inp.cu_seqlens_q, inp.cu_seqlens_k, inp.scale, True,
+                                      k_rope=kr16)
+    out, lse = _rope_e4m3_oracle(inp)
+    assert np.array_equal(out, ref_out) and np.array_equal(lse, ref_lse)
+
+
+def test_mla_rope_e4m3_matches_torch_sdpa_with_general_scales():
+    inp = _mla_rope_e4m3_small(seed=12)
+    out, lse = _rope_e4m3_oracle(inp)
+    kr = t_e4m3(inp.k_rope) * torch.from_numpy(inp.k_rope_scales.astype(np.float64))[:, None, None]
+    q, k, v = t_bf16(inp.q), t_bf16(inp.k_nope), t_bf16(inp.v)
+    for b in range(inp.batch):
+        a, e = inp.cu_seqlens_q[b], inp.cu_seqlens_q[b + 1]
+        L = e - a
+        kk = torch.cat([k[a:e], kr[a:e].expand(L, 4, 64)], dim=-1).transpose(0, 1)
+        ro, rl = _sdpa(q[a:e].transpose(0, 1), kk, v[a:e].transpose(0, 1), inp.scale,
+                       torch.ones(L, L, dtype=torch.bool).tril())
+        np.testing.assert_allclose(out[a:e], ro.transpose(0, 1).numpy(), rtol=1e-12, atol=1e-12)
+        np.testing.assert_allclose(lse[a:e], rl.transpose(0, 1).numpy(), rtol=1e-12, atol=1e-12)
+
+
+def test_mla_rope_e4m3_scale_multiplies_only_that_tokens_rope_term():
+    """Scaling token t's rope scale by c equals scaling its rope codes' values by
+    c: with c = 2 (exact) the result equals the oracle on codes re-encoded at
+    twice the value, and the change reaches only rows that can see token t."""
+    inp = _mla_rope_e4m3_small(seed=13)
+    o1, l1 = _rope_e4m3_oracle(inp)
+    t = int(inp.cu_seqlens_k[-1]) - 1  # the last token: only the one-row third sequence sees it
+    sc = inp.k_rope_scales.copy()
+    sc[t] *= 2
+    inp2 = W.MlaRopeE4m3Inputs(**{**inp.__dict__, "k_rope_scales": sc})
+    o2, l2 = _rope_e4m3_oracle(inp2)
+    first = int(inp.cu_seqlens_q[2])
+    assert np.array_equal(o1[:first], o2[:first]) and np.array_equal(l1[:first], l2[:first])
+    assert np.abs(l2[first:] - l1[first:]).max() > 1e-6
