@@ -241,6 +241,11 @@ def prefill_workload(name):
         inp = W.mla_e4m3_prefill(0)
         desc = ("fp8 MLA ragged causal prefill: the MLA workload (8 sequences L~U[512,4096], H=128) with q_nope / "
                 "k_nope in e4m3 + per-head fp32 scales (amax/448), q_rope / k_rope / v bf16, seed 0")
+    elif name == "prefill_mla_rope_fp8":
+        inp = W.mla_rope_e4m3_prefill(0)
+        desc = ("MLA ragged causal prefill with an e4m3 rope key: the MLA workload (8 sequences L~U[512,4096], "
+                "H=128) with k_rope [T,1,64] in e4m3 + one fp32 scale per token (amax/448), q / k_nope / v bf16, "
+                "seed 0")
     else:
         raise ValueError(name)
     return inp, desc
@@ -307,7 +312,10 @@ def cpu_oracle_prefill_sample(inp, budget_s=None, steps=None, warmup=0, rows_per
 
     def one():
         rows = rng.integers(0, total_rows, size=rows_per_step).astype(np.int64)
-        if is_fp8_mla(inp):
+        if is_rope_fp8(inp):
+            oracle.prefill_mla_rope_e4m3(inp.q, inp.k_nope, inp.v, inp.k_rope, inp.k_rope_scales, inp.cu_seqlens_q,
+                                         inp.cu_seqlens_k, inp.scale, True, qo_offset=inp.qo_offset, rows=rows)
+        elif is_fp8_mla(inp):
             oracle.prefill_mla_e4m3(inp.q_nope, inp.q_rope, inp.q_scale, inp.k_nope, inp.k_scale, inp.v, inp.k_rope,
                                     inp.cu_seqlens_q, inp.cu_seqlens_k, inp.scale, True, qo_offset=inp.qo_offset,
                                     rows=rows)
@@ -544,6 +552,17 @@ def decode_e2e(inp, dev, stream, sh, full_bytes, world, dist, args):
             "includes": "host schedule + pinned H2D of all inputs + pa_decode + D2H of out/lse + sync"}
 
 
+def is_rope_fp8(inp):
+    return hasattr(inp, "k_rope_scales")
+
+
+def prefill_ws_bytes(inp, sh):
+    from paged_kv_attention_fwd_gb300 import binding as B
+    if is_rope_fp8(inp):
+        return B.pa_prefill_mla_rope_fp8_workspace_size(sh)
+    return B.pa_prefill_workspace_size(sh)
+
+
 def is_fp8_mla(inp):
     return hasattr(inp, "q_nope")
 
@@ -551,6 +570,10 @@ def is_fp8_mla(inp):
 def prefill_host_arrays(inp):
     """Name -> host array (16-bit elements as int16 bit patterns) of every input the call reads."""
     h = {"cq": inp.cu_seqlens_q, "ck": inp.cu_seqlens_k}
+    if is_rope_fp8(inp):
+        h.update(q=inp.q.view(np.int16), kn=inp.k_nope.view(np.int16), v=inp.v.view(np.int16), kr=inp.k_rope,
+                 krs=inp.k_rope_scales)
+        return h
     if is_fp8_mla(inp):
         h.update(qn=inp.q_nope, qr=inp.q_rope.view(np.int16), qs=inp.q_scale, kn=inp.k_nope, ks=inp.k_scale,
                  v=inp.v.view(np.int16), kr=inp.k_rope.view(np.int16))
@@ -578,7 +601,10 @@ def prefill_shapes_for(inp, dev):
 def prefill_launch(inp, sh, d, out, lse, ws, stream):
     """One call of the library's prefill entry for this workload on device buffers `d`."""
     from paged_kv_attention_fwd_gb300 import binding as B
-    if is_fp8_mla(inp):
+    if is_rope_fp8(inp):
+        B.pa_prefill_mla_rope_fp8(sh, d["q"], d["kn"], d["v"], d["kr"], d["krs"], d["cq"], d["ck"], None, True,
+                                  inp.scale, out, lse, ws, stream=stream)
+    elif is_fp8_mla(inp):
         B.pa_prefill_mla_fp8(sh, d["qn"], d["qr"], d["qs"], d["kn"], d["ks"], d["v"], d["kr"], d["cq"], d["ck"], None,
                              True, inp.scale, out, lse, ws, stream=stream)
     else:
@@ -604,7 +630,7 @@ def run_prefill(args, rank, world, local_rank, dist):
     tq = int(inp.cu_seqlens_q[-1])
     out = torch.empty((tq, inp.num_q_heads, inp.head_dim_v), dtype=torch.bfloat16, device=dev)
     lse = torch.empty((tq, inp.num_q_heads), dtype=torch.float32, device=dev)
-    ws = torch.zeros(B.pa_prefill_workspace_size(sh), dtype=torch.uint8, device=dev)
+    ws = torch.zeros(prefill_ws_bytes(inp, sh), dtype=torch.uint8, device=dev)
     flush, l2_note = l2_policy(dev, sum(t.numel() * t.element_size() for t in d.values()))
     stream = torch.cuda.current_stream(dev)
 
@@ -672,7 +698,10 @@ def run_prefill(args, rank, world, local_rank, dist):
                    "l2": l2_note,
                    "parallelism": f"replicas x{world}"},
         "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
-        "gpu_launches": K * (2 if B.pa_prefill_workspace_size(sh) > B.PA_STATUS_BYTES else 1), "clocks": clocks,
+        # per step: the ordering kernel (with the larger workspace), the rope key's
+        # expansion (e4m3 rope key only) and the prefill kernel
+        "gpu_launches": K * (1 + (B.pa_prefill_workspace_size(sh) > B.PA_STATUS_BYTES) + is_rope_fp8(inp)),
+        "clocks": clocks,
     }
     if rank == 0:
         print(json.dumps(line), flush=True)
@@ -694,7 +723,7 @@ def prefill_e2e(inp, dev, stream, sh, flops, world, dist, args):
     lse_h = torch.empty((tq, inp.num_q_heads), dtype=torch.float32).pin_memory()
     out_d = torch.empty_like(out_h, device=dev)
     lse_d = torch.empty_like(lse_h, device=dev)
-    ws = torch.zeros(B.pa_prefill_workspace_size(sh), dtype=torch.uint8, device=dev)
+    ws = torch.zeros(prefill_ws_bytes(inp, sh), dtype=torch.uint8, device=dev)
 
     def step():
         for k in h:
@@ -855,6 +884,7 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="decode_gqa",
                     choices=["decode_gqa", "decode_fp8", "decode_tiny", "prefill_paged", "prefill_mla", "prefill_mla_fp8",
+                             "prefill_mla_rope_fp8",
                              "append"])
     ap.add_argument("--e2e-steps", type=int, default=20)
     ap.add_argument("--cpu-seconds", type=float, default=12.0)

@@ -305,14 +305,46 @@ size_t pa_prefill_workspace_size(const pa_prefill_shapes* shapes);
  * workspace as for pa_prefill.  The q_nope . k_nope products run on the e4m3
  * tensor path, the rope part and P.V in bf16; to add both into one
  * accumulator the kernel divides the query's rope part by q_scale * k_scale
- * once (rounded to bf16).  A scale that is not positive and finite is
- * recorded as PA_ERR_INVALID_ARG in the status word.
+ * once and holds it as two bf16 levels (hi + lo, about 16 significant bits).
+ * A scale that is not positive and finite is recorded as PA_ERR_INVALID_ARG
+ * in the status word.
  */
 pa_status pa_prefill_mla_fp8(const pa_prefill_shapes* shapes, const void* q_nope, const void* q_rope,
                              const float* q_scale, const void* k_nope, const float* k_scale, const void* v,
                              const void* k_rope, const int32_t* cu_seqlens_q, const int32_t* cu_seqlens_k,
                              const int32_t* qo_offset, int causal, float scale, void* out, float* lse,
                              void* workspace, size_t workspace_bytes, cudaStream_t stream);
+
+/*
+ * pa_prefill_mla_rope_fp8 -- the MLA prefill of pa_prefill with the shared
+ * rope key quantised: Modular flare_mla_prefill's overload taking k_rope and
+ * k_rope_scales.  The page gives the argument but not its granularity; here
+ * there is one fp32 scale per key token:
+ *   score(i, j, h) = scale * (<q[i, h, 0:128], k_nope[j, g]>
+ *                             + k_rope_scales[j] * <q[i, h, 128:192], k_rope[j]>)
+ *   q        bf16 [total_q, Hq, 192]      k_nope  bf16 [total_k, Hk, 128]
+ *   v        bf16 [total_k, Hk, 128]      out     bf16 [total_q, Hq, 128]
+ *   k_rope   e4m3 [total_k, 1, 64]        k_rope_scales fp32 [total_k] (device)
+ * shapes: dtype PA_KV_BF16, head_dim_qk 192, rope_dim 64, head_dim_v 128;
+ * keys are ragged (no block table); cu_seqlens, qo_offset, causal and lse as
+ * for pa_prefill.  The call first expands the rope key, once for all heads,
+ * into two bf16 levels hi + lo of code * scale (about 16 significant bits)
+ * inside the workspace, then runs the MLA prefill with both levels as
+ * key chunks.  workspace: pa_prefill_mla_rope_fp8_workspace_size(shapes)
+ * bytes, zero-filled once (the status region as for pa_prefill; the two
+ * levels, 2 x 128 bytes per key token, follow the ordering region);
+ * PA_ERR_WORKSPACE if smaller.
+ */
+pa_status pa_prefill_mla_rope_fp8(const pa_prefill_shapes* shapes, const void* q, const void* k_nope,
+                                  const void* v, const void* k_rope, const float* k_rope_scales,
+                                  const int32_t* cu_seqlens_q, const int32_t* cu_seqlens_k,
+                                  const int32_t* qo_offset, int causal, float scale, void* out, float* lse,
+                                  void* workspace, size_t workspace_bytes, cudaStream_t stream);
+
+/* Workspace bytes pa_prefill_mla_rope_fp8 needs: pa_prefill_workspace_size
+ * rounded up to 256, then two regions of total_k * 128 bytes (each rounded up
+ * to 256). */
+size_t pa_prefill_mla_rope_fp8_workspace_size(const pa_prefill_shapes* shapes);
 
 /* ----------------------------------------------------------------- mixed batches */
 

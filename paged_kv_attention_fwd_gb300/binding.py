@@ -95,6 +95,11 @@ def lib() -> ctypes.CDLL:
         L.pa_prefill_mla_fp8.argtypes = [ctypes.POINTER(pa_prefill_shapes), _P, _P, _P, _P, _P, _P, _P, _P, _P, _P,
                                          ctypes.c_int, f32, _P, _P, _P, sz, _P]
         L.pa_prefill_mla_fp8.restype = ctypes.c_int
+        L.pa_prefill_mla_rope_fp8.argtypes = [ctypes.POINTER(pa_prefill_shapes), _P, _P, _P, _P, _P, _P, _P, _P,
+                                              ctypes.c_int, f32, _P, _P, _P, sz, _P]
+        L.pa_prefill_mla_rope_fp8.restype = ctypes.c_int
+        L.pa_prefill_mla_rope_fp8_workspace_size.argtypes = [ctypes.POINTER(pa_prefill_shapes)]
+        L.pa_prefill_mla_rope_fp8_workspace_size.restype = ctypes.c_size_t
         L.pa_get_static_plan.argtypes = [ctypes.POINTER(pa_decode_shapes), ctypes.POINTER(pa_decode_plan)]
         L.pa_get_static_plan.restype = ctypes.c_int
         L.pa_get_metadata_device.argtypes = [ctypes.POINTER(pa_decode_shapes), ctypes.POINTER(pa_decode_plan), _P, _P,
@@ -233,6 +238,21 @@ def pa_prefill_mla_fp8(shapes: pa_prefill_shapes, q_nope, q_rope, q_scale, k_nop
                                     _ptr(k_scale), _ptr(v), _ptr(k_rope), _ptr(cu_seqlens_q), _ptr(cu_seqlens_k),
                                     _ptr(qo_offset), int(bool(causal)), float(scale), _ptr(out), _ptr(lse),
                                     _ptr(workspace), int(workspace_bytes), _stream(stream)))
+
+
+def pa_prefill_mla_rope_fp8(shapes: pa_prefill_shapes, q, k_nope, v, k_rope, k_rope_scales, cu_seqlens_q,
+                            cu_seqlens_k, qo_offset, causal: bool, scale: float, out, lse, workspace,
+                            workspace_bytes: Optional[int] = None, stream=None) -> None:
+    if workspace_bytes is None:
+        workspace_bytes = workspace.numel() * workspace.element_size()
+    _check(lib().pa_prefill_mla_rope_fp8(ctypes.byref(shapes), _ptr(q), _ptr(k_nope), _ptr(v), _ptr(k_rope),
+                                         _ptr(k_rope_scales), _ptr(cu_seqlens_q), _ptr(cu_seqlens_k),
+                                         _ptr(qo_offset), int(bool(causal)), float(scale), _ptr(out), _ptr(lse),
+                                         _ptr(workspace), int(workspace_bytes), _stream(stream)))
+
+
+def pa_prefill_mla_rope_fp8_workspace_size(shapes: pa_prefill_shapes) -> int:
+    return int(lib().pa_prefill_mla_rope_fp8_workspace_size(ctypes.byref(shapes)))
 
 
 def pa_get_static_plan(shapes: pa_decode_shapes) -> pa_decode_plan:

@@ -436,6 +436,7 @@ pa_status fill_prefill_args(const pa_prefill_shapes* sh, const int32_t* cu_seqle
     a->scale_log2 = scale * 1.4426950408889634f;
     a->wait_ns = g_wait_limit_ns.load();
     a->f8 = 0;
+    a->r8 = 0;
     a->q_scale = nullptr;
     a->k_scale = nullptr;
     return PA_OK;
@@ -754,6 +755,80 @@ pa_status pa_prefill_mla_fp8(const pa_prefill_shapes* sh, const void* q_nope, co
 size_t pa_prefill_workspace_size(const pa_prefill_shapes* sh) {
     if (!sh || sh->batch <= 0 || sh->max_seqlen_q <= 0) return PA_STATUS_BYTES;
     return PA_STATUS_BYTES + (size_t)sh->batch * (size_t)cdiv(sh->max_seqlen_q, 256) * 4;
+}
+
+namespace {
+// pa_prefill_mla_rope_fp8's workspace: pa_prefill's, then the rope key's two
+// bf16 levels [total_k, 64] each, every region 256-byte aligned
+size_t rope_levels_offset(const pa_prefill_shapes* sh) { return (pa_prefill_workspace_size(sh) + 255) / 256 * 256; }
+size_t rope_level_bytes(const pa_prefill_shapes* sh) {
+    return ((size_t)(sh->total_k > 0 ? sh->total_k : 0) * 128 + 255) / 256 * 256;
+}
+}  // namespace
+
+size_t pa_prefill_mla_rope_fp8_workspace_size(const pa_prefill_shapes* sh) {
+    if (!sh) return PA_STATUS_BYTES;
+    return rope_levels_offset(sh) + 2 * rope_level_bytes(sh);
+}
+
+pa_status pa_prefill_mla_rope_fp8(const pa_prefill_shapes* sh, const void* q, const void* k_nope, const void* v,
+                                  const void* k_rope, const float* k_rope_scales, const int32_t* cu_seqlens_q,
+                                  const int32_t* cu_seqlens_k, const int32_t* qo_offset, int causal, float scale,
+                                  void* out, float* lse, void* workspace, size_t workspace_bytes,
+                                  cudaStream_t stream) {
+    if (!sh) return fail(PA_ERR_INVALID_ARG, "shapes must not be NULL");
+    const int B = sh->batch, Hq = sh->num_q_heads, Hk = sh->num_kv_heads;
+    if (B < 0 || sh->total_q < 0 || sh->total_k < 0 || sh->max_seqlen_q < 0)
+        return fail(PA_ERR_INVALID_ARG, "batch, total_q, total_k and max_seqlen_q must be >= 0");
+    if (B == 0 || sh->total_q == 0 || sh->max_seqlen_q == 0) return PA_OK;
+    if (Hq <= 0 || Hk <= 0 || Hq % Hk != 0)
+        return fail(PA_ERR_INVALID_ARG, "num_q_heads (%d) must be a positive multiple of num_kv_heads (%d)", Hq, Hk);
+    if (Hq > 65535) return fail(PA_ERR_UNSUPPORTED, "num_q_heads above 65535");
+    if (sh->dtype != PA_KV_BF16)
+        return fail(PA_ERR_UNSUPPORTED, "pa_prefill_mla_rope_fp8 needs dtype PA_KV_BF16 (got %d)", sh->dtype);
+    if (sh->head_dim_qk != 192 || sh->rope_dim != 64 || sh->head_dim_v != 128)
+        return fail(PA_ERR_UNSUPPORTED, "pa_prefill_mla_rope_fp8 needs head_dim_qk 192, rope_dim 64, head_dim_v 128");
+    if (sh->total_k <= 0) return fail(PA_ERR_INVALID_ARG, "ragged keys need total_k > 0");
+    if (!q || !k_nope || !v || !k_rope || !k_rope_scales || !cu_seqlens_q || !cu_seqlens_k || !out || !workspace)
+        return fail(PA_ERR_INVALID_ARG, "a required pointer is NULL");
+    if (!aligned16(q) || !aligned16(k_nope) || !aligned16(v) || !aligned16(k_rope) || !aligned16(out) ||
+        !aligned16(workspace))
+        return fail(PA_ERR_INVALID_ARG, "q, k_nope, v, k_rope, out and workspace must be 16-byte aligned");
+    if (reinterpret_cast<uintptr_t>(k_rope_scales) % 4 != 0)
+        return fail(PA_ERR_INVALID_ARG, "k_rope_scales must be 4-byte aligned");
+    if (!std::isfinite(scale)) return fail(PA_ERR_INVALID_ARG, "scale must be finite");
+    const size_t need = pa_prefill_mla_rope_fp8_workspace_size(sh);
+    if (workspace_bytes < need) return fail(PA_ERR_WORKSPACE, "workspace needs %zu bytes, got %zu", need, workspace_bytes);
+
+    uint8_t* ws = static_cast<uint8_t*>(workspace);
+    uint16_t* hi = reinterpret_cast<uint16_t*>(ws + rope_levels_offset(sh));
+    uint16_t* lo = reinterpret_cast<uint16_t*>(ws + rope_levels_offset(sh) + rope_level_bytes(sh));
+    CUtensorMap mq, mk, mv, mr, mrl;
+    const uint64_t tq = (uint64_t)sh->total_q, tk = (uint64_t)sh->total_k;
+    {
+        const uint64_t qd[3] = {192, (uint64_t)Hq, tq}, qs[2] = {384, (uint64_t)Hq * 384};
+        const uint64_t kd[3] = {128, (uint64_t)Hk, tk}, ks[2] = {256, (uint64_t)Hk * 256};
+        const uint32_t box[3] = {64, 1, 128};
+        const uint64_t rd[2] = {64, tk}, rs[1] = {128};
+        const uint32_t rb[2] = {64, 128};
+        pa_status st = make_map_bf16(&mq, q, 3, qd, qs, box);
+        if (st == PA_OK) st = make_map_bf16(&mk, k_nope, 3, kd, ks, box);
+        if (st == PA_OK) st = make_map_bf16(&mv, v, 3, kd, ks, box);
+        if (st == PA_OK) st = make_map_bf16(&mr, hi, 2, rd, rs, rb);
+        if (st == PA_OK) st = make_map_bf16(&mrl, lo, 2, rd, rs, rb);
+        if (st != PA_OK) return st;
+    }
+    pa::PrefillArgs a;
+    pa_status st = fill_prefill_args(sh, cu_seqlens_q, cu_seqlens_k, nullptr, qo_offset, causal, scale, out, lse,
+                                     workspace, workspace_bytes, false, &a);
+    if (st != PA_OK) return st;
+    a.r8 = 1;
+    cudaError_t e = pa::launch_rope_expand(static_cast<const uint8_t*>(k_rope), k_rope_scales, hi, lo, sh->total_k,
+                                           stream);
+    if (e != cudaSuccess) return cuda_fail(e, "rope key expansion launch");
+    e = pa::launch_prefill(a, 192, &mq, &mk, &mv, &mr, &mrl, stream);
+    if (e != cudaSuccess) return cuda_fail(e, "prefill launch");
+    return PA_OK;
 }
 
 pa_status pa_get_static_plan(const pa_decode_shapes* sh, pa_decode_plan* plan) {

@@ -68,11 +68,17 @@ struct PrefillArgs {
     int32_t causal, paged, rope;
     int32_t f16;  // q, k, v, k_rope and out are fp16, else bf16
     int32_t f8;   // MLA with e4m3 q_nope / k_nope and per-head scales
+    int32_t r8;   // MLA whose rope key arrives as bf16 hi + lo levels (from e4m3 codes and scales)
     const float* q_scale;  // f8: fp32 [Hq]
     const float* k_scale;  // f8: fp32 [Hk]
     float scale_log2;
     uint64_t wait_ns;
 };
+
+// e4m3 rope key codes [tokens, 64] times one fp32 scale per token -> two bf16
+// levels hi = bf16(x), lo = bf16(x - hi), each [tokens, 64]
+cudaError_t launch_rope_expand(const uint8_t* codes, const float* scales, uint16_t* hi, uint16_t* lo,
+                               int64_t tokens, cudaStream_t stream);
 
 cudaError_t launch_prefill(const PrefillArgs& a, int head_dim_qk, const CUtensorMap* map_q,
                            const CUtensorMap* map_k, const CUtensorMap* map_v, const CUtensorMap* map_r,

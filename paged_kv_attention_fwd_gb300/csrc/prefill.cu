@@ -29,6 +29,7 @@
 // _normalize_qo_offset / _resolve_seqused_k).  Every wait is bounded.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
+#include <cuda_fp8.h>
 
 #include "pa_internal.h"
 #include "pa_ptx.cuh"
@@ -65,11 +66,14 @@ constexpr int kPrefillDoneWord = 32;
 // (the rope part); a query row the same plus a third chunk: its rope part,
 // divided by the head's scale, is held as two bf16 levels hi + lo (chunks 1
 // and 2), so the division costs no precision.
-template <bool ROPE, bool F8>
+// R8 (MLA only): the rope key arrives as two bf16 levels, hi and lo, expanded
+// from e4m3 codes and per-token scales before the launch; a key row is the
+// two per-head chunks, then hi, then lo, and the query's rope chunk meets both.
+template <bool ROPE, bool F8, bool R8 = false>
 struct PrefillLayout {
     static constexpr int kDqk = ROPE ? 192 : 128;
     static constexpr int kQChunks = F8 ? 3 : kDqk / 64;
-    static constexpr int kKChunks = F8 ? 2 : kDqk / 64;
+    static constexpr int kKChunks = F8 ? 2 : kDqk / 64 + (R8 ? 1 : 0);
     static constexpr int kTile = 16384;                 // 128 rows x 128 bytes
     static constexpr int kQBytes = kQChunks * kTile;    // one 128-row query tile
     static constexpr int kKBytes = kKChunks * kTile;    // one 128-key K tile
@@ -93,6 +97,18 @@ __device__ __forceinline__ uint32_t pack16x2(float lo, float hi, bool f16) {
     }
     const __nv_bfloat162 b = __floats2bfloat162_rn(lo, hi);
     return *reinterpret_cast<const uint32_t*>(&b);
+}
+
+// the two values of a packed 16-bit pair (low half first): fp16 or bf16
+__device__ __forceinline__ void unpack16x2(uint32_t w, bool f16, float& lo, float& hi) {
+    if (f16) {
+        const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&w));
+        lo = f.x;
+        hi = f.y;
+    } else {
+        lo = __uint_as_float(w << 16);
+        hi = __uint_as_float(w & 0xFFFF0000u);
+    }
 }
 
 __device__ __forceinline__ float ex2(float x) {
@@ -168,13 +184,14 @@ __device__ __forceinline__ bool make_item(const PrefillArgs& a, int w, PItem& it
 // region until none is left.  Every barrier's phase runs on across items,
 // so the producer loads the next item's query and first K/V tiles while the
 // current item's last tiles and output are still in progress.
-template <bool ROPE, bool PAGED, bool F8>
+template <bool ROPE, bool PAGED, bool F8, bool R8>
 __global__ void __launch_bounds__(320, 1)
     prefill_kernel(const __grid_constant__ PrefillArgs a, const __grid_constant__ CUtensorMap map_q,
                    const __grid_constant__ CUtensorMap map_k, const __grid_constant__ CUtensorMap map_v,
                    const __grid_constant__ CUtensorMap map_r, const __grid_constant__ CUtensorMap map_qr) {
     static_assert(!F8 || (ROPE && !PAGED), "e4m3 query/key parts: MLA with ragged keys only");
-    using L = PrefillLayout<ROPE, F8>;
+    static_assert(!R8 || (ROPE && !PAGED && !F8), "two-level rope key: bf16 MLA with ragged keys only");
+    using L = PrefillLayout<ROPE, F8, R8>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     __shared__ __align__(8) uint64_t bars[P_COUNT];
@@ -305,6 +322,7 @@ __global__ void __launch_bounds__(320, 1)
                         for (int c = 0; c < 2; ++c)
                             tma_load_3d(kt + c * L::kTile, &map_k, kf, c * 64, kvh, sg.k0 + j * 128);
                         if (ROPE) tma_load_2d(kt + 2 * L::kTile, &map_r, kf, 0, sg.k0 + j * 128);
+                        if (R8) tma_load_2d(kt + 3 * L::kTile, &map_qr, kf, 0, sg.k0 + j * 128);  // rope lo level
                     }
                     k_loads = g + 1;
                     // V tile
@@ -379,6 +397,13 @@ __global__ void __launch_bounds__(320, 1)
                         const int c = kk >> 2, off = (kk & 3) * 32;
                         mma_ss(tbase + s_col(x), sdesc_sw128(qb + c * L::kTile + off, 16, 1024),
                                sdesc_sw128(kb + c * L::kTile + off, 16, 1024), idesc_qk, kk > 0);
+                    }
+                    if constexpr (R8) {
+                        // the query's rope chunk against the rope key's lo level
+#pragma unroll
+                        for (int kk = 0; kk < 4; ++kk)
+                            mma_ss(tbase + s_col(x), sdesc_sw128(qb + 2 * L::kTile + kk * 32, 16, 1024),
+                                   sdesc_sw128(kb + 3 * L::kTile + kk * 32, 16, 1024), idesc_qk, 1u);
                     }
                 }
                 mma_commit(&bars[P_SF + x]);
@@ -770,12 +795,12 @@ __global__ void __launch_bounds__(512) prefill_order_kernel(const PrefillArgs a,
     }
 }
 
-template <bool ROPE, bool PAGED, bool F8>
+template <bool ROPE, bool PAGED, bool F8, bool R8 = false>
 cudaError_t launch_t(const PrefillArgs& a, const CUtensorMap* mq, const CUtensorMap* mk, const CUtensorMap* mv,
                      const CUtensorMap* mr, const CUtensorMap* mqr, cudaStream_t stream) {
-    using L = PrefillLayout<ROPE, F8>;
+    using L = PrefillLayout<ROPE, F8, R8>;
     static std::atomic<uint64_t> configured{0};
-    cudaError_t e = ensure_dynamic_smem(prefill_kernel<ROPE, PAGED, F8>, L::kSmem, configured);
+    cudaError_t e = ensure_dynamic_smem(prefill_kernel<ROPE, PAGED, F8, R8>, L::kSmem, configured);
     if (e != cudaSuccess) return e;
     if (a.order) {
         prefill_order_kernel<<<1, 512, 0, stream>>>(a, const_cast<int32_t*>(a.order));
@@ -791,8 +816,38 @@ cudaError_t launch_t(const PrefillArgs& a, const CUtensorMap* mq, const CUtensor
     if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
     if (e != cudaSuccess) return e;
     const unsigned grid = (unsigned)(items < sms ? items : sms);
-    prefill_kernel<ROPE, PAGED, F8><<<grid, L::kThreads, L::kSmem, stream>>>(a, *mq, *mk, *mv, *mr, *mqr);
+    prefill_kernel<ROPE, PAGED, F8, R8><<<grid, L::kThreads, L::kSmem, stream>>>(a, *mq, *mk, *mv, *mr, *mqr);
     return cudaGetLastError();
+}
+
+// The e4m3 rope key times its token's scale as two bf16 levels, hi = bf16(x)
+// and lo = bf16(x - hi): about 16 significant bits together, against the 4 of
+// the code and the 24 of the scale (x itself is their fp32 product).  One
+// thread per 8 codes; a token's 64 codes are 8 such groups.
+__global__ void __launch_bounds__(256) rope_expand_kernel(const uint8_t* __restrict__ codes,
+                                                          const float* __restrict__ scales,
+                                                          uint16_t* __restrict__ hi, uint16_t* __restrict__ lo,
+                                                          int64_t groups) {
+    const int64_t gi = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    if (gi >= groups) return;
+    const float s = __ldg(&scales[gi >> 3]);
+    const uint2 c = __ldg(reinterpret_cast<const uint2*>(codes) + gi);
+    const uint32_t w[2] = {c.x, c.y};
+    uint32_t h[4], l[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {  // codes 2i, 2i + 1
+        const __half2_raw hr =
+            __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)((w[i >> 1] >> ((i & 1) * 16)) & 0xFFFFu), __NV_E4M3);
+        const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&hr));
+        const float x0 = f.x * s, x1 = f.y * s;
+        const uint32_t hb = pack16x2(x0, x1, false);
+        float h0, h1;
+        unpack16x2(hb, false, h0, h1);
+        h[i] = hb;
+        l[i] = pack16x2(x0 - h0, x1 - h1, false);
+    }
+    reinterpret_cast<uint4*>(hi)[gi] = make_uint4(h[0], h[1], h[2], h[3]);
+    reinterpret_cast<uint4*>(lo)[gi] = make_uint4(l[0], l[1], l[2], l[3]);
 }
 
 }  // namespace
@@ -801,9 +856,20 @@ cudaError_t launch_prefill(const PrefillArgs& a, int head_dim_qk, const CUtensor
                            const CUtensorMap* mv, const CUtensorMap* mr, const CUtensorMap* mqr,
                            cudaStream_t stream) {
     if (a.f8) return launch_t<true, false, true>(a, mq, mk, mv, mr, mqr, stream);
+    if (a.r8) return launch_t<true, false, false, true>(a, mq, mk, mv, mr, mqr, stream);
     if (head_dim_qk == 192) return launch_t<true, false, false>(a, mq, mk, mv, mr, mqr, stream);
     return a.paged ? launch_t<false, true, false>(a, mq, mk, mv, mr, mqr, stream)
                    : launch_t<false, false, false>(a, mq, mk, mv, mr, mqr, stream);
+}
+
+cudaError_t launch_rope_expand(const uint8_t* codes, const float* scales, uint16_t* hi, uint16_t* lo,
+                               int64_t tokens, cudaStream_t stream) {
+    const int64_t groups = tokens * 8;
+    if (groups <= 0) return cudaSuccess;
+    const int64_t blocks = (groups + 255) / 256;
+    if (blocks > 0x7FFFFFFFLL) return cudaErrorInvalidValue;
+    rope_expand_kernel<<<(unsigned)blocks, 256, 0, stream>>>(codes, scales, hi, lo, groups);
+    return cudaGetLastError();
 }
 
 }  // namespace pa

@@ -106,6 +106,26 @@ def prefill_mla_fp8(inp, device, causal: bool = True, qo_offset=None, stream=Non
     return out, lse, ws, sh
 
 
+def prefill_mla_rope_fp8(inp, device, causal: bool = True, qo_offset=None, stream=None):
+    """pa_prefill_mla_rope_fp8 on an ``MlaRopeE4m3Inputs`` batch (host arrays
+    copied to ``device``).  Returns (out bf16, lse fp32, workspace, shapes)."""
+    dev = torch.device(device)
+    t8 = lambda a: torch.from_numpy(np.ascontiguousarray(a)).to(dev)
+    sh = B.pa_prefill_shapes(batch=inp.batch, num_q_heads=inp.num_q_heads, num_kv_heads=inp.num_kv_heads,
+                             head_dim_qk=192, head_dim_v=128, rope_dim=64, max_seqlen_q=inp.max_seqlen_q,
+                             total_q=int(inp.cu_seqlens_q[-1]), total_k=int(inp.cu_seqlens_k[-1]), page_size=64,
+                             max_pages_per_seq=0, num_pool_pages=0, num_sms=num_sms(dev), dtype=B.PA_KV_BF16)
+    out = torch.empty((sh.total_q, sh.num_q_heads, 128), dtype=torch.bfloat16, device=dev)
+    lse = torch.empty((sh.total_q, sh.num_q_heads), dtype=torch.float32, device=dev)
+    ws = torch.zeros(B.pa_prefill_mla_rope_fp8_workspace_size(sh), dtype=torch.uint8, device=dev)
+    qo = qo_offset if qo_offset is not None else inp.qo_offset
+    B.pa_prefill_mla_rope_fp8(sh, as_bf16(inp.q, dev), as_bf16(inp.k_nope, dev), as_bf16(inp.v, dev),
+                              t8(inp.k_rope), t8(inp.k_rope_scales), t8(inp.cu_seqlens_q), t8(inp.cu_seqlens_k),
+                              None if qo is None else t8(np.asarray(qo, np.int32)), causal, inp.scale, out, lse, ws,
+                              stream=stream)
+    return out, lse, ws, sh
+
+
 def prefill(sh: B.pa_prefill_shapes, q, k, v, cu_seqlens_q, cu_seqlens_k, scale: float, causal: bool = True,
             block_table=None, k_rope=None, qo_offset=None, out=None, lse=None, workspace=None, stream=None):
     dev = q.device

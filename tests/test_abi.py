@@ -214,3 +214,39 @@ def test_mixed_plan_rejects_e4m3_pools():
     with pytest.raises(B.PaError) as e:
         B.pa_get_mixed_plan(np.array([0, 1, 30], np.int32), np.array([5, 90], np.int32), None, sh)
     assert e.value.status == B.PA_ERR_UNSUPPORTED and "pools" in str(e.value)
+
+
+def _mla_rope_fp8_shapes(**over):
+    d = dict(batch=2, num_q_heads=8, num_kv_heads=8, head_dim_qk=192, head_dim_v=128, rope_dim=64,
+             max_seqlen_q=100, total_q=150, total_k=150, page_size=64, max_pages_per_seq=0, num_pool_pages=0,
+             num_sms=152, dtype=B.PA_KV_BF16)
+    d.update(over)
+    return B.pa_prefill_shapes(**d)
+
+
+def test_prefill_mla_rope_fp8_workspace_size():
+    sh = _mla_rope_fp8_shapes()
+    base = B.pa_prefill_workspace_size(sh)
+    # pa_prefill's workspace rounded up to 256, then two rope levels of 150 * 128 bytes, each rounded up to 256
+    assert B.pa_prefill_mla_rope_fp8_workspace_size(sh) == (base + 255) // 256 * 256 + 2 * ((150 * 128 + 255) // 256 * 256)
+
+
+@pytest.mark.parametrize("over,args,status,needle", [
+    ({"dtype": B.PA_KV_FP8_E4M3}, {}, B.PA_ERR_UNSUPPORTED, "PA_KV_BF16"),
+    ({"head_dim_qk": 128, "rope_dim": 0}, {}, B.PA_ERR_UNSUPPORTED, "192"),
+    ({"num_q_heads": 6, "num_kv_heads": 4}, {}, B.PA_ERR_INVALID_ARG, "multiple"),
+    ({"total_k": 0}, {}, B.PA_ERR_INVALID_ARG, "total_k"),
+    ({}, {"k_rope_scales": None}, B.PA_ERR_INVALID_ARG, "NULL"),
+    ({}, {"k_rope": _Fake(addr=(1 << 20) + 8)}, B.PA_ERR_INVALID_ARG, "aligned"),
+    ({}, {"k_rope_scales": _Fake(addr=(1 << 20) + 2)}, B.PA_ERR_INVALID_ARG, "4-byte"),
+    ({}, {"scale": float("nan")}, B.PA_ERR_INVALID_ARG, "finite"),
+    ({}, {"workspace": _Fake(n=4096)}, B.PA_ERR_WORKSPACE, "workspace"),
+])
+def test_prefill_mla_rope_fp8_host_validation(over, args, status, needle):
+    f = _Fake(n=1 << 20)
+    kw = dict(q=f, k_nope=f, v=f, k_rope=f, k_rope_scales=f, cu_seqlens_q=f, cu_seqlens_k=f, qo_offset=None,
+              causal=True, scale=0.07, out=f, lse=None, workspace=f)
+    kw.update(args)
+    with pytest.raises(B.PaError) as e:
+        B.pa_prefill_mla_rope_fp8(_mla_rope_fp8_shapes(**over), stream=1, **kw)
+    assert e.value.status == status and needle in str(e.value)
