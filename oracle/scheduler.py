@@ -134,3 +134,33 @@ def static_split_capacity(batch: int, num_kv_heads: int, num_sms: int, ctas_per_
         return batch * min(forced_splits, MAX_SPLITS)
     cap = num_sms * ctas_per_sm
     return batch + _cdiv(ITEMS_PER_SHARE * cap, num_kv_heads)
+
+
+def page_table_from_flat(kv_indices, kv_lens, page_size=64, columns=None):
+    """Block table from a flat list of page ids (MATE msa_interface,
+    _build_page_table_from_flat_kv_indices, with _page_counts): sequence b owns
+    the next ceil(kv_lens[b] / page_size) ids of the list, in order, in the first
+    columns of its row; every other entry is 0.  columns defaults to the largest
+    page count (the page's table width).  Raises ValueError when the list does
+    not hold exactly the implied number of ids, a length is negative, or a row
+    does not fit in ``columns``.  Plain loops: test infrastructure only."""
+    if page_size <= 0:
+        raise ValueError("page_size must be positive")
+    counts = []
+    for n in kv_lens:
+        n = int(n)
+        if n < 0:
+            raise ValueError("kv_lens must be >= 0")
+        counts.append((n + page_size - 1) // page_size)
+    if len(kv_indices) != sum(counts):
+        raise ValueError("kv_indices does not match the page count implied by kv_lens")
+    width = max(counts, default=0) if columns is None else int(columns)
+    table = [[0] * width for _ in counts]
+    start = 0
+    for b, c in enumerate(counts):
+        if c > width:
+            raise ValueError("a sequence has more pages than the table has columns")
+        for j in range(c):
+            table[b][j] = int(kv_indices[start + j])
+        start += c
+    return table

@@ -6,6 +6,7 @@ import numpy as np
 import pytest
 
 from oracle import scheduler as S
+from paged_kv_attention_fwd_gb300 import workloads as W
 
 GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
 
@@ -119,3 +120,34 @@ def test_static_capacity_bounds_every_length_mix(hk, sms, cps, forced):
             lens = rng.integers(0, 300, size=B)
         u = S.unpack(S.schedule(lens.tolist(), hk, sms, cps, forced))
         assert u["total_splits"] <= bound
+
+
+# ---------------------------------------------------------------- block table from a flat page list
+
+def test_page_table_from_flat_matches_the_hand_worked_fixture():
+    lines = [l for l in open(os.path.join(GOLDEN, "page_table_from_flat.txt")) if l.strip()]
+    lens = [int(x) for x in next(l for l in lines if l.startswith("# kv_lens:")).split(":")[1].split()]
+    idx = [int(x) for x in next(l for l in lines if l.startswith("# kv_indices:")).split(":")[1].split()]
+    rows = [[int(x) for x in l.split()] for l in lines if not l.startswith("#")]
+    assert S.page_table_from_flat(idx, lens) == rows
+
+
+def test_page_table_from_flat_round_trips_generated_block_tables():
+    """Flattening the live entries of a generated block table row by row and
+    rebuilding gives the table back (its unused entries are 0), for lengths with
+    empty sequences and exact page multiples."""
+    lens = np.array([0, 1, 63, 64, 65, 128, 1000, 4096, 7], np.int32)
+    inp = W.make_decode(len(lens), 8, 8, 64, lens, seed=3)
+    bt = inp.block_table
+    flat = [int(bt[b, j]) for b in range(len(lens)) for j in range((int(lens[b]) + 63) // 64)]
+    got = np.array(S.page_table_from_flat(flat, lens, columns=bt.shape[1]), np.int32)
+    assert np.array_equal(got, bt)
+
+
+def test_page_table_from_flat_rejects_mismatched_lists():
+    with pytest.raises(ValueError):
+        S.page_table_from_flat([1, 2], [65, 1])   # 3 pages implied
+    with pytest.raises(ValueError):
+        S.page_table_from_flat([], [-5])
+    with pytest.raises(ValueError):
+        S.page_table_from_flat([1, 2, 3], [130], columns=2)
