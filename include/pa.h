@@ -230,6 +230,29 @@ pa_status pa_decode_noalloc(const pa_decode_shapes* shapes, const pa_decode_plan
                             const int32_t* block_table, const int32_t* seq_lens, const int32_t* meta_dev,
                             float scale, void* out, float* lse, int32_t* status_host, cudaStream_t stream);
 
+/*
+ * pa_page_table_from_flat -- block table rows from a flat list of page ids, on
+ * the device (MATE msa_interface, _build_page_table_from_flat_kv_indices, page
+ * counts as in _page_counts).  Sequence b owns the next ceil(kv_lens[b] / 64)
+ * ids of kv_indices, in order; they fill the first columns of row b of
+ * block_table and every other entry of the row is written 0.  Capture-safe:
+ * no allocation, no synchronisation, lengths read on the device, so a CUDA
+ * graph can replay it with new lengths and ids.
+ *   kv_indices  int32 [num_indices] (device; may be NULL when num_indices is 0)
+ *   kv_lens     int32 [batch] (device)
+ *   block_table int32 [batch, max_pages_per_seq] (device, written in full)
+ *   workspace   >= PA_STATUS_BYTES device bytes (status word), zero-filled once
+ * Host checks: 1 <= batch <= 8192, max_pages_per_seq > 0, num_indices >= 0,
+ * pointers.  Device checks, recorded as PA_ERR_DEVICE_BOUNDS in the status
+ * word (pa_check_status): a negative length (counted as 0 pages), a sequence
+ * with more pages than max_pages_per_seq (its row keeps its first ids), or a
+ * list whose length differs from the page total the lengths imply (ids past
+ * num_indices are not read; their entries are 0).
+ */
+pa_status pa_page_table_from_flat(const int32_t* kv_indices, int64_t num_indices, const int32_t* kv_lens,
+                                  int32_t batch, int32_t max_pages_per_seq, int32_t* block_table, void* workspace,
+                                  size_t workspace_bytes, cudaStream_t stream);
+
 /* ----------------------------------------------------------------- prefill */
 
 typedef struct {

@@ -100,6 +100,8 @@ def lib() -> ctypes.CDLL:
         L.pa_prefill_mla_rope_fp8.restype = ctypes.c_int
         L.pa_prefill_mla_rope_fp8_workspace_size.argtypes = [ctypes.POINTER(pa_prefill_shapes)]
         L.pa_prefill_mla_rope_fp8_workspace_size.restype = ctypes.c_size_t
+        L.pa_page_table_from_flat.argtypes = [_P, ctypes.c_int64, _P, ctypes.c_int32, ctypes.c_int32, _P, _P, sz, _P]
+        L.pa_page_table_from_flat.restype = ctypes.c_int
         L.pa_get_static_plan.argtypes = [ctypes.POINTER(pa_decode_shapes), ctypes.POINTER(pa_decode_plan)]
         L.pa_get_static_plan.restype = ctypes.c_int
         L.pa_get_metadata_device.argtypes = [ctypes.POINTER(pa_decode_shapes), ctypes.POINTER(pa_decode_plan), _P, _P,
@@ -253,6 +255,15 @@ def pa_prefill_mla_rope_fp8(shapes: pa_prefill_shapes, q, k_nope, v, k_rope, k_r
 
 def pa_prefill_mla_rope_fp8_workspace_size(shapes: pa_prefill_shapes) -> int:
     return int(lib().pa_prefill_mla_rope_fp8_workspace_size(ctypes.byref(shapes)))
+
+
+def pa_page_table_from_flat(kv_indices, num_indices: int, kv_lens, batch: int, max_pages_per_seq: int, block_table,
+                            workspace, workspace_bytes: Optional[int] = None, stream=None) -> None:
+    if workspace_bytes is None:
+        workspace_bytes = workspace.numel() * workspace.element_size()
+    _check(lib().pa_page_table_from_flat(_ptr(kv_indices), int(num_indices), _ptr(kv_lens), int(batch),
+                                         int(max_pages_per_seq), _ptr(block_table), _ptr(workspace),
+                                         int(workspace_bytes), _stream(stream)))
 
 
 def pa_get_static_plan(shapes: pa_decode_shapes) -> pa_decode_plan:

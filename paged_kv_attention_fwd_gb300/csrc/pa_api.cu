@@ -752,6 +752,25 @@ pa_status pa_prefill_mla_fp8(const pa_prefill_shapes* sh, const void* q_nope, co
     return PA_OK;
 }
 
+pa_status pa_page_table_from_flat(const int32_t* kv_indices, int64_t num_indices, const int32_t* kv_lens,
+                                  int32_t batch, int32_t max_pages_per_seq, int32_t* block_table, void* workspace,
+                                  size_t workspace_bytes, cudaStream_t stream) {
+    if (batch <= 0 || batch > pa::kMaxBatch)
+        return fail(PA_ERR_UNSUPPORTED, "batch must be in [1, %d] (got %d)", pa::kMaxBatch, batch);
+    if (max_pages_per_seq <= 0) return fail(PA_ERR_INVALID_ARG, "max_pages_per_seq must be positive");
+    if ((int64_t)batch * max_pages_per_seq >= ((int64_t)1 << 40))
+        return fail(PA_ERR_UNSUPPORTED, "batch * max_pages_per_seq is too large");
+    if (num_indices < 0) return fail(PA_ERR_INVALID_ARG, "num_indices must be >= 0");
+    if ((num_indices > 0 && !kv_indices) || !kv_lens || !block_table || !workspace)
+        return fail(PA_ERR_INVALID_ARG, "a required pointer is NULL");
+    if (workspace_bytes < PA_STATUS_BYTES)
+        return fail(PA_ERR_WORKSPACE, "workspace needs %d bytes, got %zu", PA_STATUS_BYTES, workspace_bytes);
+    cudaError_t e = pa::launch_page_table(kv_indices, num_indices, kv_lens, batch, max_pages_per_seq, block_table,
+                                          static_cast<int*>(workspace), stream);
+    if (e != cudaSuccess) return cuda_fail(e, "page table launch");
+    return PA_OK;
+}
+
 size_t pa_prefill_workspace_size(const pa_prefill_shapes* sh) {
     if (!sh || sh->batch <= 0 || sh->max_seqlen_q <= 0) return PA_STATUS_BYTES;
     return PA_STATUS_BYTES + (size_t)sh->batch * (size_t)cdiv(sh->max_seqlen_q, 256) * 4;
@@ -834,7 +853,8 @@ pa_status pa_prefill_mla_rope_fp8(const pa_prefill_shapes* sh, const void* q, co
 pa_status pa_get_static_plan(const pa_decode_shapes* sh, pa_decode_plan* plan) {
     if (!sh || !plan) return fail(PA_ERR_INVALID_ARG, "shapes and plan must not be NULL");
     const int B = sh->batch, Hk = sh->num_kv_heads;
-    if (B <= 0 || B > 8192) return fail(PA_ERR_UNSUPPORTED, "device scheduling needs 1 <= batch <= 8192 (got %d)", B);
+    if (B <= 0 || B > pa::kMaxBatch)
+        return fail(PA_ERR_UNSUPPORTED, "device scheduling needs 1 <= batch <= %d (got %d)", pa::kMaxBatch, B);
     if (Hk <= 0 || Hk > 65535) return fail(PA_ERR_INVALID_ARG, "num_kv_heads must be in [1, 65535] (got %d)", Hk);
     if (sh->page_size != pa::kPage) return fail(PA_ERR_INVALID_ARG, "page_size must be 64 (got %d)", sh->page_size);
     if (sh->max_pages_per_seq <= 0) return fail(PA_ERR_INVALID_ARG, "max_pages_per_seq must be positive");

@@ -101,7 +101,11 @@ struct AppendArgs {
 cudaError_t launch_append(const AppendArgs& a, cudaStream_t stream);
 
 // Device-side scheduler (schedule.cu)
+constexpr int kMaxBatch = 8192;  // sequences the device-side metadata handles
 size_t schedule_smem_bytes(int B, int p2cap);
+// block table rows from a flat list of page ids (pa_page_table_from_flat)
+cudaError_t launch_page_table(const int32_t* kv_indices, int64_t num_indices, const int32_t* kv_lens, int B,
+                              int max_pages, int32_t* block_table, int* status, cudaStream_t stream);
 cudaError_t launch_schedule(const int32_t* seq_lens, int B, int Hk, int max_pages, int cps, int cap, int forced,
                             int p2cap, int32_t* meta, cudaStream_t stream);
 

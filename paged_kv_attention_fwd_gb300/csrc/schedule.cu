@@ -7,6 +7,8 @@
 // then grid-1..0, ...) instead of least-loaded-first, which is sequential.
 // One CTA of 1024 threads; shared memory holds the sort keys and the
 // per-sequence page counts, split counts and split offsets.
+#include <algorithm>
+
 #include "pa_internal.h"
 
 namespace pa {
@@ -167,6 +169,73 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
 }
 
+// Block table rows from a flat list of page ids (MATE msa_interface,
+// _build_page_table_from_flat_kv_indices, page counts as in _page_counts):
+// sequence b owns the next ceil(kv_lens[b] / 64) ids of the list, in order, in
+// the first columns of its row; every other entry is 0.  Every CTA scans the
+// page counts into shared memory (int64 starts, one thread per contiguous run
+// of sequences), then the grid fills the table with coalesced stores; CTA 0
+// checks the list against the counts.
+constexpr int kPtThreads = 1024;
+
+__global__ void __launch_bounds__(kPtThreads) page_table_kernel(const int32_t* __restrict__ kv_indices,
+                                                                int64_t num_indices, const int32_t* __restrict__ kv_lens,
+                                                                int B, int max_pages, int32_t* __restrict__ bt,
+                                                                int* status) {
+    extern __shared__ long long start[];  // [B + 1]
+    __shared__ long long warp_sum[kPtThreads / 32];
+    const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
+    const int per = (B + kPtThreads - 1) / kPtThreads;
+    const int b0 = min(B, t * per), b1 = min(B, b0 + per);
+    bool bad = false;
+    long long mine = 0;
+    for (int b = b0; b < b1; ++b) {
+        const int len = __ldg(&kv_lens[b]);
+        bad |= len < 0;
+        const long long c = len > 0 ? ((long long)len + kPage - 1) / kPage : 0;
+        bad |= c > max_pages;
+        mine += c;
+    }
+    // exclusive scan of the per-thread totals
+    long long x = mine;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const long long y = __shfl_up_sync(0xffffffffu, x, o);
+        if (lane >= o) x += y;
+    }
+    if (lane == 31) warp_sum[warp] = x;
+    __syncthreads();
+    if (warp == 0) {
+        long long w = warp_sum[lane];
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const long long y = __shfl_up_sync(0xffffffffu, w, o);
+            if (lane >= o) w += y;
+        }
+        warp_sum[lane] = w;  // inclusive over warps
+    }
+    __syncthreads();
+    long long run = x - mine + (warp > 0 ? warp_sum[warp - 1] : 0);
+    for (int b = b0; b < b1; ++b) {
+        start[b] = run;
+        const int len = __ldg(&kv_lens[b]);
+        run += len > 0 ? ((long long)len + kPage - 1) / kPage : 0;
+    }
+    if (t == kPtThreads - 1) start[B] = warp_sum[31];
+    __syncthreads();
+    if (blockIdx.x == 0) {
+        const bool any_bad = __syncthreads_or(bad) || start[B] != num_indices;
+        if (t == 0 && any_bad) atomicCAS(status, 0, PA_ERR_DEVICE_BOUNDS);
+    }
+    const long long total = (long long)B * max_pages;
+    for (long long e = (long long)blockIdx.x * kPtThreads + t; e < total; e += (long long)gridDim.x * kPtThreads) {
+        const int b = (int)(e / max_pages), c = (int)(e - (long long)b * max_pages);
+        const long long src = start[b] + c;
+        const bool live = c < start[b + 1] - start[b] && src < num_indices;
+        bt[e] = live ? __ldg(&kv_indices[src]) : 0;
+    }
+}
+
 }  // namespace
 
 size_t schedule_smem_bytes(int B, int p2cap) { return (size_t)p2cap * 8 + (size_t)(3 * B + 1) * 4; }
@@ -174,13 +243,25 @@ size_t schedule_smem_bytes(int B, int p2cap) { return (size_t)p2cap * 8 + (size_
 cudaError_t launch_schedule(const int32_t* seq_lens, int B, int Hk, int max_pages, int cps, int cap, int forced,
                             int p2cap, int32_t* meta, cudaStream_t stream) {
     const size_t smem = schedule_smem_bytes(B, p2cap);
-    static size_t configured = 0;
-    if (smem > 48 * 1024 && smem > configured) {
-        cudaError_t e = cudaFuncSetAttribute(schedule_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-        if (e != cudaSuccess) return e;
-        configured = smem;
-    }
+    // the attribute is per kernel and device: set it once per device, to the
+    // largest size the host checks allow (16384 items, 8192 sequences)
+    static std::atomic<uint64_t> configured{0};
+    cudaError_t e = ensure_dynamic_smem(schedule_kernel, (int)schedule_smem_bytes(kMaxBatch, 16384), configured);
+    if (e != cudaSuccess) return e;
     schedule_kernel<<<1, kThreads, smem, stream>>>(seq_lens, B, Hk, max_pages, cps, cap, forced, p2cap, meta);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_page_table(const int32_t* kv_indices, int64_t num_indices, const int32_t* kv_lens, int B,
+                              int max_pages, int32_t* block_table, int* status, cudaStream_t stream) {
+    static std::atomic<uint64_t> configured{0};
+    cudaError_t e = ensure_dynamic_smem(page_table_kernel, (int)((kMaxBatch + 1) * sizeof(long long)), configured);
+    if (e != cudaSuccess) return e;
+    const long long total = (long long)B * max_pages;
+    const long long want = (total + 8 * kPtThreads - 1) / (8 * kPtThreads);
+    const unsigned grid = (unsigned)std::max(1LL, std::min(want, 256LL));
+    page_table_kernel<<<grid, kPtThreads, (size_t)(B + 1) * sizeof(long long), stream>>>(
+        kv_indices, num_indices, kv_lens, B, max_pages, block_table, status);
     return cudaGetLastError();
 }
 

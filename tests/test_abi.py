@@ -250,3 +250,20 @@ def test_prefill_mla_rope_fp8_host_validation(over, args, status, needle):
     with pytest.raises(B.PaError) as e:
         B.pa_prefill_mla_rope_fp8(_mla_rope_fp8_shapes(**over), stream=1, **kw)
     assert e.value.status == status and needle in str(e.value)
+
+
+@pytest.mark.parametrize("args,status,needle", [
+    ({"batch": 0}, B.PA_ERR_UNSUPPORTED, "batch"),
+    ({"batch": 8193}, B.PA_ERR_UNSUPPORTED, "batch"),
+    ({"max_pages_per_seq": 0}, B.PA_ERR_INVALID_ARG, "max_pages_per_seq"),
+    ({"num_indices": -1}, B.PA_ERR_INVALID_ARG, "num_indices"),
+    ({"kv_lens": None}, B.PA_ERR_INVALID_ARG, "NULL"),
+    ({"workspace": _Fake(n=16)}, B.PA_ERR_WORKSPACE, "workspace"),
+])
+def test_page_table_from_flat_host_validation(args, status, needle):
+    f = _Fake()
+    kw = dict(kv_indices=f, num_indices=10, kv_lens=f, batch=4, max_pages_per_seq=8, block_table=f, workspace=f)
+    kw.update(args)
+    with pytest.raises(B.PaError) as e:
+        B.pa_page_table_from_flat(stream=1, **kw)
+    assert e.value.status == status and needle in str(e.value)
