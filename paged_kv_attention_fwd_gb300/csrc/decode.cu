@@ -22,9 +22,13 @@
 //               output accumulates in registers with the usual rescale
 //   warps 6-9   (e4m3 only) convert e4m3 pages to f16 operand tiles (exact)
 //
+// (e4m3 pages at D = 128 take decode_f8_kernel below: no conversion pass, QK
+// and PV issued from two warps, separate K and V rings.)
+//
 // Items whose sequence has more than one split write fp32 partials (output
-// normalised by its own sum, plus its log-sum-exp); combine_kernel merges
-// them.  Every wait is bounded; a timeout raises the CTA's abort flag,
+// normalised by its own sum, plus its log-sum-exp); the last warp merges a
+// sequence's splits as soon as they are all written (pa_decode), or
+// combine_kernel does afterwards.  Every wait is bounded; a timeout raises the CTA's abort flag,
 // records PA_ERR_TIMEOUT, drains in-flight copies and MMAs, frees TMEM and
 // returns.
 #include <cuda_bf16.h>

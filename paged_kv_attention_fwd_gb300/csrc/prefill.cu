@@ -5,12 +5,16 @@
 // and the MLA shape whose 64-wide rope key is shared by all heads (Modular
 // flare_mla_prefill: q depth 192 = 128 per-head + 64 shared, output depth 128),
 // also with the per-head parts of q and k in e4m3 (its overload with q_nope,
-// q_rope, q_scale and k_scales; one fp32 scale per head).
+// q_rope, q_scale and k_scales; one fp32 scale per head) or with the rope key
+// in e4m3 (its overload with k_rope_scales; one fp32 scale per key token,
+// expanded beforehand into two bf16 levels).
 //
-// One CTA per (segment b, 256-row query block, query head h): two 128-row
-// query tiles A and B that share every K/V tile.
+// Work item: (segment b, 256-row query block, query head h), two 128-row
+// query tiles A and B that share every K/V tile.  Persistent: one CTA per SM
+// takes items from a counter until none is left.
 //
-//   warp 0     producer: TMA of the two query tiles once, then 128-key K and
+//   warp 0     producer: takes the items and publishes them to the other
+//              warps, TMA of each item's two query tiles, then 128-key K and
 //              V tiles into separate rings (paged: two 64-row page slabs per
 //              tile through block_table; ragged: 3-D boxes over [T, H, D])
 //   warp 1     MMA issuer (tcgen05, fp32 accumulators in TMEM, 512 columns):
@@ -22,7 +26,9 @@
 //              per thread (its TMEM lane), row max and sum without any
 //              cross-thread exchange; P (bf16) is stored over the S columns;
 //              O is rescaled in TMEM only when the running max grows by more
-//              than 2^8 (otherwise the stale max stays exact and cheaper)
+//              than 2^8 (otherwise the stale max stays exact and cheaper);
+//              the query tile that takes an item's last K/V tile first zeroes
+//              that tile's dead V rows
 //
 // Query row i of segment b sees key j iff j < kv_len and (not causal or
 // j <= qo_offset + i), qo_offset defaulting to kv_len - q_len (MATE
