@@ -118,21 +118,59 @@ __global__ void __launch_bounds__(kThreads, 1)
         key[i] = k;
     }
     __syncthreads();
+    // Bitonic sort.  The keys are unique, so the sorted order is too and any
+    // sorting network reproduces the host rule's order.  Thread t holds the
+    // keys at positions k * kThreads + t in registers; the stages whose
+    // partner (position ^ stride) lies in the same warp run as shuffles with no
+    // barrier, the others through shared memory.
+    constexpr int kMaxPer = 16;  // 16384 items / kThreads
+    const int per = p2 > kThreads ? p2 / kThreads : 1;
+    unsigned long long kr[kMaxPer];
+#pragma unroll
+    for (int k = 0; k < kMaxPer; ++k) {
+        const int pos = k * kThreads + threadIdx.x;
+        kr[k] = (k < per && pos < p2) ? key[pos] : ~0ull;
+    }
     for (int size = 2; size <= p2; size <<= 1) {
         for (int stride = size >> 1; stride > 0; stride >>= 1) {
-            for (int t = threadIdx.x; t < p2 / 2; t += kThreads) {
-                const int lo = 2 * stride * (t / stride) + (t % stride);
-                const int hi = lo + stride;
-                const bool up = (lo & size) == 0;
-                const unsigned long long x = key[lo], y = key[hi];
-                if ((x > y) == up) {
-                    key[lo] = y;
-                    key[hi] = x;
+            if (stride < 32) {
+#pragma unroll
+                for (int k = 0; k < kMaxPer; ++k) {
+                    if (k >= per) break;
+                    const int pos = k * kThreads + threadIdx.x;
+                    const unsigned long long other = __shfl_xor_sync(0xffffffffu, kr[k], stride);
+                    const bool keep_min = ((pos & stride) == 0) == ((pos & size) == 0);
+                    kr[k] = keep_min ? min(kr[k], other) : max(kr[k], other);
                 }
+            } else {
+#pragma unroll
+                for (int k = 0; k < kMaxPer; ++k) {
+                    if (k >= per) break;
+                    const int pos = k * kThreads + threadIdx.x;
+                    if (pos < p2) key[pos] = kr[k];
+                }
+                __syncthreads();
+#pragma unroll
+                for (int k = 0; k < kMaxPer; ++k) {
+                    if (k >= per) break;
+                    const int pos = k * kThreads + threadIdx.x;
+                    if (pos < p2) {
+                        const unsigned long long other = key[pos ^ stride];
+                        const bool keep_min = ((pos & stride) == 0) == ((pos & size) == 0);
+                        kr[k] = keep_min ? min(kr[k], other) : max(kr[k], other);
+                    }
+                }
+                __syncthreads();
             }
-            __syncthreads();
         }
     }
+#pragma unroll
+    for (int k = 0; k < kMaxPer; ++k) {
+        if (k >= per) break;
+        const int pos = k * kThreads + threadIdx.x;
+        if (pos < p2) key[pos] = kr[k];
+    }
+    __syncthreads();
     // packed metadata: header, n_splits, split_indptr, cta_indptr, items
     if (threadIdx.x == 0) {
         meta[0] = kMetaMagic;

@@ -40,7 +40,7 @@ def device_meta(sh, lens):
     return plan, meta
 
 
-@pytest.mark.parametrize("case", ["uniform", "lognormal", "forced", "edges", "single"])
+@pytest.mark.parametrize("case", ["uniform", "lognormal", "forced", "edges", "single", "large"])
 def test_device_schedule_bit_exact(case):
     rng = np.random.default_rng(hash(case) % 1000)
     if case == "uniform":
@@ -51,8 +51,10 @@ def test_device_schedule_bit_exact(case):
         lens, hk, forced, mp = rng.integers(0, 3000, 40), 4, 7, 64
     elif case == "edges":
         lens, hk, forced, mp = np.array([0, 1, 63, 64, 65, 128, 129, 4096, 0, 5000]), 2, 0, 100
-    else:
+    elif case == "single":
         lens, hk, forced, mp = np.array([1]), 1, 0, 1
+    else:  # "large": ~14700 items, the sort's 16 keys per thread
+        lens, hk, forced, mp = rng.integers(0, 2001, 1800), 8, 0, 32
     lens = lens.astype(np.int32)
     sh = shapes(len(lens), hk * 2, hk, mp, 10 ** 6, forced)
     plan, meta = device_meta(sh, lens)
