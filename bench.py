@@ -207,6 +207,14 @@ def decode_workload(name):
         inp = W.gqa_decode(0)
         desc = ("batched GQA decode: B=64, Hq=32, Hk=8, D=128, bf16 KV, page 64, q_len 1, "
                 "seq_lens uniform[1,4096], seed 0")
+    elif name == "decode_gqa_fp16":
+        inp = W.gqa_decode(0, kv_dtype="f16")
+        desc = ("batched GQA decode, fp16 q / KV / out: B=64, Hq=32, Hk=8, D=128, page 64, q_len 1, "
+                "seq_lens uniform[1,4096], seed 0")
+    elif name == "decode_gqa_graph":
+        inp = W.gqa_decode(0)
+        desc = ("batched GQA decode (B=64, Hq=32, Hk=8, D=128, bf16, seq_lens uniform[1,4096], seed 0) as one "
+                "CUDA-graph replay per step: metadata written on the device from device seq_lens, then decode")
     elif name == "decode_fp8":
         inp = W.fp8_long_decode(0)
         desc = ("long-context decode, e4m3 KV with per-KV-head fp32 scales: B=128, Hq=64, Hk=8, D=128, page 64, "
@@ -220,7 +228,7 @@ def decode_workload(name):
 
 
 def kv_bytes(inp):
-    el = 2 if inp.kv_dtype == "bf16" else 1
+    el = 1 if inp.kv_dtype == "e4m3" else 2
     pages = sum((int(s) + 63) // 64 for s in inp.seq_lens)
     full = pages * 64 * inp.num_kv_heads * inp.head_dim * el * 2
     exact = int(np.sum(inp.seq_lens)) * inp.num_kv_heads * inp.head_dim * el * 2
@@ -233,6 +241,15 @@ def prefill_workload(name):
         inp = W.chunked_prefill(0)
         desc = ("chunked causal prefill against the paged cache: B=8, H=32 (Hq=Hk), D=128, page 64, q_len 512 "
                 "after a cached prefix U[0,8192], qo_offset = kv_len - q_len, seed 0")
+    elif name == "prefill_paged_fp16":
+        inp = W.chunked_prefill(0, dtype="f16")
+        desc = ("chunked causal prefill against the paged cache, fp16 q / K / V / out: B=8, H=32, D=128, page 64, "
+                "q_len 512 after a cached prefix U[0,8192], seed 0")
+    elif name == "mixed":
+        inp = W.mixed_batch(0)
+        desc = ("mixed decode + prefill batch: the GQA decode workload's 64 single-token sequences (kv U[1,4096]) "
+                "then the chunked-prefill workload's 8 x 512 new tokens after a prefix U[0,8192]; Hq=32, Hk=8, "
+                "D=128, bf16, one paged pool, one pa_mixed call, seed 0")
     elif name == "prefill_mla":
         inp = W.mla_prefill(0)
         desc = ("MLA ragged causal prefill: 8 sequences L~U[512,4096], H=128, q 192 = 128 nope + 64 rope, "
@@ -282,7 +299,7 @@ def cpu_oracle_decode_sample(inp, budget_s=None, steps=None, warmup=0):
         sub = slice(b, b + 1)
         oracle.decode(inp.q[sub], inp.k_pool, inp.v_pool, inp.block_table[sub], inp.seq_lens[sub], inp.scale,
                       inp.kv_dtype, inp.k_scale, inp.v_scale)
-        el = 2 if inp.kv_dtype == "bf16" else 1
+        el = 1 if inp.kv_dtype == "e4m3" else 2
         return ((int(inp.seq_lens[b]) + 63) // 64) * 64 * inp.num_kv_heads * inp.head_dim * el * 2
 
     for i in range(warmup):
@@ -363,7 +380,7 @@ def run_reference(args):
                 "e2e": {"value": round(gbs, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
         print(json.dumps(line), flush=True)
         return
-    if args.workload.startswith("prefill"):
+    if args.workload.startswith("prefill") or args.workload == "mixed":
         inp, desc = prefill_workload(args.workload)
         tfs, el, rows, flops = cpu_oracle_prefill_sample(inp, steps=args.steps, warmup=args.warmup, rows_per_step=8)
         line = {
@@ -404,8 +421,10 @@ def run_decode(args, rank, world, local_rank, dist):
     inp, desc = decode_workload(args.workload)
     full_bytes, exact_bytes = kv_bytes(inp)
     fp8 = inp.kv_dtype == "e4m3"
-    q = ops.as_bf16(inp.q, dev)
-    conv = ops.as_e4m3 if fp8 else ops.as_bf16
+    f16 = inp.kv_dtype == "f16"
+    graph = args.workload == "decode_gqa_graph"
+    q = ops.as_16(inp.q, dev, "f16" if f16 else "bf16")
+    conv = ops.as_e4m3 if fp8 else (lambda a, d: ops.as_16(a, d, "f16" if f16 else "bf16"))
     kp, vp = conv(inp.k_pool, dev), conv(inp.v_pool, dev)
     bt = torch.from_numpy(inp.block_table).to(dev)
     sl = torch.from_numpy(inp.seq_lens).to(dev)
@@ -413,7 +432,8 @@ def run_decode(args, rank, world, local_rank, dist):
     vs = torch.from_numpy(inp.v_scale).to(dev) if fp8 else None
     p = ops.plan_decode(inp.seq_lens, inp.block_table, inp.num_q_heads, inp.num_kv_heads, inp.head_dim,
                         inp.max_pages, inp.num_pool_pages, inp.kv_dtype, device=dev)
-    out = torch.empty((inp.batch, inp.num_q_heads, inp.head_dim), dtype=torch.bfloat16, device=dev)
+    out = torch.empty((inp.batch, inp.num_q_heads, inp.head_dim), dtype=torch.float16 if f16 else torch.bfloat16,
+                      device=dev)
     lse = torch.empty((inp.batch, inp.num_q_heads), dtype=torch.float32, device=dev)
     flush, l2_note = l2_policy(dev, full_bytes + q.numel() * q.element_size())
     stream = torch.cuda.current_stream(dev)
@@ -422,6 +442,32 @@ def run_decode(args, rank, world, local_rank, dist):
     def step_call():
         B.pa_decode(sh, plan, q, kp, vp, ks, vs, bt, sl, p.meta_dev, inp.scale, out, lse, p.workspace,
                     stream=stream)
+
+    if graph:
+        # capture-safe form: a plan sized from capacities only, metadata written on
+        # the device from device seq_lens, both launches captured in one CUDA graph
+        # and replayed per step (new lengths would be written into `sl` in place)
+        splan = B.pa_get_static_plan(sh)
+        gmeta = torch.zeros(splan.meta_ints, dtype=torch.int32, device=dev)
+        gws = torch.zeros(splan.workspace_bytes, dtype=torch.uint8, device=dev)
+        stream = torch.cuda.Stream(dev)
+        stream.wait_stream(torch.cuda.current_stream(dev))
+
+        def eager():
+            B.pa_get_metadata_device(sh, splan, sl, gmeta, stream=stream)
+            B.pa_decode(sh, splan, q, kp, vp, ks, vs, bt, sl, gmeta, inp.scale, out, lse, gws, stream=stream)
+
+        with torch.cuda.stream(stream):
+            eager()  # the first launches configure the kernels outside the capture
+        stream.synchronize()
+        cg = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(cg, stream=stream):
+            eager()
+        p.workspace = gws
+
+        def step_call():
+            with torch.cuda.stream(stream):
+                cg.replay()
 
     for _ in range(args.warmup):
         flush()
@@ -459,7 +505,9 @@ def run_decode(args, rank, world, local_rank, dist):
     achieved = full_bytes / (kern_ms * 1e-3) / 1e9
     kernel_files = ["decode.cu", "pa_ptx.cuh", "pa_internal.h"]
     kname = "decode_f8_kernel" if fp8 and inp.head_dim == 128 else "decode_kernel"
-    prof = kname + "_" + args.workload + ".md"
+    # the fp16 and graph-replayed forms run the same kernel over the same bytes as decode_gqa
+    prof_wl = "decode_gqa" if args.workload in ("decode_gqa_fp16", "decode_gqa_graph") else args.workload
+    prof = kname + "_" + prof_wl + ".md"
     roofline = {"bound": "hbm", "achieved": round(achieved, 1), "peak": pk["hbm_gbs"], "unit": "GB/s",
                 "frac": round(achieved / pk["hbm_gbs"], 4), "traffic": profiled_traffic(prof, kernel_files),
                 "kernel": kname, "peak_source": f"{pk_src} (copy bandwidth)",
@@ -467,7 +515,11 @@ def run_decode(args, rank, world, local_rank, dist):
 
     e2e = None
     if not args.no_e2e:
-        e2e = decode_e2e(inp, dev, stream, sh, full_bytes, world, dist, args)
+        if graph:
+            e2e = graph_decode_e2e(inp, dev, stream, cg, {"q": q, "k": kp, "v": vp, "bt": bt, "sl": sl}, out, lse,
+                                   full_bytes, world, dist, args)
+        else:
+            e2e = decode_e2e(inp, dev, stream, sh, full_bytes, world, dist, args)
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         import oracle
@@ -475,11 +527,11 @@ def run_decode(args, rank, world, local_rank, dist):
         cpu = {"value": round(gbs, 4), "unit": "GB/s", "cores": oracle.num_threads(), "kind": "oracle",
                "sample": f"{done} sequences of this batch through the fp64 oracle "
                          f"({nbytes / 1e9:.3f} GB of K+V pages, {el:.1f} s)"}
-    launches = K
+    launches = K * (2 if graph else 1)  # graph: the device scheduler and the decode kernel
     line = {
         "metric": METRIC, "value": round(value, 1), "unit": "GB/s", "n_gpus": world, "steps": K,
         "warmup": args.warmup, "ms_per_step": round(ms, 5), "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None, "dtype": "e4m3+bf16" if fp8 else "bf16", "data": "synthetic",
+        "vs_baseline": None, "dtype": "e4m3+bf16" if fp8 else ("f16" if f16 else "bf16"), "data": "synthetic",
         "config": {"workload": desc, "batch": inp.batch, "num_q_heads": inp.num_q_heads,
                    "num_kv_heads": inp.num_kv_heads, "head_dim": inp.head_dim, "page_size": 64,
                    "kv_bytes_per_step": full_bytes, "kv_bytes_token_exact": exact_bytes,
@@ -491,6 +543,47 @@ def run_decode(args, rank, world, local_rank, dist):
     }
     if rank == 0:
         print(json.dumps(line), flush=True)
+
+
+def graph_decode_e2e(inp, dev, stream, cg, dbuf, out, lse, full_bytes, world, dist, args):
+    """End to end for the graph-replayed decode: every step copies all inputs
+    from pinned memory into the captured buffers, replays the graph (device
+    metadata + decode) and reads out + lse back."""
+    import torch
+
+    def pinned(a):
+        return torch.from_numpy(np.ascontiguousarray(a)).pin_memory()
+
+    h = {"q": pinned(inp.q.view(np.int16)), "k": pinned(inp.k_pool.view(np.int16)),
+         "v": pinned(inp.v_pool.view(np.int16)), "bt": pinned(inp.block_table), "sl": pinned(inp.seq_lens)}
+    out_h = torch.empty(out.shape, dtype=torch.int16).pin_memory()
+    lse_h = torch.empty(lse.shape, dtype=torch.float32).pin_memory()
+
+    def step():
+        with torch.cuda.stream(stream):
+            for k in h:
+                dbuf[k].view(h[k].dtype).copy_(h[k], non_blocking=True)
+            cg.replay()
+            out_h.copy_(out.view(torch.int16), non_blocking=True)
+            lse_h.copy_(lse, non_blocking=True)
+        torch.cuda.synchronize(dev)
+
+    for _ in range(3):
+        step()
+    E = max(3, min(args.steps, args.e2e_steps))
+    if dist is not None:
+        dist.barrier()
+    torch.cuda.synchronize(dev)
+    t0 = time.perf_counter()
+    for _ in range(E):
+        step()
+    el = time.perf_counter() - t0
+    el, = max_over_ranks([el], dist, dev)
+    h2d = sum(v.numel() * v.element_size() for v in h.values())
+    d2h = out_h.numel() * 2 + lse_h.numel() * 4
+    return {"value": round(world * full_bytes * E / el / 1e9, 2), "unit": "GB/s", "h2d_bytes_per_step": h2d,
+            "d2h_bytes_per_step": d2h, "steps": E, "ms_per_step": round(el / E * 1e3, 4),
+            "includes": "pinned H2D of all inputs + graph replay (device metadata + decode) + D2H of out/lse + sync"}
 
 
 def decode_e2e(inp, dev, stream, sh, full_bytes, world, dist, args):
@@ -595,6 +688,8 @@ def prefill_shapes_for(inp, dev):
                             num_pool_pages=inp.k.shape[0] if inp.paged else 0, device=dev)
     if is_fp8_mla(inp):
         sh.dtype = B.PA_KV_FP8_E4M3
+    elif getattr(inp, "dtype", "bf16") == "f16":
+        sh.dtype = B.PA_KV_FP16
     return sh
 
 
@@ -672,7 +767,8 @@ def run_prefill(args, rank, world, local_rank, dist):
         # 640 / (256 / 2 + 384) = 1.25 x the bf16 peak
         peak = round(1.25 * peak, 1)
         peak_source += " x 1.25: e4m3 share of the flops at the nominal 2x bf16 rate"
-    prof = "prefill_kernel_" + args.workload + ".md"
+    # the fp16 chunked prefill runs the same kernel over the same bytes as prefill_paged
+    prof = "prefill_kernel_" + ("prefill_paged" if args.workload == "prefill_paged_fp16" else args.workload) + ".md"
     roofline = {"bound": "tensor", "achieved": round(tfs, 2), "peak": peak, "unit": "TFLOP/s",
                 "frac": round(tfs / peak, 4),
                 "traffic": profiled_traffic(prof, ["prefill.cu", "pa_ptx.cuh", "pa_internal.h"]),
@@ -691,7 +787,9 @@ def run_prefill(args, rank, world, local_rank, dist):
     line = {
         "metric": METRIC, "value": round(world * tfs, 2), "unit": "TFLOP/s", "n_gpus": world, "steps": K,
         "warmup": args.warmup, "ms_per_step": round(ms, 5), "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "vs_baseline": None, "data": "synthetic",
+        "dtype": ("e4m3+bf16" if (is_fp8_mla(inp) or is_rope_fp8(inp))
+                  else ("f16" if getattr(inp, "dtype", "bf16") == "f16" else "bf16")),
         "config": {"workload": desc, "total_q": tq, "num_q_heads": inp.num_q_heads,
                    "head_dim_qk": inp.head_dim_qk, "head_dim_v": inp.head_dim_v, "flops_per_step": flops,
                    "pct_tc_peak": round(100 * tfs / peak, 2),
@@ -869,6 +967,143 @@ def run_append(args, rank, world, local_rank, dist):
         print(json.dumps(line), flush=True)
 
 
+def run_mixed(args, rank, world, local_rank, dist):
+    """One pa_mixed call per step: the decode kernel on the batch's leading
+    single-token sequences, the prefill kernel on the rest.  value = attention
+    FLOPs over every visible (row, key, head) / step time (the unit the oracle
+    arm can report too); the roofline is time-weighted: the decode part's K/V
+    bytes at the HBM peak plus the prefill part's FLOPs at the bf16 peak."""
+    import torch
+    from paged_kv_attention_fwd_gb300 import binding as B
+    from paged_kv_attention_fwd_gb300 import ops
+
+    dev = torch.device("cuda", local_rank)
+    torch.cuda.set_device(dev)
+    inp, desc = prefill_workload("mixed")
+    nd = int(inp.meta["num_decode"])
+    hq, hk = inp.num_q_heads, inp.num_kv_heads
+    kl = np.diff(inp.cu_seqlens_k).astype(np.int32)
+    sh = B.pa_mixed_shapes(batch=inp.batch, num_q_heads=hq, num_kv_heads=hk, head_dim=128, page_size=64,
+                           max_pages_per_seq=inp.block_table.shape[1], num_pool_pages=inp.k.shape[0],
+                           kv_dtype=B.PA_KV_BF16, num_sms=ops.num_sms(dev), ctas_per_sm=0, forced_splits=0)
+    meta, plan = B.pa_get_mixed_plan(inp.cu_seqlens_q, kl, inp.block_table, sh)
+    if plan.num_decode != nd:
+        raise RuntimeError(f"mixed plan split at {plan.num_decode}, expected {nd}")
+    tq = int(inp.cu_seqlens_q[-1])
+    d = {"q": ops.as_bf16(inp.q, dev), "k": ops.as_bf16(inp.k, dev), "v": ops.as_bf16(inp.v, dev),
+         "bt": torch.from_numpy(inp.block_table).to(dev), "cq": torch.from_numpy(inp.cu_seqlens_q).to(dev),
+         "ck": torch.from_numpy(inp.cu_seqlens_k).to(dev), "kl": torch.from_numpy(kl).to(dev),
+         "meta": torch.from_numpy(meta).to(dev)}
+    out = torch.empty((tq, hq, 128), dtype=torch.bfloat16, device=dev)
+    lse = torch.empty((tq, hq), dtype=torch.float32, device=dev)
+    ws = torch.zeros(plan.workspace_bytes, dtype=torch.uint8, device=dev)
+    dec_ws = (plan.decode.workspace_bytes + 255) // 256 * 256 if plan.num_decode else 0
+    flush, l2_note = l2_policy(dev, sum(t.numel() * t.element_size() for t in d.values()))
+    stream = torch.cuda.current_stream(dev)
+
+    def step():
+        B.pa_mixed(sh, plan, d["q"], d["k"], d["v"], d["bt"], d["cq"], d["ck"], d["kl"], d["meta"], inp.scale, out,
+                   lse, ws, stream=stream)
+
+    def check():
+        for part in (ws, ws[dec_ws:]):
+            if B.pa_check_status(part, stream) != B.PA_OK:
+                raise RuntimeError(B.pa_last_error())
+
+    for _ in range(args.warmup):
+        flush()
+        step()
+    torch.cuda.synchronize(dev)
+    check()
+    K = args.steps
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(K)]
+    if dist is not None:
+        dist.barrier()
+    torch.cuda.synchronize(dev)
+    with ClockSampler(gpu_index(local_rank)) as clk:
+        for i in range(K):
+            flush()
+            ev[i][0].record(stream)
+            step()
+            ev[i][1].record(stream)
+        torch.cuda.synchronize(dev)
+    if dist is not None:
+        dist.barrier()
+    ms = sum(ev[i][0].elapsed_time(ev[i][1]) for i in range(K)) / K
+    ms, = max_over_ranks([ms], dist, dev)
+    check()
+    clocks = clk.summary()
+    pk, pk_src = peaks()
+    pairs = visible_pairs(inp)
+    per_pair = hq * (2 * 128 + 2 * 128)
+    flops = int(pairs.sum()) * per_pair
+    pre_flops = int(pairs[nd:].sum()) * per_pair  # decode rows come first, one row per sequence
+    dec_bytes = int(sum((int(n) + 63) // 64 for n in kl[:nd])) * 64 * hk * 128 * 2 * 2
+    t_ideal = dec_bytes / (pk["hbm_gbs"] * 1e9) + pre_flops / (pk["bf16_tflops"] * 1e12)
+    tfs = flops / (ms * 1e-3) / 1e12
+    eff_peak = flops / t_ideal / 1e12
+    roofline = {"bound": "tensor", "achieved": round(tfs, 2), "peak": round(eff_peak, 1), "unit": "TFLOP/s",
+                "frac": round(t_ideal / (ms * 1e-3), 4), "traffic": None, "kernel": "decode_kernel + prefill_kernel",
+                "peak_source": (f"{pk_src}: time-weighted -- the decode part's K/V bytes at the copy bandwidth plus "
+                                f"the prefill part's FLOPs at the cuBLAS bf16 peak ({t_ideal * 1e6:.1f} us for the "
+                                f"step); frac = that time / the measured step time"),
+                "decode_kv_bytes": dec_bytes, "prefill_flops": pre_flops, "kernel_ms": round(ms, 5)}
+    e2e = None
+    if not args.no_e2e:
+        h = {k: torch.from_numpy(np.ascontiguousarray(v)).pin_memory() for k, v in (
+            ("q", inp.q.view(np.int16)), ("k", inp.k.view(np.int16)), ("v", inp.v.view(np.int16)),
+            ("bt", inp.block_table), ("cq", inp.cu_seqlens_q), ("ck", inp.cu_seqlens_k), ("kl", kl))}
+        meta_pin = torch.empty(meta.size, dtype=torch.int32).pin_memory()
+        out_h = torch.empty((tq, hq, 128), dtype=torch.int16).pin_memory()
+        lse_h = torch.empty((tq, hq), dtype=torch.float32).pin_memory()
+
+        def e2e_step():
+            m, pl = B.pa_get_mixed_plan(inp.cu_seqlens_q, kl, None, sh)
+            meta_pin.numpy()[: m.size] = m
+            for k in h:
+                d[k].view(h[k].dtype).copy_(h[k], non_blocking=True)
+            d["meta"][: m.size].copy_(meta_pin[: m.size], non_blocking=True)
+            B.pa_mixed(sh, pl, d["q"], d["k"], d["v"], d["bt"], d["cq"], d["ck"], d["kl"], d["meta"], inp.scale,
+                       out, lse, ws, stream=stream)
+            out_h.copy_(out.view(torch.int16), non_blocking=True)
+            lse_h.copy_(lse, non_blocking=True)
+            torch.cuda.synchronize(dev)
+
+        for _ in range(3):
+            e2e_step()
+        E = max(3, min(K, args.e2e_steps))
+        t0 = time.perf_counter()
+        for _ in range(E):
+            e2e_step()
+        el = time.perf_counter() - t0
+        el, = max_over_ranks([el], dist, dev)
+        e2e = {"value": round(world * flops * E / el / 1e12, 3), "unit": "TFLOP/s",
+               "h2d_bytes_per_step": sum(v.numel() * v.element_size() for v in h.values()) + meta.size * 4,
+               "d2h_bytes_per_step": out_h.numel() * 2 + lse_h.numel() * 4, "steps": E,
+               "ms_per_step": round(el / E * 1e3, 4),
+               "includes": "host mixed plan + pinned H2D of all inputs + pa_mixed + D2H of out/lse + sync"}
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        import oracle
+        ctf, el, rows, cfl = cpu_oracle_prefill_sample(inp, budget_s=args.cpu_seconds)
+        cpu = {"value": round(ctf, 6), "unit": "TFLOP/s", "cores": oracle.num_threads(), "kind": "oracle",
+               "sample": f"{rows} random (token, head) query rows of this batch through the fp64 oracle "
+                         f"({cfl / 1e9:.2f} GFLOP, {el:.1f} s)"}
+    line = {
+        "metric": METRIC, "value": round(world * tfs, 2), "unit": "TFLOP/s", "n_gpus": world, "steps": K,
+        "warmup": args.warmup, "ms_per_step": round(ms, 5), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": desc, "num_decode": nd, "total_q": tq, "flops_per_step": flops,
+                   "pct_time_weighted_roofline": round(100 * t_ideal / (ms * 1e-3), 2), "l2": l2_note,
+                   "parallelism": f"replicas x{world}"},
+        "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
+        # per step: the decode kernel, the prefill ordering kernel and the prefill kernel
+        "gpu_launches": K * 3, "clocks": clocks,
+    }
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
 def W_cu(lengths):
     from paged_kv_attention_fwd_gb300 import workloads as W
     return W.cu_seqlens(lengths)
@@ -883,9 +1118,9 @@ def main():
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="decode_gqa",
-                    choices=["decode_gqa", "decode_fp8", "decode_tiny", "prefill_paged", "prefill_mla", "prefill_mla_fp8",
-                             "prefill_mla_rope_fp8",
-                             "append"])
+                    choices=["decode_gqa", "decode_gqa_fp16", "decode_gqa_graph", "decode_fp8", "decode_tiny",
+                             "prefill_paged", "prefill_paged_fp16", "prefill_mla", "prefill_mla_fp8",
+                             "prefill_mla_rope_fp8", "mixed", "append"])
     ap.add_argument("--e2e-steps", type=int, default=20)
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--no-e2e", action="store_true")
@@ -915,6 +1150,8 @@ def main():
         dist.barrier()
     if args.workload.startswith("prefill"):
         run_prefill(args, rank, world, local_rank, dist)
+    elif args.workload == "mixed":
+        run_mixed(args, rank, world, local_rank, dist)
     elif args.workload == "append":
         run_append(args, rank, world, local_rank, dist)
     else:

@@ -262,10 +262,10 @@ def tiny_decode(seed: int = 0) -> DecodeInputs:
         scale=1.0 / 8.0, kv_dtype="bf16")
 
 
-def gqa_decode(seed: int = 0, batch: int = 64) -> DecodeInputs:
-    """B=64, Hq=32, Hk=8, D=128, bf16, lengths uniform in [1, 4096]."""
+def gqa_decode(seed: int = 0, batch: int = 64, kv_dtype: str = "bf16") -> DecodeInputs:
+    """B=64, Hq=32, Hk=8, D=128, bf16 (or fp16), lengths uniform in [1, 4096]."""
     lens = uniform_lengths(seed, batch, 1, 4096)
-    return make_decode(batch, 32, 8, 128, lens, seed, "bf16", max_pages=64)
+    return make_decode(batch, 32, 8, 128, lens, seed, kv_dtype, max_pages=64)
 
 
 def fp8_long_decode(seed: int = 0, batch: int = 128) -> DecodeInputs:
@@ -325,11 +325,11 @@ def make_paged_prefill(q_lens, kv_lens, num_q_heads: int, num_kv_heads: int, hea
 
 
 def chunked_prefill(seed: int = 0, batch: int = 8, q_len: int = 512, max_prefix: int = 8192,
-                    heads: int = 32, head_dim: int = 128) -> PrefillInputs:
+                    heads: int = 32, head_dim: int = 128, dtype: str = "bf16") -> PrefillInputs:
     """q_len new tokens per sequence after a cached prefix uniform in [0, max_prefix]."""
     prefix = _rng(seed, _S_PREFIX).integers(0, max_prefix + 1, size=batch).astype(np.int32)
     q_lens = np.full(batch, q_len, dtype=np.int32)
-    p = make_paged_prefill(q_lens, prefix + q_len, heads, heads, head_dim, seed)
+    p = make_paged_prefill(q_lens, prefix + q_len, heads, heads, head_dim, seed, dtype=dtype)
     p.meta["prefix"] = prefix
     return p
 
@@ -352,6 +352,20 @@ def make_ragged_prefill(lens, num_heads: int, head_dim_qk: int, head_dim_v: int,
         scale=1.0 / math.sqrt(head_dim_qk), causal=causal,
         k_rope=normal_16(seed, _S_KROPE, (tk, 1, rope_dim), dtype) if rope_dim else None,
         qo_offset=None if qo_offset is None else np.asarray(qo_offset, dtype=np.int32), dtype=dtype)
+
+
+def mixed_batch(seed: int = 0) -> PrefillInputs:
+    """A serving step's batch: the GQA decode workload's 64 single-token
+    sequences (kv lengths uniform in [1, 4096]) followed by the chunked-prefill
+    workload's 8 sequences of 512 new tokens after a prefix uniform in [0, 8192];
+    Hq=32, Hk=8, D=128, bf16, one paged pool, one ragged query layout."""
+    dec = uniform_lengths(seed, 64, 1, 4096)
+    prefix = _rng(seed, _S_PREFIX).integers(0, 8193, size=8).astype(np.int32)
+    q_lens = np.concatenate([np.ones(64, np.int32), np.full(8, 512, np.int32)])
+    kv_lens = np.concatenate([dec, prefix + 512]).astype(np.int32)
+    p = make_paged_prefill(q_lens, kv_lens, 32, 8, 128, seed)
+    p.meta["num_decode"] = 64
+    return p
 
 
 def mla_prefill(seed: int = 0, batch: int = 8, lo: int = 512, hi: int = 4096,
