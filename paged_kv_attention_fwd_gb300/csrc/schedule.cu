@@ -98,13 +98,17 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int total = ind[B];
     const int items = total * Hk;
     const int grid = min(items, cap);
+    // The host rule orders work items by cost descending, then item index
+    // ascending.  An item's cost depends only on its split, and the Hk items
+    // of split g hold the consecutive indices g * Hk .. g * Hk + Hk - 1, so
+    // that order is the splits' order (cost descending, split index
+    // ascending) with each split expanded over its KV heads in order: sort the
+    // splits, not the items.
     int p2 = 1;
-    while (p2 < items) p2 <<= 1;
-    // sort keys: cost descending, then item index ascending (as the host rule)
-    for (int i = threadIdx.x; i < p2; i += kThreads) {
+    while (p2 < total) p2 <<= 1;
+    for (int g = threadIdx.x; g < p2; g += kThreads) {
         unsigned long long k = ~0ull;
-        if (i < items) {
-            const int g = i / Hk;
+        if (g < total) {
             int lo = 0, hi = B - 1;  // last b with ind[b] <= g
             while (lo < hi) {
                 const int mid = (lo + hi + 1) >> 1;
@@ -113,9 +117,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             const int b = lo, s = g - ind[b], n = nsp[b], p = pages[b];
             const int cost = (int)(((long long)(s + 1) * p) / n - ((long long)s * p) / n) + 1;
-            k = ((unsigned long long)(unsigned)(0x7FFFFFFF - cost) << 32) | (unsigned)i;
+            k = ((unsigned long long)(unsigned)(0x7FFFFFFF - cost) << 32) | (unsigned)g;
         }
-        key[i] = k;
+        key[g] = k;
     }
     __syncthreads();
     // Bitonic sort.  The keys are unique, so the sorted order is too and any
@@ -123,7 +127,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // keys at positions k * kThreads + t in registers; the stages whose
     // partner (position ^ stride) lies in the same warp run as shuffles with no
     // barrier, the others through shared memory.
-    constexpr int kMaxPer = 16;  // 16384 items / kThreads
+    constexpr int kMaxPer = 16;  // 16384 splits (Hk = 1) / kThreads
     const int per = p2 > kThreads ? p2 / kThreads : 1;
     unsigned long long kr[kMaxPer];
 #pragma unroll
@@ -191,8 +195,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         cta_ptr[c] = c * full + (last_even ? min(c, rem) : max(0, c - (grid - rem)));
     int32_t* out_items = cta_ptr + grid + 1;
     for (int r = threadIdx.x; r < items; r += kThreads) {
-        const int i = (int)(key[r] & 0xFFFFFFFFu);
-        const int g = i / Hk, kvh = i % Hk;
+        const int g = (int)(key[r / Hk] & 0xFFFFFFFFu), kvh = r % Hk;
         int lo = 0, hi = B - 1;
         while (lo < hi) {
             const int mid = (lo + hi + 1) >> 1;

@@ -40,9 +40,10 @@ def device_meta(sh, lens):
     return plan, meta
 
 
-@pytest.mark.parametrize("case", ["uniform", "lognormal", "forced", "edges", "single", "large"])
+@pytest.mark.parametrize("case", ["uniform", "lognormal", "forced", "edges", "single", "large", "wide"])
 def test_device_schedule_bit_exact(case):
-    rng = np.random.default_rng(hash(case) % 1000)
+    cases = ["uniform", "lognormal", "forced", "edges", "single", "large", "wide"]
+    rng = np.random.default_rng(100 + cases.index(case))
     if case == "uniform":
         lens, hk, forced, mp = rng.integers(1, 4097, 64), 8, 0, 64
     elif case == "lognormal":
@@ -53,8 +54,10 @@ def test_device_schedule_bit_exact(case):
         lens, hk, forced, mp = np.array([0, 1, 63, 64, 65, 128, 129, 4096, 0, 5000]), 2, 0, 100
     elif case == "single":
         lens, hk, forced, mp = np.array([1]), 1, 0, 1
-    else:  # "large": ~14700 items, the sort's 16 keys per thread
+    elif case == "large":  # ~14700 items
         lens, hk, forced, mp = rng.integers(0, 2001, 1800), 8, 0, 32
+    else:  # one KV head: as many splits as items, the sort's 16 keys per thread
+        lens, hk, forced, mp = rng.integers(0, 4097, 8192), 1, 2, 64
     lens = lens.astype(np.int32)
     sh = shapes(len(lens), hk * 2, hk, mp, 10 ** 6, forced)
     plan, meta = device_meta(sh, lens)
