@@ -66,9 +66,43 @@ def l2_policy(dev, input_bytes: int):
     import torch
     l2 = int(getattr(torch.cuda.get_device_properties(dev), "L2_cache_size", 0) or 129_000_000)
     if input_bytes >= 3 * l2:
-        return (lambda: None), (f"no flush between steps: inputs larger than L2 ({input_bytes / 1e6:.0f} MB read "
-                                f"per step = {input_bytes / l2:.1f} x the {l2 / 1e6:.0f} MB L2)")
+        return NoFlush(), (f"no flush between steps: inputs larger than L2 ({input_bytes / 1e6:.0f} MB read "
+                           f"per step = {input_bytes / l2:.1f} x the {l2 / 1e6:.0f} MB L2)")
     return L2Flush(dev), L2_NOTE
+
+
+class NoFlush:
+    """The between-steps action for inputs larger than L2: nothing."""
+
+    def __call__(self):
+        pass
+
+
+def time_steps(K, step, flush, stream):
+    """Mean device time of one step (ms) over K steps, from CUDA events on the
+    launching stream.  Without a flush the K steps run back to back between
+    one pair of events, so each launch may start its shared-memory prologue
+    while the previous step's kernel drains, as in a serving loop (every
+    kernel still waits for the one before it before touching memory).  With a
+    flush each step has its own pair of events and the flush runs outside
+    them.  The caller synchronises before and after."""
+    import torch
+    if isinstance(flush, NoFlush):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(K):
+            step()
+        e1.record(stream)
+        e1.synchronize()
+        return e0.elapsed_time(e1) / K
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(K)]
+    for i in range(K):
+        flush()
+        ev[i][0].record(stream)
+        step()
+        ev[i][1].record(stream)
+    ev[-1][1].synchronize()
+    return sum(ev[i][0].elapsed_time(ev[i][1]) for i in range(K)) / K
 
 
 PROFILES = os.path.join(ROOT, "profiles")
@@ -478,21 +512,14 @@ def run_decode(args, rank, world, local_rank, dist):
         raise RuntimeError(f"device status {st}: {B.pa_last_error()}")
 
     K = args.steps
-    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(K)]
     if dist is not None:
         dist.barrier()
     torch.cuda.synchronize(dev)
     with ClockSampler(gpu_index(local_rank)) as clk:
-        for i in range(K):
-            flush()  # between timed iterations (outside the events)
-            ev[i][0].record(stream)
-            step_call()  # one launch: decode with the split merge fused in
-            ev[i][1].record(stream)
+        ms = time_steps(K, step_call, flush, stream)  # a step: one decode launch, split merge fused in
         torch.cuda.synchronize(dev)
     if dist is not None:
         dist.barrier()
-    step_ms = [ev[i][0].elapsed_time(ev[i][1]) for i in range(K)]
-    ms = sum(step_ms) / K
     kern_ms = ms
     ms, kern_ms = max_over_ranks([ms, kern_ms], dist, dev)
     st = B.pa_check_status(p.workspace, stream)
@@ -503,7 +530,7 @@ def run_decode(args, rank, world, local_rank, dist):
     pk, pk_src = peaks()
     value = job_value(full_bytes, world, ms * 1e-3) / 1e9
     achieved = full_bytes / (kern_ms * 1e-3) / 1e9
-    kernel_files = ["decode.cu", "pa_ptx.cuh", "pa_internal.h"]
+    kernel_files = ["decode.cu", "pa_ptx.cuh", "pa_internal.h", "pa_launch.h"]
     kname = "decode_f8_kernel" if fp8 and inp.head_dim == 128 else "decode_kernel"
     # the fp16 and graph-replayed forms run the same kernel over the same bytes as decode_gqa
     prof_wl = "decode_gqa" if args.workload in ("decode_gqa_fp16", "decode_gqa_graph") else args.workload
@@ -739,20 +766,14 @@ def run_prefill(args, rank, world, local_rank, dist):
     if B.pa_check_status(ws, stream) != B.PA_OK:
         raise RuntimeError(B.pa_last_error())
     K = args.steps
-    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(K)]
     if dist is not None:
         dist.barrier()
     torch.cuda.synchronize(dev)
     with ClockSampler(gpu_index(local_rank)) as clk:
-        for i in range(K):
-            flush()
-            ev[i][0].record(stream)
-            step()
-            ev[i][1].record(stream)
+        ms = time_steps(K, step, flush, stream)
         torch.cuda.synchronize(dev)
     if dist is not None:
         dist.barrier()
-    ms = sum(ev[i][0].elapsed_time(ev[i][1]) for i in range(K)) / K
     ms, = max_over_ranks([ms], dist, dev)
     if B.pa_check_status(ws, stream) != B.PA_OK:
         raise RuntimeError(B.pa_last_error())
@@ -891,18 +912,12 @@ def run_append(args, rank, world, local_rank, dist):
         flush()
         step()
     K = args.steps
-    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(K)]
     if dist is not None:
         dist.barrier()
     torch.cuda.synchronize(dev)
     with ClockSampler(gpu_index(local_rank)) as clk:
-        for i in range(K):
-            flush()
-            ev[i][0].record(stream)
-            step()
-            ev[i][1].record(stream)
+        ms = time_steps(K, step, flush, stream)
         torch.cuda.synchronize(dev)
-    ms = sum(ev[i][0].elapsed_time(ev[i][1]) for i in range(K)) / K
     ms, = max_over_ranks([ms], dist, dev)
     if B.pa_check_status(ws, stream) != B.PA_OK:
         raise RuntimeError(B.pa_last_error())
@@ -955,7 +970,7 @@ def run_append(args, rank, world, local_rank, dist):
                    "parallelism": f"replicas x{world}"},
         "roofline": {"bound": "hbm", "achieved": round(gbs, 1), "peak": pk["hbm_gbs"], "unit": "GB/s",
                      "frac": round(gbs / pk["hbm_gbs"], 4),
-                     "traffic": profiled_traffic("append_kernel_append.md", ["append.cu", "pa_internal.h"]),
+                     "traffic": profiled_traffic("append_kernel_append.md", ["append.cu", "pa_internal.h", "pa_launch.h"]),
                      "kernel": "append_kernel",
                      "peak_source": f"{pk_src} (copy bandwidth)", "algorithmic_bytes_per_launch": nbytes,
                      "kernel_ms": round(ms, 5)},
@@ -1016,20 +1031,14 @@ def run_mixed(args, rank, world, local_rank, dist):
     torch.cuda.synchronize(dev)
     check()
     K = args.steps
-    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(K)]
     if dist is not None:
         dist.barrier()
     torch.cuda.synchronize(dev)
     with ClockSampler(gpu_index(local_rank)) as clk:
-        for i in range(K):
-            flush()
-            ev[i][0].record(stream)
-            step()
-            ev[i][1].record(stream)
+        ms = time_steps(K, step, flush, stream)
         torch.cuda.synchronize(dev)
     if dist is not None:
         dist.barrier()
-    ms = sum(ev[i][0].elapsed_time(ev[i][1]) for i in range(K)) / K
     ms, = max_over_ranks([ms], dist, dev)
     check()
     clocks = clk.summary()

@@ -11,6 +11,7 @@
 #include <cuda_fp8.h>
 
 #include "pa_internal.h"
+#include "pa_launch.h"
 
 namespace pa {
 namespace {
@@ -20,6 +21,7 @@ constexpr int kPiecesPerLane = kHeadsPerWarp * 2 * (128 / 8) / 32;  // D = 128: 
 
 // grid: x = tokens / 8 (one warp each), y = group of kHeadsPerWarp KV heads
 __global__ void __launch_bounds__(256) append_kernel(const AppendArgs a) {
+    allow_dependents_launch();  // an attention kernel after it may start its prologue
     const int hk = a.num_kv_heads;
     const int tok = (int)(blockIdx.x * 8u + (threadIdx.x >> 5));
     const int lane = threadIdx.x & 31;

@@ -39,6 +39,7 @@
 #include <mutex>
 
 #include "pa_internal.h"
+#include "pa_launch.h"
 #include "pa_ptx.cuh"
 
 namespace pa {
@@ -335,14 +336,6 @@ __global__ void __launch_bounds__(DecodeLayout<D, FP8>::kThreads, 1)
     volatile int* abort_sh = &abort_store;
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int32_t* meta = a.meta;
-    const int B = a.batch;
-    const int items_off = items_offset(meta, B);
-    int it_lo = 0, it_hi = 0;
-    if ((int)blockIdx.x < __ldg(&meta[5])) {
-        it_lo = __ldg(&meta[kMetaHeader + 2 * B + 1 + blockIdx.x]);
-        it_hi = __ldg(&meta[kMetaHeader + 2 * B + 1 + blockIdx.x + 1]);
-    }
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < L::kStages; ++s) {
@@ -368,11 +361,6 @@ __global__ void __launch_bounds__(DecodeLayout<D, FP8>::kThreads, 1)
         *abort_sh = 0;
         fence_barrier_init();
     }
-    if (warp == 1) {
-        tmem_alloc(&tmem_base_sh, kTmemCols);
-        tmem_relinquish();
-    }
-    if (warp == L::kMergeWarp) fill_item_cache(items_sh, a, it_lo, it_hi, items_off, lane);
     if (warp >= 2 && warp < 6) {
         // P rows of padding heads must read as zero in every PV product, and
         // so must the query rows past the group (the query TMA writes only
@@ -385,9 +373,25 @@ __global__ void __launch_bounds__(DecodeLayout<D, FP8>::kThreads, 1)
         }
         fence_proxy_async_smem();
     }
+    // shared memory only up to here: this part overlaps the previous kernel
+    grid_dependency_wait();
+    const int32_t* meta = a.meta;
+    const int B = a.batch;
+    const int items_off = items_offset(meta, B);
+    int it_lo = 0, it_hi = 0;
+    if ((int)blockIdx.x < __ldg(&meta[5])) {
+        it_lo = __ldg(&meta[kMetaHeader + 2 * B + 1 + blockIdx.x]);
+        it_hi = __ldg(&meta[kMetaHeader + 2 * B + 1 + blockIdx.x + 1]);
+    }
+    if (warp == 1) {
+        tmem_alloc(&tmem_base_sh, kTmemCols);
+        tmem_relinquish();
+    }
+    if (warp == L::kMergeWarp) fill_item_cache(items_sh, a, it_lo, it_hi, items_off, lane);
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
+    allow_dependents_launch();
     const uint32_t tbase = tmem_base_sh;
 
     if (warp == 0) {
@@ -1451,8 +1455,8 @@ cudaError_t launch_decode_np(const DecodeArgs& a, const CUtensorMap* mk, const C
     static std::atomic<uint64_t> configured{0};
     cudaError_t e = ensure_dynamic_smem(decode_kernel<D, FP8, NP>, L::kSmem, configured);
     if (e != cudaSuccess) return e;
-    decode_kernel<D, FP8, NP><<<grid, L::kThreads, L::kSmem, stream>>>(a, *mk, *mv, *mq);
-    return cudaGetLastError();
+    return launch_overlapped(decode_kernel<D, FP8, NP>, dim3(grid), dim3(L::kThreads), L::kSmem, stream, a, *mk, *mv,
+                             *mq);
 }
 
 // The softmax works on the group's heads padded to 4, 8 or 16 (the MMA N stays 16).

@@ -10,6 +10,7 @@
 #include <algorithm>
 
 #include "pa_internal.h"
+#include "pa_launch.h"
 
 namespace pa {
 namespace {
@@ -67,6 +68,7 @@ __device__ void block_exclusive_scan(const int* in, int* out, int n, int* tmp) {
 __global__ void __launch_bounds__(kThreads, 1)
     schedule_kernel(const int32_t* seq_lens, int B, int Hk, int max_pages, int cps, int cap, int forced,
                     int p2cap, int32_t* meta) {
+    allow_dependents_launch();  // the decode kernel's prologue overlaps this one
     extern __shared__ unsigned long long dyn[];
     unsigned long long* key = dyn;                              // [p2cap]
     int* pages = reinterpret_cast<int*>(dyn + p2cap);           // [B]
@@ -225,6 +227,7 @@ __global__ void __launch_bounds__(kPtThreads) page_table_kernel(const int32_t* _
                                                                 int* status) {
     extern __shared__ long long start[];  // [B + 1]
     __shared__ long long warp_sum[kPtThreads / 32];
+    allow_dependents_launch();  // an attention kernel after it may start its prologue
     const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
     const int per = (B + kPtThreads - 1) / kPtThreads;
     const int b0 = min(B, t * per), b1 = min(B, b0 + per);

@@ -96,6 +96,92 @@ def test_append_then_chunked_prefill():
     assert np.abs(lse.cpu().numpy() - rl).max() <= 1e-3
 
 
+def test_append_then_decode_steps_without_sync():
+    """Decode steps as a serving loop issues them: every round appends one new
+    token per sequence, then decodes over the grown cache, all on one stream
+    with no host synchronisation between the launches.  The decode may start
+    its prologue while the append is still running (the append lets its
+    dependents launch as soon as it starts), so a decode that read pages
+    before the append completed would see the stale tokens the pool was
+    filled with.  Every round must match the oracle on the pool as it stood
+    after that round's append."""
+    rounds, hq, hk, d = 4, 16, 4, 128
+    prior = np.array([0, 63, 64, 300, 1000, 5, 129, 2047], np.int32)
+    nb = len(prior)
+    base = W.make_decode(nb, hq, hk, d, prior + rounds, seed=52, kv_dtype="bf16", extra_pages=3)
+    dev = "cuda"
+    kp, vp = ops.as_bf16(base.k_pool, dev), ops.as_bf16(base.v_pool, dev)
+    bt = torch.from_numpy(base.block_table).to(dev)
+    cu = torch.from_numpy(np.arange(nb + 1, dtype=np.int32)).to(dev)
+    kn = [W.bf16_normal(52, 100 + r, (nb, hk, d)) for r in range(rounds)]
+    vn = [W.bf16_normal(52, 110 + r, (nb, hk, d)) for r in range(rounds)]
+    qs = [W.bf16_normal(52, 120 + r, (nb, hq, d)) for r in range(rounds)]
+    kn_d, vn_d, q_d = ([ops.as_bf16(x, dev) for x in xs] for xs in (kn, vn, qs))
+    start_d = [torch.from_numpy(prior + r).to(dev) for r in range(rounds)]
+    lens_d = [torch.from_numpy(prior + r + 1).to(dev) for r in range(rounds)]
+    plans = [ops.plan_decode(prior + r + 1, base.block_table, hq, hk, d, base.max_pages, base.num_pool_pages)
+             for r in range(rounds)]
+    sh = B.pa_append_shapes(batch=nb, num_kv_heads=hk, head_dim=d, page_size=64,
+                            max_pages_per_seq=base.block_table.shape[1], num_pool_pages=base.num_pool_pages,
+                            total_new=nb, kv_dtype=B.PA_KV_BF16)
+    ws = torch.zeros(B.PA_STATUS_BYTES, dtype=torch.uint8, device=dev)
+    torch.cuda.synchronize()
+    outs = []
+    for r in range(rounds):
+        B.pa_append_kv(sh, kn_d[r], vn_d[r], cu, start_d[r], bt, kp, vp, None, None, ws)
+        outs.append(ops.decode(plans[r], q_d[r], kp, vp, bt, lens_d[r], base.scale))
+    torch.cuda.synchronize()
+    assert B.pa_check_status(ws) == B.PA_OK
+    k_ref, v_ref = base.k_pool, base.v_pool
+    cu_h = np.arange(nb + 1, dtype=np.int32)
+    for r in range(rounds):
+        assert B.pa_check_status(plans[r].workspace) == B.PA_OK
+        k_ref, v_ref = oracle.append_kv(kn[r], vn[r], cu_h, prior + r, base.block_table, k_ref, v_ref)
+        ro, rl = oracle.decode(qs[r], k_ref, v_ref, base.block_table, prior + r + 1, base.scale)
+        out, lse = outs[r][0].float().cpu().numpy(), outs[r][1].cpu().numpy()
+        err = np.abs(out - ro)
+        assert err.max() <= 1e-2 and err.mean() <= 1e-3, f"round {r}: max abs err {err.max():.3g}"
+        assert np.abs(lse - rl).max() <= 1e-3, f"round {r}"
+
+
+def test_append_then_chunked_prefill_without_sync():
+    """The chunked-prefill flow on one stream with no host synchronisation:
+    the prefill reads the pages the append has just written (the pool holds
+    stale random tokens at those positions before the append)."""
+    prefix = np.array([0, 70, 500, 64], np.int32)
+    qlen = np.array([40, 129, 256, 300], np.int32)
+    base, _, _, kn, vn = case("bf16", hk=4, prior=prefix, new=qlen, seed=53)
+    dev = "cuda"
+    kp, vp = ops.as_bf16(base.k_pool, dev), ops.as_bf16(base.v_pool, dev)
+    bt = torch.from_numpy(base.block_table).to(dev)
+    q = W.bf16_normal(53, 92, (int(qlen.sum()), 8, 128))
+    q_d, kn_d, vn_d = ops.as_bf16(q, dev), ops.as_bf16(kn, dev), ops.as_bf16(vn, dev)
+    cu_new = torch.from_numpy(W.cu_seqlens(qlen)).to(dev)
+    start = torch.from_numpy(prefix).to(dev)
+    cu_k = torch.from_numpy(W.cu_seqlens(prefix + qlen)).to(dev)
+    sh_app = B.pa_append_shapes(batch=len(prefix), num_kv_heads=4, head_dim=128, page_size=64,
+                                max_pages_per_seq=base.block_table.shape[1], num_pool_pages=base.num_pool_pages,
+                                total_new=int(qlen.sum()), kv_dtype=B.PA_KV_BF16)
+    sh = ops.prefill_shapes(len(prefix), 8, 4, 128, 128, 0, int(qlen.max()), int(qlen.sum()),
+                            int((prefix + qlen).sum()), max_pages=base.max_pages, num_pool_pages=base.num_pool_pages)
+    ws = torch.zeros(B.PA_STATUS_BYTES, dtype=torch.uint8, device=dev)
+    pws = torch.zeros(B.pa_prefill_workspace_size(sh), dtype=torch.uint8, device=dev)
+    out = torch.empty((int(qlen.sum()), 8, 128), dtype=torch.bfloat16, device=dev)
+    lse = torch.empty((int(qlen.sum()), 8), dtype=torch.float32, device=dev)
+    torch.cuda.synchronize()
+    # the append and the prefill launches are adjacent in the stream
+    B.pa_append_kv(sh_app, kn_d, vn_d, cu_new, start, bt, kp, vp, None, None, ws)
+    ops.prefill(sh, q_d, kp, vp, cu_new, cu_k, base.scale, True, block_table=bt, out=out, lse=lse, workspace=pws)
+    torch.cuda.synchronize()
+    assert B.pa_check_status(ws) == B.PA_OK and B.pa_check_status(pws) == B.PA_OK
+    k_ref, v_ref = oracle.append_kv(kn, vn, W.cu_seqlens(qlen), prefix, base.block_table, base.k_pool, base.v_pool)
+    ro, rl = oracle.prefill(q, k_ref, v_ref, W.cu_seqlens(qlen), W.cu_seqlens(prefix + qlen), base.scale, True,
+                            block_table=base.block_table)
+    err = np.abs(out.float().cpu().numpy() - ro)
+    assert err.max() <= 1e-2 and err.mean() <= 1e-3
+    assert np.abs(lse.cpu().numpy() - rl).max() <= 1e-3
+
+
 def test_append_out_of_range_is_reported():
     base, prior, new, kn, vn = case("bf16")
     bt = base.block_table.copy()
