@@ -889,8 +889,8 @@ pa_status pa_get_metadata_device(const pa_decode_shapes* sh, const pa_decode_pla
     if (st != PA_OK) return st;
     if (plan->reserved != 1 || plan->num_items != check.num_items || plan->grid != check.grid)
         return fail(PA_ERR_INVALID_ARG, "the plan must come from pa_get_static_plan for these shapes");
-    int p2 = 1;
-    while (p2 < plan->num_items) p2 <<= 1;
+    int p2 = 1;  // sort keys: one per split
+    while (p2 < plan->total_splits) p2 <<= 1;
     const size_t smem = pa::schedule_smem_bytes(sh->batch, p2);
     if (smem > 227 * 1024) return fail(PA_ERR_UNSUPPORTED, "schedule needs %zu bytes of shared memory", smem);
     cudaError_t e = pa::launch_schedule(seq_lens_dev, sh->batch, sh->num_kv_heads, sh->max_pages_per_seq,

@@ -5,7 +5,8 @@
 // region).  Same split rule and packed layout as pa_get_metadata; the items,
 // sorted longest first, are dealt to the CTAs in "snake" rounds (0..grid-1,
 // then grid-1..0, ...) instead of least-loaded-first, which is sequential.
-// One CTA of 1024 threads; shared memory holds the sort keys and the
+// One CTA of 128 to 1024 threads (a power of two the launcher sizes to the
+// batch and the split capacity); shared memory holds the sort keys and the
 // per-sequence page counts, split counts and split offsets.
 #include <algorithm>
 
@@ -15,7 +16,8 @@
 namespace pa {
 namespace {
 
-constexpr int kThreads = 1024;
+constexpr int kMaxThreads = 1024;
+constexpr int kMaxPer = 16;  // sort keys per thread: 16384 splits / 1024 threads
 
 __device__ __forceinline__ long long block_sum(long long v, long long* tmp) {
     for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
@@ -23,7 +25,7 @@ __device__ __forceinline__ long long block_sum(long long v, long long* tmp) {
     if (l == 0) tmp[w] = v;
     __syncthreads();
     if (threadIdx.x < 32) {
-        long long t = tmp[threadIdx.x];
+        long long t = threadIdx.x < (blockDim.x >> 5) ? tmp[threadIdx.x] : 0;
         for (int o = 16; o > 0; o >>= 1) t += __shfl_xor_sync(0xffffffffu, t, o);
         if (threadIdx.x == 0) tmp[0] = t;
     }
@@ -35,7 +37,8 @@ __device__ __forceinline__ long long block_sum(long long v, long long* tmp) {
 
 // out[i] = in[0] + ... + in[i-1] for i in [0, n]
 __device__ void block_exclusive_scan(const int* in, int* out, int n, int* tmp) {
-    const int per = (n + kThreads - 1) / kThreads;
+    const int nw = blockDim.x >> 5;
+    const int per = (n + blockDim.x - 1) / blockDim.x;
     const int lo = min(n, (int)threadIdx.x * per), hi = min(n, lo + per);
     int local = 0;
     for (int i = lo; i < hi; ++i) local += in[i];
@@ -48,7 +51,7 @@ __device__ void block_exclusive_scan(const int* in, int* out, int n, int* tmp) {
     if (l == 31) tmp[w] = x;
     __syncthreads();
     if (threadIdx.x < 32) {  // inclusive scan of the warp totals
-        int t = tmp[threadIdx.x];
+        int t = threadIdx.x < nw ? tmp[threadIdx.x] : 0;
         for (int o = 1; o < 32; o <<= 1) {
             const int y = __shfl_up_sync(0xffffffffu, t, o);
             if (threadIdx.x >= o) t += y;
@@ -61,16 +64,19 @@ __device__ void block_exclusive_scan(const int* in, int* out, int n, int* tmp) {
         out[i] = run;
         run += in[i];
     }
-    if (threadIdx.x == 0) out[n] = tmp[31];
+    if (threadIdx.x == 0) out[n] = tmp[nw - 1];
     __syncthreads();
 }
 
-__global__ void __launch_bounds__(kThreads, 1)
+// T threads; below 1024 the launcher gives at most 4 sort keys a thread
+template <int T>
+__global__ void __launch_bounds__(T, 1)
     schedule_kernel(const int32_t* seq_lens, int B, int Hk, int max_pages, int cps, int cap, int forced,
                     int p2cap, int32_t* meta) {
+    constexpr int kPer = T == kMaxThreads ? kMaxPer : 4;
     allow_dependents_launch();  // the decode kernel's prologue overlaps this one
     extern __shared__ unsigned long long dyn[];
-    unsigned long long* key = dyn;                              // [p2cap]
+    unsigned long long* key = dyn;                              // [p2cap >= the split count]
     int* pages = reinterpret_cast<int*>(dyn + p2cap);           // [B]
     int* nsp = pages + B;                                       // [B]
     int* ind = nsp + B;                                         // [B + 1]
@@ -78,7 +84,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     __shared__ int tmp32[32];
 
     long long local = 0;
-    for (int b = threadIdx.x; b < B; b += kThreads) {
+    for (int b = threadIdx.x; b < B; b += T) {
         const int len = max(seq_lens[b], 0);
         const int p = min((len + kPage - 1) / kPage, max_pages);
         pages[b] = p;
@@ -87,7 +93,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const long long units = block_sum(local, tmp64) * Hk;
     const long long shares = 2LL * cap;  // two items per CTA share
     const long long chunk = max(4LL, (units + shares - 1) / shares);
-    for (int b = threadIdx.x; b < B; b += kThreads) {
+    for (int b = threadIdx.x; b < B; b += T) {
         const int p = pages[b];
         int n;
         if (p <= 1) n = 1;
@@ -106,9 +112,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     // that order is the splits' order (cost descending, split index
     // ascending) with each split expanded over its KV heads in order: sort the
     // splits, not the items.
+    // keys: [63:32] 0x7FFFFFFF - cost, [31:14] b, [13:0] g (the host checks
+    // give g < 16384 and b < 8192); b never decreases as g grows, so the low
+    // word orders as g does and the final pass needs no search for b
     int p2 = 1;
     while (p2 < total) p2 <<= 1;
-    for (int g = threadIdx.x; g < p2; g += kThreads) {
+    for (int g = threadIdx.x; g < p2; g += T) {
         unsigned long long k = ~0ull;
         if (g < total) {
             int lo = 0, hi = B - 1;  // last b with ind[b] <= g
@@ -119,47 +128,49 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             const int b = lo, s = g - ind[b], n = nsp[b], p = pages[b];
             const int cost = (int)(((long long)(s + 1) * p) / n - ((long long)s * p) / n) + 1;
-            k = ((unsigned long long)(unsigned)(0x7FFFFFFF - cost) << 32) | (unsigned)g;
+            k = ((unsigned long long)(unsigned)(0x7FFFFFFF - cost) << 32) | ((unsigned)b << 14) | (unsigned)g;
         }
         key[g] = k;
     }
     __syncthreads();
     // Bitonic sort.  The keys are unique, so the sorted order is too and any
     // sorting network reproduces the host rule's order.  Thread t holds the
-    // keys at positions k * kThreads + t in registers; the stages whose
-    // partner (position ^ stride) lies in the same warp run as shuffles with no
-    // barrier, the others through shared memory.
-    constexpr int kMaxPer = 16;  // 16384 splits (Hk = 1) / kThreads
-    const int per = p2 > kThreads ? p2 / kThreads : 1;
-    unsigned long long kr[kMaxPer];
+    // keys at positions k * T + t in registers (T >= p2 / 16 by the
+    // launcher); the stages whose partner (position ^ stride) lies in the same
+    // warp run as shuffles with no barrier, in the warps that hold keys only,
+    // the others through shared memory.
+    const int per = p2 > T ? p2 / T : 1;
+    const bool holds = (int)(threadIdx.x & ~31u) < p2;  // warp-uniform
+    unsigned long long kr[kPer];
 #pragma unroll
-    for (int k = 0; k < kMaxPer; ++k) {
-        const int pos = k * kThreads + threadIdx.x;
+    for (int k = 0; k < kPer; ++k) {
+        const int pos = k * T + threadIdx.x;
         kr[k] = (k < per && pos < p2) ? key[pos] : ~0ull;
     }
     for (int size = 2; size <= p2; size <<= 1) {
         for (int stride = size >> 1; stride > 0; stride >>= 1) {
             if (stride < 32) {
+                if (!holds) continue;
 #pragma unroll
-                for (int k = 0; k < kMaxPer; ++k) {
+                for (int k = 0; k < kPer; ++k) {
                     if (k >= per) break;
-                    const int pos = k * kThreads + threadIdx.x;
+                    const int pos = k * T + threadIdx.x;
                     const unsigned long long other = __shfl_xor_sync(0xffffffffu, kr[k], stride);
                     const bool keep_min = ((pos & stride) == 0) == ((pos & size) == 0);
                     kr[k] = keep_min ? min(kr[k], other) : max(kr[k], other);
                 }
             } else {
 #pragma unroll
-                for (int k = 0; k < kMaxPer; ++k) {
+                for (int k = 0; k < kPer; ++k) {
                     if (k >= per) break;
-                    const int pos = k * kThreads + threadIdx.x;
+                    const int pos = k * T + threadIdx.x;
                     if (pos < p2) key[pos] = kr[k];
                 }
                 __syncthreads();
 #pragma unroll
-                for (int k = 0; k < kMaxPer; ++k) {
+                for (int k = 0; k < kPer; ++k) {
                     if (k >= per) break;
-                    const int pos = k * kThreads + threadIdx.x;
+                    const int pos = k * T + threadIdx.x;
                     if (pos < p2) {
                         const unsigned long long other = key[pos ^ stride];
                         const bool keep_min = ((pos & stride) == 0) == ((pos & size) == 0);
@@ -171,9 +182,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
     }
 #pragma unroll
-    for (int k = 0; k < kMaxPer; ++k) {
+    for (int k = 0; k < kPer; ++k) {
         if (k >= per) break;
-        const int pos = k * kThreads + threadIdx.x;
+        const int pos = k * T + threadIdx.x;
         if (pos < p2) key[pos] = kr[k];
     }
     __syncthreads();
@@ -188,27 +199,22 @@ __global__ void __launch_bounds__(kThreads, 1)
         meta[6] = (int)min(chunk, (long long)0x7FFFFFFF);
         meta[7] = cps;
     }
-    for (int b = threadIdx.x; b < B; b += kThreads) meta[kMetaHeader + b] = nsp[b];
-    for (int b = threadIdx.x; b <= B; b += kThreads) meta[kMetaHeader + B + b] = ind[b];
+    for (int b = threadIdx.x; b < B; b += T) meta[kMetaHeader + b] = nsp[b];
+    for (int b = threadIdx.x; b <= B; b += T) meta[kMetaHeader + B + b] = ind[b];
     const int full = items / grid, rem = items % grid;
     const bool last_even = (full & 1) == 0;
     int32_t* cta_ptr = meta + kMetaHeader + 2 * B + 1;
-    for (int c = threadIdx.x; c <= grid; c += kThreads)
+    for (int c = threadIdx.x; c <= grid; c += T)
         cta_ptr[c] = c * full + (last_even ? min(c, rem) : max(0, c - (grid - rem)));
     int32_t* out_items = cta_ptr + grid + 1;
-    for (int r = threadIdx.x; r < items; r += kThreads) {
-        const int g = (int)(key[r / Hk] & 0xFFFFFFFFu), kvh = r % Hk;
-        int lo = 0, hi = B - 1;
-        while (lo < hi) {
-            const int mid = (lo + hi + 1) >> 1;
-            if (ind[mid] <= g) lo = mid;
-            else hi = mid - 1;
-        }
+    for (int r = threadIdx.x; r < items; r += T) {
+        const unsigned long long kk = key[r / Hk];
+        const int g = (int)(kk & 0x3FFFu), b = (int)((kk >> 14) & 0x3FFFFu), kvh = r % Hk;
         const int rnd = r / grid, pos = r % grid;
         const int c = (rnd & 1) == 0 ? pos : grid - 1 - pos;
         const int slot = c * full + (last_even ? min(c, rem) : max(0, c - (grid - rem))) + rnd;
-        out_items[2 * slot] = lo;
-        out_items[2 * slot + 1] = ((g - ind[lo]) << 16) | kvh;
+        out_items[2 * slot] = b;
+        out_items[2 * slot + 1] = ((g - ind[b]) << 16) | kvh;
     }
 }
 
@@ -287,13 +293,26 @@ size_t schedule_smem_bytes(int B, int p2cap) { return (size_t)p2cap * 8 + (size_
 cudaError_t launch_schedule(const int32_t* seq_lens, int B, int Hk, int max_pages, int cps, int cap, int forced,
                             int p2cap, int32_t* meta, cudaStream_t stream) {
     const size_t smem = schedule_smem_bytes(B, p2cap);
+    // a power of two with at most 4 sort keys and 4 sequences a thread, up to
+    // 1024 threads (then at most kMaxPer = 16 keys, p2cap <= 16384)
+    int threads = 128;
+    while (threads < kMaxThreads && (threads * 4 < p2cap || threads * 4 < B)) threads <<= 1;
+    if (threads * (threads == kMaxThreads ? kMaxPer : 4) < p2cap) return cudaErrorInvalidValue;
     // the attribute is per kernel and device: set it once per device, to the
-    // largest size the host checks allow (16384 items, 8192 sequences)
-    static std::atomic<uint64_t> configured{0};
-    cudaError_t e = ensure_dynamic_smem(schedule_kernel, (int)schedule_smem_bytes(kMaxBatch, 16384), configured);
-    if (e != cudaSuccess) return e;
-    schedule_kernel<<<1, kThreads, smem, stream>>>(seq_lens, B, Hk, max_pages, cps, cap, forced, p2cap, meta);
-    return cudaGetLastError();
+    // largest size the host checks allow (16384 splits, 8192 sequences)
+    static std::atomic<uint64_t> configured[4] = {};
+    auto go = [&](auto kernel, std::atomic<uint64_t>& done) {
+        cudaError_t e = ensure_dynamic_smem(kernel, (int)schedule_smem_bytes(kMaxBatch, 16384), done);
+        if (e != cudaSuccess) return e;
+        kernel<<<1, threads, smem, stream>>>(seq_lens, B, Hk, max_pages, cps, cap, forced, p2cap, meta);
+        return cudaGetLastError();
+    };
+    switch (threads) {
+        case 128: return go(schedule_kernel<128>, configured[0]);
+        case 256: return go(schedule_kernel<256>, configured[1]);
+        case 512: return go(schedule_kernel<512>, configured[2]);
+        default: return go(schedule_kernel<1024>, configured[3]);
+    }
 }
 
 cudaError_t launch_page_table(const int32_t* kv_indices, int64_t num_indices, const int32_t* kv_lens, int B,

@@ -40,9 +40,9 @@ def device_meta(sh, lens):
     return plan, meta
 
 
-@pytest.mark.parametrize("case", ["uniform", "lognormal", "forced", "edges", "single", "large", "wide"])
+@pytest.mark.parametrize("case", ["uniform", "lognormal", "forced", "edges", "single", "mid", "large", "wide"])
 def test_device_schedule_bit_exact(case):
-    cases = ["uniform", "lognormal", "forced", "edges", "single", "large", "wide"]
+    cases = ["uniform", "lognormal", "forced", "edges", "single", "large", "wide", "mid"]
     rng = np.random.default_rng(100 + cases.index(case))
     if case == "uniform":
         lens, hk, forced, mp = rng.integers(1, 4097, 64), 8, 0, 64
@@ -54,6 +54,8 @@ def test_device_schedule_bit_exact(case):
         lens, hk, forced, mp = np.array([0, 1, 63, 64, 65, 128, 129, 4096, 0, 5000]), 2, 0, 100
     elif case == "single":
         lens, hk, forced, mp = np.array([1]), 1, 0, 1
+    elif case == "mid":  # ~1000 splits: the 256-thread schedule
+        lens, hk, forced, mp = rng.integers(0, 3001, 900), 4, 0, 64
     elif case == "large":  # ~14700 items
         lens, hk, forced, mp = rng.integers(0, 2001, 1800), 8, 0, 32
     else:  # one KV head: as many splits as items, the sort's 16 keys per thread
