@@ -132,3 +132,43 @@ def test_cuda_graph_replay_with_new_lengths():
         assert np.array_equal(np.isneginf(l), np.isneginf(ref_lse))
         assert np.abs(l[fin] - ref_lse[fin]).max() <= 1e-3
     assert B.pa_check_status(ws) == B.PA_OK
+
+
+def test_cuda_graph_replay_full_size():
+    """The graph-replayed decode at the bench's full size (B=64, Hq=32, Hk=8,
+    D=128, lengths U[1,4096]): the scheduler and the decode captured once,
+    replayed with the workload's lengths and then with shorter random ones;
+    every sequence against the oracle."""
+    inp = W.gqa_decode(0)
+    dev = "cuda"
+    q, kp, vp = ops.as_bf16(inp.q, dev), ops.as_bf16(inp.k_pool, dev), ops.as_bf16(inp.v_pool, dev)
+    bt = torch.from_numpy(inp.block_table).to(dev)
+    sl = torch.from_numpy(inp.seq_lens.copy()).to(dev)
+    sh = shapes(inp.batch, 32, 8, inp.max_pages, inp.num_pool_pages)
+    plan = B.pa_get_static_plan(sh)
+    meta = torch.zeros(plan.meta_ints, dtype=torch.int32, device=dev)
+    ws = torch.zeros(plan.workspace_bytes, dtype=torch.uint8, device=dev)
+    out = torch.empty((inp.batch, 32, 128), dtype=torch.bfloat16, device=dev)
+    lse = torch.empty((inp.batch, 32), dtype=torch.float32, device=dev)
+    s = torch.cuda.Stream()
+
+    def step():
+        B.pa_get_metadata_device(sh, plan, sl, meta, stream=s)
+        B.pa_decode(sh, plan, q, kp, vp, None, None, bt, sl, meta, inp.scale, out, lse, ws, stream=s)
+
+    with torch.cuda.stream(s):
+        step()
+    s.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        step()
+    rng = np.random.default_rng(72)
+    for lens in (inp.seq_lens, np.minimum(inp.seq_lens, rng.integers(1, 4097, inp.batch)).astype(np.int32)):
+        sl.copy_(torch.from_numpy(np.ascontiguousarray(lens)))
+        g.replay()
+        torch.cuda.synchronize()
+        ref_out, ref_lse = oracle.decode(inp.q, inp.k_pool, inp.v_pool, inp.block_table, lens, inp.scale)
+        err = np.abs(out.float().cpu().numpy() - ref_out)
+        assert err.max() <= 1e-2 and err.mean() <= 1e-3, f"max abs err {err.max():.3g}"
+        assert np.abs(lse.cpu().numpy() - ref_lse).max() <= 1e-3
+    assert B.pa_check_status(ws) == B.PA_OK

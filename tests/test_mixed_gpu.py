@@ -22,11 +22,14 @@ def gpu():
     build()
 
 
-def run_mixed(q_lens, kv_lens, hq=8, hk=2, seed=60, dtype="bf16"):
-    inp = W.make_paged_prefill(q_lens, kv_lens, hq, hk, 128, seed=seed, extra_pages=2, dtype=dtype)
+def mixed_gpu(inp, dtype="bf16"):
+    """One pa_mixed call over a paged prefill input (its leading one-row
+    sequences become the decode part); returns out, lse, the plan and both
+    parts' status words."""
     dev = "cuda"
-    kl = np.asarray(kv_lens, np.int32)
-    sh = B.pa_mixed_shapes(batch=len(q_lens), num_q_heads=hq, num_kv_heads=hk, head_dim=128, page_size=64,
+    hq, hk = inp.num_q_heads, inp.num_kv_heads
+    kl = np.diff(inp.cu_seqlens_k).astype(np.int32)
+    sh = B.pa_mixed_shapes(batch=inp.batch, num_q_heads=hq, num_kv_heads=hk, head_dim=128, page_size=64,
                            max_pages_per_seq=inp.block_table.shape[1], num_pool_pages=inp.k.shape[0],
                            kv_dtype=B.PA_KV_FP16 if dtype == "f16" else B.PA_KV_BF16, num_sms=ops.num_sms(),
                            ctas_per_sm=0, forced_splits=0)
@@ -42,9 +45,15 @@ def run_mixed(q_lens, kv_lens, hq=8, hk=2, seed=60, dtype="bf16"):
     # status words of both parts (decode workspace first, prefill after it)
     dec = (plan.decode.workspace_bytes + 255) // 256 * 256 if plan.num_decode else 0
     st = (B.pa_check_status(ws), B.pa_check_status(ws[dec:]))
+    return out.float().cpu().numpy(), lse.cpu().numpy(), plan, st
+
+
+def run_mixed(q_lens, kv_lens, hq=8, hk=2, seed=60, dtype="bf16"):
+    inp = W.make_paged_prefill(q_lens, kv_lens, hq, hk, 128, seed=seed, extra_pages=2, dtype=dtype)
+    out, lse, plan, st = mixed_gpu(inp, dtype)
     ro, rl = oracle.prefill(inp.q, inp.k, inp.v, inp.cu_seqlens_q, inp.cu_seqlens_k, inp.scale, True,
                             block_table=inp.block_table, dtype=dtype)
-    return out.float().cpu().numpy(), lse.cpu().numpy(), ro, rl, plan, st
+    return out, lse, ro, rl, plan, st
 
 
 @pytest.mark.parametrize("q_lens,kv_lens", [
@@ -71,3 +80,23 @@ def test_mixed_batch_fp16():
     err = np.abs(out - ro)
     assert np.all(np.isfinite(out)) and err.max() <= 1e-2 and err.mean() <= 1e-3
     assert np.abs(lse - rl).max() <= 1e-3
+
+
+def test_mixed_full_size_sampled():
+    """The bench's mixed step at full size (64 decodes of kv U[1,4096], then
+    8 x 512-token chunks after a prefix U[0,8192]; Hq=32, Hk=8, D=128): every
+    decode row and sampled rows of every chunk against the oracle."""
+    from tests.test_prefill_gpu import sample_rows
+    inp = W.mixed_batch(0)
+    out, lse, plan, st = mixed_gpu(inp)
+    assert st == (B.PA_OK, B.PA_OK) and plan.num_decode == 64
+    rows = sample_rows(inp, per_seq=24)
+    ro, rl = oracle.prefill(inp.q, inp.k, inp.v, inp.cu_seqlens_q, inp.cu_seqlens_k, inp.scale, True,
+                            block_table=inp.block_table, rows=rows)
+    hq = inp.num_q_heads
+    o, l = out.reshape(-1, 128)[rows], lse.reshape(-1)[rows]
+    assert np.all(np.isfinite(out))
+    err = np.abs(o - ro)
+    assert err.max() <= 1e-2 and err.mean() <= 1e-3, f"max abs err {err.max():.3g}"
+    assert np.abs(l - rl).max() <= 1e-3
+    assert len({int(r) // hq for r in rows if int(r) // hq < 64}) == 64  # every decode row sampled
