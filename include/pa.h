@@ -175,6 +175,15 @@ pa_status pa_get_metadata_device(const pa_decode_shapes* shapes, const pa_decode
  *
  * With fp8 KV the query is used in fp16 (exact for |q| in [2^-14, 65504];
  * smaller magnitudes round to fp16 subnormals).
+ *
+ * Stream order: the call is asynchronous on `stream`.  For every page type
+ * but e4m3 at D = 128 (which has a kernel of its own, launched plainly) the
+ * kernel is launched with programmatic stream serialization: its CTAs may
+ * start their shared-memory set-up while the
+ * previous kernel in the stream finishes, and touch no global memory until
+ * that kernel has completed, so every input written and every buffer read by
+ * earlier work in the stream is ordered as for a plain launch.  Under stream
+ * capture that dependency becomes a programmatic edge of the graph.
  */
 pa_status pa_decode(const pa_decode_shapes* shapes, const pa_decode_plan* plan, const void* q,
                     const void* k_pool, const void* v_pool, const float* k_scale, const float* v_scale,
