@@ -391,7 +391,6 @@ __global__ void __launch_bounds__(DecodeLayout<D, FP8>::kThreads, 1)
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
-    allow_dependents_launch();
     const uint32_t tbase = tmem_base_sh;
 
     if (warp == 0) {
@@ -802,6 +801,10 @@ __global__ void __launch_bounds__(DecodeLayout<D, FP8>::kThreads, 1)
         }
     }
 
+    // the next programmatic launch may take this SM once every CTA is here
+    // (issued after the prologue instead, its CTAs would wait on the SMs of
+    // this launch's tail: 0.6% slower)
+    allow_dependents_launch();
     __syncthreads();
     if (warp == 1) {
         tc_fence_after();
