@@ -18,7 +18,6 @@ Inputs are the raw bit-pattern arrays produced by the seeded generator
 from __future__ import annotations
 
 import ctypes
-import os
 from typing import Optional
 
 import numpy as np
