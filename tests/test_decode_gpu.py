@@ -229,3 +229,27 @@ def test_fp16_decode(hq, hk, d):
     assert st == B.PA_OK
     ref_out, ref_lse = reference(inp)
     assert_close(out, lse, ref_out, ref_lse, "f16")
+
+
+def test_max_batch_host_and_device_plans():
+    """8192 sequences, the most the device scheduler takes, lengths U[0, 300]
+    (empty, one-page and multi-page sequences mixed), Hq=4, Hk=1, D=64: the
+    host plan and the device-written plan both against the oracle."""
+    bsz = 8192
+    lens = np.random.default_rng(91).integers(0, 301, bsz).astype(np.int32)
+    inp = W.make_decode(bsz, 4, 1, 64, lens, seed=91)
+    ref_out, ref_lse = reference(inp)
+    out, lse, st, p = run(inp)
+    assert st == B.PA_OK
+    assert_close(out, lse, ref_out, ref_lse, "bf16")
+    q, kp, vp, bt, sl, _, _ = to_dev(inp)
+    sh = p.shapes
+    plan = B.pa_get_static_plan(sh)
+    meta = torch.zeros(plan.meta_ints, dtype=torch.int32, device="cuda")
+    ws = torch.zeros(plan.workspace_bytes, dtype=torch.uint8, device="cuda")
+    o2 = torch.empty((bsz, 4, 64), dtype=torch.bfloat16, device="cuda")
+    l2 = torch.empty((bsz, 4), dtype=torch.float32, device="cuda")
+    B.pa_get_metadata_device(sh, plan, sl, meta)
+    B.pa_decode(sh, plan, q, kp, vp, None, None, bt, sl, meta, inp.scale, o2, l2, ws)
+    assert B.pa_check_status(ws) == B.PA_OK
+    assert_close(o2.float().cpu().numpy(), l2.cpu().numpy(), ref_out, ref_lse, "bf16")
