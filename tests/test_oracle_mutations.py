@@ -7,6 +7,7 @@ on the CPU, points the oracle module at it, and runs the pins of
 its input); the case passes when one does.  The oracle's own source and
 library are not touched.
 """
+import importlib.util
 import inspect
 import os
 import shutil
@@ -16,6 +17,7 @@ import pytest
 
 import oracle
 from oracle import build as oracle_build
+from oracle import scheduler as scheduler_src
 from tests import test_oracle as pins
 
 # (mistake, text in the oracle's source, replacement, which occurrence, occurrences)
@@ -36,26 +38,60 @@ MUTATIONS = [
      "kd[j * Dqk + Dk + d] = 0.0;", 0, 1),
     ("e4m3 exponent bias 8", "mag = ldexp(1.0 + (double)m / 8.0, e - 7);",
      "mag = ldexp(1.0 + (double)m / 8.0, e - 8);", 0, 1),
+    ("append: page row p / 64", "int64_t dst = ((page * Hk + h) * ORACLE_PAGE + p % ORACLE_PAGE) * D;",
+     "int64_t dst = ((page * Hk + h) * ORACLE_PAGE + p / ORACLE_PAGE) * D;", 0, 1),
+    ("append: e4m3 scale multiplied", "float kf = (float)oracle_bf16_to_double(k_new[src + d]) / k_scale[h];",
+     "float kf = (float)oracle_bf16_to_double(k_new[src + d]) * k_scale[h];", 0, 1),
+    ("fp8 MLA: q_scale dropped", "double qs = (double)q_scale[h], ks = (double)k_scale[g];",
+     "double qs = 1.0, ks = (double)k_scale[g];", 0, 1),
+    ("fp8 MLA: k_scale of head 0", "double qs = (double)q_scale[h], ks = (double)k_scale[g];",
+     "double qs = (double)q_scale[h], ks = (double)k_scale[0];", 0, 1),
+    ("e4m3 rope key: token scale dropped", "double rs = (double)k_rope_scales[t];", "double rs = 1.0;", 0, 1),
+]
+
+# the same for the scheduler's restatement (oracle/scheduler.py) and its pins
+SCHEDULER_MUTATIONS = [
+    ("chunk rounded down", "chunk = max(MIN_CHUNK, _cdiv(units, cap * ITEMS_PER_SHARE))",
+     "chunk = max(MIN_CHUNK, units // (cap * ITEMS_PER_SHARE))"),
+    ("last split one page long", "return (s * pages) // nsplit, ((s + 1) * pages) // nsplit",
+     "return (s * pages) // nsplit, ((s + 1) * pages) // nsplit + (s + 1 == nsplit)"),
+    ("item cost without the +1", "items.append((hi - lo + 1, len(items), b, s, kvh))",
+     "items.append((hi - lo, len(items), b, s, kvh))"),
+    ("ties by descending index", "key=lambda it: (-it[0], it[1])", "key=lambda it: (-it[0], -it[1])"),
+    ("snake dealing without the turn", "per_cta[pos if rnd % 2 == 0 else grid - 1 - pos]", "per_cta[pos]"),
+    ("forced splits not capped by the pages", "n.append(min(forced_splits, p, MAX_SPLITS))",
+     "n.append(min(forced_splits, MAX_SPLITS))"),
 ]
 
 
-def pin_calls():
-    """Every pin of tests/test_oracle.py as a no-argument call (parametrized
-    pins once per parameter value)."""
+def pin_calls(module=pins):
+    """Every pin of a test module as a no-argument call (parametrized pins once
+    per parameter set)."""
     calls = []
-    for name, fn in inspect.getmembers(pins, inspect.isfunction):
-        if not name.startswith("test_") or fn.__module__ != pins.__name__:
+    for name, fn in inspect.getmembers(module, inspect.isfunction):
+        if not name.startswith("test_") or fn.__module__ != module.__name__:
             continue
         params = list(inspect.signature(fn).parameters)
         if not params:
             calls.append((name, fn, {}))
             continue
         marks = [m for m in getattr(fn, "pytestmark", []) if m.name == "parametrize"]
-        assert len(marks) == 1 and len(params) == 1, f"{name}: one parametrized argument expected"
-        argname, values = marks[0].args[0], marks[0].args[1]
-        for v in values:
-            calls.append((f"{name}[{v}]", fn, {argname: v}))
+        assert len(marks) == 1, f"{name}: one parametrize mark expected"
+        argnames = [x.strip() for x in marks[0].args[0].split(",")]
+        assert sorted(argnames) == sorted(params), f"{name}: every argument comes from the mark"
+        for v in marks[0].args[1]:
+            kw = dict(zip(argnames, v if len(argnames) > 1 else (v,)))
+            calls.append((f"{name}[{v}]", fn, kw))
     return calls
+
+
+def first_failing_pin(module):
+    for name, fn, kw in pin_calls(module):
+        try:
+            fn(**kw)
+        except Exception:  # a failed assertion, or the oracle refusing its input
+            return name
+    return None
 
 
 def build_mutant(tmp_path, old, new, which, count):
@@ -81,15 +117,35 @@ def test_a_planted_mistake_fails_a_pin(tmp_path, monkeypatch, mistake, old, new,
     monkeypatch.setattr(oracle, "_LIB", lib)
     monkeypatch.setattr(oracle, "_lib", None)
     monkeypatch.setattr(oracle, "_build", lambda *a, **k: lib)
-    caught = None
-    for name, fn, kw in pin_calls():
-        try:
-            fn(**kw)
-        except Exception:  # a failed assertion, or the oracle refusing its input
-            caught = name
-            break
+    caught = first_failing_pin(pins)
     monkeypatch.setattr(oracle, "_lib", None)  # the next user reloads the real library
     assert caught is not None, f"no pin fails with the mistake: {mistake}"
+
+
+@pytest.mark.parametrize("mistake,old,new", SCHEDULER_MUTATIONS, ids=[m[0] for m in SCHEDULER_MUTATIONS])
+def test_a_planted_scheduler_mistake_fails_a_pin(tmp_path, monkeypatch, mistake, old, new):
+    from tests import test_scheduler_oracle as sched_pins
+    src = open(scheduler_src.__file__).read()
+    assert src.count(old) == 1, f"the scheduler source changed: {old!r}"
+    path = tmp_path / "scheduler_mutant.py"
+    path.write_text(src.replace(old, new))
+    spec = importlib.util.spec_from_file_location("scheduler_mutant", path)
+    mutant = importlib.util.module_from_spec(spec)
+    spec.loader.exec_module(mutant)
+    monkeypatch.setattr(sched_pins, "S", mutant)
+    assert first_failing_pin(sched_pins) is not None, f"no pin fails with the mistake: {mistake}"
+
+
+def test_scheduler_pins_pass_on_an_unmodified_copy(tmp_path, monkeypatch):
+    from tests import test_scheduler_oracle as sched_pins
+    path = tmp_path / "scheduler_copy.py"
+    path.write_text(open(scheduler_src.__file__).read())
+    spec = importlib.util.spec_from_file_location("scheduler_copy", path)
+    copy = importlib.util.module_from_spec(spec)
+    spec.loader.exec_module(copy)
+    monkeypatch.setattr(sched_pins, "S", copy)
+    for name, fn, kw in pin_calls(sched_pins):
+        fn(**kw)
 
 
 def test_pins_pass_on_the_unmodified_source(tmp_path, monkeypatch):
@@ -99,7 +155,7 @@ def test_pins_pass_on_the_unmodified_source(tmp_path, monkeypatch):
     monkeypatch.setattr(oracle, "_LIB", lib)
     monkeypatch.setattr(oracle, "_lib", None)
     monkeypatch.setattr(oracle, "_build", lambda *a, **k: lib)
-    for name, fn, kw in pin_calls():
+    for name, fn, kw in pin_calls(pins):
         fn(**kw)
     monkeypatch.setattr(oracle, "_lib", None)
     assert os.path.exists(lib)

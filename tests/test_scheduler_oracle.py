@@ -103,6 +103,30 @@ def test_snake_dealing_properties():
     assert max(sizes) - min(sizes) <= 1  # one item per CTA per round
 
 
+def test_chunk_is_rounded_up_worked_by_hand():
+    """One sequence of 1001 pages, one KV head, 10 CTAs: units / (2 items a
+    CTA share x 10) = 1001 / 20 = 50.05, so chunk = 51 (rounded up, and above
+    the floor of 4), and the sequence takes ceil(1001 / 51) = ceil(19.6) = 20
+    splits of 50 or 51 pages."""
+    u = S.unpack(S.schedule([1001 * 64], 1, 10, 1))
+    assert u["chunk"] == 51
+    assert u["n_splits"] == [20] and u["total_splits"] == 20
+    widths = [hi - lo for lo, hi in (S.split_range(1001, 20, s) for s in range(20))]
+    assert sorted(set(widths)) == [50, 51] and sum(widths) == 1001
+
+
+def test_snake_dealing_worked_by_hand():
+    """Six one-split sequences of 5, 4, 3, 2, 1 and 0 pages (one KV head, one
+    split each): item costs 6, 5, 4, 3, 2, 1 (pages + 1), already longest
+    first.  Three CTAs take them in the rounds 0, 1, 2 then 2, 1, 0, so CTA 0
+    holds sequences 0 and 5, CTA 1 sequences 1 and 4, CTA 2 sequences 2 and 3:
+    every CTA carries a cost of 7."""
+    u = S.unpack(S.schedule([5 * 64, 4 * 64, 3 * 64, 2 * 64, 64, 0], 1, 3, 1, forced_splits=1, dealing="snake"))
+    cp = u["cta_indptr"]
+    per_cta = [[b for b, _, _ in u["items"][cp[c]:cp[c + 1]]] for c in range(3)]
+    assert per_cta == [[0, 5], [1, 4], [2, 3]]
+
+
 @pytest.mark.parametrize("hk,sms,cps,forced", [(8, 152, 1, 0), (1, 4, 2, 0), (3, 7, 1, 5)])
 def test_static_capacity_bounds_every_length_mix(hk, sms, cps, forced):
     rng = np.random.default_rng(hk * 10 + sms)
