@@ -61,6 +61,11 @@ SCHEDULER_MUTATIONS = [
     ("snake dealing without the turn", "per_cta[pos if rnd % 2 == 0 else grid - 1 - pos]", "per_cta[pos]"),
     ("forced splits not capped by the pages", "n.append(min(forced_splits, p, MAX_SPLITS))",
      "n.append(min(forced_splits, MAX_SPLITS))"),
+    ("flat page list: page count rounded down", "counts.append((n + page_size - 1) // page_size)",
+     "counts.append(n // page_size)"),
+    ("flat page list: offset not advanced", "        start += c\n    return table", "    return table"),
+    ("flat page list: ids right-aligned", "table[b][j] = int(kv_indices[start + j])",
+     "table[b][width - c + j] = int(kv_indices[start + j])"),
 ]
 
 
