@@ -267,3 +267,28 @@ def test_page_table_from_flat_host_validation(args, status, needle):
     with pytest.raises(B.PaError) as e:
         B.pa_page_table_from_flat(stream=1, **kw)
     assert e.value.status == status and needle in str(e.value)
+
+
+def test_missing_library_fails_loudly(monkeypatch, tmp_path):
+    """Without libpa.so every call raises: there is no CPU fallback."""
+    monkeypatch.setattr(B, "LIB_PATH", str(tmp_path / "libpa.so"))
+    monkeypatch.setattr(B, "_lib", None)
+    with pytest.raises(RuntimeError, match="not built"):
+        B.pa_version()
+    sh = B.pa_decode_shapes(batch=1, num_q_heads=1, num_kv_heads=1, head_dim=64, page_size=64, max_pages_per_seq=1,
+                            num_pool_pages=1, kv_dtype=B.PA_KV_BF16, num_sms=1, ctas_per_sm=0, forced_splits=0)
+    with pytest.raises(RuntimeError, match="not built"):
+        B.pa_get_metadata(np.array([1], np.int32), None, sh)
+
+
+def test_product_path_never_imports_the_oracle():
+    """The package's modules neither import nor load anything under oracle/."""
+    import os
+    import re
+    pkg = os.path.dirname(B.__file__)
+    for root, _, files in os.walk(pkg):
+        for f in files:
+            if f.endswith((".py", ".cu", ".h", ".cuh")):
+                src = open(os.path.join(root, f)).read()
+                assert not re.search(r"^\s*(import oracle|from oracle)", src, re.M), f
+                assert "liboracle" not in src and "oracle.c" not in src, f
