@@ -150,7 +150,8 @@ def prefill(q, k, v, cu_seqlens_q, cu_seqlens_k, scale: float, causal: bool = Tr
                             float(scale), _p(rr), nrows if rr is not None else 0,
                             _p(out), _p(lse), {"bf16": 0, "f16": 2}[dtype])
     if rc != 0:
-        raise ValueError("oracle_prefill: a referenced page id is out of range")
+        raise ValueError("oracle_prefill: a referenced page id is out of range, or a paged segment's kv_len "
+                         "exceeds max_pages * 64")
     if rr is None:
         return out.reshape(total_q, Hq, Dv), lse.reshape(total_q, Hq)
     return out, lse

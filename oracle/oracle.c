@@ -209,7 +209,9 @@ int oracle_decode(int B, int Hq, int Hk, int D, int max_pages, int64_t num_pages
  *   rows   optional list of (token * Hq + h) rows to evaluate (NULL: all);
  *          out/lse are then [nrows, Dv] / [nrows]
  *   elem_kind  0: q, k, v, k_rope are bf16; 2: fp16
- * Returns 0, or -1 on an out-of-range page id.
+ * Returns 0, or -1 on an out-of-range page id or (paged keys) a kv_len above
+ * max_pages * 64, which the block table cannot address (those rows are left
+ * as NaN).
  */
 int oracle_prefill(int B, int Hq, int Hk, int Dqk, int Dv, int rope_dim, int max_pages,
                    int64_t num_pages, const uint16_t* q, const uint16_t* k, const uint16_t* v,
@@ -242,6 +244,13 @@ int oracle_prefill(int B, int Hq, int Hk, int Dqk, int Dv, int rope_dim, int max
             if (n < 0) n = 0;
         }
         double* o = out + r * Dv;
+        if (block_table && kv_len > (int64_t)max_pages * ORACLE_PAGE) {
+            /* the segment's keys run past the block table's row */
+            for (int d = 0; d < Dv; ++d) o[d] = NAN;
+            lse[r] = NAN;
+            bad |= 1;
+            continue;
+        }
         double* qd = (double*)malloc(sizeof(double) * Dqk);
         double* kd = (double*)malloc(sizeof(double) * (size_t)(n ? n : 1) * Dqk);
         double* vd = (double*)malloc(sizeof(double) * (size_t)(n ? n : 1) * Dv);

@@ -319,6 +319,23 @@ def test_explicit_qo_offset_and_non_causal():
     assert np.all(np.isneginf(neg[1][:3, :])) and np.all(np.isfinite(neg[1][3:8]))
 
 
+def test_paged_prefill_refuses_keys_past_the_block_table():
+    """A paged segment's keys are addressed through its block-table row (the
+    FlashMLA paged-cache diagram: page block_table[b, j // 64], row j % 64); a
+    kv_len above max_pages * 64 has no page for its last keys, and the oracle
+    refuses it instead of reading the next row of the table."""
+    inp = W.make_paged_prefill([4, 4], [64, 100], 2, 1, 64, seed=25)
+    assert inp.block_table.shape[1] == 2
+    cu_k = inp.cu_seqlens_k.copy()
+    cu_k[1:] += 200  # sequence 0 now claims 264 keys, more than 2 pages hold
+    with pytest.raises(ValueError):
+        oracle.prefill(inp.q, inp.k, inp.v, inp.cu_seqlens_q, cu_k, inp.scale, True, block_table=inp.block_table)
+    # at exactly max_pages * 64 keys the call is valid
+    cu_ok = np.array([0, 128, 228], np.int32)
+    bt = inp.block_table.copy()
+    oracle.prefill(inp.q, inp.k, inp.v, inp.cu_seqlens_q, cu_ok, inp.scale, True, block_table=bt)
+
+
 def test_ragged_equals_separate_calls():
     inp = W.make_ragged_prefill([5, 40, 17], 4, 32, 32, seed=23, num_kv_heads=2)
     out, lse = oracle.prefill(inp.q, inp.k, inp.v, inp.cu_seqlens_q, inp.cu_seqlens_k, inp.scale, True)
