@@ -20,6 +20,7 @@ Prints one JSON line (rank 0).
 from __future__ import annotations
 
 import argparse
+import ctypes
 import hashlib
 import json
 import os
@@ -58,16 +59,29 @@ class L2Flush:
         torch.sum(self.buf, dim=0, out=self.out)
 
 
-def l2_policy(dev, input_bytes: int):
-    """Inputs of at least three times L2 need no flush: a step's first reads
-    evict whatever the previous step left.  Smaller inputs are flushed.
-    Returns (callable run between steps, the config note)."""
-    import torch
-    l2 = int(getattr(torch.cuda.get_device_properties(dev), "L2_cache_size", 0) or 129_000_000)
+NOMINAL_L2_BYTES = 129_000_000
+
+
+def l2_note_for(input_bytes: int, l2: int = NOMINAL_L2_BYTES) -> str:
+    """The config's statement of the L2 policy for a workload whose steps read
+    `input_bytes`: inputs of at least three times L2 need no flush (a step's
+    first reads evict whatever the previous step left); smaller ones are
+    flushed."""
     if input_bytes >= 3 * l2:
-        return NoFlush(), (f"no flush between steps: inputs larger than L2 ({input_bytes / 1e6:.0f} MB read "
-                           f"per step = {input_bytes / l2:.1f} x the {l2 / 1e6:.0f} MB L2)")
-    return L2Flush(dev), L2_NOTE
+        return f"no flush between steps: inputs larger than L2 ({input_bytes / 1e6:.0f} MB read per step, over 3x L2)"
+    return L2_NOTE
+
+
+def l2_policy(dev, input_bytes: int):
+    """Returns (callable run between steps, the config note), decided with the
+    device's own L2 size."""
+    import torch
+    l2 = int(getattr(torch.cuda.get_device_properties(dev), "L2_cache_size", 0) or NOMINAL_L2_BYTES)
+    note = l2_note_for(input_bytes, l2)
+    if note != l2_note_for(input_bytes):
+        raise RuntimeError(f"the L2 policy for {input_bytes} B differs between this device's L2 ({l2} B) and "
+                           f"the nominal {NOMINAL_L2_BYTES} B the reference arm states")
+    return (NoFlush() if note != L2_NOTE else L2Flush(dev)), note
 
 
 class NoFlush:
@@ -319,6 +333,29 @@ def prefill_flops(inp, causal=True):
     return pairs * inp.num_q_heads * (2 * inp.head_dim_qk + 2 * inp.head_dim_v)
 
 
+def decode_input_bytes(inp):
+    """Bytes a decode step reads from its inputs: K+V pages and the queries."""
+    return kv_bytes(inp)[0] + inp.q.size * 2
+
+
+def decode_config(inp, desc, world):
+    """The workload as both arms state it (nothing here depends on the implementation)."""
+    full, exact = kv_bytes(inp)
+    return {"workload": desc, "batch": inp.batch, "num_q_heads": inp.num_q_heads, "num_kv_heads": inp.num_kv_heads,
+            "head_dim": inp.head_dim, "page_size": 64, "kv_bytes_per_step": full, "kv_bytes_token_exact": exact,
+            "l2": l2_note_for(decode_input_bytes(inp)), "parallelism": f"replicas x{world}"}
+
+
+def prefill_config(inp, desc, world, extra=None):
+    """The workload as both arms state it (nothing here depends on the implementation)."""
+    nbytes = sum(np.asarray(a).nbytes for a in prefill_host_arrays(inp).values())
+    cfg = {"workload": desc, "total_q": int(inp.cu_seqlens_q[-1]), "num_q_heads": inp.num_q_heads,
+           "head_dim_qk": inp.head_dim_qk, "head_dim_v": inp.head_dim_v, "flops_per_step": prefill_flops(inp),
+           "l2": l2_note_for(nbytes), "parallelism": f"replicas x{world}"}
+    cfg.update(extra or {})
+    return cfg
+
+
 # ------------------------------------------------------------------ reference arm (the oracle)
 
 def cpu_oracle_decode_sample(inp, budget_s=None, steps=None, warmup=0):
@@ -407,7 +444,9 @@ def run_reference(args):
         line = {"impl": "reference", "metric": METRIC, "value": round(gbs, 4), "unit": "GB/s", "n_gpus": args.gpus,
                 "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(el / args.steps * 1e3, 4),
                 "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
-                "data": "synthetic", "config": {"workload": desc, "implementation": "CPU oracle append"},
+                "data": "synthetic", "implementation": "CPU oracle append",
+                "config": {"workload": desc, "bytes_per_step": 4 * int(qlen.sum()) * kn.shape[1] * 128 * 2,
+                           "l2": L2_NOTE, "parallelism": f"replicas x{args.gpus}"},
                 "cpu_baseline": {"value": round(gbs, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
                                  "sample": "one sequence's 512 new tokens per step"},
                 "e2e": {"value": round(gbs, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
@@ -420,7 +459,9 @@ def run_reference(args):
             "impl": "reference", "metric": METRIC, "value": round(tfs, 6), "unit": "TFLOP/s", "n_gpus": args.gpus,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(el / args.steps * 1e3, 4),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": {"workload": desc, "implementation": "fp64 CPU oracle (oracle/oracle.c), OpenMP"},
+            "implementation": "fp64 CPU oracle (oracle/oracle.c), OpenMP",
+            "config": prefill_config(inp, desc, args.gpus,
+                                     {"num_decode": int(inp.meta["num_decode"])} if args.workload == "mixed" else None),
             "cpu_baseline": {"value": round(tfs, 6), "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
                              "sample": f"{rows} random (token, head) query rows, 8 per step"},
             "e2e": {"value": round(tfs, 6), "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
@@ -434,7 +475,8 @@ def run_reference(args):
         "impl": "reference", "metric": METRIC, "value": round(gbs, 4), "unit": "GB/s", "n_gpus": args.gpus,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(el / done * 1e3, 4),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": desc, "implementation": "fp64 CPU oracle (oracle/oracle.c), OpenMP"},
+        "implementation": "fp64 CPU oracle (oracle/oracle.c), OpenMP",
+        "config": decode_config(inp, desc, args.gpus),
         "cpu_baseline": {"value": round(gbs, 4), "unit": "GB/s", "cores": cores, "kind": "oracle",
                          "sample": sample},
         "e2e": {"value": round(gbs, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
@@ -468,13 +510,15 @@ def run_decode(args, rank, world, local_rank, dist):
     out = torch.empty((inp.batch, inp.num_q_heads, inp.head_dim), dtype=torch.float16 if f16 else torch.bfloat16,
                       device=dev)
     lse = torch.empty((inp.batch, inp.num_q_heads), dtype=torch.float32, device=dev)
-    flush, l2_note = l2_policy(dev, full_bytes + q.numel() * q.element_size())
+    flush, l2_note = l2_policy(dev, decode_input_bytes(inp))
+    cfg = decode_config(inp, desc, world)
+    assert cfg["l2"] == l2_note
     stream = torch.cuda.current_stream(dev)
     sh, plan = p.shapes, p.plan
 
-    def step_call():
-        B.pa_decode(sh, plan, q, kp, vp, ks, vs, bt, sl, p.meta_dev, inp.scale, out, lse, p.workspace,
-                    stream=stream)
+    # the C call with its arguments marshalled once, as a serving loop would hold it
+    step_call = B.prepared("pa_decode", sh, plan, q, kp, vp, ks, vs, bt, sl, p.meta_dev, ctypes.c_float(inp.scale),
+                           out, lse, p.workspace, ctypes.c_size_t(p.workspace.numel()), stream=stream)
 
     if graph:
         # capture-safe form: a plan sized from capacities only, metadata written on
@@ -558,17 +602,11 @@ def run_decode(args, rank, world, local_rank, dist):
         "metric": METRIC, "value": round(value, 1), "unit": "GB/s", "n_gpus": world, "steps": K,
         "warmup": args.warmup, "ms_per_step": round(ms, 5), "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "e4m3+bf16" if fp8 else ("f16" if f16 else "bf16"), "data": "synthetic",
-        "config": {"workload": desc, "batch": inp.batch, "num_q_heads": inp.num_q_heads,
-                   "num_kv_heads": inp.num_kv_heads, "head_dim": inp.head_dim, "page_size": 64,
-                   "kv_bytes_per_step": full_bytes, "kv_bytes_token_exact": exact_bytes,
-                   "pct_hbm_peak": round(100 * value / world / pk["hbm_gbs"], 2),
-                   "splits": plan.total_splits, "ctas": plan.grid,
-                   "l2": l2_note,
-                   "parallelism": f"replicas x{world}"},
+        "config": cfg,
+        "schedule": {"splits": plan.total_splits, "ctas": plan.grid},
         "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": launches, "clocks": clocks,
     }
-    if rank == 0:
-        print(json.dumps(line), flush=True)
+    return line
 
 
 def graph_decode_e2e(inp, dev, stream, cg, dbuf, out, lse, full_bytes, world, dist, args):
@@ -733,6 +771,21 @@ def prefill_launch(inp, sh, d, out, lse, ws, stream):
                      out, lse, ws, stream=stream)
 
 
+def prefill_prepared(inp, sh, d, out, lse, ws, stream):
+    """prefill_launch as one C call with its arguments marshalled once."""
+    from paged_kv_attention_fwd_gb300 import binding as B
+    nb = ctypes.c_size_t(ws.numel())
+    sc = ctypes.c_float(inp.scale)
+    if is_rope_fp8(inp):
+        return B.prepared("pa_prefill_mla_rope_fp8", sh, d["q"], d["kn"], d["v"], d["kr"], d["krs"], d["cq"], d["ck"],
+                          None, 1, sc, out, lse, ws, nb, stream=stream)
+    if is_fp8_mla(inp):
+        return B.prepared("pa_prefill_mla_fp8", sh, d["qn"], d["qr"], d["qs"], d["kn"], d["ks"], d["v"], d["kr"],
+                          d["cq"], d["ck"], None, 1, sc, out, lse, ws, nb, stream=stream)
+    return B.prepared("pa_prefill", sh, d["q"], d["k"], d["v"], d.get("kr"), d["cq"], d["ck"], d.get("bt"), None, 1,
+                      sc, out, lse, ws, nb, stream=stream)
+
+
 def prefill_device(inp, dev):
     import torch
     d = {k: torch.from_numpy(np.ascontiguousarray(v)).to(dev) for k, v in prefill_host_arrays(inp).items()}
@@ -753,10 +806,11 @@ def run_prefill(args, rank, world, local_rank, dist):
     lse = torch.empty((tq, inp.num_q_heads), dtype=torch.float32, device=dev)
     ws = torch.zeros(prefill_ws_bytes(inp, sh), dtype=torch.uint8, device=dev)
     flush, l2_note = l2_policy(dev, sum(t.numel() * t.element_size() for t in d.values()))
+    cfg = prefill_config(inp, desc, world)
+    assert cfg["l2"] == l2_note
     stream = torch.cuda.current_stream(dev)
 
-    def step():
-        prefill_launch(inp, sh, d, out, lse, ws, stream)
+    step = prefill_prepared(inp, sh, d, out, lse, ws, stream)
 
     for _ in range(args.warmup):
         flush()
@@ -810,19 +864,14 @@ def run_prefill(args, rank, world, local_rank, dist):
         "vs_baseline": None, "data": "synthetic",
         "dtype": ("e4m3+bf16" if (is_fp8_mla(inp) or is_rope_fp8(inp))
                   else ("f16" if getattr(inp, "dtype", "bf16") == "f16" else "bf16")),
-        "config": {"workload": desc, "total_q": tq, "num_q_heads": inp.num_q_heads,
-                   "head_dim_qk": inp.head_dim_qk, "head_dim_v": inp.head_dim_v, "flops_per_step": flops,
-                   "pct_tc_peak": round(100 * tfs / peak, 2),
-                   "l2": l2_note,
-                   "parallelism": f"replicas x{world}"},
+        "config": cfg,
         "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
         # per step: the ordering kernel (with the larger workspace), the rope key's
         # expansion (e4m3 rope key only) and the prefill kernel
         "gpu_launches": K * (1 + (B.pa_prefill_workspace_size(sh) > B.PA_STATUS_BYTES) + is_rope_fp8(inp)),
         "clocks": clocks,
     }
-    if rank == 0:
-        print(json.dumps(line), flush=True)
+    return line
 
 
 def prefill_e2e(inp, dev, stream, sh, flops, world, dist, args):
@@ -965,8 +1014,7 @@ def run_append(args, rank, world, local_rank, dist):
         "metric": METRIC, "value": round(world * gbs, 1), "unit": "GB/s", "n_gpus": world, "steps": K,
         "warmup": args.warmup, "ms_per_step": round(ms, 5), "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-        "config": {"workload": desc, "bytes_per_step": nbytes, "l2": L2_NOTE,
-                   "parallelism": f"replicas x{world}"},
+        "config": {"workload": desc, "bytes_per_step": nbytes, "l2": L2_NOTE, "parallelism": f"replicas x{world}"},
         "roofline": {"bound": "hbm", "achieved": round(gbs, 1), "peak": pk["hbm_gbs"], "unit": "GB/s",
                      "frac": round(gbs / pk["hbm_gbs"], 4),
                      "traffic": profiled_traffic("append_kernel_append.md", ["append.cu", "pa_internal.h", "pa_launch.h"]),
@@ -977,8 +1025,7 @@ def run_append(args, rank, world, local_rank, dist):
         "e2e": e2e,
         "gpu_launches": K, "clocks": clk.summary(),
     }
-    if rank == 0:
-        print(json.dumps(line), flush=True)
+    return line
 
 
 def run_mixed(args, rank, world, local_rank, dist):
@@ -1013,6 +1060,7 @@ def run_mixed(args, rank, world, local_rank, dist):
     ws = torch.zeros(plan.workspace_bytes, dtype=torch.uint8, device=dev)
     dec_ws = (plan.decode.workspace_bytes + 255) // 256 * 256 if plan.num_decode else 0
     flush, l2_note = l2_policy(dev, sum(t.numel() * t.element_size() for t in d.values()))
+    cfg = prefill_config(inp, desc, world, {"num_decode": nd})
     stream = torch.cuda.current_stream(dev)
 
     def step():
@@ -1101,15 +1149,42 @@ def run_mixed(args, rank, world, local_rank, dist):
         "metric": METRIC, "value": round(world * tfs, 2), "unit": "TFLOP/s", "n_gpus": world, "steps": K,
         "warmup": args.warmup, "ms_per_step": round(ms, 5), "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-        "config": {"workload": desc, "num_decode": nd, "total_q": tq, "flops_per_step": flops,
-                   "pct_time_weighted_roofline": round(100 * t_ideal / (ms * 1e-3), 2), "l2": l2_note,
-                   "parallelism": f"replicas x{world}"},
+        "config": cfg,
         "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
         # per step: the decode kernel, the prefill ordering kernel and the prefill kernel
         "gpu_launches": K * 3, "clocks": clocks,
     }
-    if rank == 0:
-        print(json.dumps(line), flush=True)
+    return line
+
+
+SECONDARY = ("decode_fp8", "prefill_paged", "prefill_mla")
+
+
+def run_workload(args, rank, world, local_rank, dist):
+    """Run one workload; returns its JSON record (every rank)."""
+    if args.workload.startswith("prefill"):
+        return run_prefill(args, rank, world, local_rank, dist)
+    if args.workload == "mixed":
+        return run_mixed(args, rank, world, local_rank, dist)
+    if args.workload == "append":
+        return run_append(args, rank, world, local_rank, dist)
+    return run_decode(args, rank, world, local_rank, dist)
+
+
+def secondary_record(line):
+    """A workload's record as it sits under the headline's "secondary" key."""
+    keep = ("value", "unit", "ms_per_step", "steps", "warmup", "dtype", "config", "schedule", "roofline",
+            "cpu_baseline", "e2e", "gpu_launches", "clocks")
+    return {k: line[k] for k in keep if k in line}
+
+
+def release_device_memory():
+    import gc
+
+    import torch
+    gc.collect()
+    torch.cuda.synchronize()
+    torch.cuda.empty_cache()
 
 
 def W_cu(lengths):
@@ -1133,6 +1208,9 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-secondary", action="store_true",
+                    help="with the default workload, skip the e4m3 decode and the two prefill records")
+    ap.add_argument("--secondary-cpu-seconds", type=float, default=4.0)
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
@@ -1156,14 +1234,17 @@ def main():
         build()
     if dist is not None:
         dist.barrier()
-    if args.workload.startswith("prefill"):
-        run_prefill(args, rank, world, local_rank, dist)
-    elif args.workload == "mixed":
-        run_mixed(args, rank, world, local_rank, dist)
-    elif args.workload == "append":
-        run_append(args, rank, world, local_rank, dist)
-    else:
-        run_decode(args, rank, world, local_rank, dist)
+    line = run_workload(args, rank, world, local_rank, dist)
+    if args.workload == "decode_gqa" and not args.no_secondary:
+        # the rest of the metric in the same process: the e4m3 long-context decode
+        # and both prefill shapes, each timed under the headline's own protocol
+        line["secondary"] = {}
+        for wl in SECONDARY:
+            sub = argparse.Namespace(**{**vars(args), "workload": wl, "cpu_seconds": args.secondary_cpu_seconds})
+            line["secondary"][wl] = secondary_record(run_workload(sub, rank, world, local_rank, dist))
+            release_device_memory()
+    if rank == 0:
+        print(json.dumps(line), flush=True)
     if dist is not None:
         dist.destroy_process_group()
 

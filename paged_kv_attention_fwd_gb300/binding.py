@@ -187,6 +187,33 @@ def pa_decode(shapes: pa_decode_shapes, plan: pa_decode_plan, q, k_pool, v_pool,
                            _stream(stream)))
 
 
+def prepared(name: str, *args, stream=None):
+    """A repeatable call of the C function `name` with its arguments
+    marshalled once: tensors and arrays become their addresses now, structures
+    are passed by reference, the stream is resolved now.  For loops that call
+    one entry point on the same buffers every step (the buffers must stay
+    allocated while the callable is in use).  The callable raises PaError on a
+    non-OK status, like the wrappers above."""
+    f = getattr(lib(), name)
+    cargs = []
+    for a in args:
+        if isinstance(a, ctypes.Structure):
+            cargs.append(ctypes.byref(a))
+        elif a is None or isinstance(a, np.ndarray) or hasattr(a, "data_ptr"):
+            cargs.append(_ptr(a))
+        else:
+            cargs.append(a)
+    cargs.append(_stream(stream))
+    cargs = tuple(cargs)
+
+    def call() -> None:
+        st = f(*cargs)
+        if st != PA_OK:
+            _check(st)
+
+    return call
+
+
 def pa_decode_attend(shapes: pa_decode_shapes, plan: pa_decode_plan, q, k_pool, v_pool, k_scale, v_scale,
                      block_table, seq_lens, meta_dev, scale: float, out, lse, workspace,
                      workspace_bytes: Optional[int] = None, stream=None) -> None:

@@ -48,14 +48,32 @@ def check_common(d, bound, unit):
     assert "sm_mhz" in c and "sm_max_mhz" in c and "reasons" in c
 
 
-def test_default_line_with_e2e_and_cpu_baseline():
-    d = run_bench()
-    check_common(d, "hbm", "GB/s")
+def check_legs(d, unit):
     e = d["e2e"]
-    assert e["value"] > 0 and e["unit"] == "GB/s" and e["h2d_bytes_per_step"] > 0 and e["d2h_bytes_per_step"] > 0
+    assert e["value"] > 0 and e["unit"] == unit and e["h2d_bytes_per_step"] > 0 and e["d2h_bytes_per_step"] > 0
     cb = d["cpu_baseline"]
     assert cb["kind"] == "oracle" and cb["value"] > 0 and cb["cores"] >= 1 and cb["sample"]
+
+
+def test_default_line_with_e2e_cpu_baseline_and_secondary_records():
+    d = run_bench("--cpu-seconds", "2", "--secondary-cpu-seconds", "1")
+    check_common(d, "hbm", "GB/s")
+    check_legs(d, "GB/s")
     assert d["gpu_launches"] == d["steps"]  # one decode launch a step
+    # the rest of the metric, each record timed in the same process
+    sec = d["secondary"]
+    assert set(sec) == {"decode_fp8", "prefill_paged", "prefill_mla"}
+    for name, r in sec.items():
+        unit, bound = ("GB/s", "hbm") if name.startswith("decode") else ("TFLOP/s", "tensor")
+        assert r["unit"] == unit and r["value"] > 0 and r["steps"] == 5 and r["ms_per_step"] > 0
+        rf = r["roofline"]
+        assert rf["bound"] == bound and abs(rf["frac"] - rf["achieved"] / rf["peak"]) < 1e-3
+        # achieved is recomputable from the record: algorithmic work / kernel time
+        work = rf.get("algorithmic_flops_per_launch", rf.get("algorithmic_bytes_per_launch"))
+        scale = 1e12 if unit == "TFLOP/s" else 1e9
+        assert abs(work / (rf["kernel_ms"] * 1e-3) / scale - rf["achieved"]) <= 1e-3 * rf["achieved"] + 0.05
+        check_legs(r, unit)
+        assert "sm_mhz" in r["clocks"] and "workload" in r["config"]
 
 
 def test_prefill_line():

@@ -64,3 +64,17 @@ def test_reference_arm_runs_on_rank_0_only():
                         "decode_tiny", "--steps", "3", "--warmup", "3"], env=env, capture_output=True, text=True,
                        timeout=300)
     assert r.returncode == 0 and r.stdout.strip() == ""
+
+
+def test_reference_arm_states_the_same_config_as_ours():
+    """The reference arm's config is built by the same function as the GPU
+    arm's (the workload only, nothing about the implementation)."""
+    sys.path.insert(0, ROOT)
+    import bench
+    r = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference", "--workload",
+                        "decode_tiny", "--steps", "3", "--warmup", "3"], capture_output=True, text=True, timeout=300)
+    assert r.returncode == 0, r.stderr[-2000:]
+    line = json.loads([l for l in r.stdout.splitlines() if l.startswith("{")][0])
+    inp, desc = bench.decode_workload("decode_tiny")
+    assert line["config"] == bench.decode_config(inp, desc, 1)
+    assert line["impl"] == "reference" and "implementation" not in line["config"]
