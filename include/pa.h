@@ -225,14 +225,21 @@ pa_status pa_decode_combine(const pa_decode_shapes* shapes, const pa_decode_plan
  * process exits.  The call allocates nothing and frees nothing.
  *   - plan->workspace_bytes above 16 MiB is rejected with PA_ERR_WORKSPACE.
  *   - The first call on a device looks up the scratch array's device address
- *     (with that device current); make that first call before any stream
- *     capture.
+ *     (with that device current) and keeps it for later calls; make that
+ *     first call before any stream capture.  The address belongs to the
+ *     device's context: after cudaDeviceReset the next call (again outside
+ *     any capture) looks it up anew in the new context.
  *   - All calls share the one array, which keeps the last call's contents;
  *     the status word is cleared at the start of each call.  Calls that may
  *     overlap on the GPU (other streams, other host threads) race on it.
+ *   - Every host-side check (the same as pa_decode's) runs before anything
+ *     is enqueued; a rejected call leaves the stream untouched.
  *   - status_host: NULL, or a host int32 that receives the device status word
- *     (PA_OK or the first device-detected fault); the call then waits for
- *     `stream` before returning.
+ *     (PA_OK or the first device-detected fault: PA_ERR_DEVICE_BOUNDS,
+ *     PA_ERR_TIMEOUT); the call then waits for `stream` before returning.
+ *     With NULL the call does not wait, and a device-detected fault is not
+ *     reported: the status word sits in the private scratch array, and the
+ *     next call clears it.
  */
 pa_status pa_decode_noalloc(const pa_decode_shapes* shapes, const pa_decode_plan* plan, const void* q,
                             const void* k_pool, const void* v_pool, const float* k_scale, const float* v_scale,

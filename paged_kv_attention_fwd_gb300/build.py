@@ -16,8 +16,8 @@ ROOT = os.path.dirname(HERE)
 CSRC = os.path.join(HERE, "csrc")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libpa.so")
-SOURCES = ["pa_api.cu", "decode.cu", "prefill.cu", "append.cu", "schedule.cu"]
-HEADERS = ["pa_ptx.cuh", "pa_internal.h", "pa_launch.h"]
+SOURCES = ["pa_api.cu", "decode.cu", "prefill.cu", "prefill_pair.cu", "append.cu", "schedule.cu"]
+HEADERS = ["pa_ptx.cuh", "pa_internal.h", "pa_launch.h", "prefill_common.cuh"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "--expt-relaxed-constexpr",
          "-I", os.path.join(ROOT, "include")]

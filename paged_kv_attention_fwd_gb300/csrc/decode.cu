@@ -1514,22 +1514,59 @@ constexpr size_t kNoAllocScratchBytes = size_t(16) << 20;  // 16 MiB
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
 
 std::mutex g_noalloc_mutex;
-void* g_noalloc_ptr[128] = {};  // device address of the scratch, per device ordinal
+struct NoAllocSlot {
+    unsigned long long ctx_id;  // the context the address was looked up in (0: none yet)
+    void* ptr;                  // device address of the scratch array in that context
+};
+NoAllocSlot g_noalloc_slot[128] = {};  // per device ordinal
+
+typedef CUresult (*CtxGetCurrentFn)(CUcontext*);
+typedef CUresult (*CtxGetIdFn)(CUcontext, unsigned long long*);
+
+// The unique id of the calling thread's current context (0 if unknown).  A
+// context created after cudaDeviceReset gets a new id, and with it a new copy
+// of this library's module and of the scratch array.
+unsigned long long current_ctx_id() {
+    static CtxGetCurrentFn get_current = nullptr;
+    static CtxGetIdFn get_id = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            get_current = reinterpret_cast<CtxGetCurrentFn>(p);
+        p = nullptr;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            get_id = reinterpret_cast<CtxGetIdFn>(p);
+    });
+    CUcontext ctx = nullptr;
+    unsigned long long id = 0;
+    if (!get_current || !get_id || get_current(&ctx) != CUDA_SUCCESS || !ctx || get_id(ctx, &id) != CUDA_SUCCESS)
+        return 0;
+    return id;
+}
 
 // In host code the array's name is only a host-side stand-in; its device
-// address has to be asked for, once per device, with that device current.
+// address has to be asked for with the device current.  That is done once per
+// device and context: the first call on a device (or the first after its
+// context was reset) looks it up, later calls reuse it.
 pa_status noalloc_scratch(void** out) {
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess || dev < 0 || dev >= 128) return PA_ERR_CUDA;
+    const unsigned long long id = current_ctx_id();
     std::lock_guard<std::mutex> lock(g_noalloc_mutex);
-    if (!g_noalloc_ptr[dev]) {
+    NoAllocSlot& slot = g_noalloc_slot[dev];
+    if (!slot.ptr || id == 0 || slot.ctx_id != id) {
         void* p = nullptr;
         e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
         if (e != cudaSuccess || !p) return PA_ERR_CUDA;
-        g_noalloc_ptr[dev] = p;
+        slot.ptr = p;
+        slot.ctx_id = current_ctx_id();  // the lookup has made the device's context current
     }
-    *out = g_noalloc_ptr[dev];
+    *out = slot.ptr;
     return PA_OK;
 }
 
@@ -1540,6 +1577,7 @@ extern "C" pa_status pa_decode_noalloc(const pa_decode_shapes* shapes, const pa_
                                        const float* v_scale, const int32_t* block_table, const int32_t* seq_lens,
                                        const int32_t* meta_dev, float scale, void* out, float* lse,
                                        int32_t* status_host, cudaStream_t stream) {
+    pa::NvtxRange nvtx_range("pa_decode_noalloc");
     if (!plan) {
         pa::set_last_error("plan must not be NULL");
         return PA_ERR_INVALID_ARG;
@@ -1559,6 +1597,10 @@ extern "C" pa_status pa_decode_noalloc(const pa_decode_shapes* shapes, const pa_
         pa::set_last_error("could not look up the device address of the no-alloc scratch array");
         return st;
     }
+    // every host-side check before anything is enqueued
+    st = pa::check_decode_call(shapes, plan, q, k_pool, v_pool, k_scale, v_scale, block_table, seq_lens, meta_dev,
+                               scale, out, scratch, kNoAllocScratchBytes);
+    if (st != PA_OK) return st;
     // the status word must start at zero; the partials are written before read
     if (cudaMemsetAsync(scratch, 0, PA_STATUS_BYTES, stream) != cudaSuccess) {
         pa::set_last_error("clearing the no-alloc status word failed");

@@ -75,9 +75,62 @@ pa_status make_map_16(bool f16, CUtensorMap* map, const void* base, int rank, co
                     strides_bytes, box);
 }
 
+// Encoded tensor maps of recent calls.  A serving loop passes the same
+// buffers with the same shapes call after call; a map is a pure function of
+// (type, base address, dims, strides, box), so a hit skips the driver's
+// encode.  Sixteen entries, replaced round-robin, under one mutex.
+struct MapKey {
+    CUtensorMapDataType dtype;
+    const void* base;
+    int rank;
+    uint64_t dims[5], strides[4];
+    uint32_t box[5];
+    bool operator==(const MapKey& o) const {
+        if (dtype != o.dtype || base != o.base || rank != o.rank) return false;
+        for (int i = 0; i < rank; ++i) {
+            if (dims[i] != o.dims[i] || box[i] != o.box[i]) return false;
+            if (i + 1 < rank && strides[i] != o.strides[i]) return false;
+        }
+        return true;
+    }
+};
+
+struct MapCache {
+    static constexpr int kEntries = 16;
+    std::mutex mu;
+    MapKey key[kEntries];
+    CUtensorMap map[kEntries];
+    bool used[kEntries] = {};
+    int next = 0;
+};
+
+MapCache& map_cache() {
+    static MapCache c;
+    return c;
+}
+
 // Tiled map, 128-byte swizzle (the box's inner extent is 128 bytes).
 pa_status make_map(CUtensorMapDataType dtype, CUtensorMap* map, const void* base, int rank, const uint64_t* dims,
                    const uint64_t* strides_bytes, const uint32_t* box) {
+    MapKey key;
+    std::memset(&key, 0, sizeof key);
+    key.dtype = dtype;
+    key.base = base;
+    key.rank = rank;
+    for (int i = 0; i < rank; ++i) {
+        key.dims[i] = dims[i];
+        key.box[i] = box[i];
+        if (i + 1 < rank) key.strides[i] = strides_bytes[i];
+    }
+    MapCache& cache = map_cache();
+    {
+        std::lock_guard<std::mutex> lock(cache.mu);
+        for (int i = 0; i < MapCache::kEntries; ++i)
+            if (cache.used[i] && cache.key[i] == key) {
+                *map = cache.map[i];
+                return PA_OK;
+            }
+    }
     EncodeTiledFn enc = encode_fn();
     if (!enc) return fail(PA_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
     cuuint64_t d[5], s[4];
@@ -92,6 +145,12 @@ pa_status make_map(CUtensorMapDataType dtype, CUtensorMap* map, const void* base
                      CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                      CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (r != CUDA_SUCCESS) return fail(PA_ERR_INVALID_ARG, "cuTensorMapEncodeTiled failed (CUresult %d)", (int)r);
+    std::lock_guard<std::mutex> lock(cache.mu);
+    const int slot = cache.next;
+    cache.next = (slot + 1) % MapCache::kEntries;
+    cache.key[slot] = key;
+    cache.map[slot] = *map;
+    cache.used[slot] = true;
     return PA_OK;
 }
 
@@ -121,6 +180,7 @@ pa_status pa_set_wait_limit_ns(uint64_t limit_ns) {
 
 pa_status pa_get_metadata(const int32_t* seq_lens_host, const int32_t* block_table_host, const pa_decode_shapes* sh,
                           int32_t* meta_host, size_t meta_capacity_ints, pa_decode_plan* plan) {
+    pa::NvtxRange nvtx_range("pa_get_metadata");
     if (!sh || !plan) return fail(PA_ERR_INVALID_ARG, "shapes and plan must not be NULL");
     const int B = sh->batch, Hk = sh->num_kv_heads;
     if (B < 0) return fail(PA_ERR_INVALID_ARG, "batch must be >= 0 (got %d)", B);
@@ -277,22 +337,26 @@ pa_status pa_decode_attend(const pa_decode_shapes* sh, const pa_decode_plan* pla
                            const int32_t* block_table, const int32_t* seq_lens, const int32_t* meta_dev,
                            float scale, void* out, float* lse, void* workspace, size_t workspace_bytes,
                            cudaStream_t stream) {
+    pa::NvtxRange nvtx_range("pa_decode_attend");
     return decode_launch(false, sh, plan, q, k_pool, v_pool, k_scale, v_scale, block_table, seq_lens, meta_dev,
                          scale, out, lse, workspace, workspace_bytes, stream);
 }
 
-namespace {
-pa_status decode_launch(bool fused, const pa_decode_shapes* sh, const pa_decode_plan* plan, const void* q,
-                        const void* k_pool, const void* v_pool, const float* k_scale, const float* v_scale,
-                        const int32_t* block_table, const int32_t* seq_lens, const int32_t* meta_dev, float scale,
-                        void* out, float* lse, void* workspace, size_t workspace_bytes, cudaStream_t stream) {
+}  // extern "C"
+
+namespace pa {
+// Every host-side check of a decode call (shapes, plan, pointers, alignment,
+// workspace size, scale), without launching anything.
+pa_status check_decode_call(const pa_decode_shapes* sh, const pa_decode_plan* plan, const void* q,
+                            const void* k_pool, const void* v_pool, const float* k_scale, const float* v_scale,
+                            const int32_t* block_table, const int32_t* seq_lens, const int32_t* meta_dev,
+                            float scale, const void* out, const void* workspace, size_t workspace_bytes) {
     pa_status st = validate_decode_common(sh, plan, out, meta_dev, workspace, workspace_bytes);
     if (st != PA_OK || sh->batch == 0) return st;
-    const int B = sh->batch, Hq = sh->num_q_heads, Hk = sh->num_kv_heads, D = sh->head_dim;
+    const int Hk = sh->num_kv_heads;
     if (sh->kv_dtype != PA_KV_BF16 && sh->kv_dtype != PA_KV_FP8_E4M3 && sh->kv_dtype != PA_KV_FP16)
         return fail(PA_ERR_INVALID_ARG, "unknown kv_dtype %d", sh->kv_dtype);
     const bool fp8 = sh->kv_dtype == PA_KV_FP8_E4M3;
-    const bool f16 = sh->kv_dtype == PA_KV_FP16;
     if (sh->max_pages_per_seq <= 0 || sh->num_pool_pages <= 0)
         return fail(PA_ERR_INVALID_ARG, "max_pages_per_seq and num_pool_pages must be positive");
     if ((int64_t)sh->num_pool_pages * Hk * pa::kPage >= ((int64_t)1 << 31))
@@ -303,6 +367,23 @@ pa_status decode_launch(bool fused, const pa_decode_shapes* sh, const pa_decode_
     if (!aligned16(q) || !aligned16(k_pool) || !aligned16(v_pool))
         return fail(PA_ERR_INVALID_ARG, "q, pools, out and workspace must be 16-byte aligned");
     if (!std::isfinite(scale)) return fail(PA_ERR_INVALID_ARG, "scale must be finite");
+    return PA_OK;
+}
+}  // namespace pa
+
+extern "C" {
+
+namespace {
+pa_status decode_launch(bool fused, const pa_decode_shapes* sh, const pa_decode_plan* plan, const void* q,
+                        const void* k_pool, const void* v_pool, const float* k_scale, const float* v_scale,
+                        const int32_t* block_table, const int32_t* seq_lens, const int32_t* meta_dev, float scale,
+                        void* out, float* lse, void* workspace, size_t workspace_bytes, cudaStream_t stream) {
+    pa_status st = pa::check_decode_call(sh, plan, q, k_pool, v_pool, k_scale, v_scale, block_table, seq_lens,
+                                         meta_dev, scale, out, workspace, workspace_bytes);
+    if (st != PA_OK || sh->batch == 0) return st;
+    const int B = sh->batch, Hq = sh->num_q_heads, Hk = sh->num_kv_heads, D = sh->head_dim;
+    const bool fp8 = sh->kv_dtype == PA_KV_FP8_E4M3;
+    const bool f16 = sh->kv_dtype == PA_KV_FP16;
 
     pa::DecodeArgs a;
     a.q = static_cast<const uint16_t*>(q);
@@ -373,6 +454,7 @@ pa_status decode_launch(bool fused, const pa_decode_shapes* sh, const pa_decode_
 
 pa_status pa_decode_combine(const pa_decode_shapes* sh, const pa_decode_plan* plan, const int32_t* meta_dev,
                             void* out, float* lse, void* workspace, size_t workspace_bytes, cudaStream_t stream) {
+    pa::NvtxRange nvtx_range("pa_decode_combine");
     pa_status st = validate_decode_common(sh, plan, out, meta_dev, workspace, workspace_bytes);
     if (st != PA_OK || sh->batch == 0) return st;
     if (plan->total_splits == sh->batch) return PA_OK;
@@ -395,11 +477,15 @@ pa_status pa_decode(const pa_decode_shapes* sh, const pa_decode_plan* plan, cons
                     const void* v_pool, const float* k_scale, const float* v_scale, const int32_t* block_table,
                     const int32_t* seq_lens, const int32_t* meta_dev, float scale, void* out, float* lse,
                     void* workspace, size_t workspace_bytes, cudaStream_t stream) {
+    pa::NvtxRange nvtx_range("pa_decode");
     return decode_launch(true, sh, plan, q, k_pool, v_pool, k_scale, v_scale, block_table, seq_lens, meta_dev,
                          scale, out, lse, workspace, workspace_bytes, stream);
 }
 
 namespace {
+// bf16 / fp16 prefill on CTA pairs (prefill_pair.cu) instead of one CTA per item
+constexpr bool kPairPrefill = false;
+
 // The launch arguments common to pa_prefill and pa_prefill_mla_fp8.
 pa_status fill_prefill_args(const pa_prefill_shapes* sh, const int32_t* cu_seqlens_q, const int32_t* cu_seqlens_k,
                             const int32_t* block_table, const int32_t* qo_offset, int causal, float scale, void* out,
@@ -421,6 +507,7 @@ pa_status fill_prefill_args(const pa_prefill_shapes* sh, const int32_t* cu_seqle
     a->max_pages = paged ? sh->max_pages_per_seq : 0;
     a->num_pool_pages = paged ? sh->num_pool_pages : 0;
     a->total_q = sh->total_q;
+    a->q_block = 256;
     a->num_q_tiles = (int32_t)cdiv(sh->max_seqlen_q, 256);
     // the longest-first unit order lives after the status word when the
     // workspace has room for it (see pa_prefill_workspace_size)
@@ -447,6 +534,7 @@ pa_status pa_prefill(const pa_prefill_shapes* sh, const void* q, const void* k, 
                      const int32_t* cu_seqlens_q, const int32_t* cu_seqlens_k, const int32_t* block_table,
                      const int32_t* qo_offset, int causal, float scale, void* out, float* lse, void* workspace,
                      size_t workspace_bytes, cudaStream_t stream) {
+    pa::NvtxRange nvtx_range("pa_prefill");
     if (!sh) return fail(PA_ERR_INVALID_ARG, "shapes must not be NULL");
     const int B = sh->batch, Hq = sh->num_q_heads, Hk = sh->num_kv_heads;
     if (B < 0 || sh->total_q < 0 || sh->total_k < 0 || sh->max_seqlen_q < 0)
@@ -523,6 +611,31 @@ pa_status pa_prefill(const pa_prefill_shapes* sh, const void* q, const void* k, 
     st = fill_prefill_args(sh, cu_seqlens_q, cu_seqlens_k, block_table, qo_offset, causal, scale, out, lse, workspace,
                            workspace_bytes, f16, &a);
     if (st != PA_OK) return st;
+    if (kPairPrefill) {
+        // CTA pairs (512-row work items); each CTA loads 64 keys of a K tile,
+        // so the ragged K and rope maps take 64-row boxes
+        pa::PrefillArgs ap = a;
+        ap.q_block = 512;
+        ap.num_q_tiles = (int32_t)cdiv(sh->max_seqlen_q, 512);
+        CUtensorMap mk2 = mk, mr2 = mr;
+        if (!paged) {
+            const uint64_t dk_dims[3] = {(uint64_t)dk, (uint64_t)Hk, (uint64_t)sh->total_k};
+            const uint64_t dk_str[2] = {(uint64_t)dk * 2, (uint64_t)Hk * dk * 2};
+            const uint32_t box[3] = {64, 1, 64};
+            st = make_map_16(f16, &mk2, k, 3, dk_dims, dk_str, box);
+            if (st == PA_OK && rope) {
+                const uint64_t rd[2] = {64, (uint64_t)sh->total_k};
+                const uint64_t rs[1] = {128};
+                const uint32_t rb[2] = {64, 64};
+                st = make_map_16(f16, &mr2, k_rope, 2, rd, rs, rb);
+            }
+            if (st != PA_OK) return st;
+        }
+        cudaError_t e = pa::launch_prefill_pair(ap, dqk, &mq, &mk2, &mv, &mr2, stream);
+        if (e == cudaSuccess) return PA_OK;
+        if (e != cudaErrorNotSupported) return cuda_fail(e, "prefill launch");
+        // no cluster of two CTAs fits on this device: one CTA per work item
+    }
     CUtensorMap mqr;
     std::memset(&mqr, 0, sizeof mqr);
     cudaError_t e = pa::launch_prefill(a, dqk, &mq, &mk, &mv, &mr, &mqr, stream);
@@ -534,6 +647,7 @@ pa_status pa_append_kv(const pa_append_shapes* sh, const void* k_new, const void
                        const int32_t* cu_seqlens_new, const int32_t* start_pos, const int32_t* block_table,
                        void* k_pool, void* v_pool, const float* k_scale, const float* v_scale, void* workspace,
                        size_t workspace_bytes, cudaStream_t stream) {
+    pa::NvtxRange nvtx_range("pa_append_kv");
     if (!sh) return fail(PA_ERR_INVALID_ARG, "shapes must not be NULL");
     if (sh->batch < 0 || sh->total_new < 0) return fail(PA_ERR_INVALID_ARG, "batch and total_new must be >= 0");
     if (sh->batch == 0 || sh->total_new == 0) return PA_OK;
@@ -617,6 +731,7 @@ pa_prefill_shapes mixed_prefill_shapes(const pa_mixed_shapes* sh, const pa_mixed
 pa_status pa_get_mixed_plan(const int32_t* cu_q, const int32_t* kv_lens, const int32_t* block_table_host,
                         const pa_mixed_shapes* sh, int32_t* meta_host, size_t meta_capacity_ints,
                         pa_mixed_plan* plan) {
+    pa::NvtxRange nvtx_range("pa_get_mixed_plan");
     if (!sh || !plan) return fail(PA_ERR_INVALID_ARG, "shapes and plan must not be NULL");
     const int B = sh->batch;
     if (B < 0) return fail(PA_ERR_INVALID_ARG, "batch must be >= 0");
@@ -667,6 +782,7 @@ pa_status pa_mixed(const pa_mixed_shapes* sh, const pa_mixed_plan* plan, const v
                    const void* v_pool, const int32_t* block_table, const int32_t* cu_seqlens_q,
                    const int32_t* cu_seqlens_k, const int32_t* kv_lens, const int32_t* meta_dev, float scale,
                    void* out, float* lse, void* workspace, size_t workspace_bytes, cudaStream_t stream) {
+    pa::NvtxRange nvtx_range("pa_mixed");
     if (!sh || !plan) return fail(PA_ERR_INVALID_ARG, "shapes and plan must not be NULL");
     if (workspace_bytes < plan->workspace_bytes)
         return fail(PA_ERR_WORKSPACE, "workspace has %zu bytes, the plan needs %zu", workspace_bytes,
@@ -696,6 +812,7 @@ pa_status pa_prefill_mla_fp8(const pa_prefill_shapes* sh, const void* q_nope, co
                              const void* k_rope, const int32_t* cu_seqlens_q, const int32_t* cu_seqlens_k,
                              const int32_t* qo_offset, int causal, float scale, void* out, float* lse,
                              void* workspace, size_t workspace_bytes, cudaStream_t stream) {
+    pa::NvtxRange nvtx_range("pa_prefill_mla_fp8");
     if (!sh) return fail(PA_ERR_INVALID_ARG, "shapes must not be NULL");
     const int B = sh->batch, Hq = sh->num_q_heads, Hk = sh->num_kv_heads;
     if (B < 0 || sh->total_q < 0 || sh->total_k < 0 || sh->max_seqlen_q < 0)
@@ -755,6 +872,7 @@ pa_status pa_prefill_mla_fp8(const pa_prefill_shapes* sh, const void* q_nope, co
 pa_status pa_page_table_from_flat(const int32_t* kv_indices, int64_t num_indices, const int32_t* kv_lens,
                                   int32_t batch, int32_t max_pages_per_seq, int32_t* block_table, void* workspace,
                                   size_t workspace_bytes, cudaStream_t stream) {
+    pa::NvtxRange nvtx_range("pa_page_table_from_flat");
     if (batch <= 0 || batch > pa::kMaxBatch)
         return fail(PA_ERR_UNSUPPORTED, "batch must be in [1, %d] (got %d)", pa::kMaxBatch, batch);
     if (max_pages_per_seq <= 0) return fail(PA_ERR_INVALID_ARG, "max_pages_per_seq must be positive");
@@ -795,6 +913,7 @@ pa_status pa_prefill_mla_rope_fp8(const pa_prefill_shapes* sh, const void* q, co
                                   const int32_t* cu_seqlens_k, const int32_t* qo_offset, int causal, float scale,
                                   void* out, float* lse, void* workspace, size_t workspace_bytes,
                                   cudaStream_t stream) {
+    pa::NvtxRange nvtx_range("pa_prefill_mla_rope_fp8");
     if (!sh) return fail(PA_ERR_INVALID_ARG, "shapes must not be NULL");
     const int B = sh->batch, Hq = sh->num_q_heads, Hk = sh->num_kv_heads;
     if (B < 0 || sh->total_q < 0 || sh->total_k < 0 || sh->max_seqlen_q < 0)
@@ -851,6 +970,7 @@ pa_status pa_prefill_mla_rope_fp8(const pa_prefill_shapes* sh, const void* q, co
 }
 
 pa_status pa_get_static_plan(const pa_decode_shapes* sh, pa_decode_plan* plan) {
+    pa::NvtxRange nvtx_range("pa_get_static_plan");
     if (!sh || !plan) return fail(PA_ERR_INVALID_ARG, "shapes and plan must not be NULL");
     const int B = sh->batch, Hk = sh->num_kv_heads;
     if (B <= 0 || B > pa::kMaxBatch)
@@ -882,6 +1002,7 @@ pa_status pa_get_static_plan(const pa_decode_shapes* sh, pa_decode_plan* plan) {
 
 pa_status pa_get_metadata_device(const pa_decode_shapes* sh, const pa_decode_plan* plan, const int32_t* seq_lens_dev,
                                  int32_t* meta_dev, cudaStream_t stream) {
+    pa::NvtxRange nvtx_range("pa_get_metadata_device");
     if (!sh || !plan) return fail(PA_ERR_INVALID_ARG, "shapes and plan must not be NULL");
     if (!seq_lens_dev || !meta_dev) return fail(PA_ERR_INVALID_ARG, "seq_lens_dev and meta_dev must not be NULL");
     pa_decode_plan check;
@@ -900,6 +1021,7 @@ pa_status pa_get_metadata_device(const pa_decode_shapes* sh, const pa_decode_pla
 }
 
 pa_status pa_check_status(void* workspace, cudaStream_t stream) {
+    pa::NvtxRange nvtx_range("pa_check_status");
     if (!workspace) return fail(PA_ERR_INVALID_ARG, "workspace must not be NULL");
     int32_t word = 0;
     cudaError_t e = cudaMemcpyAsync(&word, workspace, sizeof word, cudaMemcpyDeviceToHost, stream);

@@ -9,6 +9,10 @@
 
 #include "../../include/pa.h"
 
+// NVTX v3 is header-only: without a profiler attached each push/pop is a
+// check of one function pointer.
+#include <nvtx3/nvToolsExt.h>
+
 namespace pa {
 
 constexpr int kPage = 64;
@@ -64,7 +68,8 @@ struct PrefillArgs {
     float* lse;      // [total_q, Hq] or nullptr
     int* status;
     int32_t batch, num_q_heads, num_kv_heads, group, max_pages, num_pool_pages, total_q;
-    int32_t num_q_tiles;  // 256-row query blocks per segment: ceil(max_seqlen_q / 256)
+    int32_t num_q_tiles;  // query blocks per segment: ceil(max_seqlen_q / q_block)
+    int32_t q_block;      // query rows of one work item: 256 (one CTA) or 512 (a CTA pair)
     int32_t causal, paged, rope;
     int32_t f16;  // q, k, v, k_rope and out are fp16, else bf16
     int32_t f8;   // MLA with e4m3 q_nope / k_nope and per-head scales
@@ -79,6 +84,16 @@ struct PrefillArgs {
 // levels hi = bf16(x), lo = bf16(x - hi), each [tokens, 64]
 cudaError_t launch_rope_expand(const uint8_t* codes, const float* scales, uint16_t* hi, uint16_t* lo,
                                int64_t tokens, cudaStream_t stream);
+
+// The longest-first order of the work units, into a.order (nothing when it is null).
+cudaError_t launch_prefill_order(const PrefillArgs& a, cudaStream_t stream);
+
+// The bf16 / fp16 prefill on CTA pairs (prefill_pair.cu): a.q_block must be
+// 512; map_k and map_r have 64-row boxes (each CTA loads 64 keys of a tile).
+// Returns cudaErrorNotSupported when no 2-CTA cluster fits on the device.
+cudaError_t launch_prefill_pair(const PrefillArgs& a, int head_dim_qk, const CUtensorMap* map_q,
+                                const CUtensorMap* map_k, const CUtensorMap* map_v, const CUtensorMap* map_r,
+                                cudaStream_t stream);
 
 cudaError_t launch_prefill(const PrefillArgs& a, int head_dim_qk, const CUtensorMap* map_q,
                            const CUtensorMap* map_k, const CUtensorMap* map_v, const CUtensorMap* map_r,
@@ -111,6 +126,21 @@ cudaError_t launch_schedule(const int32_t* seq_lens, int B, int Hk, int max_page
 
 // Record a message for pa_last_error() on this host thread (pa_api.cu).
 void set_last_error(const char* msg);
+
+// The host-side checks of a decode call, launching nothing (pa_api.cu).
+pa_status check_decode_call(const pa_decode_shapes* sh, const pa_decode_plan* plan, const void* q,
+                            const void* k_pool, const void* v_pool, const float* k_scale, const float* v_scale,
+                            const int32_t* block_table, const int32_t* seq_lens, const int32_t* meta_dev,
+                            float scale, const void* out, const void* workspace, size_t workspace_bytes);
+
+// A named NVTX range over one library call (from construction to the end of
+// the scope), so a timeline shows which pa_* call enqueued which kernels.
+struct NvtxRange {
+    explicit NvtxRange(const char* name) { nvtxRangePushA(name); }
+    ~NvtxRange() { nvtxRangePop(); }
+    NvtxRange(const NvtxRange&) = delete;
+    NvtxRange& operator=(const NvtxRange&) = delete;
+};
 
 // Allow `kernel` `bytes` of dynamic shared memory on the current device.  A
 // function attribute belongs to one device's context, so it is set once per

@@ -4,9 +4,12 @@ Such callers (a host framework that owns all device memory through its own
 pool, a loop that cannot pay for an allocation's synchronisation) get one
 entry point that uses the library's fixed 16 MiB scratch array instead of a
 caller workspace.  These tests call it through the C ABI and check that its
-output matches pa_decode's within the decode tolerances, on calls made one
-after another (the scratch keeps the previous call's contents), and that a
-plan needing more scratch than the fixed size is refused with a clear error.
+output matches pa_decode's and the fp64 oracle's within the decode
+tolerances, on calls made one after another (the scratch keeps the previous
+call's contents); that the device status word comes back through
+status_host, clean or with a recorded fault; that host-side checks run
+before anything is enqueued; and that a plan needing more scratch than the
+fixed size is refused with a clear error.
 This file is collected last on purpose.
 """
 import math
@@ -15,6 +18,7 @@ import numpy as np
 import pytest
 import torch
 
+import oracle
 from paged_kv_attention_fwd_gb300 import binding as B
 from paged_kv_attention_fwd_gb300 import ops
 from paged_kv_attention_fwd_gb300 import workloads as W
@@ -73,6 +77,62 @@ def test_noalloc_after_a_different_call_e4m3():
     lens = W.lognormal_lengths(22, 12, math.log(1500.0), 1.0, 64, 6000)
     inp = W.make_decode(12, 64, 8, 128, lens, seed=22, kv_dtype="e4m3")
     _check_against_pa_decode(inp, calls=2, max_tol=5e-2, mean_tol=5e-3)
+
+
+def test_noalloc_matches_the_oracle_and_reports_a_clean_status():
+    """Two calls in a row against the fp64 oracle (same tolerances as every
+    decode test: max |out| error 1e-2, mean 1e-3, lse 1e-3), each reading the
+    device status word back through status_host."""
+    inp = W.make_decode(10, 16, 4, 128, W.uniform_lengths(23, 10, 1, 3000), seed=23)
+    q, kp, vp, ks, vs, bt, sl = _device_inputs(inp)
+    p = ops.plan_decode(inp.seq_lens, inp.block_table, inp.num_q_heads, inp.num_kv_heads, inp.head_dim,
+                        inp.max_pages, inp.num_pool_pages, inp.kv_dtype)
+    assert p.plan.total_splits > inp.batch
+    ref_out, ref_lse = oracle.decode(inp.q, inp.k_pool, inp.v_pool, inp.block_table, inp.seq_lens, inp.scale)
+    for _ in range(2):
+        out = torch.full((inp.batch, inp.num_q_heads, inp.head_dim), float("nan"), dtype=torch.bfloat16, device="cuda")
+        lse = torch.full((inp.batch, inp.num_q_heads), float("nan"), dtype=torch.float32, device="cuda")
+        st = B.pa_decode_noalloc(p.shapes, p.plan, q, kp, vp, ks, vs, bt, sl, p.meta_dev, inp.scale, out, lse)
+        assert st == B.PA_OK
+        err = np.abs(out.float().cpu().numpy() - ref_out)
+        assert err.max() <= 1e-2 and err.mean() <= 1e-3
+        assert np.abs(lse.cpu().numpy() - ref_lse).max() <= 1e-3
+
+
+def test_noalloc_reports_a_device_fault_through_status_host():
+    """An out-of-range page id in a live block-table slot is recorded by the
+    kernel (the load is skipped, nothing faults) and comes back through
+    status_host; the next clean call clears the word and reports PA_OK."""
+    inp = W.make_decode(4, 8, 4, 128, [100, 700, 1500, 2100], seed=24)
+    q, kp, vp, ks, vs, bt, sl = _device_inputs(inp)
+    p = ops.plan_decode(inp.seq_lens, inp.block_table, inp.num_q_heads, inp.num_kv_heads, inp.head_dim,
+                        inp.max_pages, inp.num_pool_pages, inp.kv_dtype)
+    bad = inp.block_table.copy()
+    bad[2, 5] = inp.num_pool_pages + 7  # 1500 keys: 24 pages, slot 5 is live
+    bad_d = torch.from_numpy(bad).to("cuda")
+    out = torch.empty((inp.batch, inp.num_q_heads, inp.head_dim), dtype=torch.bfloat16, device="cuda")
+    lse = torch.empty((inp.batch, inp.num_q_heads), dtype=torch.float32, device="cuda")
+    st = B.pa_decode_noalloc(p.shapes, p.plan, q, kp, vp, ks, vs, bad_d, sl, p.meta_dev, inp.scale, out, lse)
+    assert st == B.PA_ERR_DEVICE_BOUNDS
+    st = B.pa_decode_noalloc(p.shapes, p.plan, q, kp, vp, ks, vs, bt, sl, p.meta_dev, inp.scale, out, lse)
+    assert st == B.PA_OK
+
+
+def test_noalloc_checks_arguments_before_enqueuing_anything():
+    """A call refused on the host (here a NULL query) returns its error
+    before the status word is cleared or any kernel is enqueued; the next
+    valid call runs normally."""
+    inp = W.make_decode(2, 8, 4, 128, [100, 200], seed=25)
+    q, kp, vp, ks, vs, bt, sl = _device_inputs(inp)
+    p = ops.plan_decode(inp.seq_lens, inp.block_table, inp.num_q_heads, inp.num_kv_heads, inp.head_dim,
+                        inp.max_pages, inp.num_pool_pages, inp.kv_dtype)
+    out = torch.empty((2, 8, 128), dtype=torch.bfloat16, device="cuda")
+    lse = torch.empty((2, 8), dtype=torch.float32, device="cuda")
+    with pytest.raises(B.PaError) as e:
+        B.pa_decode_noalloc(p.shapes, p.plan, None, kp, vp, ks, vs, bt, sl, p.meta_dev, inp.scale, out, lse)
+    assert e.value.status == B.PA_ERR_INVALID_ARG
+    st = B.pa_decode_noalloc(p.shapes, p.plan, q, kp, vp, ks, vs, bt, sl, p.meta_dev, inp.scale, out, lse)
+    assert st == B.PA_OK
 
 
 def test_noalloc_rejects_plans_beyond_its_scratch():
