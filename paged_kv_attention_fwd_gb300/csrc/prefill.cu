@@ -282,46 +282,60 @@ __global__ void __launch_bounds__(320, 1)
             const uint32_t idesc_pv = idesc_f16(128, 128, !a.f16, false, true);
             constexpr uint32_t idesc_qk8 = idesc_e4m3(128, 128, false, false);
             const uint32_t qa = smem_u32(sm + L::kQOff);
+            // Descriptors are built once: an MMA's operands differ from the first by
+            // constant offsets, added to the start-address word (14 bits of 16-byte
+            // units; shared memory stays below 256 KB, so it never carries).  The
+            // issuing thread shares its SMSP with softmax warps, so every
+            // instruction it saves between MMAs keeps the tensor pipe fed.
+            const uint64_t qdesc = sdesc_sw128(qa, 16, 1024);
+            const uint64_t kdesc = sdesc_sw128(smem_u32(sm + L::kKOff), 16, 1024);
+            const uint64_t vdesc = sdesc_sw128(smem_u32(sm + L::kVOff), 16384, 1024);
+            const uint32_t q_lo = (uint32_t)qdesc, q_hi = (uint32_t)(qdesc >> 32);
+            const uint32_t k_lo = (uint32_t)kdesc, k_hi = (uint32_t)(kdesc >> 32);
+            const uint32_t v_lo = (uint32_t)vdesc, v_hi = (uint32_t)(vdesc >> 32);
             auto qk = [&](int x, int kslot) {
-                const uint32_t qb = qa + x * L::kQBytes;
-                const uint32_t kb = smem_u32(sm + L::kKOff + kslot * L::kKBytes);
+                const uint32_t qw = q_lo + (uint32_t)((x * L::kQBytes) >> 4);
+                const uint32_t kw = k_lo + (uint32_t)((kslot * L::kKBytes) >> 4);
+                const uint32_t dt = tbase + s_col(x);
                 if constexpr (F8) {
                     // per-head part on the e4m3 path (32 bytes of depth per MMA), then
                     // the rope part in bf16, hi and lo query levels against the same
                     // k_rope chunk, all into one accumulator
+                    mma_f8_ss_w<0>(dt, qw, q_hi, kw, k_hi, idesc_qk8);
 #pragma unroll
-                    for (int kk = 0; kk < 4; ++kk)
-                        mma_f8_ss(tbase + s_col(x), sdesc_sw128(qb + kk * 32, 16, 1024),
-                                  sdesc_sw128(kb + kk * 32, 16, 1024), idesc_qk8, kk > 0);
+                    for (int kk = 1; kk < 4; ++kk)
+                        mma_f8_ss_w<1>(dt, qw + (uint32_t)(kk * 2), q_hi, kw + (uint32_t)(kk * 2), k_hi, idesc_qk8);
 #pragma unroll
                     for (int lvl = 1; lvl <= 2; ++lvl)
 #pragma unroll
                         for (int kk = 0; kk < 4; ++kk)
-                            mma_ss(tbase + s_col(x), sdesc_sw128(qb + lvl * L::kTile + kk * 32, 16, 1024),
-                                   sdesc_sw128(kb + L::kTile + kk * 32, 16, 1024), idesc_qk, 1u);
+                            mma_ss_w<1>(dt, qw + (uint32_t)((lvl * L::kTile + kk * 32) >> 4), q_hi,
+                                        kw + (uint32_t)((L::kTile + kk * 32) >> 4), k_hi, idesc_qk);
                 } else {
+                    mma_ss_w<0>(dt, qw, q_hi, kw, k_hi, idesc_qk);
 #pragma unroll
-                    for (int kk = 0; kk < L::kDqk / 16; ++kk) {
-                        const int c = kk >> 2, off = (kk & 3) * 32;
-                        mma_ss(tbase + s_col(x), sdesc_sw128(qb + c * L::kTile + off, 16, 1024),
-                               sdesc_sw128(kb + c * L::kTile + off, 16, 1024), idesc_qk, kk > 0);
+                    for (int kk = 1; kk < L::kDqk / 16; ++kk) {
+                        const uint32_t off = (uint32_t)(((kk >> 2) * L::kTile + (kk & 3) * 32) >> 4);
+                        mma_ss_w<1>(dt, qw + off, q_hi, kw + off, k_hi, idesc_qk);
                     }
                     if constexpr (R8) {
                         // the query's rope chunk against the rope key's lo level
 #pragma unroll
                         for (int kk = 0; kk < 4; ++kk)
-                            mma_ss(tbase + s_col(x), sdesc_sw128(qb + 2 * L::kTile + kk * 32, 16, 1024),
-                                   sdesc_sw128(kb + 3 * L::kTile + kk * 32, 16, 1024), idesc_qk, 1u);
+                            mma_ss_w<1>(dt, qw + (uint32_t)((2 * L::kTile + kk * 32) >> 4), q_hi,
+                                        kw + (uint32_t)((3 * L::kTile + kk * 32) >> 4), k_hi, idesc_qk);
                     }
                 }
                 mma_commit(&bars[P_SF + x]);
             };
             auto pv = [&](int x, int vslot, bool first) {
-                const uint32_t vb = smem_u32(sm + L::kVOff + vslot * L::kVBytes);
+                const uint32_t vw = v_lo + (uint32_t)((vslot * L::kVBytes) >> 4);
+                const uint32_t dt = tbase + o_col(x), at = tbase + s_col(x);
+                if (first) mma_ts_w<0>(dt, at, vw, v_hi, idesc_pv);
+                else mma_ts_w<1>(dt, at, vw, v_hi, idesc_pv);
 #pragma unroll
-                for (int kk = 0; kk < 8; ++kk)
-                    mma_ts(tbase + o_col(x), tbase + s_col(x) + kk * 8, sdesc_sw128(vb + kk * 2048, 16384, 1024),
-                           idesc_pv, (!first || kk > 0) ? 1u : 0u);
+                for (int kk = 1; kk < 8; ++kk)
+                    mma_ts_w<1>(dt, at + kk * 8, vw + (uint32_t)((kk * 2048) >> 4), v_hi, idesc_pv);
                 mma_commit(&bars[P_OD + x]);
             };
             bool ok = true;

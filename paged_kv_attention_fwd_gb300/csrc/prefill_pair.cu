@@ -29,10 +29,12 @@
 //              in the one-CTA kernel's order (QK_A(j+1) right after PV_A(j));
 //              rank 1: idle after the TMEM allocation
 //   warps 2-5  softmax of tile A, warps 6-9 of tile B, in both CTAs: one
-//              query row per thread (its TMEM lane); P (16-bit) over the S
-//              columns; O rescaled in TMEM only when the running max grows by
-//              more than 2^8.  Rank 0's warps of the tile that takes an item's
-//              last K/V tile zero that tile's dead V rows in both CTAs.
+//              query row per thread (its TMEM lane), S read in 32-column
+//              chunks with the next chunk's load in flight; P (16-bit) over
+//              the S columns; O rescaled in TMEM only when the running max
+//              grows by more than 2^8.  Rank 0's warps of the tile that takes
+//              an item's last K/V tile zero that tile's dead V rows in both
+//              CTAs.
 //
 // Query row i of segment b sees key j iff j < kv_len and (not causal or
 // j <= qo_offset + i), qo_offset defaulting to kv_len - q_len (MATE
@@ -80,7 +82,7 @@ struct PairLayout {
     static constexpr int kVOff = kKOff + kNS * kKBytes;
     static constexpr int kBytes = kVOff + kNS * kVBytes;
     static constexpr int kSmem = kBytes + 1024;
-    static constexpr int kThreads = 320;
+    static constexpr int kThreads = 320;  // producer, MMA issuer, 8 softmax warps
     static_assert(kNS <= kMaxStages, "ring depth");
     static_assert(kSmem + 1024 <= 232448, "shared memory per CTA (dynamic + static)");
 };
@@ -288,26 +290,38 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(320, 1)
             const uint32_t idesc_qk = idesc_f16(256, 128, !a.f16, false, false);
             const uint32_t idesc_pv = idesc_f16(256, 128, !a.f16, false, true);
             const uint32_t qa = smem_u32(sm + L::kQOff);
+            // Descriptors are built once: an MMA's operands differ from the first by
+            // constant offsets, added to the start-address word (14 bits of 16-byte
+            // units; shared memory stays below 256 KB, so it never carries).
+            const uint64_t qdesc = sdesc_sw128(qa, 16, 1024);
+            const uint64_t kdesc = sdesc_sw128(smem_u32(sm + L::kKOff), 16, 1024);
+            const uint64_t vdesc = sdesc_sw128(smem_u32(sm + L::kVOff), 8192, 1024);
+            const uint32_t q_lo = (uint32_t)qdesc, q_hi = (uint32_t)(qdesc >> 32);
+            const uint32_t k_lo = (uint32_t)kdesc, k_hi = (uint32_t)(kdesc >> 32);
+            const uint32_t v_lo = (uint32_t)vdesc, v_hi = (uint32_t)(vdesc >> 32);
             auto qk = [&](int x, int kslot) {
-                const uint32_t qb = qa + x * L::kQBytes;
-                const uint32_t kb = smem_u32(sm + L::kKOff + kslot * L::kKBytes);
+                const uint32_t qw = q_lo + (uint32_t)((x * L::kQBytes) >> 4);
+                const uint32_t kw = k_lo + (uint32_t)((kslot * L::kKBytes) >> 4);
+                const uint32_t dt = tbase + s_col(x);
+                mma_pair_ss_w<0>(dt, qw, q_hi, kw, k_hi, idesc_qk);
 #pragma unroll
-                for (int kk = 0; kk < L::kDqk / 16; ++kk) {
-                    const int c = kk >> 2, off = (kk & 3) * 32;
-                    mma_pair_ss(tbase + s_col(x), sdesc_sw128(qb + c * L::kQTile + off, 16, 1024),
-                                sdesc_sw128(kb + c * L::kKTile + off, 16, 1024), idesc_qk, kk > 0);
-                }
+                for (int kk = 1; kk < L::kDqk / 16; ++kk)
+                    mma_pair_ss_w<1>(dt, qw + (uint32_t)(((kk >> 2) * L::kQTile + (kk & 3) * 32) >> 4), q_hi,
+                                     kw + (uint32_t)(((kk >> 2) * L::kKTile + (kk & 3) * 32) >> 4), k_hi, idesc_qk);
                 mma_commit_pair_mc(&bars[B_SF + x], 3);
             };
             // O_x is read by the softmax only after the item's last PV_x (the epilogue,
             // which waits on O_D) and, for a rescale, after S_x of the next tile has
-            // landed -- whose commit follows PV_x of this tile in issue order
+            // landed -- whose commit follows PV_x of this tile in issue order.  Keys
+            // 16kk..16kk+15: P at TMEM columns 8kk..8kk+7 of S_x.
             auto pv = [&](int x, int vslot, bool first, bool last) {
-                const uint32_t vb = smem_u32(sm + L::kVOff + vslot * L::kVBytes);
+                const uint32_t vw = v_lo + (uint32_t)((vslot * L::kVBytes) >> 4);
+                const uint32_t dt = tbase + o_col(x), at = tbase + s_col(x);
+                if (first) mma_pair_ts_w<0>(dt, at, vw, v_hi, idesc_pv);
+                else mma_pair_ts_w<1>(dt, at, vw, v_hi, idesc_pv);
 #pragma unroll
-                for (int kk = 0; kk < 8; ++kk)
-                    mma_pair_ts(tbase + o_col(x), tbase + s_col(x) + kk * 8, sdesc_sw128(vb + kk * 2048, 8192, 1024),
-                                idesc_pv, (!first || kk > 0) ? 1u : 0u);
+                for (int kk = 1; kk < 8; ++kk)
+                    mma_pair_ts_w<1>(dt, at + kk * 8, vw + (uint32_t)((kk * 2048) >> 4), v_hi, idesc_pv);
                 if (last) mma_commit_pair_mc(&bars[B_OD + x], 3);
             };
             bool ok = true;
@@ -377,10 +391,17 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(320, 1)
         }
     } else {
         // ---------------------------------------------------------------- softmax (A: warps 2-5, B: 6-9)
+        // One query row per thread (its TMEM lane).  S is read in 32-column
+        // chunks with the next chunk's load in flight while the current chunk
+        // is reduced (pass 1: the row max) or exponentiated (pass 2: P, 16-bit,
+        // written over S columns already read: keys 32c..32c+31 -> P columns
+        // 16c..16c+15), so the load latency is paid once per pass.
         const int x = warp >= 6 ? 1 : 0;
         const int q4 = warp & 3;
         const int row = q4 * 32 + lane;  // query row within this CTA's half of the tile = TMEM lane
         const uint32_t lane_addr = (uint32_t)(q4 * 32) << 16;
+        const uint32_t s_addr = tbase + lane_addr + s_col(x);
+        const uint32_t o_addr = tbase + lane_addr + o_col(x);
         const bool f16 = a.f16 != 0;
         bool ok = true;
         uint32_t kit = 0, gt = 0, ns = 0;  // items, K/V tiles before this item, S tiles of this query tile
@@ -420,117 +441,119 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(320, 1)
                     // every key of the tile visible to every row of the warp, positive scale:
                     // no per-element masking, and the max can be taken on the raw scores
                     const bool full = __all_sync(0xffffffffu, vis >= 128) && sl2 > 0.f;
-                    // One read of S per 64-column half: the half's max, then P = exp2(s - m)
-                    // against the running max m, written over S columns already read (keys
-                    // 64h..64h+63 -> P columns 32h..32h+31).  m is raised only when a half's
-                    // max passes it by 2^8 (until then the stale max is exact and p <= 256);
-                    // what was computed against the old m -- the running sum, this tile's
-                    // first half of P, O of the earlier tiles -- is then scaled by 2^(old - new).
-                    const bool had_o = m_run != -INFINITY;  // O holds earlier tiles' P.V
-                    float rs0 = 0.f, rs1 = 0.f, f_tile = 1.f, f_p0 = 1.f;
-                    bool grew = false;
-#pragma unroll 1
-                    for (int hh = 0; hh < 2; ++hh) {
-                        uint32_t r[64], pw[32];
-                        tmem_ld_x32(tbase + lane_addr + s_col(x) + hh * 64, *reinterpret_cast<uint32_t(*)[32]>(&r[0]));
-                        tmem_ld_x32(tbase + lane_addr + s_col(x) + hh * 64 + 32,
-                                    *reinterpret_cast<uint32_t(*)[32]>(&r[32]));
-                        tmem_ld_wait();
-                        reg_fence(r);
-                        float mh;
-                        {
-                            float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+                    // pass 1: row max of the scaled, masked scores
+                    float mt;
+                    {
+                        float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+                        uint32_t ra[32], rb[32];
+                        auto reduce = [&](const uint32_t (&r)[32], int c) {
                             if (full) {
 #pragma unroll
-                                for (int kk = 0; kk < 64; kk += 2)
+                                for (int kk = 0; kk < 32; kk += 2)
                                     m4[(kk >> 1) & 3] =
                                         fmax3(m4[(kk >> 1) & 3], __uint_as_float(r[kk]), __uint_as_float(r[kk + 1]));
                             } else {
 #pragma unroll
-                                for (int kk = 0; kk < 64; ++kk)
-                                    if (hh * 64 + kk < vis) m4[kk & 3] = fmaxf(m4[kk & 3], __uint_as_float(r[kk]) * sl2);
+                                for (int kk = 0; kk < 32; ++kk)
+                                    if (c * 32 + kk < vis) m4[kk & 3] = fmaxf(m4[kk & 3], __uint_as_float(r[kk]) * sl2);
                             }
-                            mh = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
-                            if (full) mh *= sl2;
-                        }
-                        const bool g = mh > m_run + kRescaleThreshold;
-                        const bool had_p0 = hh == 1 && m_run != -INFINITY;  // this row's first half holds P
-                        float f = 1.f;
-                        if (g) {
-                            if (m_run != -INFINITY) f = ex2(m_run - mh);
-                            m_run = mh;
-                            l_run *= f;
-                            rs0 *= f;
-                            rs1 *= f;
-                            f_tile *= f;
-                            grew = true;
-                        }
-                        if (hh == 1) f_p0 = (g && had_p0) ? f : 1.f;
-                        const bool none = m_run == -INFINITY;
-                        const bool fast = __all_sync(0xffffffffu, full && !none);
-                        const float neg_m = -m_run;
-                        if (fast) {
-                            const uint64_t sc2 = f2_pack(__float_as_uint(sl2), __float_as_uint(sl2));
-                            const uint64_t nm2 = f2_pack(__float_as_uint(neg_m), __float_as_uint(neg_m));
-                            uint64_t acc2 = f2_pack(0u, 0u);
-#pragma unroll
-                            for (int kk = 0; kk < 32; ++kk) {
-                                float x0, x1;
-                                f2_unpack(f2_fma(f2_pack(r[2 * kk], r[2 * kk + 1]), sc2, nm2), x0, x1);
-                                const float p0 = ex2(x0), p1 = ex2(x1);
-                                acc2 = f2_add(acc2, f2_pack(__float_as_uint(p0), __float_as_uint(p1)));
-                                pw[kk] = pack16x2(p0, p1, f16);
-                            }
-                            float a0, a1;
-                            f2_unpack(acc2, a0, a1);
-                            rs0 += a0;
-                            rs1 += a1;
-                        } else {
-#pragma unroll
-                            for (int kk = 0; kk < 32; ++kk) {
-                                const int key = hh * 64 + 2 * kk;
-                                const float p0 =
-                                    (none || key >= vis) ? 0.f : ex2(__uint_as_float(r[2 * kk]) * sl2 - m_run);
-                                const float p1 =
-                                    (none || key + 1 >= vis) ? 0.f : ex2(__uint_as_float(r[2 * kk + 1]) * sl2 - m_run);
-                                rs0 += p0;
-                                rs1 += p1;
-                                pw[kk] = pack16x2(p0, p1, f16);
-                            }
-                        }
-                        tmem_st_x32(tbase + lane_addr + s_col(x) + hh * 32, pw);
-                    }
-                    if (__any_sync(0xffffffffu, f_p0 != 1.f)) {
-                        // rare: the second half raised the max; bring the first half's P to it
-                        tmem_st_wait();
-                        uint32_t q[32];
-                        tmem_ld_x32(tbase + lane_addr + s_col(x), q);
+                        };
+                        tmem_ld_x32(s_addr, ra);
                         tmem_ld_wait();
-                        reg_fence(q);
-#pragma unroll
-                        for (int kk = 0; kk < 32; ++kk) {
-                            float lo, hi;
-                            unpack16x2(q[kk], f16, lo, hi);
-                            q[kk] = pack16x2(lo * f_p0, hi * f_p0, f16);
-                        }
-                        tmem_st_x32(tbase + lane_addr + s_col(x), q);
+                        reg_fence(ra);
+                        tmem_ld_x32(s_addr + 32, rb);
+                        reduce(ra, 0);
+                        tmem_ld_wait();
+                        reg_fence(rb);
+                        tmem_ld_x32(s_addr + 64, ra);
+                        reduce(rb, 1);
+                        tmem_ld_wait();
+                        reg_fence(ra);
+                        tmem_ld_x32(s_addr + 96, rb);
+                        reduce(ra, 2);
+                        tmem_ld_wait();
+                        reg_fence(rb);
+                        reduce(rb, 3);
+                        mt = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
+                        if (full) mt *= sl2;
                     }
-                    l_run += rs0 + rs1;
-                    // O of the earlier tiles follows the max (PV_x of the previous tile retired
-                    // before this S_x landed: one commit covers both)
-                    if (__any_sync(0xffffffffu, grew && had_o && j > 0)) {
-                        const float alpha = (grew && had_o) ? f_tile : 1.f;
+                    // conditional rescale: keep the stale max unless the new one is 2^8 larger
+                    const bool grow = mt > m_run + kRescaleThreshold;
+                    const float m_new = grow ? mt : m_run;
+                    if (__any_sync(0xffffffffu, grow && j > 0 && m_run != -INFINITY)) {
+                        // PV_x of the previous tile retired before this S_x landed (one commit covers both)
+                        const float alpha = (grow && m_run != -INFINITY) ? ex2(m_run - m_new) : 1.f;
 #pragma unroll
                         for (int c = 0; c < 4; ++c) {
                             uint32_t o[32];
-                            tmem_ld_x32(tbase + lane_addr + o_col(x) + c * 32, o);
+                            tmem_ld_x32(o_addr + c * 32, o);
                             tmem_ld_wait();
                             reg_fence(o);
 #pragma unroll
                             for (int kk = 0; kk < 32; ++kk) o[kk] = __float_as_uint(__uint_as_float(o[kk]) * alpha);
-                            tmem_st_x32(tbase + lane_addr + o_col(x) + c * 32, o);
+                            tmem_st_x32(o_addr + c * 32, o);
                         }
                     }
+                    if (grow) {
+                        if (m_run != -INFINITY) l_run *= ex2(m_run - m_new);
+                        m_run = m_new;
+                    }
+                    const bool none = m_run == -INFINITY;
+                    const bool fast = __all_sync(0xffffffffu, full && !none);
+                    const float neg_m = -m_run;
+                    // pass 2: P = exp2(x - m); two packed partial sums keep the adds off one chain
+                    uint64_t acc[2] = {f2_pack(0u, 0u), f2_pack(0u, 0u)};
+                    float rsm = 0.f;
+                    {
+                        uint32_t ra[32], rb[32];
+                        auto expo = [&](const uint32_t (&r)[32], int c) {
+                            uint32_t pw[16];
+                            if (fast) {
+                                const uint64_t sc2 = f2_pack(__float_as_uint(sl2), __float_as_uint(sl2));
+                                const uint64_t nm2 = f2_pack(__float_as_uint(neg_m), __float_as_uint(neg_m));
+#pragma unroll
+                                for (int kk = 0; kk < 16; ++kk) {
+                                    float x0, x1;
+                                    f2_unpack(f2_fma(f2_pack(r[2 * kk], r[2 * kk + 1]), sc2, nm2), x0, x1);
+                                    const float p0 = ex2(x0), p1 = ex2(x1);
+                                    acc[kk & 1] = f2_add(acc[kk & 1], f2_pack(__float_as_uint(p0), __float_as_uint(p1)));
+                                    pw[kk] = pack16x2(p0, p1, f16);
+                                }
+                            } else {
+#pragma unroll
+                                for (int kk = 0; kk < 16; ++kk) {
+                                    const int key = c * 32 + 2 * kk;
+                                    const float p0 =
+                                        (none || key >= vis) ? 0.f : ex2(__uint_as_float(r[2 * kk]) * sl2 - m_run);
+                                    const float p1 =
+                                        (none || key + 1 >= vis) ? 0.f : ex2(__uint_as_float(r[2 * kk + 1]) * sl2 - m_run);
+                                    rsm += p0 + p1;
+                                    pw[kk] = pack16x2(p0, p1, f16);
+                                }
+                            }
+                            tmem_st_x16(s_addr + c * 16, pw);
+                        };
+                        tmem_ld_x32(s_addr, ra);
+                        tmem_ld_wait();
+                        reg_fence(ra);
+                        tmem_ld_x32(s_addr + 32, rb);
+                        expo(ra, 0);
+                        tmem_ld_wait();
+                        reg_fence(rb);
+                        tmem_ld_x32(s_addr + 64, ra);
+                        expo(rb, 1);
+                        tmem_ld_wait();
+                        reg_fence(ra);
+                        tmem_ld_x32(s_addr + 96, rb);
+                        expo(ra, 2);
+                        tmem_ld_wait();
+                        reg_fence(rb);
+                        expo(rb, 3);
+                    }
+                    float a0, a1, b0, b1;
+                    f2_unpack(acc[0], a0, a1);
+                    f2_unpack(acc[1], b0, b1);
+                    l_run += (a0 + a1) + (b0 + b1) + rsm;
                 }
                 if (zeroer && j == nkv - 1) {
                     // the V tile's halves of both CTAs landed once rank 0's full barrier completed
@@ -573,7 +596,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(320, 1)
 #pragma unroll
                     for (int c = 0; c < 4; ++c) {
                         uint32_t o[32];
-                        tmem_ld_x32(tbase + lane_addr + o_col(x) + c * 32, o);
+                        tmem_ld_x32(o_addr + c * 32, o);
                         tmem_ld_wait();
                         reg_fence(o);
                         if (write) {
