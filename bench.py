@@ -845,7 +845,7 @@ def run_prefill(args, rank, world, local_rank, dist):
     prof = "prefill_kernel_" + ("prefill_paged" if args.workload == "prefill_paged_fp16" else args.workload) + ".md"
     roofline = {"bound": "tensor", "achieved": round(tfs, 2), "peak": peak, "unit": "TFLOP/s",
                 "frac": round(tfs / peak, 4),
-                "traffic": profiled_traffic(prof, ["prefill.cu", "pa_ptx.cuh", "pa_internal.h"]),
+                "traffic": profiled_traffic(prof, ["prefill.cu", "prefill_common.cuh", "pa_ptx.cuh", "pa_internal.h"]),
                 "kernel": "prefill_kernel", "peak_source": peak_source,
                 "algorithmic_flops_per_launch": flops, "kernel_ms": round(ms, 5)}
     e2e = None
