@@ -92,13 +92,14 @@ struct PrefillLayout {
 // region until none is left.  Every barrier's phase runs on across items,
 // so the producer loads the next item's query and first K/V tiles while the
 // current item's last tiles and output are still in progress.
-template <bool ROPE, bool PAGED, bool F8, bool R8>
+template <bool ROPE, bool PAGED, bool F8, bool R8, bool F16>
 __global__ void __launch_bounds__(320, 1)
     prefill_kernel(const __grid_constant__ PrefillArgs a, const __grid_constant__ CUtensorMap map_q,
                    const __grid_constant__ CUtensorMap map_k, const __grid_constant__ CUtensorMap map_v,
                    const __grid_constant__ CUtensorMap map_r, const __grid_constant__ CUtensorMap map_qr) {
     static_assert(!F8 || (ROPE && !PAGED), "e4m3 query/key parts: MLA with ragged keys only");
     static_assert(!R8 || (ROPE && !PAGED && !F8), "two-level rope key: bf16 MLA with ragged keys only");
+    static_assert(!F16 || (!F8 && !R8), "the e4m3 variants take bf16 parts");
     using L = PrefillLayout<ROPE, F8, R8>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -278,8 +279,8 @@ __global__ void __launch_bounds__(320, 1)
     } else if (warp == 1) {
         // ---------------------------------------------------------------- MMA issuer
         if (lane == 0) {
-            const uint32_t idesc_qk = idesc_f16(128, 128, !a.f16, false, false);
-            const uint32_t idesc_pv = idesc_f16(128, 128, !a.f16, false, true);
+            constexpr uint32_t idesc_qk = idesc_f16(128, 128, !F16, false, false);
+            constexpr uint32_t idesc_pv = idesc_f16(128, 128, !F16, false, true);
             constexpr uint32_t idesc_qk8 = idesc_e4m3(128, 128, false, false);
             const uint32_t qa = smem_u32(sm + L::kQOff);
             // Descriptors are built once: an MMA's operands differ from the first by
@@ -334,8 +335,8 @@ __global__ void __launch_bounds__(320, 1)
                 if (first) mma_ts_w<0>(dt, at, vw, v_hi, idesc_pv);
                 else mma_ts_w<1>(dt, at, vw, v_hi, idesc_pv);
 #pragma unroll
-                for (int kk = 1; kk < 8; ++kk)
-                    mma_ts_w<1>(dt, at + kk * 8, vw + (uint32_t)((kk * 2048) >> 4), v_hi, idesc_pv);
+                for (int kk = 1; kk < 8; ++kk)  // P of keys 64..127 sits 32 columns further on
+                    mma_ts_w<1>(dt, at + kk * 8 + (kk >= 4 ? 32 : 0), vw + (uint32_t)((kk * 2048) >> 4), v_hi, idesc_pv);
                 mma_commit(&bars[P_OD + x]);
             };
             bool ok = true;
@@ -416,7 +417,9 @@ __global__ void __launch_bounds__(320, 1)
         const int q4 = warp & 3;
         const int row = q4 * 32 + lane;           // query row within the tile = TMEM lane
         const uint32_t lane_addr = (uint32_t)(q4 * 32) << 16;
-        const bool f16 = a.f16 != 0;
+        // a compile-time element type: the P conversions in the exponential loop
+        // carry no per-pair branch
+        constexpr bool f16 = F16;
         bool ok = true;
         uint32_t kit = 0, gt = 0, ns = 0;  // items, K/V tiles before this item, S tiles of this query tile
         for (;;) {
@@ -488,13 +491,14 @@ __global__ void __launch_bounds__(320, 1)
                 // every key of the tile visible to every row of the warp, positive scale:
                 // no per-element masking, and the max can be taken on the raw scores
                 const bool full = __all_sync(0xffffffffu, vis >= 128) && sl2 > 0.f;
-                // pass 1: row max of the scaled, masked scores (S read from TMEM, 64 columns per wait)
+                // pass 1: row max of the scaled, masked scores (S read from TMEM, 64 columns
+                // per wait); the second half stays in registers for pass 2
                 float mt;
+                uint32_t r[64];
                 {
                     float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll 1
                     for (int hh = 0; hh < 2; ++hh) {
-                        uint32_t r[64];
                         tmem_ld_x32(tbase + lane_addr + s_col(x) + hh * 64, *reinterpret_cast<uint32_t(*)[32]>(&r[0]));
                         tmem_ld_x32(tbase + lane_addr + s_col(x) + hh * 64 + 32, *reinterpret_cast<uint32_t(*)[32]>(&r[32]));
                         tmem_ld_wait();
@@ -542,15 +546,19 @@ __global__ void __launch_bounds__(320, 1)
                 const bool fast = __all_sync(0xffffffffu, full && !none);
                 const float neg_m = -m_run;
                 float rs0 = 0.f, rs1 = 0.f;
-                // pass 2: P = exp2(x - m) in bf16, written over S columns already read
-                // (keys 64h..64h+63 -> P columns 32h..32h+31)
+                // pass 2: P = exp2(x - m) in 16 bits, written over S columns already read:
+                // keys 64..127 first, from the registers, to P columns 64..95, then keys
+                // 0..63, read again, to P columns 0..31
 #pragma unroll 1
-                for (int hh = 0; hh < 2; ++hh) {
-                    uint32_t r[64], pw[32];
-                    tmem_ld_x32(tbase + lane_addr + s_col(x) + hh * 64, *reinterpret_cast<uint32_t(*)[32]>(&r[0]));
-                    tmem_ld_x32(tbase + lane_addr + s_col(x) + hh * 64 + 32, *reinterpret_cast<uint32_t(*)[32]>(&r[32]));
-                    tmem_ld_wait();
-                    reg_fence(r);
+                for (int t = 0; t < 2; ++t) {
+                    const int hh = 1 - t;
+                    uint32_t pw[32];
+                    if (t == 1) {
+                        tmem_ld_x32(tbase + lane_addr + s_col(x), *reinterpret_cast<uint32_t(*)[32]>(&r[0]));
+                        tmem_ld_x32(tbase + lane_addr + s_col(x) + 32, *reinterpret_cast<uint32_t(*)[32]>(&r[32]));
+                        tmem_ld_wait();
+                        reg_fence(r);
+                    }
                     if (fast) {
                         const uint64_t sc2 = f2_pack(__float_as_uint(sl2), __float_as_uint(sl2));
                         const uint64_t nm2 = f2_pack(__float_as_uint(neg_m), __float_as_uint(neg_m));
@@ -578,7 +586,7 @@ __global__ void __launch_bounds__(320, 1)
                             pw[k] = pack16x2(p0, p1, f16);
                         }
                     }
-                    tmem_st_x32(tbase + lane_addr + s_col(x) + hh * 32, pw);
+                    tmem_st_x32(tbase + lane_addr + s_col(x) + hh * 64, pw);
                 }
                 const float rs = rs0 + rs1;
                 l_run += rs;
@@ -717,12 +725,12 @@ __global__ void __launch_bounds__(512) prefill_order_kernel(const PrefillArgs a,
     }
 }
 
-template <bool ROPE, bool PAGED, bool F8, bool R8 = false>
+template <bool ROPE, bool PAGED, bool F8, bool R8 = false, bool F16 = false>
 cudaError_t launch_t(const PrefillArgs& a, const CUtensorMap* mq, const CUtensorMap* mk, const CUtensorMap* mv,
                      const CUtensorMap* mr, const CUtensorMap* mqr, cudaStream_t stream) {
     using L = PrefillLayout<ROPE, F8, R8>;
     static std::atomic<uint64_t> configured{0};
-    cudaError_t e = ensure_dynamic_smem(prefill_kernel<ROPE, PAGED, F8, R8>, L::kSmem, configured);
+    cudaError_t e = ensure_dynamic_smem(prefill_kernel<ROPE, PAGED, F8, R8, F16>, L::kSmem, configured);
     if (e != cudaSuccess) return e;
     if (a.order) {
         prefill_order_kernel<<<1, 512, 0, stream>>>(a, const_cast<int32_t*>(a.order));
@@ -738,7 +746,7 @@ cudaError_t launch_t(const PrefillArgs& a, const CUtensorMap* mq, const CUtensor
     if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
     if (e != cudaSuccess) return e;
     const unsigned grid = (unsigned)(items < sms ? items : sms);
-    prefill_kernel<ROPE, PAGED, F8, R8><<<grid, L::kThreads, L::kSmem, stream>>>(a, *mq, *mk, *mv, *mr, *mqr);
+    prefill_kernel<ROPE, PAGED, F8, R8, F16><<<grid, L::kThreads, L::kSmem, stream>>>(a, *mq, *mk, *mv, *mr, *mqr);
     return cudaGetLastError();
 }
 
@@ -785,9 +793,14 @@ cudaError_t launch_prefill(const PrefillArgs& a, int head_dim_qk, const CUtensor
                            cudaStream_t stream) {
     if (a.f8) return launch_t<true, false, true>(a, mq, mk, mv, mr, mqr, stream);
     if (a.r8) return launch_t<true, false, false, true>(a, mq, mk, mv, mr, mqr, stream);
-    if (head_dim_qk == 192) return launch_t<true, false, false>(a, mq, mk, mv, mr, mqr, stream);
-    return a.paged ? launch_t<false, true, false>(a, mq, mk, mv, mr, mqr, stream)
-                   : launch_t<false, false, false>(a, mq, mk, mv, mr, mqr, stream);
+    if (head_dim_qk == 192)
+        return a.f16 ? launch_t<true, false, false, false, true>(a, mq, mk, mv, mr, mqr, stream)
+                     : launch_t<true, false, false, false, false>(a, mq, mk, mv, mr, mqr, stream);
+    if (a.paged)
+        return a.f16 ? launch_t<false, true, false, false, true>(a, mq, mk, mv, mr, mqr, stream)
+                     : launch_t<false, true, false, false, false>(a, mq, mk, mv, mr, mqr, stream);
+    return a.f16 ? launch_t<false, false, false, false, true>(a, mq, mk, mv, mr, mqr, stream)
+                 : launch_t<false, false, false, false, false>(a, mq, mk, mv, mr, mqr, stream);
 }
 
 cudaError_t launch_rope_expand(const uint8_t* codes, const float* scales, uint16_t* hi, uint16_t* lo,
