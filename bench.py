@@ -91,31 +91,17 @@ class NoFlush:
         pass
 
 
-def gate(stream):
-    """Hold the (idle, synchronised) stream for ~0.1 ms with torch's spin kernel,
-    so that the host enqueues the start event and the first steps behind it:
-    the events then bracket the device's execution of the K steps, not the
-    host's latency to its first launch.  Nothing of the gate is timed."""
-    import torch
-    sleep = getattr(torch.cuda, "_sleep", None)
-    if sleep is not None:
-        with torch.cuda.stream(stream):
-            sleep(200000)
-
-
 def time_steps(K, step, flush, stream):
     """Mean device time of one step (ms) over K steps, from CUDA events on the
     launching stream.  Without a flush the K steps run back to back between
     one pair of events, so each launch may start its shared-memory prologue
     while the previous step's kernel drains, as in a serving loop (every
-    kernel still waits for the one before it before touching memory), behind
-    a short gate kernel (see gate()).  With a flush each step has its own pair
-    of events and the flush runs outside them.  The caller synchronises before
-    and after."""
+    kernel still waits for the one before it before touching memory).  With a
+    flush each step has its own pair of events and the flush runs outside
+    them.  The caller synchronises before and after."""
     import torch
     if isinstance(flush, NoFlush):
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        gate(stream)
         e0.record(stream)
         for _ in range(K):
             step()
