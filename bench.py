@@ -546,19 +546,20 @@ def run_decode(args, rank, world, local_rank, dist):
             with torch.cuda.stream(stream):
                 cg.replay()
 
-    for _ in range(args.warmup):
-        flush()
-        step_call()
-    torch.cuda.synchronize(dev)
-    st = B.pa_check_status(p.workspace, stream)
-    if st != B.PA_OK:
-        raise RuntimeError(f"device status {st}: {B.pa_last_error()}")
-
     K = args.steps
-    if dist is not None:
-        dist.barrier()
-    torch.cuda.synchronize(dev)
+    # the warm-up runs inside the sampler's window, after its settling pause,
+    # so the timed steps follow it on a GPU that has not gone idle
     with ClockSampler(gpu_index(local_rank)) as clk:
+        for _ in range(args.warmup):
+            flush()
+            step_call()
+        torch.cuda.synchronize(dev)
+        st = B.pa_check_status(p.workspace, stream)
+        if st != B.PA_OK:
+            raise RuntimeError(f"device status {st}: {B.pa_last_error()}")
+        if dist is not None:
+            dist.barrier()
+        torch.cuda.synchronize(dev)
         ms = time_steps(K, step_call, flush, stream)  # a step: one decode launch, split merge fused in
         torch.cuda.synchronize(dev)
     if dist is not None:
@@ -812,17 +813,17 @@ def run_prefill(args, rank, world, local_rank, dist):
 
     step = prefill_prepared(inp, sh, d, out, lse, ws, stream)
 
-    for _ in range(args.warmup):
-        flush()
-        step()
-    torch.cuda.synchronize(dev)
-    if B.pa_check_status(ws, stream) != B.PA_OK:
-        raise RuntimeError(B.pa_last_error())
     K = args.steps
-    if dist is not None:
-        dist.barrier()
-    torch.cuda.synchronize(dev)
-    with ClockSampler(gpu_index(local_rank)) as clk:
+    with ClockSampler(gpu_index(local_rank)) as clk:  # warm-up inside the window, as for the decode
+        for _ in range(args.warmup):
+            flush()
+            step()
+        torch.cuda.synchronize(dev)
+        if B.pa_check_status(ws, stream) != B.PA_OK:
+            raise RuntimeError(B.pa_last_error())
+        if dist is not None:
+            dist.barrier()
+        torch.cuda.synchronize(dev)
         ms = time_steps(K, step, flush, stream)
         torch.cuda.synchronize(dev)
     if dist is not None:
@@ -956,14 +957,14 @@ def run_append(args, rank, world, local_rank, dist):
     def step():
         B.pa_append_kv(sh, knd, vnd, cu, sp, bt, kp, vp, None, None, ws, stream=stream)
 
-    for _ in range(args.warmup):
-        flush()
-        step()
     K = args.steps
-    if dist is not None:
-        dist.barrier()
-    torch.cuda.synchronize(dev)
-    with ClockSampler(gpu_index(local_rank)) as clk:
+    with ClockSampler(gpu_index(local_rank)) as clk:  # warm-up inside the window, as for the decode
+        for _ in range(args.warmup):
+            flush()
+            step()
+        if dist is not None:
+            dist.barrier()
+        torch.cuda.synchronize(dev)
         ms = time_steps(K, step, flush, stream)
         torch.cuda.synchronize(dev)
     ms, = max_over_ranks([ms], dist, dev)
@@ -1072,16 +1073,16 @@ def run_mixed(args, rank, world, local_rank, dist):
             if B.pa_check_status(part, stream) != B.PA_OK:
                 raise RuntimeError(B.pa_last_error())
 
-    for _ in range(args.warmup):
-        flush()
-        step()
-    torch.cuda.synchronize(dev)
-    check()
     K = args.steps
-    if dist is not None:
-        dist.barrier()
-    torch.cuda.synchronize(dev)
-    with ClockSampler(gpu_index(local_rank)) as clk:
+    with ClockSampler(gpu_index(local_rank)) as clk:  # warm-up inside the window, as for the decode
+        for _ in range(args.warmup):
+            flush()
+            step()
+        torch.cuda.synchronize(dev)
+        check()
+        if dist is not None:
+            dist.barrier()
+        torch.cuda.synchronize(dev)
         ms = time_steps(K, step, flush, stream)
         torch.cuda.synchronize(dev)
     if dist is not None:
