@@ -38,6 +38,7 @@
 #include <cuda_fp8.h>
 
 #include "pa_internal.h"
+#include "pa_launch.h"
 #include "pa_ptx.cuh"
 #include "prefill_common.cuh"
 
@@ -133,6 +134,9 @@ __global__ void __launch_bounds__(320, 1)
         *abort_sh = 0;
         fence_barrier_init();
     }
+    // launched as a programmatic dependent (of the unit-order kernel, or of
+    // whatever the stream ran before): nothing global and no TMEM before this
+    grid_dependency_wait();
     if (warp == 1) {
         tmem_alloc(&tmem_base_sh, 512);
         tmem_relinquish();
@@ -687,6 +691,9 @@ __global__ void __launch_bounds__(320, 1)
 //   [63:40] 0xFFFFFF - kv_len   [39:20] b   [19:0] 0xFFFFF - query block
 // with kv_len forced to 0 for idle units (their rows lie past q_len).
 __global__ void __launch_bounds__(512) prefill_order_kernel(const PrefillArgs a, int32_t* order) {
+    // the prefill kernel may be scheduled now: it runs its barrier set-up and
+    // then waits for this kernel's completion before reading the order
+    allow_dependents_launch();
     __shared__ unsigned long long key[4096];
     const int n = a.batch * a.num_q_tiles;
     int p2 = 1;
@@ -746,8 +753,8 @@ cudaError_t launch_t(const PrefillArgs& a, const CUtensorMap* mq, const CUtensor
     if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
     if (e != cudaSuccess) return e;
     const unsigned grid = (unsigned)(items < sms ? items : sms);
-    prefill_kernel<ROPE, PAGED, F8, R8, F16><<<grid, L::kThreads, L::kSmem, stream>>>(a, *mq, *mk, *mv, *mr, *mqr);
-    return cudaGetLastError();
+    return launch_overlapped(prefill_kernel<ROPE, PAGED, F8, R8, F16>, dim3(grid), dim3(L::kThreads), L::kSmem, stream,
+                             a, *mq, *mk, *mv, *mr, *mqr);
 }
 
 // The e4m3 rope key times its token's scale as two bf16 levels, hi = bf16(x)
