@@ -490,6 +490,16 @@ const char* pa_last_error(void);
  * this call (default 2e9).  Process-wide. */
 pa_status pa_set_wait_limit_ns(uint64_t limit_ns);
 
+/* Form of the bf16 / fp16 pa_prefill for calls made after this one
+ * (process-wide): enable = 0, the default, runs one CTA per 256-row work item
+ * on the tensor cores of its SM; enable != 0 runs CTA pairs (cta_group::2,
+ * M = 256 over two SMs, 512-row work items).  Both compute the same result
+ * within the stated tolerances; the pair form is slower on the measured
+ * workloads and kept for comparison.  The e4m3 MLA entry points are not
+ * affected.  Always returns PA_OK; falls back to the one-CTA form where no
+ * cluster of two CTAs fits. */
+pa_status pa_set_prefill_cta_pairs(int enable);
+
 /*
  * Test hook for failure detection: launch one CTA that waits, with the time
  * limit given, on a barrier that nothing arrives on, then records

@@ -120,10 +120,11 @@ def lib() -> ctypes.CDLL:
         L.pa_check_status.argtypes = [_P, _P]
         L.pa_last_error.restype = ctypes.c_char_p
         L.pa_set_wait_limit_ns.argtypes = [u64]
+        L.pa_set_prefill_cta_pairs.argtypes = [i32]
         L.pa_debug_wait_timeout.argtypes = [_P, u64, _P]
         L.pa_version.restype = i32
         for f in ("pa_get_metadata", "pa_decode", "pa_decode_attend", "pa_decode_combine", "pa_prefill", "pa_check_status", "pa_set_wait_limit_ns",
-                  "pa_debug_wait_timeout"):
+                  "pa_set_prefill_cta_pairs", "pa_debug_wait_timeout"):
             getattr(L, f).restype = ctypes.c_int
         _lib = L
     return _lib
@@ -351,6 +352,10 @@ def pa_check_status(workspace, stream=None) -> int:
 
 def pa_set_wait_limit_ns(limit_ns: int) -> None:
     _check(lib().pa_set_wait_limit_ns(int(limit_ns)))
+
+
+def pa_set_prefill_cta_pairs(enable: bool) -> None:
+    _check(lib().pa_set_prefill_cta_pairs(1 if enable else 0))
 
 
 def pa_debug_wait_timeout(workspace, limit_ns: int, stream=None) -> None:

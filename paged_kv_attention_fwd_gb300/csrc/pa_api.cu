@@ -19,6 +19,9 @@ namespace {
 
 thread_local std::string g_last_error;
 std::atomic<uint64_t> g_wait_limit_ns{2000000000ull};
+// pa_prefill's bf16 / fp16 form: 0 one CTA per 256-row work item (default),
+// 1 CTA pairs on 512-row items (prefill_pair.cu)
+std::atomic<int> g_prefill_cta_pairs{0};
 
 pa_status fail(pa_status st, const char* fmt, ...) {
     char buf[512];
@@ -175,6 +178,11 @@ const char* pa_last_error(void) { return g_last_error.c_str(); }
 pa_status pa_set_wait_limit_ns(uint64_t limit_ns) {
     if (limit_ns == 0) return fail(PA_ERR_INVALID_ARG, "wait limit must be positive");
     g_wait_limit_ns.store(limit_ns);
+    return PA_OK;
+}
+
+pa_status pa_set_prefill_cta_pairs(int enable) {
+    g_prefill_cta_pairs.store(enable != 0 ? 1 : 0);
     return PA_OK;
 }
 
@@ -483,9 +491,6 @@ pa_status pa_decode(const pa_decode_shapes* sh, const pa_decode_plan* plan, cons
 }
 
 namespace {
-// bf16 / fp16 prefill on CTA pairs (prefill_pair.cu) instead of one CTA per item
-constexpr bool kPairPrefill = false;
-
 // The launch arguments common to pa_prefill and pa_prefill_mla_fp8.
 pa_status fill_prefill_args(const pa_prefill_shapes* sh, const int32_t* cu_seqlens_q, const int32_t* cu_seqlens_k,
                             const int32_t* block_table, const int32_t* qo_offset, int causal, float scale, void* out,
@@ -611,7 +616,7 @@ pa_status pa_prefill(const pa_prefill_shapes* sh, const void* q, const void* k, 
     st = fill_prefill_args(sh, cu_seqlens_q, cu_seqlens_k, block_table, qo_offset, causal, scale, out, lse, workspace,
                            workspace_bytes, f16, &a);
     if (st != PA_OK) return st;
-    if (kPairPrefill) {
+    if (g_prefill_cta_pairs.load() != 0) {
         // CTA pairs (512-row work items); each CTA loads 64 keys of a K tile,
         // so the ragged K and rope maps take 64-row boxes
         pa::PrefillArgs ap = a;
