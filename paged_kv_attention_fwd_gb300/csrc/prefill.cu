@@ -566,17 +566,19 @@ __global__ void __launch_bounds__(320, 1)
                     if (fast) {
                         const uint64_t sc2 = f2_pack(__float_as_uint(sl2), __float_as_uint(sl2));
                         const uint64_t nm2 = f2_pack(__float_as_uint(neg_m), __float_as_uint(neg_m));
-                        uint64_t acc2 = f2_pack(0u, 0u);
+                        // two running sums, alternate pairs: half the add chain's length
+                        uint64_t acc2 = f2_pack(0u, 0u), acc2b = f2_pack(0u, 0u);
 #pragma unroll
                         for (int k = 0; k < 32; ++k) {
                             float x0, x1;
                             f2_unpack(f2_fma(f2_pack(r[2 * k], r[2 * k + 1]), sc2, nm2), x0, x1);
                             const float p0 = ex2(x0), p1 = ex2(x1);
-                            acc2 = f2_add(acc2, f2_pack(__float_as_uint(p0), __float_as_uint(p1)));
+                            if (k & 1) acc2b = f2_add(acc2b, f2_pack(__float_as_uint(p0), __float_as_uint(p1)));
+                            else acc2 = f2_add(acc2, f2_pack(__float_as_uint(p0), __float_as_uint(p1)));
                             pw[k] = pack16x2(p0, p1, f16);
                         }
                         float a0, a1;
-                        f2_unpack(acc2, a0, a1);
+                        f2_unpack(f2_add(acc2, acc2b), a0, a1);
                         rs0 += a0;
                         rs1 += a1;
                     } else {
