@@ -24,7 +24,9 @@
 //              one tile overlaps the other tile's MMAs
 //   warps 2-5  softmax of tile A, warps 6-9 softmax of tile B: one query row
 //              per thread (its TMEM lane), row max and sum without any
-//              cross-thread exchange; P (bf16) is stored over the S columns;
+//              cross-thread exchange; P (bf16 or fp16) is stored over the S
+//              columns it replaces (keys 0..63 -> columns 0..31, keys 64..127
+//              -> columns 64..95);
 //              O is rescaled in TMEM only when the running max grows by more
 //              than 2^8 (otherwise the stale max stays exact and cheaper);
 //              the query tile that takes an item's last K/V tile first zeroes
