@@ -304,3 +304,51 @@ def test_large_outputs_under_the_ulp_rule(kind):
     abs_mean, _ = reference(absv)
     assert np.abs(ro).max() >= 8
     assert_close_16(out, lse, ro, rl, abs_mean)
+
+
+def test_prefill_in_cuda_graph_replayed_with_new_inputs():
+    """pa_prefill captured once in a CUDA graph -- the unit-order kernel and
+    the prefill kernel, launched as its programmatic dependent -- then
+    replayed with new query values and shorter key ranges (the order and the
+    causal offsets come from the device lengths at replay time); every replay
+    against the oracle."""
+    from dataclasses import replace
+
+    base = W.make_paged_prefill([300, 200, 300, 130], [1500, 900, 300, 1100], 16, 4, 128, seed=13)
+    dev = "cuda"
+    q = ops.as_16(base.q, dev, base.dtype)
+    k = ops.as_16(base.k, dev, base.dtype)
+    v = ops.as_16(base.v, dev, base.dtype)
+    cq = torch.from_numpy(base.cu_seqlens_q).to(dev)
+    ck = torch.from_numpy(base.cu_seqlens_k).to(dev)
+    bt = torch.from_numpy(base.block_table).to(dev)
+    sh = ops.prefill_shapes(base.batch, base.num_q_heads, base.num_kv_heads, 128, 128, 0, base.max_seqlen_q,
+                            int(base.cu_seqlens_q[-1]), int(base.cu_seqlens_k[-1]),
+                            max_pages=base.block_table.shape[1], num_pool_pages=base.k.shape[0], dtype=base.dtype)
+    out = torch.empty((int(base.cu_seqlens_q[-1]), 16, 128), dtype=torch.bfloat16, device=dev)
+    lse = torch.empty((int(base.cu_seqlens_q[-1]), 16), dtype=torch.float32, device=dev)
+    ws = torch.zeros(B.pa_prefill_workspace_size(sh), dtype=torch.uint8, device=dev)
+    s = torch.cuda.Stream()
+
+    def step():
+        ops.prefill(sh, q, k, v, cq, ck, base.scale, True, block_table=bt, out=out, lse=lse, workspace=ws, stream=s)
+
+    with torch.cuda.stream(s):
+        step()  # eager once: the first launches configure the kernels
+    s.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        step()
+    q_lens = np.diff(base.cu_seqlens_q)
+    kv_lens = np.diff(base.cu_seqlens_k)
+    for trial, shrink in enumerate([0, 97, 250]):
+        new_q = W.normal_16(100 + trial, 7, base.q.shape, base.dtype)
+        new_kv = np.maximum(kv_lens - shrink, q_lens).astype(np.int32)  # never fewer keys than queries
+        case = replace(base, q=new_q, cu_seqlens_k=W.cu_seqlens(new_kv))
+        q.copy_(ops.as_16(new_q, dev, base.dtype))
+        ck.copy_(torch.from_numpy(case.cu_seqlens_k))
+        g.replay()
+        torch.cuda.synchronize()
+        ref_out, ref_lse = reference(case)
+        assert_close(out.float().cpu().numpy(), lse.cpu().numpy(), ref_out, ref_lse)
+    assert B.pa_check_status(ws) == B.PA_OK
